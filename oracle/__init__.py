@@ -1,0 +1,214 @@
+"""Test-infrastructure oracle of the Gated DeltaNet sublayer (plain sequential fp64 C on the CPU).
+
+Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg import this
+package.  It shares no code with the CUDA library in ``linear_attention_ssm_gb300``; both sides
+only share the seeded input generators, which hold none of the method's arithmetic.
+
+Every function takes CPU tensors (bf16 as ``torch.bfloat16``, fp32 as ``torch.float32``) and
+returns float64 tensors.  The C source, ``gdn_oracle.c``, states what each step computes and the
+page/section it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# mutation bits (negative controls planted in the oracle, never in the CUDA path)
+MUT_SILU_GATE = 0x001
+MUT_NO_CONV = 0x002
+MUT_DROP_CARRY = 0x004
+MUT_TRANSPOSE = 0x008
+MUT_TILED_HEADS = 0x010
+MUT_CONV_SHIFT = 0x020
+MUT_DECAY_SIGN = 0x040
+MUT_NO_BETA = 0x080
+MUT_NO_QNORM = 0x100
+
+
+def build(force: bool = False) -> str:
+    """Compile gdn_oracle.c into liboracle.so beside it (gcc, -O2, no target-specific flags)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            D = ctypes.c_double
+            lib.oracle_round_bf16.argtypes = [D]
+            lib.oracle_round_bf16.restype = ctypes.c_uint16
+            lib.oracle_num_threads.restype = I
+            lib.oracle_conv1d_prefill.argtypes = [I, I, I, P, P, P, I, P, P, P, P, I]
+            lib.oracle_conv1d_prefill.restype = I
+            lib.oracle_gdn_recurrence.argtypes = [
+                I, I, I, I, I, P, P, P, P, I, D, D, P, P, P, P, I, I, I]
+            lib.oracle_gdn_recurrence.restype = I
+            lib.oracle_gated_rmsnorm.argtypes = [ctypes.c_long, I, P, P, P, D, P, I]
+            lib.oracle_gated_rmsnorm.restype = I
+            lib.oracle_decode_step.argtypes = [
+                I, I, I, I, I, I, P, P, P, P, P, P, P, P, D, D, D, P, P, I, I]
+            lib.oracle_decode_step.restype = I
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _bf16_bits(t: torch.Tensor) -> torch.Tensor:
+    assert t.dtype == torch.bfloat16, t.dtype
+    return t.detach().cpu().contiguous().view(torch.int16)
+
+
+def _f32(t):
+    return None if t is None else t.detach().cpu().to(torch.float32).contiguous()
+
+
+def _f64(t):
+    return None if t is None else t.detach().cpu().to(torch.float64).contiguous()
+
+
+def _i32(t):
+    return torch.as_tensor(t, dtype=torch.int32).cpu().contiguous()
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def round_bf16(x: torch.Tensor) -> torch.Tensor:
+    """Round float64 values to bf16 with ties to even, directly from the exact value."""
+    lib = _load()
+    flat = x.detach().cpu().to(torch.float64).reshape(-1).tolist()
+    bits = np.array([lib.oracle_round_bf16(v) for v in flat], dtype=np.uint16)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).reshape(x.shape)
+
+
+def conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in=None, mutation: int = 0):
+    """Causal depthwise conv1d + SiLU, rounded once to bf16.
+
+    Returns (y bf16 [T,C], y_exact float64 [T,C], conv_state_out bf16 [N,C,W-1]).
+    """
+    lib = _load()
+    T, C = x.shape
+    W = conv_w.shape[1]
+    cu = _i32(cu_seqlens)
+    N = cu.numel() - 1
+    xb, wb = _bf16_bits(x), _bf16_bits(conv_w)
+    sin = _bf16_bits(conv_state_in) if conv_state_in is not None else None
+    y = torch.empty((T, C), dtype=torch.int16)
+    y_exact = torch.empty((T, C), dtype=torch.float64)
+    sout = torch.empty((N, C, W - 1), dtype=torch.int16)
+    rc = lib.oracle_conv1d_prefill(C, W, T, _ptr(xb), _ptr(wb), _ptr(cu), N, _ptr(sin), _ptr(y),
+                                   _ptr(y_exact), _ptr(sout), int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_conv1d_prefill failed ({rc})")
+    return y.view(torch.bfloat16), y_exact, sout.view(torch.bfloat16)
+
+
+def gdn_recurrence(qkv, g, beta, cu_seqlens, num_k_heads, num_v_heads, head_k_dim, head_v_dim,
+                   q_scale, l2_eps=1e-6, state_in=None, heads=None, nthreads: int = 0,
+                   mutation: int = 0):
+    """The gated delta rule, token by token, one chain per (sequence, V head).
+
+    qkv: bf16 [T, 2*Hk*Dk + Hv*Dv]; g, beta: [T, Hv]; state_in: [N, Hv, Dv, Dk] or None.
+    Returns (o float64 [T, Hv, Dv], state_out float64 [N, Hv, Dv, Dk]).  With ``heads`` only
+    those V heads are computed (the others are NaN).
+    """
+    lib = _load()
+    T = qkv.shape[0]
+    cu = _i32(cu_seqlens)
+    N = cu.numel() - 1
+    hk, hv, dk, dv = num_k_heads, num_v_heads, head_k_dim, head_v_dim
+    assert qkv.shape[1] == 2 * hk * dk + hv * dv
+    q = _bf16_bits(qkv)
+    gg, bb = _f32(g), _f32(beta)
+    sin = _f64(state_in)
+    o = torch.full((T, hv, dv), float("nan"), dtype=torch.float64)
+    sout = torch.full((N, hv, dv, dk), float("nan"), dtype=torch.float64)
+    hl = _i32(heads) if heads is not None else None
+    rc = lib.oracle_gdn_recurrence(hk, hv, dk, dv, T, _ptr(q), _ptr(gg), _ptr(bb), _ptr(cu), N,
+                                   float(q_scale), float(l2_eps), _ptr(sin), _ptr(o), _ptr(sout),
+                                   _ptr(hl), 0 if hl is None else hl.numel(), int(nthreads),
+                                   int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_gdn_recurrence failed ({rc})")
+    return o, sout
+
+
+def gated_rmsnorm(o, z, norm_w, eps=1e-6, mutation: int = 0):
+    """out = o * (mean(o^2) + eps)^-1/2 * w * sigmoid(z) over the last dim; float64 result."""
+    lib = _load()
+    dv = o.shape[-1]
+    oo = _f64(o).reshape(-1, dv)
+    zz = _bf16_bits(z).reshape(-1, dv)
+    ww = _bf16_bits(norm_w)
+    out = torch.empty_like(oo)
+    lib.oracle_gated_rmsnorm(oo.shape[0], dv, _ptr(oo), _ptr(zz), _ptr(ww), float(eps), _ptr(out),
+                             int(mutation))
+    return out.reshape(o.shape)
+
+
+def decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, num_k_heads, num_v_heads,
+                head_k_dim, head_v_dim, q_scale, l2_eps=1e-6, rms_eps=1e-6, nthreads: int = 0,
+                mutation: int = 0):
+    """One decode token per sequence.
+
+    conv_state (bf16 [B,C,W-1]) and state (float64 [B,Hv,Dv,Dk]) are returned updated (new
+    tensors; the arguments are not modified).  Returns (out float64 [B,Hv,Dv],
+    o_raw float64 [B,Hv,Dv], conv_state', state').
+    """
+    lib = _load()
+    B, C = x.shape
+    W = conv_w.shape[1]
+    hk, hv, dk, dv = num_k_heads, num_v_heads, head_k_dim, head_v_dim
+    cs = _bf16_bits(conv_state).clone()
+    st = _f64(state).clone()
+    out = torch.empty((B, hv, dv), dtype=torch.float64)
+    o_raw = torch.empty((B, hv, dv), dtype=torch.float64)
+    rc = lib.oracle_decode_step(hk, hv, dk, dv, W, B, _ptr(_bf16_bits(x)), _ptr(_bf16_bits(conv_w)),
+                                _ptr(cs), _ptr(_f32(g)), _ptr(_f32(beta)), _ptr(st),
+                                _ptr(_bf16_bits(z)), _ptr(_bf16_bits(norm_w)), float(q_scale),
+                                float(l2_eps), float(rms_eps), _ptr(out), _ptr(o_raw),
+                                int(nthreads), int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_step failed ({rc})")
+    return out, o_raw, cs.view(torch.bfloat16), st
+
+
+def prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, num_k_heads, num_v_heads, head_k_dim,
+            head_v_dim, q_scale, l2_eps=1e-6, rms_eps=1e-6, state_in=None, conv_state_in=None,
+            heads=None, nthreads: int = 0, mutation: int = 0):
+    """The whole prefill sublayer: conv1d+SiLU -> recurrence -> gated RMSNorm.
+
+    Returns a dict with y (bf16 conv output), o (float64), out (float64 gated output),
+    state (float64 final states) and conv_state (bf16).
+    """
+    y, _, cs = conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in, mutation=mutation)
+    o, st = gdn_recurrence(y, g, beta, cu_seqlens, num_k_heads, num_v_heads, head_k_dim,
+                           head_v_dim, q_scale, l2_eps, state_in, heads=heads, nthreads=nthreads,
+                           mutation=mutation)
+    out = gated_rmsnorm(o, z, norm_w, rms_eps, mutation=mutation)
+    return {"y": y, "o": o, "out": out, "state": st, "conv_state": cs}

@@ -1,0 +1,370 @@
+/*
+ * gdn_oracle.c -- plain, sequential fp64 CPU oracle of the Gated DeltaNet (GDN) sublayer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call this file: only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg load it.  It shares no code,
+ * header, table or helper with the CUDA library; it reads bf16 inputs as raw 16-bit patterns
+ * and fp32 inputs as floats, and computes everything in double precision, in the order the
+ * method defines, one token at a time.
+ *
+ * What it computes (sources are the pages' titles and sections):
+ *   1. causal depthwise conv1d, width W (4), no bias, over the packed [q | k | v] channels,
+ *      followed by SiLU and one rounding to bf16 -- pegainfer PR #1152 "Reference golden for
+ *      the GDN sublayer", Summary (depthwise conv, conv kernel 4, conv1d weight only) and
+ *      "Commands + measured numbers" (the conv leg is a bf16 tensor compared bit-exact);
+ *      GLM-5.3-Flash kernel TDD ledger, slice I3 (the decode step equals the full width-4
+ *      causal convolution).
+ *   2. head expansion q/k by repeat_interleave (V head h reads K head h / (Hv/Hk)) and L2
+ *      normalisation x / sqrt(sum x^2 + eps) -- PR #1152 Summary (V/K ratio 3,
+ *      repeat_interleave) and its Code review (prepare: head expand + L2 norm);
+ *      GLM-5.3-Flash ledger slice I2a (independent x/sqrt(sum(x^2)+eps), not max(norm, eps),
+ *      not an RMS norm).
+ *   3. the gated delta rule with an fp32 [value, key] state carried across chunks, calls and
+ *      sequences:  S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *      o_t = q_scale * S_t q_t  -- PR #1152 Code review (f32 recurrent state, cross-chunk
+ *      carry); GLM-5.3-Flash ledger slice I2 (FP32 [value,key] state, separate q output scale).
+ *      It is evaluated as its expanded form: S <- exp(g) S;  e = beta (v - S k);  S <- S + e k^T.
+ *   4. gated RMSNorm with a sigmoid output gate: out = o * (mean(o^2) + eps)^-1/2 * w * sigmoid(z)
+ *      -- PR #1152 Summary (output_gate_type "sigmoid", not silu) and Code review item 6
+ *      (rms_norm_eps == 1e-6).
+ *   5. the one-token decode step: conv step on a (W-1)-deep shift register of raw inputs,
+ *      then steps 2-4 for one token -- Qwen3.8 kernel architecture and TDD ledger, "Current
+ *      dense-27B kernel map" (scalar GDN recurrence and fused output gate).
+ *
+ * Mutations (negative controls) can be planted here, on the CPU, through the `mutation`
+ * bit set; 0 is the method.  See ORACLE_MUT_* below.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORACLE_MUT_SILU_GATE 0x001 /* gate by z*sigmoid(z) instead of sigmoid(z)            */
+#define ORACLE_MUT_NO_CONV 0x002   /* skip the conv leg: q|k|v = raw input                  */
+#define ORACLE_MUT_DROP_CARRY 0x004 /* restart from the initial state at every 64th token */
+#define ORACLE_MUT_TRANSPOSE 0x008 /* read/write the state as [key, value]                  */
+#define ORACLE_MUT_TILED_HEADS 0x010 /* V head h reads K head h % Hk                        */
+#define ORACLE_MUT_CONV_SHIFT 0x020 /* conv window shifted one position into the past       */
+#define ORACLE_MUT_DECAY_SIGN 0x040 /* decay by exp(-g)                                     */
+#define ORACLE_MUT_NO_BETA 0x080    /* beta forced to 1                                     */
+#define ORACLE_MUT_NO_QNORM 0x100   /* q is not L2-normalised                               */
+
+/* ---------------------------------------------------------------- bf16 <-> double */
+
+static double bf16_to_double(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Round a double to the nearest bf16 (1 sign, 8 exponent, 7 stored mantissa bits), ties to
+ * even, directly from the exact value (no intermediate rounding to float). */
+uint16_t oracle_round_bf16(double x) {
+  if (isnan(x)) return 0x7FC0;
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double ax = fabs(x);
+  if (ax == 0.0) return sign;
+  if (isinf(ax)) return sign | 0x7F80;
+  int e;
+  (void)frexp(ax, &e);           /* ax = m * 2^e, 0.5 <= m < 1: leading bit weighs 2^(e-1) */
+  int qexp = e - 8;              /* 8 significant bits -> quantum 2^(e-8)                  */
+  if (qexp < -133) qexp = -133;  /* subnormal bf16 quantum is 2^-133                       */
+  double r = nearbyint(ldexp(ax, -qexp)); /* round to integer, ties to even                 */
+  double y = ldexp(r, qexp);
+  if (y > 3.3895313892515355e38) return sign | 0x7F80; /* above the largest finite bf16   */
+  float f = (float)y;            /* exact: y has at most 8 significant bits                */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return sign | (uint16_t)(u >> 16);
+}
+
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* ---------------------------------------------------------------- 1. conv1d + SiLU (prefill) */
+
+/*
+ * x:          [T, C] bf16 raw conv input (packed q|k|v channels, token-major)
+ * w:          [C, W] bf16; w[c, W-1] multiplies the current token, w[c, 0] the oldest
+ * cu_seqlens: [N+1] token offsets of the packed sequences
+ * state_in:   [N, C, W-1] bf16 raw inputs preceding each sequence, oldest first, or NULL (zeros)
+ * y:          [T, C] bf16 = round_bf16(silu(sum_i w[c,i] x[t-(W-1)+i, c]))
+ * y_exact:    [T, C] double, the same before rounding, or NULL
+ * state_out:  [N, C, W-1] bf16, the last W-1 raw inputs of each sequence (history shifted in)
+ */
+int oracle_conv1d_prefill(int C, int W, int T, const uint16_t* x, const uint16_t* w,
+                          const int32_t* cu_seqlens, int N, const uint16_t* state_in,
+                          uint16_t* y, double* y_exact, uint16_t* state_out, int mutation) {
+  if (C <= 0 || W < 1 || T < 0 || N < 0) return 1;
+  if (cu_seqlens[0] != 0 || cu_seqlens[N] != T) return 2;
+  for (int n = 0; n < N; ++n)
+    if (cu_seqlens[n + 1] < cu_seqlens[n]) return 2;
+  const int H = W - 1;
+  for (int n = 0; n < N; ++n) {
+    const int s = cu_seqlens[n], L = cu_seqlens[n + 1] - s;
+    for (int c = 0; c < C; ++c) {
+      /* value of the raw input at position p relative to the sequence start (p may be < 0) */
+#define RAW(p) ((p) >= 0 ? bf16_to_double(x[(size_t)(s + (p)) * C + c])                     \
+                         : ((p) >= -H && state_in                                           \
+                                ? bf16_to_double(state_in[((size_t)n * C + c) * H + H + (p)]) \
+                                : 0.0))
+      for (int t = 0; t < L; ++t) {
+        double a;
+        if (mutation & ORACLE_MUT_NO_CONV) {
+          a = RAW(t);
+        } else {
+          double acc = 0.0;
+          for (int i = 0; i < W; ++i) {
+            int p = t - H + i;
+            if (mutation & ORACLE_MUT_CONV_SHIFT) p -= 1;
+            acc += bf16_to_double(w[(size_t)c * W + i]) * RAW(p);
+          }
+          a = acc * sigmoid(acc); /* SiLU */
+        }
+        if (y_exact) y_exact[(size_t)(s + t) * C + c] = a;
+        if (y) y[(size_t)(s + t) * C + c] = oracle_round_bf16(a);
+      }
+      if (state_out && H > 0) {
+        /* read every slot before writing so that state_out may alias state_in */
+        double slot[16];
+        for (int j = 0; j < H && j < 16; ++j) slot[j] = RAW(L - H + j);
+        for (int j = 0; j < H && j < 16; ++j)
+          state_out[((size_t)n * C + c) * H + j] = oracle_round_bf16(slot[j]);
+      }
+#undef RAW
+    }
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------- 2+3. the recurrence */
+
+typedef struct {
+  int hk, hv, dk, dv;
+  const uint16_t* qkv;   /* [T, 2*hk*dk + hv*dv] bf16 */
+  const float* g;        /* [T, hv] */
+  const float* beta;     /* [T, hv] */
+  const int32_t* cu;     /* [N+1] */
+  int N;
+  double q_scale, l2_eps;
+  const double* state_in; /* [N, hv, dv, dk] or NULL */
+  double* o;              /* [T, hv, dv] */
+  double* state_out;      /* [N, hv, dv, dk] or NULL */
+  const int32_t* heads;   /* subset of V heads to compute, or NULL for all */
+  int nheads;
+  int mutation;
+  long next;              /* work counter */
+  pthread_mutex_t lock;
+} rec_job;
+
+static void rec_chain(rec_job* J, int n, int h) {
+  const int hk = J->hk, hv = J->hv, dk = J->dk, dv = J->dv;
+  const int C = 2 * hk * dk + hv * dv;
+  const int ratio = hv / hk;
+  const int j = (J->mutation & ORACLE_MUT_TILED_HEADS) ? (h % hk) : (h / ratio);
+  const size_t sdim = (size_t)dv * dk;
+  double* S = (double*)malloc(sizeof(double) * sdim);
+  double* S0 = (double*)malloc(sizeof(double) * sdim);
+  double* qn = (double*)malloc(sizeof(double) * dk);
+  double* kn = (double*)malloc(sizeof(double) * dk);
+  double* e = (double*)malloc(sizeof(double) * dv);
+  /* S[r*dk + i]: row r = value index, column i = key index ([value, key] layout) */
+  for (int r = 0; r < dv; ++r)
+    for (int i = 0; i < dk; ++i) {
+      double v0 = 0.0;
+      if (J->state_in) {
+        const double* si = J->state_in + ((size_t)n * hv + h) * sdim;
+        v0 = (J->mutation & ORACLE_MUT_TRANSPOSE) ? si[(size_t)i * dv + r] : si[(size_t)r * dk + i];
+      }
+      S0[(size_t)r * dk + i] = v0;
+      S[(size_t)r * dk + i] = v0;
+    }
+  const int s = J->cu[n], L = J->cu[n + 1] - s;
+  for (int tt = 0; tt < L; ++tt) {
+    const size_t t = (size_t)(s + tt);
+    if ((J->mutation & ORACLE_MUT_DROP_CARRY) && tt > 0 && tt % 64 == 0)
+      memcpy(S, S0, sizeof(double) * sdim);
+    const uint16_t* row = J->qkv + t * C;
+    /* L2 normalisation of q and k of K head j (x / sqrt(sum x^2 + eps)) */
+    double sq = 0.0, sk = 0.0;
+    for (int i = 0; i < dk; ++i) {
+      double qv = bf16_to_double(row[j * dk + i]);
+      double kv = bf16_to_double(row[hk * dk + j * dk + i]);
+      qn[i] = qv;
+      kn[i] = kv;
+      sq += qv * qv;
+      sk += kv * kv;
+    }
+    const double iq = (J->mutation & ORACLE_MUT_NO_QNORM) ? 1.0 : 1.0 / sqrt(sq + J->l2_eps);
+    const double ik = 1.0 / sqrt(sk + J->l2_eps);
+    for (int i = 0; i < dk; ++i) {
+      qn[i] *= iq;
+      kn[i] *= ik;
+    }
+    const double gt = (double)J->g[t * hv + h];
+    const double alpha = exp((J->mutation & ORACLE_MUT_DECAY_SIGN) ? -gt : gt);
+    const double b = (J->mutation & ORACLE_MUT_NO_BETA) ? 1.0 : (double)J->beta[t * hv + h];
+    const uint16_t* vrow = row + 2 * hk * dk + (size_t)h * dv;
+    /* decay, then the delta correction against the decayed state */
+    for (size_t x = 0; x < sdim; ++x) S[x] *= alpha;
+    for (int r = 0; r < dv; ++r) {
+      double u = 0.0;
+      for (int i = 0; i < dk; ++i) u += S[(size_t)r * dk + i] * kn[i];
+      e[r] = b * (bf16_to_double(vrow[r]) - u);
+    }
+    for (int r = 0; r < dv; ++r)
+      for (int i = 0; i < dk; ++i) S[(size_t)r * dk + i] += e[r] * kn[i];
+    /* o_t = q_scale * S_t q_t */
+    double* orow = J->o + (t * hv + h) * dv;
+    for (int r = 0; r < dv; ++r) {
+      double acc = 0.0;
+      for (int i = 0; i < dk; ++i) acc += S[(size_t)r * dk + i] * qn[i];
+      orow[r] = J->q_scale * acc;
+    }
+  }
+  if (J->state_out) {
+    double* so = J->state_out + ((size_t)n * hv + h) * sdim;
+    for (int r = 0; r < dv; ++r)
+      for (int i = 0; i < dk; ++i) {
+        if (J->mutation & ORACLE_MUT_TRANSPOSE)
+          so[(size_t)i * dv + r] = S[(size_t)r * dk + i];
+        else
+          so[(size_t)r * dk + i] = S[(size_t)r * dk + i];
+      }
+  }
+  free(S); free(S0); free(qn); free(kn); free(e);
+}
+
+static void* rec_worker(void* arg) {
+  rec_job* J = (rec_job*)arg;
+  const long nh = J->heads ? J->nheads : J->hv;
+  const long total = (long)J->N * nh;
+  for (;;) {
+    pthread_mutex_lock(&J->lock);
+    long w = J->next++;
+    pthread_mutex_unlock(&J->lock);
+    if (w >= total) break;
+    int n = (int)(w / nh);
+    int h = J->heads ? J->heads[w % nh] : (int)(w % nh);
+    rec_chain(J, n, h);
+  }
+  return NULL;
+}
+
+int oracle_num_threads(void) {
+  long c = sysconf(_SC_NPROCESSORS_ONLN);
+  return c > 0 ? (int)c : 1;
+}
+
+/*
+ * The gated delta rule over packed variable-length sequences (one chain per (sequence, V head)).
+ * qkv:      [T, 2*hk*dk + hv*dv] bf16 conv output: q heads, then k heads, then v heads
+ * g, beta:  [T, hv] fp32 (log decay and write strength)
+ * state_in: [N, hv, dv, dk] double initial states ([value, key]) or NULL for zeros
+ * o:        [T, hv, dv] double;  state_out: [N, hv, dv, dk] double or NULL
+ * heads:    optional list of V heads to compute (the other heads of o/state_out are untouched)
+ * nthreads: worker threads over the independent chains (<= 0: all online cores)
+ */
+int oracle_gdn_recurrence(int hk, int hv, int dk, int dv, int T, const uint16_t* qkv,
+                          const float* g, const float* beta, const int32_t* cu_seqlens, int N,
+                          double q_scale, double l2_eps, const double* state_in, double* o,
+                          double* state_out, const int32_t* heads, int nheads, int nthreads,
+                          int mutation) {
+  if (hk <= 0 || hv <= 0 || dk <= 0 || dv <= 0 || hv % hk != 0 || N < 0) return 1;
+  if (cu_seqlens[0] != 0 || cu_seqlens[N] != T) return 2;
+  for (int n = 0; n < N; ++n)
+    if (cu_seqlens[n + 1] < cu_seqlens[n]) return 2;
+  rec_job J;
+  J.hk = hk; J.hv = hv; J.dk = dk; J.dv = dv;
+  J.qkv = qkv; J.g = g; J.beta = beta; J.cu = cu_seqlens; J.N = N;
+  J.q_scale = q_scale; J.l2_eps = l2_eps;
+  J.state_in = state_in; J.o = o; J.state_out = state_out;
+  J.heads = heads; J.nheads = nheads; J.mutation = mutation; J.next = 0;
+  pthread_mutex_init(&J.lock, NULL);
+  if (nthreads <= 0) nthreads = oracle_num_threads();
+  const long work = (long)N * (heads ? nheads : hv);
+  if (nthreads > work) nthreads = work > 0 ? (int)work : 1;
+  if (nthreads <= 1) {
+    rec_worker(&J);
+  } else {
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+    for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, rec_worker, &J);
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    free(th);
+  }
+  pthread_mutex_destroy(&J.lock);
+  return 0;
+}
+
+/* ---------------------------------------------------------------- 4. gated RMSNorm */
+
+/*
+ * o:   [rows, dv] double (rows = tokens * V heads), z: [rows, dv] bf16, w: [dv] bf16
+ * out: [rows, dv] double = o * (mean_d o^2 + eps)^(-1/2) * w * sigmoid(z)
+ */
+int oracle_gated_rmsnorm(long rows, int dv, const double* o, const uint16_t* z,
+                         const uint16_t* w, double eps, double* out, int mutation) {
+  for (long r = 0; r < rows; ++r) {
+    const double* orow = o + (size_t)r * dv;
+    double ss = 0.0;
+    for (int d = 0; d < dv; ++d) ss += orow[d] * orow[d];
+    const double inv = 1.0 / sqrt(ss / dv + eps);
+    for (int d = 0; d < dv; ++d) {
+      const double zz = bf16_to_double(z[(size_t)r * dv + d]);
+      const double gate = (mutation & ORACLE_MUT_SILU_GATE) ? zz * sigmoid(zz) : sigmoid(zz);
+      out[(size_t)r * dv + d] = orow[d] * inv * bf16_to_double(w[d]) * gate;
+    }
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------- 5. decode step */
+
+/*
+ * One token for each of B independent sequences.
+ * x:          [B, C] bf16 raw conv input of this step
+ * conv_state: [B, C, W-1] bf16 in/out shift register of the previous W-1 raw inputs, oldest first
+ * state:      [B, hv, dv, dk] double in/out recurrent state
+ * g, beta:    [B, hv] fp32;  z: [B, hv, dv] bf16;  norm_w: [dv] bf16
+ * out:        [B, hv, dv] double gated output;  o_raw: [B, hv, dv] double or NULL (pre-norm)
+ */
+int oracle_decode_step(int hk, int hv, int dk, int dv, int W, int B, const uint16_t* x,
+                       const uint16_t* conv_w, uint16_t* conv_state, const float* g,
+                       const float* beta, double* state, const uint16_t* z,
+                       const uint16_t* norm_w, double q_scale, double l2_eps, double rms_eps,
+                       double* out, double* o_raw, int nthreads, int mutation) {
+  const int C = 2 * hk * dk + hv * dv;
+  const int H = W - 1;
+  uint16_t* a = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)B * C);
+  double* o = o_raw ? o_raw : (double*)malloc(sizeof(double) * (size_t)B * hv * dv);
+  int32_t* cu = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B + 1));
+  /* conv step: window = [state[0..H-1], x]; y = sum_i w[c,i] window[i]; state <- window[1..H] */
+  for (int b = 0; b < B; ++b) {
+    for (int c = 0; c < C; ++c) {
+      double win[17];
+      uint16_t* st = conv_state + ((size_t)b * C + c) * H;
+      for (int i = 0; i < H; ++i) win[i] = bf16_to_double(st[i]);
+      win[H] = bf16_to_double(x[(size_t)b * C + c]);
+      double acc = 0.0;
+      if (mutation & ORACLE_MUT_CONV_SHIFT) {
+        for (int i = 1; i < W; ++i) acc += bf16_to_double(conv_w[(size_t)c * W + i]) * win[i - 1];
+      } else {
+        for (int i = 0; i < W; ++i) acc += bf16_to_double(conv_w[(size_t)c * W + i]) * win[i];
+      }
+      const double act = (mutation & ORACLE_MUT_NO_CONV) ? win[H] : acc * sigmoid(acc);
+      a[(size_t)b * C + c] = oracle_round_bf16(act);
+      for (int i = 0; i < H; ++i) st[i] = oracle_round_bf16(win[i + 1]);
+    }
+    cu[b] = b;
+  }
+  cu[B] = B;
+  int rc = oracle_gdn_recurrence(hk, hv, dk, dv, B, a, g, beta, cu, B, q_scale, l2_eps, state, o,
+                                 state, NULL, 0, nthreads, mutation & ~ORACLE_MUT_DROP_CARRY);
+  if (rc == 0) rc = oracle_gated_rmsnorm((long)B * hv, dv, o, z, norm_w, rms_eps, out, mutation);
+  free(a);
+  free(cu);
+  if (!o_raw) free(o);
+  return rc;
+}

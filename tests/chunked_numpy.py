@@ -1,0 +1,51 @@
+"""The chunk-wise (WY) form of the gated delta rule, in plain numpy fp64 (test helper).
+
+This is a second, independently structured derivation of the same recurrence, following the
+stage order the pegainfer PR #1152 page gives for its production prefill ("prepare -> cumsum ->
+A -> solve -> recompute -> state -> output", Consumer / Shipped-line diff) with 64-token
+chunks.  The sequential oracle must agree with it at any length, in particular across chunk
+boundaries (GLM-5.3-Flash kernel TDD ledger, slice I4: "chunk path matches sequential state
+and output" at 63/64/65).  It is used only to pin the oracle and to document the chunk algebra
+that the CUDA kernels implement; it is never compared against the GPU directly.
+
+Within one chunk of length L (tokens 1..L), with gamma_t = sum_{i<=t} g_i:
+  A[t, j]  = beta_t exp(gamma_t - gamma_j) k_t . k_j          (j < t, else 0)
+  T        = (I + A)^-1                                        (unit lower triangular)
+  U        = T diag(beta) V,   W = T diag(beta exp(gamma)) K
+  E        = U - W S0^T                                        (rows e_t^T)
+  O        = q_scale [diag(exp(gamma)) Q S0^T + (mask_{j<=t} exp(gamma_t - gamma_j) Q K^T) E]
+  S_L      = exp(gamma_L) S0 + E^T diag(exp(gamma_L - gamma)) K
+"""
+from __future__ import annotations
+
+import numpy as np
+from scipy.linalg import solve_triangular
+
+
+def l2n(x, eps):
+    return x / np.sqrt((x * x).sum(-1, keepdims=True) + eps)
+
+
+def chunked_chain(q, k, v, g, beta, S0, q_scale, chunk=64):
+    """q, k: [T, Dk] (already L2-normalised); v: [T, Dv]; g, beta: [T]; S0: [Dv, Dk]."""
+    T = q.shape[0]
+    S = S0.astype(np.float64).copy()
+    O = np.zeros((T, v.shape[1]))
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(T, c0 + chunk))
+        Q, K, V, G, B = q[sl], k[sl], v[sl], g[sl], beta[sl]
+        L = Q.shape[0]
+        gam = np.cumsum(G)
+        diff = gam[:, None] - gam[None, :]
+        lower_strict = np.tril(np.ones((L, L)), -1)
+        lower_incl = np.tril(np.ones((L, L)), 0)
+        decay = np.exp(np.where(lower_incl > 0, diff, -np.inf))
+        A = (B[:, None] * decay * (K @ K.T)) * lower_strict
+        Tm = solve_triangular(np.eye(L) + A, np.eye(L), lower=True, unit_diagonal=True)
+        U = Tm @ (B[:, None] * V)
+        W = Tm @ ((B * np.exp(gam))[:, None] * K)
+        E = U - W @ S.T
+        P = decay * (Q @ K.T) * lower_incl
+        O[sl] = q_scale * ((np.exp(gam)[:, None] * Q) @ S.T + P @ E)
+        S = np.exp(gam[-1]) * S + E.T @ (np.exp(gam[-1] - gam)[:, None] * K)
+    return O, S

@@ -1,0 +1,390 @@
+"""Pins of the CPU oracle against facts other than itself (CPU only).
+
+Each test checks the oracle against a library routine, a closed form, an invariant the pages
+state, exact rational arithmetic, or an independently structured algorithm, chosen so that a
+dropped term, a wrong sign, a wrong index or a transposed operand in the oracle fails one of
+them.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from linear_attention_ssm_gb300.synth import Geometry, prefill_inputs, decode_inputs, cu_seqlens_of
+from tests.chunked_numpy import chunked_chain, l2n
+
+SMALL = Geometry(num_k_heads=2, num_v_heads=6, head_k_dim=8, head_v_dim=4, conv_width=4)
+
+
+def bf(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+# ------------------------------------------------------------------ bf16 rounding
+
+def _nearest_bf16_bruteforce(x: float) -> int:
+    """Nearest bf16 to x among the three neighbours of a candidate, ties to the even pattern."""
+    cand = int(torch.tensor([x], dtype=torch.float32).to(torch.bfloat16).view(torch.int16)[0]) & 0xFFFF
+    best = None
+    for b in (cand - 1, cand, cand + 1):
+        b &= 0xFFFF
+        val = float(torch.tensor([b], dtype=torch.int32).to(torch.int16).view(torch.bfloat16)[0].float())
+        if math.isnan(val) or math.isinf(val):
+            continue
+        d = abs(Fraction(x) - Fraction(val))
+        key = (d, b & 1)
+        if best is None or key < best[0]:
+            best = (key, b)
+    return best[1]
+
+
+def test_round_bf16_matches_bruteforce_and_ties_to_even():
+    rng = np.random.default_rng(0)
+    xs = list(rng.standard_normal(300) * np.exp(rng.uniform(-20, 20, 300)))
+    # exact midpoints between consecutive bf16 values must go to the even pattern
+    for b in (0x3F80, 0x3F81, 0x4049, 0xC2F7, 0x0081):
+        lo = float(torch.tensor([b], dtype=torch.int32).to(torch.int16).view(torch.bfloat16)[0].float())
+        hi = float(torch.tensor([b + 1], dtype=torch.int32).to(torch.int16).view(torch.bfloat16)[0].float())
+        xs.append((lo + hi) / 2)
+    got = oracle.round_bf16(torch.tensor(xs, dtype=torch.float64)).view(torch.int16)
+    for x, gbits in zip(xs, got.tolist()):
+        assert (gbits & 0xFFFF) == _nearest_bf16_bruteforce(x), x
+
+
+# ------------------------------------------------------------------ conv1d + SiLU
+
+def _torch_conv_silu(x, w, cu, state_in):
+    """Depthwise causal conv1d via torch.nn.functional.conv1d (fp64), then F.silu."""
+    C, W = w.shape
+    outs, states = [], []
+    for n in range(cu.numel() - 1):
+        s, e = int(cu[n]), int(cu[n + 1])
+        hist = state_in[n].double().T if state_in is not None else torch.zeros(W - 1, C, dtype=torch.float64)
+        seq = torch.cat([hist, x[s:e].double()], 0)  # [W-1+L, C]
+        y = F.conv1d(seq.T[None], w.double()[:, None, :], groups=C)[0].T  # [L, C]
+        outs.append(F.silu(y))
+        states.append(seq[-(W - 1):].T)
+    return torch.cat(outs, 0), torch.stack(states, 0)
+
+
+@pytest.mark.parametrize("with_state", [False, True])
+def test_conv_matches_torch_conv1d(with_state):
+    gen = torch.Generator().manual_seed(1)
+    lengths = [1, 2, 3, 5, 9]
+    cu = cu_seqlens_of(lengths)
+    T, C, W = sum(lengths), 24, 4
+    x = torch.randn(T, C, generator=gen).to(torch.bfloat16)
+    w = (0.5 * torch.randn(C, W, generator=gen)).to(torch.bfloat16)
+    st = torch.randn(len(lengths), C, W - 1, generator=gen).to(torch.bfloat16) if with_state else None
+    y, y_exact, st_out = oracle.conv1d_prefill(x, w, cu, st)
+    ref, ref_state = _torch_conv_silu(x, w, cu, st)
+    assert torch.allclose(y_exact, ref, rtol=1e-12, atol=1e-14)
+    # the stored conv output is the exact value rounded once to bf16
+    assert torch.equal(y.view(torch.int16), oracle.round_bf16(y_exact).view(torch.int16))
+    # torch's own bf16 rounding of the fp64 value agrees to within one ulp everywhere
+    ulp_gap = (y.view(torch.int16).int() - ref.to(torch.bfloat16).view(torch.int16).int()).abs()
+    assert int(ulp_gap.max()) <= 1
+    assert torch.equal(st_out.double(), ref_state)
+
+
+def test_conv_split_call_equals_one_call():
+    gen = torch.Generator().manual_seed(2)
+    C, W, T = 16, 4, 11
+    x = torch.randn(T, C, generator=gen).to(torch.bfloat16)
+    w = torch.randn(C, W, generator=gen).to(torch.bfloat16)
+    st0 = torch.randn(1, C, W - 1, generator=gen).to(torch.bfloat16)
+    y_all, _, st_all = oracle.conv1d_prefill(x, w, [0, T], st0)
+    for cut in (1, 2, 3, 7):
+        y1, _, st1 = oracle.conv1d_prefill(x[:cut], w, [0, cut], st0)
+        y2, _, st2 = oracle.conv1d_prefill(x[cut:], w, [0, T - cut], st1)
+        assert torch.equal(torch.cat([y1, y2]).view(torch.int16), y_all.view(torch.int16))
+        assert torch.equal(st2.view(torch.int16), st_all.view(torch.int16))
+
+
+# ------------------------------------------------------------------ the recurrence
+
+def _expand_qkv(qkv, geo):
+    hk, hv, dk, dv = geo.num_k_heads, geo.num_v_heads, geo.head_k_dim, geo.head_v_dim
+    T = qkv.shape[0]
+    a = qkv.double().numpy()
+    q = a[:, : hk * dk].reshape(T, hk, dk)
+    k = a[:, hk * dk: 2 * hk * dk].reshape(T, hk, dk)
+    v = a[:, 2 * hk * dk:].reshape(T, hv, dv)
+    return q, k, v
+
+
+def _product_form(qkv, g, beta, cu, geo, q_scale, eps, state0):
+    """S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T with explicit matrices;
+    q/k heads expanded with np.repeat (repeat_interleave)."""
+    hk, hv, dk = geo.num_k_heads, geo.num_v_heads, geo.head_k_dim
+    q, k, v = _expand_qkv(qkv, geo)
+    q = np.repeat(q, hv // hk, axis=1)
+    k = np.repeat(k, hv // hk, axis=1)
+    T = qkv.shape[0]
+    o = np.zeros((T, hv, geo.head_v_dim))
+    S_fin = np.zeros((len(cu) - 1, hv, geo.head_v_dim, dk))
+    for n in range(len(cu) - 1):
+        for h in range(hv):
+            S = state0[n, h].double().numpy().copy()
+            for t in range(int(cu[n]), int(cu[n + 1])):
+                kn = l2n(k[t, h], eps)
+                qn = l2n(q[t, h], eps)
+                b = float(beta[t, h])
+                S = math.exp(float(g[t, h])) * S @ (np.eye(dk) - b * np.outer(kn, kn)) + b * np.outer(v[t, h], kn)
+                o[t, h] = q_scale * S @ qn
+            S_fin[n, h] = S
+    return o, S_fin
+
+
+def test_recurrence_matches_product_form():
+    geo = SMALL
+    inp = prefill_inputs([5, 1, 9], seed=3, geo=geo, random_conv_state=True)
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"], inp["conv_state0"])
+    o, st = oracle.gdn_recurrence(y, inp["g"], inp["beta"], inp["cu_seqlens"], geo.num_k_heads,
+                                  geo.num_v_heads, geo.head_k_dim, geo.head_v_dim, 0.37, 1e-6,
+                                  inp["state0"])
+    o_ref, st_ref = _product_form(y, inp["g"], inp["beta"], inp["cu_seqlens"], geo, 0.37, 1e-6, inp["state0"])
+    np.testing.assert_allclose(o.numpy(), o_ref, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(st.numpy(), st_ref, rtol=1e-11, atol=1e-13)
+
+
+def test_recurrence_exact_rational_case():
+    """Two tokens, Dk = Dv = 2, one head, eps = 0, g = 0: checked in exact rational arithmetic.
+    k's are (3,4)/5 and (0,1); with g = 0 the product form has rational entries only."""
+    geo = Geometry(num_k_heads=1, num_v_heads=1, head_k_dim=2, head_v_dim=2, conv_width=4)
+    qraw = [[1.0, 0.0], [0.0, 2.0]]
+    kraw = [[3.0, 4.0], [0.0, 1.0]]
+    vraw = [[1.0, -2.0], [0.5, 3.0]]
+    betas = [0.5, 0.25]
+    qkv = bf([qraw[t] + kraw[t] + vraw[t] for t in range(2)])
+    g = torch.zeros(2, 1)
+    beta = torch.tensor([[b] for b in betas])
+    S0 = torch.tensor([[[[0.5, -1.0], [2.0, 0.25]]]])
+    o, st = oracle.gdn_recurrence(qkv, g, beta, [0, 2], 1, 1, 2, 2, 1.0, 0.0, S0)
+
+    def nrm(x):
+        n2 = sum(Fraction(a) ** 2 for a in x)
+        r = Fraction(math.isqrt(n2.numerator), math.isqrt(n2.denominator))
+        assert r * r == n2
+        return [Fraction(a) / r for a in x]
+
+    S = [[Fraction(0.5), Fraction(-1)], [Fraction(2), Fraction(0.25)]]
+    outs = []
+    for t in range(2):
+        kn, qn, b = nrm(kraw[t]), nrm(qraw[t]), Fraction(betas[t])
+        M = [[(1 if i == j else 0) - b * kn[i] * kn[j] for j in range(2)] for i in range(2)]
+        S = [[sum(S[r][i] * M[i][c] for i in range(2)) + b * Fraction(vraw[t][r]) * kn[c]
+              for c in range(2)] for r in range(2)]
+        outs.append([sum(S[r][i] * qn[i] for i in range(2)) for r in range(2)])
+    for t in range(2):
+        for r in range(2):
+            assert abs(float(o[t, 0, r]) - float(outs[t][r])) < 1e-14
+    for r in range(2):
+        for c in range(2):
+            assert abs(float(st[0, 0, r, c]) - float(S[r][c])) < 1e-14
+
+
+def test_beta_zero_is_pure_decay_closed_form():
+    geo = SMALL
+    inp = prefill_inputs([7, 3], seed=4, geo=geo)
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    beta0 = torch.zeros_like(inp["beta"])
+    o, st = oracle.gdn_recurrence(y, inp["g"], beta0, inp["cu_seqlens"], geo.num_k_heads, geo.num_v_heads,
+                                  geo.head_k_dim, geo.head_v_dim, 0.5, 1e-6, inp["state0"])
+    q, _, _ = _expand_qkv(y, geo)
+    cu = inp["cu_seqlens"].tolist()
+    for n in range(2):
+        s, e = cu[n], cu[n + 1]
+        for h in range(geo.num_v_heads):
+            S0 = inp["state0"][n, h].double().numpy()
+            gam = np.cumsum(inp["g"][s:e, h].double().numpy())
+            np.testing.assert_allclose(st[n, h].numpy(), math.exp(gam[-1]) * S0, rtol=1e-12)
+            for i, t in enumerate(range(s, e)):
+                qn = l2n(q[t, h // 3], 1e-6)
+                np.testing.assert_allclose(o[t, h].numpy(), 0.5 * math.exp(gam[i]) * S0 @ qn, rtol=1e-11, atol=1e-14)
+
+
+def test_beta_one_projects_key_onto_value():
+    """beta = 1, g = 0: after each token the state maps that token's (normalised) key to its value."""
+    geo = SMALL
+    inp = prefill_inputs([6], seed=5, geo=geo)
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    _, k, v = _expand_qkv(y, geo)
+    for L in range(1, 7):
+        o, st = oracle.gdn_recurrence(y[:L], torch.zeros(L, geo.num_v_heads), torch.ones(L, geo.num_v_heads),
+                                      [0, L], geo.num_k_heads, geo.num_v_heads, geo.head_k_dim, geo.head_v_dim,
+                                      1.0, 1e-6, inp["state0"])
+        for h in range(geo.num_v_heads):
+            kn = l2n(k[L - 1, h // 3], 1e-6)
+            # S k_hat = v exactly when ||k_hat|| = 1; with eps the norm is 1 - O(eps)
+            Sk = st[0, h].numpy() @ kn
+            resid = v[L - 1, h] - Sk
+            assert np.abs(resid).max() < 1e-5 * max(1.0, np.abs(v[L - 1, h]).max())
+    # with eps = 0 the property is exact to rounding
+    o, st = oracle.gdn_recurrence(y[:3], torch.zeros(3, geo.num_v_heads), torch.ones(3, geo.num_v_heads),
+                                  [0, 3], geo.num_k_heads, geo.num_v_heads, geo.head_k_dim, geo.head_v_dim,
+                                  1.0, 0.0, inp["state0"])
+    for h in range(geo.num_v_heads):
+        kn = l2n(k[2, h // 3], 0.0)
+        np.testing.assert_allclose(st[0, h].numpy() @ kn, v[2, h], rtol=1e-12, atol=1e-12)
+
+
+def test_orthonormal_keys_closed_form():
+    """g = 0, beta = 1, orthonormal keys: S = S0 (I - sum k k^T) + sum v k^T."""
+    dk, dv = 4, 3
+    geo = Geometry(num_k_heads=1, num_v_heads=1, head_k_dim=dk, head_v_dim=dv, conv_width=4)
+    gen = torch.Generator().manual_seed(6)
+    T = 3
+    keys = torch.zeros(T, dk)
+    keys[0, 2], keys[1, 0], keys[2, 3] = 2.0, -1.0, 0.5   # orthogonal; normalised by the oracle
+    qs = torch.randn(T, dk, generator=gen)
+    vs = torch.randn(T, dv, generator=gen)
+    qkv = torch.cat([qs, keys, vs], 1).to(torch.bfloat16)
+    S0 = torch.randn(1, 1, dv, dk, generator=gen)
+    o, st = oracle.gdn_recurrence(qkv, torch.zeros(T, 1), torch.ones(T, 1), [0, T], 1, 1, dk, dv, 1.0, 0.0, S0)
+    kn = l2n(keys.double().numpy(), 0.0)
+    vb = qkv[:, 2 * dk:].double().numpy()
+    ref = S0[0, 0].double().numpy() @ (np.eye(dk) - kn.T @ kn) + vb.T @ kn
+    np.testing.assert_allclose(st[0, 0].numpy(), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_state_layout_is_value_by_key():
+    """With beta = 0 and g = 0 the output is q_scale * S0 q_hat: rows of S0 index the value dim."""
+    dk, dv = 8, 4
+    gen = torch.Generator().manual_seed(7)
+    qkv = torch.randn(1, 2 * dk + dv, generator=gen).to(torch.bfloat16)
+    S0 = torch.randn(1, 1, dv, dk, generator=gen)
+    o, _ = oracle.gdn_recurrence(qkv, torch.zeros(1, 1), torch.zeros(1, 1), [0, 1], 1, 1, dk, dv, 1.0, 0.0, S0)
+    qn = F.normalize(qkv[0, :dk].double(), dim=0)       # library normalisation (eps = 0 case)
+    np.testing.assert_allclose(o[0, 0].numpy(), (S0[0, 0].double() @ qn).numpy(), rtol=1e-12)
+
+
+def test_l2_norm_form_is_sqrt_sum_plus_eps():
+    """A tiny q (norm 1e-4, eps 1e-6): x/sqrt(sum x^2 + eps), not x/max(||x||, eps)."""
+    dk, dv = 2, 1
+    qkv = torch.tensor([[1e-4, 0.0, 1.0, 0.0, 1.0]]).to(torch.bfloat16)
+    q0 = float(qkv[0, 0].float())
+    S0 = torch.tensor([[[[1.0, 0.0]]]])
+    o, _ = oracle.gdn_recurrence(qkv, torch.zeros(1, 1), torch.zeros(1, 1), [0, 1], 1, 1, dk, dv, 1.0, 1e-6, S0)
+    assert abs(float(o[0, 0, 0]) - q0 / math.sqrt(q0 * q0 + 1e-6)) < 1e-15
+    assert abs(float(o[0, 0, 0]) - 1.0) > 0.5   # the max(norm, eps) form would give 1
+
+
+def test_head_expansion_is_repeat_interleave():
+    geo = SMALL
+    ratio = geo.num_v_heads // geo.num_k_heads
+    inp = prefill_inputs([9], seed=8, geo=geo)
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    hk, dk = geo.num_k_heads, geo.head_k_dim
+    T = y.shape[0]
+    q = y[:, : hk * dk].reshape(T, hk, dk).repeat_interleave(ratio, dim=1).reshape(T, -1)
+    k = y[:, hk * dk: 2 * hk * dk].reshape(T, hk, dk).repeat_interleave(ratio, dim=1).reshape(T, -1)
+    expanded = torch.cat([q, k, y[:, 2 * hk * dk:]], 1)
+    args = (inp["g"], inp["beta"], [0, T])
+    o1, s1 = oracle.gdn_recurrence(y, *args, hk, geo.num_v_heads, dk, geo.head_v_dim, 0.3, 1e-6, inp["state0"])
+    o2, s2 = oracle.gdn_recurrence(expanded, *args, geo.num_v_heads, geo.num_v_heads, dk, geo.head_v_dim,
+                                   0.3, 1e-6, inp["state0"])
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    o3, _ = oracle.gdn_recurrence(y, *args, hk, geo.num_v_heads, dk, geo.head_v_dim, 0.3, 1e-6,
+                                  inp["state0"], mutation=oracle.MUT_TILED_HEADS)
+    assert not torch.allclose(o1, o3)
+
+
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 80, 128, 130])
+def test_sequential_oracle_equals_chunked_wy_form(L):
+    geo = Geometry(num_k_heads=1, num_v_heads=3, head_k_dim=128, head_v_dim=128, conv_width=4)
+    inp = prefill_inputs([L], seed=100 + L, geo=geo)
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    qs = geo.q_scale
+    o, st = oracle.gdn_recurrence(y, inp["g"], inp["beta"], [0, L], 1, 3, 128, 128, qs, 1e-6, inp["state0"])
+    q, k, v = _expand_qkv(y, geo)
+    for h in range(3):
+        O, S = chunked_chain(l2n(q[:, 0], 1e-6), l2n(k[:, 0], 1e-6), v[:, h], inp["g"][:, h].double().numpy(),
+                             inp["beta"][:, h].double().numpy(), inp["state0"][0, h].double().numpy(), qs)
+        np.testing.assert_allclose(o[:, h].numpy(), O, rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(st[0, h].numpy(), S, rtol=1e-9, atol=1e-11)
+
+
+def test_split_sequence_with_carried_state_equals_one_call():
+    geo = SMALL
+    inp = prefill_inputs([20], seed=9, geo=geo)
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    a = (geo.num_k_heads, geo.num_v_heads, geo.head_k_dim, geo.head_v_dim, 0.25, 1e-6)
+    o, st = oracle.gdn_recurrence(y, inp["g"], inp["beta"], [0, 20], *a, inp["state0"])
+    o1, st1 = oracle.gdn_recurrence(y[:13], inp["g"][:13], inp["beta"][:13], [0, 13], *a, inp["state0"])
+    o2, st2 = oracle.gdn_recurrence(y[13:], inp["g"][13:], inp["beta"][13:], [0, 7], *a, st1)
+    assert torch.equal(torch.cat([o1, o2]), o) and torch.equal(st2, st)
+
+
+# ------------------------------------------------------------------ gated RMSNorm
+
+def test_gated_rmsnorm_matches_torch_rms_norm_times_sigmoid():
+    gen = torch.Generator().manual_seed(10)
+    o = torch.randn(5, 3, 16, generator=gen, dtype=torch.float64)
+    z = torch.randn(5, 3, 16, generator=gen).to(torch.bfloat16)
+    w = (1 + 0.1 * torch.randn(16, generator=gen)).to(torch.bfloat16)
+    out = oracle.gated_rmsnorm(o, z, w, 1e-6)
+    ref = F.rms_norm(o, (16,), weight=w.double(), eps=1e-6) * torch.sigmoid(z.double())
+    assert torch.allclose(out, ref, rtol=1e-13, atol=1e-15)
+    # sigma(0) = 1/2
+    half = oracle.gated_rmsnorm(o, torch.zeros_like(z), w, 1e-6)
+    assert torch.allclose(half, 0.5 * F.rms_norm(o, (16,), weight=w.double(), eps=1e-6), rtol=1e-14)
+    # a constant row normalises to sign(o) * |o| / sqrt(o^2 + eps)
+    c = torch.full((1, 16), -3.0, dtype=torch.float64)
+    big = torch.full((1, 16), 40.0).to(torch.bfloat16)   # sigmoid(40) = 1 - 4e-18
+    one = torch.ones(16).to(torch.bfloat16)
+    out_c = oracle.gated_rmsnorm(c, big, one, 1e-6)
+    assert torch.allclose(out_c, torch.full_like(c, -3.0 / math.sqrt(9.0 + 1e-6)), rtol=1e-14)
+    silu = oracle.gated_rmsnorm(o, z, w, 1e-6, mutation=oracle.MUT_SILU_GATE)
+    assert not torch.allclose(silu, out, rtol=1e-3)
+
+
+# ------------------------------------------------------------------ decode
+
+def test_decode_steps_equal_prefill():
+    """T decode steps equal one T-token prefill of every sequence (conv step = full conv)."""
+    geo = SMALL
+    B, T = 3, 5
+    d = decode_inputs(B, T, seed=11, geo=geo)
+    a = dict(num_k_heads=geo.num_k_heads, num_v_heads=geo.num_v_heads, head_k_dim=geo.head_k_dim,
+             head_v_dim=geo.head_v_dim, q_scale=0.3)
+    cs, st = d["conv_state0"], d["state0"].double()
+    outs = []
+    for s in range(T):
+        out, _, cs, st = oracle.decode_step(d["x"][s], d["conv_w"], cs, d["g"][s], d["beta"][s], st,
+                                            d["z"][s], d["norm_w"], **a)
+        outs.append(out)
+    dec = torch.stack(outs, 1)  # [B, T, Hv, Dv]
+    # the same tokens as B packed sequences of length T
+    x = d["x"].transpose(0, 1).reshape(B * T, -1)
+    g = d["g"].transpose(0, 1).reshape(B * T, -1)
+    beta = d["beta"].transpose(0, 1).reshape(B * T, -1)
+    z = d["z"].transpose(0, 1).reshape(B * T, geo.num_v_heads, geo.head_v_dim)
+    ref = oracle.prefill(x, d["conv_w"], cu_seqlens_of([T] * B), g, beta, z, d["norm_w"],
+                         state_in=d["state0"], conv_state_in=d["conv_state0"], **a)
+    assert torch.allclose(dec.reshape(B * T, geo.num_v_heads, -1), ref["out"], rtol=1e-12, atol=1e-14)
+    assert torch.allclose(st, ref["state"], rtol=1e-12, atol=1e-14)
+    assert torch.equal(cs.view(torch.int16), ref["conv_state"].view(torch.int16))
+
+
+# ------------------------------------------------------------------ mutations are live
+
+@pytest.mark.parametrize("mut", [oracle.MUT_NO_CONV, oracle.MUT_DROP_CARRY, oracle.MUT_TRANSPOSE,
+                                 oracle.MUT_TILED_HEADS, oracle.MUT_CONV_SHIFT, oracle.MUT_DECAY_SIGN,
+                                 oracle.MUT_NO_BETA, oracle.MUT_SILU_GATE, oracle.MUT_NO_QNORM])
+def test_each_planted_mutation_changes_the_output(mut):
+    geo = SMALL
+    inp = prefill_inputs([130], seed=12, geo=geo)
+    a = dict(num_k_heads=geo.num_k_heads, num_v_heads=geo.num_v_heads, head_k_dim=geo.head_k_dim,
+             head_v_dim=geo.head_v_dim, q_scale=geo.q_scale, state_in=inp["state0"])
+    base = oracle.prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"], inp["g"], inp["beta"], inp["z"],
+                          inp["norm_w"], **a)
+    mutd = oracle.prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"], inp["g"], inp["beta"], inp["z"],
+                          inp["norm_w"], mutation=mut, **a)
+    assert (base["out"] - mutd["out"]).abs().max() > 1e-3

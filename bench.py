@@ -1,0 +1,370 @@
+#!/usr/bin/env python3
+"""Benchmark of the GDN sublayer hot path on GB300 (one JSON line on stdout, rank 0).
+
+One step = one pass of the prefill sublayer over the 4 x 4096-token batch (conv1d+SiLU kernel,
+then the chunk-wise gated delta rule kernel with the sigmoid-gated RMSNorm fused; conv and
+recurrent states written), inputs resident in HBM.  The headline value is prefill tokens/s.
+The same line carries the fused decode step (256 sequences, one token each, 64 pre-generated
+steps cycled) in seq-steps/s, the roofline of the dominant kernels, an end-to-end number
+through host buffers, the fp64 CPU oracle timed on this host's cores, and the SM clocks seen
+during the timed region.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Under torchrun every rank runs an independent replica (the path has no exchange step); the
+reported value is the sum over ranks of the tokens processed divided by the slowest rank's
+time.  `--impl reference` times the CPU oracle itself on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s and decode seq-steps/s on 1 GB300; % of roofline"
+# algorithmic bytes of the chunk-prefill kernel: per token qkv 20480 + g 192 + beta 192 + z 12288
+# + out 12288; per sequence the fp32 state read and written (2 x 48 x 128 x 128 x 4)
+CHUNK_BYTES_PER_TOKEN = 20480 + 192 + 192 + 12288 + 12288
+STATE_BYTES_PER_SEQ = 2 * 48 * 128 * 128 * 4
+# algorithmic bytes of one decode step per sequence: state in+out, conv state in+out (3 x 10240
+# bf16 each way), x 20480, g+beta 384, z 12288, out 12288
+DECODE_BYTES_PER_SEQ = STATE_BYTES_PER_SEQ + 2 * 10240 * 3 * 2 + 20480 + 384 + 12288 + 12288
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-steps", type=int, default=640)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def traffic_record(kernel):
+    """ncu DRAM bytes per launch of `kernel`, if captured on the current source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+        src = os.path.join(ROOT, "linear_attention_ssm_gb300", "csrc", rec["source"])
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if digest != rec["source_sha256_16"]:
+            return None
+        return rec
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index):
+        import torch
+        ident = None
+        try:
+            ident = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            ident = vis.split(",")[device_index] if vis else str(device_index)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.06)
+        self.proc.terminate()
+        out = self.proc.communicate(timeout=10)[0]
+        sm, mx, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(inp, tokens_per_seq):
+    """The oracle (conv -> recurrence -> gated norm, fp64, all V heads) on the first
+    `tokens_per_seq` tokens of every sequence.  Returns (tokens/s, cores, description)."""
+    import torch
+    import oracle
+    from linear_attention_ssm_gb300.synth import cu_seqlens_of
+    lengths = inp["lengths"]
+    cu = inp["cu_seqlens"].tolist()
+    idx = torch.cat([torch.arange(cu[n], cu[n] + min(tokens_per_seq, lengths[n])) for n in range(len(lengths))])
+    sub = [min(tokens_per_seq, L) for L in lengths]
+    t0 = time.perf_counter()
+    oracle.prefill(inp["x"][idx], inp["conv_w"], cu_seqlens_of(sub), inp["g"][idx], inp["beta"][idx], inp["z"][idx],
+                   inp["norm_w"], 16, 48, 128, 128, inp["q_scale"], state_in=inp["state0"])
+    dt = time.perf_counter() - t0
+    ntok = sum(sub)
+    return ntok / dt, oracle.num_threads(), (f"first {tokens_per_seq} tokens of each of the {len(lengths)} "
+                                             f"sequences ({ntok} tokens, all 48 V heads), fp64, {dt:.2f} s")
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import torch  # noqa: F401
+    import oracle
+    from linear_attention_ssm_gb300.synth import BATCHED_LENGTHS, prefill_inputs
+    oracle.build()
+    inp = prefill_inputs(BATCHED_LENGTHS, seed=2)
+    per_step = 64
+    for _ in range(args.warmup):
+        cpu_oracle_sample(inp, per_step)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        tps, cores, desc = cpu_oracle_sample(inp, per_step)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    tokens = per_step * len(BATCHED_LENGTHS) * args.steps
+    value = tokens / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill 4 x 4096 tokens (sampled: first 64 tokens of each sequence per step)",
+                   "global_batch": 4, "seq_len": 4096, "parallelism": "cpu threads"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {desc}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import linear_attention_ssm_gb300 as gdn
+    from linear_attention_ssm_gb300 import build as gdn_build
+    from linear_attention_ssm_gb300.synth import (BATCHED_LENGTHS, DECODE_BATCH, DECODE_STEPS, decode_inputs,
+                                                  prefill_inputs)
+    if not os.path.exists(gdn.binding.LIB_PATH):
+        gdn_build.build()
+    gdn.load_library()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    hbm_peak, _, peak_kind = peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---------------- prefill, 4 x 4096 tokens
+    inp = prefill_inputs(BATCHED_LENGTHS, seed=2)
+    N, T = len(BATCHED_LENGTHS), sum(BATCHED_LENGTHS)
+    x, w, cu = inp["x"].to(dev), inp["conv_w"].to(dev), inp["cu_seqlens"].to(dev)
+    g, beta, z, nw = inp["g"].to(dev), inp["beta"].to(dev), inp["z"].to(dev), inp["norm_w"].to(dev)
+    state_in = inp["state0"].to(dev)
+    state_out = torch.empty_like(state_in)
+    cs_in = inp["conv_state0"].to(dev)
+    cs_out = torch.empty_like(cs_in)
+    qkv = torch.empty_like(x)
+    out = torch.empty((T, 48, 128), dtype=torch.bfloat16, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev_conv = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def prefill_step(i=None):
+        if i is not None:
+            ev_conv[i][0].record(stream)
+        gdn.gdn_conv1d_prefill(x, w, cu, cs_in, cs_out, qkv)
+        if i is not None:
+            ev_conv[i][1].record(stream)
+            ev[i][0].record(stream)
+        gdn.gdn_chunk_prefill(qkv, g, beta, cu, inp["q_scale"], 1e-6, state_in, state_out, z, nw, 1e-6, out)
+        if i is not None:
+            ev[i][1].record(stream)
+
+    for _ in range(max(args.warmup, 1)):
+        prefill_step()
+    gdn.gdn_check_device_errors()
+    barrier()
+    clocks = ClockSampler(local)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        prefill_step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    gdn.gdn_check_device_errors()
+    ms = max_over_ranks(start.elapsed_time(end))
+    ms_per_step = ms / args.steps
+    value = world * T / (ms_per_step / 1000.0)
+    chunk_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    conv_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_conv)
+    chunk_bytes = CHUNK_BYTES_PER_TOKEN * T + STATE_BYTES_PER_SEQ * N
+    chunk_gbs = chunk_bytes / (chunk_ms / 1000.0) / 1e9
+    rec = traffic_record("chunk_prefill")
+    roofline = {"kernel": "chunk_prefill (tcgen05, fused gated norm)", "bound": "hbm", "achieved": chunk_gbs,
+                "peak": hbm_peak, "unit": "GB/s", "frac": chunk_gbs / hbm_peak,
+                "peak_kind": peak_kind + " (copy bandwidth)",
+                "traffic": rec["bytes_per_launch"] if rec else None,
+                "algorithmic_bytes_per_launch": chunk_bytes, "avg_launch_ms": chunk_ms}
+    conv_bytes = T * 10240 * 2 * 2 + N * 10240 * 3 * 2 * 2 + 10240 * 4 * 2
+    conv_roof = {"kernel": "conv1d_prefill", "bound": "hbm", "achieved": conv_bytes / (conv_ms / 1000) / 1e9,
+                 "peak": hbm_peak, "unit": "GB/s", "avg_launch_ms": conv_ms}
+    conv_roof["frac"] = conv_roof["achieved"] / hbm_peak
+
+    # ---------------- end to end through host buffers (pinned), same step
+    h_x, h_g, h_b, h_z = (inp["x"].pin_memory(), inp["g"].pin_memory(), inp["beta"].pin_memory(),
+                          inp["z"].pin_memory())
+    h_state, h_cs = inp["state0"].pin_memory(), inp["conv_state0"].pin_memory()
+    h_out = torch.empty((T, 48, 128), dtype=torch.bfloat16).pin_memory()
+    h_state_out = torch.empty_like(h_state).pin_memory()
+    h_cs_out = torch.empty_like(h_cs).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_x, h_g, h_b, h_z, h_state, h_cs))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_state_out, h_cs_out))
+
+    def e2e_step():
+        x.copy_(h_x, non_blocking=True)
+        g.copy_(h_g, non_blocking=True)
+        beta.copy_(h_b, non_blocking=True)
+        z.copy_(h_z, non_blocking=True)
+        state_in.copy_(h_state, non_blocking=True)
+        cs_in.copy_(h_cs, non_blocking=True)
+        prefill_step()
+        h_out.copy_(out, non_blocking=True)
+        h_state_out.copy_(state_out, non_blocking=True)
+        h_cs_out.copy_(cs_out, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2)) / args.e2e_steps
+    e2e_value = world * T / (e2e_ms / 1000.0)
+    del h_x, h_g, h_b, h_z
+
+    # ---------------- decode: 256 sequences, 64 pre-generated steps cycled
+    del x, qkv, z, out
+    torch.cuda.empty_cache()
+    d = decode_inputs(DECODE_BATCH, DECODE_STEPS, seed=4)
+    B = DECODE_BATCH
+    dx, dg, db, dz = d["x"].to(dev), d["g"].to(dev), d["beta"].to(dev), d["z"].to(dev)
+    dw, dnw = d["conv_w"].to(dev), d["norm_w"].to(dev)
+    dstate, dcs = d["state0"].to(dev), d["conv_state0"].to(dev)
+    dout = torch.empty((B, 48, 128), dtype=torch.bfloat16, device=dev)
+
+    def decode_step(s):
+        gdn.gdn_decode_step(dx[s], dw, dcs, dg[s], db[s], dstate, dz[s], dnw, d["q_scale"], out=dout)
+
+    for s in range(max(args.warmup, 1)):
+        decode_step(s % DECODE_STEPS)
+    barrier()
+    s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s3.record(stream)
+    for s in range(args.decode_steps):
+        decode_step(s % DECODE_STEPS)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    gdn.gdn_check_device_errors()
+    dec_ms = max_over_ranks(s3.elapsed_time(e3)) / args.decode_steps
+    dec_bytes = DECODE_BYTES_PER_SEQ * B
+    dec_gbs = dec_bytes / (dec_ms / 1000) / 1e9
+    decode = {"metric": "decode seq-steps/s", "value": world * B / (dec_ms / 1000), "unit": "seq-steps/s",
+              "ms_per_step": dec_ms, "steps": args.decode_steps, "batch": B,
+              "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak,
+                           "unit": "GB/s", "frac": dec_gbs / hbm_peak, "traffic": None,
+                           "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_ms}}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu_baseline:
+        tps, cores, desc = cpu_oracle_sample(inp, 160)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "GDN prefill sublayer, 4 sequences x 4096 tokens (conv1d+SiLU -> chunk-wise "
+                                   "gated delta rule -> sigmoid-gated RMSNorm), Hk=16 Hv=48 Dk=Dv=128, chunk 64",
+                       "global_batch": 4 * world, "seq_len": 4096, "tokens_per_step_per_gpu": T,
+                       "l2": "inputs larger than L2 (x 335 MB per step)", "parallelism": f"replicas x{world}"},
+            "roofline": roofline, "roofline_conv": conv_roof,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "decode": decode, "cpu_baseline": cpu, "clocks": clk,
+            "gpu_launches": 3 * args.steps,
+            "arithmetic": "bf16 tensor-core operands (fp32 operands split into bf16 hi+lo), fp32 accumulate and state",
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet (GDN) sublayer library, libgdn.so.
+ *
+ * The sublayer, as the pages define it (pegainfer PR #1152 "Reference golden for the GDN
+ * sublayer", Summary and Code review; GLM-5.3-Flash kernel TDD ledger, slices I2-I4):
+ *
+ *   prefill:  x --(causal depthwise conv1d, width 4, + SiLU)--> qkv (bf16)
+ *             qkv --(head expansion by repeat_interleave, L2 norm of q and k,
+ *                    chunk-wise gated delta rule with an fp32 [value, key] state)--> o
+ *             o, z --(gated RMSNorm with a sigmoid output gate)--> out
+ *   decode:   the same for one token per sequence, fused in one launch (Qwen3.8 kernel
+ *             architecture and TDD ledger, "Current dense-27B kernel map": scalar GDN
+ *             recurrence and fused output gate).
+ *
+ * The recurrence (per sequence and V head; S is Dv x Dk, rows index the value dimension):
+ *   S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,    o_t = q_scale S_t q_t
+ * with k_t, q_t the L2-normalised key/query of K head floor(h / (Hv/Hk)).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous, row-major, and
+ *     16-byte aligned (else GDN_ERR_MISALIGNED).  The library never allocates, frees or keeps
+ *     a reference to caller memory after the call returns.
+ *   - bf16 tensors are passed as gdn_bf16 (raw 16-bit patterns); fp32 as float.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call is
+ *     asynchronous on that stream; arguments are validated on the host before any launch, and
+ *     a call that returns an error has launched nothing.
+ *   - Geometry: C = 2*Hk*Dk + Hv*Dv conv channels packed [q heads | k heads | v heads].  This
+ *     build supports Dk = Dv = 128, conv width 4, Hv a multiple of Hk, Hk <= 64, Hv <= 192;
+ *     anything else is refused with GDN_ERR_UNSUPPORTED_GEOMETRY, never silently mis-tiled.
+ *   - Device-side argument faults (for example a cu_seqlens array that is not monotonic or does
+ *     not end at total_tokens) are never turned into out-of-range accesses: the kernels clamp,
+ *     skip the bad sequence and raise a device error word, reported by gdn_check_device_errors.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+typedef uint16_t gdn_bf16; /* IEEE bfloat16 bit pattern */
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARGUMENT = 1,     /* null pointer, negative size, aliasing that is not allowed */
+  GDN_ERR_UNSUPPORTED_GEOMETRY = 2, /* geometry outside what the kernels are built for         */
+  GDN_ERR_MISALIGNED = 3,           /* a tensor pointer is not 16-byte aligned                  */
+  GDN_ERR_CUDA = 4,                 /* a CUDA runtime call or kernel launch failed              */
+  GDN_ERR_TIMEOUT = 5,              /* a bounded in-kernel wait ran out (device error word)     */
+  GDN_ERR_DEVICE_ARGUMENT = 6,      /* a kernel found a bad device-side argument (cu_seqlens)   */
+  GDN_ERR_WORKSPACE = 7             /* workspace missing or smaller than the queried size       */
+} gdn_status;
+
+/* Head geometry.  Pages: 16 K heads, 48 V heads, head dim 128, conv kernel 4
+ * (pegainfer PR #1152, Summary). */
+typedef struct {
+  int32_t num_k_heads; /* Hk */
+  int32_t num_v_heads; /* Hv, a multiple of Hk; V head h reads K head h / (Hv/Hk) */
+  int32_t head_k_dim;  /* Dk (128) */
+  int32_t head_v_dim;  /* Dv (128) */
+  int32_t conv_width;  /* W  (4)   */
+} gdn_geometry;
+
+/* Tokens per chunk of the chunk-wise prefill.  A chunk never crosses a sequence boundary.
+ * (pegainfer PR #1152, Validation: S=16/64 run one chunk, S=80/128 run two.) */
+#define GDN_CHUNK_SIZE 64
+
+/* Human-readable name of a status code (static storage). */
+GDN_API const char* gdn_status_string(gdn_status status);
+
+/* Detail of the last error returned on the calling host thread ("" if none). */
+GDN_API const char* gdn_last_error_message(void);
+
+/* Library version string (static storage). */
+GDN_API const char* gdn_version(void);
+
+/*
+ * Causal depthwise conv1d (width W, no bias) + SiLU over packed variable-length sequences.
+ * pegainfer PR #1152, Summary (depthwise conv, conv kernel 4, only conv1d.weight stored) and
+ * "Commands + measured numbers" (the conv leg, compared bit-exact); GLM-5.3-Flash ledger,
+ * slice I3 (a decode step equals the full width-4 causal convolution).
+ *
+ *   y[t, c] = bf16( silu( sum_{i<W} w[c, i] * xin(t - (W-1) + i, c) ) ),  silu(a) = a*sigmoid(a)
+ *
+ * where xin(p, c) is x[p, c] inside the token's own sequence, the conv state of that sequence
+ * for the W-1 positions before its start, and 0 when conv_state_in is NULL.  Accumulation is
+ * fp32; the result is rounded once to bf16 (round to nearest even).
+ *
+ *   x              [total_tokens, C] bf16
+ *   conv_w         [C, W] bf16; w[c, W-1] multiplies the current token
+ *   cu_seqlens     [num_seqs + 1] int32 (device): sequence n is tokens cu[n] .. cu[n+1]-1;
+ *                  cu[0] = 0, non-decreasing, cu[num_seqs] = total_tokens
+ *   conv_state_in  [num_seqs, C, W-1] bf16 raw inputs before each sequence (oldest first), or NULL
+ *   conv_state_out [num_seqs, C, W-1] bf16 last W-1 raw inputs of each sequence, or NULL; may be
+ *                  the same buffer as conv_state_in (updated in place)
+ *   y              [total_tokens, C] bf16; must not overlap x
+ * total_tokens == 0 or num_seqs == 0 is a no-op that returns GDN_OK.
+ */
+GDN_API gdn_status gdn_conv1d_prefill(const gdn_geometry* geo, const gdn_bf16* x,
+                                      const gdn_bf16* conv_w, const int32_t* cu_seqlens,
+                                      int32_t num_seqs, int32_t total_tokens,
+                                      const gdn_bf16* conv_state_in, gdn_bf16* conv_state_out,
+                                      gdn_bf16* y, void* stream);
+
+/*
+ * Bytes of device workspace gdn_chunk_prefill needs for these sizes (0 is possible).  The
+ * workspace holds the per-call sequence schedule; its contents need no initialisation.
+ */
+GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_geometry* geo, int32_t num_seqs,
+                                                int32_t total_tokens);
+
+/*
+ * Chunk-wise gated delta rule over packed variable-length sequences (prefill), optionally
+ * fused with the sigmoid-gated RMSNorm.  pegainfer PR #1152, Consumer (stage order
+ * prepare -> cumsum -> A -> solve -> recompute -> state -> output) and Code review (f32
+ * recurrent state carried across chunks); GLM-5.3-Flash ledger, slice I4 (the chunk path
+ * matches the sequential state and output at 63/64/65 tokens).
+ *
+ *   qkv        [total_tokens, C] bf16 conv output (gdn_conv1d_prefill's y): q heads | k heads | v heads
+ *   g, beta    [total_tokens, Hv] fp32 log decay (<= 0) and write strength
+ *   cu_seqlens [num_seqs + 1] int32 (device), as for gdn_conv1d_prefill
+ *   q_scale    output scale applied to S q (1/sqrt(Dk) for the pages' model)
+ *   l2_eps     epsilon of the q/k L2 norm x / sqrt(sum x^2 + eps) (1e-6)
+ *   state_in   [num_seqs, Hv, Dv, Dk] fp32 initial states ([value, key]), or NULL for zeros
+ *   state_out  [num_seqs, Hv, Dv, Dk] fp32 final states; may be the same buffer as state_in
+ *   z, norm_w  NULL: `out` receives o = q_scale S_t q_t (bf16).  Otherwise z [total_tokens, Hv, Dv]
+ *              and norm_w [Dv] bf16, and `out` receives the gated RMSNorm of o:
+ *              o * (mean_d o^2 + rms_eps)^(-1/2) * norm_w * sigmoid(z), computed from the fp32 o
+ *   out        [total_tokens, Hv, Dv] bf16
+ *   workspace  device memory of at least gdn_chunk_prefill_workspace_size() bytes (NULL if 0)
+ */
+GDN_API gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g,
+                                     const float* beta, const int32_t* cu_seqlens,
+                                     int32_t num_seqs, int32_t total_tokens, float q_scale,
+                                     float l2_eps, const float* state_in, float* state_out,
+                                     const gdn_bf16* z, const gdn_bf16* norm_w, float rms_eps,
+                                     gdn_bf16* out, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
+ * Sigmoid-gated RMSNorm, one row per (token, V head).  pegainfer PR #1152, Summary
+ * (output_gate_type "sigmoid"; the in-tree kernel that hard-codes silu is wrong) and Code
+ * review (rms_norm_eps == 1e-6).
+ *   out[r, d] = o[r, d] * (mean_d o[r, :]^2 + eps)^(-1/2) * norm_w[d] * sigmoid(z[r, d])
+ *   o, z, out  [total_tokens, Hv, Dv] bf16 (out may alias o);  norm_w [Dv] bf16
+ */
+GDN_API gdn_status gdn_gated_rmsnorm(const gdn_geometry* geo, const gdn_bf16* o, const gdn_bf16* z,
+                                     const gdn_bf16* norm_w, float eps, gdn_bf16* out,
+                                     int32_t total_tokens, void* stream);
+
+/*
+ * One fused decode step for `batch` independent sequences (one token each): conv step on the
+ * conv shift register + SiLU, L2 norm of q/k, the gated delta rule update of the fp32 state in
+ * place, and the sigmoid-gated RMSNorm.  Qwen3.8 kernel architecture and TDD ledger, "Current
+ * dense-27B kernel map" (scalar GDN recurrence and fused output gate); spark_model
+ * layer_struct.rs, the strided decode kernel fields (one launch for all sequences, state read
+ * once and written once).
+ *
+ *   x           [batch, C] bf16 raw conv input of this token
+ *   conv_w      [C, W] bf16
+ *   conv_state  [batch, C, W-1] bf16, in/out: the previous W-1 raw inputs, oldest first
+ *   g, beta     [batch, Hv] fp32
+ *   state       [batch, Hv, Dv, Dk] fp32, in/out
+ *   z           [batch, Hv, Dv] bf16;  norm_w [Dv] bf16
+ *   out         [batch, Hv, Dv] bf16 gated output
+ */
+GDN_API gdn_status gdn_decode_step(const gdn_geometry* geo, const gdn_bf16* x,
+                                   const gdn_bf16* conv_w, gdn_bf16* conv_state, const float* g,
+                                   const float* beta, float* state, const gdn_bf16* z,
+                                   const gdn_bf16* norm_w, float q_scale, float l2_eps,
+                                   float rms_eps, gdn_bf16* out, int32_t batch, void* stream);
+
+/*
+ * Waits for `stream`, then reads and clears the library's device error word.  Returns GDN_OK,
+ * GDN_ERR_DEVICE_ARGUMENT (a kernel skipped a sequence with bad cu_seqlens entries),
+ * GDN_ERR_TIMEOUT (a bounded in-kernel wait ran out) or GDN_ERR_CUDA.  The word is per device
+ * and shared by all streams; the kernels only ever set bits in it.
+ */
+GDN_API gdn_status gdn_check_device_errors(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

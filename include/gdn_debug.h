@@ -1,0 +1,37 @@
+/*
+ * gdn_debug.h -- verification hooks of libgdn.so (not needed on the hot path).
+ *
+ * The chunk-wise prefill has two builds of the same data flow: mode 0 issues every contraction
+ * on the tcgen05 tensor cores (the default and the product path), mode 1 replaces each MMA
+ * group by a CUDA-core loop that reads the same swizzled shared-memory operand tiles and writes
+ * the same tensor-memory accumulators.  Comparing the two isolates a fault to either the
+ * tensor-core descriptors or the surrounding data flow.  There is no counterpart on the pages.
+ */
+#ifndef GDN_DEBUG_H_
+#define GDN_DEBUG_H_
+
+#include "gdn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Select the chunk-prefill build used by later gdn_chunk_prefill calls in this process:
+ * 0 = tensor cores (default), 1 = CUDA-core emulation of the MMAs.  Not thread-safe. */
+GDN_API gdn_status gdn_debug_set_chunk_mode(int mode);
+
+/* The mode last selected (0 or 1). */
+GDN_API int gdn_debug_get_chunk_mode(void);
+
+/* One tensor-core tile, D = A * B^T: A [128][64] and B [n_cols][64] bf16 row-major (device),
+ * D [128][n_cols] fp32 (device), n_cols 64 or 128.  The operands are staged in the same
+ * 128-byte-swizzled K-major shared-memory layout and descriptors the chunk prefill uses.
+ * *status (device, caller-zeroed) gets bit 0 if the bounded wait for the MMA ran out. */
+GDN_API gdn_status gdn_debug_mma_probe(const gdn_bf16* A, const gdn_bf16* B, int n_cols, float* D,
+                                       unsigned* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_DEBUG_H_ */

@@ -5,3 +5,18 @@ The Python surface is a thin ctypes binding over the C entry points declared in
 the library; the first call does, and fails loudly when the CUDA library is missing.
 """
 from .synth import Geometry, QWEN_GDN  # noqa: F401
+from .binding import (  # noqa: F401
+    GdnError,
+    gdn_check_device_errors,
+    gdn_chunk_prefill,
+    gdn_chunk_prefill_workspace_size,
+    gdn_conv1d_prefill,
+    gdn_debug_get_chunk_mode,
+    gdn_debug_mma_probe,
+    gdn_debug_set_chunk_mode,
+    gdn_decode_step,
+    gdn_gated_rmsnorm,
+    gdn_prefill,
+    gdn_version,
+    load_library,
+)

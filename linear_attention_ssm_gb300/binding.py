@@ -1,0 +1,246 @@
+"""Thin ctypes binding of libgdn.so: one Python function per C entry point, same names.
+
+Argument marshalling only -- dtype/shape/device checks, output allocation when not supplied,
+and the current torch stream.  Every step of the computation runs in the library's CUDA kernels;
+there is no fallback of any kind: if ``libgdn.so`` is missing or cannot be loaded, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .synth import QWEN_GDN, Geometry
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn.so")
+
+GDN_OK = 0
+_lock = threading.Lock()
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, name: str, message: str):
+        super().__init__(f"{name}: {message}")
+        self.status = status
+        self.name = name
+
+
+class _Geo(ctypes.Structure):
+    _fields_ = [("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
+                ("head_k_dim", ctypes.c_int32), ("head_v_dim", ctypes.c_int32),
+                ("conv_width", ctypes.c_int32)]
+
+
+def load_library():
+    """Load libgdn.so (built by ``linear_attention_ssm_gb300.build``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m linear_attention_ssm_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        G = ctypes.POINTER(_Geo)
+        sig = {
+            "gdn_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "gdn_last_error_message": ([], ctypes.c_char_p),
+            "gdn_version": ([], ctypes.c_char_p),
+            "gdn_conv1d_prefill": ([G, P, P, P, I, I, P, P, P, P], ctypes.c_int),
+            "gdn_chunk_prefill_workspace_size": ([G, I, I], S),
+            "gdn_chunk_prefill": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P, S, P], ctypes.c_int),
+            "gdn_gated_rmsnorm": ([G, P, P, P, F, P, I, P], ctypes.c_int),
+            "gdn_decode_step": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
+            "gdn_check_device_errors": ([P], ctypes.c_int),
+            "gdn_debug_set_chunk_mode": ([ctypes.c_int], ctypes.c_int),
+            "gdn_debug_get_chunk_mode": ([], ctypes.c_int),
+            "gdn_debug_mma_probe": ([P, P, ctypes.c_int, P, P, P], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != GDN_OK:
+        lib = load_library()
+        name = lib.gdn_status_string(status).decode()
+        msg = lib.gdn_last_error_message().decode()
+        raise GdnError(status, name, msg)
+
+
+def _geo(geo: Geometry):
+    return ctypes.byref(_Geo(geo.num_k_heads, geo.num_v_heads, geo.head_k_dim, geo.head_v_dim,
+                             geo.conv_width))
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t, dtype, name, shape=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def gdn_version() -> str:
+    return load_library().gdn_version().decode()
+
+
+def gdn_conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in=None, conv_state_out=None, y=None,
+                       geometry: Geometry = QWEN_GDN, stream=None):
+    """Causal depthwise conv1d + SiLU over packed sequences; returns y [T, C] bf16."""
+    lib = load_library()
+    C, W = geometry.conv_dim, geometry.conv_width
+    _dev(x, torch.bfloat16, "x")
+    T = x.shape[0]
+    N = cu_seqlens.numel() - 1
+    _dev(x, torch.bfloat16, "x", (T, C))
+    _dev(conv_w, torch.bfloat16, "conv_w", (C, W))
+    _dev(cu_seqlens, torch.int32, "cu_seqlens", (N + 1,))
+    _dev(conv_state_in, torch.bfloat16, "conv_state_in", (N, C, W - 1))
+    _dev(conv_state_out, torch.bfloat16, "conv_state_out", (N, C, W - 1))
+    if y is None:
+        y = torch.empty((T, C), dtype=torch.bfloat16, device=x.device)
+    _dev(y, torch.bfloat16, "y", (T, C))
+    _check(lib.gdn_conv1d_prefill(_geo(geometry), _p(x), _p(conv_w), _p(cu_seqlens), N, T,
+                                  _p(conv_state_in), _p(conv_state_out), _p(y), _stream(stream)))
+    return y
+
+
+def gdn_chunk_prefill_workspace_size(num_seqs: int, total_tokens: int,
+                                     geometry: Geometry = QWEN_GDN) -> int:
+    return int(load_library().gdn_chunk_prefill_workspace_size(_geo(geometry), num_seqs, total_tokens))
+
+
+def gdn_chunk_prefill(qkv, g, beta, cu_seqlens, q_scale, l2_eps=1e-6, state_in=None, state_out=None,
+                      z=None, norm_w=None, rms_eps=1e-6, out=None, workspace=None,
+                      geometry: Geometry = QWEN_GDN, stream=None):
+    """Chunk-wise gated delta rule (optionally fused with the gated RMSNorm when z is given).
+
+    Returns out [T, Hv, Dv] bf16 (o itself when z is None).  state_out, when given, receives the
+    final fp32 states [N, Hv, Dv, Dk]; it may be state_in itself.
+    """
+    lib = load_library()
+    C, hv, dv, dk = geometry.conv_dim, geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
+    N = cu_seqlens.numel() - 1
+    T = qkv.shape[0]
+    _dev(qkv, torch.bfloat16, "qkv", (T, C))
+    _dev(g, torch.float32, "g", (T, hv))
+    _dev(beta, torch.float32, "beta", (T, hv))
+    _dev(cu_seqlens, torch.int32, "cu_seqlens", (N + 1,))
+    _dev(state_in, torch.float32, "state_in", (N, hv, dv, dk))
+    _dev(state_out, torch.float32, "state_out", (N, hv, dv, dk))
+    _dev(z, torch.bfloat16, "z", (T, hv, dv))
+    _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
+    if out is None:
+        out = torch.empty((T, hv, dv), dtype=torch.bfloat16, device=qkv.device)
+    _dev(out, torch.bfloat16, "out", (T, hv, dv))
+    need = lib.gdn_chunk_prefill_workspace_size(_geo(geometry), N, T)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=qkv.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.gdn_chunk_prefill(_geo(geometry), _p(qkv), _p(g), _p(beta), _p(cu_seqlens), N, T,
+                                 float(q_scale), float(l2_eps), _p(state_in), _p(state_out), _p(z),
+                                 _p(norm_w), float(rms_eps), _p(out), _p(workspace), wbytes,
+                                 _stream(stream)))
+    return out
+
+
+def gdn_gated_rmsnorm(o, z, norm_w, eps=1e-6, out=None, geometry: Geometry = QWEN_GDN, stream=None):
+    lib = load_library()
+    hv, dv = geometry.num_v_heads, geometry.head_v_dim
+    T = o.shape[0]
+    _dev(o, torch.bfloat16, "o", (T, hv, dv))
+    _dev(z, torch.bfloat16, "z", (T, hv, dv))
+    _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
+    if out is None:
+        out = torch.empty_like(o)
+    _dev(out, torch.bfloat16, "out", (T, hv, dv))
+    _check(lib.gdn_gated_rmsnorm(_geo(geometry), _p(o), _p(z), _p(norm_w), float(eps), _p(out), T,
+                                 _stream(stream)))
+    return out
+
+
+def gdn_decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps=1e-6,
+                    rms_eps=1e-6, out=None, geometry: Geometry = QWEN_GDN, stream=None):
+    """One fused decode step; conv_state and state are updated in place.  Returns out."""
+    lib = load_library()
+    C, W = geometry.conv_dim, geometry.conv_width
+    hv, dv, dk = geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
+    B = x.shape[0]
+    _dev(x, torch.bfloat16, "x", (B, C))
+    _dev(conv_w, torch.bfloat16, "conv_w", (C, W))
+    _dev(conv_state, torch.bfloat16, "conv_state", (B, C, W - 1))
+    _dev(g, torch.float32, "g", (B, hv))
+    _dev(beta, torch.float32, "beta", (B, hv))
+    _dev(state, torch.float32, "state", (B, hv, dv, dk))
+    _dev(z, torch.bfloat16, "z", (B, hv, dv))
+    _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
+    if out is None:
+        out = torch.empty((B, hv, dv), dtype=torch.bfloat16, device=x.device)
+    _dev(out, torch.bfloat16, "out", (B, hv, dv))
+    _check(lib.gdn_decode_step(_geo(geometry), _p(x), _p(conv_w), _p(conv_state), _p(g), _p(beta),
+                               _p(state), _p(z), _p(norm_w), float(q_scale), float(l2_eps),
+                               float(rms_eps), _p(out), B, _stream(stream)))
+    return out
+
+
+def gdn_check_device_errors(stream=None):
+    """Synchronise the stream and raise GdnError if a kernel flagged a device-side fault."""
+    _check(load_library().gdn_check_device_errors(_stream(stream)))
+
+
+def gdn_debug_set_chunk_mode(mode: int):
+    _check(load_library().gdn_debug_set_chunk_mode(int(mode)))
+
+
+def gdn_debug_get_chunk_mode() -> int:
+    return int(load_library().gdn_debug_get_chunk_mode())
+
+
+def gdn_debug_mma_probe(A, B, stream=None):
+    """D = A @ B.T on one tcgen05 tile (A [128, 64], B [64 or 128, 64] bf16 CUDA tensors)."""
+    lib = load_library()
+    _dev(A, torch.bfloat16, "A", (128, 64))
+    n = B.shape[0]
+    _dev(B, torch.bfloat16, "B", (n, 64))
+    D = torch.full((128, n), float("nan"), dtype=torch.float32, device=A.device)
+    status = torch.zeros(1, dtype=torch.int32, device=A.device)
+    _check(lib.gdn_debug_mma_probe(_p(A), _p(B), n, _p(D), _p(status), _stream(stream)))
+    return D, status
+
+
+def gdn_prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, q_scale, l2_eps=1e-6, rms_eps=1e-6,
+                state_in=None, state_out=None, conv_state_in=None, conv_state_out=None,
+                qkv_buf=None, out=None, geometry: Geometry = QWEN_GDN, stream=None):
+    """The whole prefill sublayer: gdn_conv1d_prefill, then gdn_chunk_prefill with the gated
+    RMSNorm fused into its epilogue.  Returns out [T, Hv, Dv] bf16."""
+    qkv = gdn_conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in, conv_state_out, qkv_buf,
+                             geometry=geometry, stream=stream)
+    return gdn_chunk_prefill(qkv, g, beta, cu_seqlens, q_scale, l2_eps, state_in, state_out, z,
+                             norm_w, rms_eps, out, geometry=geometry, stream=stream)

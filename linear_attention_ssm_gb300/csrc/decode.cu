@@ -1,0 +1,198 @@
+// decode.cu -- one fused GDN decode step: conv step + SiLU, L2 norm of q/k, gated delta rule
+// update of the fp32 state in place, sigmoid-gated RMSNorm.
+//
+// Qwen3.8 kernel architecture and TDD ledger, "Current dense-27B kernel map" (scalar GDN
+// recurrence and fused output gate); spark_model layer_struct.rs, fields of the strided decode
+// kernels (one launch for all sequences; the state read once and written once, 1R+1W);
+// GLM-5.3-Flash kernel TDD ledger, slice I3 (a conv step equals the full width-4 causal conv).
+//
+// One CTA per (sequence, K head): it owns the q/k channels of that K head and the v channels of
+// the Hv/Hk V heads that read it, so no two CTAs touch the same conv-state channel and the
+// in-place conv-state update is race-free.  Each warp streams 16 rows ([value] index) of a
+// head's 128 x 128 state: a row is 32 lanes x float4 over the key dimension, so both
+// contractions (S k and S q) are warp-shuffle reductions and every state byte is read once and
+// written once.
+#include "gdn_common.cuh"
+#include "gdn_kernels.h"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRowsPerWarp = kHeadDim / (kThreads / 32);  // 16
+constexpr int kMaxRatio = 12;                             // V heads per K head handled by one CTA
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ conv_w, uint16_t* conv_state,
+    const float* __restrict__ g, const float* __restrict__ beta, float* state,
+    const uint16_t* __restrict__ z, const uint16_t* __restrict__ norm_w, float q_scale, float l2_eps,
+    float rms_eps, uint16_t* __restrict__ out, int Hk, int Hv) {
+  const int j = blockIdx.x;        // K head
+  const int b = blockIdx.y;        // sequence
+  const int R = Hv / Hk;
+  const int C = 2 * Hk * kHeadDim + Hv * kHeadDim;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  __shared__ float s_q[kHeadDim], s_k[kHeadDim];
+  __shared__ float s_v[kMaxRatio][kHeadDim];
+  __shared__ float s_o[kMaxRatio][kHeadDim];
+  __shared__ float s_norm[2];
+
+  // ---- conv step + SiLU for the CTA's 32 + 16R channel octets
+  const int n_oct = 32 + 16 * R;
+  if (tid < n_oct) {
+    int c;
+    float* dst;
+    if (tid < 16) { c = j * kHeadDim + tid * 8; dst = s_q + tid * 8; }
+    else if (tid < 32) { c = Hk * kHeadDim + j * kHeadDim + (tid - 16) * 8; dst = s_k + (tid - 16) * 8; }
+    else {
+      const int hh = (tid - 32) >> 4, o = (tid - 32) & 15;
+      c = 2 * Hk * kHeadDim + (j * R + hh) * kHeadDim + o * 8;
+      dst = s_v[hh] + o * 8;
+    }
+    float xv[8], wv[32], st[24];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(x + (size_t)b * C + c)), xv);
+    const uint4* wp = reinterpret_cast<const uint4*>(conv_w + (size_t)c * kConvWidth);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float t8[8];
+      unpack8(__ldg(wp + i), t8);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) wv[i * 8 + e] = t8[e];
+    }
+    uint4* sp = reinterpret_cast<uint4*>(conv_state + ((size_t)b * C + c) * (kConvWidth - 1));
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      float t8[8];
+      unpack8(sp[i], t8);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) st[i * 8 + e] = t8[e];
+    }
+    // channel ch: weights wv[ch*4 + 0..3], state st[ch*3 + 0..2] (oldest first)
+    float ns[24];
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      float acc = wv[ch * 4 + 0] * st[ch * 3 + 0];
+      acc = fmaf(wv[ch * 4 + 1], st[ch * 3 + 1], acc);
+      acc = fmaf(wv[ch * 4 + 2], st[ch * 3 + 2], acc);
+      acc = fmaf(wv[ch * 4 + 3], xv[ch], acc);
+      dst[ch] = bf2f(f2bf(acc / (1.0f + expf(-acc))));  // the bf16 conv output
+      ns[ch * 3 + 0] = st[ch * 3 + 1];
+      ns[ch * 3 + 1] = st[ch * 3 + 2];
+      ns[ch * 3 + 2] = xv[ch];
+    }
+    uint32_t pk[12];
+#pragma unroll
+    for (int i = 0; i < 12; ++i) pk[i] = pack_bf2(ns[2 * i], ns[2 * i + 1]);  // exact (bf16 inputs)
+    sp[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    sp[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    sp[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+  }
+  __syncthreads();
+
+  // ---- L2 norms of q and k: x / sqrt(sum x^2 + eps)
+  if (warp < 2) {
+    const float* src = warp == 0 ? s_q : s_k;
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { const float v = src[lane * 4 + i]; ss = fmaf(v, v, ss); }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    if (lane == 0) s_norm[warp] = rsqrtf(ss + l2_eps);
+  }
+  __syncthreads();
+  const float4 qn = make_float4(s_q[lane * 4] * s_norm[0], s_q[lane * 4 + 1] * s_norm[0],
+                                s_q[lane * 4 + 2] * s_norm[0], s_q[lane * 4 + 3] * s_norm[0]);
+  const float4 kn = make_float4(s_k[lane * 4] * s_norm[1], s_k[lane * 4 + 1] * s_norm[1],
+                                s_k[lane * 4 + 2] * s_norm[1], s_k[lane * 4 + 3] * s_norm[1]);
+
+  // ---- state update, one V head at a time
+  for (int hh = 0; hh < R; ++hh) {
+    const int h = j * R + hh;
+    const float alpha = expf(__ldg(g + (size_t)b * Hv + h));
+    const float bt = __ldg(beta + (size_t)b * Hv + h);
+    float4* S = reinterpret_cast<float4*>(state + (((size_t)b * Hv + h) * kHeadDim + warp * kRowsPerWarp) * kHeadDim);
+    float4 row[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) row[i] = S[i * 32 + lane];
+    float d[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i)
+      d[i] = row[i].x * kn.x + row[i].y * kn.y + row[i].z * kn.z + row[i].w * kn.w;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) d[i] += __shfl_xor_sync(0xffffffffu, d[i], m);
+    float o[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int r = warp * kRowsPerWarp + i;
+      const float e = bt * (s_v[hh][r] - alpha * d[i]);  // delta against the decayed state
+      float4 sn;
+      sn.x = fmaf(alpha, row[i].x, e * kn.x);
+      sn.y = fmaf(alpha, row[i].y, e * kn.y);
+      sn.z = fmaf(alpha, row[i].z, e * kn.z);
+      sn.w = fmaf(alpha, row[i].w, e * kn.w);
+      S[i * 32 + lane] = sn;
+      o[i] = sn.x * qn.x + sn.y * qn.y + sn.z * qn.z + sn.w * qn.w;
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) o[i] += __shfl_xor_sync(0xffffffffu, o[i], m);
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) s_o[hh][warp * kRowsPerWarp + i] = q_scale * o[i];
+    }
+  }
+  __syncthreads();
+
+  // ---- sigmoid-gated RMSNorm of each V head's 128 outputs
+  for (int hh = warp; hh < R; hh += kThreads / 32) {
+    const int h = j * R + hh;
+    float ov[4], ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { ov[i] = s_o[hh][lane * 4 + i]; ss = fmaf(ov[i], ov[i], ss); }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    const float rstd = rsqrtf(ss * (1.0f / kHeadDim) + rms_eps);
+    const size_t base = ((size_t)b * Hv + h) * kHeadDim + lane * 4;
+    const uint2 zz = __ldg(reinterpret_cast<const uint2*>(z + base));
+    const uint2 ww = __ldg(reinterpret_cast<const uint2*>(norm_w + lane * 4));
+    const float zf[4] = {__uint_as_float(zz.x << 16), __uint_as_float(zz.x & 0xFFFF0000u),
+                         __uint_as_float(zz.y << 16), __uint_as_float(zz.y & 0xFFFF0000u)};
+    const float wf[4] = {__uint_as_float(ww.x << 16), __uint_as_float(ww.x & 0xFFFF0000u),
+                         __uint_as_float(ww.y << 16), __uint_as_float(ww.y & 0xFFFF0000u)};
+    float r4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r4[i] = ov[i] * rstd * wf[i] * sigmoidf_(zf[i]);
+    *reinterpret_cast<uint2*>(out + base) = make_uint2(pack_bf2(r4[0], r4[1]), pack_bf2(r4[2], r4[3]));
+  }
+}
+
+}  // namespace
+
+int decode_max_ratio() { return kMaxRatio; }
+
+cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
+                               uint16_t* conv_state, const float* g, const float* beta, float* state,
+                               const uint16_t* z, const uint16_t* norm_w, float q_scale, float l2_eps,
+                               float rms_eps, uint16_t* out, int B, int Hk, int Hv) {
+  if (B <= 0) return cudaSuccess;
+  dim3 grid(Hk, B);
+  decode_step_kernel<<<grid, kThreads, 0, env.stream>>>(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale,
+                                                        l2_eps, rms_eps, out, Hk, Hv);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,281 @@
+// gdn_api.cu -- the C ABI of libgdn.so: host-side validation, then one launch per call.
+//
+// Every entry point checks its arguments on the host before it launches anything; a call that
+// returns an error has launched nothing.  Device-side faults (bad cu_seqlens contents, a bounded
+// wait that ran out) set bits in a per-device error word that gdn_check_device_errors() reads.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/gdn.h"
+#include "../../include/gdn_debug.h"
+#include "gdn_common.cuh"
+#include "gdn_kernels.h"
+
+namespace {
+
+__device__ unsigned g_gdn_error_word;
+
+thread_local std::string g_last_error;
+int g_chunk_mode = 0;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {nullptr};
+
+gdn_status fail(gdn_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+gdn_status fail(gdn_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+gdn_status ok() {
+  g_last_error.clear();
+  return GDN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na && nb && x < y + nb && y < x + na;
+}
+
+gdn_status check_geometry(const gdn_geometry* geo) {
+  if (!geo) return fail(GDN_ERR_INVALID_ARGUMENT, "geometry is NULL");
+  if (geo->num_k_heads <= 0 || geo->num_v_heads <= 0 || geo->num_v_heads % geo->num_k_heads != 0)
+    return fail(GDN_ERR_UNSUPPORTED_GEOMETRY, "num_v_heads (%d) must be a positive multiple of num_k_heads (%d)",
+                geo->num_v_heads, geo->num_k_heads);
+  if (geo->head_k_dim != gdn::kHeadDim || geo->head_v_dim != gdn::kHeadDim)
+    return fail(GDN_ERR_UNSUPPORTED_GEOMETRY, "head dims must be %d (got Dk=%d, Dv=%d)", gdn::kHeadDim,
+                geo->head_k_dim, geo->head_v_dim);
+  if (geo->conv_width != gdn::kConvWidth)
+    return fail(GDN_ERR_UNSUPPORTED_GEOMETRY, "conv width must be %d (got %d)", gdn::kConvWidth, geo->conv_width);
+  if (geo->num_k_heads > 64 || geo->num_v_heads > 192)
+    return fail(GDN_ERR_UNSUPPORTED_GEOMETRY, "at most 64 K heads and 192 V heads (got %d, %d)", geo->num_k_heads,
+                geo->num_v_heads);
+  return GDN_OK;
+}
+
+int conv_channels(const gdn_geometry* g) {
+  return 2 * g->num_k_heads * g->head_k_dim + g->num_v_heads * g->head_v_dim;
+}
+
+#define GDN_REQUIRE(ptr, name)                                                            \
+  do {                                                                                    \
+    if (!(ptr)) return fail(GDN_ERR_INVALID_ARGUMENT, "%s is NULL", name);                \
+    if (!aligned16(ptr)) return fail(GDN_ERR_MISALIGNED, "%s is not 16-byte aligned", name); \
+  } while (0)
+#define GDN_OPTIONAL(ptr, name)                                                           \
+  do {                                                                                    \
+    if ((ptr) && !aligned16(ptr)) return fail(GDN_ERR_MISALIGNED, "%s is not 16-byte aligned", name); \
+  } while (0)
+
+gdn_status make_env(void* stream, gdn::LaunchEnv* env) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(GDN_ERR_CUDA, "device index %d out of range", dev);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_gdn_error_word);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  env->err = g_err_ptr[dev];
+  env->num_sms = 0;
+  env->stream = static_cast<cudaStream_t>(stream);
+  return GDN_OK;
+}
+
+gdn_status launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARGUMENT: return "GDN_ERR_INVALID_ARGUMENT";
+    case GDN_ERR_UNSUPPORTED_GEOMETRY: return "GDN_ERR_UNSUPPORTED_GEOMETRY";
+    case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+    case GDN_ERR_DEVICE_ARGUMENT: return "GDN_ERR_DEVICE_ARGUMENT";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+  }
+  return "GDN_ERR_UNKNOWN";
+}
+
+const char* gdn_last_error_message(void) { return g_last_error.c_str(); }
+
+const char* gdn_version(void) { return "gdn-gb300 0.1 (sm_103a)"; }
+
+gdn_status gdn_conv1d_prefill(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w,
+                              const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                              const gdn_bf16* conv_state_in, gdn_bf16* conv_state_out, gdn_bf16* y, void* stream) {
+  gdn_status s = check_geometry(geo);
+  if (s != GDN_OK) return s;
+  if (num_seqs < 0 || total_tokens < 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "negative size (num_seqs=%d, total_tokens=%d)", num_seqs, total_tokens);
+  if (num_seqs == 0 && total_tokens > 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "total_tokens=%d with no sequence", total_tokens);
+  if (num_seqs == 0) return ok();
+  GDN_REQUIRE(conv_w, "conv_w");
+  if (!cu_seqlens) return fail(GDN_ERR_INVALID_ARGUMENT, "cu_seqlens is NULL");
+  if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) return fail(GDN_ERR_MISALIGNED, "cu_seqlens is not 4-byte aligned");
+  GDN_OPTIONAL(conv_state_in, "conv_state_in");
+  GDN_OPTIONAL(conv_state_out, "conv_state_out");
+  const int C = conv_channels(geo);
+  if (total_tokens > 0) {
+    GDN_REQUIRE(x, "x");
+    GDN_REQUIRE(y, "y");
+    const size_t bytes = (size_t)total_tokens * C * 2;
+    if (overlaps(x, bytes, y, bytes)) return fail(GDN_ERR_INVALID_ARGUMENT, "y overlaps x");
+  } else if (!conv_state_out) {
+    return ok();
+  }
+  gdn::LaunchEnv env;
+  if ((s = make_env(stream, &env)) != GDN_OK) return s;
+  return launched(gdn::launch_conv1d_prefill(env, x, conv_w, cu_seqlens, num_seqs, total_tokens, C, conv_state_in,
+                                             conv_state_out, y),
+                  "conv1d launch");
+}
+
+size_t gdn_chunk_prefill_workspace_size(const gdn_geometry* geo, int32_t num_seqs, int32_t total_tokens) {
+  (void)geo;
+  (void)num_seqs;
+  (void)total_tokens;
+  return 0;
+}
+
+gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g, const float* beta,
+                             const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens, float q_scale,
+                             float l2_eps, const float* state_in, float* state_out, const gdn_bf16* z,
+                             const gdn_bf16* norm_w, float rms_eps, gdn_bf16* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  gdn_status s = check_geometry(geo);
+  if (s != GDN_OK) return s;
+  if (num_seqs < 0 || total_tokens < 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "negative size (num_seqs=%d, total_tokens=%d)", num_seqs, total_tokens);
+  if (num_seqs == 0 && total_tokens > 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "total_tokens=%d with no sequence", total_tokens);
+  if ((long)num_seqs * geo->num_v_heads > 0x7FFFFFFFL)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "num_seqs * num_v_heads exceeds the grid limit");
+  if (num_seqs == 0) return ok();
+  if (!cu_seqlens) return fail(GDN_ERR_INVALID_ARGUMENT, "cu_seqlens is NULL");
+  if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) return fail(GDN_ERR_MISALIGNED, "cu_seqlens is not 4-byte aligned");
+  if (total_tokens > 0) {
+    GDN_REQUIRE(qkv, "qkv");
+    GDN_REQUIRE(out, "out");
+    if (!g || !beta) return fail(GDN_ERR_INVALID_ARGUMENT, "g or beta is NULL");
+    if ((reinterpret_cast<uintptr_t>(g) | reinterpret_cast<uintptr_t>(beta)) & 3u)
+      return fail(GDN_ERR_MISALIGNED, "g or beta is not 4-byte aligned");
+  }
+  GDN_OPTIONAL(state_in, "state_in");
+  GDN_OPTIONAL(state_out, "state_out");
+  if (z) {
+    GDN_REQUIRE(z, "z");
+    GDN_REQUIRE(norm_w, "norm_w");
+  }
+  if (!(l2_eps >= 0.f) || !(rms_eps >= 0.f)) return fail(GDN_ERR_INVALID_ARGUMENT, "eps must be >= 0");
+  const size_t need = gdn_chunk_prefill_workspace_size(geo, num_seqs, total_tokens);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need, workspace_bytes);
+  if (state_in && state_out && state_in != state_out) {
+    const size_t sb = (size_t)num_seqs * geo->num_v_heads * gdn::kHeadDim * gdn::kHeadDim * 4;
+    if (overlaps(state_in, sb, state_out, sb))
+      return fail(GDN_ERR_INVALID_ARGUMENT, "state_out partially overlaps state_in");
+  }
+  gdn::LaunchEnv env;
+  if ((s = make_env(stream, &env)) != GDN_OK) return s;
+  return launched(gdn::launch_chunk_prefill(env, g_chunk_mode, qkv, g, beta, cu_seqlens, num_seqs, total_tokens,
+                                            geo->num_k_heads, geo->num_v_heads, q_scale, l2_eps, state_in,
+                                            state_out, z, norm_w, rms_eps, out),
+                  "chunk prefill launch");
+}
+
+gdn_status gdn_gated_rmsnorm(const gdn_geometry* geo, const gdn_bf16* o, const gdn_bf16* z, const gdn_bf16* norm_w,
+                             float eps, gdn_bf16* out, int32_t total_tokens, void* stream) {
+  gdn_status s = check_geometry(geo);
+  if (s != GDN_OK) return s;
+  if (total_tokens < 0) return fail(GDN_ERR_INVALID_ARGUMENT, "negative total_tokens");
+  if (total_tokens == 0) return ok();
+  GDN_REQUIRE(o, "o");
+  GDN_REQUIRE(z, "z");
+  GDN_REQUIRE(norm_w, "norm_w");
+  GDN_REQUIRE(out, "out");
+  if (!(eps >= 0.f)) return fail(GDN_ERR_INVALID_ARGUMENT, "eps must be >= 0");
+  gdn::LaunchEnv env;
+  if ((s = make_env(stream, &env)) != GDN_OK) return s;
+  return launched(gdn::launch_gated_rmsnorm(env, o, z, norm_w, eps, out, (long)total_tokens * geo->num_v_heads),
+                  "gated rmsnorm launch");
+}
+
+gdn_status gdn_decode_step(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w, gdn_bf16* conv_state,
+                           const float* g, const float* beta, float* state, const gdn_bf16* z,
+                           const gdn_bf16* norm_w, float q_scale, float l2_eps, float rms_eps, gdn_bf16* out,
+                           int32_t batch, void* stream) {
+  gdn_status s = check_geometry(geo);
+  if (s != GDN_OK) return s;
+  if (geo->num_v_heads / geo->num_k_heads > gdn::decode_max_ratio())
+    return fail(GDN_ERR_UNSUPPORTED_GEOMETRY, "decode supports at most %d V heads per K head",
+                gdn::decode_max_ratio());
+  if (batch < 0 || batch > 65535) return fail(GDN_ERR_INVALID_ARGUMENT, "batch must be in [0, 65535] (got %d)", batch);
+  if (batch == 0) return ok();
+  GDN_REQUIRE(x, "x");
+  GDN_REQUIRE(conv_w, "conv_w");
+  GDN_REQUIRE(conv_state, "conv_state");
+  GDN_REQUIRE(state, "state");
+  GDN_REQUIRE(z, "z");
+  GDN_REQUIRE(norm_w, "norm_w");
+  GDN_REQUIRE(out, "out");
+  if (!g || !beta) return fail(GDN_ERR_INVALID_ARGUMENT, "g or beta is NULL");
+  if ((reinterpret_cast<uintptr_t>(g) | reinterpret_cast<uintptr_t>(beta)) & 3u)
+    return fail(GDN_ERR_MISALIGNED, "g or beta is not 4-byte aligned");
+  if (!(l2_eps >= 0.f) || !(rms_eps >= 0.f)) return fail(GDN_ERR_INVALID_ARGUMENT, "eps must be >= 0");
+  gdn::LaunchEnv env;
+  if ((s = make_env(stream, &env)) != GDN_OK) return s;
+  return launched(gdn::launch_decode_step(env, x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps,
+                                          rms_eps, out, batch, geo->num_k_heads, geo->num_v_heads),
+                  "decode launch");
+}
+
+gdn_status gdn_check_device_errors(void* stream) {
+  gdn::LaunchEnv env;
+  gdn_status s = make_env(stream, &env);
+  if (s != GDN_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(env.stream);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  unsigned word = 0;
+  e = cudaMemcpy(&word, env.err, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
+  if (word) {
+    const unsigned zero = 0;
+    e = cudaMemcpy(env.err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "clearing the device error word: %s", cudaGetErrorString(e));
+  }
+  if (word & gdn::kErrTimeout) return fail(GDN_ERR_TIMEOUT, "an in-kernel wait ran out (word 0x%x)", word);
+  if (word & gdn::kErrDeviceArgument)
+    return fail(GDN_ERR_DEVICE_ARGUMENT, "a kernel rejected cu_seqlens contents (word 0x%x)", word);
+  return ok();
+}
+
+gdn_status gdn_debug_set_chunk_mode(int mode) {
+  if (mode != 0 && mode != 1) return fail(GDN_ERR_INVALID_ARGUMENT, "mode must be 0 or 1");
+  g_chunk_mode = mode;
+  return ok();
+}
+
+int gdn_debug_get_chunk_mode(void) { return g_chunk_mode; }
+
+}  // extern "C"

@@ -1,0 +1,30 @@
+// gdn_kernels.h -- internal launch functions of the GDN kernels (host side of each .cu file).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+cudaError_t launch_conv1d_prefill(const LaunchEnv& env, const uint16_t* x, const uint16_t* w, const int32_t* cu,
+                                  int N, int T, int C, const uint16_t* state_in, uint16_t* state_out,
+                                  uint16_t* y);
+
+cudaError_t launch_gated_rmsnorm(const LaunchEnv& env, const uint16_t* o, const uint16_t* z, const uint16_t* w,
+                                 float eps, uint16_t* out, long rows);
+
+int decode_max_ratio();
+cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
+                               uint16_t* conv_state, const float* g, const float* beta, float* state,
+                               const uint16_t* z, const uint16_t* norm_w, float q_scale, float l2_eps,
+                               float rms_eps, uint16_t* out, int B, int Hk, int Hv);
+
+// mode 0: tcgen05 tensor cores; mode 1: the same data flow with the MMAs emulated on CUDA cores
+cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t* qkv, const float* g,
+                                 const float* beta, const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale,
+                                 float l2_eps, const float* state_in, float* state_out, const uint16_t* z,
+                                 const uint16_t* norm_w, float rms_eps, uint16_t* out);
+
+}  // namespace gdn

@@ -1,0 +1,95 @@
+"""Shared helpers of the GPU parity tests: tolerances, guard (canary) buffers, comparisons."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+# Tolerances of the GDN sublayer's GPU path against the fp64 oracle:
+#   output:      max |got - want| <= 2e-2 * max |want|       (bf16 output)
+#   final state: ||got - want||_2 <= 1e-4 * ||want||_2         (fp32 state)
+#   conv output: within one bf16 ulp of the oracle's rounding of the exact value
+OUT_TOL = 2e-2
+STATE_TOL = 1e-4
+NEG_CONTROL_RATIO = 10.0  # a planted fault must exceed the output bound by this factor
+
+DEV = "cuda"
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def lib():
+    need_gpu()
+    import linear_attention_ssm_gb300 as g
+    g.load_library()
+    return g
+
+
+def to_dev(t):
+    return None if t is None else t.to(DEV).contiguous()
+
+
+def out_error_ratio(got, want):
+    """max |got - want| / (OUT_TOL * max |want|): <= 1 passes."""
+    got = got.detach().double().cpu()
+    want = want.detach().double().cpu()
+    bound = OUT_TOL * want.abs().max().item()
+    err = (got - want).abs().max().item()
+    return err / bound if bound > 0 else (0.0 if err == 0 else float("inf"))
+
+
+def assert_out_close(got, want, what="out"):
+    r = out_error_ratio(got, want)
+    assert torch.isfinite(got.detach().float()).all(), f"{what}: non-finite values"
+    assert r <= 1.0, f"{what}: max error is {r:.3g}x the bound ({OUT_TOL} * absmax)"
+    return r
+
+
+def state_rel_l2(got, want):
+    got = got.detach().double().cpu()
+    want = want.detach().double().cpu()
+    return ((got - want).norm() / want.norm().clamp_min(1e-300)).item()
+
+
+def assert_state_close(got, want, what="state"):
+    assert torch.isfinite(got.detach().float()).all(), f"{what}: non-finite values"
+    r = state_rel_l2(got, want)
+    assert r <= STATE_TOL, f"{what}: relative L2 error {r:.3g} > {STATE_TOL}"
+    return r
+
+
+def assert_bf16_within_one_ulp(got, want, what="conv"):
+    a = got.detach().cpu().view(torch.int16).int()
+    b = want.detach().cpu().view(torch.int16).int()
+    # same sign => adjacent patterns differ by one; +0/-0 treated as equal
+    diff = (a - b).abs()
+    zero_pair = ((a & 0x7FFF) == 0) & ((b & 0x7FFF) == 0)
+    diff = torch.where(zero_pair, torch.zeros_like(diff), diff)
+    assert int(diff.max()) <= 1, f"{what}: {int((diff > 1).sum())} elements differ by more than one bf16 ulp"
+    return float((diff == 0).float().mean())
+
+
+class Guarded:
+    """A device tensor with poisoned guard regions on both sides, to catch out-of-range writes."""
+
+    GUARD = 64  # elements on each side (keeps 16-byte alignment for 2- and 4-byte types)
+
+    def __init__(self, shape, dtype, fill=None):
+        n = 1
+        for s in shape:
+            n *= s
+        self.n = n
+        self.buf = torch.empty(n + 2 * self.GUARD, dtype=dtype, device=DEV)
+        self.buf.view(torch.uint8).fill_(0x7F)
+        self.t = self.buf[self.GUARD:self.GUARD + n].view(shape)
+        if fill is not None:
+            self.t.copy_(fill)
+        self.pattern = self.buf[:self.GUARD].clone()
+
+    def check(self, what="buffer"):
+        assert torch.equal(self.buf[:self.GUARD].view(torch.uint8), self.pattern.view(torch.uint8)), \
+            f"{what}: write below the buffer"
+        assert torch.equal(self.buf[self.GUARD + self.n:].view(torch.uint8), self.pattern.view(torch.uint8)), \
+            f"{what}: write above the buffer"

@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol, and rejects bad
+arguments on the host before any launch (no compute call is made here)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INCLUDE = os.path.join(ROOT, "include")
+
+from linear_attention_ssm_gb300 import binding  # noqa: E402
+from linear_attention_ssm_gb300.synth import QWEN_GDN, Geometry  # noqa: E402
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(INCLUDE):
+        if fn.endswith(".h"):
+            text = open(os.path.join(INCLUDE, fn)).read()
+            names |= set(re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(binding.LIB_PATH):
+        from linear_attention_ssm_gb300 import build
+        build.build()
+    return binding.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("gdn_conv1d_prefill", "gdn_chunk_prefill", "gdn_gated_rmsnorm", "gdn_decode_step",
+                     "gdn_chunk_prefill_workspace_size", "gdn_check_device_errors", "gdn_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_chunk_size_constant_matches_pages():
+    text = open(os.path.join(INCLUDE, "gdn.h")).read()
+    assert re.search(r"#define\s+GDN_CHUNK_SIZE\s+64\b", text)
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert lib.gdn_status_string(code).decode().startswith("GDN_")
+
+
+FAKE = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced: every call below fails
+ODD = ctypes.c_void_p(0x10002)       # validation before any launch
+
+
+def _geo(**kw):
+    g = dict(num_k_heads=16, num_v_heads=48, head_k_dim=128, head_v_dim=128, conv_width=4)
+    g.update(kw)
+    return ctypes.byref(binding._Geo(g["num_k_heads"], g["num_v_heads"], g["head_k_dim"],
+                                     g["head_v_dim"], g["conv_width"]))
+
+
+def _chunk(lib, geo=None, qkv=FAKE, g=FAKE, beta=FAKE, cu=FAKE, N=1, T=16, state_in=None, state_out=None,
+           z=None, norm_w=None, out=FAKE, l2=1e-6, ws=None, wsb=0):
+    return lib.gdn_chunk_prefill(geo or _geo(), qkv, g, beta, cu, N, T, 0.088, l2, state_in, state_out, z,
+                                 norm_w, 1e-6, out, ws, wsb, None)
+
+
+def test_chunk_prefill_rejects_bad_arguments(lib):
+    E = binding
+    assert _chunk(lib, geo=_geo(head_k_dim=64)) == 2           # unsupported geometry
+    assert _chunk(lib, geo=_geo(num_v_heads=40)) == 2          # Hv not a multiple of Hk
+    assert _chunk(lib, geo=_geo(conv_width=3)) == 2
+    assert _chunk(lib, cu=None) == 1                            # null cu_seqlens
+    assert _chunk(lib, qkv=None) == 1
+    assert _chunk(lib, qkv=ODD) == 3                            # misaligned
+    assert _chunk(lib, out=ODD) == 3
+    assert _chunk(lib, N=-1) == 1
+    assert _chunk(lib, N=0, T=5) == 1                           # tokens without a sequence
+    assert _chunk(lib, z=FAKE, norm_w=None) == 1                # gate without its weight
+    assert _chunk(lib, l2=-1.0) == 1
+    assert "l2" in lib.gdn_last_error_message().decode() or "eps" in lib.gdn_last_error_message().decode()
+    assert lib.gdn_chunk_prefill(None, FAKE, FAKE, FAKE, FAKE, 1, 16, 1.0, 1e-6, None, None, None, None, 1e-6,
+                                 FAKE, None, 0, None) == 1
+    assert E.GDN_OK == 0
+
+
+def test_conv_rejects_bad_arguments(lib):
+    geo = _geo()
+    assert lib.gdn_conv1d_prefill(geo, FAKE, FAKE, None, 1, 8, None, None, FAKE, None) == 1
+    assert lib.gdn_conv1d_prefill(geo, ODD, FAKE, FAKE, 1, 8, None, None, FAKE, None) == 3
+    assert lib.gdn_conv1d_prefill(geo, FAKE, FAKE, FAKE, 1, 8, None, None, FAKE, None) == 1  # y overlaps x
+    assert lib.gdn_conv1d_prefill(_geo(conv_width=2), FAKE, FAKE, FAKE, 1, 8, None, None, FAKE, None) == 2
+    # nothing to do is not an error
+    assert lib.gdn_conv1d_prefill(geo, None, None, None, 0, 0, None, None, None, None) == 0
+
+
+def test_decode_and_norm_reject_bad_arguments(lib):
+    geo = _geo()
+    args = [geo, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.088, 1e-6, 1e-6, FAKE]
+    assert lib.gdn_decode_step(*args, -1, None) == 1
+    assert lib.gdn_decode_step(*args, 70000, None) == 1
+    assert lib.gdn_decode_step(*args, 0, None) == 0
+    bad = list(args)
+    bad[6] = ODD   # state
+    assert lib.gdn_decode_step(*bad, 4, None) == 3
+    assert lib.gdn_decode_step(_geo(num_k_heads=1, num_v_heads=48), *args[1:], 4, None) == 2
+    assert lib.gdn_gated_rmsnorm(geo, FAKE, None, FAKE, 1e-6, FAKE, 4, None) == 1
+    assert lib.gdn_gated_rmsnorm(geo, FAKE, FAKE, FAKE, 1e-6, ODD, 4, None) == 3
+    assert lib.gdn_gated_rmsnorm(geo, None, None, None, 1e-6, None, 0, None) == 0
+
+
+def test_workspace_query_is_callable(lib):
+    assert lib.gdn_chunk_prefill_workspace_size(_geo(), 8, 32735) >= 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(4, QWEN_GDN.conv_dim, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        binding.gdn_conv1d_prefill(x, x, torch.zeros(2, dtype=torch.int32))

@@ -12,19 +12,25 @@
 //   E      = T (diag(beta) V - diag(beta Gamma) K^ S0^T)                       (the WY solve)
 //   O      = q_scale [diag(Gamma) Q^ S0^T + (mask_{j<=t} exp(gamma_t-gamma_j) Q^ K^^T) E]
 //   S_L    = Gamma_L S0 + E^T diag(exp(gamma_L - gamma)) K^
-// This file evaluates it "value-major", i.e. every product is written with the value index of
-// the state as the 128-row M dimension of a tcgen05 MMA (M = 128, N in {64, 128}, K = 16 per
-// instruction, bf16 operands in 128-byte-swizzled shared memory, fp32 accumulators in tensor
-// memory).  The fp32 state itself lives in tensor memory for the whole sequence.
+// Every product is written "value-major": the value index of the state is the 128-row M
+// dimension of a tcgen05 MMA (M = 128, N in {64, 128}, K = 16 per instruction, bf16 operands in
+// 128-byte-swizzled K-major shared memory, fp32 accumulators in tensor memory).  The fp32 state
+// lives in tensor memory for a whole sequence.
 //
 // Precision: operands that are exact in bf16 (the raw conv outputs q, k, v) are fed as they are;
-// the L2-norm factors, beta and the decay exponentials are applied in fp32 as diagonal scalings
-// in the epilogues.  fp32 operands on the state path (S0, the right-hand side R, the solve T,
-// the scaled E) are split into bf16 hi + lo pairs, giving ~16-bit operands; products that only
-// feed the output (S0 q, E P^T) use the hi part alone.
+// the L2-norm factors, beta and the decay exponentials are fp32 diagonal scalings applied in the
+// epilogues.  fp32 operands on the state path (S0, the right-hand side R, the solve T, the scaled
+// E) are split into bf16 hi + lo pairs (~16-bit operands); products that only feed the output
+// (S0 q, E P^T) use the hi part alone.
 //
-// One CTA of 128 threads per (sequence, V head); thread r owns row r of every accumulator (TMEM
-// lane r).  The phases of a chunk run back to back, separated by mbarrier waits on the MMAs.
+// Launch: a persistent grid (one CTA of 256 threads per SM) pulls (sequence, V head) work items
+// from a counter in longest-sequence-first order (the order and the counter live in the caller's
+// workspace and are written by a one-CTA schedule kernel launched first).  Within an item the
+// chunks run in order; q/k and v tiles of the next chunk are fetched by TMA as soon as their
+// buffers are free, so HBM latency hides behind the current chunk.  Thread (row, half) owns
+// tensor-memory lane `row` and half of the accumulator columns in every epilogue.
+#include <cuda.h>
+
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 
@@ -32,27 +38,25 @@ namespace gdn {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 
 // ---- shared memory map (byte offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_QK = 0;         // 32 KB: 2 K-blocks x 128 rows (k tokens 0..63, q tokens 64..127)
 constexpr uint32_t OFF_KT = 32768;     // 16 KB: K^T, 128 key rows x 64 tokens
-constexpr uint32_t OFF_SHI = 49152;    // 32 KB: S0 hi, 2 K-blocks x 128 value rows
-constexpr uint32_t OFF_SLO = 81920;    // 32 KB: S0 lo
-constexpr uint32_t OFF_RHI = 114688;   // 16 KB: R hi, then E~ hi (128 value rows x 64 tokens)
-constexpr uint32_t OFF_RLO = 131072;   // 16 KB: R lo, then E~ lo
+constexpr uint32_t OFF_S = 49152;      // 64 KB: S0 hi (32 KB) + lo (32 KB); also the solve work area
+                                       //        and the output staging (both dead while S0 is live)
+constexpr uint32_t OFF_R = 114688;     // 32 KB: R hi/lo (16 KB each), then E~ hi/lo
 constexpr uint32_t OFF_T = 147456;     // 16 KB: T hi (8 KB) + T lo (8 KB); then E bf16 (16 KB)
 constexpr uint32_t OFF_P = 163840;     //  8 KB: P, 64 token rows x 64
-constexpr uint32_t OFF_V = 172032;     // 16 KB: V, [64 tokens][128] bf16, plain row-major
-constexpr uint32_t OFF_WORK = 188416;  // fp32 work: solve (A, T, block temp) or output staging
-constexpr uint32_t LDA = 65;           // row stride (floats) of the solve matrices
-constexpr uint32_t LDO = 132;          // row stride (floats) of the output staging
-constexpr uint32_t WORK_BYTES = (2 * 64 * LDA + 3 * 256) * 4;  // 36352 >= 64 * LDO * 4
-constexpr uint32_t OFF_VEC = OFF_WORK + WORK_BYTES;            // per-token vectors, 8 x 64 floats
-constexpr uint32_t OFF_BAR = OFF_VEC + 8 * 64 * 4;             // 4 mbarriers + TMEM address
-constexpr uint32_t SMEM_USED = OFF_BAR + 64;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;               // + alignment slack
-static_assert(64 * LDO * 4 <= WORK_BYTES, "output staging must fit the work area");
+constexpr uint32_t OFF_V = 172032;     // 16 KB: V, 2 K-blocks of 64 value columns x 64 token rows
+constexpr uint32_t OFF_VEC = 188416;   // per-token vectors (8 x 64 floats) + norm partials (256)
+constexpr uint32_t OFF_BAR = OFF_VEC + (8 * 64 + 256) * 4;  // mbarriers, TMEM address, item slot
+constexpr uint32_t SMEM_USED = OFF_BAR + 128;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;            // + alignment slack
+constexpr uint32_t LDA = 65;   // row stride (floats) of the solve matrices
+constexpr uint32_t LDO = 132;  // row stride (floats) of the output staging
+static_assert((2 * 64 * LDA + 3 * 256) * 4 <= 65536, "solve work must fit the S0 area");
+static_assert(64 * LDO * 4 <= 65536, "output staging must fit the S0 area");
 static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
 // ---- tensor memory columns (fp32, lane = value row)
@@ -61,16 +65,21 @@ constexpr uint32_t COL_X = 128;   //  64: S0 K^T
 constexpr uint32_t COL_E = 192;   //  64: E^T
 constexpr uint32_t COL_O1 = 256;  //  64: S0 Q^T
 constexpr uint32_t COL_O2 = 320;  //  64: E^T P^T
-constexpr uint32_t COL_G = 384;   //  64: [K; Q] K^T (Gram, rows 0..63, and Q K^T, rows 64..127)
+constexpr uint32_t COL_G = 384;   //  64: [K; Q] K^T (Gram rows 0..63, Q K^T rows 64..127)
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint32_t kWaitLimit = 1u << 20;  // polls of one mbarrier before giving up
+constexpr int kScheduleSortMax = 4096;     // longest-first ordering up to this many sequences
+constexpr uint32_t kBytesQK = 4 * 64 * 128;  // four 64 x 64 bf16 boxes
+constexpr uint32_t kBytesV = 2 * 64 * 128;
 
 struct ChunkParams {
-  const uint16_t* qkv;
+  CUtensorMap tmap;  // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle
   const float* g;
   const float* beta;
   const int32_t* cu;
+  const int32_t* order;     // longest-first sequence order (workspace)
+  unsigned* counter;        // work-item counter (workspace, zeroed by the schedule kernel)
   const float* state_in;
   float* state_out;
   const uint16_t* z;
@@ -81,23 +90,9 @@ struct ChunkParams {
   float q_scale, l2_eps, rms_eps;
 };
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
-
-// Writes 8 consecutive fp32 values (columns k0..k0+7 of `row`, k0 % 8 == 0) of an fp32 matrix
-// as a bf16 hi/lo pair into two K-major swizzled tiles.
-__device__ __forceinline__ void store8_split(uint32_t hi_tile, uint32_t lo_tile, uint32_t kb_stride, int row, int k0,
+// Writes 8 consecutive fp32 values (columns k0..k0+7 of `row`, k0 % 8 == 0) as a bf16 hi (and
+// optionally lo) pair into K-major 128-byte-swizzled tiles.
+__device__ __forceinline__ void store8_split(uint8_t* hi_tile, uint8_t* lo_tile, uint32_t kb_stride, int row, int k0,
                                              const float* v) {
   uint32_t h[4], l[4];
 #pragma unroll
@@ -108,21 +103,25 @@ __device__ __forceinline__ void store8_split(uint32_t hi_tile, uint32_t lo_tile,
     l[i] = pack_bf2(a - bf2f(ah), b - bf2f(bh));
   }
   const uint32_t off = sw128_offset(row, k0, kb_stride);
-  st_shared_v4(hi_tile + off, h[0], h[1], h[2], h[3]);
-  if (lo_tile) st_shared_v4(lo_tile + off, l[0], l[1], l[2], l[3]);
+  *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  if (lo_tile) *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// CUDA-core stand-in of one M=128 MMA group for verification: thread r computes row r of
-// D (+)= A * B^T from the same swizzled operand tiles and writes it to tensor memory.
+__device__ __forceinline__ float ld_bf(const uint8_t* base, uint32_t off) {
+  return bf2f(*reinterpret_cast<const uint16_t*>(base + off));
+}
+
+// CUDA-core stand-in of one M=128 MMA group for verification: thread (row, half) computes
+// columns [half*N/2, (half+1)*N/2) of row `row` of D (+)= A * B^T from the same swizzled tiles.
 template <int N, int K>
-__device__ void emu_mma(uint32_t t_lane_col, uint32_t a_tile, uint32_t a_kbs, uint32_t b_tile, uint32_t b_kbs,
-                        bool accumulate, int r) {
+__device__ void emu_mma(uint32_t t_lane, uint32_t col, const uint8_t* a_tile, uint32_t a_kbs, const uint8_t* b_tile,
+                        uint32_t b_kbs, bool accumulate, int row, int half) {
   float arow[K];
 #pragma unroll 8
-  for (int k = 0; k < K; ++k) arow[k] = bf2f(ld_shared_u16(a_tile + sw128_offset(r, k, a_kbs)));
-  for (int n0 = 0; n0 < N; n0 += 32) {
+  for (int k = 0; k < K; ++k) arow[k] = ld_bf(a_tile, sw128_offset(row, k, a_kbs));
+  for (int n0 = half * (N / 2); n0 < (half + 1) * (N / 2); n0 += 32) {
     float d[32];
-    if (accumulate) tmem_ld32(t_lane_col + n0, d);
+    if (accumulate) tmem_ld32(t_lane + col + n0, d);
     else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) d[i] = 0.f;
@@ -130,26 +129,28 @@ __device__ void emu_mma(uint32_t t_lane_col, uint32_t a_tile, uint32_t a_kbs, ui
     for (int n = 0; n < 32; ++n) {
       float s = 0.f;
 #pragma unroll 8
-      for (int k = 0; k < K; ++k) s = fmaf(arow[k], bf2f(ld_shared_u16(b_tile + sw128_offset(n0 + n, k, b_kbs))), s);
+      for (int k = 0; k < K; ++k) s = fmaf(arow[k], ld_bf(b_tile, sw128_offset(n0 + n, k, b_kbs)), s);
       d[n] += s;
     }
-    tmem_st32(t_lane_col + n0, d);
+    tmem_st32(t_lane + col + n0, d);
   }
 }
 
 // T = (I + A)^-1 for a strictly lower triangular 64 x 64 A (row stride LDA), by 16 x 16 blocks:
-// the four diagonal blocks by forward substitution (one thread per column), then the
-// off-diagonal blocks by block distance d: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
+// the four diagonal blocks by right-looking forward substitution with the column in registers
+// (one thread per column), then the off-diagonal blocks by block distance d:
+// T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
 __device__ void solve_unit_lower(const float* sA, float* sT, float* sM, int tid) {
   if (tid < 64) {
     const int b = tid >> 4, c = tid & 15, o = b * 16;
     float x[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float v = (i == c) ? 1.f : 0.f;
+    for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
 #pragma unroll
-      for (int k = 0; k < i; ++k) v -= sA[(o + i) * LDA + o + k] * x[k];
-      x[i] = (i < c) ? 0.f : v;
+    for (int k = 0; k < 15; ++k) {
+      const float xk = x[k];
+#pragma unroll
+      for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-sA[(o + i) * LDA + o + k], xk, x[i]);
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) sT[(o + i) * LDA + o + c] = x[i];
@@ -167,7 +168,8 @@ __device__ void solve_unit_lower(const float* sA, float* sT, float* sM, int tid)
       float acc = 0.f;
       for (int kb = jb; kb < i; ++kb)
 #pragma unroll
-        for (int u = 0; u < 16; ++u) acc = fmaf(sA[(i * 16 + r) * LDA + kb * 16 + u], sT[(kb * 16 + u) * LDA + jb * 16 + cc], acc);
+        for (int u = 0; u < 16; ++u)
+          acc = fmaf(sA[(i * 16 + r) * LDA + kb * 16 + u], sT[(kb * 16 + u) * LDA + jb * 16 + cc], acc);
       sM[bi * 256 + e] = acc;
     }
     __syncthreads();
@@ -175,7 +177,9 @@ __device__ void solve_unit_lower(const float* sA, float* sT, float* sM, int tid)
       const int bi = idx >> 8, e = idx & 255, r = e >> 4, cc = e & 15;
       const int i = d + bi, jb = i - d;
       float acc = 0.f;
-      for (int u = 0; u <= r; ++u) acc = fmaf(sT[(i * 16 + r) * LDA + i * 16 + u], sM[bi * 256 + u * 16 + cc], acc);
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (u <= r) acc = fmaf(sT[(i * 16 + r) * LDA + i * 16 + u], sM[bi * 256 + u * 16 + cc], acc);
       sT[(i * 16 + r) * LDA + jb * 16 + cc] = -acc;
     }
     __syncthreads();
@@ -183,42 +187,35 @@ __device__ void solve_unit_lower(const float* sA, float* sT, float* sM, int tid)
 }
 
 template <bool kEmulate>
-__global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const ChunkParams p) {
+__global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid_constant__ ChunkParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, half = warp >> 2;
+  const int row = q4 * 32 + lane;  // tensor-memory lane = accumulator row owned by this thread
 
-  const int h = blockIdx.x % p.Hv;
-  const int n = blockIdx.x / p.Hv;
   const int ratio = p.Hv / p.Hk;
-  const int kh = h / ratio;
-  const int C = 2 * p.Hk * kHeadDim + p.Hv * kHeadDim;
-  const int seq_s = __ldg(p.cu + n), seq_e = __ldg(p.cu + n + 1);
-  if (seq_s < 0 || seq_e < seq_s || seq_e > p.T) {
-    if (tid == 0) raise_error(p.err, kErrDeviceArgument);
-    return;
-  }
+  const long total_items = (long)p.N * p.Hv;
 
   float* s_gam = reinterpret_cast<float*>(sm + OFF_VEC);
   float* s_beta = s_gam + 64;
   float* s_ik = s_gam + 128;
   float* s_iq = s_gam + 192;
-  float* s_cx = s_gam + 256;   // beta_t Gamma_t ik_t
-  float* s_co = s_gam + 320;   // Gamma_t iq_t q_scale
-  float* s_cs = s_gam + 384;   // exp(gamma_L - gamma_t) ik_t
+  float* s_cx = s_gam + 256;  // beta_t Gamma_t ik_t
+  float* s_co = s_gam + 320;  // Gamma_t iq_t q_scale
+  float* s_cs = s_gam + 384;  // exp(gamma_L - gamma_t) ik_t
   float* s_g = s_gam + 448;
-  float* s_work = reinterpret_cast<float*>(sm + OFF_WORK);
+  float* s_part = s_gam + 512;  // 2 x 128 partial sums of squares
+  float* s_work = reinterpret_cast<float*>(sm + OFF_S);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 32);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 64);
+  int* item_slot = reinterpret_cast<int*>(sm + OFF_BAR + 72);
   const uint32_t bar_g = smem_u32(&bars[0]), bar_x = smem_u32(&bars[1]), bar_e = smem_u32(&bars[2]),
-                 bar_s = smem_u32(&bars[3]);
+                 bar_s = smem_u32(&bars[3]), bar_qk = smem_u32(&bars[4]), bar_v = smem_u32(&bars[5]);
 
   if (tid == 0) {
-    mbar_init(bar_g, 1);
-    mbar_init(bar_x, 1);
-    mbar_init(bar_e, 1);
-    mbar_init(bar_s, 1);
+    for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[i]), 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -226,345 +223,455 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const ChunkP
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lane quarter, column 0
-
-  // ---- initial state -> tensor memory (thread r: value row r)
-  {
-    const size_t row_off = (((size_t)n * p.Hv + h) * kHeadDim + tid) * kHeadDim;
-    for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
-      float v[32];
-      if (p.state_in) {
-        const float4* src = reinterpret_cast<const float4*>(p.state_in + row_off + c0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 f = __ldg(src + i);
-          v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.f;
-      }
-      tmem_st32(tl + COL_S + c0, v);
-    }
-  }
+  const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);  // this warp's lane quarter, column 0
 
   constexpr uint32_t ID64 = idesc_bf16_f32(128, 64);
   constexpr uint32_t ID128 = idesc_bf16_f32(128, 128);
   bool ok = true;
-  uint32_t phase = 0;
+  uint32_t ph_mma = 0, ph_qk = 0, ph_v = 0;  // phase parities
+  bool pend_qk = false, pend_v = false;      // TMA loads issued and not yet awaited (uniform)
 
-  // one MMA group: either issued on the tensor cores by thread 0 and awaited on `bar`, or emulated
-  auto finish_group = [&](uint32_t bar) {
+  auto wait_bar = [&](uint32_t bar, uint32_t& ph) {
+    const bool got = mbar_wait(bar, ph, kWaitLimit);
+    ph ^= 1u;
+    if (!got) raise_error(p.err, kErrTimeout);
+    ok = __syncthreads_and(got ? 1 : 0) != 0 && ok;
+  };
+  auto finish_group = [&](uint32_t bar) {  // MMAs of a group issued (or emulated): wait for them
     if constexpr (!kEmulate) {
       if (tid == 0) mma_commit(bar);
-      const bool got = mbar_wait(bar, phase, kWaitLimit);
-      if (!got) raise_error(p.err, kErrTimeout);
-      ok = __syncthreads_and(got ? 1 : 0) != 0;
+      uint32_t ph = ph_mma;
+      wait_bar(bar, ph);
       tc_fence_after();
     } else {
+      fence_proxy_async_smem();  // the emulated operand reads precede later TMA writes
       tc_fence_before();
       __syncthreads();
       tc_fence_after();
     }
   };
-  auto operands_ready = [&]() {  // smem operand writes by all threads -> visible to the MMA
+  auto operands_ready = [&]() {  // generic-proxy smem writes by all threads -> visible to MMA / TMA
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
   };
-
-  for (int c0 = seq_s; c0 < seq_e && ok; c0 += kChunk, phase ^= 1u) {
-    const int L = min(kChunk, seq_e - c0);
-
-    // ================= prepare: loads, norms, K^T, cumsum
-    if (tid < 64) {
-      float gv = 0.f, bv = 0.f;
-      if (tid < L) {
-        gv = __ldg(p.g + (size_t)(c0 + tid) * p.Hv + h);
-        bv = __ldg(p.beta + (size_t)(c0 + tid) * p.Hv + h);
-      }
-      s_g[tid] = gv;
-      s_beta[tid] = bv;
+  auto issue_qk = [&](int c0, int kh) {  // q and k tiles of the chunk starting at token c0
+    mbar_arrive_expect_tx(bar_qk, kBytesQK);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+      tma_load_2d(sb + OFF_QK + kb * 16384, &p.tmap, p.Hk * kHeadDim + kh * kHeadDim + kb * 64, c0, bar_qk);
+      tma_load_2d(sb + OFF_QK + kb * 16384 + 8192, &p.tmap, kh * kHeadDim + kb * 64, c0, bar_qk);
     }
-    for (int i = tid; i < 64 * 16; i += kThreads) {
-      const int t = i >> 4, kc = i & 15;
-      uint4 kq = make_uint4(0, 0, 0, 0), qq = kq, vv = kq;
-      if (t < L) {
-        const uint16_t* row = p.qkv + (size_t)(c0 + t) * C;
-        qq = __ldg(reinterpret_cast<const uint4*>(row + kh * kHeadDim + kc * 8));
-        kq = __ldg(reinterpret_cast<const uint4*>(row + p.Hk * kHeadDim + kh * kHeadDim + kc * 8));
-        vv = __ldg(reinterpret_cast<const uint4*>(row + 2 * p.Hk * kHeadDim + h * kHeadDim + kc * 8));
-      }
-      const uint32_t swz = (uint32_t)(((kc & 7) ^ (t & 7)) << 4);
-      const uint32_t kb = (uint32_t)(kc >> 3) * 16384u;
-      st_shared_v4(sb + OFF_QK + kb + t * 128 + swz, kq.x, kq.y, kq.z, kq.w);
-      st_shared_v4(sb + OFF_QK + kb + (64 + t) * 128 + swz, qq.x, qq.y, qq.z, qq.w);
-      st_shared_v4(sb + OFF_V + t * 256 + kc * 16, vv.x, vv.y, vv.z, vv.w);
-    }
+  };
+  auto issue_v = [&](int c0, int h) {
+    mbar_arrive_expect_tx(bar_v, kBytesV);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+      tma_load_2d(sb + OFF_V + kb * 8192, &p.tmap, 2 * p.Hk * kHeadDim + h * kHeadDim + kb * 64, c0, bar_v);
+  };
+
+  for (;;) {
+    if (tid == 0) *item_slot = (int)atomicAdd(p.counter, 1u);
     __syncthreads();
-    {
-      // L2 norms: thread t < 64 -> key row t, thread 64 + t -> query row t
-      const int row = tid;
-      float ss = 0.f;
-#pragma unroll
-      for (int kc = 0; kc < 16; ++kc) {
-        const uint4 u = ld_shared_v4(sb + OFF_QK + (kc >> 3) * 16384 + row * 128 + (((kc & 7) ^ (row & 7)) << 4));
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = __uint_as_float(w4[e] << 16), b = __uint_as_float(w4[e] & 0xFFFF0000u);
-          ss = fmaf(a, a, ss);
-          ss = fmaf(b, b, ss);
-        }
-      }
-      const float inv = 1.0f / sqrtf(ss + p.l2_eps);
-      if (tid < 64) s_ik[tid] = inv; else s_iq[tid - 64] = inv;
-      // K^T: thread = key index, 8 chunks of 8 tokens
-      const int nk = tid;
-#pragma unroll
-      for (int tc = 0; tc < 8; ++tc) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int t0 = tc * 8 + 2 * u;
-          const uint32_t a = ld_shared_u16(sb + OFF_QK + sw128_offset(t0, nk, 16384));
-          const uint32_t b = ld_shared_u16(sb + OFF_QK + sw128_offset(t0 + 1, nk, 16384));
-          w4[u] = a | (b << 16);
-        }
-        st_shared_v4(sb + OFF_KT + nk * 128 + (((tc ^ (nk & 7)) & 7) << 4), w4[0], w4[1], w4[2], w4[3]);
-      }
-    }
-    if (tid == 0) {
-      float acc = 0.f;
-      for (int t = 0; t < 64; ++t) { acc += s_g[t]; s_gam[t] = acc; }
-    }
+    const long w = *item_slot;
     __syncthreads();
-    if (tid < 64) {
-      const int t = tid;
-      const float gam = s_gam[t], gamL = s_gam[L - 1];
-      const float Gam = expf(gam);
-      s_cx[t] = s_beta[t] * Gam * s_ik[t];
-      s_co[t] = Gam * s_iq[t] * p.q_scale;
-      s_cs[t] = (t < L) ? expf(gamL - gam) * s_ik[t] : 0.f;
+    if (w >= total_items || !ok) break;
+    const int h = (int)(w % p.Hv);
+    const int ni = (int)(w / p.Hv);
+    const int n = p.order ? __ldg(p.order + ni) : ni;
+    const int kh = h / ratio;
+    const int seq_s = __ldg(p.cu + n), seq_e = __ldg(p.cu + n + 1);
+    if (n < 0 || n >= p.N || seq_s < 0 || seq_e < seq_s || seq_e > p.T) {
+      if (tid == 0) raise_error(p.err, kErrDeviceArgument);
+      continue;
     }
-    operands_ready();
+    if (tid == 0 && seq_e > seq_s) {
+      issue_qk(seq_s, kh);
+      issue_v(seq_s, h);
+    }
+    pend_qk = pend_v = seq_e > seq_s;
 
-    // ================= Gram: G = [K; Q] K^T  (M = 128, N = 64, K = 128)
-    if constexpr (!kEmulate) {
-      if (tid == 0) {
+    // ---- initial state -> tensor memory (thread (row, half): 64 columns of row `row`)
+    {
+      const size_t row_off = (((size_t)n * p.Hv + h) * kHeadDim + row) * kHeadDim;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_bf16(tmem + COL_G, sw128_desc(sb + OFF_QK + off), sw128_desc(sb + OFF_QK + off), ID64, ks > 0);
+      for (int c = 0; c < 2; ++c) {
+        const int c0 = half * 64 + c * 32;
+        float v[32];
+        if (p.state_in) {
+          const float4* src = reinterpret_cast<const float4*>(p.state_in + row_off + c0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 f = __ldg(src + i);
+            v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        tmem_st32(tl + COL_S + c0, v);
+      }
+    }
+
+    for (int c0 = seq_s; c0 < seq_e && ok; c0 += kChunk, ph_mma ^= 1u) {
+      const int L = min(kChunk, seq_e - c0);
+      const bool has_next = c0 + kChunk < seq_e;
+
+      // ================= prepare: g, beta, norms, K^T, cumsum, per-token factors
+      if (tid < 64) {
+        float gv = 0.f, bv = 0.f;
+        if (tid < L) {
+          gv = __ldg(p.g + (size_t)(c0 + tid) * p.Hv + h);
+          bv = __ldg(p.beta + (size_t)(c0 + tid) * p.Hv + h);
+        }
+        s_g[tid] = gv;
+        s_beta[tid] = bv;
+      }
+      wait_bar(bar_qk, ph_qk);
+      pend_qk = false;
+      if (!ok) break;
+      {
+        // partial sums of squares: rows 0..63 keys, 64..127 queries; half = K-block
+        const int r = tid & 127, kb = tid >> 7;
+        float ss = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 u = *reinterpret_cast<const uint4*>(sm + OFF_QK + kb * 16384 + r * 128 + (((c ^ (r & 7)) & 7) << 4));
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = __uint_as_float(w4[e] << 16), b = __uint_as_float(w4[e] & 0xFFFF0000u);
+            ss = fmaf(a, a, ss);
+            ss = fmaf(b, b, ss);
+          }
+        }
+        s_part[kb * 128 + r] = ss;
+        // K^T: thread (key n, token half) gathers 32 tokens into 4 swizzled 16-byte chunks
+        const int nk = tid & 127, th = tid >> 7;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int tc = th * 4 + q;
+          uint32_t w4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int t0 = tc * 8 + 2 * u;
+            const uint32_t a = *reinterpret_cast<const uint16_t*>(sm + OFF_QK + sw128_offset(t0, nk, 16384));
+            const uint32_t b = *reinterpret_cast<const uint16_t*>(sm + OFF_QK + sw128_offset(t0 + 1, nk, 16384));
+            w4[u] = a | (b << 16);
+          }
+          *reinterpret_cast<uint4*>(sm + OFF_KT + nk * 128 + (((tc ^ (nk & 7)) & 7) << 4)) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
-    } else {
-      emu_mma<64, 128>(tl + COL_G, sb + OFF_QK, 16384, sb + OFF_QK, 16384, false, tid);
-    }
-    finish_group(bar_g);
-    if (!ok) break;
-
-    // ================= A (rows 0..63) and P (rows 64..127) from the Gram tile
-    {
-      float gr[64];
-      tmem_ld32(tl + COL_G, *reinterpret_cast<float(*)[32]>(gr));
-      tmem_ld32(tl + COL_G + 32, *reinterpret_cast<float(*)[32]>(gr + 32));
-      float* sA = s_work;
+      if (warp == 0) {
+        // inclusive scan of g over the chunk (lane l holds tokens 2l and 2l+1)
+        const float g0 = s_g[2 * lane], g1 = s_g[2 * lane + 1];
+        float s = g0 + g1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float v = __shfl_up_sync(0xffffffffu, s, o);
+          if (lane >= o) s += v;
+        }
+        s_gam[2 * lane + 1] = s;
+        s_gam[2 * lane] = s - g1;
+      }
+      __syncthreads();
+      if (tid < 128) {
+        const float inv = 1.0f / sqrtf(s_part[tid] + s_part[128 + tid] + p.l2_eps);
+        if (tid < 64) s_ik[tid] = inv; else s_iq[tid - 64] = inv;
+      }
+      __syncthreads();
       if (tid < 64) {
         const int t = tid;
-        const float bt = s_beta[t] * s_ik[t], gt = s_gam[t];
-#pragma unroll 8
-        for (int j = 0; j < 64; ++j) sA[t * LDA + j] = (j < t) ? bt * expf(gt - s_gam[j]) * gr[j] * s_ik[j] : 0.f;
-      } else {
-        const int t = tid - 64;
-        const float qt = s_iq[t] * p.q_scale, gt = s_gam[t];
+        const float gam = s_gam[t], gamL = s_gam[L - 1];
+        const float Gam = expf(gam);
+        s_cx[t] = s_beta[t] * Gam * s_ik[t];
+        s_co[t] = Gam * s_iq[t] * p.q_scale;
+        s_cs[t] = (t < L) ? expf(gamL - gam) * s_ik[t] : 0.f;
+      }
+      operands_ready();
+
+      // ================= Gram: G = [K; Q] K^T  (M = 128, N = 64, K = 128)
+      if constexpr (!kEmulate) {
+        if (tid == 0) {
 #pragma unroll
-        for (int j0 = 0; j0 < 64; j0 += 8) {
-          float v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int j = j0 + u;
-            v[u] = (j <= t) ? qt * expf(gt - s_gam[j]) * gr[j] * s_ik[j] : 0.f;
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_bf16(tmem + COL_G, sw128_desc(sb + OFF_QK + off), sw128_desc(sb + OFF_QK + off), ID64, ks > 0);
           }
-          store8_split(sb + OFF_P, 0, 0, t, j0, v);
+        }
+      } else {
+        emu_mma<64, 128>(tl, COL_G, sm + OFF_QK, 16384, sm + OFF_QK, 16384, false, row, half);
+      }
+      finish_group(bar_g);
+      if (!ok) break;
+
+      // ================= A (rows 0..63) and P (rows 64..127) from the Gram tile
+      {
+        float gr[32];
+        tmem_ld32(tl + COL_G + half * 32, gr);
+        float* sA = s_work;
+        if (row < 64) {
+          const int t = row;
+          const float bt = s_beta[t] * s_ik[t], gt = s_gam[t];
+#pragma unroll 8
+          for (int i = 0; i < 32; ++i) {
+            const int j = half * 32 + i;
+            sA[t * LDA + j] = (j < t) ? bt * expf(gt - s_gam[j]) * gr[i] * s_ik[j] : 0.f;
+          }
+        } else {
+          const int t = row - 64;
+          const float qt = s_iq[t] * p.q_scale, gt = s_gam[t];
+#pragma unroll
+          for (int i0 = 0; i0 < 32; i0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int j = half * 32 + i0 + u;
+              v[u] = (j <= t) ? qt * expf(gt - s_gam[j]) * gr[i0 + u] * s_ik[j] : 0.f;
+            }
+            store8_split(sm + OFF_P, nullptr, 0, t, half * 32 + i0, v);
+          }
         }
       }
-    }
-    __syncthreads();
+      __syncthreads();
 
-    // ================= solve: T = (I + A)^-1, then T hi/lo -> operand tiles
-    {
-      float* sA = s_work;
-      float* sTf = s_work + 64 * LDA;
-      float* sM = s_work + 2 * 64 * LDA;
-      solve_unit_lower(sA, sTf, sM, tid);
-      for (int i = tid; i < 64 * 8; i += kThreads) {
-        const int t = i >> 3, k0 = (i & 7) * 8;
-        store8_split(sb + OFF_T, sb + OFF_T + 8192, 0, t, k0, sTf + t * LDA + k0);
-      }
-    }
-    // ================= S0 -> hi/lo operand tiles; tensor memory state <- Gamma_L S0
-    {
-      const float gL = expf(s_gam[L - 1]);
-      for (int k0 = 0; k0 < kHeadDim; k0 += 32) {
-        float v[32];
-        tmem_ld32(tl + COL_S + k0, v);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) store8_split(sb + OFF_SHI, sb + OFF_SLO, 16384, tid, k0 + 8 * q, v + 8 * q);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= gL;
-        tmem_st32(tl + COL_S + k0, v);
-      }
-    }
-    operands_ready();
-
-    // ================= X = S0 K^T (hi + lo), O1 = S0_hi Q^T
-    if constexpr (!kEmulate) {
-      if (tid == 0) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          const uint64_t bk = sw128_desc(sb + OFF_QK + off), bq = sw128_desc(sb + OFF_QK + 8192 + off);
-          mma_bf16(tmem + COL_X, sw128_desc(sb + OFF_SHI + off), bk, ID64, ks > 0);
-          mma_bf16(tmem + COL_X, sw128_desc(sb + OFF_SLO + off), bk, ID64, 1);
-          mma_bf16(tmem + COL_O1, sw128_desc(sb + OFF_SHI + off), bq, ID64, ks > 0);
+      // ================= solve: T = (I + A)^-1, then T hi/lo -> operand tiles
+      {
+        float* sA = s_work;
+        float* sTf = s_work + 64 * LDA;
+        float* sM = s_work + 2 * 64 * LDA;
+        solve_unit_lower(sA, sTf, sM, tid);
+        for (int i = tid; i < 64 * 8; i += kThreads) {
+          const int t = i >> 3, k0 = (i & 7) * 8;
+          store8_split(sm + OFF_T, sm + OFF_T + 8192, 0, t, k0, sTf + t * LDA + k0);
         }
       }
-    } else {
-      emu_mma<64, 128>(tl + COL_X, sb + OFF_SHI, 16384, sb + OFF_QK, 16384, false, tid);
-      emu_mma<64, 128>(tl + COL_X, sb + OFF_SLO, 16384, sb + OFF_QK, 16384, true, tid);
-      emu_mma<64, 128>(tl + COL_O1, sb + OFF_SHI, 16384, sb + OFF_QK + 8192, 16384, false, tid);
-    }
-    finish_group(bar_x);
-    if (!ok) break;
+      __syncthreads();  // the solve work area is about to be overwritten by S0 hi/lo
 
-    // ================= R = diag(beta) V - diag(beta Gamma ik) (S0 K^T)^T  -> hi/lo (value-major)
-    {
-      const uint16_t* sV = reinterpret_cast<const uint16_t*>(sm + OFF_V);
-      for (int t0 = 0; t0 < 64; t0 += 32) {
+      // ================= S0 -> hi/lo operand tiles; tensor memory state <- Gamma_L S0
+      {
+        const float gL = expf(s_gam[L - 1]);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int k0 = half * 64 + c * 32;
+          float v[32];
+          tmem_ld32(tl + COL_S + k0, v);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) store8_split(sm + OFF_S, sm + OFF_S + 32768, 16384, row, k0 + 8 * q, v + 8 * q);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= gL;
+          tmem_st32(tl + COL_S + k0, v);
+        }
+      }
+      operands_ready();
+
+      // ================= X = S0 K^T (hi + lo), O1 = S0_hi Q^T
+      if constexpr (!kEmulate) {
+        if (tid == 0) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            const uint64_t bk = sw128_desc(sb + OFF_QK + off), bq = sw128_desc(sb + OFF_QK + 8192 + off);
+            mma_bf16(tmem + COL_X, sw128_desc(sb + OFF_S + off), bk, ID64, ks > 0);
+            mma_bf16(tmem + COL_X, sw128_desc(sb + OFF_S + 32768 + off), bk, ID64, 1);
+            mma_bf16(tmem + COL_O1, sw128_desc(sb + OFF_S + off), bq, ID64, ks > 0);
+          }
+        }
+      } else {
+        emu_mma<64, 128>(tl, COL_X, sm + OFF_S, 16384, sm + OFF_QK, 16384, false, row, half);
+        emu_mma<64, 128>(tl, COL_X, sm + OFF_S + 32768, 16384, sm + OFF_QK, 16384, true, row, half);
+        emu_mma<64, 128>(tl, COL_O1, sm + OFF_S, 16384, sm + OFF_QK + 8192, 16384, false, row, half);
+      }
+      finish_group(bar_x);
+      if (!ok) break;
+      // the q/k tile is free: fetch the next chunk's
+      if (tid == 0 && has_next) issue_qk(c0 + kChunk, kh);
+      pend_qk = has_next;
+
+      // ================= R = diag(beta) V - diag(beta Gamma ik) (S0 K^T)^T  -> hi/lo (value-major)
+      wait_bar(bar_v, ph_v);
+      pend_v = false;
+      if (!ok) break;
+      {
         float x[32];
-        tmem_ld32(tl + COL_X + t0, x);
+        tmem_ld32(tl + COL_X + half * 32, x);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int t = t0 + i;
-          x[i] = s_beta[t] * bf2f(sV[t * kHeadDim + tid]) - s_cx[t] * x[i];
+          const int t = half * 32 + i;
+          x[i] = s_beta[t] * ld_bf(sm + OFF_V, sw128_offset(t, row, 8192)) - s_cx[t] * x[i];
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) store8_split(sb + OFF_RHI, sb + OFF_RLO, 0, tid, t0 + 8 * q, x + 8 * q);
+        for (int q = 0; q < 4; ++q) store8_split(sm + OFF_R, sm + OFF_R + 16384, 0, row, half * 32 + 8 * q, x + 8 * q);
       }
-    }
-    operands_ready();
+      operands_ready();
+      if (tid == 0 && has_next) issue_v(c0 + kChunk, h);
+      pend_v = has_next;
 
-    // ================= E^T = R T^T  (hi*hi + hi*lo + lo*hi)
-    if constexpr (!kEmulate) {
-      if (tid == 0) {
+      // ================= E^T = R T^T  (hi*hi + hi*lo + lo*hi)
+      if constexpr (!kEmulate) {
+        if (tid == 0) {
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t off = ks * 32;
-          const uint64_t rh = sw128_desc(sb + OFF_RHI + off), rl = sw128_desc(sb + OFF_RLO + off);
-          mma_bf16(tmem + COL_E, rh, sw128_desc(sb + OFF_T + off), ID64, ks > 0);
-          mma_bf16(tmem + COL_E, rh, sw128_desc(sb + OFF_T + 8192 + off), ID64, 1);
-          mma_bf16(tmem + COL_E, rl, sw128_desc(sb + OFF_T + off), ID64, 1);
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t off = ks * 32;
+            const uint64_t rh = sw128_desc(sb + OFF_R + off), rl = sw128_desc(sb + OFF_R + 16384 + off);
+            mma_bf16(tmem + COL_E, rh, sw128_desc(sb + OFF_T + off), ID64, ks > 0);
+            mma_bf16(tmem + COL_E, rh, sw128_desc(sb + OFF_T + 8192 + off), ID64, 1);
+            mma_bf16(tmem + COL_E, rl, sw128_desc(sb + OFF_T + off), ID64, 1);
+          }
+        }
+      } else {
+        emu_mma<64, 64>(tl, COL_E, sm + OFF_R, 0, sm + OFF_T, 0, false, row, half);
+        emu_mma<64, 64>(tl, COL_E, sm + OFF_R, 0, sm + OFF_T + 8192, 0, true, row, half);
+        emu_mma<64, 64>(tl, COL_E, sm + OFF_R + 16384, 0, sm + OFF_T, 0, true, row, half);
+      }
+      finish_group(bar_e);
+      if (!ok) break;
+
+      // ================= E~ = E diag(exp(gamma_L - gamma) ik) -> hi/lo;  E -> bf16 (output operand)
+      {
+        float ev[32], es[32];
+        tmem_ld32(tl + COL_E + half * 32, ev);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) es[i] = ev[i] * s_cs[half * 32 + i];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          store8_split(sm + OFF_R, sm + OFF_R + 16384, 0, row, half * 32 + 8 * q, es + 8 * q);
+          store8_split(sm + OFF_T, nullptr, 0, row, half * 32 + 8 * q, ev + 8 * q);
         }
       }
-    } else {
-      emu_mma<64, 64>(tl + COL_E, sb + OFF_RHI, 0, sb + OFF_T, 0, false, tid);
-      emu_mma<64, 64>(tl + COL_E, sb + OFF_RHI, 0, sb + OFF_T + 8192, 0, true, tid);
-      emu_mma<64, 64>(tl + COL_E, sb + OFF_RLO, 0, sb + OFF_T, 0, true, tid);
-    }
-    finish_group(bar_e);
-    if (!ok) break;
+      operands_ready();
 
-    // ================= E~ = E diag(exp(gamma_L - gamma) ik) -> hi/lo;  E -> bf16 (output operand)
-    for (int t0 = 0; t0 < 64; t0 += 32) {
-      float ev[32], es[32];
-      tmem_ld32(tl + COL_E + t0, ev);
+      // ================= S += E~ K  (N = 128 keys; B = K^T rows),  O2 = E P^T
+      if constexpr (!kEmulate) {
+        if (tid == 0) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) es[i] = ev[i] * s_cs[t0 + i];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        store8_split(sb + OFF_RHI, sb + OFF_RLO, 0, tid, t0 + 8 * q, es + 8 * q);
-        store8_split(sb + OFF_T, 0, 0, tid, t0 + 8 * q, ev + 8 * q);
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t off = ks * 32;
+            const uint64_t bkt = sw128_desc(sb + OFF_KT + off);
+            mma_bf16(tmem + COL_S, sw128_desc(sb + OFF_R + off), bkt, ID128, 1);
+            mma_bf16(tmem + COL_S, sw128_desc(sb + OFF_R + 16384 + off), bkt, ID128, 1);
+            mma_bf16(tmem + COL_O2, sw128_desc(sb + OFF_T + off), sw128_desc(sb + OFF_P + off), ID64, ks > 0);
+          }
+        }
+      } else {
+        emu_mma<128, 64>(tl, COL_S, sm + OFF_R, 0, sm + OFF_KT, 0, true, row, half);
+        emu_mma<128, 64>(tl, COL_S, sm + OFF_R + 16384, 0, sm + OFF_KT, 0, true, row, half);
+        emu_mma<64, 64>(tl, COL_O2, sm + OFF_T, 0, sm + OFF_P, 0, false, row, half);
       }
-    }
-    operands_ready();
+      finish_group(bar_s);
+      if (!ok) break;
 
-    // ================= S += E~ K  (N = 128 keys; B = K^T rows),  O2 = E P^T
-    if constexpr (!kEmulate) {
-      if (tid == 0) {
+      // ================= output: o = O1 diag(Gamma iq q_scale) + O2, staged token-major in the
+      // (now dead) S0 area, then the sigmoid-gated RMSNorm over the value dimension
+      {
+        float o1[32], o2[32];
+        tmem_ld32(tl + COL_O1 + half * 32, o1);
+        tmem_ld32(tl + COL_O2 + half * 32, o2);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t off = ks * 32;
-          const uint64_t bkt = sw128_desc(sb + OFF_KT + off);
-          mma_bf16(tmem + COL_S, sw128_desc(sb + OFF_RHI + off), bkt, ID128, 1);
-          mma_bf16(tmem + COL_S, sw128_desc(sb + OFF_RLO + off), bkt, ID128, 1);
-          mma_bf16(tmem + COL_O2, sw128_desc(sb + OFF_T + off), sw128_desc(sb + OFF_P + off), ID64, ks > 0);
+        for (int i = 0; i < 32; ++i) {
+          const int t = half * 32 + i;
+          s_work[t * LDO + row] = fmaf(o1[i], s_co[t], o2[i]);
         }
       }
-    } else {
-      emu_mma<128, 64>(tl + COL_S, sb + OFF_RHI, 0, sb + OFF_KT, 0, true, tid);
-      emu_mma<128, 64>(tl + COL_S, sb + OFF_RLO, 0, sb + OFF_KT, 0, true, tid);
-      emu_mma<64, 64>(tl + COL_O2, sb + OFF_T, 0, sb + OFF_P, 0, false, tid);
-    }
-    finish_group(bar_s);
-    if (!ok) break;
-
-    // ================= output: o = O1 diag(Gamma iq q_scale) + O2, staged token-major, then
-    // (optionally) the sigmoid-gated RMSNorm over the value dimension, coalesced bf16 stores
-    for (int t0 = 0; t0 < 64; t0 += 32) {
-      float o1[32], o2[32];
-      tmem_ld32(tl + COL_O1 + t0, o1);
-      tmem_ld32(tl + COL_O2 + t0, o2);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s_work[(t0 + i) * LDO + tid] = fmaf(o1[i], s_co[t0 + i], o2[i]);
-    }
-    __syncthreads();
-    {
-      float wf[4] = {1.f, 1.f, 1.f, 1.f};
-      if (p.z) {
-        const uint2 ww = __ldg(reinterpret_cast<const uint2*>(p.norm_w + lane * 4));
-        wf[0] = __uint_as_float(ww.x << 16); wf[1] = __uint_as_float(ww.x & 0xFFFF0000u);
-        wf[2] = __uint_as_float(ww.y << 16); wf[3] = __uint_as_float(ww.y & 0xFFFF0000u);
-      }
-      for (int t = warp; t < L; t += kThreads / 32) {
-        const float4 v = *reinterpret_cast<const float4*>(s_work + t * LDO + lane * 4);
-        float r4[4] = {v.x, v.y, v.z, v.w};
-        const size_t base = ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4;
+      __syncthreads();
+      {
+        float wf[4] = {1.f, 1.f, 1.f, 1.f};
         if (p.z) {
-          float ss = r4[0] * r4[0] + r4[1] * r4[1] + r4[2] * r4[2] + r4[3] * r4[3];
-#pragma unroll
-          for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-          const float rstd = rsqrtf(ss * (1.0f / kHeadDim) + p.rms_eps);
-          const uint2 zz = __ldg(reinterpret_cast<const uint2*>(p.z + base));
-          const float zf[4] = {__uint_as_float(zz.x << 16), __uint_as_float(zz.x & 0xFFFF0000u),
-                               __uint_as_float(zz.y << 16), __uint_as_float(zz.y & 0xFFFF0000u)};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) r4[i] = r4[i] * rstd * wf[i] * sigmoidf_(zf[i]);
+          const uint2 ww = __ldg(reinterpret_cast<const uint2*>(p.norm_w + lane * 4));
+          wf[0] = __uint_as_float(ww.x << 16); wf[1] = __uint_as_float(ww.x & 0xFFFF0000u);
+          wf[2] = __uint_as_float(ww.y << 16); wf[3] = __uint_as_float(ww.y & 0xFFFF0000u);
         }
-        *reinterpret_cast<uint2*>(p.out + base) = make_uint2(pack_bf2(r4[0], r4[1]), pack_bf2(r4[2], r4[3]));
+        for (int t = warp; t < L; t += kThreads / 32) {
+          const float4 v = *reinterpret_cast<const float4*>(s_work + t * LDO + lane * 4);
+          float r4[4] = {v.x, v.y, v.z, v.w};
+          const size_t base = ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4;
+          if (p.z) {
+            float ss = r4[0] * r4[0] + r4[1] * r4[1] + r4[2] * r4[2] + r4[3] * r4[3];
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+            const float rstd = rsqrtf(ss * (1.0f / kHeadDim) + p.rms_eps);
+            const uint2 zz = __ldg(reinterpret_cast<const uint2*>(p.z + base));
+            const float zf[4] = {__uint_as_float(zz.x << 16), __uint_as_float(zz.x & 0xFFFF0000u),
+                                 __uint_as_float(zz.y << 16), __uint_as_float(zz.y & 0xFFFF0000u)};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) r4[i] = r4[i] * rstd * wf[i] * sigmoidf_(zf[i]);
+          }
+          *reinterpret_cast<uint2*>(p.out + base) = make_uint2(pack_bf2(r4[0], r4[1]), pack_bf2(r4[2], r4[3]));
+        }
+      }
+      __syncthreads();
+    }
+    if (!ok) break;
+
+    // ---- final state -> global
+    if (p.state_out) {
+      const size_t row_off = (((size_t)n * p.Hv + h) * kHeadDim + row) * kHeadDim;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int c0 = half * 64 + c * 32;
+        float v[32];
+        tmem_ld32(tl + COL_S + c0, v);
+        float4* dst = reinterpret_cast<float4*>(p.state_out + row_off + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       }
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
   }
 
-  // ---- final state -> global (thread r: value row r)
-  if (ok && p.state_out) {
-    const size_t row_off = (((size_t)n * p.Hv + h) * kHeadDim + tid) * kHeadDim;
-    for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
-      float v[32];
-      tmem_ld32(tl + COL_S + c0, v);
-      float4* dst = reinterpret_cast<float4*>(p.state_out + row_off + c0);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    }
-  }
+  // after an early exit, let loads still in flight land before the CTA leaves (bounded)
+  if (pend_qk) mbar_wait(bar_qk, ph_qk, kWaitLimit);
+  if (pend_v) mbar_wait(bar_v, ph_v, kWaitLimit);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+}
+
+// One CTA: longest-first order of the sequences (ties by index) and a zeroed work counter.
+// Sequences with inconsistent cu_seqlens get length 0 here; the main kernel reports them.
+__global__ void __launch_bounds__(1024) chunk_schedule_kernel(const int32_t* cu, int N, int32_t* order,
+                                                              unsigned* counter) {
+  extern __shared__ int32_t s_len[];
+  if (threadIdx.x == 0) *counter = 0u;
+  const bool sorted = N <= kScheduleSortMax;
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    if (sorted) s_len[i] = max(0, __ldg(cu + i + 1) - __ldg(cu + i));
+    else order[i] = i;
+  }
+  if (!sorted) return;
+  __syncthreads();
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const int li = s_len[i];
+    int rank = 0;
+    for (int j = 0; j < N; ++j) {
+      const int lj = s_len[j];
+      rank += (lj > li) || (lj == li && j < i);
+    }
+    order[rank] = i;
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
 }
 
 template <bool kEmulate>
@@ -578,22 +685,55 @@ cudaError_t launch_impl(const LaunchEnv& env, const ChunkParams& p) {
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  const long blocks = (long)p.N * p.Hv;
-  chunk_prefill_kernel<kEmulate><<<(unsigned)blocks, kThreads, SMEM_BYTES, env.stream>>>(p);
+  static int sm_count[64] = {0};
+  int sms = dev < 64 ? sm_count[dev] : 0;
+  if (sms == 0) {
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) sm_count[dev] = sms;
+  }
+  const long items = (long)p.N * p.Hv;
+  const int grid = (int)(items < sms ? items : sms);
+  chunk_prefill_kernel<kEmulate><<<grid, kThreads, SMEM_BYTES, env.stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+size_t chunk_prefill_workspace_bytes(int N) {
+  return 256 + (((size_t)(N > 0 ? N : 0) * sizeof(int32_t) + 255) / 256) * 256;
+}
+
 cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t* qkv, const float* g,
                                  const float* beta, const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale,
                                  float l2_eps, const float* state_in, float* state_out, const uint16_t* z,
-                                 const uint16_t* norm_w, float rms_eps, uint16_t* out) {
+                                 const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace) {
   if (N <= 0) return cudaSuccess;
   ChunkParams p;
-  p.qkv = qkv; p.g = g; p.beta = beta; p.cu = cu; p.state_in = state_in; p.state_out = state_out;
+  memset(&p, 0, sizeof p);
+  const int C = 2 * Hk * kHeadDim + Hv * kHeadDim;
+  if (T > 0) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(&p.tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(qkv), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.counter = reinterpret_cast<unsigned*>(ws);
+  p.order = reinterpret_cast<const int32_t*>(ws + 256);
+  p.g = g; p.beta = beta; p.cu = cu; p.state_in = state_in; p.state_out = state_out;
   p.z = z; p.norm_w = norm_w; p.out = out; p.err = env.err;
   p.N = N; p.T = T; p.Hk = Hk; p.Hv = Hv; p.q_scale = q_scale; p.l2_eps = l2_eps; p.rms_eps = rms_eps;
+  const size_t sched_smem = N <= kScheduleSortMax ? (size_t)N * sizeof(int32_t) : 0;
+  chunk_schedule_kernel<<<1, 1024, sched_smem, env.stream>>>(cu, N, reinterpret_cast<int32_t*>(ws + 256), p.counter);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   return mode == 1 ? launch_impl<true>(env, p) : launch_impl<false>(env, p);
 }
 

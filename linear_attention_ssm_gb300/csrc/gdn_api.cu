@@ -153,9 +153,8 @@ gdn_status gdn_conv1d_prefill(const gdn_geometry* geo, const gdn_bf16* x, const 
 
 size_t gdn_chunk_prefill_workspace_size(const gdn_geometry* geo, int32_t num_seqs, int32_t total_tokens) {
   (void)geo;
-  (void)num_seqs;
   (void)total_tokens;
-  return 0;
+  return num_seqs > 0 ? gdn::chunk_prefill_workspace_bytes(num_seqs) : 0;
 }
 
 gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g, const float* beta,
@@ -191,6 +190,8 @@ gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const
   const size_t need = gdn_chunk_prefill_workspace_size(geo, num_seqs, total_tokens);
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need, workspace_bytes);
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(GDN_ERR_MISALIGNED, "workspace is not 256-byte aligned");
   if (state_in && state_out && state_in != state_out) {
     const size_t sb = (size_t)num_seqs * geo->num_v_heads * gdn::kHeadDim * gdn::kHeadDim * 4;
     if (overlaps(state_in, sb, state_out, sb))
@@ -200,7 +201,7 @@ gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const
   if ((s = make_env(stream, &env)) != GDN_OK) return s;
   return launched(gdn::launch_chunk_prefill(env, g_chunk_mode, qkv, g, beta, cu_seqlens, num_seqs, total_tokens,
                                             geo->num_k_heads, geo->num_v_heads, q_scale, l2_eps, state_in,
-                                            state_out, z, norm_w, rms_eps, out),
+                                            state_out, z, norm_w, rms_eps, out, workspace),
                   "chunk prefill launch");
 }
 

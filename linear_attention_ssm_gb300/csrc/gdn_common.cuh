@@ -62,6 +62,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, uint32
   return false;
 }
 
+// Arrive on the mbarrier and add `bytes` to the transaction count the phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(addr), "r"(bytes) : "memory");
+}
+
+// ------------------------------------------------------------------ TMA
+
+// 2D tiled bulk tensor load global -> shared; completion is signalled on `bar` (complete_tx).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ proxy / tcgen05 fences
 
 // generic-proxy shared-memory writes -> visible to the async proxy (tensor-core operand reads)

@@ -21,10 +21,13 @@ cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const ui
                                const uint16_t* z, const uint16_t* norm_w, float q_scale, float l2_eps,
                                float rms_eps, uint16_t* out, int B, int Hk, int Hv);
 
+// Workspace of the chunk prefill: a work counter and the longest-first sequence order.
+size_t chunk_prefill_workspace_bytes(int N);
+
 // mode 0: tcgen05 tensor cores; mode 1: the same data flow with the MMAs emulated on CUDA cores
 cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t* qkv, const float* g,
                                  const float* beta, const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale,
                                  float l2_eps, const float* state_in, float* state_out, const uint16_t* z,
-                                 const uint16_t* norm_w, float rms_eps, uint16_t* out);
+                                 const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace);
 
 }  // namespace gdn

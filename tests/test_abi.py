@@ -115,8 +115,13 @@ def test_decode_and_norm_reject_bad_arguments(lib):
     assert lib.gdn_gated_rmsnorm(geo, None, None, None, 1e-6, None, 0, None) == 0
 
 
-def test_workspace_query_is_callable(lib):
-    assert lib.gdn_chunk_prefill_workspace_size(_geo(), 8, 32735) >= 0
+def test_workspace_is_required_and_aligned(lib):
+    need = lib.gdn_chunk_prefill_workspace_size(_geo(), 8, 32735)
+    assert need >= 8 * 4
+    assert lib.gdn_chunk_prefill_workspace_size(_geo(), 0, 0) == 0
+    assert _chunk(lib, N=8, T=32735) == 7                                    # missing workspace
+    assert _chunk(lib, N=8, T=32735, ws=FAKE, wsb=need - 1) == 7             # too small
+    assert _chunk(lib, N=8, T=32735, ws=ctypes.c_void_p(0x10010), wsb=need) == 3  # not 256-byte aligned
 
 
 def test_binding_refuses_cpu_tensors():

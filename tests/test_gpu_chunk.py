@@ -182,3 +182,28 @@ def test_negative_control_dropped_carry_localises_to_the_tail():
     tail = out_error_ratio(out[64:], bad["out"][64:])
     assert head <= 1.0
     assert tail > NEG_CONTROL_RATIO
+
+
+def test_many_sequences_longest_first_schedule():
+    """300 sequences of mixed lengths: every (sequence, head) item is processed exactly once by
+    the persistent grid in longest-first order."""
+    gen = torch.Generator().manual_seed(16)
+    lengths = torch.randint(0, 150, (300,), generator=gen).tolist()
+    inp = prefill_inputs(lengths, seed=16)
+    ref = run_oracle(inp, heads=[0, 5, 47])
+    out, st = run_gpu(inp, ref["y"])
+    for h in (0, 5, 47):
+        assert_out_close(out[:, h], ref["out"][:, h], f"out, head {h}")
+        assert_state_close(st[:, h], ref["state"][:, h], f"states, head {h}")
+
+
+def test_more_sequences_than_the_sorted_schedule():
+    """5000 short sequences (beyond the longest-first sort limit): identity order."""
+    gen = torch.Generator().manual_seed(17)
+    lengths = torch.randint(0, 3, (5000,), generator=gen).tolist()
+    inp = prefill_inputs(lengths, seed=17)
+    ref = run_oracle(inp, heads=[3, 44])
+    out, st = run_gpu(inp, ref["y"])
+    for h in (3, 44):
+        assert_out_close(out[:, h], ref["out"][:, h], f"out, head {h}")
+        assert_state_close(st[:, h], ref["state"][:, h], f"states, head {h}")

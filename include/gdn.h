@@ -179,6 +179,34 @@ GDN_API gdn_status gdn_decode_step(const gdn_geometry* geo, const gdn_bf16* x,
                                    const gdn_bf16* norm_w, float q_scale, float l2_eps,
                                    float rms_eps, gdn_bf16* out, int32_t batch, void* stream);
 
+/* Capacity of the fixed scratch used by gdn_chunk_prefill_noalloc. */
+#define GDN_NOALLOC_MAX_SEQS 16384
+#define GDN_NOALLOC_SCRATCH_BYTES (256 + 4 * GDN_NOALLOC_MAX_SEQS) /* 65,792 bytes */
+
+/*
+ * gdn_chunk_prefill for callers that cannot allocate device memory when they call it -- for
+ * example a host that hands all device memory to its own pool up front, or a latency-critical
+ * loop where cudaMalloc/cudaFree (which can synchronise the device) are not allowed.  Same
+ * arguments, results and errors as gdn_chunk_prefill, without the workspace pair: the call
+ * allocates nothing and calls no allocating routine.
+ *
+ * Its scratch is one fixed device array of GDN_NOALLOC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library keeps until the process exits; it holds the schedule of up to
+ * GDN_NOALLOC_MAX_SEQS sequences, and a larger num_seqs is refused with GDN_ERR_INVALID_ARGUMENT
+ * (nothing launched).  The first call on a device looks up that array's device address with the
+ * device current; make this first call before any stream capture.  All calls on a device share
+ * the array and it keeps the last call's contents: each call rewrites the whole schedule and
+ * zeroes its work counter before the main kernel reads them, but two calls whose kernels overlap
+ * on the GPU (for example on two unordered streams) race on the array and give wrong results.
+ * There is no counterpart of this entry point on the pages.
+ */
+GDN_API gdn_status gdn_chunk_prefill_noalloc(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g,
+                                             const float* beta, const int32_t* cu_seqlens, int32_t num_seqs,
+                                             int32_t total_tokens, float q_scale, float l2_eps,
+                                             const float* state_in, float* state_out, const gdn_bf16* z,
+                                             const gdn_bf16* norm_w, float rms_eps, gdn_bf16* out,
+                                             void* stream);
+
 /*
  * Waits for `stream`, then reads and clears the library's device error word.  Returns GDN_OK,
  * GDN_ERR_DEVICE_ARGUMENT (a kernel skipped a sequence with bad cu_seqlens entries),

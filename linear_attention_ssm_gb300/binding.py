@@ -55,6 +55,7 @@ def load_library():
             "gdn_conv1d_prefill": ([G, P, P, P, I, I, P, P, P, P], ctypes.c_int),
             "gdn_chunk_prefill_workspace_size": ([G, I, I], S),
             "gdn_chunk_prefill": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P, S, P], ctypes.c_int),
+            "gdn_chunk_prefill_noalloc": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
             "gdn_gated_rmsnorm": ([G, P, P, P, F, P, I, P], ctypes.c_int),
             "gdn_decode_step": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
             "gdn_check_device_errors": ([P], ctypes.c_int),

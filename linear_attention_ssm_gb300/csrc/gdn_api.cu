@@ -251,6 +251,42 @@ gdn_status gdn_decode_step(const gdn_geometry* geo, const gdn_bf16* x, const gdn
                   "decode launch");
 }
 
+// ---- allocation-free chunk prefill: the schedule lives in a fixed device array of this file
+}  // extern "C"
+
+namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_chunk_prefill_noalloc(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g,
+                                     const float* beta, const int32_t* cu_seqlens, int32_t num_seqs,
+                                     int32_t total_tokens, float q_scale, float l2_eps, const float* state_in,
+                                     float* state_out, const gdn_bf16* z, const gdn_bf16* norm_w, float rms_eps,
+                                     gdn_bf16* out, void* stream) {
+  if (num_seqs > GDN_NOALLOC_MAX_SEQS)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "num_seqs=%d exceeds the %d sequences of the fixed scratch", num_seqs,
+                GDN_NOALLOC_MAX_SEQS);
+  if (gdn_chunk_prefill_workspace_size(geo, num_seqs, total_tokens) > GDN_NOALLOC_SCRATCH_BYTES)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "the fixed scratch is too small for num_seqs=%d", num_seqs);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(GDN_ERR_CUDA, "device index %d out of range", dev);
+  if (!g_noalloc_ptr[dev]) {
+    // host code only sees a stand-in for the array: its device address comes from the runtime
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr)
+      return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = ptr;
+  }
+  return gdn_chunk_prefill(geo, qkv, g, beta, cu_seqlens, num_seqs, total_tokens, q_scale, l2_eps, state_in,
+                           state_out, z, norm_w, rms_eps, out, g_noalloc_ptr[dev], GDN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 gdn_status gdn_check_device_errors(void* stream) {
   gdn::LaunchEnv env;
   gdn_status s = make_env(stream, &env);

@@ -49,7 +49,8 @@ constexpr uint32_t OFF_R = 114688;     // 32 KB: R hi/lo (16 KB each), then E~ h
 constexpr uint32_t OFF_T = 147456;     // 16 KB: T hi (8 KB) + T lo (8 KB); then E bf16 (16 KB)
 constexpr uint32_t OFF_P = 163840;     //  8 KB: P, 64 token rows x 64
 constexpr uint32_t OFF_V = 172032;     // 16 KB: V, 2 K-blocks of 64 value columns x 64 token rows
-constexpr uint32_t OFF_VEC = 188416;   // per-token vectors (8 x 64 floats) + norm partials (256)
+constexpr uint32_t OFF_Z = 188416;     // 16 KB: z of the chunk, [64 tokens][128] bf16 (gate input)
+constexpr uint32_t OFF_VEC = 204800;   // per-token vectors (8 x 64 floats) + norm partials (256)
 constexpr uint32_t OFF_BAR = OFF_VEC + (8 * 64 + 256) * 4;  // mbarriers, TMEM address, item slot
 constexpr uint32_t SMEM_USED = OFF_BAR + 128;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;            // + alignment slack
@@ -72,9 +73,11 @@ constexpr uint32_t kWaitLimit = 1u << 20;  // polls of one mbarrier before givin
 constexpr int kScheduleSortMax = 4096;     // longest-first ordering up to this many sequences
 constexpr uint32_t kBytesQK = 4 * 64 * 128;  // four 64 x 64 bf16 boxes
 constexpr uint32_t kBytesV = 2 * 64 * 128;
+constexpr uint32_t kBytesZ = 64 * 256;
 
 struct ChunkParams {
-  CUtensorMap tmap;  // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle
+  CUtensorMap tmap;    // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle
+  CUtensorMap tmap_z;  // z [T][Hv * 128] bf16, box 128 x 64, no swizzle (valid when z != NULL)
   const float* g;
   const float* beta;
   const int32_t* cu;
@@ -212,10 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 64);
   int* item_slot = reinterpret_cast<int*>(sm + OFF_BAR + 72);
   const uint32_t bar_g = smem_u32(&bars[0]), bar_x = smem_u32(&bars[1]), bar_e = smem_u32(&bars[2]),
-                 bar_s = smem_u32(&bars[3]), bar_qk = smem_u32(&bars[4]), bar_v = smem_u32(&bars[5]);
+                 bar_s = smem_u32(&bars[3]), bar_qk = smem_u32(&bars[4]), bar_v = smem_u32(&bars[5]),
+                 bar_z = smem_u32(&bars[6]);
 
   if (tid == 0) {
-    for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 7; ++i) mbar_init(smem_u32(&bars[i]), 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -228,8 +232,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   constexpr uint32_t ID64 = idesc_bf16_f32(128, 64);
   constexpr uint32_t ID128 = idesc_bf16_f32(128, 128);
   bool ok = true;
-  uint32_t ph_mma = 0, ph_qk = 0, ph_v = 0;  // phase parities
-  bool pend_qk = false, pend_v = false;      // TMA loads issued and not yet awaited (uniform)
+  uint32_t ph_mma = 0, ph_qk = 0, ph_v = 0, ph_z = 0;  // phase parities
+  bool pend_qk = false, pend_v = false, pend_z = false;  // TMA loads issued, not yet awaited
+  const bool gated = p.z != nullptr;
+  float wf[4] = {1.f, 1.f, 1.f, 1.f};  // norm weight of this lane's 4 value columns
+  if (gated) {
+    const uint2 ww = __ldg(reinterpret_cast<const uint2*>(p.norm_w + lane * 4));
+    wf[0] = __uint_as_float(ww.x << 16); wf[1] = __uint_as_float(ww.x & 0xFFFF0000u);
+    wf[2] = __uint_as_float(ww.y << 16); wf[3] = __uint_as_float(ww.y & 0xFFFF0000u);
+  }
+  float g_next = 0.f, b_next = 0.f;  // g and beta of the next chunk (threads 0..63)
 
   auto wait_bar = [&](uint32_t bar, uint32_t& ph) {
     const bool got = mbar_wait(bar, ph, kWaitLimit);
@@ -271,6 +283,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       tma_load_2d(sb + OFF_V + kb * 8192, &p.tmap, 2 * p.Hk * kHeadDim + h * kHeadDim + kb * 64, c0, bar_v);
   };
 
+  auto issue_z = [&](int c0, int h) {
+    mbar_arrive_expect_tx(bar_z, kBytesZ);
+    tma_load_2d(sb + OFF_Z, &p.tmap_z, h * kHeadDim, c0, bar_z);
+  };
+  auto load_gb = [&](int c0, int L, int h) {  // g, beta of a chunk -> registers of threads < 64
+    g_next = 0.f;
+    b_next = 0.f;
+    if (tid < L) {
+      g_next = __ldg(p.g + (size_t)(c0 + tid) * p.Hv + h);
+      b_next = __ldg(p.beta + (size_t)(c0 + tid) * p.Hv + h);
+    }
+  };
+
   for (;;) {
     if (tid == 0) *item_slot = (int)atomicAdd(p.counter, 1u);
     __syncthreads();
@@ -289,8 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     if (tid == 0 && seq_e > seq_s) {
       issue_qk(seq_s, kh);
       issue_v(seq_s, h);
+      if (gated) issue_z(seq_s, h);
     }
     pend_qk = pend_v = seq_e > seq_s;
+    pend_z = gated && seq_e > seq_s;
+    if (seq_e > seq_s) load_gb(seq_s, min(kChunk, seq_e - seq_s), h);
 
     // ---- initial state -> tensor memory (thread (row, half): 64 columns of row `row`)
     {
@@ -319,14 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       const bool has_next = c0 + kChunk < seq_e;
 
       // ================= prepare: g, beta, norms, K^T, cumsum, per-token factors
-      if (tid < 64) {
-        float gv = 0.f, bv = 0.f;
-        if (tid < L) {
-          gv = __ldg(p.g + (size_t)(c0 + tid) * p.Hv + h);
-          bv = __ldg(p.beta + (size_t)(c0 + tid) * p.Hv + h);
-        }
-        s_g[tid] = gv;
-        s_beta[tid] = bv;
+      if (tid < 64) {  // fetched one chunk ahead
+        s_g[tid] = g_next;
+        s_beta[tid] = b_next;
       }
       wait_bar(bar_qk, ph_qk);
       pend_qk = false;
@@ -489,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       // the q/k tile is free: fetch the next chunk's
       if (tid == 0 && has_next) issue_qk(c0 + kChunk, kh);
       pend_qk = has_next;
+      if (has_next) load_gb(c0 + kChunk, min(kChunk, seq_e - c0 - kChunk), h);
 
       // ================= R = diag(beta) V - diag(beta Gamma ik) (S0 K^T)^T  -> hi/lo (value-major)
       wait_bar(bar_v, ph_v);
@@ -575,24 +599,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
           s_work[t * LDO + row] = fmaf(o1[i], s_co[t], o2[i]);
         }
       }
-      __syncthreads();
+      if (gated) {
+        wait_bar(bar_z, ph_z);
+        pend_z = false;
+        if (!ok) break;
+      } else {
+        __syncthreads();
+      }
       {
-        float wf[4] = {1.f, 1.f, 1.f, 1.f};
-        if (p.z) {
-          const uint2 ww = __ldg(reinterpret_cast<const uint2*>(p.norm_w + lane * 4));
-          wf[0] = __uint_as_float(ww.x << 16); wf[1] = __uint_as_float(ww.x & 0xFFFF0000u);
-          wf[2] = __uint_as_float(ww.y << 16); wf[3] = __uint_as_float(ww.y & 0xFFFF0000u);
-        }
         for (int t = warp; t < L; t += kThreads / 32) {
           const float4 v = *reinterpret_cast<const float4*>(s_work + t * LDO + lane * 4);
           float r4[4] = {v.x, v.y, v.z, v.w};
           const size_t base = ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4;
-          if (p.z) {
+          if (gated) {
             float ss = r4[0] * r4[0] + r4[1] * r4[1] + r4[2] * r4[2] + r4[3] * r4[3];
 #pragma unroll
             for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
             const float rstd = rsqrtf(ss * (1.0f / kHeadDim) + p.rms_eps);
-            const uint2 zz = __ldg(reinterpret_cast<const uint2*>(p.z + base));
+            const uint2 zz = *reinterpret_cast<const uint2*>(sm + OFF_Z + t * 256 + lane * 8);
             const float zf[4] = {__uint_as_float(zz.x << 16), __uint_as_float(zz.x & 0xFFFF0000u),
                                  __uint_as_float(zz.y << 16), __uint_as_float(zz.y & 0xFFFF0000u)};
 #pragma unroll
@@ -601,7 +625,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
           *reinterpret_cast<uint2*>(p.out + base) = make_uint2(pack_bf2(r4[0], r4[1]), pack_bf2(r4[2], r4[3]));
         }
       }
+      fence_proxy_async_smem();  // z reads above precede the next z tile's TMA write
       __syncthreads();
+      if (gated && has_next) {
+        if (tid == 0) issue_z(c0 + kChunk, h);
+        pend_z = true;
+      }
     }
     if (!ok) break;
 
@@ -626,6 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   // after an early exit, let loads still in flight land before the CTA leaves (bounded)
   if (pend_qk) mbar_wait(bar_qk, ph_qk, kWaitLimit);
   if (pend_v) mbar_wait(bar_v, ph_v, kWaitLimit);
+  if (pend_z) mbar_wait(bar_z, ph_z, kWaitLimit);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -723,6 +753,15 @@ cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t*
                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (z) {
+      const cuuint64_t zdims[2] = {(cuuint64_t)Hv * kHeadDim, (cuuint64_t)T};
+      const cuuint64_t zstrides[1] = {(cuuint64_t)Hv * kHeadDim * 2};
+      const cuuint32_t zbox[2] = {128, 64};
+      const CUresult rz = enc(&p.tmap_z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(z), zdims,
+                              zstrides, zbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (rz != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.counter = reinterpret_cast<unsigned*>(ws);

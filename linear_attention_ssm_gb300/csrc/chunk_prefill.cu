@@ -51,12 +51,11 @@ constexpr uint32_t OFF_P = 163840;     //  8 KB: P, 64 token rows x 64
 constexpr uint32_t OFF_V = 172032;     // 16 KB: V, 2 K-blocks of 64 value columns x 64 token rows
 constexpr uint32_t OFF_Z = 188416;     // 16 KB: z of the chunk, [64 tokens][128] bf16 (gate input)
 constexpr uint32_t OFF_VEC = 204800;   // per-token vectors (8 x 64 floats) + norm partials (256)
-constexpr uint32_t OFF_BAR = OFF_VEC + (8 * 64 + 256) * 4;  // mbarriers, TMEM address, item slot
+constexpr uint32_t OFF_M = OFF_VEC + (8 * 64 + 256) * 4;    // 3.75 KB: block products of the solve
+constexpr uint32_t OFF_BAR = OFF_M + 3 * 16 * 20 * 4;        // mbarriers, TMEM address, item slot
 constexpr uint32_t SMEM_USED = OFF_BAR + 128;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;            // + alignment slack
-constexpr uint32_t LDA = 65;   // row stride (floats) of the solve matrices
 constexpr uint32_t LDO = 132;  // row stride (floats) of the output staging
-static_assert((2 * 64 * LDA + 3 * 256) * 4 <= 65536, "solve work must fit the S0 area");
 static_assert(64 * LDO * 4 <= 65536, "output staging must fit the S0 area");
 static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
@@ -139,11 +138,19 @@ __device__ void emu_mma(uint32_t t_lane, uint32_t col, const uint8_t* a_tile, ui
   }
 }
 
-// T = (I + A)^-1 for a strictly lower triangular 64 x 64 A (row stride LDA), by 16 x 16 blocks:
-// the four diagonal blocks by right-looking forward substitution with the column in registers
-// (one thread per column), then the off-diagonal blocks by block distance d:
-// T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
-__device__ void solve_unit_lower(const float* sA, float* sT, float* sM, int tid) {
+// Element (r, c) of the 64 x 64 fp32 inverse T: rows of 64 floats whose 16-byte groups are
+// XOR-permuted by the row, so float4 reads of a row segment and float4 writes of a block row
+// spread over the banks.
+__device__ __forceinline__ int tidx(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 15)) & 15) << 2) + (c & 3); }
+
+// T = (I + A)^-1 for a strictly lower triangular 64 x 64 A, by 16 x 16 blocks.  A is given
+// transposed (sAt[k * 64 + r] = A[r][k]).  The four diagonal blocks are inverted by
+// right-looking forward substitution with one column per thread held in registers; then, for
+// block distance d = 1, 2, 3, every off-diagonal block (i, j = i - d) is
+//   M  = sum_{k=j}^{i-1} A_ik T_kj,    T_ij = -T_ii M,
+// each 16 x 16 product split over two warps, a lane holding one row and four columns.
+__device__ void solve_unit_lower(const float* sAt, float* sT, float* sM, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
   if (tid < 64) {
     const int b = tid >> 4, c = tid & 15, o = b * 16;
     float x[16];
@@ -153,37 +160,47 @@ __device__ void solve_unit_lower(const float* sA, float* sT, float* sM, int tid)
     for (int k = 0; k < 15; ++k) {
       const float xk = x[k];
 #pragma unroll
-      for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-sA[(o + i) * LDA + o + k], xk, x[i]);
+      for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-sAt[(o + k) * 64 + o + i], xk, x[i]);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) sT[(o + i) * LDA + o + c] = x[i];
+    for (int i = 0; i < 16; ++i) sT[tidx(o + i, o + c)] = x[i];
   }
   for (int idx = tid; idx < 64 * 64; idx += kThreads) {
     const int r = idx >> 6, cc = idx & 63;
-    if ((cc >> 4) > (r >> 4)) sT[r * LDA + cc] = 0.f;
+    if ((cc >> 4) > (r >> 4)) sT[tidx(r, cc)] = 0.f;
   }
   __syncthreads();
+  const int r = (warp & 1) * 8 + (lane >> 2);  // row inside the 16 x 16 block
+  const int c0 = (lane & 3) * 4;               // first of this lane's four columns
   for (int d = 1; d < 4; ++d) {
     const int nb = 4 - d;
-    for (int idx = tid; idx < nb * 256; idx += kThreads) {
-      const int bi = idx >> 8, e = idx & 255, r = e >> 4, cc = e & 15;
-      const int i = d + bi, jb = i - d;
-      float acc = 0.f;
-      for (int kb = jb; kb < i; ++kb)
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-          acc = fmaf(sA[(i * 16 + r) * LDA + kb * 16 + u], sT[(kb * 16 + u) * LDA + jb * 16 + cc], acc);
-      sM[bi * 256 + e] = acc;
+    const int bi = warp >> 1, i = d + bi, jb = i - d;
+    if (warp < 2 * nb) {
+      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll 4
+      for (int k = jb * 16; k < i * 16; ++k) {
+        const float a = sAt[k * 64 + i * 16 + r];
+        const float4 bv = *reinterpret_cast<const float4*>(sT + tidx(k, jb * 16 + c0));
+        acc0 = fmaf(a, bv.x, acc0);
+        acc1 = fmaf(a, bv.y, acc1);
+        acc2 = fmaf(a, bv.z, acc2);
+        acc3 = fmaf(a, bv.w, acc3);
+      }
+      *reinterpret_cast<float4*>(sM + bi * 320 + r * 20 + c0) = make_float4(acc0, acc1, acc2, acc3);
     }
     __syncthreads();
-    for (int idx = tid; idx < nb * 256; idx += kThreads) {
-      const int bi = idx >> 8, e = idx & 255, r = e >> 4, cc = e & 15;
-      const int i = d + bi, jb = i - d;
-      float acc = 0.f;
+    if (warp < 2 * nb) {
+      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
-      for (int u = 0; u < 16; ++u)
-        if (u <= r) acc = fmaf(sT[(i * 16 + r) * LDA + i * 16 + u], sM[bi * 256 + u * 16 + cc], acc);
-      sT[(i * 16 + r) * LDA + jb * 16 + cc] = -acc;
+      for (int u = 0; u < 16; ++u) {
+        const float a = sT[tidx(i * 16 + r, i * 16 + u)];  // zero above the diagonal
+        const float4 bv = *reinterpret_cast<const float4*>(sM + bi * 320 + u * 20 + c0);
+        acc0 = fmaf(a, bv.x, acc0);
+        acc1 = fmaf(a, bv.y, acc1);
+        acc2 = fmaf(a, bv.z, acc2);
+        acc3 = fmaf(a, bv.w, acc3);
+      }
+      *reinterpret_cast<float4*>(sT + tidx(i * 16 + r, jb * 16 + c0)) = make_float4(-acc0, -acc1, -acc2, -acc3);
     }
     __syncthreads();
   }
@@ -201,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   const int ratio = p.Hv / p.Hk;
   const long total_items = (long)p.N * p.Hv;
 
-  float* s_gam = reinterpret_cast<float*>(sm + OFF_VEC);
+  float* s_gam = reinterpret_cast<float*>(sm + OFF_VEC);  // within-chunk cumsum of g, times log2(e)
   float* s_beta = s_gam + 64;
   float* s_ik = s_gam + 128;
   float* s_iq = s_gam + 192;
@@ -257,6 +274,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       tc_fence_after();
     } else {
       fence_proxy_async_smem();  // the emulated operand reads precede later TMA writes
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+    }
+  };
+  auto await_group = [&](uint32_t bar) {  // an MMA group committed earlier on `bar` (or emulated)
+    if constexpr (!kEmulate) {
+      uint32_t ph = ph_mma;
+      wait_bar(bar, ph);
+      tc_fence_after();
+    } else {
+      fence_proxy_async_smem();
       tc_fence_before();
       __syncthreads();
       tc_fence_after();
@@ -388,8 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         }
       }
       if (warp == 0) {
-        // inclusive scan of g over the chunk (lane l holds tokens 2l and 2l+1)
-        const float g0 = s_g[2 * lane], g1 = s_g[2 * lane + 1];
+        // inclusive scan of g over the chunk, in log2 units (lane l holds tokens 2l and 2l+1)
+        const float g0 = s_g[2 * lane] * kLog2e, g1 = s_g[2 * lane + 1] * kLog2e;
         float s = g0 + g1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -408,14 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       if (tid < 64) {
         const int t = tid;
         const float gam = s_gam[t], gamL = s_gam[L - 1];
-        const float Gam = expf(gam);
+        const float Gam = ex2_approx(gam);
         s_cx[t] = s_beta[t] * Gam * s_ik[t];
         s_co[t] = Gam * s_iq[t] * p.q_scale;
-        s_cs[t] = (t < L) ? expf(gamL - gam) * s_ik[t] : 0.f;
+        s_cs[t] = (t < L) ? ex2_approx(gamL - gam) * s_ik[t] : 0.f;
       }
       operands_ready();
 
-      // ================= Gram: G = [K; Q] K^T  (M = 128, N = 64, K = 128)
+      // ================= Gram: G = [K; Q] K^T  (M = 128, N = 64, K = 128), issued asynchronously
       if constexpr (!kEmulate) {
         if (tid == 0) {
 #pragma unroll
@@ -423,59 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
             mma_bf16(tmem + COL_G, sw128_desc(sb + OFF_QK + off), sw128_desc(sb + OFF_QK + off), ID64, ks > 0);
           }
+          mma_commit(bar_g);
         }
       } else {
         emu_mma<64, 128>(tl, COL_G, sm + OFF_QK, 16384, sm + OFF_QK, 16384, false, row, half);
       }
-      finish_group(bar_g);
-      if (!ok) break;
 
-      // ================= A (rows 0..63) and P (rows 64..127) from the Gram tile
+      // ================= S0 -> hi/lo operand tiles; tensor memory state <- Gamma_L S0 (under the Gram)
       {
-        float gr[32];
-        tmem_ld32(tl + COL_G + half * 32, gr);
-        float* sA = s_work;
-        if (row < 64) {
-          const int t = row;
-          const float bt = s_beta[t] * s_ik[t], gt = s_gam[t];
-#pragma unroll 8
-          for (int i = 0; i < 32; ++i) {
-            const int j = half * 32 + i;
-            sA[t * LDA + j] = (j < t) ? bt * expf(gt - s_gam[j]) * gr[i] * s_ik[j] : 0.f;
-          }
-        } else {
-          const int t = row - 64;
-          const float qt = s_iq[t] * p.q_scale, gt = s_gam[t];
-#pragma unroll
-          for (int i0 = 0; i0 < 32; i0 += 8) {
-            float v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int j = half * 32 + i0 + u;
-              v[u] = (j <= t) ? qt * expf(gt - s_gam[j]) * gr[i0 + u] * s_ik[j] : 0.f;
-            }
-            store8_split(sm + OFF_P, nullptr, 0, t, half * 32 + i0, v);
-          }
-        }
-      }
-      __syncthreads();
-
-      // ================= solve: T = (I + A)^-1, then T hi/lo -> operand tiles
-      {
-        float* sA = s_work;
-        float* sTf = s_work + 64 * LDA;
-        float* sM = s_work + 2 * 64 * LDA;
-        solve_unit_lower(sA, sTf, sM, tid);
-        for (int i = tid; i < 64 * 8; i += kThreads) {
-          const int t = i >> 3, k0 = (i & 7) * 8;
-          store8_split(sm + OFF_T, sm + OFF_T + 8192, 0, t, k0, sTf + t * LDA + k0);
-        }
-      }
-      __syncthreads();  // the solve work area is about to be overwritten by S0 hi/lo
-
-      // ================= S0 -> hi/lo operand tiles; tensor memory state <- Gamma_L S0
-      {
-        const float gL = expf(s_gam[L - 1]);
+        const float gL = ex2_approx(s_gam[L - 1]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int k0 = half * 64 + c * 32;
@@ -490,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       }
       operands_ready();
 
-      // ================= X = S0 K^T (hi + lo), O1 = S0_hi Q^T
+      // ================= X = S0 K^T (hi + lo), O1 = S0_hi Q^T, issued asynchronously
       if constexpr (!kEmulate) {
         if (tid == 0) {
 #pragma unroll
@@ -501,13 +486,63 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
             mma_bf16(tmem + COL_X, sw128_desc(sb + OFF_S + 32768 + off), bk, ID64, 1);
             mma_bf16(tmem + COL_O1, sw128_desc(sb + OFF_S + off), bq, ID64, ks > 0);
           }
+          mma_commit(bar_x);
         }
       } else {
         emu_mma<64, 128>(tl, COL_X, sm + OFF_S, 16384, sm + OFF_QK, 16384, false, row, half);
         emu_mma<64, 128>(tl, COL_X, sm + OFF_S + 32768, 16384, sm + OFF_QK, 16384, true, row, half);
         emu_mma<64, 128>(tl, COL_O1, sm + OFF_S, 16384, sm + OFF_QK + 8192, 16384, false, row, half);
       }
-      finish_group(bar_x);
+      await_group(bar_g);
+      if (!ok) break;
+
+      // ================= A (rows 0..63) and P (rows 64..127) from the Gram tile (X/O1 run meanwhile)
+      {
+        float gr[32];
+        tmem_ld32(tl + COL_G + half * 32, gr);
+        float* sAt = reinterpret_cast<float*>(sm + OFF_R);  // A transposed
+        if (row < 64) {
+          const int t = row;
+          const float bt = s_beta[t] * s_ik[t], gt = s_gam[t];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int j = half * 32 + i;
+            const float a = bt * ex2_approx(gt - s_gam[j]) * gr[i] * s_ik[j];
+            sAt[j * 64 + t] = (j < t) ? a : 0.f;
+          }
+        } else {
+          const int t = row - 64;
+          const float qt = s_iq[t] * p.q_scale, gt = s_gam[t];
+#pragma unroll
+          for (int i0 = 0; i0 < 32; i0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int j = half * 32 + i0 + u;
+              const float a = qt * ex2_approx(gt - s_gam[j]) * gr[i0 + u] * s_ik[j];
+              v[u] = (j <= t) ? a : 0.f;
+            }
+            store8_split(sm + OFF_P, nullptr, 0, t, half * 32 + i0, v);
+          }
+        }
+      }
+      __syncthreads();
+
+      // ================= solve: T = (I + A)^-1, then T hi/lo -> operand tiles
+      {
+        const float* sAt = reinterpret_cast<const float*>(sm + OFF_R);
+        float* sTf = reinterpret_cast<float*>(sm + OFF_R + 16384);
+        float* sM = reinterpret_cast<float*>(sm + OFF_M);
+        solve_unit_lower(sAt, sTf, sM, tid);
+        for (int i = tid; i < 64 * 8; i += kThreads) {
+          const int t = i >> 3, k0 = (i & 7) * 8;
+          const float4 v0 = *reinterpret_cast<const float4*>(sTf + tidx(t, k0));
+          const float4 v1 = *reinterpret_cast<const float4*>(sTf + tidx(t, k0 + 4));
+          const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          store8_split(sm + OFF_T, sm + OFF_T + 8192, 0, t, k0, v);
+        }
+      }
+      await_group(bar_x);  // also orders the solve's reads of the R area before R is written
       if (!ok) break;
       // the q/k tile is free: fetch the next chunk's
       if (tid == 0 && has_next) issue_qk(c0 + kChunk, kh);
@@ -607,22 +642,38 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         __syncthreads();
       }
       {
-        for (int t = warp; t < L; t += kThreads / 32) {
-          const float4 v = *reinterpret_cast<const float4*>(s_work + t * LDO + lane * 4);
-          float r4[4] = {v.x, v.y, v.z, v.w};
-          const size_t base = ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4;
-          if (gated) {
-            float ss = r4[0] * r4[0] + r4[1] * r4[1] + r4[2] * r4[2] + r4[3] * r4[3];
+        // warp w: tokens w, w + 8, ..., w + 56, all eight in flight together
+        constexpr int kTok = kChunk / (kThreads / 32);
+        float r[kTok][4], ss[kTok];
 #pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-            const float rstd = rsqrtf(ss * (1.0f / kHeadDim) + p.rms_eps);
-            const uint2 zz = *reinterpret_cast<const uint2*>(sm + OFF_Z + t * 256 + lane * 8);
+        for (int i = 0; i < kTok; ++i) {
+          const float4 v = *reinterpret_cast<const float4*>(s_work + (warp + 8 * i) * LDO + lane * 4);
+          r[i][0] = v.x; r[i][1] = v.y; r[i][2] = v.z; r[i][3] = v.w;
+          ss[i] = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+        if (gated) {
+#pragma unroll
+          for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+            for (int i = 0; i < kTok; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], m);
+#pragma unroll
+          for (int i = 0; i < kTok; ++i) {
+            const float rstd = rsqrtf(ss[i] * (1.0f / kHeadDim) + p.rms_eps);
+            const uint2 zz = *reinterpret_cast<const uint2*>(sm + OFF_Z + (warp + 8 * i) * 256 + lane * 8);
             const float zf[4] = {__uint_as_float(zz.x << 16), __uint_as_float(zz.x & 0xFFFF0000u),
                                  __uint_as_float(zz.y << 16), __uint_as_float(zz.y & 0xFFFF0000u)};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) r4[i] = r4[i] * rstd * wf[i] * sigmoidf_(zf[i]);
+            for (int e = 0; e < 4; ++e) r[i][e] = r[i][e] * rstd * wf[e] * sigmoid_fast(zf[e]);
           }
-          *reinterpret_cast<uint2*>(p.out + base) = make_uint2(pack_bf2(r4[0], r4[1]), pack_bf2(r4[2], r4[3]));
+        }
+#pragma unroll
+        for (int i = 0; i < kTok; ++i) {
+          const int t = warp + 8 * i;
+          if (t < L) {
+            const size_t base = ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4;
+            *reinterpret_cast<uint2*>(p.out + base) =
+                make_uint2(pack_bf2(r[i][0], r[i][1]), pack_bf2(r[i][2], r[i][3]));
+          }
         }
       }
       fence_proxy_async_smem();  // z reads above precede the next z tile's TMA write

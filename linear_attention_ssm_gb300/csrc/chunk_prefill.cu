@@ -20,8 +20,9 @@
 // Precision: operands that are exact in bf16 (the raw conv outputs q, k, v) are fed as they are;
 // the L2-norm factors, beta and the decay exponentials are fp32 diagonal scalings applied in the
 // epilogues.  fp32 operands on the state path (S0, the right-hand side R, the solve T, the scaled
-// E) are split into bf16 hi + lo pairs (~16-bit operands); products that only feed the output
-// (S0 q, E P^T) use the hi part alone.
+// E) are split into bf16 hi + lo pairs (~16-bit operands); the output-only product E P^T uses
+// the hi part alone.  S0 K^T and S0 Q^T share one N = 128 MMA chain (the q/k tile stacks the
+// 64 key rows over the 64 query rows).
 //
 // Launch: a persistent grid (one CTA of 256 threads per SM) pulls (sequence, V head) work items
 // from a counter in longest-sequence-first order (the order and the counter live in the caller's
@@ -51,8 +52,8 @@ constexpr uint32_t OFF_P = 163840;     //  8 KB: P, 64 token rows x 64
 constexpr uint32_t OFF_V = 172032;     // 16 KB: V, 2 K-blocks of 64 value columns x 64 token rows
 constexpr uint32_t OFF_Z = 188416;     // 16 KB: z of the chunk, [64 tokens][128] bf16 (gate input)
 constexpr uint32_t OFF_VEC = 204800;   // per-token vectors (8 x 64 floats) + norm partials (256)
-constexpr uint32_t OFF_M = OFF_VEC + (8 * 64 + 256) * 4;    // 3.75 KB: block products of the solve
-constexpr uint32_t OFF_BAR = OFF_M + 3 * 16 * 20 * 4;        // mbarriers, TMEM address, item slot
+constexpr uint32_t OFF_M = OFF_VEC + (8 * 64 + 256) * 4;    // 7.5 KB: the solve's six B_ik blocks
+constexpr uint32_t OFF_BAR = OFF_M + 6 * 16 * 20 * 4;        // mbarriers, TMEM address, item slot
 constexpr uint32_t SMEM_USED = OFF_BAR + 128;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;            // + alignment slack
 constexpr uint32_t LDO = 132;  // row stride (floats) of the output staging
@@ -61,9 +62,9 @@ static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory li
 
 // ---- tensor memory columns (fp32, lane = value row)
 constexpr uint32_t COL_S = 0;     // 128: the recurrent state
-constexpr uint32_t COL_X = 128;   //  64: S0 K^T
-constexpr uint32_t COL_E = 192;   //  64: E^T
-constexpr uint32_t COL_O1 = 256;  //  64: S0 Q^T
+constexpr uint32_t COL_X = 128;   //  64: S0 K^T   } one N = 128 accumulator: S0 [K; Q]^T
+constexpr uint32_t COL_O1 = 192;  //  64: S0 Q^T   }
+constexpr uint32_t COL_E = 256;   //  64: E^T
 constexpr uint32_t COL_O2 = 320;  //  64: E^T P^T
 constexpr uint32_t COL_G = 384;   //  64: [K; Q] K^T (Gram rows 0..63, Q K^T rows 64..127)
 constexpr uint32_t TMEM_COLS = 512;
@@ -143,13 +144,19 @@ __device__ void emu_mma(uint32_t t_lane, uint32_t col, const uint8_t* a_tile, ui
 // spread over the banks.
 __device__ __forceinline__ int tidx(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 15)) & 15) << 2) + (c & 3); }
 
-// T = (I + A)^-1 for a strictly lower triangular 64 x 64 A, by 16 x 16 blocks.  A is given
-// transposed (sAt[k * 64 + r] = A[r][k]).  The four diagonal blocks are inverted by
-// right-looking forward substitution with one column per thread held in registers; then, for
-// block distance d = 1, 2, 3, every off-diagonal block (i, j = i - d) is
-//   M  = sum_{k=j}^{i-1} A_ik T_kj,    T_ij = -T_ii M,
-// each 16 x 16 product split over two warps, a lane holding one row and four columns.
-__device__ void solve_unit_lower(const float* sAt, float* sT, float* sM, int tid) {
+// Index of block pair (i, k), i > k, among the six strictly-lower 16 x 16 blocks.
+__device__ __forceinline__ int pair_index(int i, int k) { return (i * (i - 1)) / 2 + k; }
+
+// T = (I + A)^-1 for a strictly lower triangular 64 x 64 A, both in the tidx layout, by 16 x 16
+// blocks (block row/column indices 0..3), in five barrier-separated steps:
+//   1. T_ii = (I + A_ii)^-1 for the four diagonal blocks: right-looking forward substitution,
+//      one column per thread held in registers;
+//   2. B_ik = T_ii A_ik for the six blocks below the diagonal (all independent);
+//   3-5. for block distance d = 1, 2, 3:  T_ij = - sum_{k=j}^{i-1} B_ik T_kj  (j = i - d),
+// which is block forward substitution on (I + A) T = I with the diagonal blocks pre-inverted.
+// Each 16 x 16 block product is split over two warps, a lane holding one row and four columns.
+// The strictly upper blocks of T are never written; readers treat them as zero.
+__device__ void solve_unit_lower(const float* sA, float* sT, float* sB, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   if (tid < 64) {
     const int b = tid >> 4, c = tid & 15, o = b * 16;
@@ -160,45 +167,52 @@ __device__ void solve_unit_lower(const float* sAt, float* sT, float* sM, int tid
     for (int k = 0; k < 15; ++k) {
       const float xk = x[k];
 #pragma unroll
-      for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-sAt[(o + k) * 64 + o + i], xk, x[i]);
+      for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-sA[tidx(o + i, o + k)], xk, x[i]);
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) sT[tidx(o + i, o + c)] = x[i];
   }
-  for (int idx = tid; idx < 64 * 64; idx += kThreads) {
-    const int r = idx >> 6, cc = idx & 63;
-    if ((cc >> 4) > (r >> 4)) sT[tidx(r, cc)] = 0.f;
-  }
   __syncthreads();
   const int r = (warp & 1) * 8 + (lane >> 2);  // row inside the 16 x 16 block
   const int c0 = (lane & 3) * 4;               // first of this lane's four columns
+  // step 2: twelve half-block tasks (six blocks x two row halves) over eight warps
+  for (int task = warp; task < 12; task += 8) {
+    const int pidx = task >> 1;
+    const int i = pidx < 1 ? 1 : (pidx < 3 ? 2 : 3), k = pidx - pair_index(i, 0);
+    const int rr = (task & 1) * 8 + (lane >> 2);
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float a = sT[tidx(i * 16 + rr, i * 16 + u)];  // zero above the diagonal
+      const float4 bv = *reinterpret_cast<const float4*>(sA + tidx(i * 16 + u, k * 16 + c0));
+      acc0 = fmaf(a, bv.x, acc0);
+      acc1 = fmaf(a, bv.y, acc1);
+      acc2 = fmaf(a, bv.z, acc2);
+      acc3 = fmaf(a, bv.w, acc3);
+    }
+    *reinterpret_cast<float4*>(sB + pidx * 320 + rr * 20 + c0) = make_float4(acc0, acc1, acc2, acc3);
+  }
+  __syncthreads();
+  // steps 3-5
+#pragma unroll
   for (int d = 1; d < 4; ++d) {
     const int nb = 4 - d;
-    const int bi = warp >> 1, i = d + bi, jb = i - d;
     if (warp < 2 * nb) {
-      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll 4
-      for (int k = jb * 16; k < i * 16; ++k) {
-        const float a = sAt[k * 64 + i * 16 + r];
-        const float4 bv = *reinterpret_cast<const float4*>(sT + tidx(k, jb * 16 + c0));
-        acc0 = fmaf(a, bv.x, acc0);
-        acc1 = fmaf(a, bv.y, acc1);
-        acc2 = fmaf(a, bv.z, acc2);
-        acc3 = fmaf(a, bv.w, acc3);
-      }
-      *reinterpret_cast<float4*>(sM + bi * 320 + r * 20 + c0) = make_float4(acc0, acc1, acc2, acc3);
-    }
-    __syncthreads();
-    if (warp < 2 * nb) {
+      const int i = d + (warp >> 1), jb = i - d;
       float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const float a = sT[tidx(i * 16 + r, i * 16 + u)];  // zero above the diagonal
-        const float4 bv = *reinterpret_cast<const float4*>(sM + bi * 320 + u * 20 + c0);
-        acc0 = fmaf(a, bv.x, acc0);
-        acc1 = fmaf(a, bv.y, acc1);
-        acc2 = fmaf(a, bv.z, acc2);
-        acc3 = fmaf(a, bv.w, acc3);
+      for (int kk = 0; kk < d; ++kk) {
+        const int k = jb + kk;
+        const float* Bik = sB + pair_index(i, k) * 320 + r * 20;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const float a = Bik[u];
+          const float4 bv = *reinterpret_cast<const float4*>(sT + tidx(k * 16 + u, jb * 16 + c0));
+          acc0 = fmaf(a, bv.x, acc0);
+          acc1 = fmaf(a, bv.y, acc1);
+          acc2 = fmaf(a, bv.z, acc2);
+          acc3 = fmaf(a, bv.w, acc3);
+        }
       }
       *reinterpret_cast<float4*>(sT + tidx(i * 16 + r, jb * 16 + c0)) = make_float4(-acc0, -acc1, -acc2, -acc3);
     }
@@ -475,23 +489,21 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       }
       operands_ready();
 
-      // ================= X = S0 K^T (hi + lo), O1 = S0_hi Q^T, issued asynchronously
+      // ================= [X | O1] = S0 [K; Q]^T (hi + lo, N = 128), issued asynchronously
       if constexpr (!kEmulate) {
         if (tid == 0) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            const uint64_t bk = sw128_desc(sb + OFF_QK + off), bq = sw128_desc(sb + OFF_QK + 8192 + off);
-            mma_bf16(tmem + COL_X, sw128_desc(sb + OFF_S + off), bk, ID64, ks > 0);
-            mma_bf16(tmem + COL_X, sw128_desc(sb + OFF_S + 32768 + off), bk, ID64, 1);
-            mma_bf16(tmem + COL_O1, sw128_desc(sb + OFF_S + off), bq, ID64, ks > 0);
+            const uint64_t bkq = sw128_desc(sb + OFF_QK + off);
+            mma_bf16(tmem + COL_X, sw128_desc(sb + OFF_S + off), bkq, ID128, ks > 0);
+            mma_bf16(tmem + COL_X, sw128_desc(sb + OFF_S + 32768 + off), bkq, ID128, 1);
           }
           mma_commit(bar_x);
         }
       } else {
-        emu_mma<64, 128>(tl, COL_X, sm + OFF_S, 16384, sm + OFF_QK, 16384, false, row, half);
-        emu_mma<64, 128>(tl, COL_X, sm + OFF_S + 32768, 16384, sm + OFF_QK, 16384, true, row, half);
-        emu_mma<64, 128>(tl, COL_O1, sm + OFF_S, 16384, sm + OFF_QK + 8192, 16384, false, row, half);
+        emu_mma<128, 128>(tl, COL_X, sm + OFF_S, 16384, sm + OFF_QK, 16384, false, row, half);
+        emu_mma<128, 128>(tl, COL_X, sm + OFF_S + 32768, 16384, sm + OFF_QK, 16384, true, row, half);
       }
       await_group(bar_g);
       if (!ok) break;
@@ -500,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       {
         float gr[32];
         tmem_ld32(tl + COL_G + half * 32, gr);
-        float* sAt = reinterpret_cast<float*>(sm + OFF_R);  // A transposed
+        float* sA = reinterpret_cast<float*>(sm + OFF_R);  // tidx layout
         if (row < 64) {
           const int t = row;
           const float bt = s_beta[t] * s_ik[t], gt = s_gam[t];
@@ -508,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
           for (int i = 0; i < 32; ++i) {
             const int j = half * 32 + i;
             const float a = bt * ex2_approx(gt - s_gam[j]) * gr[i] * s_ik[j];
-            sAt[j * 64 + t] = (j < t) ? a : 0.f;
+            sA[tidx(t, j)] = (j < t) ? a : 0.f;
           }
         } else {
           const int t = row - 64;
@@ -530,14 +542,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
 
       // ================= solve: T = (I + A)^-1, then T hi/lo -> operand tiles
       {
-        const float* sAt = reinterpret_cast<const float*>(sm + OFF_R);
+        const float* sA = reinterpret_cast<const float*>(sm + OFF_R);
         float* sTf = reinterpret_cast<float*>(sm + OFF_R + 16384);
-        float* sM = reinterpret_cast<float*>(sm + OFF_M);
-        solve_unit_lower(sAt, sTf, sM, tid);
+        float* sB = reinterpret_cast<float*>(sm + OFF_M);
+        solve_unit_lower(sA, sTf, sB, tid);
         for (int i = tid; i < 64 * 8; i += kThreads) {
           const int t = i >> 3, k0 = (i & 7) * 8;
-          const float4 v0 = *reinterpret_cast<const float4*>(sTf + tidx(t, k0));
-          const float4 v1 = *reinterpret_cast<const float4*>(sTf + tidx(t, k0 + 4));
+          // the strictly upper blocks of T are zero (never written by the solve)
+          const bool upper = (k0 >> 4) > (t >> 4);
+          const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 v0 = upper ? z4 : *reinterpret_cast<const float4*>(sTf + tidx(t, k0));
+          const float4 v1 = upper ? z4 : *reinterpret_cast<const float4*>(sTf + tidx(t, k0 + 4));
           const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
           store8_split(sm + OFF_T, sm + OFF_T + 8192, 0, t, k0, v);
         }

@@ -107,12 +107,24 @@ __global__ void __launch_bounds__(kThreadsX) conv1d_silu_kernel(
     for (int i = 0; i < 3; ++i) {
       const int p = t - 3 + i;
       if (p >= seq_start) h[i] = load_oct(x + (size_t)p * C + c);
-      else h[i] = st[3 - (seq_start - p)];  // p = seq_start - 3 + j  ->  slot j
+      else {  // p = seq_start - 3 + j  ->  slot j (selects keep st in registers)
+        const int j = 3 - (seq_start - p);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) h[i].v[k] = j == 0 ? st[0].v[k] : (j == 1 ? st[1].v[k] : st[2].v[k]);
+      }
     }
   };
   history_at(t0, n, s);
 
-  for (int t = t0; t < t1; ++t) {
+  // all raw inputs of the run first, so that the whole run's loads are in flight together
+  uint4 raw[kRun];
+#pragma unroll
+  for (int i = 0; i < kRun; ++i)
+    if (t0 + i < t1) raw[i] = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + i) * C + c);
+#pragma unroll
+  for (int i = 0; i < kRun; ++i) {
+    const int t = t0 + i;
+    if (t >= t1) break;
     while (t >= e) {  // next sequence (skips empty ones)
       ++n;
       if (n >= N) { raise_error(err, kErrDeviceArgument); return; }
@@ -121,21 +133,29 @@ __global__ void __launch_bounds__(kThreadsX) conv1d_silu_kernel(
       if (e < s || e > T) { raise_error(err, kErrDeviceArgument); return; }
       if (t < e) history_at(t, n, s);
     }
-    const Oct cur = load_oct(x + (size_t)t * C + c);
+    Oct cur;
+    {
+      const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        cur.v[2 * k] = __uint_as_float(w4[k] << 16);
+        cur.v[2 * k + 1] = __uint_as_float(w4[k] & 0xFFFF0000u);
+      }
+    }
     uint32_t packed[4];
 #pragma unroll
-    for (int i = 0; i < 8; i += 2) {
+    for (int q = 0; q < 8; q += 2) {
       float a[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int ch = i + u;
+        const int ch = q + u;
         float acc = wt[ch][0] * h[0].v[ch];
         acc = fmaf(wt[ch][1], h[1].v[ch], acc);
         acc = fmaf(wt[ch][2], h[2].v[ch], acc);
         acc = fmaf(wt[ch][3], cur.v[ch], acc);
-        a[u] = acc / (1.0f + expf(-acc));
+        a[u] = acc * rcp_approx(1.0f + ex2_approx(-acc * kLog2e));  // silu(acc)
       }
-      packed[i >> 1] = pack_bf2(a[0], a[1]);
+      packed[q >> 1] = pack_bf2(a[0], a[1]);
     }
     *reinterpret_cast<uint4*>(y + (size_t)t * C + c) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     h[0] = h[1];

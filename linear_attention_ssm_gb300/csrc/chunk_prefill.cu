@@ -28,8 +28,8 @@
 // from a counter in longest-sequence-first order (the order and the counter live in the caller's
 // workspace and are written by a one-CTA schedule kernel launched first).  Within an item the
 // chunks run in order; q/k and v tiles of the next chunk are fetched by TMA as soon as their
-// buffers are free, so HBM latency hides behind the current chunk.  Thread (row, half) owns
-// tensor-memory lane `row` and half of the accumulator columns in every epilogue.
+// buffers are free, so HBM latency hides behind the current chunk.  Thread (row, part) owns
+// tensor-memory lane `row` and a quarter of the accumulator columns in every epilogue.
 #include <cuda.h>
 
 #include "gdn_common.cuh"
@@ -39,7 +39,10 @@ namespace gdn {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kParts = 2;                 // warps sharing one tensor-memory lane quarter
+constexpr int kThreads = 128 * kParts;    // 8 warps
+constexpr int kW = 64 / kParts;           // columns of a 64-wide accumulator per thread
+constexpr int kWarps = kThreads / 32;
 
 // ---- shared memory map (byte offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_QK = 0;         // 32 KB: 2 K-blocks x 128 rows (k tokens 0..63, q tokens 64..127)
@@ -51,8 +54,8 @@ constexpr uint32_t OFF_T = 147456;     // 16 KB: T hi (8 KB) + T lo (8 KB); then
 constexpr uint32_t OFF_P = 163840;     //  8 KB: P, 64 token rows x 64
 constexpr uint32_t OFF_V = 172032;     // 16 KB: V, 2 K-blocks of 64 value columns x 64 token rows
 constexpr uint32_t OFF_Z = 188416;     // 16 KB: z of the chunk, [64 tokens][128] bf16 (gate input)
-constexpr uint32_t OFF_VEC = 204800;   // per-token vectors (8 x 64 floats) + norm partials (256)
-constexpr uint32_t OFF_M = OFF_VEC + (8 * 64 + 256) * 4;    // 7.5 KB: the solve's six B_ik blocks
+constexpr uint32_t OFF_VEC = 204800;   // per-token vectors (8 x 64 floats) + norm partials
+constexpr uint32_t OFF_M = OFF_VEC + (8 * 64 + 128 * kParts) * 4;  // 7.5 KB: the solve's six B_ik blocks
 constexpr uint32_t OFF_BAR = OFF_M + 6 * 16 * 20 * 4;        // mbarriers, TMEM address, item slot
 constexpr uint32_t SMEM_USED = OFF_BAR + 128;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;            // + alignment slack
@@ -101,9 +104,8 @@ __device__ __forceinline__ void store8_split(uint8_t* hi_tile, uint8_t* lo_tile,
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float a = v[2 * i], b = v[2 * i + 1];
-    const uint16_t ah = f2bf(a), bh = f2bf(b);
-    h[i] = (uint32_t)ah | ((uint32_t)bh << 16);
-    l[i] = pack_bf2(a - bf2f(ah), b - bf2f(bh));
+    h[i] = pack_bf2(a, b);
+    if (lo_tile) l[i] = pack_bf2(a - __uint_as_float(h[i] << 16), b - __uint_as_float(h[i] & 0xFFFF0000u));
   }
   const uint32_t off = sw128_offset(row, k0, kb_stride);
   *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
@@ -114,28 +116,26 @@ __device__ __forceinline__ float ld_bf(const uint8_t* base, uint32_t off) {
   return bf2f(*reinterpret_cast<const uint16_t*>(base + off));
 }
 
-// CUDA-core stand-in of one M=128 MMA group for verification: thread (row, half) computes
-// columns [half*N/2, (half+1)*N/2) of row `row` of D (+)= A * B^T from the same swizzled tiles.
+// CUDA-core stand-in of one M=128 MMA group for verification: thread (row, part) computes
+// columns [part*N/kParts, (part+1)*N/kParts) of row `row` of D (+)= A * B^T from the same
+// swizzled tiles.
 template <int N, int K>
 __device__ void emu_mma(uint32_t t_lane, uint32_t col, const uint8_t* a_tile, uint32_t a_kbs, const uint8_t* b_tile,
-                        uint32_t b_kbs, bool accumulate, int row, int half) {
-  float arow[K];
-#pragma unroll 8
-  for (int k = 0; k < K; ++k) arow[k] = ld_bf(a_tile, sw128_offset(row, k, a_kbs));
-  for (int n0 = half * (N / 2); n0 < (half + 1) * (N / 2); n0 += 32) {
-    float d[32];
-    if (accumulate) tmem_ld32(t_lane + col + n0, d);
+                        uint32_t b_kbs, bool accumulate, int row, int part) {
+  for (int n0 = part * (N / kParts); n0 < (part + 1) * (N / kParts); n0 += 16) {
+    float d[16];
+    if (accumulate) tmem_ld16(t_lane + col + n0, d);
     else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) d[i] = 0.f;
+      for (int i = 0; i < 16; ++i) d[i] = 0.f;
     }
-    for (int n = 0; n < 32; ++n) {
+    for (int n = 0; n < 16; ++n) {
       float s = 0.f;
-#pragma unroll 8
-      for (int k = 0; k < K; ++k) s = fmaf(arow[k], ld_bf(b_tile, sw128_offset(n0 + n, k, b_kbs)), s);
+      for (int k = 0; k < K; ++k)
+        s = fmaf(ld_bf(a_tile, sw128_offset(row, k, a_kbs)), ld_bf(b_tile, sw128_offset(n0 + n, k, b_kbs)), s);
       d[n] += s;
     }
-    tmem_st32(t_lane + col + n0, d);
+    tmem_st16(t_lane + col + n0, d);
   }
 }
 
@@ -175,8 +175,8 @@ __device__ void solve_unit_lower(const float* sA, float* sT, float* sB, int tid)
   __syncthreads();
   const int r = (warp & 1) * 8 + (lane >> 2);  // row inside the 16 x 16 block
   const int c0 = (lane & 3) * 4;               // first of this lane's four columns
-  // step 2: twelve half-block tasks (six blocks x two row halves) over eight warps
-  for (int task = warp; task < 12; task += 8) {
+  // step 2: twelve half-block tasks (six blocks x two row halves)
+  for (int task = warp; task < 12; task += kWarps) {
     const int pidx = task >> 1;
     const int i = pidx < 1 ? 1 : (pidx < 3 ? 2 : 3), k = pidx - pair_index(i, 0);
     const int rr = (task & 1) * 8 + (lane >> 2);
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q4 = warp & 3, half = warp >> 2;
+  const int q4 = warp & 3, part = warp >> 2;
   const int row = q4 * 32 + lane;  // tensor-memory lane = accumulator row owned by this thread
 
   const int ratio = p.Hv / p.Hk;
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   float* s_co = s_gam + 320;  // Gamma_t iq_t q_scale
   float* s_cs = s_gam + 384;  // exp(gamma_L - gamma_t) ik_t
   float* s_g = s_gam + 448;
-  float* s_part = s_gam + 512;  // 2 x 128 partial sums of squares
+  float* s_part = s_gam + 512;  // kParts x 128 partial sums of squares
   float* s_work = reinterpret_cast<float*>(sm + OFF_S);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 64);
@@ -363,12 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     pend_z = gated && seq_e > seq_s;
     if (seq_e > seq_s) load_gb(seq_s, min(kChunk, seq_e - seq_s), h);
 
-    // ---- initial state -> tensor memory (thread (row, half): 64 columns of row `row`)
+    // ---- initial state -> tensor memory (thread (row, part): 128 / kParts columns of row `row`)
     {
       const size_t row_off = (((size_t)n * p.Hv + h) * kHeadDim + row) * kHeadDim;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int c0 = half * 64 + c * 32;
+      for (int cq = 0; cq < 4 / kParts; ++cq) {
+        const int c0 = part * (128 / kParts) + cq * 32;
         float v[32];
         if (p.state_in) {
           const float4* src = reinterpret_cast<const float4*>(p.state_in + row_off + c0);
@@ -398,11 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       pend_qk = false;
       if (!ok) break;
       {
-        // partial sums of squares: rows 0..63 keys, 64..127 queries; half = K-block
-        const int r = tid & 127, kb = tid >> 7;
+        // partial sums of squares: rows 0..63 keys, 64..127 queries; each part sums 128 / kParts columns
+        const int r = tid & 127, kq = tid >> 7;
         float ss = 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int cc = 0; cc < 16 / kParts; ++cc) {
+          const int chunk = kq * (16 / kParts) + cc, kb = chunk >> 3, c = chunk & 7;
           const uint4 u = *reinterpret_cast<const uint4*>(sm + OFF_QK + kb * 16384 + r * 128 + (((c ^ (r & 7)) & 7) << 4));
           const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -412,18 +413,21 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
             ss = fmaf(b, b, ss);
           }
         }
-        s_part[kb * 128 + r] = ss;
-        // K^T: thread (key n, token half) gathers 32 tokens into 4 swizzled 16-byte chunks
+        s_part[kq * 128 + r] = ss;
+        // K^T: thread (key n, token part) gathers 64 / kParts tokens into swizzled 16-byte chunks;
+        // within a chunk of 8 tokens the source swizzle term depends on the token's low bits only
         const int nk = tid & 127, th = tid >> 7;
+        const uint8_t* kb_base = sm + OFF_QK + (nk >> 6) * 16384 + ((nk & 7) << 1);
+        const int nsw = (nk >> 3) & 7;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int tc = th * 4 + q;
+        for (int q = 0; q < 8 / kParts; ++q) {
+          const int tc = th * (8 / kParts) + q;
+          const uint8_t* src = kb_base + tc * 1024;
           uint32_t w4[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int t0 = tc * 8 + 2 * u;
-            const uint32_t a = *reinterpret_cast<const uint16_t*>(sm + OFF_QK + sw128_offset(t0, nk, 16384));
-            const uint32_t b = *reinterpret_cast<const uint16_t*>(sm + OFF_QK + sw128_offset(t0 + 1, nk, 16384));
+            const uint32_t a = *reinterpret_cast<const uint16_t*>(src + (2 * u) * 128 + ((nsw ^ (2 * u)) << 4));
+            const uint32_t b = *reinterpret_cast<const uint16_t*>(src + (2 * u + 1) * 128 + ((nsw ^ (2 * u + 1)) << 4));
             w4[u] = a | (b << 16);
           }
           *reinterpret_cast<uint4*>(sm + OFF_KT + nk * 128 + (((tc ^ (nk & 7)) & 7) << 4)) =
@@ -444,7 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       }
       __syncthreads();
       if (tid < 128) {
-        const float inv = 1.0f / sqrtf(s_part[tid] + s_part[128 + tid] + p.l2_eps);
+        float ss = 0.f;
+#pragma unroll
+        for (int q = 0; q < kParts; ++q) ss += s_part[q * 128 + tid];
+        const float inv = 1.0f / sqrtf(ss + p.l2_eps);
         if (tid < 64) s_ik[tid] = inv; else s_iq[tid - 64] = inv;
       }
       __syncthreads();
@@ -469,15 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
           mma_commit(bar_g);
         }
       } else {
-        emu_mma<64, 128>(tl, COL_G, sm + OFF_QK, 16384, sm + OFF_QK, 16384, false, row, half);
+        emu_mma<64, 128>(tl, COL_G, sm + OFF_QK, 16384, sm + OFF_QK, 16384, false, row, part);
       }
 
       // ================= S0 -> hi/lo operand tiles; tensor memory state <- Gamma_L S0 (under the Gram)
       {
         const float gL = ex2_approx(s_gam[L - 1]);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int k0 = half * 64 + c * 32;
+        for (int cq = 0; cq < 4 / kParts; ++cq) {
+          const int k0 = part * (128 / kParts) + cq * 32;
           float v[32];
           tmem_ld32(tl + COL_S + k0, v);
 #pragma unroll
@@ -502,39 +509,53 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
           mma_commit(bar_x);
         }
       } else {
-        emu_mma<128, 128>(tl, COL_X, sm + OFF_S, 16384, sm + OFF_QK, 16384, false, row, half);
-        emu_mma<128, 128>(tl, COL_X, sm + OFF_S + 32768, 16384, sm + OFF_QK, 16384, true, row, half);
+        emu_mma<128, 128>(tl, COL_X, sm + OFF_S, 16384, sm + OFF_QK, 16384, false, row, part);
+        emu_mma<128, 128>(tl, COL_X, sm + OFF_S + 32768, 16384, sm + OFF_QK, 16384, true, row, part);
       }
       await_group(bar_g);
       if (!ok) break;
 
       // ================= A (rows 0..63) and P (rows 64..127) from the Gram tile (X/O1 run meanwhile)
       {
-        float gr[32];
-        tmem_ld32(tl + COL_G + half * 32, gr);
+        float gr[kW];
+        tmem_ld_cols<kW>(tl + COL_G + part * kW, gr);
         float* sA = reinterpret_cast<float*>(sm + OFF_R);  // tidx layout
         if (row < 64) {
           const int t = row;
           const float bt = s_beta[t] * s_ik[t], gt = s_gam[t];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int j = half * 32 + i;
-            const float a = bt * ex2_approx(gt - s_gam[j]) * gr[i] * s_ik[j];
-            sA[tidx(t, j)] = (j < t) ? a : 0.f;
+          for (int i4 = 0; i4 < kW; i4 += 4) {
+            const int j0 = part * kW + i4;
+            const float4 gj = *reinterpret_cast<const float4*>(s_gam + j0);
+            const float4 kj = *reinterpret_cast<const float4*>(s_ik + j0);
+            const float gv[4] = {gj.x, gj.y, gj.z, gj.w}, kv[4] = {kj.x, kj.y, kj.z, kj.w};
+            float a[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float val = bt * ex2_approx(gt - gv[u]) * gr[i4 + u] * kv[u];
+              a[u] = (j0 + u < t) ? val : 0.f;
+            }
+            *reinterpret_cast<float4*>(sA + tidx(t, j0)) = make_float4(a[0], a[1], a[2], a[3]);
           }
         } else {
           const int t = row - 64;
           const float qt = s_iq[t] * p.q_scale, gt = s_gam[t];
 #pragma unroll
-          for (int i0 = 0; i0 < 32; i0 += 8) {
+          for (int i0 = 0; i0 < kW; i0 += 8) {
             float v[8];
+            const int j0 = part * kW + i0;
+            const float4 g0 = *reinterpret_cast<const float4*>(s_gam + j0);
+            const float4 g1 = *reinterpret_cast<const float4*>(s_gam + j0 + 4);
+            const float4 k0v = *reinterpret_cast<const float4*>(s_ik + j0);
+            const float4 k1v = *reinterpret_cast<const float4*>(s_ik + j0 + 4);
+            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const float kv[8] = {k0v.x, k0v.y, k0v.z, k0v.w, k1v.x, k1v.y, k1v.z, k1v.w};
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const int j = half * 32 + i0 + u;
-              const float a = qt * ex2_approx(gt - s_gam[j]) * gr[i0 + u] * s_ik[j];
-              v[u] = (j <= t) ? a : 0.f;
+              const float a = qt * ex2_approx(gt - gv[u]) * gr[i0 + u] * kv[u];
+              v[u] = (j0 + u <= t) ? a : 0.f;
             }
-            store8_split(sm + OFF_P, nullptr, 0, t, half * 32 + i0, v);
+            store8_split(sm + OFF_P, nullptr, 0, t, part * kW + i0, v);
           }
         }
       }
@@ -569,15 +590,25 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       pend_v = false;
       if (!ok) break;
       {
-        float x[32];
-        tmem_ld32(tl + COL_X + half * 32, x);
+        float x[kW];
+        tmem_ld_cols<kW>(tl + COL_X + part * kW, x);
+        // V[t][row] for t = part * kW + i: the swizzle term depends on i & 7 only
+        const uint8_t* vb = sm + OFF_V + (row >> 6) * 8192 + part * kW * 128 + ((row & 7) << 1);
+        const int rsw = (row >> 3) & 7;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int t = half * 32 + i;
-          x[i] = s_beta[t] * ld_bf(sm + OFF_V, sw128_offset(t, row, 8192)) - s_cx[t] * x[i];
+        for (int i4 = 0; i4 < kW; i4 += 4) {
+          const float4 bt = *reinterpret_cast<const float4*>(s_beta + part * kW + i4);
+          const float4 cx = *reinterpret_cast<const float4*>(s_cx + part * kW + i4);
+          const float btv[4] = {bt.x, bt.y, bt.z, bt.w}, cxv[4] = {cx.x, cx.y, cx.z, cx.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i4 + u;
+            const float v = bf2f(*reinterpret_cast<const uint16_t*>(vb + i * 128 + ((rsw ^ (i & 7)) << 4)));
+            x[i] = btv[u] * v - cxv[u] * x[i];
+          }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) store8_split(sm + OFF_R, sm + OFF_R + 16384, 0, row, half * 32 + 8 * q, x + 8 * q);
+        for (int q = 0; q < kW / 8; ++q) store8_split(sm + OFF_R, sm + OFF_R + 16384, 0, row, part * kW + 8 * q, x + 8 * q);
       }
       operands_ready();
       if (tid == 0 && has_next) issue_v(c0 + kChunk, h);
@@ -596,23 +627,29 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
           }
         }
       } else {
-        emu_mma<64, 64>(tl, COL_E, sm + OFF_R, 0, sm + OFF_T, 0, false, row, half);
-        emu_mma<64, 64>(tl, COL_E, sm + OFF_R, 0, sm + OFF_T + 8192, 0, true, row, half);
-        emu_mma<64, 64>(tl, COL_E, sm + OFF_R + 16384, 0, sm + OFF_T, 0, true, row, half);
+        emu_mma<64, 64>(tl, COL_E, sm + OFF_R, 0, sm + OFF_T, 0, false, row, part);
+        emu_mma<64, 64>(tl, COL_E, sm + OFF_R, 0, sm + OFF_T + 8192, 0, true, row, part);
+        emu_mma<64, 64>(tl, COL_E, sm + OFF_R + 16384, 0, sm + OFF_T, 0, true, row, part);
       }
       finish_group(bar_e);
       if (!ok) break;
 
       // ================= E~ = E diag(exp(gamma_L - gamma) ik) -> hi/lo;  E -> bf16 (output operand)
       {
-        float ev[32], es[32];
-        tmem_ld32(tl + COL_E + half * 32, ev);
+        float ev[kW], es[kW];
+        tmem_ld_cols<kW>(tl + COL_E + part * kW, ev);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) es[i] = ev[i] * s_cs[half * 32 + i];
+        for (int i4 = 0; i4 < kW; i4 += 4) {
+          const float4 cs = *reinterpret_cast<const float4*>(s_cs + part * kW + i4);
+          es[i4] = ev[i4] * cs.x;
+          es[i4 + 1] = ev[i4 + 1] * cs.y;
+          es[i4 + 2] = ev[i4 + 2] * cs.z;
+          es[i4 + 3] = ev[i4 + 3] * cs.w;
+        }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          store8_split(sm + OFF_R, sm + OFF_R + 16384, 0, row, half * 32 + 8 * q, es + 8 * q);
-          store8_split(sm + OFF_T, nullptr, 0, row, half * 32 + 8 * q, ev + 8 * q);
+        for (int q = 0; q < kW / 8; ++q) {
+          store8_split(sm + OFF_R, sm + OFF_R + 16384, 0, row, part * kW + 8 * q, es + 8 * q);
+          store8_split(sm + OFF_T, nullptr, 0, row, part * kW + 8 * q, ev + 8 * q);
         }
       }
       operands_ready();
@@ -630,9 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
           }
         }
       } else {
-        emu_mma<128, 64>(tl, COL_S, sm + OFF_R, 0, sm + OFF_KT, 0, true, row, half);
-        emu_mma<128, 64>(tl, COL_S, sm + OFF_R + 16384, 0, sm + OFF_KT, 0, true, row, half);
-        emu_mma<64, 64>(tl, COL_O2, sm + OFF_T, 0, sm + OFF_P, 0, false, row, half);
+        emu_mma<128, 64>(tl, COL_S, sm + OFF_R, 0, sm + OFF_KT, 0, true, row, part);
+        emu_mma<128, 64>(tl, COL_S, sm + OFF_R + 16384, 0, sm + OFF_KT, 0, true, row, part);
+        emu_mma<64, 64>(tl, COL_O2, sm + OFF_T, 0, sm + OFF_P, 0, false, row, part);
       }
       finish_group(bar_s);
       if (!ok) break;
@@ -640,13 +677,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       // ================= output: o = O1 diag(Gamma iq q_scale) + O2, staged token-major in the
       // (now dead) S0 area, then the sigmoid-gated RMSNorm over the value dimension
       {
-        float o1[32], o2[32];
-        tmem_ld32(tl + COL_O1 + half * 32, o1);
-        tmem_ld32(tl + COL_O2 + half * 32, o2);
+        float o1[kW], o2[kW];
+        tmem_ld_cols<kW>(tl + COL_O1 + part * kW, o1);
+        tmem_ld_cols<kW>(tl + COL_O2 + part * kW, o2);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int t = half * 32 + i;
-          s_work[t * LDO + row] = fmaf(o1[i], s_co[t], o2[i]);
+        for (int i4 = 0; i4 < kW; i4 += 4) {
+          const int t0 = part * kW + i4;
+          const float4 co = *reinterpret_cast<const float4*>(s_co + t0);
+          s_work[t0 * LDO + row] = fmaf(o1[i4], co.x, o2[i4]);
+          s_work[(t0 + 1) * LDO + row] = fmaf(o1[i4 + 1], co.y, o2[i4 + 1]);
+          s_work[(t0 + 2) * LDO + row] = fmaf(o1[i4 + 2], co.z, o2[i4 + 2]);
+          s_work[(t0 + 3) * LDO + row] = fmaf(o1[i4 + 3], co.w, o2[i4 + 3]);
         }
       }
       if (gated) {
@@ -657,12 +698,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         __syncthreads();
       }
       {
-        // warp w: tokens w, w + 8, ..., w + 56, all eight in flight together
-        constexpr int kTok = kChunk / (kThreads / 32);
+        // warp w: tokens w, w + kWarps, ..., all in flight together
+        constexpr int kTok = kChunk / kWarps;
         float r[kTok][4], ss[kTok];
 #pragma unroll
         for (int i = 0; i < kTok; ++i) {
-          const float4 v = *reinterpret_cast<const float4*>(s_work + (warp + 8 * i) * LDO + lane * 4);
+          const float4 v = *reinterpret_cast<const float4*>(s_work + (warp + kWarps * i) * LDO + lane * 4);
           r[i][0] = v.x; r[i][1] = v.y; r[i][2] = v.z; r[i][3] = v.w;
           ss[i] = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
         }
@@ -674,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
 #pragma unroll
           for (int i = 0; i < kTok; ++i) {
             const float rstd = rsqrtf(ss[i] * (1.0f / kHeadDim) + p.rms_eps);
-            const uint2 zz = *reinterpret_cast<const uint2*>(sm + OFF_Z + (warp + 8 * i) * 256 + lane * 8);
+            const uint2 zz = *reinterpret_cast<const uint2*>(sm + OFF_Z + (warp + kWarps * i) * 256 + lane * 8);
             const float zf[4] = {__uint_as_float(zz.x << 16), __uint_as_float(zz.x & 0xFFFF0000u),
                                  __uint_as_float(zz.y << 16), __uint_as_float(zz.y & 0xFFFF0000u)};
 #pragma unroll
@@ -683,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         }
 #pragma unroll
         for (int i = 0; i < kTok; ++i) {
-          const int t = warp + 8 * i;
+          const int t = warp + kWarps * i;
           if (t < L) {
             const size_t base = ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4;
             *reinterpret_cast<uint2*>(p.out + base) =
@@ -704,8 +745,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     if (p.state_out) {
       const size_t row_off = (((size_t)n * p.Hv + h) * kHeadDim + row) * kHeadDim;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int c0 = half * 64 + c * 32;
+      for (int cq = 0; cq < 4 / kParts; ++cq) {
+        const int c0 = part * (128 / kParts) + cq * 32;
         float v[32];
         tmem_ld32(tl + COL_S + c0, v);
         float4* dst = reinterpret_cast<float4*>(p.state_out + row_off + c0);

@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-steps", type=int, default=640)
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--varlen-steps", type=int, default=10)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -127,6 +128,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def slowest_rank_ms(ms, world, device):
+    """The largest of the ranks' timings (every rank calls this; world 1 needs no group)."""
+    if world == 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank, world, slowest_ms):
+    """Whole-job throughput of `world` independent replicas: all ranks' units / slowest time."""
+    return world * units_per_rank / (slowest_ms / 1000.0)
+
+
 def cpu_oracle_sample(inp, tokens_per_seq):
     """The oracle (conv -> recurrence -> gated norm, fp64, all V heads) on the first
     `tokens_per_seq` tokens of every sequence.  Returns (tokens/s, cores, description)."""
@@ -185,8 +202,8 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     import linear_attention_ssm_gb300 as gdn
     from linear_attention_ssm_gb300 import build as gdn_build
-    from linear_attention_ssm_gb300.synth import (BATCHED_LENGTHS, DECODE_BATCH, DECODE_STEPS, decode_inputs,
-                                                  prefill_inputs)
+    from linear_attention_ssm_gb300.synth import (BATCHED_LENGTHS, DECODE_BATCH, DECODE_STEPS, VARLEN_LENGTHS,
+                                                  decode_inputs, prefill_inputs)
     if not os.path.exists(gdn.binding.LIB_PATH):
         gdn_build.build()
     gdn.load_library()
@@ -199,11 +216,7 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return slowest_rank_ms(v, world, dev)
 
     hbm_peak, _, peak_kind = peaks()
     stream = torch.cuda.current_stream()
@@ -249,7 +262,7 @@ def run_ours(args, rank, world, local):
     gdn.gdn_check_device_errors()
     ms = max_over_ranks(start.elapsed_time(end))
     ms_per_step = ms / args.steps
-    value = world * T / (ms_per_step / 1000.0)
+    value = replica_throughput(T, world, ms_per_step)
     chunk_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     conv_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_conv)
     chunk_bytes = CHUNK_BYTES_PER_TOKEN * T + STATE_BYTES_PER_SEQ * N
@@ -261,8 +274,10 @@ def run_ours(args, rank, world, local):
                 "traffic": rec["bytes_per_launch"] if rec else None,
                 "algorithmic_bytes_per_launch": chunk_bytes, "avg_launch_ms": chunk_ms}
     conv_bytes = T * 10240 * 2 * 2 + N * 10240 * 3 * 2 * 2 + 10240 * 4 * 2
+    crec = traffic_record("conv1d_prefill")
     conv_roof = {"kernel": "conv1d_prefill", "bound": "hbm", "achieved": conv_bytes / (conv_ms / 1000) / 1e9,
-                 "peak": hbm_peak, "unit": "GB/s", "avg_launch_ms": conv_ms}
+                 "peak": hbm_peak, "unit": "GB/s", "avg_launch_ms": conv_ms,
+                 "algorithmic_bytes_per_launch": conv_bytes, "traffic": crec["bytes_per_launch"] if crec else None}
     conv_roof["frac"] = conv_roof["achieved"] / hbm_peak
 
     # ---------------- end to end through host buffers (pinned), same step
@@ -296,12 +311,48 @@ def run_ours(args, rank, world, local):
     e2.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(s2.elapsed_time(e2)) / args.e2e_steps
-    e2e_value = world * T / (e2e_ms / 1000.0)
+    e2e_value = replica_throughput(T, world, e2e_ms)
     del h_x, h_g, h_b, h_z
 
-    # ---------------- decode: 256 sequences, 64 pre-generated steps cycled
+    # ---------------- varlen prefill: 8 packed sequences, 32,735 tokens (same path)
     del x, qkv, z, out
     torch.cuda.empty_cache()
+    varlen = None
+    if args.varlen_steps > 0:
+        vin = prefill_inputs(VARLEN_LENGTHS, seed=3)
+        vN, vT = len(VARLEN_LENGTHS), sum(VARLEN_LENGTHS)
+        vx, vcu = vin["x"].to(dev), vin["cu_seqlens"].to(dev)
+        vg, vb, vz = vin["g"].to(dev), vin["beta"].to(dev), vin["z"].to(dev)
+        vs_in = vin["state0"].to(dev)
+        vs_out = torch.empty_like(vs_in)
+        vcs_in = vin["conv_state0"].to(dev)
+        vcs_out = torch.empty_like(vcs_in)
+        vqkv = torch.empty_like(vx)
+        vout = torch.empty((vT, 48, 128), dtype=torch.bfloat16, device=dev)
+
+        def varlen_step():
+            gdn.gdn_conv1d_prefill(vx, w, vcu, vcs_in, vcs_out, vqkv)
+            gdn.gdn_chunk_prefill(vqkv, vg, vb, vcu, vin["q_scale"], 1e-6, vs_in, vs_out, vz, nw, 1e-6, vout)
+
+        for _ in range(max(args.warmup, 1)):
+            varlen_step()
+        barrier()
+        s4, e4 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s4.record(stream)
+        for _ in range(args.varlen_steps):
+            varlen_step()
+        e4.record(stream)
+        torch.cuda.synchronize()
+        gdn.gdn_check_device_errors()
+        v_ms = max_over_ranks(s4.elapsed_time(e4)) / args.varlen_steps
+        varlen = {"workload": "varlen prefill, 8 packed sequences {1,17,63,64,65,1000,8191,22334} = 32,735 tokens",
+                  "value": world * vT / (v_ms / 1000.0), "unit": "tokens/s", "ms_per_step": v_ms,
+                  "steps": args.varlen_steps,
+                  "roofline_tokens_per_s": hbm_peak * 1e9 / (CHUNK_BYTES_PER_TOKEN + STATE_BYTES_PER_SEQ * vN / vT)}
+        del vin, vx, vqkv, vz, vout
+        torch.cuda.empty_cache()
+
+    # ---------------- decode: 256 sequences, 64 pre-generated steps cycled
     d = decode_inputs(DECODE_BATCH, DECODE_STEPS, seed=4)
     B = DECODE_BATCH
     dx, dg, db, dz = d["x"].to(dev), d["g"].to(dev), d["beta"].to(dev), d["z"].to(dev)
@@ -328,7 +379,8 @@ def run_ours(args, rank, world, local):
     decode = {"metric": "decode seq-steps/s", "value": world * B / (dec_ms / 1000), "unit": "seq-steps/s",
               "ms_per_step": dec_ms, "steps": args.decode_steps, "batch": B,
               "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak,
-                           "unit": "GB/s", "frac": dec_gbs / hbm_peak, "traffic": None,
+                           "unit": "GB/s", "frac": dec_gbs / hbm_peak,
+                           "traffic": (traffic_record("decode_step") or {}).get("bytes_per_launch"),
                            "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_ms}}
 
     cpu = None
@@ -348,7 +400,7 @@ def run_ours(args, rank, world, local):
             "roofline": roofline, "roofline_conv": conv_roof,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            "decode": decode, "cpu_baseline": cpu, "clocks": clk,
+            "decode": decode, "varlen": varlen, "cpu_baseline": cpu, "clocks": clk,
             "gpu_launches": 3 * args.steps,
             "arithmetic": "bf16 tensor-core operands (fp32 operands split into bf16 hi+lo), fp32 accumulate and state",
         }

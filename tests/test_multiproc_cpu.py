@@ -1,0 +1,51 @@
+"""The multi-rank path of bench.py (independent replicas, slowest-rank timing) with two gloo
+ranks on the CPU."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local_ms = [2.0, 3.5][rank]          # rank 1 is the slow one
+        slow = bench.slowest_rank_ms(local_ms, world, "cpu")
+        results[rank] = (slow, bench.replica_throughput(1000, world, slow))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_rank():
+    ctx = mp.get_context("spawn")
+    manager = ctx.Manager()
+    results = manager.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, results)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert results[0] == results[1]
+    slow, value = results[0]
+    assert slow == 3.5
+    assert value == pytest.approx(2 * 1000 / 3.5e-3)
+
+
+def test_single_rank_needs_no_group():
+    assert bench.slowest_rank_ms(1.25, 1, "cpu") == 1.25
+    assert bench.replica_throughput(16384, 1, 2.0) == pytest.approx(16384 / 2e-3)

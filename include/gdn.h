@@ -112,11 +112,24 @@ GDN_API gdn_status gdn_conv1d_prefill(const gdn_geometry* geo, const gdn_bf16* x
                                       gdn_bf16* y, void* stream);
 
 /*
- * Bytes of device workspace gdn_chunk_prefill needs for these sizes (0 is possible).  The
- * workspace holds the per-call sequence schedule; its contents need no initialisation.
+ * Bytes of device workspace for the fast path of gdn_chunk_prefill at these sizes (0 when
+ * num_seqs == 0).  With at least this much, the call runs as two kernels: one that forms, for
+ * every 64-token chunk at once, the quantities that do not depend on the recurrent state (the
+ * intra-chunk decay factors, the solve (I + A)^-1 and the masked query-key product, about 25 KB
+ * per chunk and V head), and one that carries the state through the chunks.  The workspace
+ * contents need no initialisation and are dead when the call's kernels finish.
  */
 GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_geometry* geo, int32_t num_seqs,
                                                 int32_t total_tokens);
+
+/*
+ * Smallest workspace gdn_chunk_prefill accepts (the per-call sequence schedule: 256 bytes plus
+ * 4 bytes per sequence, rounded up to 256).  With less than gdn_chunk_prefill_workspace_size()
+ * but at least this, the call runs one fused kernel that forms the state-independent quantities
+ * chunk by chunk on the state chain itself: same results within the stated tolerances, slower.
+ */
+GDN_API size_t gdn_chunk_prefill_min_workspace_size(const gdn_geometry* geo, int32_t num_seqs,
+                                                    int32_t total_tokens);
 
 /*
  * Chunk-wise gated delta rule over packed variable-length sequences (prefill), optionally
@@ -136,7 +149,8 @@ GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_geometry* geo, int32_t
  *              and norm_w [Dv] bf16, and `out` receives the gated RMSNorm of o:
  *              o * (mean_d o^2 + rms_eps)^(-1/2) * norm_w * sigmoid(z), computed from the fp32 o
  *   out        [total_tokens, Hv, Dv] bf16
- *   workspace  device memory of at least gdn_chunk_prefill_workspace_size() bytes (NULL if 0)
+ *   workspace  256-byte aligned device memory of at least gdn_chunk_prefill_min_workspace_size()
+ *              bytes (NULL if 0); gdn_chunk_prefill_workspace_size() bytes select the fast path
  */
 GDN_API gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g,
                                      const float* beta, const int32_t* cu_seqlens,
@@ -198,7 +212,8 @@ GDN_API gdn_status gdn_decode_step(const gdn_geometry* geo, const gdn_bf16* x,
  * the array and it keeps the last call's contents: each call rewrites the whole schedule and
  * zeroes its work counter before the main kernel reads them, but two calls whose kernels overlap
  * on the GPU (for example on two unordered streams) race on the array and give wrong results.
- * There is no counterpart of this entry point on the pages.
+ * The scratch holds the minimum workspace only, so the call runs gdn_chunk_prefill's one-kernel
+ * path.  There is no counterpart of this entry point on the pages.
  */
 GDN_API gdn_status gdn_chunk_prefill_noalloc(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g,
                                              const float* beta, const int32_t* cu_seqlens, int32_t num_seqs,

@@ -1,11 +1,14 @@
 /*
  * gdn_debug.h -- verification hooks of libgdn.so (not needed on the hot path).
  *
- * The chunk-wise prefill has two builds of the same data flow: mode 0 issues every contraction
- * on the tcgen05 tensor cores (the default and the product path), mode 1 replaces each MMA
- * group by a CUDA-core loop that reads the same swizzled shared-memory operand tiles and writes
- * the same tensor-memory accumulators.  Comparing the two isolates a fault to either the
- * tensor-core descriptors or the surrounding data flow.  There is no counterpart on the pages.
+ * The chunk-wise prefill has two designs: the split path (a prep kernel for the state-independent
+ * quantities of all chunks, then the state kernel) and the fused one-kernel path, which has two
+ * builds of one data flow.  Mode 0 (the default and the product path) runs the split path when
+ * the workspace holds it and the fused tensor-core build otherwise; mode 1 runs the fused build
+ * with each MMA group replaced by a CUDA-core loop that reads the same swizzled shared-memory
+ * operand tiles and writes the same tensor-memory accumulators; mode 2 runs the fused
+ * tensor-core build whatever the workspace.  Comparing them isolates a fault to the tensor-core
+ * descriptors, the fused data flow or the split data flow.  There is no counterpart on the pages.
  */
 #ifndef GDN_DEBUG_H_
 #define GDN_DEBUG_H_
@@ -17,10 +20,11 @@ extern "C" {
 #endif
 
 /* Select the chunk-prefill build used by later gdn_chunk_prefill calls in this process:
- * 0 = tensor cores (default), 1 = CUDA-core emulation of the MMAs.  Not thread-safe. */
+ * 0 = split path when the workspace allows, else fused (default); 1 = fused with CUDA-core
+ * emulation of the MMAs; 2 = fused on the tensor cores.  Not thread-safe. */
 GDN_API gdn_status gdn_debug_set_chunk_mode(int mode);
 
-/* The mode last selected (0 or 1). */
+/* The mode last selected (0, 1 or 2). */
 GDN_API int gdn_debug_get_chunk_mode(void);
 
 /* One tensor-core tile, D = A * B^T: A [128][64] and B [n_cols][64] bf16 row-major (device),

@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     GdnError,
     gdn_check_device_errors,
     gdn_chunk_prefill,
+    gdn_chunk_prefill_min_workspace_size,
     gdn_chunk_prefill_workspace_size,
     gdn_conv1d_prefill,
     gdn_debug_get_chunk_mode,

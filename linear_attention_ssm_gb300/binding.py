@@ -54,6 +54,7 @@ def load_library():
             "gdn_version": ([], ctypes.c_char_p),
             "gdn_conv1d_prefill": ([G, P, P, P, I, I, P, P, P, P], ctypes.c_int),
             "gdn_chunk_prefill_workspace_size": ([G, I, I], S),
+            "gdn_chunk_prefill_min_workspace_size": ([G, I, I], S),
             "gdn_chunk_prefill": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P, S, P], ctypes.c_int),
             "gdn_chunk_prefill_noalloc": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
             "gdn_gated_rmsnorm": ([G, P, P, P, F, P, I, P], ctypes.c_int),
@@ -136,6 +137,11 @@ def gdn_conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in=None, conv_state_out
 def gdn_chunk_prefill_workspace_size(num_seqs: int, total_tokens: int,
                                      geometry: Geometry = QWEN_GDN) -> int:
     return int(load_library().gdn_chunk_prefill_workspace_size(_geo(geometry), num_seqs, total_tokens))
+
+
+def gdn_chunk_prefill_min_workspace_size(num_seqs: int, total_tokens: int,
+                                         geometry: Geometry = QWEN_GDN) -> int:
+    return int(load_library().gdn_chunk_prefill_min_workspace_size(_geo(geometry), num_seqs, total_tokens))
 
 
 def gdn_chunk_prefill(qkv, g, beta, cu_seqlens, q_scale, l2_eps=1e-6, state_in=None, state_out=None,

@@ -32,17 +32,13 @@
 // tensor-memory lane `row` and a quarter of the accumulator columns in every epilogue.
 #include <cuda.h>
 
+#include "chunk_common.cuh"
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 
 namespace gdn {
 
 namespace {
-
-constexpr int kParts = 2;                 // warps sharing one tensor-memory lane quarter
-constexpr int kThreads = 128 * kParts;    // 8 warps
-constexpr int kW = 64 / kParts;           // columns of a 64-wide accumulator per thread
-constexpr int kWarps = kThreads / 32;
 
 // ---- shared memory map (byte offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_QK = 0;         // 32 KB: 2 K-blocks x 128 rows (k tokens 0..63, q tokens 64..127)
@@ -72,12 +68,6 @@ constexpr uint32_t COL_O2 = 320;  //  64: E^T P^T
 constexpr uint32_t COL_G = 384;   //  64: [K; Q] K^T (Gram rows 0..63, Q K^T rows 64..127)
 constexpr uint32_t TMEM_COLS = 512;
 
-constexpr uint32_t kWaitLimit = 1u << 20;  // polls of one mbarrier before giving up
-constexpr int kScheduleSortMax = 4096;     // longest-first ordering up to this many sequences
-constexpr uint32_t kBytesQK = 4 * 64 * 128;  // four 64 x 64 bf16 boxes
-constexpr uint32_t kBytesV = 2 * 64 * 128;
-constexpr uint32_t kBytesZ = 64 * 256;
-
 struct ChunkParams {
   CUtensorMap tmap;    // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle
   CUtensorMap tmap_z;  // z [T][Hv * 128] bf16, box 128 x 64, no swizzle (valid when z != NULL)
@@ -95,130 +85,6 @@ struct ChunkParams {
   int N, T, Hk, Hv;
   float q_scale, l2_eps, rms_eps;
 };
-
-// Writes 8 consecutive fp32 values (columns k0..k0+7 of `row`, k0 % 8 == 0) as a bf16 hi (and
-// optionally lo) pair into K-major 128-byte-swizzled tiles.
-__device__ __forceinline__ void store8_split(uint8_t* hi_tile, uint8_t* lo_tile, uint32_t kb_stride, int row, int k0,
-                                             const float* v) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float a = v[2 * i], b = v[2 * i + 1];
-    h[i] = pack_bf2(a, b);
-    if (lo_tile) l[i] = pack_bf2(a - __uint_as_float(h[i] << 16), b - __uint_as_float(h[i] & 0xFFFF0000u));
-  }
-  const uint32_t off = sw128_offset(row, k0, kb_stride);
-  *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
-  if (lo_tile) *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
-__device__ __forceinline__ float ld_bf(const uint8_t* base, uint32_t off) {
-  return bf2f(*reinterpret_cast<const uint16_t*>(base + off));
-}
-
-// CUDA-core stand-in of one M=128 MMA group for verification: thread (row, part) computes
-// columns [part*N/kParts, (part+1)*N/kParts) of row `row` of D (+)= A * B^T from the same
-// swizzled tiles.
-template <int N, int K>
-__device__ void emu_mma(uint32_t t_lane, uint32_t col, const uint8_t* a_tile, uint32_t a_kbs, const uint8_t* b_tile,
-                        uint32_t b_kbs, bool accumulate, int row, int part) {
-  for (int n0 = part * (N / kParts); n0 < (part + 1) * (N / kParts); n0 += 16) {
-    float d[16];
-    if (accumulate) tmem_ld16(t_lane + col + n0, d);
-    else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) d[i] = 0.f;
-    }
-    for (int n = 0; n < 16; ++n) {
-      float s = 0.f;
-      for (int k = 0; k < K; ++k)
-        s = fmaf(ld_bf(a_tile, sw128_offset(row, k, a_kbs)), ld_bf(b_tile, sw128_offset(n0 + n, k, b_kbs)), s);
-      d[n] += s;
-    }
-    tmem_st16(t_lane + col + n0, d);
-  }
-}
-
-// Element (r, c) of the 64 x 64 fp32 inverse T: rows of 64 floats whose 16-byte groups are
-// XOR-permuted by the row, so float4 reads of a row segment and float4 writes of a block row
-// spread over the banks.
-__device__ __forceinline__ int tidx(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 15)) & 15) << 2) + (c & 3); }
-
-// Index of block pair (i, k), i > k, among the six strictly-lower 16 x 16 blocks.
-__device__ __forceinline__ int pair_index(int i, int k) { return (i * (i - 1)) / 2 + k; }
-
-// T = (I + A)^-1 for a strictly lower triangular 64 x 64 A, both in the tidx layout, by 16 x 16
-// blocks (block row/column indices 0..3), in five barrier-separated steps:
-//   1. T_ii = (I + A_ii)^-1 for the four diagonal blocks: right-looking forward substitution,
-//      one column per thread held in registers;
-//   2. B_ik = T_ii A_ik for the six blocks below the diagonal (all independent);
-//   3-5. for block distance d = 1, 2, 3:  T_ij = - sum_{k=j}^{i-1} B_ik T_kj  (j = i - d),
-// which is block forward substitution on (I + A) T = I with the diagonal blocks pre-inverted.
-// Each 16 x 16 block product is split over two warps, a lane holding one row and four columns.
-// The strictly upper blocks of T are never written; readers treat them as zero.
-__device__ void solve_unit_lower(const float* sA, float* sT, float* sB, int tid) {
-  const int warp = tid >> 5, lane = tid & 31;
-  if (tid < 64) {
-    const int b = tid >> 4, c = tid & 15, o = b * 16;
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
-#pragma unroll
-    for (int k = 0; k < 15; ++k) {
-      const float xk = x[k];
-#pragma unroll
-      for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-sA[tidx(o + i, o + k)], xk, x[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) sT[tidx(o + i, o + c)] = x[i];
-  }
-  __syncthreads();
-  const int r = (warp & 1) * 8 + (lane >> 2);  // row inside the 16 x 16 block
-  const int c0 = (lane & 3) * 4;               // first of this lane's four columns
-  // step 2: twelve half-block tasks (six blocks x two row halves)
-  for (int task = warp; task < 12; task += kWarps) {
-    const int pidx = task >> 1;
-    const int i = pidx < 1 ? 1 : (pidx < 3 ? 2 : 3), k = pidx - pair_index(i, 0);
-    const int rr = (task & 1) * 8 + (lane >> 2);
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const float a = sT[tidx(i * 16 + rr, i * 16 + u)];  // zero above the diagonal
-      const float4 bv = *reinterpret_cast<const float4*>(sA + tidx(i * 16 + u, k * 16 + c0));
-      acc0 = fmaf(a, bv.x, acc0);
-      acc1 = fmaf(a, bv.y, acc1);
-      acc2 = fmaf(a, bv.z, acc2);
-      acc3 = fmaf(a, bv.w, acc3);
-    }
-    *reinterpret_cast<float4*>(sB + pidx * 320 + rr * 20 + c0) = make_float4(acc0, acc1, acc2, acc3);
-  }
-  __syncthreads();
-  // steps 3-5
-#pragma unroll
-  for (int d = 1; d < 4; ++d) {
-    const int nb = 4 - d;
-    if (warp < 2 * nb) {
-      const int i = d + (warp >> 1), jb = i - d;
-      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < d; ++kk) {
-        const int k = jb + kk;
-        const float* Bik = sB + pair_index(i, k) * 320 + r * 20;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float a = Bik[u];
-          const float4 bv = *reinterpret_cast<const float4*>(sT + tidx(k * 16 + u, jb * 16 + c0));
-          acc0 = fmaf(a, bv.x, acc0);
-          acc1 = fmaf(a, bv.y, acc1);
-          acc2 = fmaf(a, bv.z, acc2);
-          acc3 = fmaf(a, bv.w, acc3);
-        }
-      }
-      *reinterpret_cast<float4*>(sT + tidx(i * 16 + r, jb * 16 + c0)) = make_float4(-acc0, -acc1, -acc2, -acc3);
-    }
-    __syncthreads();
-  }
-}
 
 template <bool kEmulate>
 __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid_constant__ ChunkParams p) {
@@ -771,20 +637,54 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   }
 }
 
-// One CTA: longest-first order of the sequences (ties by index) and a zeroed work counter.
-// Sequences with inconsistent cu_seqlens get length 0 here; the main kernel reports them.
+// One CTA: longest-first order of the sequences (ties by index), a zeroed work counter and,
+// when `chunk_off` is given, the exclusive prefix sum over sequences of their 64-token chunk
+// counts (chunk_off[N] = total chunks).  Sequences with inconsistent cu_seqlens count as empty
+// here; the main kernels report them.
 __global__ void __launch_bounds__(1024) chunk_schedule_kernel(const int32_t* cu, int N, int32_t* order,
-                                                              unsigned* counter) {
+                                                              unsigned* counter, int32_t* chunk_off) {
   extern __shared__ int32_t s_len[];
-  if (threadIdx.x == 0) *counter = 0u;
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) *counter = 0u;
+  if (chunk_off) {
+    // per-thread contiguous range, then a block-wide exclusive scan of the range totals
+    const int per = (N + 1023) / 1024, lo = min(N, tid * per), hi = min(N, lo + per);
+    int local = 0;
+    for (int i = lo; i < hi; ++i) local += (max(0, __ldg(cu + i + 1) - __ldg(cu + i)) + kChunk - 1) / kChunk;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = s_warp[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += v;
+      }
+      s_warp[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    int run = incl - local + (warp > 0 ? s_warp[warp - 1] : 0);
+    for (int i = lo; i < hi; ++i) {
+      chunk_off[i] = run;
+      run += (max(0, __ldg(cu + i + 1) - __ldg(cu + i)) + kChunk - 1) / kChunk;
+    }
+    if (tid == 1023) chunk_off[N] = s_warp[31];
+  }
   const bool sorted = N <= kScheduleSortMax;
-  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+  for (int i = tid; i < N; i += blockDim.x) {
     if (sorted) s_len[i] = max(0, __ldg(cu + i + 1) - __ldg(cu + i));
     else order[i] = i;
   }
   if (!sorted) return;
   __syncthreads();
-  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+  for (int i = tid; i < N; i += blockDim.x) {
     const int li = s_len[i];
     int rank = 0;
     for (int j = 0; j < N; ++j) {
@@ -822,13 +722,9 @@ cudaError_t launch_impl(const LaunchEnv& env, const ChunkParams& p) {
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  static int sm_count[64] = {0};
-  int sms = dev < 64 ? sm_count[dev] : 0;
-  if (sms == 0) {
-    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) sm_count[dev] = sms;
-  }
+  int sms = 0;
+  cudaError_t e = device_sm_count(&sms);
+  if (e != cudaSuccess) return e;
   const long items = (long)p.N * p.Hv;
   const int grid = (int)(items < sms ? items : sms);
   chunk_prefill_kernel<kEmulate><<<grid, kThreads, SMEM_BYTES, env.stream>>>(p);
@@ -837,6 +733,52 @@ cudaError_t launch_impl(const LaunchEnv& env, const ChunkParams& p) {
 
 }  // namespace
 
+cudaError_t device_sm_count(int* sms) {
+  static int sm_count[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && sm_count[dev] > 0) {
+    *sms = sm_count[dev];
+    return cudaSuccess;
+  }
+  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && dev < 64) sm_count[dev] = *sms;
+  return e;
+}
+
+cudaError_t encode_chunk_tensor_maps(CUtensorMap* qkv_map, CUtensorMap* z_map, const uint16_t* qkv,
+                                     const uint16_t* z, int T, int Hk, int Hv) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const int C = 2 * Hk * kHeadDim + Hv * kHeadDim;
+  const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
+  const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(qkv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(qkv), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (z && z_map) {
+    const cuuint64_t zdims[2] = {(cuuint64_t)Hv * kHeadDim, (cuuint64_t)T};
+    const cuuint64_t zstrides[1] = {(cuuint64_t)Hv * kHeadDim * 2};
+    const cuuint32_t zbox[2] = {128, 64};
+    const CUresult rz = enc(z_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(z), zdims, zstrides, zbox,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rz != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_chunk_schedule(cudaStream_t stream, const int32_t* cu, int N, int32_t* order, unsigned* counter,
+                                  int32_t* chunk_off) {
+  const size_t sched_smem = N <= kScheduleSortMax ? (size_t)N * sizeof(int32_t) : 0;
+  chunk_schedule_kernel<<<1, 1024, sched_smem, stream>>>(cu, N, order, counter, chunk_off);
+  return cudaGetLastError();
+}
+
 size_t chunk_prefill_workspace_bytes(int N) {
   return 256 + (((size_t)(N > 0 ? N : 0) * sizeof(int32_t) + 255) / 256) * 256;
 }
@@ -844,31 +786,17 @@ size_t chunk_prefill_workspace_bytes(int N) {
 cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t* qkv, const float* g,
                                  const float* beta, const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale,
                                  float l2_eps, const float* state_in, float* state_out, const uint16_t* z,
-                                 const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace) {
+                                 const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace,
+                                 size_t workspace_bytes) {
   if (N <= 0) return cudaSuccess;
+  if (mode == 0 && workspace_bytes >= split_workspace_bytes(N, T, Hk, Hv))
+    return launch_chunk_prefill_split(env, qkv, g, beta, cu, N, T, Hk, Hv, q_scale, l2_eps, state_in, state_out, z,
+                                      norm_w, rms_eps, out, workspace);
   ChunkParams p;
   memset(&p, 0, sizeof p);
-  const int C = 2 * Hk * kHeadDim + Hv * kHeadDim;
   if (T > 0) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
-    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
-    const cuuint32_t box[2] = {64, 64};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(&p.tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(qkv), dims, strides, box,
-                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (z) {
-      const cuuint64_t zdims[2] = {(cuuint64_t)Hv * kHeadDim, (cuuint64_t)T};
-      const cuuint64_t zstrides[1] = {(cuuint64_t)Hv * kHeadDim * 2};
-      const cuuint32_t zbox[2] = {128, 64};
-      const CUresult rz = enc(&p.tmap_z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(z), zdims,
-                              zstrides, zbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-      if (rz != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
+    cudaError_t e = encode_chunk_tensor_maps(&p.tmap, &p.tmap_z, qkv, z, T, Hk, Hv);
+    if (e != cudaSuccess) return e;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.counter = reinterpret_cast<unsigned*>(ws);
@@ -876,9 +804,7 @@ cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t*
   p.g = g; p.beta = beta; p.cu = cu; p.state_in = state_in; p.state_out = state_out;
   p.z = z; p.norm_w = norm_w; p.out = out; p.err = env.err;
   p.N = N; p.T = T; p.Hk = Hk; p.Hv = Hv; p.q_scale = q_scale; p.l2_eps = l2_eps; p.rms_eps = rms_eps;
-  const size_t sched_smem = N <= kScheduleSortMax ? (size_t)N * sizeof(int32_t) : 0;
-  chunk_schedule_kernel<<<1, 1024, sched_smem, env.stream>>>(cu, N, reinterpret_cast<int32_t*>(ws + 256), p.counter);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_chunk_schedule(env.stream, cu, N, reinterpret_cast<int32_t*>(ws + 256), p.counter, nullptr);
   if (e != cudaSuccess) return e;
   return mode == 1 ? launch_impl<true>(env, p) : launch_impl<false>(env, p);
 }

@@ -1,0 +1,767 @@
+// chunk_split.cu -- chunk-wise (WY) gated delta rule prefill as two kernels: a parallel prep
+// kernel for everything that does not depend on the recurrent state, and a persistent state
+// kernel that carries the state through the chunks of each (sequence, V head).
+//
+// The method: pegainfer PR #1152 "Reference golden for the GDN sublayer", Consumer / Shipped-line
+// diff (prepare, cumsum, A, solve are per chunk; recompute, state, output follow the state
+// chain) and Code review (f32 recurrent state carried across chunks).  The algebra is the one of
+// the fused kernel (chunk_prefill.cu): for one chunk of L <= 64 tokens with start state S0,
+//   A[t,j] = beta_t exp(gamma_t - gamma_j) k^_t.k^_j (j < t),  T = (I + A)^-1,
+//   P[t,j] = q_scale iq_t exp(gamma_t - gamma_j) q_t.k^_j (j <= t),
+//   E      = T (diag(beta) V - diag(beta Gamma) K^ S0^T),
+//   O      = diag(Gamma iq q_scale) Q S0^T + P E,     S_L = Gamma_L S0 + E^T diag(exp(gamma_L - gamma)) K^.
+// A, T, P and the per-token factors depend on q, k, g and beta only, so the prep kernel forms
+// them for every chunk at once (one CTA per (chunk, K head): the Gram [K; Q] K^T of the K head
+// on the tensor cores, then per V head of the group the scalings, the blocked solve and the
+// bf16 operand images) and writes them to a per-(chunk, V head) record in the workspace.  The
+// state kernel then runs only the state-dependent chain per chunk:
+//   S0 -> bf16 hi/lo (two key halves)  ->  [X | O1] = S0 [K; Q]^T
+//   R = diag(beta) V - diag(c_x) X^T   ->  E^T = R T^T
+//   E~ = E diag(c_s)                   ->  S = Gamma_L S0 + E~^T K  (K read MN-major from the q/k tile),
+//                                          O2 = E P^T
+//   o = O1 diag(c_o) + O2  ->  sigmoid-gated RMSNorm  ->  out
+// with the records fetched by 1D bulk copies and q/k, v by TMA.  The state kernel uses 256 of
+// the 512 tensor-memory columns and ~108 KB of shared memory, so two CTAs share an SM and one
+// CTA's waits hide behind the other's work.
+#include <cuda.h>
+
+#include "chunk_common.cuh"
+#include "gdn_common.cuh"
+#include "gdn_kernels.h"
+
+namespace gdn {
+
+namespace {
+
+// ---- per-(chunk, V head) record in the workspace (bytes)
+constexpr uint32_t REC_T = 0;          // T hi (8 KB) + T lo (8 KB): 64 x 64 bf16, K-major 128-byte swizzle
+constexpr uint32_t REC_P = 16384;      // P (8 KB), same layout
+constexpr uint32_t REC_VEC = 24576;    // 5 x 64 fp32: beta, c_x, c_s, c_o, misc (misc[0] = Gamma_L)
+constexpr uint32_t kRecTP = 24576;     // T and P: one bulk copy
+constexpr uint32_t kRecVec = 5 * 64 * 4;
+constexpr uint32_t REC_BYTES = REC_VEC + kRecVec;  // 25,856
+static_assert(REC_BYTES % 128 == 0, "records must stay 16-byte aligned");
+constexpr int V_BETA = 0, V_CX = 64, V_CS = 128, V_CO = 192, V_MISC = 256;  // float offsets in the vector block
+
+// ---- prep kernel shared memory
+constexpr uint32_t PR_QK = 0;                 // 32 KB [K; Q] tile (TMA)
+constexpr uint32_t PR_A = 32768;              // 16 KB A, fp32 solve layout
+constexpr uint32_t PR_T = 49152;              // 16 KB T, fp32 solve layout
+constexpr uint32_t PR_B = 65536;              // 7.5 KB the solve's six B_ik blocks
+constexpr uint32_t PR_VEC = PR_B + 6 * 16 * 20 * 4;  // gamma, beta, ik, iq (64 each), partial sums (kParts x 128)
+constexpr uint32_t PR_BAR = PR_VEC + (4 * 64 + kParts * 128) * 4;
+constexpr uint32_t PR_USED = PR_BAR + 64;
+constexpr uint32_t PR_BYTES = PR_USED + 1024;
+
+// ---- state kernel shared memory
+constexpr uint32_t SS_QK = 0;         // 32 KB [K; Q] tile (TMA)
+constexpr uint32_t SS_W = 32768;      // 32 KB: S0 key-half hi/lo, then R hi/lo, then E~ hi/lo, then output staging
+constexpr uint32_t SS_T = 65536;      // 16 KB T hi/lo (record), then E bf16
+constexpr uint32_t SS_P = 81920;      //  8 KB P (record; follows T so one bulk copy fills both)
+constexpr uint32_t SS_V = 90112;      // 16 KB V (TMA)
+constexpr uint32_t SS_VEC = 106496;   // 2 x per-token vector block (double buffered)
+constexpr uint32_t SS_BAR = SS_VEC + 2 * kRecVec;
+constexpr uint32_t SS_USED = SS_BAR + 128;
+constexpr uint32_t SS_BYTES = SS_USED + 1024;
+static_assert(2 * (SS_BYTES + 1024) <= 233472, "two state CTAs must share an SM");
+static_assert(SS_P == SS_T + 16384, "T and P must be contiguous");
+
+// ---- state kernel tensor memory columns
+constexpr uint32_t SC_S = 0;      // 128: the recurrent state
+constexpr uint32_t SC_X = 128;    //  64: S0 K^T, then E^T, then E P^T
+constexpr uint32_t SC_O1 = 192;   //  64: S0 Q^T
+constexpr uint32_t SC_COLS = 256;
+
+struct PrepParams {
+  CUtensorMap tmap;  // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle
+  const float* g;
+  const float* beta;
+  const int32_t* cu;
+  const int32_t* chunk_off;
+  uint8_t* rec;
+  unsigned* err;
+  int N, T, Hk, Hv;
+  float q_scale, l2_eps;
+};
+
+struct StateParams {
+  CUtensorMap tmap;
+  const int32_t* cu;
+  const int32_t* order;
+  unsigned* counter;
+  const int32_t* chunk_off;
+  const uint8_t* rec;
+  const float* state_in;
+  float* state_out;
+  const uint16_t* z;
+  const uint16_t* norm_w;
+  uint16_t* out;
+  unsigned* err;
+  int N, T, Hk, Hv, nc_max;
+  float rms_eps;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
+}
+
+// q and k tiles of K head kh for the chunk starting at token c0: K rows 0..63, Q rows 64..127 of
+// each 64-feature block (blocks 16 KB apart)
+__device__ __forceinline__ void issue_qk_tiles(uint32_t dst, const CUtensorMap* tmap, int Hk, int c0, int kh,
+                                               uint32_t bar) {
+  mbar_arrive_expect_tx(bar, kBytesQK);
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb) {
+    tma_load_2d(dst + kb * 16384, tmap, Hk * kHeadDim + kh * kHeadDim + kb * 64, c0, bar);
+    tma_load_2d(dst + kb * 16384 + 8192, tmap, kh * kHeadDim + kb * 64, c0, bar);
+  }
+}
+
+// One CTA per (chunk, K head); grid (chunks bound, Hk).  Thread (row, part) owns Gram row `row`
+// (rows 0..63: key t, the A side; rows 64..127: query t, the P side) and kW of its columns.
+__global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_constant__ PrepParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const uint32_t sb = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, part = warp >> 2;
+  const int row = q4 * 32 + lane;
+  const int gc = blockIdx.x, kh = blockIdx.y;
+  const int ratio = p.Hv / p.Hk;
+
+  if (gc >= __ldg(p.chunk_off + p.N)) return;  // beyond the last chunk (uniform over the CTA)
+  // the sequence of this chunk: the last n with chunk_off[n] <= gc (never an empty one)
+  int lo = 0, hi = p.N - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.chunk_off + mid) <= gc) lo = mid; else hi = mid - 1;
+  }
+  const int n = lo;
+  const int seq_s = __ldg(p.cu + n), seq_e = __ldg(p.cu + n + 1);
+  const int c0 = seq_s + (gc - __ldg(p.chunk_off + n)) * kChunk;
+  if (seq_s < 0 || seq_e < seq_s || seq_e > p.T || c0 >= seq_e) {
+    if (tid == 0) raise_error(p.err, kErrDeviceArgument);
+    return;
+  }
+  const int L = min(kChunk, seq_e - c0);
+
+  float* s_gam = reinterpret_cast<float*>(sm + PR_VEC);  // cumsum of g (log2 units) of the current V head
+  float* s_beta = s_gam + 64;
+  float* s_ik = s_gam + 128;
+  float* s_iq = s_gam + 192;
+  float* s_part = s_gam + 256;
+  float* sA = reinterpret_cast<float*>(sm + PR_A);
+  float* sT = reinterpret_cast<float*>(sm + PR_T);
+  float* sB = reinterpret_cast<float*>(sm + PR_B);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PR_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PR_BAR + 32);
+  const uint32_t bar_qk = smem_u32(&bars[0]), bar_g = smem_u32(&bars[1]);
+
+  if (tid == 0) {
+    mbar_init(bar_qk, 1);
+    mbar_init(bar_g, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 64);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+  if (tid == 0) issue_qk_tiles(sb + PR_QK, &p.tmap, p.Hk, c0, kh, bar_qk);
+
+  // g, beta of the group's first V head (threads < 64; zero beyond the sequence end)
+  float g_next = 0.f, b_next = 0.f;
+  auto load_gb = [&](int h) {
+    g_next = 0.f;
+    b_next = 0.f;
+    if (tid < L) {
+      g_next = __ldg(p.g + (size_t)(c0 + tid) * p.Hv + h);
+      b_next = __ldg(p.beta + (size_t)(c0 + tid) * p.Hv + h);
+    }
+  };
+  load_gb(kh * ratio);
+
+  bool ok = mbar_wait(bar_qk, 0, kWaitLimit);
+  if (!ok) raise_error(p.err, kErrTimeout);
+  ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  const bool qk_pending = !ok;
+  bool gram_pending = false;
+  if (ok) {
+    // Gram G = [K; Q] K^T (M = 128, N = 64, K = 128) on the raw bf16 tiles
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+        mma_bf16(tmem, sw128_desc(sb + PR_QK + off), sw128_desc(sb + PR_QK + off), idesc_bf16_f32(128, 64), ks > 0);
+      }
+      mma_commit(bar_g);
+    }
+    gram_pending = true;
+    // L2-norm factors: rows 0..63 keys, 64..127 queries; each part sums 64 of the 128 features
+    {
+      const int r = tid & 127, kq = tid >> 7;
+      float ss = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 16 / kParts; ++cc) {
+        const int chunk = kq * (16 / kParts) + cc, kb = chunk >> 3, c = chunk & 7;
+        const uint4 u = *reinterpret_cast<const uint4*>(sm + PR_QK + kb * 16384 + r * 128 + (((c ^ (r & 7)) & 7) << 4));
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = __uint_as_float(w4[e] << 16), b = __uint_as_float(w4[e] & 0xFFFF0000u);
+          ss = fmaf(a, a, ss);
+          ss = fmaf(b, b, ss);
+        }
+      }
+      s_part[kq * 128 + r] = ss;
+    }
+    __syncthreads();
+    if (tid < 128) {
+      float ss = 0.f;
+#pragma unroll
+      for (int q = 0; q < kParts; ++q) ss += s_part[q * 128 + tid];
+      const float inv = 1.0f / sqrtf(ss + p.l2_eps);
+      if (tid < 64) s_ik[tid] = inv; else s_iq[tid - 64] = inv;
+    }
+    const bool got = mbar_wait(bar_g, 0, kWaitLimit);
+    if (!got) raise_error(p.err, kErrTimeout);
+    ok = __syncthreads_and(got ? 1 : 0) != 0;
+    gram_pending = !ok;
+    tc_fence_after();
+  }
+  if (ok) {
+    float gr[kW];  // raw Gram row `row`, columns part * kW ..
+    tmem_ld_cols<kW>(tl + part * kW, gr);
+    for (int r = 0; r < ratio; ++r) {
+      const int h = kh * ratio + r;
+      uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * REC_BYTES;
+      if (tid < 64) {
+        s_gam[tid] = g_next * kLog2e;
+        s_beta[tid] = b_next;
+      }
+      __syncthreads();
+      if (warp == 0) {  // inclusive scan of g over the chunk (lane l holds tokens 2l, 2l + 1)
+        const float g0 = s_gam[2 * lane], g1 = s_gam[2 * lane + 1];
+        float s = g0 + g1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float v = __shfl_up_sync(0xffffffffu, s, o);
+          if (lane >= o) s += v;
+        }
+        s_gam[2 * lane + 1] = s;
+        s_gam[2 * lane] = s - g1;
+      }
+      __syncthreads();
+      if (r + 1 < ratio) load_gb(h + 1);  // in flight during this head's work
+      if (tid < 64) {  // per-token factors
+        const int t = tid;
+        const float gt = s_gam[t], gL = s_gam[L - 1];
+        const float Gam = ex2_approx(gt), bt = s_beta[t];
+        float* vec = reinterpret_cast<float*>(rec + REC_VEC);
+        vec[V_BETA + t] = bt;
+        vec[V_CX + t] = bt * Gam * s_ik[t];
+        vec[V_CS + t] = (t < L) ? ex2_approx(gL - gt) * s_ik[t] : 0.f;
+        vec[V_CO + t] = Gam * s_iq[t] * p.q_scale;
+        vec[V_MISC + t] = (t == 0) ? ex2_approx(gL) : 0.f;
+      }
+      // A (rows 0..63, into the solve layout) and P (rows 64..127, straight to the record)
+      if (row < 64) {
+        const int t = row;
+        const float bt = s_beta[t] * s_ik[t], gt = s_gam[t];
+#pragma unroll
+        for (int i4 = 0; i4 < kW; i4 += 4) {
+          const int j0 = part * kW + i4;
+          const float4 gj = *reinterpret_cast<const float4*>(s_gam + j0);
+          const float4 kj = *reinterpret_cast<const float4*>(s_ik + j0);
+          const float gv[4] = {gj.x, gj.y, gj.z, gj.w}, kv[4] = {kj.x, kj.y, kj.z, kj.w};
+          float a[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float val = bt * ex2_approx(gt - gv[u]) * gr[i4 + u] * kv[u];
+            a[u] = (j0 + u < t) ? val : 0.f;
+          }
+          *reinterpret_cast<float4*>(sA + tidx(t, j0)) = make_float4(a[0], a[1], a[2], a[3]);
+        }
+      } else {
+        const int t = row - 64;
+        const float qt = s_iq[t] * p.q_scale, gt = s_gam[t];
+#pragma unroll
+        for (int i0 = 0; i0 < kW; i0 += 8) {
+          float v[8];
+          const int j0 = part * kW + i0;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float a = qt * ex2_approx(gt - s_gam[j0 + u]) * gr[i0 + u] * s_ik[j0 + u];
+            v[u] = (j0 + u <= t) ? a : 0.f;
+          }
+          store8_split(rec + REC_P, nullptr, 0, t, j0, v);
+        }
+      }
+      __syncthreads();
+      solve_unit_lower(sA, sT, sB, tid);
+      for (int i = tid; i < 64 * 8; i += kThreads) {
+        const int t = i >> 3, k0 = (i & 7) * 8;
+        const bool upper = (k0 >> 4) > (t >> 4);  // strictly upper blocks of T are zero
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 v0 = upper ? z4 : *reinterpret_cast<const float4*>(sT + tidx(t, k0));
+        const float4 v1 = upper ? z4 : *reinterpret_cast<const float4*>(sT + tidx(t, k0 + 4));
+        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        store8_split(rec + REC_T, rec + REC_T + 8192, 0, t, k0, v);
+      }
+    }
+  }
+  // leave only after the Gram MMA and the tile load have landed (bounded, after an early exit)
+  if (qk_pending) mbar_wait(bar_qk, 0, kWaitLimit);
+  if (gram_pending) mbar_wait(bar_g, 0, kWaitLimit);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
+// Persistent; pulls (sequence, V head) items in longest-first order.  Thread (row, part) owns
+// tensor-memory lane `row` (a value row of the state) and kW of the 64 columns of every
+// token-indexed accumulator.
+__global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_constant__ StateParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const uint32_t sb = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, part = warp >> 2;
+  const int row = q4 * 32 + lane;
+  const int ratio = p.Hv / p.Hk;
+  const long total_items = (long)p.N * p.Hv;
+
+  float* s_work = reinterpret_cast<float*>(sm + SS_W);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SS_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SS_BAR + 64);
+  int* item_slot = reinterpret_cast<int*>(sm + SS_BAR + 72);
+  const uint32_t bar_qk = smem_u32(&bars[0]), bar_v = smem_u32(&bars[1]), bar_rec = smem_u32(&bars[2]),
+                 bar_h = smem_u32(&bars[3]), bar_x = smem_u32(&bars[4]), bar_e = smem_u32(&bars[5]),
+                 bar_s = smem_u32(&bars[6]);
+
+  if (tid == 0) {
+    for (int i = 0; i < 7; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), SC_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+
+  constexpr uint32_t ID64 = idesc_bf16_f32(128, 64);
+  constexpr uint32_t ID128 = idesc_bf16_f32(128, 128);
+  constexpr uint32_t ID128_BMN = idesc_bf16_f32_bmn(128, 128);
+  bool ok = true;
+  uint32_t ph_mma = 0, ph_qk = 0, ph_v = 0, ph_rec = 0;
+  bool pend_qk = false, pend_v = false, pend_rec = false;
+  const bool gated = p.z != nullptr;
+  float wf[4] = {1.f, 1.f, 1.f, 1.f};
+  if (gated) {
+    const uint2 ww = __ldg(reinterpret_cast<const uint2*>(p.norm_w + lane * 4));
+    wf[0] = __uint_as_float(ww.x << 16); wf[1] = __uint_as_float(ww.x & 0xFFFF0000u);
+    wf[2] = __uint_as_float(ww.y << 16); wf[3] = __uint_as_float(ww.y & 0xFFFF0000u);
+  }
+
+  auto wait_bar = [&](uint32_t bar, uint32_t& ph) {
+    const bool got = mbar_wait(bar, ph, kWaitLimit);
+    ph ^= 1u;
+    if (!got) raise_error(p.err, kErrTimeout);
+    ok = __syncthreads_and(got ? 1 : 0) != 0 && ok;
+  };
+  auto await_mma = [&](uint32_t bar) {
+    uint32_t ph = ph_mma;
+    wait_bar(bar, ph);
+    tc_fence_after();
+  };
+  auto operands_ready = [&]() {
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  };
+  auto issue_v = [&](int c0, int h) {
+    mbar_arrive_expect_tx(bar_v, kBytesV);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+      tma_load_2d(sb + SS_V + kb * 8192, &p.tmap, 2 * p.Hk * kHeadDim + h * kHeadDim + kb * 64, c0, bar_v);
+  };
+  auto issue_rec = [&](int gc, int h, int vb) {
+    const uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * REC_BYTES;
+    mbar_arrive_expect_tx(bar_rec, kRecTP + kRecVec);
+    bulk_load(sb + SS_T, rec + REC_T, kRecTP, bar_rec);
+    bulk_load(sb + SS_VEC + vb * kRecVec, rec + REC_VEC, kRecVec, bar_rec);
+  };
+  // S0 columns [k0, k0 + 64) -> hi/lo operand tiles (64 keys = one K block); state <- Gamma_L S0 there
+  auto convert_half = [&](int k0, float gL) {
+    float v[kW];
+    tmem_ld_cols<kW>(tl + SC_S + k0 + part * kW, v);
+#pragma unroll
+    for (int q = 0; q < kW / 8; ++q) store8_split(sm + SS_W, sm + SS_W + 16384, 0, row, part * kW + 8 * q, v + 8 * q);
+#pragma unroll
+    for (int i = 0; i < kW; ++i) v[i] *= gL;
+    tmem_st32(tl + SC_S + k0 + part * kW, v);
+  };
+
+  for (;;) {
+    if (tid == 0) *item_slot = (int)atomicAdd(p.counter, 1u);
+    __syncthreads();
+    const long w = *item_slot;
+    __syncthreads();
+    if (w >= total_items || !ok) break;
+    const int h = (int)(w % p.Hv);
+    const int ni = (int)(w / p.Hv);
+    const int n = p.order ? __ldg(p.order + ni) : ni;
+    const int kh = h / ratio;
+    const int seq_s = __ldg(p.cu + n), seq_e = __ldg(p.cu + n + 1);
+    const int gc0 = __ldg(p.chunk_off + n);
+    if (n < 0 || n >= p.N || seq_s < 0 || seq_e < seq_s || seq_e > p.T || gc0 < 0 ||
+        gc0 + (seq_e - seq_s + kChunk - 1) / kChunk > p.nc_max) {
+      if (tid == 0) raise_error(p.err, kErrDeviceArgument);
+      continue;
+    }
+    if (tid == 0 && seq_e > seq_s) {
+      issue_qk_tiles(sb + SS_QK, &p.tmap, p.Hk, seq_s, kh, bar_qk);
+      issue_v(seq_s, h);
+      issue_rec(gc0, h, 0);
+    }
+    pend_qk = pend_v = pend_rec = seq_e > seq_s;
+
+    // ---- initial state -> tensor memory
+    {
+      const size_t row_off = (((size_t)n * p.Hv + h) * kHeadDim + row) * kHeadDim;
+#pragma unroll
+      for (int cq = 0; cq < 4 / kParts; ++cq) {
+        const int c0 = part * (128 / kParts) + cq * 32;
+        float v[32];
+        if (p.state_in) {
+          const float4* src = reinterpret_cast<const float4*>(p.state_in + row_off + c0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 f = __ldg(src + i);
+            v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        tmem_st32(tl + SC_S + c0, v);
+      }
+    }
+
+    int vb = 0;
+    for (int c0 = seq_s, gc = gc0; c0 < seq_e && ok; c0 += kChunk, ++gc, ph_mma ^= 1u, vb ^= 1) {
+      const int L = min(kChunk, seq_e - c0);
+      const bool has_next = c0 + kChunk < seq_e;
+      const float* vec = reinterpret_cast<const float*>(sm + SS_VEC + vb * kRecVec);
+
+      wait_bar(bar_rec, ph_rec);
+      pend_rec = false;
+      wait_bar(bar_qk, ph_qk);
+      pend_qk = false;
+      if (!ok) break;
+      const float gL = vec[V_MISC];
+
+      // ================= [X | O1] = S0 [K; Q]^T, hi + lo, one 64-key half at a time
+      convert_half(0, gL);
+      operands_ready();
+      if (tid == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bkq = sw128_desc(sb + SS_QK + ks * 32);
+          mma_bf16(tmem + SC_X, sw128_desc(sb + SS_W + ks * 32), bkq, ID128, ks > 0);
+          mma_bf16(tmem + SC_X, sw128_desc(sb + SS_W + 16384 + ks * 32), bkq, ID128, 1);
+        }
+        mma_commit(bar_h);
+      }
+      await_mma(bar_h);
+      if (!ok) break;
+      convert_half(64, gL);
+      operands_ready();
+      if (tid == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bkq = sw128_desc(sb + SS_QK + 16384 + ks * 32);
+          mma_bf16(tmem + SC_X, sw128_desc(sb + SS_W + ks * 32), bkq, ID128, 1);
+          mma_bf16(tmem + SC_X, sw128_desc(sb + SS_W + 16384 + ks * 32), bkq, ID128, 1);
+        }
+        mma_commit(bar_x);
+      }
+      await_mma(bar_x);
+      wait_bar(bar_v, ph_v);
+      pend_v = false;
+      if (!ok) break;
+
+      // ================= R = diag(beta) V - diag(c_x) X^T -> hi/lo (value-major)
+      {
+        float x[kW];
+        tmem_ld_cols<kW>(tl + SC_X + part * kW, x);
+        const uint8_t* vbase = sm + SS_V + (row >> 6) * 8192 + part * kW * 128 + ((row & 7) << 1);
+        const int rsw = (row >> 3) & 7;
+#pragma unroll
+        for (int i4 = 0; i4 < kW; i4 += 4) {
+          const float4 bt = *reinterpret_cast<const float4*>(vec + V_BETA + part * kW + i4);
+          const float4 cx = *reinterpret_cast<const float4*>(vec + V_CX + part * kW + i4);
+          const float btv[4] = {bt.x, bt.y, bt.z, bt.w}, cxv[4] = {cx.x, cx.y, cx.z, cx.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i4 + u;
+            const float v = bf2f(*reinterpret_cast<const uint16_t*>(vbase + i * 128 + ((rsw ^ (i & 7)) << 4)));
+            x[i] = btv[u] * v - cxv[u] * x[i];
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kW / 8; ++q) store8_split(sm + SS_W, sm + SS_W + 16384, 0, row, part * kW + 8 * q, x + 8 * q);
+      }
+      operands_ready();
+      if (tid == 0) {
+        if (has_next) issue_v(c0 + kChunk, h);
+        // E^T = R T^T  (hi*hi + hi*lo + lo*hi)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t off = ks * 32;
+          const uint64_t rh = sw128_desc(sb + SS_W + off), rl = sw128_desc(sb + SS_W + 16384 + off);
+          mma_bf16(tmem + SC_X, rh, sw128_desc(sb + SS_T + off), ID64, ks > 0);
+          mma_bf16(tmem + SC_X, rh, sw128_desc(sb + SS_T + 8192 + off), ID64, 1);
+          mma_bf16(tmem + SC_X, rl, sw128_desc(sb + SS_T + off), ID64, 1);
+        }
+        mma_commit(bar_e);
+      }
+      pend_v = has_next;
+      await_mma(bar_e);
+      if (!ok) break;
+
+      // ================= E~ = E diag(c_s) -> hi/lo;  E -> bf16 (output operand, over T)
+      {
+        float ev[kW];
+        tmem_ld_cols<kW>(tl + SC_X + part * kW, ev);
+#pragma unroll
+        for (int q = 0; q < kW / 8; ++q) {
+          const float4 c0v = *reinterpret_cast<const float4*>(vec + V_CS + part * kW + 8 * q);
+          const float4 c1v = *reinterpret_cast<const float4*>(vec + V_CS + part * kW + 8 * q + 4);
+          const float* e8 = ev + 8 * q;
+          const float es[8] = {e8[0] * c0v.x, e8[1] * c0v.y, e8[2] * c0v.z, e8[3] * c0v.w,
+                               e8[4] * c1v.x, e8[5] * c1v.y, e8[6] * c1v.z, e8[7] * c1v.w};
+          store8_split(sm + SS_W, sm + SS_W + 16384, 0, row, part * kW + 8 * q, es);
+          store8_split(sm + SS_T, nullptr, 0, row, part * kW + 8 * q, e8);
+        }
+      }
+      operands_ready();
+      if (tid == 0) {
+        // S += E~ K: B = the raw k rows of the q/k tile read MN-major (N = 128 keys, 16 tokens per step)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bk = sw128_mn_desc(sb + SS_QK + ks * 2048, 16384);
+          mma_bf16(tmem + SC_S, sw128_desc(sb + SS_W + ks * 32), bk, ID128_BMN, 1);
+          mma_bf16(tmem + SC_S, sw128_desc(sb + SS_W + 16384 + ks * 32), bk, ID128_BMN, 1);
+          mma_bf16(tmem + SC_X, sw128_desc(sb + SS_T + ks * 32), sw128_desc(sb + SS_P + ks * 32), ID64, ks > 0);
+        }
+        mma_commit(bar_s);
+      }
+      // the gate input of this thread's output elements, in flight during the MMAs
+      constexpr int kTok = kChunk / kWarps;
+      uint2 zr[kTok];
+      if (gated) {
+#pragma unroll
+        for (int i = 0; i < kTok; ++i) {
+          const int t = warp + kWarps * i;
+          zr[i] = t < L ? __ldg(reinterpret_cast<const uint2*>(p.z + ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4))
+                        : make_uint2(0u, 0u);
+        }
+      }
+      await_mma(bar_s);
+      if (!ok) break;
+      if (tid == 0 && has_next) {
+        issue_qk_tiles(sb + SS_QK, &p.tmap, p.Hk, c0 + kChunk, kh, bar_qk);
+        issue_rec(gc + 1, h, vb ^ 1);
+      }
+      pend_qk = pend_rec = has_next;
+
+      // ================= output: o = O1 diag(c_o) + O2 staged token-major, then the gated RMSNorm
+#pragma unroll
+      for (int hh = 0; hh < kW; hh += 16) {  // 16 columns at a time: the gate inputs stay in registers
+        float o1[16], o2[16];
+        tmem_ld16(tl + SC_O1 + part * kW + hh, o1);
+        tmem_ld16(tl + SC_X + part * kW + hh, o2);
+#pragma unroll
+        for (int i4 = 0; i4 < 16; i4 += 4) {
+          const int t0 = part * kW + hh + i4;
+          const float4 co = *reinterpret_cast<const float4*>(vec + V_CO + t0);
+          s_work[t0 * 128 + row] = fmaf(o1[i4], co.x, o2[i4]);
+          s_work[(t0 + 1) * 128 + row] = fmaf(o1[i4 + 1], co.y, o2[i4 + 1]);
+          s_work[(t0 + 2) * 128 + row] = fmaf(o1[i4 + 2], co.z, o2[i4 + 2]);
+          s_work[(t0 + 3) * 128 + row] = fmaf(o1[i4 + 3], co.w, o2[i4 + 3]);
+        }
+      }
+      __syncthreads();
+      {
+        float r[kTok][4], ss[kTok];
+#pragma unroll
+        for (int i = 0; i < kTok; ++i) {
+          const float4 v = *reinterpret_cast<const float4*>(s_work + (warp + kWarps * i) * 128 + lane * 4);
+          r[i][0] = v.x; r[i][1] = v.y; r[i][2] = v.z; r[i][3] = v.w;
+          ss[i] = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+        if (gated) {
+#pragma unroll
+          for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+            for (int i = 0; i < kTok; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], m);
+#pragma unroll
+          for (int i = 0; i < kTok; ++i) {
+            const float rstd = rsqrtf(ss[i] * (1.0f / kHeadDim) + p.rms_eps);
+            const float zf[4] = {__uint_as_float(zr[i].x << 16), __uint_as_float(zr[i].x & 0xFFFF0000u),
+                                 __uint_as_float(zr[i].y << 16), __uint_as_float(zr[i].y & 0xFFFF0000u)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) r[i][e] = r[i][e] * rstd * wf[e] * sigmoid_fast(zf[e]);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kTok; ++i) {
+          const int t = warp + kWarps * i;
+          if (t < L) {
+            const size_t base = ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4;
+            *reinterpret_cast<uint2*>(p.out + base) =
+                make_uint2(pack_bf2(r[i][0], r[i][1]), pack_bf2(r[i][2], r[i][3]));
+          }
+        }
+      }
+      fence_proxy_async_smem();  // vector-block reads precede the bulk copy that refills the buffer
+      tc_fence_before();
+      __syncthreads();  // staging reads and accumulator reads done before the next chunk reuses them
+      tc_fence_after();
+    }
+    if (!ok) break;
+
+    // ---- final state -> global
+    if (p.state_out) {
+      const size_t row_off = (((size_t)n * p.Hv + h) * kHeadDim + row) * kHeadDim;
+#pragma unroll
+      for (int cq = 0; cq < 4 / kParts; ++cq) {
+        const int c0 = part * (128 / kParts) + cq * 32;
+        float v[32];
+        tmem_ld32(tl + SC_S + c0, v);
+        float4* dst = reinterpret_cast<float4*>(p.state_out + row_off + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+
+  // after an early exit, let copies still in flight land before the CTA leaves (bounded)
+  if (pend_qk) mbar_wait(bar_qk, ph_qk, kWaitLimit);
+  if (pend_v) mbar_wait(bar_v, ph_v, kWaitLimit);
+  if (pend_rec) mbar_wait(bar_rec, ph_rec, kWaitLimit);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, SC_COLS);
+  }
+}
+
+}  // namespace
+
+namespace {
+
+size_t pad256(size_t b) { return (b + 255) / 256 * 256; }
+
+// upper bound of sum_n ceil(L_n / 64) for N sequences of T tokens in total
+long chunk_bound(int N, int T) { return ((long)T + 63L * N) / kChunk; }
+
+struct SplitLayout {
+  unsigned* counter;
+  int32_t* order;
+  int32_t* chunk_off;
+  uint8_t* rec;
+};
+
+SplitLayout split_layout(void* workspace, int N) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SplitLayout l;
+  l.counter = reinterpret_cast<unsigned*>(ws);
+  l.order = reinterpret_cast<int32_t*>(ws + 256);
+  l.chunk_off = reinterpret_cast<int32_t*>(ws + 256 + pad256((size_t)N * 4));
+  l.rec = ws + 256 + pad256((size_t)N * 4) + pad256((size_t)(N + 1) * 4);
+  return l;
+}
+
+template <typename K>
+cudaError_t set_smem_once(K kernel, uint32_t bytes, int (&done)[64]) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && done[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  // the largest shared-memory carveout, so that as many CTAs as the footprint allows share an SM
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e == cudaSuccess && dev < 64) done[dev] = 1;
+  return e;
+}
+
+}  // namespace
+
+size_t split_workspace_bytes(int N, int T, int Hk, int Hv) {
+  (void)Hk;
+  if (N <= 0) return 0;
+  return 256 + pad256((size_t)N * 4) + pad256((size_t)(N + 1) * 4) +
+         (size_t)chunk_bound(N, T) * (size_t)Hv * REC_BYTES;
+}
+
+cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv, const float* g, const float* beta,
+                                       const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale, float l2_eps,
+                                       const float* state_in, float* state_out, const uint16_t* z,
+                                       const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace) {
+  static int prep_set[64] = {0}, state_set[64] = {0};
+  if (N <= 0) return cudaSuccess;
+  const SplitLayout lay = split_layout(workspace, N);
+  const long nc_max = chunk_bound(N, T);
+  CUtensorMap tmap;
+  memset(&tmap, 0, sizeof tmap);
+  if (T > 0) {
+    cudaError_t e = encode_chunk_tensor_maps(&tmap, nullptr, qkv, nullptr, T, Hk, Hv);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = launch_chunk_schedule(env.stream, cu, N, lay.order, lay.counter, lay.chunk_off);
+  if (e != cudaSuccess) return e;
+
+  if (T > 0 && nc_max > 0) {
+    if ((e = set_smem_once(chunk_prep_kernel, PR_BYTES, prep_set)) != cudaSuccess) return e;
+    PrepParams pp;
+    memset(&pp, 0, sizeof pp);
+    pp.tmap = tmap;
+    pp.g = g; pp.beta = beta; pp.cu = cu; pp.chunk_off = lay.chunk_off; pp.rec = lay.rec; pp.err = env.err;
+    pp.N = N; pp.T = T; pp.Hk = Hk; pp.Hv = Hv; pp.q_scale = q_scale; pp.l2_eps = l2_eps;
+    chunk_prep_kernel<<<dim3((unsigned)nc_max, (unsigned)Hk), kThreads, PR_BYTES, env.stream>>>(pp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+
+  if ((e = set_smem_once(chunk_state_kernel, SS_BYTES, state_set)) != cudaSuccess) return e;
+  StateParams sp;
+  memset(&sp, 0, sizeof sp);
+  sp.tmap = tmap;
+  sp.cu = cu; sp.order = lay.order; sp.counter = lay.counter; sp.chunk_off = lay.chunk_off; sp.rec = lay.rec;
+  sp.state_in = state_in; sp.state_out = state_out; sp.z = z; sp.norm_w = norm_w; sp.out = out; sp.err = env.err;
+  sp.N = N; sp.T = T; sp.Hk = Hk; sp.Hv = Hv; sp.nc_max = (int)nc_max; sp.rms_eps = rms_eps;
+  int sms = 0;
+  if ((e = device_sm_count(&sms)) != cudaSuccess) return e;
+  // Two CTAs per SM: 2 x 256 tensor-memory columns, 2 x (SS_BYTES + 1 KB reserved) of shared
+  // memory and 2 x 256 threads x 128 registers all fit.  (The runtime's occupancy query reports one
+  // CTA per SM for any kernel that allocates tensor memory, but the hardware co-schedules two; a
+  // CTA that cannot be resident runs later, finds no work and exits.)
+  constexpr int per_sm = 2;
+  const long items = (long)N * Hv;
+  const long slots = (long)sms * per_sm;
+  const int grid = (int)(items < slots ? items : slots);
+  chunk_state_kernel<<<grid, kThreads, SS_BYTES, env.stream>>>(sp);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -12,7 +12,7 @@ namespace gdn {
 
 namespace {
 
-constexpr int kRun = 16;          // tokens per thread
+constexpr int kRun = 8;           // tokens per thread
 constexpr int kThreadsX = 128;    // channel octets per block
 
 struct Oct {
@@ -61,7 +61,7 @@ __device__ __forceinline__ int seq_of_token(const int32_t* cu, int N, int t) {
   return lo;
 }
 
-__global__ void __launch_bounds__(kThreadsX) conv1d_silu_kernel(
+__global__ void __launch_bounds__(kThreadsX, 4) conv1d_silu_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, const int32_t* __restrict__ cu,
     int N, int T, int C, const uint16_t* __restrict__ state_in, uint16_t* __restrict__ y,
     unsigned* err) {

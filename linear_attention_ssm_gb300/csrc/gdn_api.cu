@@ -152,6 +152,11 @@ gdn_status gdn_conv1d_prefill(const gdn_geometry* geo, const gdn_bf16* x, const 
 }
 
 size_t gdn_chunk_prefill_workspace_size(const gdn_geometry* geo, int32_t num_seqs, int32_t total_tokens) {
+  if (!geo || num_seqs <= 0 || total_tokens < 0 || geo->num_k_heads <= 0 || geo->num_v_heads <= 0) return 0;
+  return gdn::split_workspace_bytes(num_seqs, total_tokens, geo->num_k_heads, geo->num_v_heads);
+}
+
+size_t gdn_chunk_prefill_min_workspace_size(const gdn_geometry* geo, int32_t num_seqs, int32_t total_tokens) {
   (void)geo;
   (void)total_tokens;
   return num_seqs > 0 ? gdn::chunk_prefill_workspace_bytes(num_seqs) : 0;
@@ -187,7 +192,7 @@ gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const
     GDN_REQUIRE(norm_w, "norm_w");
   }
   if (!(l2_eps >= 0.f) || !(rms_eps >= 0.f)) return fail(GDN_ERR_INVALID_ARGUMENT, "eps must be >= 0");
-  const size_t need = gdn_chunk_prefill_workspace_size(geo, num_seqs, total_tokens);
+  const size_t need = gdn_chunk_prefill_min_workspace_size(geo, num_seqs, total_tokens);
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need, workspace_bytes);
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -201,7 +206,7 @@ gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const
   if ((s = make_env(stream, &env)) != GDN_OK) return s;
   return launched(gdn::launch_chunk_prefill(env, g_chunk_mode, qkv, g, beta, cu_seqlens, num_seqs, total_tokens,
                                             geo->num_k_heads, geo->num_v_heads, q_scale, l2_eps, state_in,
-                                            state_out, z, norm_w, rms_eps, out, workspace),
+                                            state_out, z, norm_w, rms_eps, out, workspace, workspace_bytes),
                   "chunk prefill launch");
 }
 
@@ -269,7 +274,7 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_geometry* geo, const gdn_bf16* qk
   if (num_seqs > GDN_NOALLOC_MAX_SEQS)
     return fail(GDN_ERR_INVALID_ARGUMENT, "num_seqs=%d exceeds the %d sequences of the fixed scratch", num_seqs,
                 GDN_NOALLOC_MAX_SEQS);
-  if (gdn_chunk_prefill_workspace_size(geo, num_seqs, total_tokens) > GDN_NOALLOC_SCRATCH_BYTES)
+  if (gdn_chunk_prefill_min_workspace_size(geo, num_seqs, total_tokens) > GDN_NOALLOC_SCRATCH_BYTES)
     return fail(GDN_ERR_INVALID_ARGUMENT, "the fixed scratch is too small for num_seqs=%d", num_seqs);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -308,7 +313,7 @@ gdn_status gdn_check_device_errors(void* stream) {
 }
 
 gdn_status gdn_debug_set_chunk_mode(int mode) {
-  if (mode != 0 && mode != 1) return fail(GDN_ERR_INVALID_ARGUMENT, "mode must be 0 or 1");
+  if (mode < 0 || mode > 2) return fail(GDN_ERR_INVALID_ARGUMENT, "mode must be 0, 1 or 2");
   g_chunk_mode = mode;
   return ok();
 }

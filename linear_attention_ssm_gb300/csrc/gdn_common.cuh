@@ -96,6 +96,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// 1D bulk copy global -> shared of `bytes` (multiple of 16; both addresses 16-byte aligned);
+// completion is signalled on `bar` (complete_tx).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ proxy / tcgen05 fences
 
 // generic-proxy shared-memory writes -> visible to the async proxy (tensor-core operand reads)
@@ -213,10 +221,25 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
          | ((uint64_t)2 << 61);                  // 128-byte swizzle
 }
 
+// Descriptor of an MN-major operand in the 128-byte-swizzle layout: each 128-byte row holds 64
+// consecutive M/N elements of one K index, groups of 8 K rows are 1024 bytes apart and blocks
+// of 64 M/N elements are `mn_block_bytes` apart.  Same physical layout as a K-major tile whose
+// rows are K indices, so a TMA box of 64 tokens x 64 features serves as B with N = features.
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t mn_block_bytes) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4)
+         | ((uint64_t)((mn_block_bytes >> 4) & 0x3FFFu) << 16)  // stride between 64-element M/N blocks
+         | ((uint64_t)(1024 >> 4) << 32)                         // stride between 8-row K groups
+         | ((uint64_t)1 << 46)
+         | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor: D fp32, A and B bf16, both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+
+// As above with B MN-major (the transpose-B bit).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) { return idesc_bf16_f32(M, N) | (1u << 16); }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,

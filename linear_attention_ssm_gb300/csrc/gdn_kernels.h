@@ -1,6 +1,7 @@
 // gdn_kernels.h -- internal launch functions of the GDN kernels (host side of each .cu file).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,13 +22,29 @@ cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const ui
                                const uint16_t* z, const uint16_t* norm_w, float q_scale, float l2_eps,
                                float rms_eps, uint16_t* out, int B, int Hk, int Hv);
 
-// Workspace of the chunk prefill: a work counter and the longest-first sequence order.
+// Workspace of the fused chunk prefill: a work counter and the longest-first sequence order.
 size_t chunk_prefill_workspace_bytes(int N);
+// Workspace of the split chunk prefill (prep kernel + state kernel): the above, per-sequence
+// chunk offsets, and per-chunk operand images (K^T per K head; T, P and per-token factors per
+// V head).
+size_t split_workspace_bytes(int N, int T, int Hk, int Hv);
 
-// mode 0: tcgen05 tensor cores; mode 1: the same data flow with the MMAs emulated on CUDA cores
+cudaError_t device_sm_count(int* sms);
+cudaError_t encode_chunk_tensor_maps(CUtensorMap* qkv_map, CUtensorMap* z_map, const uint16_t* qkv,
+                                     const uint16_t* z, int T, int Hk, int Hv);
+cudaError_t launch_chunk_schedule(cudaStream_t stream, const int32_t* cu, int N, int32_t* order, unsigned* counter,
+                                  int32_t* chunk_off);
+
+// mode 0: tensor cores, split path when the workspace holds it (else fused); mode 1: fused, MMAs
+// emulated on CUDA cores; mode 2: fused, tensor cores.
 cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t* qkv, const float* g,
                                  const float* beta, const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale,
                                  float l2_eps, const float* state_in, float* state_out, const uint16_t* z,
-                                 const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace);
+                                 const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace,
+                                 size_t workspace_bytes);
+cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv, const float* g, const float* beta,
+                                       const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale, float l2_eps,
+                                       const float* state_in, float* state_out, const uint16_t* z,
+                                       const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace);
 
 }  // namespace gdn

@@ -116,12 +116,27 @@ def test_decode_and_norm_reject_bad_arguments(lib):
 
 
 def test_workspace_is_required_and_aligned(lib):
-    need = lib.gdn_chunk_prefill_workspace_size(_geo(), 8, 32735)
-    assert need >= 8 * 4
+    need = lib.gdn_chunk_prefill_min_workspace_size(_geo(), 8, 32735)
+    assert need == 512                                   # counter block + 8 sequence slots, 256-rounded
+    assert lib.gdn_chunk_prefill_min_workspace_size(_geo(), 0, 0) == 0
     assert lib.gdn_chunk_prefill_workspace_size(_geo(), 0, 0) == 0
     assert _chunk(lib, N=8, T=32735) == 7                                    # missing workspace
     assert _chunk(lib, N=8, T=32735, ws=FAKE, wsb=need - 1) == 7             # too small
     assert _chunk(lib, N=8, T=32735, ws=ctypes.c_void_p(0x10010), wsb=need) == 3  # not 256-byte aligned
+
+
+def test_fast_path_workspace_size():
+    """Header blocks plus one 25,856-byte record per (chunk, V head), with the chunk count bounded
+    by sum_n ceil(L_n / 64) <= (T + 63 N) / 64."""
+    lib = binding.load_library()
+    rec = 2 * 8192 + 8192 + 5 * 64 * 4
+    for n, t in ((1, 16), (4, 4 * 4096), (8, 32735), (3, 0)):
+        chunks = (t + 63 * n) // 64
+        head = 256 + -(-4 * n // 256) * 256 + -(-4 * (n + 1) // 256) * 256
+        assert lib.gdn_chunk_prefill_workspace_size(_geo(), n, t) == head + chunks * 48 * rec
+    # the bound covers the worst case: every sequence one token past a chunk boundary
+    lengths = [65] * 7
+    assert sum(-(-L // 64) for L in lengths) <= (sum(lengths) + 63 * 7) // 64
 
 
 def test_binding_refuses_cpu_tensors():

@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 GEO = QWEN_GDN
 
 
-@pytest.fixture(params=[0, 1], ids=["tensor_cores", "emulated"])
+@pytest.fixture(params=[0, 1, 2], ids=["split", "emulated", "fused"])
 def mode(request):
     g = lib()
     g.gdn_debug_set_chunk_mode(request.param)
@@ -117,9 +117,11 @@ def test_state_in_place():
     assert_state_close(st, ref["state"])
 
 
-def test_small_geometry():
-    """Hk = 2, Hv = 6 (ratio 3): head expansion indices at another head count."""
-    geo = Geometry(num_k_heads=2, num_v_heads=6)
+@pytest.mark.parametrize("hk,hv", [(2, 6), (4, 4), (2, 8)])
+def test_small_geometry(hk, hv, mode):
+    """Other head counts and V/K ratios (3, 1, 4): head expansion indices and the prep kernel's
+    loop over the V heads of a K head."""
+    geo = Geometry(num_k_heads=hk, num_v_heads=hv)
     inp = prefill_inputs([100, 30], seed=11, geo=geo)
     ref = run_oracle(inp, geo=geo)
     out, st = run_gpu(inp, ref["y"], geo=geo)
@@ -207,3 +209,30 @@ def test_more_sequences_than_the_sorted_schedule():
     for h in (3, 44):
         assert_out_close(out[:, h], ref["out"][:, h], f"out, head {h}")
         assert_state_close(st[:, h], ref["state"][:, h], f"states, head {h}")
+
+
+def test_minimum_workspace_runs_the_fused_kernel():
+    """With only the minimum workspace, the default mode runs the one-kernel path: bit-identical
+    to forcing it, and within the tolerances of the oracle like the split path."""
+    g = lib()
+    inp = prefill_inputs([150, 64, 9], seed=41)
+    ref = run_oracle(inp)
+    N, T = 3, ref["y"].shape[0]
+    args = (ref["y"].to(DEV), inp["g"].to(DEV), inp["beta"].to(DEV), inp["cu_seqlens"].to(DEV), inp["q_scale"], 1e-6,
+            inp["state0"].to(DEV))
+    small = torch.empty(g.gdn_chunk_prefill_min_workspace_size(N, T), dtype=torch.uint8, device=DEV)
+    assert g.gdn_chunk_prefill_workspace_size(N, T) > small.numel()
+    results = []
+    for mode_, ws in ((0, small), (2, None), (0, None)):
+        g.gdn_debug_set_chunk_mode(mode_)
+        try:
+            st = torch.empty((N, 48, 128, 128), dtype=torch.float32, device=DEV)
+            out = g.gdn_chunk_prefill(*args, st, inp["z"].to(DEV), inp["norm_w"].to(DEV), 1e-6, workspace=ws)
+            g.gdn_check_device_errors()
+        finally:
+            g.gdn_debug_set_chunk_mode(0)
+        results.append((out, st))
+    assert torch.equal(results[0][0], results[1][0]) and torch.equal(results[0][1], results[1][1])
+    for out, st in results:
+        assert_out_close(out, ref["out"])
+        assert_state_close(st, ref["state"])

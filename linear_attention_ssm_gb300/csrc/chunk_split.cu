@@ -36,22 +36,27 @@ namespace {
 // ---- per-(chunk, V head) record in the workspace (bytes)
 constexpr uint32_t REC_T = 0;          // T hi (8 KB) + T lo (8 KB): 64 x 64 bf16, K-major 128-byte swizzle
 constexpr uint32_t REC_P = 16384;      // P (8 KB), same layout
-constexpr uint32_t REC_VEC = 24576;    // 5 x 64 fp32: beta, c_x, c_s, c_o, misc (misc[0] = Gamma_L)
+constexpr uint32_t REC_VEC = 24576;    // 5 x 64 fp32: beta, -c_x, c_s, c_o, misc (misc[0] = Gamma_L)
 constexpr uint32_t kRecTP = 24576;     // T and P: one bulk copy
 constexpr uint32_t kRecVec = 5 * 64 * 4;
 constexpr uint32_t REC_BYTES = REC_VEC + kRecVec;  // 25,856
 static_assert(REC_BYTES % 128 == 0, "records must stay 16-byte aligned");
-constexpr int V_BETA = 0, V_CX = 64, V_CS = 128, V_CO = 192, V_MISC = 256;  // float offsets in the vector block
+constexpr int V_BETA = 0, V_NCX = 64, V_CS = 128, V_CO = 192, V_MISC = 256;  // float offsets in the vector block
 
-// ---- prep kernel shared memory
-constexpr uint32_t PR_QK = 0;                 // 32 KB [K; Q] tile (TMA)
-constexpr uint32_t PR_A = 32768;              // 16 KB A, fp32 solve layout
-constexpr uint32_t PR_T = 49152;              // 16 KB T, fp32 solve layout
-constexpr uint32_t PR_B = 65536;              // 7.5 KB the solve's six B_ik blocks
-constexpr uint32_t PR_VEC = PR_B + 6 * 16 * 20 * 4;  // gamma, beta, ik, iq (64 each), partial sums (kParts x 128)
-constexpr uint32_t PR_BAR = PR_VEC + (4 * 64 + kParts * 128) * 4;
+// ---- prep kernel shared memory: up to kGroup V heads of one K head are solved together
+constexpr int kGroup = 3;
+constexpr uint32_t kTriBytes = 10 * 16 * 16 * 4;             // the 10 lower 16 x 16 blocks of a 64 x 64 fp32 matrix
+constexpr uint32_t kBBytes = 6 * 16 * 20 * 4;                // the solve's six B_ik blocks
+constexpr uint32_t kHeadBuf = 2 * kTriBytes + kBBytes;       // A, T, B of one V head (27.5 KB)
+constexpr uint32_t PR_QK = 0;                                // 32 KB [K; Q] tile (TMA); dead once the Gram and
+                                                             // the norms are taken, then the heads' buffers
+constexpr uint32_t PR_HEADS = 0;
+constexpr uint32_t PR_VEC = kGroup * kHeadBuf;               // gamma, beta (kGroup x 64 each), ik, iq, partial sums
+constexpr uint32_t PR_BAR = PR_VEC + (2 * kGroup * 64 + 2 * 64 + kParts * 128) * 4;
 constexpr uint32_t PR_USED = PR_BAR + 64;
 constexpr uint32_t PR_BYTES = PR_USED + 1024;
+static_assert(PR_VEC >= 32768, "the q/k tile must fit under the head buffers");
+static_assert(2 * (PR_BYTES + 1024) <= 233472, "two prep CTAs must share an SM");
 
 // ---- state kernel shared memory
 constexpr uint32_t SS_QK = 0;         // 32 KB [K; Q] tile (TMA)
@@ -86,6 +91,7 @@ struct PrepParams {
 
 struct StateParams {
   CUtensorMap tmap;
+  CUtensorMap tmap_z;  // z [T][Hv * 128] bf16, box 128 x 64 (valid when z != NULL): L2 prefetch only
   const int32_t* cu;
   const int32_t* order;
   unsigned* counter;
@@ -117,8 +123,95 @@ __device__ __forceinline__ void issue_qk_tiles(uint32_t dst, const CUtensorMap* 
   }
 }
 
+// Element (r, c), c / 16 <= r / 16, of a 64 x 64 fp32 lower block-triangular matrix stored as its
+// ten 16 x 16 blocks (block row i, column j at index i (i + 1) / 2 + j), each row-major with the
+// 16-byte groups of row r XOR-permuted by r & 3: float4 accesses of one row segment by 32 lanes
+// that hold 32 consecutive rows spread over all banks.
+__device__ __forceinline__ int tri(int r, int c) {
+  const int bi = r >> 4, bj = c >> 4;
+  return ((bi * (bi + 1)) / 2 + bj) * 256 + (r & 15) * 16 + ((((c & 15) >> 2) ^ (r & 3)) << 2) + (c & 3);
+}
+
+// T_g = (I + A_g)^-1 for G <= kGroup strictly lower triangular 64 x 64 matrices at once (head g's
+// A, T and B blocks at base + g * kHeadBuf bytes): the five steps of the blocked forward
+// substitution of solve_unit_lower, each step's independent block tasks of all G heads spread
+// over the CTA's warps, so the G solves share the five barriers.
+__device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid < 64 * G) {  // step 1: diagonal blocks, one column per thread
+    const int g = tid >> 6, b = (tid >> 4) & 3, c = tid & 15, o = b * 16;
+    const float* sA = reinterpret_cast<const float*>(base + g * kHeadBuf);
+    float* sT = reinterpret_cast<float*>(base + g * kHeadBuf + kTriBytes);
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
+#pragma unroll
+    for (int k = 0; k < 15; ++k) {
+      const float xk = x[k];
+#pragma unroll
+      for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-sA[tri(o + i, o + k)], xk, x[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sT[tri(o + i, o + c)] = x[i];  // zeros above the diagonal included
+  }
+  __syncthreads();
+  const int c0 = (lane & 3) * 4;
+  // step 2: B_ik = T_ii A_ik, twelve half-block tasks per head
+  for (int task = warp; task < 12 * G; task += kWarps) {
+    const int g = task / 12, tt = task - 12 * g;
+    const float* sA = reinterpret_cast<const float*>(base + g * kHeadBuf);
+    const float* sT = reinterpret_cast<const float*>(base + g * kHeadBuf + kTriBytes);
+    float* sB = reinterpret_cast<float*>(base + g * kHeadBuf + 2 * kTriBytes);
+    const int pidx = tt >> 1;
+    const int i = pidx < 1 ? 1 : (pidx < 3 ? 2 : 3), k = pidx - pair_index(i, 0);
+    const int rr = (tt & 1) * 8 + (lane >> 2);
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float a = sT[tri(i * 16 + rr, i * 16 + u)];
+      const float4 bv = *reinterpret_cast<const float4*>(sA + tri(i * 16 + u, k * 16 + c0));
+      acc0 = fmaf(a, bv.x, acc0);
+      acc1 = fmaf(a, bv.y, acc1);
+      acc2 = fmaf(a, bv.z, acc2);
+      acc3 = fmaf(a, bv.w, acc3);
+    }
+    *reinterpret_cast<float4*>(sB + pidx * 320 + rr * 20 + c0) = make_float4(acc0, acc1, acc2, acc3);
+  }
+  __syncthreads();
+  // steps 3-5: T_ij = - sum_{k=j}^{i-1} B_ik T_kj for block distance d = i - j
+#pragma unroll
+  for (int d = 1; d < 4; ++d) {
+    const int per = 2 * (4 - d);
+    for (int task = warp; task < per * G; task += kWarps) {
+      const int g = task / per, w = task - per * g;
+      float* sT = reinterpret_cast<float*>(base + g * kHeadBuf + kTriBytes);
+      const float* sB = reinterpret_cast<const float*>(base + g * kHeadBuf + 2 * kTriBytes);
+      const int i = d + (w >> 1), jb = i - d;
+      const int r = (w & 1) * 8 + (lane >> 2);
+      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < d; ++kk) {
+        const int k = jb + kk;
+        const float* Bik = sB + pair_index(i, k) * 320 + r * 20;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const float a = Bik[u];
+          const float4 bv = *reinterpret_cast<const float4*>(sT + tri(k * 16 + u, jb * 16 + c0));
+          acc0 = fmaf(a, bv.x, acc0);
+          acc1 = fmaf(a, bv.y, acc1);
+          acc2 = fmaf(a, bv.z, acc2);
+          acc3 = fmaf(a, bv.w, acc3);
+        }
+      }
+      *reinterpret_cast<float4*>(sT + tri(i * 16 + r, jb * 16 + c0)) = make_float4(-acc0, -acc1, -acc2, -acc3);
+    }
+    __syncthreads();
+  }
+}
+
 // One CTA per (chunk, K head); grid (chunks bound, Hk).  Thread (row, part) owns Gram row `row`
-// (rows 0..63: key t, the A side; rows 64..127: query t, the P side) and kW of its columns.
+// (rows 0..63: key t, the A side; rows 64..127: query t, the P side) and kW of its columns.  The
+// V heads of the K head are processed kGroup at a time.
 __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_constant__ PrepParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -145,14 +238,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
   }
   const int L = min(kChunk, seq_e - c0);
 
-  float* s_gam = reinterpret_cast<float*>(sm + PR_VEC);  // cumsum of g (log2 units) of the current V head
-  float* s_beta = s_gam + 64;
-  float* s_ik = s_gam + 128;
-  float* s_iq = s_gam + 192;
-  float* s_part = s_gam + 256;
-  float* sA = reinterpret_cast<float*>(sm + PR_A);
-  float* sT = reinterpret_cast<float*>(sm + PR_T);
-  float* sB = reinterpret_cast<float*>(sm + PR_B);
+  float* s_gam = reinterpret_cast<float*>(sm + PR_VEC);  // [kGroup][64] cumsum of g, log2 units
+  float* s_beta = s_gam + kGroup * 64;                    // [kGroup][64]
+  float* s_ik = s_beta + kGroup * 64;
+  float* s_iq = s_ik + 64;
+  float* s_part = s_iq + 64;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PR_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PR_BAR + 32);
   const uint32_t bar_qk = smem_u32(&bars[0]), bar_g = smem_u32(&bars[1]);
@@ -170,17 +260,19 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
   const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
   if (tid == 0) issue_qk_tiles(sb + PR_QK, &p.tmap, p.Hk, c0, kh, bar_qk);
 
-  // g, beta of the group's first V head (threads < 64; zero beyond the sequence end)
+  // g, beta of a group of V heads: thread -> (token tid / G, head tid % G), zero past the sequence end
   float g_next = 0.f, b_next = 0.f;
-  auto load_gb = [&](int h) {
+  auto load_gb = [&](int h0, int G) {
     g_next = 0.f;
     b_next = 0.f;
-    if (tid < L) {
-      g_next = __ldg(p.g + (size_t)(c0 + tid) * p.Hv + h);
-      b_next = __ldg(p.beta + (size_t)(c0 + tid) * p.Hv + h);
+    const int t = tid / G;
+    if (tid < 64 * G && t < L) {
+      const size_t o = (size_t)(c0 + t) * p.Hv + h0 + (tid - t * G);
+      g_next = __ldg(p.g + o);
+      b_next = __ldg(p.beta + o);
     }
   };
-  load_gb(kh * ratio);
+  load_gb(kh * ratio, min(kGroup, ratio));
 
   bool ok = mbar_wait(bar_qk, 0, kWaitLimit);
   if (!ok) raise_error(p.err, kErrTimeout);
@@ -226,89 +318,100 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
     }
     const bool got = mbar_wait(bar_g, 0, kWaitLimit);
     if (!got) raise_error(p.err, kErrTimeout);
-    ok = __syncthreads_and(got ? 1 : 0) != 0;
+    ok = __syncthreads_and(got ? 1 : 0) != 0;  // also: the q/k tile is dead from here on
     gram_pending = !ok;
     tc_fence_after();
   }
   if (ok) {
     float gr[kW];  // raw Gram row `row`, columns part * kW ..
     tmem_ld_cols<kW>(tl + part * kW, gr);
-    for (int r = 0; r < ratio; ++r) {
-      const int h = kh * ratio + r;
-      uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * REC_BYTES;
-      if (tid < 64) {
-        s_gam[tid] = g_next * kLog2e;
-        s_beta[tid] = b_next;
+    for (int g0 = 0; g0 < ratio; g0 += kGroup) {
+      const int G = min(kGroup, ratio - g0), h0 = kh * ratio + g0;
+      if (tid < 64 * G) {
+        const int t = tid / G, g = tid - t * G;
+        s_gam[g * 64 + t] = g_next * kLog2e;
+        s_beta[g * 64 + t] = b_next;
       }
       __syncthreads();
-      if (warp == 0) {  // inclusive scan of g over the chunk (lane l holds tokens 2l, 2l + 1)
-        const float g0 = s_gam[2 * lane], g1 = s_gam[2 * lane + 1];
-        float s = g0 + g1;
+      if (warp < G) {  // inclusive scan of g over the chunk (lane l holds tokens 2l, 2l + 1)
+        float* gam = s_gam + warp * 64;
+        const float g0v = gam[2 * lane], g1v = gam[2 * lane + 1];
+        float sc = g0v + g1v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const float v = __shfl_up_sync(0xffffffffu, s, o);
-          if (lane >= o) s += v;
+          const float v = __shfl_up_sync(0xffffffffu, sc, o);
+          if (lane >= o) sc += v;
         }
-        s_gam[2 * lane + 1] = s;
-        s_gam[2 * lane] = s - g1;
+        gam[2 * lane + 1] = sc;
+        gam[2 * lane] = sc - g1v;
       }
       __syncthreads();
-      if (r + 1 < ratio) load_gb(h + 1);  // in flight during this head's work
-      if (tid < 64) {  // per-token factors
-        const int t = tid;
-        const float gt = s_gam[t], gL = s_gam[L - 1];
-        const float Gam = ex2_approx(gt), bt = s_beta[t];
-        float* vec = reinterpret_cast<float*>(rec + REC_VEC);
+      if (g0 + kGroup < ratio) load_gb(h0 + kGroup, min(kGroup, ratio - g0 - kGroup));  // in flight meanwhile
+      if (tid < 64 * G) {  // per-token factors of the G heads
+        const int g = tid >> 6, t = tid & 63;
+        const float* gam = s_gam + g * 64;
+        const float gt = gam[t], gL = gam[L - 1];
+        const float Gam = ex2_approx(gt), bt = s_beta[g * 64 + t];
+        float* vec = reinterpret_cast<float*>(p.rec + ((size_t)gc * p.Hv + h0 + g) * REC_BYTES + REC_VEC);
         vec[V_BETA + t] = bt;
-        vec[V_CX + t] = bt * Gam * s_ik[t];
+        vec[V_NCX + t] = -(bt * Gam * s_ik[t]);
         vec[V_CS + t] = (t < L) ? ex2_approx(gL - gt) * s_ik[t] : 0.f;
         vec[V_CO + t] = Gam * s_iq[t] * p.q_scale;
         vec[V_MISC + t] = (t == 0) ? ex2_approx(gL) : 0.f;
       }
-      // A (rows 0..63, into the solve layout) and P (rows 64..127, straight to the record)
-      if (row < 64) {
-        const int t = row;
-        const float bt = s_beta[t] * s_ik[t], gt = s_gam[t];
+      // A (rows 0..63, blocks on and below the diagonal) and P (rows 64..127, straight to the record)
+      for (int g = 0; g < G; ++g) {
+        const float* gam = s_gam + g * 64;
+        if (row < 64) {
+          const int t = row;
+          float* sA = reinterpret_cast<float*>(sm + PR_HEADS + g * kHeadBuf);
+          const float bt = s_beta[g * 64 + t] * s_ik[t], gt = gam[t];
 #pragma unroll
-        for (int i4 = 0; i4 < kW; i4 += 4) {
-          const int j0 = part * kW + i4;
-          const float4 gj = *reinterpret_cast<const float4*>(s_gam + j0);
-          const float4 kj = *reinterpret_cast<const float4*>(s_ik + j0);
-          const float gv[4] = {gj.x, gj.y, gj.z, gj.w}, kv[4] = {kj.x, kj.y, kj.z, kj.w};
-          float a[4];
+          for (int i4 = 0; i4 < kW; i4 += 4) {
+            const int j0 = part * kW + i4;
+            if ((j0 >> 4) > (t >> 4)) continue;  // above the diagonal blocks: never read
+            const float4 gj = *reinterpret_cast<const float4*>(gam + j0);
+            const float4 kj = *reinterpret_cast<const float4*>(s_ik + j0);
+            const float gv[4] = {gj.x, gj.y, gj.z, gj.w}, kv[4] = {kj.x, kj.y, kj.z, kj.w};
+            float a[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float val = bt * ex2_approx(gt - gv[u]) * gr[i4 + u] * kv[u];
-            a[u] = (j0 + u < t) ? val : 0.f;
+            for (int u = 0; u < 4; ++u) {
+              const float val = bt * ex2_approx(gt - gv[u]) * gr[i4 + u] * kv[u];
+              a[u] = (j0 + u < t) ? val : 0.f;
+            }
+            *reinterpret_cast<float4*>(sA + tri(t, j0)) = make_float4(a[0], a[1], a[2], a[3]);
           }
-          *reinterpret_cast<float4*>(sA + tidx(t, j0)) = make_float4(a[0], a[1], a[2], a[3]);
-        }
-      } else {
-        const int t = row - 64;
-        const float qt = s_iq[t] * p.q_scale, gt = s_gam[t];
+        } else {
+          const int t = row - 64;
+          uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h0 + g) * REC_BYTES;
+          const float qt = s_iq[t] * p.q_scale, gt = gam[t];
 #pragma unroll
-        for (int i0 = 0; i0 < kW; i0 += 8) {
-          float v[8];
-          const int j0 = part * kW + i0;
+          for (int i0 = 0; i0 < kW; i0 += 8) {
+            float v[8];
+            const int j0 = part * kW + i0;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const float a = qt * ex2_approx(gt - s_gam[j0 + u]) * gr[i0 + u] * s_ik[j0 + u];
-            v[u] = (j0 + u <= t) ? a : 0.f;
+            for (int u = 0; u < 8; ++u) {
+              const float a = qt * ex2_approx(gt - gam[j0 + u]) * gr[i0 + u] * s_ik[j0 + u];
+              v[u] = (j0 + u <= t) ? a : 0.f;
+            }
+            store8_split(rec + REC_P, nullptr, 0, t, j0, v);
           }
-          store8_split(rec + REC_P, nullptr, 0, t, j0, v);
         }
       }
       __syncthreads();
-      solve_unit_lower(sA, sT, sB, tid);
-      for (int i = tid; i < 64 * 8; i += kThreads) {
-        const int t = i >> 3, k0 = (i & 7) * 8;
+      solve_tri_batched(sm + PR_HEADS, G, tid);
+      for (int i = tid; i < 64 * 8 * G; i += kThreads) {
+        const int g = i >> 9, t = (i >> 3) & 63, k0 = (i & 7) * 8;
+        const float* sT = reinterpret_cast<const float*>(sm + PR_HEADS + g * kHeadBuf + kTriBytes);
+        uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h0 + g) * REC_BYTES;
         const bool upper = (k0 >> 4) > (t >> 4);  // strictly upper blocks of T are zero
         const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 v0 = upper ? z4 : *reinterpret_cast<const float4*>(sT + tidx(t, k0));
-        const float4 v1 = upper ? z4 : *reinterpret_cast<const float4*>(sT + tidx(t, k0 + 4));
+        const float4 v0 = upper ? z4 : *reinterpret_cast<const float4*>(sT + tri(t, k0));
+        const float4 v1 = upper ? z4 : *reinterpret_cast<const float4*>(sT + tri(t, k0 + 4));
         const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
         store8_split(rec + REC_T, rec + REC_T + 8192, 0, t, k0, v);
       }
+      __syncthreads();  // T reads done before the next group's A writes
     }
   }
   // leave only after the Gram MMA and the tile load have landed (bounded, after an early exit)
@@ -374,6 +477,13 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
     if (!got) raise_error(p.err, kErrTimeout);
     ok = __syncthreads_and(got ? 1 : 0) != 0 && ok;
   };
+  auto wait_two = [&](uint32_t bar_a, uint32_t& ph_a, uint32_t bar_b, uint32_t& ph_b) {  // one barrier for both
+    const bool got = mbar_wait(bar_a, ph_a, kWaitLimit) && mbar_wait(bar_b, ph_b, kWaitLimit);
+    ph_a ^= 1u;
+    ph_b ^= 1u;
+    if (!got) raise_error(p.err, kErrTimeout);
+    ok = __syncthreads_and(got ? 1 : 0) != 0 && ok;
+  };
   auto await_mma = [&](uint32_t bar) {
     uint32_t ph = ph_mma;
     wait_bar(bar, ph);
@@ -397,6 +507,16 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
     bulk_load(sb + SS_T, rec + REC_T, kRecTP, bar_rec);
     bulk_load(sb + SS_VEC + vb * kRecVec, rec + REC_VEC, kRecVec, bar_rec);
   };
+  // L2 prefetch of a chunk's operands, issued one chunk (or, for z, one chain) ahead of their loads
+  auto prefetch_inputs = [&](int c0, int gc, int kh, int h) {
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+      tma_prefetch_2d(&p.tmap, p.Hk * kHeadDim + kh * kHeadDim + kb * 64, c0);
+      tma_prefetch_2d(&p.tmap, kh * kHeadDim + kb * 64, c0);
+      tma_prefetch_2d(&p.tmap, 2 * p.Hk * kHeadDim + h * kHeadDim + kb * 64, c0);
+    }
+    bulk_prefetch_l2(p.rec + ((size_t)gc * p.Hv + h) * REC_BYTES, REC_BYTES);
+  };
   // S0 columns [k0, k0 + 64) -> hi/lo operand tiles (64 keys = one K block); state <- Gamma_L S0 there
   auto convert_half = [&](int k0, float gL) {
     float v[kW];
@@ -404,7 +524,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
 #pragma unroll
     for (int q = 0; q < kW / 8; ++q) store8_split(sm + SS_W, sm + SS_W + 16384, 0, row, part * kW + 8 * q, v + 8 * q);
 #pragma unroll
-    for (int i = 0; i < kW; ++i) v[i] *= gL;
+    for (int i = 0; i < kW; i += 2) {
+      const float2 m = __fmul2_rn(make_float2(v[i], v[i + 1]), make_float2(gL, gL));
+      v[i] = m.x;
+      v[i + 1] = m.y;
+    }
     tmem_st32(tl + SC_S + k0 + part * kW, v);
   };
 
@@ -460,23 +584,23 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       const bool has_next = c0 + kChunk < seq_e;
       const float* vec = reinterpret_cast<const float*>(sm + SS_VEC + vb * kRecVec);
 
-      wait_bar(bar_rec, ph_rec);
-      pend_rec = false;
-      wait_bar(bar_qk, ph_qk);
-      pend_qk = false;
+      wait_two(bar_rec, ph_rec, bar_qk, ph_qk);
+      pend_rec = pend_qk = false;
       if (!ok) break;
       const float gL = vec[V_MISC];
+      if (tid == 0) {
+        if (gated) tma_prefetch_2d(&p.tmap_z, h * kHeadDim, c0);  // read by this chunk's output stage
+        if (has_next) prefetch_inputs(c0 + kChunk, gc + 1, kh, h);
+      }
 
-      // ================= [X | O1] = S0 [K; Q]^T, hi + lo, one 64-key half at a time
+      // ================= [X | O1] = S0 [K; Q]^T one 64-key half at a time: X from the hi and lo
+      // parts of S0, the output-only O1 from the hi part
       convert_half(0, gL);
       operands_ready();
       if (tid == 0) {
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bkq = sw128_desc(sb + SS_QK + ks * 32);
-          mma_bf16(tmem + SC_X, sw128_desc(sb + SS_W + ks * 32), bkq, ID128, ks > 0);
-          mma_bf16(tmem + SC_X, sw128_desc(sb + SS_W + 16384 + ks * 32), bkq, ID128, 1);
-        }
+        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W), sw128_desc(sb + SS_QK), ID128, 0);
+        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W + 16384), sw128_desc(sb + SS_QK), ID64, 1);
         mma_commit(bar_h);
       }
       await_mma(bar_h);
@@ -485,15 +609,15 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       operands_ready();
       if (tid == 0) {
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bkq = sw128_desc(sb + SS_QK + 16384 + ks * 32);
-          mma_bf16(tmem + SC_X, sw128_desc(sb + SS_W + ks * 32), bkq, ID128, 1);
-          mma_bf16(tmem + SC_X, sw128_desc(sb + SS_W + 16384 + ks * 32), bkq, ID128, 1);
-        }
+        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W), sw128_desc(sb + SS_QK + 16384), ID128, 1);
+        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W + 16384), sw128_desc(sb + SS_QK + 16384), ID64, 1);
         mma_commit(bar_x);
       }
-      await_mma(bar_x);
-      wait_bar(bar_v, ph_v);
+      {
+        uint32_t ph = ph_mma;
+        wait_two(bar_x, ph, bar_v, ph_v);
+        tc_fence_after();
+      }
       pend_v = false;
       if (!ok) break;
 
@@ -501,19 +625,21 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       {
         float x[kW];
         tmem_ld_cols<kW>(tl + SC_X + part * kW, x);
+        // V[t][row] for t = part * kW + i: the swizzle term depends on i & 7 only
         const uint8_t* vbase = sm + SS_V + (row >> 6) * 8192 + part * kW * 128 + ((row & 7) << 1);
         const int rsw = (row >> 3) & 7;
+        auto v_at = [&](int i) {
+          return bf2f(*reinterpret_cast<const uint16_t*>(vbase + i * 128 + ((rsw ^ (i & 7)) << 4)));
+        };
 #pragma unroll
         for (int i4 = 0; i4 < kW; i4 += 4) {
           const float4 bt = *reinterpret_cast<const float4*>(vec + V_BETA + part * kW + i4);
-          const float4 cx = *reinterpret_cast<const float4*>(vec + V_CX + part * kW + i4);
-          const float btv[4] = {bt.x, bt.y, bt.z, bt.w}, cxv[4] = {cx.x, cx.y, cx.z, cx.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i4 + u;
-            const float v = bf2f(*reinterpret_cast<const uint16_t*>(vbase + i * 128 + ((rsw ^ (i & 7)) << 4)));
-            x[i] = btv[u] * v - cxv[u] * x[i];
-          }
+          const float4 nc = *reinterpret_cast<const float4*>(vec + V_NCX + part * kW + i4);
+          const float2 r0 = __ffma2_rn(make_float2(nc.x, nc.y), make_float2(x[i4], x[i4 + 1]),
+                                       __fmul2_rn(make_float2(bt.x, bt.y), make_float2(v_at(i4), v_at(i4 + 1))));
+          const float2 r1 = __ffma2_rn(make_float2(nc.z, nc.w), make_float2(x[i4 + 2], x[i4 + 3]),
+                                       __fmul2_rn(make_float2(bt.z, bt.w), make_float2(v_at(i4 + 2), v_at(i4 + 3))));
+          x[i4] = r0.x; x[i4 + 1] = r0.y; x[i4 + 2] = r1.x; x[i4 + 3] = r1.y;
         }
 #pragma unroll
         for (int q = 0; q < kW / 8; ++q) store8_split(sm + SS_W, sm + SS_W + 16384, 0, row, part * kW + 8 * q, x + 8 * q);
@@ -523,13 +649,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
         if (has_next) issue_v(c0 + kChunk, h);
         // E^T = R T^T  (hi*hi + hi*lo + lo*hi)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t off = ks * 32;
-          const uint64_t rh = sw128_desc(sb + SS_W + off), rl = sw128_desc(sb + SS_W + 16384 + off);
-          mma_bf16(tmem + SC_X, rh, sw128_desc(sb + SS_T + off), ID64, ks > 0);
-          mma_bf16(tmem + SC_X, rh, sw128_desc(sb + SS_T + 8192 + off), ID64, 1);
-          mma_bf16(tmem + SC_X, rl, sw128_desc(sb + SS_T + off), ID64, 1);
-        }
+        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W), sw128_desc(sb + SS_T), ID64, 0);
+        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W), sw128_desc(sb + SS_T + 8192), ID64, 1);
+        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W + 16384), sw128_desc(sb + SS_T), ID64, 1);
         mma_commit(bar_e);
       }
       pend_v = has_next;
@@ -545,8 +667,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
           const float4 c0v = *reinterpret_cast<const float4*>(vec + V_CS + part * kW + 8 * q);
           const float4 c1v = *reinterpret_cast<const float4*>(vec + V_CS + part * kW + 8 * q + 4);
           const float* e8 = ev + 8 * q;
-          const float es[8] = {e8[0] * c0v.x, e8[1] * c0v.y, e8[2] * c0v.z, e8[3] * c0v.w,
-                               e8[4] * c1v.x, e8[5] * c1v.y, e8[6] * c1v.z, e8[7] * c1v.w};
+          const float2 p0 = __fmul2_rn(make_float2(e8[0], e8[1]), make_float2(c0v.x, c0v.y));
+          const float2 p1 = __fmul2_rn(make_float2(e8[2], e8[3]), make_float2(c0v.z, c0v.w));
+          const float2 p2 = __fmul2_rn(make_float2(e8[4], e8[5]), make_float2(c1v.x, c1v.y));
+          const float2 p3 = __fmul2_rn(make_float2(e8[6], e8[7]), make_float2(c1v.z, c1v.w));
+          const float es[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
           store8_split(sm + SS_W, sm + SS_W + 16384, 0, row, part * kW + 8 * q, es);
           store8_split(sm + SS_T, nullptr, 0, row, part * kW + 8 * q, e8);
         }
@@ -554,13 +679,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       operands_ready();
       if (tid == 0) {
         // S += E~ K: B = the raw k rows of the q/k tile read MN-major (N = 128 keys, 16 tokens per step)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bk = sw128_mn_desc(sb + SS_QK + ks * 2048, 16384);
-          mma_bf16(tmem + SC_S, sw128_desc(sb + SS_W + ks * 32), bk, ID128_BMN, 1);
-          mma_bf16(tmem + SC_S, sw128_desc(sb + SS_W + 16384 + ks * 32), bk, ID128_BMN, 1);
-          mma_bf16(tmem + SC_X, sw128_desc(sb + SS_T + ks * 32), sw128_desc(sb + SS_P + ks * 32), ID64, ks > 0);
-        }
+        mma_bf16_k4<2, 128>(tmem + SC_S, sw128_desc(sb + SS_W), sw128_mn_desc(sb + SS_QK, 16384), ID128_BMN, 1);
+        mma_bf16_k4<2, 128>(tmem + SC_S, sw128_desc(sb + SS_W + 16384), sw128_mn_desc(sb + SS_QK, 16384), ID128_BMN, 1);
+        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_T), sw128_desc(sb + SS_P), ID64, 0);
         mma_commit(bar_s);
       }
       // the gate input of this thread's output elements, in flight during the MMAs
@@ -586,16 +707,19 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
 #pragma unroll
       for (int hh = 0; hh < kW; hh += 16) {  // 16 columns at a time: the gate inputs stay in registers
         float o1[16], o2[16];
-        tmem_ld16(tl + SC_O1 + part * kW + hh, o1);
-        tmem_ld16(tl + SC_X + part * kW + hh, o2);
+        tmem_ld16x2(tl + SC_O1 + part * kW + hh, tl + SC_X + part * kW + hh, o1, o2);
 #pragma unroll
         for (int i4 = 0; i4 < 16; i4 += 4) {
           const int t0 = part * kW + hh + i4;
           const float4 co = *reinterpret_cast<const float4*>(vec + V_CO + t0);
-          s_work[t0 * 128 + row] = fmaf(o1[i4], co.x, o2[i4]);
-          s_work[(t0 + 1) * 128 + row] = fmaf(o1[i4 + 1], co.y, o2[i4 + 1]);
-          s_work[(t0 + 2) * 128 + row] = fmaf(o1[i4 + 2], co.z, o2[i4 + 2]);
-          s_work[(t0 + 3) * 128 + row] = fmaf(o1[i4 + 3], co.w, o2[i4 + 3]);
+          const float2 a = __ffma2_rn(make_float2(o1[i4], o1[i4 + 1]), make_float2(co.x, co.y),
+                                      make_float2(o2[i4], o2[i4 + 1]));
+          const float2 b = __ffma2_rn(make_float2(o1[i4 + 2], o1[i4 + 3]), make_float2(co.z, co.w),
+                                      make_float2(o2[i4 + 2], o2[i4 + 3]));
+          s_work[t0 * 128 + row] = a.x;
+          s_work[(t0 + 1) * 128 + row] = a.y;
+          s_work[(t0 + 2) * 128 + row] = b.x;
+          s_work[(t0 + 3) * 128 + row] = b.y;
         }
       }
       __syncthreads();
@@ -618,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
             const float zf[4] = {__uint_as_float(zr[i].x << 16), __uint_as_float(zr[i].x & 0xFFFF0000u),
                                  __uint_as_float(zr[i].y << 16), __uint_as_float(zr[i].y & 0xFFFF0000u)};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) r[i][e] = r[i][e] * rstd * wf[e] * sigmoid_fast(zf[e]);
+            for (int e = 0; e < 4; ++e) r[i][e] = r[i][e] * rstd * wf[e] * sigmoid_tanh(zf[e]);
           }
         }
 #pragma unroll
@@ -723,10 +847,11 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
   if (N <= 0) return cudaSuccess;
   const SplitLayout lay = split_layout(workspace, N);
   const long nc_max = chunk_bound(N, T);
-  CUtensorMap tmap;
+  CUtensorMap tmap, tmap_z;
   memset(&tmap, 0, sizeof tmap);
+  memset(&tmap_z, 0, sizeof tmap_z);
   if (T > 0) {
-    cudaError_t e = encode_chunk_tensor_maps(&tmap, nullptr, qkv, nullptr, T, Hk, Hv);
+    cudaError_t e = encode_chunk_tensor_maps(&tmap, &tmap_z, qkv, z, T, Hk, Hv);
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = launch_chunk_schedule(env.stream, cu, N, lay.order, lay.counter, lay.chunk_off);
@@ -747,6 +872,7 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
   StateParams sp;
   memset(&sp, 0, sizeof sp);
   sp.tmap = tmap;
+  sp.tmap_z = tmap_z;
   sp.cu = cu; sp.order = lay.order; sp.counter = lay.counter; sp.chunk_off = lay.chunk_off; sp.rec = lay.rec;
   sp.state_in = state_in; sp.state_out = state_out; sp.z = z; sp.norm_w = norm_w; sp.out = out; sp.err = env.err;
   sp.N = N; sp.T = T; sp.Hk = Hk; sp.Hv = Hv; sp.nc_max = (int)nc_max; sp.rms_eps = rms_eps;

@@ -48,6 +48,14 @@ __device__ __forceinline__ float rcp_approx(float x) {
 }
 // sigmoid(x) = 1 / (1 + e^-x) from the two approximations above (output-side gate only)
 __device__ __forceinline__ float sigmoid_fast(float x) { return rcp_approx(1.0f + ex2_approx(-x * kLog2e)); }
+// hardware tanh approximation (max relative error about 2^-11)
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// sigmoid(x) = (1 + tanh(x / 2)) / 2: one special-function operation
+__device__ __forceinline__ float sigmoid_tanh(float x) { return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f); }
 
 __device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
@@ -102,6 +110,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+// L2 prefetch hints (no completion to wait for): a 2D tensor box, or `bytes` (multiple of 16,
+// 16-byte aligned) of contiguous global memory.
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // ------------------------------------------------------------------ proxy / tcgen05 fences
@@ -163,6 +181,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Two 16-column loads (for example of two accumulators) behind one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)[16], float (&b)[16]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(r[16 + i]);
+  }
 }
 
 // N (16 or 32) columns of this warp's 32 lanes.
@@ -249,6 +290,27 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "setp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four consecutive K = 16 steps of one accumulation, issued back to back: the A and B descriptors
+// advance by AS and BS descriptor units (16 bytes) per step.  The first step accumulates onto D
+// when `acc_first` is nonzero, the other three always do.
+template <uint32_t AS, uint32_t BS>
+__device__ __forceinline__ void mma_bf16_k4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t acc_first) {
+  asm volatile(
+      "{\n.reg .pred p, q;\n.reg .b64 a1, a2, a3, b1, b2, b3;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "setp.ne.b32 q, %5, 0;\n"
+      "add.s64 a1, %1, %6;\nadd.s64 a2, %1, %7;\nadd.s64 a3, %1, %8;\n"
+      "add.s64 b1, %2, %9;\nadd.s64 b2, %2, %10;\nadd.s64 b3, %2, %11;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, q;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, q;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, q;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc_first), "r"(1u), "n"(AS), "n"(2 * AS), "n"(3 * AS), "n"(BS),
+      "n"(2 * BS), "n"(3 * BS)
       : "memory");
 }
 

@@ -63,7 +63,7 @@ constexpr uint32_t SS_QK = 0;         // 32 KB [K; Q] tile (TMA)
 constexpr uint32_t SS_W = 32768;      // 32 KB: S0 key-half hi/lo, then R hi/lo, then E~ hi/lo, then output staging
 constexpr uint32_t SS_T = 65536;      // 16 KB T hi/lo (record), then E bf16
 constexpr uint32_t SS_P = 81920;      //  8 KB P (record; follows T so one bulk copy fills both)
-constexpr uint32_t SS_V = 90112;      // 16 KB V (TMA)
+constexpr uint32_t SS_V = 90112;      // 16 KB V (TMA), then z of the chunk (TMA; gate input of the output stage)
 constexpr uint32_t SS_VEC = 106496;   // 2 x per-token vector block (double buffered)
 constexpr uint32_t SS_BAR = SS_VEC + 2 * kRecVec;
 constexpr uint32_t SS_USED = SS_BAR + 128;
@@ -156,6 +156,29 @@ __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
   }
   __syncthreads();
   const int c0 = (lane & 3) * 4;
+  // Row u of a 16 x 16 block, columns c0..c0+3: float4 offset u * 16 + lane_off[u & 3] (the XOR
+  // swizzle of the row's float4 index by u & 3, resolved per lane once).
+  int lane_off[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) lane_off[m] = (((c0 >> 2) ^ m) << 2);
+  // 16 entries of row r of a tri-layout block (four float4 reads)
+  auto tri_row = [&](const float* blk, int r, float (&v)[16]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 f = *reinterpret_cast<const float4*>(blk + r * 16 + ((q ^ (r & 3)) << 2));
+      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+    }
+  };
+  // acc (two chains of four columns) += sum_u a[u] * blk[u][c0..c0+3]
+  auto row_times_block = [&](const float (&a)[16], const float* blk, float2 (&acc)[4]) {
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float4 bv = *reinterpret_cast<const float4*>(blk + u * 16 + lane_off[u & 3]);
+      float2* ac = acc + 2 * (u & 1);
+      ac[0] = __ffma2_rn(make_float2(a[u], a[u]), make_float2(bv.x, bv.y), ac[0]);
+      ac[1] = __ffma2_rn(make_float2(a[u], a[u]), make_float2(bv.z, bv.w), ac[1]);
+    }
+  };
   // step 2: B_ik = T_ii A_ik, twelve half-block tasks per head
   for (int task = warp; task < 12 * G; task += kWarps) {
     const int g = task / 12, tt = task - 12 * g;
@@ -165,17 +188,12 @@ __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
     const int pidx = tt >> 1;
     const int i = pidx < 1 ? 1 : (pidx < 3 ? 2 : 3), k = pidx - pair_index(i, 0);
     const int rr = (tt & 1) * 8 + (lane >> 2);
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const float a = sT[tri(i * 16 + rr, i * 16 + u)];
-      const float4 bv = *reinterpret_cast<const float4*>(sA + tri(i * 16 + u, k * 16 + c0));
-      acc0 = fmaf(a, bv.x, acc0);
-      acc1 = fmaf(a, bv.y, acc1);
-      acc2 = fmaf(a, bv.z, acc2);
-      acc3 = fmaf(a, bv.w, acc3);
-    }
-    *reinterpret_cast<float4*>(sB + pidx * 320 + rr * 20 + c0) = make_float4(acc0, acc1, acc2, acc3);
+    float a[16];
+    tri_row(sT + (i * (i + 1) / 2 + i) * 256, rr, a);  // row rr of T_ii (zero above the diagonal)
+    float2 acc[4] = {};
+    row_times_block(a, sA + (i * (i + 1) / 2 + k) * 256, acc);
+    *reinterpret_cast<float4*>(sB + pidx * 320 + rr * 20 + c0) =
+        make_float4(acc[0].x + acc[2].x, acc[0].y + acc[2].y, acc[1].x + acc[3].x, acc[1].y + acc[3].y);
   }
   __syncthreads();
   // steps 3-5: T_ij = - sum_{k=j}^{i-1} B_ik T_kj for block distance d = i - j
@@ -188,22 +206,21 @@ __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
       const float* sB = reinterpret_cast<const float*>(base + g * kHeadBuf + 2 * kTriBytes);
       const int i = d + (w >> 1), jb = i - d;
       const int r = (w & 1) * 8 + (lane >> 2);
-      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+      float2 acc[4] = {};
 #pragma unroll
       for (int kk = 0; kk < d; ++kk) {
         const int k = jb + kk;
         const float* Bik = sB + pair_index(i, k) * 320 + r * 20;
+        float a[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float a = Bik[u];
-          const float4 bv = *reinterpret_cast<const float4*>(sT + tri(k * 16 + u, jb * 16 + c0));
-          acc0 = fmaf(a, bv.x, acc0);
-          acc1 = fmaf(a, bv.y, acc1);
-          acc2 = fmaf(a, bv.z, acc2);
-          acc3 = fmaf(a, bv.w, acc3);
+        for (int q = 0; q < 4; ++q) {
+          const float4 f = *reinterpret_cast<const float4*>(Bik + 4 * q);
+          a[4 * q] = f.x; a[4 * q + 1] = f.y; a[4 * q + 2] = f.z; a[4 * q + 3] = f.w;
         }
+        row_times_block(a, sT + (k * (k + 1) / 2 + jb) * 256, acc);
       }
-      *reinterpret_cast<float4*>(sT + tri(i * 16 + r, jb * 16 + c0)) = make_float4(-acc0, -acc1, -acc2, -acc3);
+      *reinterpret_cast<float4*>(sT + tri(i * 16 + r, jb * 16 + c0)) =
+          make_float4(-(acc[0].x + acc[2].x), -(acc[0].y + acc[2].y), -(acc[1].x + acc[3].x), -(acc[1].y + acc[3].y));
     }
     __syncthreads();
   }
@@ -323,8 +340,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
     tc_fence_after();
   }
   if (ok) {
-    float gr[kW];  // raw Gram row `row`, columns part * kW ..
-    tmem_ld_cols<kW>(tl + part * kW, gr);
     for (int g0 = 0; g0 < ratio; g0 += kGroup) {
       const int G = min(kGroup, ratio - g0), h0 = kh * ratio + g0;
       if (tid < 64 * G) {
@@ -359,8 +374,20 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
         vec[V_CO + t] = Gam * s_iq[t] * p.q_scale;
         vec[V_MISC + t] = (t == 0) ? ex2_approx(gL) : 0.f;
       }
-      // A (rows 0..63, blocks on and below the diagonal) and P (rows 64..127, straight to the record)
-      for (int g = 0; g < G; ++g) {
+      // A (rows 0..63, blocks on and below the diagonal) and P (rows 64..127, straight to the record);
+      // the warps whose 32 rows and 32 columns all lie above the diagonal (token j > t) have no work
+      float gr[kW];  // raw Gram row `row`, columns part * kW ..
+      tmem_ld_cols<kW>(tl + part * kW, gr);
+      const bool all_masked = part == 1 && (q4 & 1) == 0;
+      if (all_masked && row >= 64) {  // P is zero there (A's blocks above the diagonal are never read)
+        const float zero8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int g = 0; g < G; ++g) {
+          uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h0 + g) * REC_BYTES;
+#pragma unroll
+          for (int i0 = 0; i0 < kW; i0 += 8) store8_split(rec + REC_P, nullptr, 0, row - 64, part * kW + i0, zero8);
+        }
+      }
+      for (int g = 0; g < G && !all_masked; ++g) {
         const float* gam = s_gam + g * 64;
         if (row < 64) {
           const int t = row;
@@ -444,10 +471,10 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
   int* item_slot = reinterpret_cast<int*>(sm + SS_BAR + 72);
   const uint32_t bar_qk = smem_u32(&bars[0]), bar_v = smem_u32(&bars[1]), bar_rec = smem_u32(&bars[2]),
                  bar_h = smem_u32(&bars[3]), bar_x = smem_u32(&bars[4]), bar_e = smem_u32(&bars[5]),
-                 bar_s = smem_u32(&bars[6]);
+                 bar_s = smem_u32(&bars[6]), bar_z = smem_u32(&bars[7]);
 
   if (tid == 0) {
-    for (int i = 0; i < 7; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&bars[i]), 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), SC_COLS);
@@ -461,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
   constexpr uint32_t ID128 = idesc_bf16_f32(128, 128);
   constexpr uint32_t ID128_BMN = idesc_bf16_f32_bmn(128, 128);
   bool ok = true;
-  uint32_t ph_mma = 0, ph_qk = 0, ph_v = 0, ph_rec = 0;
-  bool pend_qk = false, pend_v = false, pend_rec = false;
+  uint32_t ph_mma = 0, ph_qk = 0, ph_v = 0, ph_rec = 0, ph_z = 0;
+  bool pend_qk = false, pend_v = false, pend_rec = false, pend_z = false;
   const bool gated = p.z != nullptr;
   float wf[4] = {1.f, 1.f, 1.f, 1.f};
   if (gated) {
@@ -500,6 +527,10 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb)
       tma_load_2d(sb + SS_V + kb * 8192, &p.tmap, 2 * p.Hk * kHeadDim + h * kHeadDim + kb * 64, c0, bar_v);
+  };
+  auto issue_z = [&](int c0, int h) {  // into the V buffer, once R has consumed V
+    mbar_arrive_expect_tx(bar_z, kBytesZ);
+    tma_load_2d(sb + SS_V, &p.tmap_z, h * kHeadDim, c0, bar_z);
   };
   auto issue_rec = [&](int gc, int h, int vb) {
     const uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * REC_BYTES;
@@ -646,15 +677,17 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       }
       operands_ready();
       if (tid == 0) {
-        if (has_next) issue_v(c0 + kChunk, h);
+        // the V buffer is free: the gate input of this chunk (gated), else the next chunk's v
+        if (gated) issue_z(c0, h);
+        else if (has_next) issue_v(c0 + kChunk, h);
         // E^T = R T^T  (hi*hi + hi*lo + lo*hi)
-#pragma unroll
         mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W), sw128_desc(sb + SS_T), ID64, 0);
         mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W), sw128_desc(sb + SS_T + 8192), ID64, 1);
         mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W + 16384), sw128_desc(sb + SS_T), ID64, 1);
         mma_commit(bar_e);
       }
-      pend_v = has_next;
+      pend_z = gated;
+      pend_v = !gated && has_next;
       await_mma(bar_e);
       if (!ok) break;
 
@@ -684,17 +717,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
         mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_T), sw128_desc(sb + SS_P), ID64, 0);
         mma_commit(bar_s);
       }
-      // the gate input of this thread's output elements, in flight during the MMAs
       constexpr int kTok = kChunk / kWarps;
-      uint2 zr[kTok];
-      if (gated) {
-#pragma unroll
-        for (int i = 0; i < kTok; ++i) {
-          const int t = warp + kWarps * i;
-          zr[i] = t < L ? __ldg(reinterpret_cast<const uint2*>(p.z + ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4))
-                        : make_uint2(0u, 0u);
-        }
-      }
       await_mma(bar_s);
       if (!ok) break;
       if (tid == 0 && has_next) {
@@ -722,7 +745,13 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
           s_work[(t0 + 3) * 128 + row] = b.y;
         }
       }
-      __syncthreads();
+      if (gated) {
+        wait_bar(bar_z, ph_z);
+        pend_z = false;
+        if (!ok) break;
+      } else {
+        __syncthreads();
+      }
       {
         float r[kTok][4], ss[kTok];
 #pragma unroll
@@ -739,8 +768,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
 #pragma unroll
           for (int i = 0; i < kTok; ++i) {
             const float rstd = rsqrtf(ss[i] * (1.0f / kHeadDim) + p.rms_eps);
-            const float zf[4] = {__uint_as_float(zr[i].x << 16), __uint_as_float(zr[i].x & 0xFFFF0000u),
-                                 __uint_as_float(zr[i].y << 16), __uint_as_float(zr[i].y & 0xFFFF0000u)};
+            const uint2 zz = *reinterpret_cast<const uint2*>(sm + SS_V + (warp + kWarps * i) * 256 + lane * 8);
+            const float zf[4] = {__uint_as_float(zz.x << 16), __uint_as_float(zz.x & 0xFFFF0000u),
+                                 __uint_as_float(zz.y << 16), __uint_as_float(zz.y & 0xFFFF0000u)};
 #pragma unroll
             for (int e = 0; e < 4; ++e) r[i][e] = r[i][e] * rstd * wf[e] * sigmoid_tanh(zf[e]);
           }
@@ -755,10 +785,14 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
           }
         }
       }
-      fence_proxy_async_smem();  // vector-block reads precede the bulk copy that refills the buffer
+      fence_proxy_async_smem();  // vector-block and z reads precede the copies that refill those buffers
       tc_fence_before();
       __syncthreads();  // staging reads and accumulator reads done before the next chunk reuses them
       tc_fence_after();
+      if (gated && has_next) {
+        if (tid == 0) issue_v(c0 + kChunk, h);
+        pend_v = true;
+      }
     }
     if (!ok) break;
 
@@ -784,6 +818,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
   if (pend_qk) mbar_wait(bar_qk, ph_qk, kWaitLimit);
   if (pend_v) mbar_wait(bar_v, ph_v, kWaitLimit);
   if (pend_rec) mbar_wait(bar_rec, ph_rec, kWaitLimit);
+  if (pend_z) mbar_wait(bar_z, ph_z, kWaitLimit);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

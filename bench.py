@@ -317,7 +317,7 @@ def run_ours(args, rank, world, local):
     e2e_value = replica_throughput(T, world, e2e_ms)
     del h_x, h_g, h_b, h_z
 
-    # ---------------- varlen prefill: 8 packed sequences, 32,735 tokens (same path)
+    # ---------------- varlen prefill: 8 packed sequences, 31,735 tokens (same path)
     del x, qkv, z, out, ws
     torch.cuda.empty_cache()
     varlen = None
@@ -350,7 +350,7 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         gdn.gdn_check_device_errors()
         v_ms = max_over_ranks(s4.elapsed_time(e4)) / args.varlen_steps
-        varlen = {"workload": "varlen prefill, 8 packed sequences {1,17,63,64,65,1000,8191,22334} = 32,735 tokens",
+        varlen = {"workload": "varlen prefill, 8 packed sequences {1,17,63,64,65,1000,8191,22334} = 31,735 tokens",
                   "value": world * vT / (v_ms / 1000.0), "unit": "tokens/s", "ms_per_step": v_ms,
                   "steps": args.varlen_steps,
                   "roofline_tokens_per_s": hbm_peak * 1e9 / (CHUNK_BYTES_PER_TOKEN + STATE_BYTES_PER_SEQ * vN / vT)}

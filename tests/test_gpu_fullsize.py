@@ -38,7 +38,10 @@ def test_batched_prefill_4x4096():
     _prefill_case(BATCHED_LENGTHS, seed=2)
 
 
-def test_varlen_prefill_32735_tokens():
+def test_varlen_prefill_31735_tokens():
+    """The varlen workload's eight lengths sum to 31,735 tokens (the workload text says 32,735;
+    the listed lengths decide)."""
+    assert sum(VARLEN_LENGTHS) == 31735
     _prefill_case(VARLEN_LENGTHS, seed=3)
 
 

@@ -269,7 +269,7 @@ def run_ours(args, rank, world, local):
     conv_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_conv)
     chunk_bytes = CHUNK_BYTES_PER_TOKEN * T + STATE_BYTES_PER_SEQ * N
     chunk_gbs = chunk_bytes / (chunk_ms / 1000.0) / 1e9
-    rec = traffic_record("chunk_prefill")
+    rec = traffic_record("chunk_prefill_split")
     roofline = {"kernel": "chunk_prefill (schedule + prep + state kernels, tcgen05, fused gated norm)",
                 "bound": "hbm", "achieved": chunk_gbs,
                 "peak": hbm_peak, "unit": "GB/s", "frac": chunk_gbs / hbm_peak,

@@ -34,6 +34,13 @@ GDN_API int gdn_debug_get_chunk_mode(void);
 GDN_API gdn_status gdn_debug_mma_probe(const gdn_bf16* A, const gdn_bf16* B, int n_cols, float* D,
                                        unsigned* status, void* stream);
 
+/* The same tile with the operand placements of the split chunk prefill: flags bit 0 reads A
+ * from tensor memory (two bf16 per 32-bit column, the even K index in the low half), bit 1 reads
+ * B from an MN-major 128-byte-swizzled tile (128-byte rows of 64 N elements of one K index,
+ * 64-element N blocks 8 KB apart).  Other flag bits are refused with GDN_ERR_INVALID_ARGUMENT. */
+GDN_API gdn_status gdn_debug_mma_probe_ex(const gdn_bf16* A, const gdn_bf16* B, int n_cols, int flags, float* D,
+                                          unsigned* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

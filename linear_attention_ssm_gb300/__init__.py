@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     gdn_conv1d_prefill,
     gdn_debug_get_chunk_mode,
     gdn_debug_mma_probe,
+    gdn_debug_mma_probe_ex,
     gdn_debug_set_chunk_mode,
     gdn_decode_step,
     gdn_gated_rmsnorm,

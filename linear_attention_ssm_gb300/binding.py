@@ -63,6 +63,7 @@ def load_library():
             "gdn_debug_set_chunk_mode": ([ctypes.c_int], ctypes.c_int),
             "gdn_debug_get_chunk_mode": ([], ctypes.c_int),
             "gdn_debug_mma_probe": ([P, P, ctypes.c_int, P, P, P], ctypes.c_int),
+            "gdn_debug_mma_probe_ex": ([P, P, ctypes.c_int, ctypes.c_int, P, P, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -239,6 +240,18 @@ def gdn_debug_mma_probe(A, B, stream=None):
     D = torch.full((128, n), float("nan"), dtype=torch.float32, device=A.device)
     status = torch.zeros(1, dtype=torch.int32, device=A.device)
     _check(lib.gdn_debug_mma_probe(_p(A), _p(B), n, _p(D), _p(status), _stream(stream)))
+    return D, status
+
+
+def gdn_debug_mma_probe_ex(A, B, flags, stream=None):
+    """As gdn_debug_mma_probe with flags: bit 0 A from tensor memory, bit 1 B MN-major."""
+    lib = load_library()
+    _dev(A, torch.bfloat16, "A", (128, 64))
+    n = B.shape[0]
+    _dev(B, torch.bfloat16, "B", (n, 64))
+    D = torch.full((128, n), float("nan"), dtype=torch.float32, device=A.device)
+    status = torch.zeros(1, dtype=torch.int32, device=A.device)
+    _check(lib.gdn_debug_mma_probe_ex(_p(A), _p(B), n, int(flags), _p(D), _p(status), _stream(stream)))
     return D, status
 
 

@@ -16,14 +16,16 @@
 // bf16 operand images) and writes them to a per-(chunk, V head) record in the workspace.  The
 // state kernel then runs only the state-dependent chain per chunk:
 //   S0 -> bf16 hi/lo (two key halves)  ->  [X | O1] = S0 [K; Q]^T
-//   R = diag(beta) V - diag(c_x) X^T   ->  E^T = R T^T
-//   E~ = E diag(c_s)                   ->  S = Gamma_L S0 + E~^T K  (K read MN-major from the q/k tile),
-//                                          O2 = E P^T
+//   R = diag(beta) V - diag(c_x) X^T   ->  E^T = R T^T               (R read from tensor memory)
+//   E~ = E diag(c_s)                   ->  S = Gamma_L S0 + E~^T K  (E~ from tensor memory, K read
+//                                          MN-major from the q/k tile), O2 = E P^T
 //   o = O1 diag(c_o) + O2  ->  sigmoid-gated RMSNorm  ->  out
 // with the records fetched by 1D bulk copies and q/k, v by TMA.  The state kernel uses 256 of
 // the 512 tensor-memory columns and ~108 KB of shared memory, so two CTAs share an SM and one
 // CTA's waits hide behind the other's work.
 #include <cuda.h>
+
+#include <mutex>
 
 #include "chunk_common.cuh"
 #include "gdn_common.cuh"
@@ -60,7 +62,7 @@ static_assert(2 * (PR_BYTES + 1024) <= 233472, "two prep CTAs must share an SM")
 
 // ---- state kernel shared memory
 constexpr uint32_t SS_QK = 0;         // 32 KB [K; Q] tile (TMA)
-constexpr uint32_t SS_W = 32768;      // 32 KB: S0 key-half hi/lo, then R hi/lo, then E~ hi/lo, then output staging
+constexpr uint32_t SS_W = 32768;      // 32 KB: S0 key-half hi/lo, then the output staging (o1 c_o, then + O2)
 constexpr uint32_t SS_T = 65536;      // 16 KB T hi/lo (record), then E bf16
 constexpr uint32_t SS_P = 81920;      //  8 KB P (record; follows T so one bulk copy fills both)
 constexpr uint32_t SS_V = 90112;      // 16 KB V (TMA), then z of the chunk (TMA; gate input of the output stage)
@@ -73,9 +75,15 @@ static_assert(SS_P == SS_T + 16384, "T and P must be contiguous");
 
 // ---- state kernel tensor memory columns
 constexpr uint32_t SC_S = 0;      // 128: the recurrent state
-constexpr uint32_t SC_X = 128;    //  64: S0 K^T, then E^T, then E P^T
-constexpr uint32_t SC_O1 = 192;   //  64: S0 Q^T
+constexpr uint32_t SC_X = 128;    //  64: S0 K^T, then R (bf16 hi/lo pairs: MMA operand), then E~ (likewise)
+constexpr uint32_t SC_O1 = 192;   //  64: S0 Q^T, then E^T, then E P^T
 constexpr uint32_t SC_COLS = 256;
+
+// The chunks of sequence n (nch of them) are split into nseg contiguous segments; segment k holds
+// chunk indices [k nch / nseg, (k + 1) nch / nseg).  The prep kernel of segment k + 1 can then run
+// beside the state kernel of segment k.
+__host__ __device__ __forceinline__ int seg_begin(int k, int nch, int nseg) { return (int)(((long)k * nch) / nseg); }
+constexpr int kMaxSegments = 4;
 
 struct PrepParams {
   CUtensorMap tmap;  // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle
@@ -83,13 +91,16 @@ struct PrepParams {
   const float* beta;
   const int32_t* cu;
   const int32_t* chunk_off;
+  const int32_t* seg_pref;  // this segment's exclusive prefix over sequences of their chunk counts [N + 1]
   uint8_t* rec;
   unsigned* err;
-  int N, T, Hk, Hv;
+  int N, T, Hk, Hv, seg, nseg, nc_max;
   float q_scale, l2_eps;
 };
 
 struct StateParams {
+  int seg, nseg;              // chunk segment processed by this launch
+  const float* state_src;     // state at the segment start: state_in (may be NULL) for the first, else state_out
   CUtensorMap tmap;
   CUtensorMap tmap_z;  // z [T][Hv * 128] bf16, box 128 x 64 (valid when z != NULL): L2 prefetch only
   const int32_t* cu;
@@ -226,9 +237,9 @@ __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
   }
 }
 
-// One CTA per (chunk, K head); grid (chunks bound, Hk).  Thread (row, part) owns Gram row `row`
-// (rows 0..63: key t, the A side; rows 64..127: query t, the P side) and kW of its columns.  The
-// V heads of the K head are processed kGroup at a time.
+// Persistent CTAs walk the (chunk, K head) units of one chunk segment.  Thread (row, part) owns
+// Gram row `row` (rows 0..63: key t, the A side; rows 64..127: query t, the P side) and kW of its
+// columns.  The V heads of the K head are processed kGroup at a time.
 __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_constant__ PrepParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -236,24 +247,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, part = warp >> 2;
   const int row = q4 * 32 + lane;
-  const int gc = blockIdx.x, kh = blockIdx.y;
   const int ratio = p.Hv / p.Hk;
-
-  if (gc >= __ldg(p.chunk_off + p.N)) return;  // beyond the last chunk (uniform over the CTA)
-  // the sequence of this chunk: the last n with chunk_off[n] <= gc (never an empty one)
-  int lo = 0, hi = p.N - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(p.chunk_off + mid) <= gc) lo = mid; else hi = mid - 1;
-  }
-  const int n = lo;
-  const int seq_s = __ldg(p.cu + n), seq_e = __ldg(p.cu + n + 1);
-  const int c0 = seq_s + (gc - __ldg(p.chunk_off + n)) * kChunk;
-  if (seq_s < 0 || seq_e < seq_s || seq_e > p.T || c0 >= seq_e) {
-    if (tid == 0) raise_error(p.err, kErrDeviceArgument);
-    return;
-  }
-  const int L = min(kChunk, seq_e - c0);
+  const long units = (long)__ldg(p.seg_pref + p.N) * p.Hk;
+  if ((long)blockIdx.x >= units) return;  // uniform over the CTA
 
   float* s_gam = reinterpret_cast<float*>(sm + PR_VEC);  // [kGroup][64] cumsum of g, log2 units
   float* s_beta = s_gam + kGroup * 64;                    // [kGroup][64]
@@ -275,7 +271,31 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+
+  bool ok = true, qk_pending = false, gram_pending = false;
+  uint32_t ph = 0;  // parity of both barriers: each completes once per unit
+  for (long u = blockIdx.x; u < units && ok; u += gridDim.x, ph ^= 1u) {
+  const int cu_ = (int)(u / p.Hk), kh = (int)(u - (long)cu_ * p.Hk);
+  // the sequence of this unit: the last n with seg_pref[n] <= cu_ (never one without chunks here)
+  int lo = 0, hi = p.N - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.seg_pref + mid) <= cu_) lo = mid; else hi = mid - 1;
+  }
+  const int n = lo;
+  const int seq_s = __ldg(p.cu + n), seq_e = __ldg(p.cu + n + 1);
+  const int nch = (max(0, seq_e - seq_s) + kChunk - 1) / kChunk;
+  const int j = seg_begin(p.seg, nch, p.nseg) + (cu_ - __ldg(p.seg_pref + n));
+  const int gc = __ldg(p.chunk_off + n) + j;
+  const int c0 = seq_s + j * kChunk;
+  if (seq_s < 0 || seq_e < seq_s || seq_e > p.T || c0 >= seq_e || gc < 0 || gc >= p.nc_max) {
+    if (tid == 0) raise_error(p.err, kErrDeviceArgument);
+    ph ^= 1u;  // no barrier completed for this unit
+    continue;
+  }
+  const int L = min(kChunk, seq_e - c0);
   if (tid == 0) issue_qk_tiles(sb + PR_QK, &p.tmap, p.Hk, c0, kh, bar_qk);
+  qk_pending = true;
 
   // g, beta of a group of V heads: thread -> (token tid / G, head tid % G), zero past the sequence end
   float g_next = 0.f, b_next = 0.f;
@@ -291,11 +311,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
   };
   load_gb(kh * ratio, min(kGroup, ratio));
 
-  bool ok = mbar_wait(bar_qk, 0, kWaitLimit);
-  if (!ok) raise_error(p.err, kErrTimeout);
-  ok = __syncthreads_and(ok ? 1 : 0) != 0;
-  const bool qk_pending = !ok;
-  bool gram_pending = false;
+  {
+    const bool got = mbar_wait(bar_qk, ph, kWaitLimit);
+    if (!got) raise_error(p.err, kErrTimeout);
+    ok = __syncthreads_and(got ? 1 : 0) != 0;
+    qk_pending = !ok;
+  }
   if (ok) {
     // Gram G = [K; Q] K^T (M = 128, N = 64, K = 128) on the raw bf16 tiles
     if (tid == 0) {
@@ -333,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
       const float inv = 1.0f / sqrtf(ss + p.l2_eps);
       if (tid < 64) s_ik[tid] = inv; else s_iq[tid - 64] = inv;
     }
-    const bool got = mbar_wait(bar_g, 0, kWaitLimit);
+    const bool got = mbar_wait(bar_g, ph, kWaitLimit);
     if (!got) raise_error(p.err, kErrTimeout);
     ok = __syncthreads_and(got ? 1 : 0) != 0;  // also: the q/k tile is dead from here on
     gram_pending = !ok;
@@ -441,9 +462,15 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
       __syncthreads();  // T reads done before the next group's A writes
     }
   }
+  // the unit's reads of the shared buffers precede the next unit's tile load into them
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  }
   // leave only after the Gram MMA and the tile load have landed (bounded, after an early exit)
-  if (qk_pending) mbar_wait(bar_qk, 0, kWaitLimit);
-  if (gram_pending) mbar_wait(bar_g, 0, kWaitLimit);
+  if (qk_pending) mbar_wait(bar_qk, ph ^ 1u, kWaitLimit);
+  if (gram_pending) mbar_wait(bar_g, ph ^ 1u, kWaitLimit);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -548,6 +575,21 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
     }
     bulk_prefetch_l2(p.rec + ((size_t)gc * p.Hv + h) * REC_BYTES, REC_BYTES);
   };
+  // 32 fp32 values of this thread's row (tokens part * kW ..) -> bf16 hi / lo pairs in tensor memory:
+  // hi in 16 columns at `taddr`, lo in the next 16 (the even token in the low half of a column)
+  auto store_split_tmem = [&](uint32_t taddr, const float (&v)[kW]) {
+    float hw[kW / 2], lw[kW / 2];
+#pragma unroll
+    for (int j = 0; j < kW / 2; ++j) {
+      const uint32_t hp = pack_bf2(v[2 * j], v[2 * j + 1]);
+      const float2 rem = __ffma2_rn(make_float2(__uint_as_float(hp << 16), __uint_as_float(hp & 0xFFFF0000u)),
+                                    make_float2(-1.f, -1.f), make_float2(v[2 * j], v[2 * j + 1]));
+      hw[j] = __uint_as_float(hp);
+      lw[j] = __uint_as_float(pack_bf2(rem.x, rem.y));
+    }
+    tmem_st16(taddr, hw);
+    tmem_st16(taddr + kW / 2, lw);
+  };
   // S0 columns [k0, k0 + 64) -> hi/lo operand tiles (64 keys = one K block); state <- Gamma_L S0 there
   auto convert_half = [&](int k0, float gL) {
     float v[kW];
@@ -573,10 +615,15 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
     const int ni = (int)(w / p.Hv);
     const int n = p.order ? __ldg(p.order + ni) : ni;
     const int kh = h / ratio;
-    const int seq_s = __ldg(p.cu + n), seq_e = __ldg(p.cu + n + 1);
-    const int gc0 = __ldg(p.chunk_off + n);
-    if (n < 0 || n >= p.N || seq_s < 0 || seq_e < seq_s || seq_e > p.T || gc0 < 0 ||
-        gc0 + (seq_e - seq_s + kChunk - 1) / kChunk > p.nc_max) {
+    const int seq_lo = __ldg(p.cu + n), seq_hi = __ldg(p.cu + n + 1);
+    const int nch = (max(0, seq_hi - seq_lo) + kChunk - 1) / kChunk;
+    const int jb = seg_begin(p.seg, nch, p.nseg), je = seg_begin(p.seg + 1, nch, p.nseg);
+    if (p.seg > 0 && jb == je) continue;  // no chunk in this segment: the state is already in state_out
+    // this launch's part of the sequence: chunks [jb, je)
+    const int seq_s = seq_lo + jb * kChunk, seq_e = min(seq_hi, seq_lo + je * kChunk);
+    const int gc0 = __ldg(p.chunk_off + n) + jb;
+    if (n < 0 || n >= p.N || seq_lo < 0 || seq_hi < seq_lo || seq_hi > p.T || gc0 < 0 ||
+        gc0 + (je - jb) > p.nc_max) {
       if (tid == 0) raise_error(p.err, kErrDeviceArgument);
       continue;
     }
@@ -594,8 +641,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       for (int cq = 0; cq < 4 / kParts; ++cq) {
         const int c0 = part * (128 / kParts) + cq * 32;
         float v[32];
-        if (p.state_in) {
-          const float4* src = reinterpret_cast<const float4*>(p.state_in + row_off + c0);
+        if (p.state_src) {
+          const float4* src = reinterpret_cast<const float4*>(p.state_src + row_off + c0);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float4 f = __ldg(src + i);
@@ -672,29 +719,50 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
                                        __fmul2_rn(make_float2(bt.z, bt.w), make_float2(v_at(i4 + 2), v_at(i4 + 3))));
           x[i4] = r0.x; x[i4 + 1] = r0.y; x[i4 + 2] = r1.x; x[i4 + 3] = r1.y;
         }
-#pragma unroll
-        for (int q = 0; q < kW / 8; ++q) store8_split(sm + SS_W, sm + SS_W + 16384, 0, row, part * kW + 8 * q, x + 8 * q);
+        store_split_tmem(tl + SC_X + part * kW, x);  // over this thread's own X columns
       }
+      // O1 leaves its columns (they take E next): into registers now, staged while the E MMAs run
+      float o1[kW];
+      tmem_ld_cols<kW>(tl + SC_O1 + part * kW, o1);
       operands_ready();
       if (tid == 0) {
         // the V buffer is free: the gate input of this chunk (gated), else the next chunk's v
         if (gated) issue_z(c0, h);
         else if (has_next) issue_v(c0 + kChunk, h);
-        // E^T = R T^T  (hi*hi + hi*lo + lo*hi)
-        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W), sw128_desc(sb + SS_T), ID64, 0);
-        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W), sw128_desc(sb + SS_T + 8192), ID64, 1);
-        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W + 16384), sw128_desc(sb + SS_T), ID64, 1);
+        // E^T = R T^T  (hi*hi + hi*lo + lo*hi), R from tensor memory (hi / lo pairs of 32 tokens per
+        // thread part: hi at columns 32 p, lo at 32 p + 16 of the X region)
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp)
+          mma_bf16_k2_ta<2>(tmem + SC_O1, tmem + SC_X + 32 * pp, sw128_desc(sb + SS_T) + 4 * pp, ID64, pp);
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp)
+          mma_bf16_k2_ta<2>(tmem + SC_O1, tmem + SC_X + 32 * pp, sw128_desc(sb + SS_T + 8192) + 4 * pp, ID64, 1);
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp)
+          mma_bf16_k2_ta<2>(tmem + SC_O1, tmem + SC_X + 32 * pp + 16, sw128_desc(sb + SS_T) + 4 * pp, ID64, 1);
         mma_commit(bar_e);
       }
       pend_z = gated;
       pend_v = !gated && has_next;
+      // o1 diag(c_o) -> the staging area (token-major fp32), free since the X MMAs completed
+#pragma unroll
+      for (int i4 = 0; i4 < kW; i4 += 4) {
+        const int t0 = part * kW + i4;
+        const float4 co = *reinterpret_cast<const float4*>(vec + V_CO + t0);
+        const float2 a = __fmul2_rn(make_float2(o1[i4], o1[i4 + 1]), make_float2(co.x, co.y));
+        const float2 b = __fmul2_rn(make_float2(o1[i4 + 2], o1[i4 + 3]), make_float2(co.z, co.w));
+        s_work[t0 * 128 + row] = a.x;
+        s_work[(t0 + 1) * 128 + row] = a.y;
+        s_work[(t0 + 2) * 128 + row] = b.x;
+        s_work[(t0 + 3) * 128 + row] = b.y;
+      }
       await_mma(bar_e);
       if (!ok) break;
 
-      // ================= E~ = E diag(c_s) -> hi/lo;  E -> bf16 (output operand, over T)
+      // ================= E~ = E diag(c_s) -> hi/lo (tensor memory, over R);  E -> bf16 (output operand, over T)
       {
-        float ev[kW];
-        tmem_ld_cols<kW>(tl + SC_X + part * kW, ev);
+        float ev[kW], es[kW];
+        tmem_ld_cols<kW>(tl + SC_O1 + part * kW, ev);
 #pragma unroll
         for (int q = 0; q < kW / 8; ++q) {
           const float4 c0v = *reinterpret_cast<const float4*>(vec + V_CS + part * kW + 8 * q);
@@ -704,17 +772,25 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
           const float2 p1 = __fmul2_rn(make_float2(e8[2], e8[3]), make_float2(c0v.z, c0v.w));
           const float2 p2 = __fmul2_rn(make_float2(e8[4], e8[5]), make_float2(c1v.x, c1v.y));
           const float2 p3 = __fmul2_rn(make_float2(e8[6], e8[7]), make_float2(c1v.z, c1v.w));
-          const float es[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
-          store8_split(sm + SS_W, sm + SS_W + 16384, 0, row, part * kW + 8 * q, es);
+          float* s8 = es + 8 * q;
+          s8[0] = p0.x; s8[1] = p0.y; s8[2] = p1.x; s8[3] = p1.y; s8[4] = p2.x; s8[5] = p2.y; s8[6] = p3.x; s8[7] = p3.y;
           store8_split(sm + SS_T, nullptr, 0, row, part * kW + 8 * q, e8);
         }
+        store_split_tmem(tl + SC_X + part * kW, es);
       }
       operands_ready();
       if (tid == 0) {
         // S += E~ K: B = the raw k rows of the q/k tile read MN-major (N = 128 keys, 16 tokens per step)
-        mma_bf16_k4<2, 128>(tmem + SC_S, sw128_desc(sb + SS_W), sw128_mn_desc(sb + SS_QK, 16384), ID128_BMN, 1);
-        mma_bf16_k4<2, 128>(tmem + SC_S, sw128_desc(sb + SS_W + 16384), sw128_mn_desc(sb + SS_QK, 16384), ID128_BMN, 1);
-        mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_T), sw128_desc(sb + SS_P), ID64, 0);
+        // (E~ from tensor memory as R was), O2 = E P^T into the E columns
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp)
+          mma_bf16_k2_ta<128>(tmem + SC_S, tmem + SC_X + 32 * pp, sw128_mn_desc(sb + SS_QK, 16384) + 256 * pp,
+                              ID128_BMN, 1);
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp)
+          mma_bf16_k2_ta<128>(tmem + SC_S, tmem + SC_X + 32 * pp + 16, sw128_mn_desc(sb + SS_QK, 16384) + 256 * pp,
+                              ID128_BMN, 1);
+        mma_bf16_k4<2, 2>(tmem + SC_O1, sw128_desc(sb + SS_T), sw128_desc(sb + SS_P), ID64, 0);
         mma_commit(bar_s);
       }
       constexpr int kTok = kChunk / kWarps;
@@ -726,23 +802,14 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       }
       pend_qk = pend_rec = has_next;
 
-      // ================= output: o = O1 diag(c_o) + O2 staged token-major, then the gated RMSNorm
+      // ================= output: o = O1 diag(c_o) (staged) + O2, then the gated RMSNorm
+      {
+        float o2a[16], o2b[16];
+        tmem_ld16x2(tl + SC_O1 + part * kW, tl + SC_O1 + part * kW + 16, o2a, o2b);
 #pragma unroll
-      for (int hh = 0; hh < kW; hh += 16) {  // 16 columns at a time: the gate inputs stay in registers
-        float o1[16], o2[16];
-        tmem_ld16x2(tl + SC_O1 + part * kW + hh, tl + SC_X + part * kW + hh, o1, o2);
-#pragma unroll
-        for (int i4 = 0; i4 < 16; i4 += 4) {
-          const int t0 = part * kW + hh + i4;
-          const float4 co = *reinterpret_cast<const float4*>(vec + V_CO + t0);
-          const float2 a = __ffma2_rn(make_float2(o1[i4], o1[i4 + 1]), make_float2(co.x, co.y),
-                                      make_float2(o2[i4], o2[i4 + 1]));
-          const float2 b = __ffma2_rn(make_float2(o1[i4 + 2], o1[i4 + 3]), make_float2(co.z, co.w),
-                                      make_float2(o2[i4 + 2], o2[i4 + 3]));
-          s_work[t0 * 128 + row] = a.x;
-          s_work[(t0 + 1) * 128 + row] = a.y;
-          s_work[(t0 + 2) * 128 + row] = b.x;
-          s_work[(t0 + 3) * 128 + row] = b.y;
+        for (int i = 0; i < 16; ++i) {
+          s_work[(part * kW + i) * 128 + row] += o2a[i];
+          s_work[(part * kW + 16 + i) * 128 + row] += o2b[i];
         }
       }
       if (gated) {
@@ -753,26 +820,35 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
         __syncthreads();
       }
       {
-        float r[kTok][4], ss[kTok];
+        float2 r[kTok][2];
+        float ss[kTok];
 #pragma unroll
         for (int i = 0; i < kTok; ++i) {
           const float4 v = *reinterpret_cast<const float4*>(s_work + (warp + kWarps * i) * 128 + lane * 4);
-          r[i][0] = v.x; r[i][1] = v.y; r[i][2] = v.z; r[i][3] = v.w;
-          ss[i] = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+          r[i][0] = make_float2(v.x, v.y);
+          r[i][1] = make_float2(v.z, v.w);
+          const float2 q2 = __ffma2_rn(r[i][1], r[i][1], __fmul2_rn(r[i][0], r[i][0]));
+          ss[i] = q2.x + q2.y;
         }
         if (gated) {
 #pragma unroll
           for (int m = 16; m >= 1; m >>= 1)
 #pragma unroll
             for (int i = 0; i < kTok; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], m);
+          const float2 half2 = make_float2(0.5f, 0.5f);
+          const float2 w01 = make_float2(wf[0], wf[1]), w23 = make_float2(wf[2], wf[3]);
 #pragma unroll
           for (int i = 0; i < kTok; ++i) {
-            const float rstd = rsqrtf(ss[i] * (1.0f / kHeadDim) + p.rms_eps);
+            const float rstd = rsqrtf(fmaf(ss[i], 1.0f / kHeadDim, p.rms_eps));
             const uint2 zz = *reinterpret_cast<const uint2*>(sm + SS_V + (warp + kWarps * i) * 256 + lane * 8);
-            const float zf[4] = {__uint_as_float(zz.x << 16), __uint_as_float(zz.x & 0xFFFF0000u),
-                                 __uint_as_float(zz.y << 16), __uint_as_float(zz.y & 0xFFFF0000u)};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) r[i][e] = r[i][e] * rstd * wf[e] * sigmoid_tanh(zf[e]);
+            // sigmoid(z) = (1 + tanh(z / 2)) / 2
+            const float2 h01 = __fmul2_rn(make_float2(__uint_as_float(zz.x << 16), __uint_as_float(zz.x & 0xFFFF0000u)), half2);
+            const float2 h23 = __fmul2_rn(make_float2(__uint_as_float(zz.y << 16), __uint_as_float(zz.y & 0xFFFF0000u)), half2);
+            const float2 s01 = __ffma2_rn(half2, make_float2(tanh_approx(h01.x), tanh_approx(h01.y)), half2);
+            const float2 s23 = __ffma2_rn(half2, make_float2(tanh_approx(h23.x), tanh_approx(h23.y)), half2);
+            const float2 rs = make_float2(rstd, rstd);
+            r[i][0] = __fmul2_rn(__fmul2_rn(r[i][0], __fmul2_rn(w01, rs)), s01);
+            r[i][1] = __fmul2_rn(__fmul2_rn(r[i][1], __fmul2_rn(w23, rs)), s23);
           }
         }
 #pragma unroll
@@ -781,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
           if (t < L) {
             const size_t base = ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4;
             *reinterpret_cast<uint2*>(p.out + base) =
-                make_uint2(pack_bf2(r[i][0], r[i][1]), pack_bf2(r[i][2], r[i][3]));
+                make_uint2(pack_bf2(r[i][0].x, r[i][0].y), pack_bf2(r[i][1].x, r[i][1].y));
           }
         }
       }
@@ -827,6 +903,51 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
   }
 }
 
+// One CTA: for every segment k < nseg, the exclusive prefix over sequences of their chunk counts in
+// segment k (seg_pref[k (N + 1) + n]; the total at n = N), and the per-segment work counters zeroed.
+// Sequences with inconsistent cu_seqlens count as empty here; the main kernels report them.
+__global__ void __launch_bounds__(1024) chunk_segments_kernel(const int32_t* cu, int N, int nseg, int32_t* seg_pref,
+                                                              unsigned* counters) {
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < kMaxSegments) counters[tid] = 0u;
+  const int per = (N + 1023) / 1024, lo = min(N, tid * per), hi = min(N, lo + per);
+  for (int k = 0; k < nseg; ++k) {
+    auto len = [&](int i) {
+      const int nch = (max(0, __ldg(cu + i + 1) - __ldg(cu + i)) + kChunk - 1) / kChunk;
+      return seg_begin(k + 1, nch, nseg) - seg_begin(k, nch, nseg);
+    };
+    int local = 0;
+    for (int i = lo; i < hi; ++i) local += len(i);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = s_warp[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += v;
+      }
+      s_warp[lane] = w;
+    }
+    __syncthreads();
+    int32_t* pref = seg_pref + (size_t)k * (N + 1);
+    int run = incl - local + (warp > 0 ? s_warp[warp - 1] : 0);
+    for (int i = lo; i < hi; ++i) {
+      pref[i] = run;
+      run += len(i);
+    }
+    if (tid == 1023) pref[N] = s_warp[31];
+    __syncthreads();  // s_warp is reused by the next segment
+  }
+}
+
 }  // namespace
 
 namespace {
@@ -837,20 +958,46 @@ size_t pad256(size_t b) { return (b + 255) / 256 * 256; }
 long chunk_bound(int N, int T) { return ((long)T + 63L * N) / kChunk; }
 
 struct SplitLayout {
-  unsigned* counter;
+  unsigned* counters;  // one work counter per segment
   int32_t* order;
   int32_t* chunk_off;
+  int32_t* seg_pref;   // kMaxSegments x (N + 1)
   uint8_t* rec;
 };
 
 SplitLayout split_layout(void* workspace, int N) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   SplitLayout l;
-  l.counter = reinterpret_cast<unsigned*>(ws);
-  l.order = reinterpret_cast<int32_t*>(ws + 256);
-  l.chunk_off = reinterpret_cast<int32_t*>(ws + 256 + pad256((size_t)N * 4));
-  l.rec = ws + 256 + pad256((size_t)N * 4) + pad256((size_t)(N + 1) * 4);
+  size_t off = 256;
+  l.counters = reinterpret_cast<unsigned*>(ws);
+  l.order = reinterpret_cast<int32_t*>(ws + off);
+  off += pad256((size_t)N * 4);
+  l.chunk_off = reinterpret_cast<int32_t*>(ws + off);
+  off += pad256((size_t)(N + 1) * 4);
+  l.seg_pref = reinterpret_cast<int32_t*>(ws + off);
+  off += pad256((size_t)kMaxSegments * (N + 1) * 4);
+  l.rec = ws + off;
   return l;
+}
+
+// Per-device side stream for the prep kernels of later segments (created on first use).
+cudaError_t side_stream(cudaStream_t* out) {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!streams[dev]) {
+    e = cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking);
+    if (e != cudaSuccess) {
+      streams[dev] = nullptr;
+      return e;
+    }
+  }
+  *out = streams[dev];
+  return cudaSuccess;
 }
 
 template <typename K>
@@ -870,7 +1017,7 @@ cudaError_t set_smem_once(K kernel, uint32_t bytes, int (&done)[64]) {
 size_t split_workspace_bytes(int N, int T, int Hk, int Hv) {
   (void)Hk;
   if (N <= 0) return 0;
-  return 256 + pad256((size_t)N * 4) + pad256((size_t)(N + 1) * 4) +
+  return 256 + pad256((size_t)N * 4) + pad256((size_t)(N + 1) * 4) + pad256((size_t)kMaxSegments * (N + 1) * 4) +
          (size_t)chunk_bound(N, T) * (size_t)Hv * REC_BYTES;
 }
 
@@ -889,40 +1036,86 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
     cudaError_t e = encode_chunk_tensor_maps(&tmap, &tmap_z, qkv, z, T, Hk, Hv);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = launch_chunk_schedule(env.stream, cu, N, lay.order, lay.counter, lay.chunk_off);
+  cudaError_t e = launch_chunk_schedule(env.stream, cu, N, lay.order, lay.counters, lay.chunk_off);
   if (e != cudaSuccess) return e;
-
-  if (T > 0 && nc_max > 0) {
-    if ((e = set_smem_once(chunk_prep_kernel, PR_BYTES, prep_set)) != cudaSuccess) return e;
-    PrepParams pp;
-    memset(&pp, 0, sizeof pp);
-    pp.tmap = tmap;
-    pp.g = g; pp.beta = beta; pp.cu = cu; pp.chunk_off = lay.chunk_off; pp.rec = lay.rec; pp.err = env.err;
-    pp.N = N; pp.T = T; pp.Hk = Hk; pp.Hv = Hv; pp.q_scale = q_scale; pp.l2_eps = l2_eps;
-    chunk_prep_kernel<<<dim3((unsigned)nc_max, (unsigned)Hk), kThreads, PR_BYTES, env.stream>>>(pp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-
+  if ((e = set_smem_once(chunk_prep_kernel, PR_BYTES, prep_set)) != cudaSuccess) return e;
   if ((e = set_smem_once(chunk_state_kernel, SS_BYTES, state_set)) != cudaSuccess) return e;
-  StateParams sp;
-  memset(&sp, 0, sizeof sp);
-  sp.tmap = tmap;
-  sp.tmap_z = tmap_z;
-  sp.cu = cu; sp.order = lay.order; sp.counter = lay.counter; sp.chunk_off = lay.chunk_off; sp.rec = lay.rec;
-  sp.state_in = state_in; sp.state_out = state_out; sp.z = z; sp.norm_w = norm_w; sp.out = out; sp.err = env.err;
-  sp.N = N; sp.T = T; sp.Hk = Hk; sp.Hv = Hv; sp.nc_max = (int)nc_max; sp.rms_eps = rms_eps;
   int sms = 0;
   if ((e = device_sm_count(&sms)) != cudaSuccess) return e;
-  // Two CTAs per SM: 2 x 256 tensor-memory columns, 2 x (SS_BYTES + 1 KB reserved) of shared
+
+  // Segments: with a state_out buffer to carry the state between launches, a long enough input
+  // and no stream capture in progress, the chunks of every sequence are split into kMaxSegments
+  // parts and the prep kernel of part k + 1 (on a side stream) runs beside the state kernel of
+  // part k; otherwise one part, everything on the caller's stream.
+  int nseg = 1;
+  cudaStream_t side = env.stream;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (state_out && T >= 64 * kChunk && cudaStreamIsCapturing(env.stream, &cap) == cudaSuccess &&
+      cap == cudaStreamCaptureStatusNone && side_stream(&side) == cudaSuccess)
+    nseg = kMaxSegments;
+  if (nseg == 1) side = env.stream;
+  chunk_segments_kernel<<<1, 1024, 0, env.stream>>>(cu, N, nseg, lay.seg_pref, lay.counters);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  cudaEvent_t ev[kMaxSegments + 1] = {};
+  auto destroy_events = [&]() {
+    for (int k = 0; k <= kMaxSegments; ++k)
+      if (ev[k]) cudaEventDestroy(ev[k]);
+  };
+  if (nseg > 1) {
+    for (int k = 0; k <= nseg && e == cudaSuccess; ++k) e = cudaEventCreateWithFlags(&ev[k], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[nseg], env.stream);  // schedule and segment tables written
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, ev[nseg], 0);
+    if (e != cudaSuccess) {
+      destroy_events();
+      return e;
+    }
+  }
+
+  PrepParams pp;
+  memset(&pp, 0, sizeof pp);
+  pp.tmap = tmap;
+  pp.g = g; pp.beta = beta; pp.cu = cu; pp.chunk_off = lay.chunk_off; pp.rec = lay.rec; pp.err = env.err;
+  pp.N = N; pp.T = T; pp.Hk = Hk; pp.Hv = Hv; pp.nseg = nseg; pp.nc_max = (int)nc_max;
+  pp.q_scale = q_scale; pp.l2_eps = l2_eps;
+
+  StateParams sp;
+  memset(&sp, 0, sizeof sp);
+  sp.nseg = nseg;
+  sp.tmap = tmap;
+  sp.tmap_z = tmap_z;
+  sp.cu = cu; sp.order = lay.order; sp.chunk_off = lay.chunk_off; sp.rec = lay.rec;
+  sp.state_in = state_in; sp.state_out = state_out; sp.z = z; sp.norm_w = norm_w; sp.out = out; sp.err = env.err;
+  sp.N = N; sp.T = T; sp.Hk = Hk; sp.Hv = Hv; sp.nc_max = (int)nc_max; sp.rms_eps = rms_eps;
+  // Two state CTAs per SM: 2 x 256 tensor-memory columns, 2 x (SS_BYTES + 1 KB reserved) of shared
   // memory and 2 x 256 threads x 128 registers all fit.  (The runtime's occupancy query reports one
   // CTA per SM for any kernel that allocates tensor memory, but the hardware co-schedules two; a
   // CTA that cannot be resident runs later, finds no work and exits.)
   constexpr int per_sm = 2;
   const long items = (long)N * Hv;
   const long slots = (long)sms * per_sm;
-  const int grid = (int)(items < slots ? items : slots);
-  chunk_state_kernel<<<grid, kThreads, SS_BYTES, env.stream>>>(sp);
-  return cudaGetLastError();
+  const int state_grid = (int)(items < slots ? items : slots);
+
+  for (int k = 0; k < nseg && e == cudaSuccess; ++k) {
+    if (T > 0 && nc_max > 0) {
+      pp.seg = k;
+      pp.seg_pref = lay.seg_pref + (size_t)k * (N + 1);
+      chunk_prep_kernel<<<(unsigned)slots, kThreads, PR_BYTES, side>>>(pp);
+      if ((e = cudaGetLastError()) != cudaSuccess) break;
+    }
+    if (nseg > 1) {
+      e = cudaEventRecord(ev[k], side);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(env.stream, ev[k], 0);
+      if (e != cudaSuccess) break;
+    }
+    sp.seg = k;
+    sp.counter = lay.counters + k;
+    sp.state_src = k == 0 ? state_in : state_out;
+    chunk_state_kernel<<<state_grid, kThreads, SS_BYTES, env.stream>>>(sp);
+    e = cudaGetLastError();
+  }
+  destroy_events();  // released once the work recorded on them completes
+  return e;
 }
 
 }  // namespace gdn

@@ -314,6 +314,42 @@ __device__ __forceinline__ void mma_bf16_k4(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// As mma_bf16_k4 with A in tensor memory: A (128 rows = lanes, K along columns, two bf16 per
+// 32-bit column, the even K index in the low half) starts at column a_tmem and advances 8
+// columns per K = 16 step.
+template <uint32_t BS>
+__device__ __forceinline__ void mma_bf16_k4_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t acc_first) {
+  asm volatile(
+      "{\n.reg .pred p, q;\n.reg .b64 b1, b2, b3;\n.reg .b32 a1, a2, a3;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "setp.ne.b32 q, %5, 0;\n"
+      "add.u32 a1, %1, 8;\nadd.u32 a2, %1, 16;\nadd.u32 a3, %1, 24;\n"
+      "add.s64 b1, %2, %6;\nadd.s64 b2, %2, %7;\nadd.s64 b3, %2, %8;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, q;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, q;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, q;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc_first), "r"(1u), "n"(BS), "n"(2 * BS), "n"(3 * BS)
+      : "memory");
+}
+
+// Two K = 16 steps with A in tensor memory (advancing 8 columns) and B advancing BS units.
+template <uint32_t BS>
+__device__ __forceinline__ void mma_bf16_k2_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t acc_first) {
+  asm volatile(
+      "{\n.reg .pred p, q;\n.reg .b64 b1;\n.reg .b32 a1;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "setp.ne.b32 q, %5, 0;\n"
+      "add.u32 a1, %1, 8;\n"
+      "add.s64 b1, %2, %6;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, q;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc_first), "r"(1u), "n"(BS)
+      : "memory");
+}
+
 // Arrive once on the mbarrier when every tcgen05 MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t mbar_addr) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar_addr)

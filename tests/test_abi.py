@@ -132,7 +132,9 @@ def test_fast_path_workspace_size():
     rec = 2 * 8192 + 8192 + 5 * 64 * 4
     for n, t in ((1, 16), (4, 4 * 4096), (8, 32735), (3, 0)):
         chunks = (t + 63 * n) // 64
-        head = 256 + -(-4 * n // 256) * 256 + -(-4 * (n + 1) // 256) * 256
+        pad = lambda b: -(-b // 256) * 256
+        # counters, order, chunk offsets, four per-segment chunk prefixes
+        head = 256 + pad(4 * n) + pad(4 * (n + 1)) + pad(4 * 4 * (n + 1))
         assert lib.gdn_chunk_prefill_workspace_size(_geo(), n, t) == head + chunks * 48 * rec
     # the bound covers the worst case: every sequence one token past a chunk boundary
     lengths = [65] * 7

@@ -35,3 +35,28 @@ def test_mma_probe_structured_operands():
     assert int(status.item()) == 0
     ref = A.to(torch.bfloat16).double() @ B.to(torch.bfloat16).double().T
     assert torch.equal(D.cpu().double(), ref)
+
+
+@pytest.mark.parametrize("flags", [1, 2, 3], ids=["a_tmem", "b_mn", "a_tmem_b_mn"])
+@pytest.mark.parametrize("n", [64, 128])
+def test_mma_probe_operand_placements(n, flags):
+    """A from tensor memory and B MN-major, as the split chunk prefill's state kernel uses them:
+    structured operands (a permutation of rows, columns or K would show) and random ones."""
+    g = lib()
+    A = torch.zeros(128, 64)
+    for r in range(128):
+        A[r, (5 * r) % 64] = 1.0 + (r // 64)
+    B = torch.arange(n * 64, dtype=torch.float32).reshape(n, 64) % 251 - 125
+    D, status = g.gdn_debug_mma_probe_ex(A.to(torch.bfloat16).to(DEV), B.to(torch.bfloat16).to(DEV), flags)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = A.to(torch.bfloat16).double() @ B.to(torch.bfloat16).double().T
+    assert torch.equal(D.cpu().double(), ref)
+    gen = torch.Generator().manual_seed(100 + n + flags)
+    A = torch.randn(128, 64, generator=gen).to(torch.bfloat16)
+    B = torch.randn(n, 64, generator=gen).to(torch.bfloat16)
+    D, status = g.gdn_debug_mma_probe_ex(A.to(DEV), B.to(DEV), flags)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = A.double() @ B.double().T
+    assert (D.cpu().double() - ref).abs().max().item() < 1e-3 * ref.abs().max().item()

@@ -236,3 +236,27 @@ def test_minimum_workspace_runs_the_fused_kernel():
     for out, st in results:
         assert_out_close(out, ref["out"])
         assert_state_close(st, ref["state"])
+
+
+def test_segmented_split_path():
+    """Inputs of 4,096 tokens or more run the split path as four chunk segments per sequence (the
+    state carried through state_out between segment launches, prep of the next segment beside the
+    state kernel of the current one): sequences of 1..4095 tokens, an empty one, several
+    segment-boundary positions, state in place and out of place."""
+    geo = Geometry(num_k_heads=2, num_v_heads=6)
+    lengths = [4095, 1, 0, 200, 64, 2000, 130]
+    inp = prefill_inputs(lengths, seed=51, geo=geo)
+    ref = run_oracle(inp, geo=geo)
+    out, st = run_gpu(inp, ref["y"], geo=geo)
+    assert_out_close(out, ref["out"])
+    for n in range(len(lengths)):
+        assert_state_close(st[n], ref["state"][n], f"state of sequence {n}")
+    # in place
+    g = lib()
+    s2 = inp["state0"].to(DEV).clone()
+    o2 = g.gdn_chunk_prefill(ref["y"].to(DEV), inp["g"].to(DEV), inp["beta"].to(DEV), inp["cu_seqlens"].to(DEV),
+                             inp["q_scale"], 1e-6, s2, s2, inp["z"].to(DEV), inp["norm_w"].to(DEV), 1e-6,
+                             geometry=geo)
+    g.gdn_check_device_errors()
+    assert torch.equal(o2, out)
+    assert torch.equal(s2, st)

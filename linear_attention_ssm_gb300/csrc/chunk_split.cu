@@ -20,7 +20,7 @@
 //   E~ = E diag(c_s)                   ->  S = Gamma_L S0 + E~^T K  (E~ from tensor memory, K read
 //                                          MN-major from the q/k tile), O2 = E P^T
 //   o = O1 diag(c_o) + O2  ->  sigmoid-gated RMSNorm  ->  out
-// with the records fetched by 1D bulk copies and q/k, v by TMA.  The state kernel uses 256 of
+// with the records fetched by 1D bulk copies and q/k, v, z by TMA.  The state kernel uses 256 of
 // the 512 tensor-memory columns and ~108 KB of shared memory, so two CTAs share an SM and one
 // CTA's waits hide behind the other's work.
 #include <cuda.h>
@@ -102,7 +102,7 @@ struct StateParams {
   int seg, nseg;              // chunk segment processed by this launch
   const float* state_src;     // state at the segment start: state_in (may be NULL) for the first, else state_out
   CUtensorMap tmap;
-  CUtensorMap tmap_z;  // z [T][Hv * 128] bf16, box 128 x 64 (valid when z != NULL): L2 prefetch only
+  CUtensorMap tmap_z;  // z [T][Hv * 128] bf16, box 128 x 64, no swizzle (valid when z != NULL)
   const int32_t* cu;
   const int32_t* order;
   unsigned* counter;
@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
     mbar_init(bar_qk, 1);
     mbar_init(bar_g, 1);
     fence_mbar_init();
+    prefetch_tensormap(&p.tmap);
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 64);
   tc_fence_before();
@@ -503,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
   if (tid == 0) {
     for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&bars[i]), 1);
     fence_mbar_init();
+    prefetch_tensormap(&p.tmap);
+    if (p.z) prefetch_tensormap(&p.tmap_z);
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), SC_COLS);
   tc_fence_before();
@@ -564,16 +567,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
     mbar_arrive_expect_tx(bar_rec, kRecTP + kRecVec);
     bulk_load(sb + SS_T, rec + REC_T, kRecTP, bar_rec);
     bulk_load(sb + SS_VEC + vb * kRecVec, rec + REC_VEC, kRecVec, bar_rec);
-  };
-  // L2 prefetch of a chunk's operands, issued one chunk (or, for z, one chain) ahead of their loads
-  auto prefetch_inputs = [&](int c0, int gc, int kh, int h) {
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      tma_prefetch_2d(&p.tmap, p.Hk * kHeadDim + kh * kHeadDim + kb * 64, c0);
-      tma_prefetch_2d(&p.tmap, kh * kHeadDim + kb * 64, c0);
-      tma_prefetch_2d(&p.tmap, 2 * p.Hk * kHeadDim + h * kHeadDim + kb * 64, c0);
-    }
-    bulk_prefetch_l2(p.rec + ((size_t)gc * p.Hv + h) * REC_BYTES, REC_BYTES);
   };
   // 32 fp32 values of this thread's row (tokens part * kW ..) -> bf16 hi / lo pairs in tensor memory:
   // hi in 16 columns at `taddr`, lo in the next 16 (the even token in the low half of a column)
@@ -666,10 +659,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       pend_rec = pend_qk = false;
       if (!ok) break;
       const float gL = vec[V_MISC];
-      if (tid == 0) {
-        if (gated) tma_prefetch_2d(&p.tmap_z, h * kHeadDim, c0);  // read by this chunk's output stage
-        if (has_next) prefetch_inputs(c0 + kChunk, gc + 1, kh, h);
-      }
 
       // ================= [X | O1] = S0 [K; Q]^T one 64-key half at a time: X from the hi and lo
       // parts of S0, the output-only O1 from the hi part
@@ -726,9 +715,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       tmem_ld_cols<kW>(tl + SC_O1 + part * kW, o1);
       operands_ready();
       if (tid == 0) {
-        // the V buffer is free: the gate input of this chunk (gated), else the next chunk's v
-        if (gated) issue_z(c0, h);
-        else if (has_next) issue_v(c0 + kChunk, h);
         // E^T = R T^T  (hi*hi + hi*lo + lo*hi), R from tensor memory (hi / lo pairs of 32 tokens per
         // thread part: hi at columns 32 p, lo at 32 p + 16 of the X region)
 #pragma unroll
@@ -741,6 +727,10 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
         for (int pp = 0; pp < 2; ++pp)
           mma_bf16_k2_ta<2>(tmem + SC_O1, tmem + SC_X + 32 * pp + 16, sw128_desc(sb + SS_T) + 4 * pp, ID64, 1);
         mma_commit(bar_e);
+      } else if (tid == 32) {
+        // the V buffer is free: the gate input of this chunk (gated), else the next chunk's v
+        if (gated) issue_z(c0, h);
+        else if (has_next) issue_v(c0 + kChunk, h);
       }
       pend_z = gated;
       pend_v = !gated && has_next;
@@ -796,9 +786,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       constexpr int kTok = kChunk / kWarps;
       await_mma(bar_s);
       if (!ok) break;
-      if (tid == 0 && has_next) {
-        issue_qk_tiles(sb + SS_QK, &p.tmap, p.Hk, c0 + kChunk, kh, bar_qk);
-        issue_rec(gc + 1, h, vb ^ 1);
+      if (has_next) {  // two issuing threads in different warps, so neither lags by both
+        if (tid == 0) issue_qk_tiles(sb + SS_QK, &p.tmap, p.Hk, c0 + kChunk, kh, bar_qk);
+        else if (tid == 32) issue_rec(gc + 1, h, vb ^ 1);
       }
       pend_qk = pend_rec = has_next;
 
@@ -841,11 +831,10 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
           for (int i = 0; i < kTok; ++i) {
             const float rstd = rsqrtf(fmaf(ss[i], 1.0f / kHeadDim, p.rms_eps));
             const uint2 zz = *reinterpret_cast<const uint2*>(sm + SS_V + (warp + kWarps * i) * 256 + lane * 8);
-            // sigmoid(z) = (1 + tanh(z / 2)) / 2
-            const float2 h01 = __fmul2_rn(make_float2(__uint_as_float(zz.x << 16), __uint_as_float(zz.x & 0xFFFF0000u)), half2);
-            const float2 h23 = __fmul2_rn(make_float2(__uint_as_float(zz.y << 16), __uint_as_float(zz.y & 0xFFFF0000u)), half2);
-            const float2 s01 = __ffma2_rn(half2, make_float2(tanh_approx(h01.x), tanh_approx(h01.y)), half2);
-            const float2 s23 = __ffma2_rn(half2, make_float2(tanh_approx(h23.x), tanh_approx(h23.y)), half2);
+            // sigmoid(z) = (1 + tanh(z / 2)) / 2, the tanh of a bf16 pair in one operation (z is bf16;
+            // halving it is exact)
+            const float2 s01 = __ffma2_rn(half2, tanh_half_bf16x2(zz.x), half2);
+            const float2 s23 = __ffma2_rn(half2, tanh_half_bf16x2(zz.y), half2);
             const float2 rs = make_float2(rstd, rstd);
             r[i][0] = __fmul2_rn(__fmul2_rn(r[i][0], __fmul2_rn(w01, rs)), s01);
             r[i][1] = __fmul2_rn(__fmul2_rn(r[i][1], __fmul2_rn(w23, rs)), s23);
@@ -866,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       __syncthreads();  // staging reads and accumulator reads done before the next chunk reuses them
       tc_fence_after();
       if (gated && has_next) {
-        if (tid == 0) issue_v(c0 + kChunk, h);
+        if (tid == 64) issue_v(c0 + kChunk, h);
         pend_v = true;
       }
     }

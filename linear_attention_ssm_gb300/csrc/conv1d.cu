@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kConvThreads, 2) conv1d_silu_kernel(const __gr
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&full[s]), 1);
     fence_mbar_init();
+    prefetch_tensormap(&p.tmap);
   }
   __syncthreads();
   auto issue = [&](long item, int s) {

@@ -54,6 +54,14 @@ __device__ __forceinline__ float tanh_approx(float x) {
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// tanh(z / 2) of the two bf16 values packed in `zz` (low half first), by the bf16x2 hardware tanh
+// (about bf16 precision), returned as two floats
+__device__ __forceinline__ float2 tanh_half_bf16x2(uint32_t zz) {
+  const __nv_bfloat162 z2 = *reinterpret_cast<const __nv_bfloat162*>(&zz);
+  const __nv_bfloat162 t2 = h2tanh_approx(__hmul2(z2, __floats2bfloat162_rn(0.5f, 0.5f)));
+  const uint32_t t = *reinterpret_cast<const uint32_t*>(&t2);
+  return make_float2(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u));
+}
 // sigmoid(x) = (1 + tanh(x / 2)) / 2: one special-function operation
 __device__ __forceinline__ float sigmoid_tanh(float x) { return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f); }
 
@@ -117,6 +125,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
                : "memory");
+}
+// bring a tensor map (kernel parameter) into the TMA unit's descriptor cache
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

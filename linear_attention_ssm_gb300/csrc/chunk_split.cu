@@ -495,14 +495,15 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
 
   float* s_work = reinterpret_cast<float*>(sm + SS_W);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SS_BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SS_BAR + 64);
-  int* item_slot = reinterpret_cast<int*>(sm + SS_BAR + 72);
-  const uint32_t bar_qk = smem_u32(&bars[0]), bar_v = smem_u32(&bars[1]), bar_rec = smem_u32(&bars[2]),
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SS_BAR + 96);
+  int* item_slot = reinterpret_cast<int*>(sm + SS_BAR + 104);
+  const uint32_t bar_qk = smem_u32(&bars[0]), bar_v = smem_u32(&bars[1]), bar_tp = smem_u32(&bars[2]),
                  bar_h = smem_u32(&bars[3]), bar_x = smem_u32(&bars[4]), bar_e = smem_u32(&bars[5]),
                  bar_s = smem_u32(&bars[6]), bar_z = smem_u32(&bars[7]);
+  const uint32_t bar_vec0 = smem_u32(&bars[8]);  // one barrier per vector buffer: bar_vec0 + 8 * buffer
 
   if (tid == 0) {
-    for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 10; ++i) mbar_init(smem_u32(&bars[i]), 1);
     fence_mbar_init();
     prefetch_tensormap(&p.tmap);
     if (p.z) prefetch_tensormap(&p.tmap_z);
@@ -518,8 +519,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
   constexpr uint32_t ID128 = idesc_bf16_f32(128, 128);
   constexpr uint32_t ID128_BMN = idesc_bf16_f32_bmn(128, 128);
   bool ok = true;
-  uint32_t ph_mma = 0, ph_qk = 0, ph_v = 0, ph_rec = 0, ph_z = 0;
-  bool pend_qk = false, pend_v = false, pend_rec = false, pend_z = false;
+  uint32_t ph_mma = 0, ph_qk = 0, ph_v = 0, ph_tp = 0, ph_z = 0;
+  uint32_t ph_vec = 0, pend_vec = 0;  // bit b: parity of / load in flight on vector buffer b
+  bool pend_qk = false, pend_v = false, pend_tp = false, pend_z = false;
   const bool gated = p.z != nullptr;
   float wf[4] = {1.f, 1.f, 1.f, 1.f};
   if (gated) {
@@ -562,11 +564,17 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
     mbar_arrive_expect_tx(bar_z, kBytesZ);
     tma_load_2d(sb + SS_V, &p.tmap_z, h * kHeadDim, c0, bar_z);
   };
-  auto issue_rec = [&](int gc, int h, int vb) {
+  // a chunk's record: T and P (needed from the E MMA on), and its vector block (needed at chunk
+  // start; double buffered, so it is fetched a whole chunk ahead)
+  auto issue_tp = [&](int gc, int h) {
     const uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * REC_BYTES;
-    mbar_arrive_expect_tx(bar_rec, kRecTP + kRecVec);
-    bulk_load(sb + SS_T, rec + REC_T, kRecTP, bar_rec);
-    bulk_load(sb + SS_VEC + vb * kRecVec, rec + REC_VEC, kRecVec, bar_rec);
+    mbar_arrive_expect_tx(bar_tp, kRecTP);
+    bulk_load(sb + SS_T, rec + REC_T, kRecTP, bar_tp);
+  };
+  auto issue_vec = [&](int gc, int h, int vb) {
+    const uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * REC_BYTES;
+    mbar_arrive_expect_tx(bar_vec0 + 8 * vb, kRecVec);
+    bulk_load(sb + SS_VEC + vb * kRecVec, rec + REC_VEC, kRecVec, bar_vec0 + 8 * vb);
   };
   // 32 fp32 values of this thread's row (tokens part * kW ..) -> bf16 hi / lo pairs in tensor memory:
   // hi in 16 columns at `taddr`, lo in the next 16 (the even token in the low half of a column)
@@ -621,11 +629,13 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       continue;
     }
     if (tid == 0 && seq_e > seq_s) {
+      issue_vec(gc0, h, 0);
       issue_qk_tiles(sb + SS_QK, &p.tmap, p.Hk, seq_s, kh, bar_qk);
       issue_v(seq_s, h);
-      issue_rec(gc0, h, 0);
+      issue_tp(gc0, h);
     }
-    pend_qk = pend_v = pend_rec = seq_e > seq_s;
+    pend_qk = pend_v = pend_tp = seq_e > seq_s;
+    if (seq_e > seq_s) pend_vec |= 1u;
 
     // ---- initial state -> tensor memory
     {
@@ -655,15 +665,27 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       const bool has_next = c0 + kChunk < seq_e;
       const float* vec = reinterpret_cast<const float*>(sm + SS_VEC + vb * kRecVec);
 
-      wait_two(bar_rec, ph_rec, bar_qk, ph_qk);
-      pend_rec = pend_qk = false;
+      {
+        const bool got = mbar_wait(bar_vec0 + 8 * vb, (ph_vec >> vb) & 1u, kWaitLimit);
+        ph_vec ^= 1u << vb;
+        pend_vec &= ~(1u << vb);
+        if (!got) raise_error(p.err, kErrTimeout);
+        ok = __syncthreads_and(got ? 1 : 0) != 0 && ok;
+      }
       if (!ok) break;
       const float gL = vec[V_MISC];
+      if (tid == 32 && has_next) issue_vec(gc + 1, h, vb ^ 1);  // that buffer's last reader was chunk c - 1
+      if (has_next) pend_vec |= 1u << (vb ^ 1);
 
       // ================= [X | O1] = S0 [K; Q]^T one 64-key half at a time: X from the hi and lo
       // parts of S0, the output-only O1 from the hi part
       convert_half(0, gL);
-      operands_ready();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      wait_bar(bar_qk, ph_qk);  // the q/k tile (its latency overlaps the conversion above)
+      pend_qk = false;
+      tc_fence_after();
+      if (!ok) break;
       if (tid == 0) {
 #pragma unroll
         mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W), sw128_desc(sb + SS_QK), ID128, 0);
@@ -713,7 +735,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       // O1 leaves its columns (they take E next): into registers now, staged while the E MMAs run
       float o1[kW];
       tmem_ld_cols<kW>(tl + SC_O1 + part * kW, o1);
-      operands_ready();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      wait_bar(bar_tp, ph_tp);  // T and P of this chunk
+      pend_tp = false;
+      tc_fence_after();
+      if (!ok) break;
       if (tid == 0) {
         // E^T = R T^T  (hi*hi + hi*lo + lo*hi), R from tensor memory (hi / lo pairs of 32 tokens per
         // thread part: hi at columns 32 p, lo at 32 p + 16 of the X region)
@@ -788,9 +815,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       if (!ok) break;
       if (has_next) {  // two issuing threads in different warps, so neither lags by both
         if (tid == 0) issue_qk_tiles(sb + SS_QK, &p.tmap, p.Hk, c0 + kChunk, kh, bar_qk);
-        else if (tid == 32) issue_rec(gc + 1, h, vb ^ 1);
+        else if (tid == 32) issue_tp(gc + 1, h);
       }
-      pend_qk = pend_rec = has_next;
+      pend_qk = pend_tp = has_next;
 
       // ================= output: o = O1 diag(c_o) (staged) + O2, then the gated RMSNorm
       {
@@ -882,7 +909,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
   // after an early exit, let copies still in flight land before the CTA leaves (bounded)
   if (pend_qk) mbar_wait(bar_qk, ph_qk, kWaitLimit);
   if (pend_v) mbar_wait(bar_v, ph_v, kWaitLimit);
-  if (pend_rec) mbar_wait(bar_rec, ph_rec, kWaitLimit);
+  if (pend_tp) mbar_wait(bar_tp, ph_tp, kWaitLimit);
+  if (pend_vec & 1u) mbar_wait(bar_vec0, ph_vec & 1u, kWaitLimit);
+  if (pend_vec & 2u) mbar_wait(bar_vec0 + 8, (ph_vec >> 1) & 1u, kWaitLimit);
   if (pend_z) mbar_wait(bar_z, ph_z, kWaitLimit);
   tc_fence_before();
   __syncthreads();

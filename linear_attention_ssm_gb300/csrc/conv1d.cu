@@ -3,7 +3,7 @@
 // pegainfer PR #1152 "Reference golden for the GDN sublayer", Summary (depthwise conv, conv
 // kernel 4, no bias) and "Commands + measured numbers" (the conv leg is a bf16 tensor compared
 // bit-exact).  Memory-bound: tiles of 128 channels x 64 tokens (plus the 3-token halo) are staged
-// in shared memory by TMA through a 6-deep ring per CTA, each thread slides the 4-tap window over
+// in shared memory by TMA through a 4-deep ring per CTA, each thread slides the 4-tap window over
 // 16 tokens of a channel pair, and every output pair is written once as one 32-bit store.
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
@@ -12,15 +12,15 @@ namespace gdn {
 
 namespace {
 
-// Prefill kernel: persistent CTAs walk (channel slab, token tile) items; each item's raw inputs
-// (kSlab channels x (kTile + 3) tokens, the 3-token halo included) are staged in shared memory
-// by TMA through a kStages-deep ring, so every SM keeps ~100 KB of loads in flight.  Thread
+// Prefill kernel: persistent CTAs (three per SM) walk (channel slab, token tile) items; each item's
+// raw inputs (kSlab channels x (kTile + 3) tokens, the 3-token halo included) are staged in shared
+// memory by TMA through a kStages-deep ring, so every SM keeps ~200 KB of loads in flight.  Thread
 // (channel pair, token quarter) slides a 4-tap window over its 16 tokens.
 constexpr int kSlab = 128;                     // channels per tile: 256-byte rows
 constexpr int kTile = 64;                      // tokens per tile
 constexpr int kHalo = kConvWidth - 1;          // 3 earlier tokens
 constexpr int kRows = kTile + kHalo;           // rows staged per tile
-constexpr int kStages = 6;
+constexpr int kStages = 4;
 constexpr uint32_t kStageBytes = kRows * kSlab * 2;  // 17,152
 constexpr int kConvThreads = 256;              // 64 channel pairs x 4 token quarters
 constexpr int kQuarter = kTile / 4;
@@ -87,7 +87,7 @@ __device__ __forceinline__ float2 bf2x2(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
 }
 
-__global__ void __launch_bounds__(kConvThreads, 2) conv1d_silu_kernel(const __grid_constant__ ConvParams p) {
+__global__ void __launch_bounds__(kConvThreads, 3) conv1d_silu_kernel(const __grid_constant__ ConvParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kStages * kStageBytes);
@@ -279,7 +279,7 @@ cudaError_t launch_conv1d_prefill(const LaunchEnv& env, const uint16_t* x, const
     int sms = 0;
     if ((e = device_sm_count(&sms)) != cudaSuccess) return e;
     const long items = (long)p.nslab * p.ntile;
-    const long slots = 2L * sms;
+    const long slots = 3L * sms;  // three CTAs per SM (69 KB of shared memory, 80 registers)
     conv1d_silu_kernel<<<(unsigned)(items < slots ? items : slots), kConvThreads, kConvSmem, env.stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -49,7 +49,46 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--varlen-steps", type=int, default=10)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", default=None,
+                    help="run only the prefill (conv + chunk) on these comma-separated sequence lengths, "
+                         "--steps times after --warmup, for profiling; prints one timing line")
     return ap.parse_args()
+
+
+def run_profile_case(args, local):
+    """A small prefill workload for profilers: --warmup untimed calls, then --steps calls."""
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import linear_attention_ssm_gb300 as gdn
+    from linear_attention_ssm_gb300.synth import prefill_inputs
+    lengths = [int(v) for v in args.profile_case.split(",")]
+    inp = prefill_inputs(lengths, seed=2)
+    N, T = len(lengths), sum(lengths)
+    x, w, cu = inp["x"].to(dev), inp["conv_w"].to(dev), inp["cu_seqlens"].to(dev)
+    g, beta, z, nw = inp["g"].to(dev), inp["beta"].to(dev), inp["z"].to(dev), inp["norm_w"].to(dev)
+    state_in = inp["state0"].to(dev)
+    state_out = torch.empty_like(state_in)
+    qkv = torch.empty_like(x)
+    out = torch.empty((T, 48, 128), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(gdn.gdn_chunk_prefill_workspace_size(N, T), dtype=torch.uint8, device=dev)
+
+    def step():
+        gdn.gdn_conv1d_prefill(x, w, cu, None, None, qkv)
+        gdn.gdn_chunk_prefill(qkv, g, beta, cu, inp["q_scale"], 1e-6, state_in, state_out, z, nw, 1e-6, out,
+                              workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    gdn.gdn_check_device_errors()
+    print(json.dumps({"profile_case": lengths, "tokens": T, "ms_per_step": e0.elapsed_time(e1) / max(args.steps, 1)}))
 
 
 def dist_env():
@@ -418,7 +457,9 @@ def run_ours(args, rank, world, local):
 def main():
     args = parse()
     rank, world, local = dist_env()
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args, local)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local)

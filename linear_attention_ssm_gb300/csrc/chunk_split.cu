@@ -102,7 +102,8 @@ struct StateParams {
   int seg, nseg;              // chunk segment processed by this launch
   const float* state_src;     // state at the segment start: state_in (may be NULL) for the first, else state_out
   CUtensorMap tmap;
-  CUtensorMap tmap_z;  // z [T][Hv * 128] bf16, box 128 x 64, no swizzle (valid when z != NULL)
+  CUtensorMap tmap_z;    // z [T][Hv * 128] bf16, box 128 x 64, no swizzle (valid when z != NULL)
+  CUtensorMap tmap_out;  // out, same shape and box as z (valid when z != NULL)
   const int32_t* cu;
   const int32_t* order;
   unsigned* counter;
@@ -506,7 +507,10 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
     for (int i = 0; i < 10; ++i) mbar_init(smem_u32(&bars[i]), 1);
     fence_mbar_init();
     prefetch_tensormap(&p.tmap);
-    if (p.z) prefetch_tensormap(&p.tmap_z);
+    if (p.z) {
+      prefetch_tensormap(&p.tmap_z);
+      prefetch_tensormap(&p.tmap_out);
+    }
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), SC_COLS);
   tc_fence_before();
@@ -867,24 +871,33 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
             r[i][1] = __fmul2_rn(__fmul2_rn(r[i][1], __fmul2_rn(w23, rs)), s23);
           }
         }
+        // a full gated chunk goes out as one TMA store of a tile staged over its z rows (each warp
+        // overwrites only the z rows it has read); otherwise rows t < L are stored directly
+        const bool tile_store = gated && L == kChunk;
 #pragma unroll
         for (int i = 0; i < kTok; ++i) {
           const int t = warp + kWarps * i;
-          if (t < L) {
-            const size_t base = ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4;
-            *reinterpret_cast<uint2*>(p.out + base) =
-                make_uint2(pack_bf2(r[i][0].x, r[i][0].y), pack_bf2(r[i][1].x, r[i][1].y));
+          const uint2 packed = make_uint2(pack_bf2(r[i][0].x, r[i][0].y), pack_bf2(r[i][1].x, r[i][1].y));
+          if (tile_store) {
+            *reinterpret_cast<uint2*>(sm + SS_V + t * 256 + lane * 8) = packed;
+          } else if (t < L) {
+            *reinterpret_cast<uint2*>(p.out + ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4) = packed;
           }
         }
       }
-      fence_proxy_async_smem();  // vector-block and z reads precede the copies that refill those buffers
+      fence_proxy_async_smem();  // vector-block and z reads, output tile writes -> the async proxy
       tc_fence_before();
       __syncthreads();  // staging reads and accumulator reads done before the next chunk reuses them
       tc_fence_after();
-      if (gated && has_next) {
-        if (tid == 64) issue_v(c0 + kChunk, h);
-        pend_v = true;
+      if (tid == 64) {
+        if (gated && L == kChunk) {
+          tma_store_2d(&p.tmap_out, h * kHeadDim, c0, sb + SS_V);
+          bulk_commit_group();
+          bulk_wait_group_read0();  // the tile has been read out before the buffer takes the next v
+        }
+        if (gated && has_next) issue_v(c0 + kChunk, h);
       }
+      if (gated && has_next) pend_v = true;
     }
     if (!ok) break;
 
@@ -906,6 +919,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
     tc_fence_after();
   }
 
+  if (tid == 64) bulk_wait_group0();  // output tile stores complete
   // after an early exit, let copies still in flight land before the CTA leaves (bounded)
   if (pend_qk) mbar_wait(bar_qk, ph_qk, kWaitLimit);
   if (pend_v) mbar_wait(bar_v, ph_v, kWaitLimit);
@@ -1102,6 +1116,11 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
   sp.nseg = nseg;
   sp.tmap = tmap;
   sp.tmap_z = tmap_z;
+  if (z && T > 0) {
+    if ((e = encode_bf16_2d(&sp.tmap_out, out, (uint64_t)Hv * kHeadDim, (uint64_t)T, (uint64_t)Hv * kHeadDim * 2, 128,
+                            kChunk)) != cudaSuccess)
+      return e;
+  }
   sp.cu = cu; sp.order = lay.order; sp.chunk_off = lay.chunk_off; sp.rec = lay.rec;
   sp.state_in = state_in; sp.state_out = state_out; sp.z = z; sp.norm_w = norm_w; sp.out = out; sp.err = env.err;
   sp.N = N; sp.T = T; sp.Hk = Hk; sp.Hv = Hv; sp.nc_max = (int)nc_max; sp.rms_eps = rms_eps;

@@ -120,6 +120,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
+// 2D tiled bulk tensor store shared -> global (bulk-group completion): x must be 16-byte aligned
+// in bytes, and the box must lie where the caller may write.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap), "r"(x),
+               "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the committed bulk stores of this thread have finished reading shared memory / have completed
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // L2 prefetch hints (no completion to wait for): a 2D tensor box, or `bytes` (multiple of 16,
 // 16-byte aligned) of contiguous global memory.
 __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int x, int y) {

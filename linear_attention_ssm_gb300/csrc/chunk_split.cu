@@ -53,8 +53,9 @@ constexpr uint32_t kHeadBuf = 2 * kTriBytes + kBBytes;       // A, T, B of one V
 constexpr uint32_t PR_QK = 0;                                // 32 KB [K; Q] tile (TMA); dead once the Gram and
                                                              // the norms are taken, then the heads' buffers
 constexpr uint32_t PR_HEADS = 0;
-constexpr uint32_t PR_VEC = kGroup * kHeadBuf;               // gamma, beta (kGroup x 64 each), ik, iq, partial sums
-constexpr uint32_t PR_BAR = PR_VEC + (2 * kGroup * 64 + 2 * 64 + kParts * 128) * 4;
+constexpr uint32_t PR_VEC = kGroup * kHeadBuf;               // gamma, beta (kGroup x 64 each), ik, iq, partial sums,
+                                                             // gamma - log2 ik (kGroup x 64)
+constexpr uint32_t PR_BAR = PR_VEC + (3 * kGroup * 64 + 2 * 64 + kParts * 128) * 4;
 constexpr uint32_t PR_USED = PR_BAR + 64;
 constexpr uint32_t PR_BYTES = PR_USED + 1024;
 static_assert(PR_VEC >= 32768, "the q/k tile must fit under the head buffers");
@@ -265,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
   float* s_ik = s_beta + kGroup * 64;
   float* s_iq = s_ik + 64;
   float* s_part = s_iq + 64;
+  float* s_gk = s_part + kParts * 128;  // [kGroup][64] gamma_j - log2 ik_j: exp2(gamma_t - s_gk[j]) = decay ik_j
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PR_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PR_BAR + 32);
   const uint32_t bar_qk = smem_u32(&bars[0]), bar_g = smem_u32(&bars[1]);
@@ -404,7 +406,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
         vec[V_CS + t] = (t < L) ? ex2_approx(gL - gt) * s_ik[t] : 0.f;
         vec[V_CO + t] = Gam * s_iq[t] * p.q_scale;
         vec[V_MISC + t] = (t == 0) ? ex2_approx(gL) : 0.f;
+        s_gk[g * 64 + t] = gt - lg2_approx(s_ik[t]);
       }
+      __syncthreads();
       // A (rows 0..63, blocks on and below the diagonal) and P (rows 64..127, straight to the record);
       // the warps whose 32 rows and 32 columns all lie above the diagonal (token j > t) have no work
       float gr[kW];  // raw Gram row `row`, columns part * kW ..
@@ -419,38 +423,39 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
         }
       }
       for (int g = 0; g < G && !all_masked; ++g) {
-        const float* gam = s_gam + g * 64;
+        // a pair of columns j, j + 1: scale * gram * exp2(gamma_t - gk_j), with gk_j = gamma_j - log2 ik_j
+        const float* gk = s_gk + g * 64;
+        const int t = row & 63;
+        const float gt = s_gam[g * 64 + t];
+        const float scale = row < 64 ? s_beta[g * 64 + t] * s_ik[t] : s_iq[t] * p.q_scale;
+        const float2 gt2 = make_float2(gt, gt), neg1 = make_float2(-1.f, -1.f);
+        auto pair = [&](int j, int i) {  // columns j, j + 1 (this thread's gram entries i, i + 1)
+          const float2 d = __ffma2_rn(*reinterpret_cast<const float2*>(gk + j), neg1, gt2);
+          return __fmul2_rn(__fmul2_rn(make_float2(gr[i], gr[i + 1]), make_float2(scale, scale)),
+                            make_float2(ex2_approx(d.x), ex2_approx(d.y)));
+        };
         if (row < 64) {
-          const int t = row;
           float* sA = reinterpret_cast<float*>(sm + PR_HEADS + g * kHeadBuf);
-          const float bt = s_beta[g * 64 + t] * s_ik[t], gt = gam[t];
 #pragma unroll
           for (int i4 = 0; i4 < kW; i4 += 4) {
             const int j0 = part * kW + i4;
             if ((j0 >> 4) > (t >> 4)) continue;  // above the diagonal blocks: never read
-            const float4 gj = *reinterpret_cast<const float4*>(gam + j0);
-            const float4 kj = *reinterpret_cast<const float4*>(s_ik + j0);
-            const float gv[4] = {gj.x, gj.y, gj.z, gj.w}, kv[4] = {kj.x, kj.y, kj.z, kj.w};
-            float a[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float val = bt * ex2_approx(gt - gv[u]) * gr[i4 + u] * kv[u];
-              a[u] = (j0 + u < t) ? val : 0.f;
-            }
-            *reinterpret_cast<float4*>(sA + tri(t, j0)) = make_float4(a[0], a[1], a[2], a[3]);
+            const float2 a01 = pair(j0, i4), a23 = pair(j0 + 2, i4 + 2);
+            *reinterpret_cast<float4*>(sA + tri(t, j0)) =
+                make_float4(j0 < t ? a01.x : 0.f, j0 + 1 < t ? a01.y : 0.f, j0 + 2 < t ? a23.x : 0.f,
+                            j0 + 3 < t ? a23.y : 0.f);
           }
         } else {
-          const int t = row - 64;
           uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h0 + g) * REC_BYTES;
-          const float qt = s_iq[t] * p.q_scale, gt = gam[t];
 #pragma unroll
           for (int i0 = 0; i0 < kW; i0 += 8) {
-            float v[8];
             const int j0 = part * kW + i0;
+            float v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float a = qt * ex2_approx(gt - gam[j0 + u]) * gr[i0 + u] * s_ik[j0 + u];
-              v[u] = (j0 + u <= t) ? a : 0.f;
+            for (int u = 0; u < 8; u += 2) {
+              const float2 a = pair(j0 + u, i0 + u);
+              v[u] = j0 + u <= t ? a.x : 0.f;
+              v[u + 1] = j0 + u + 1 <= t ? a.y : 0.f;
             }
             store8_split(rec + REC_P, nullptr, 0, t, j0, v);
           }

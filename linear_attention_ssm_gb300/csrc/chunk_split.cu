@@ -80,19 +80,12 @@ constexpr uint32_t SC_X = 128;    //  64: S0 K^T, then R (bf16 hi/lo pairs: MMA 
 constexpr uint32_t SC_O1 = 192;   //  64: S0 Q^T, then E^T, then E P^T
 constexpr uint32_t SC_COLS = 256;
 
-// The chunks of sequence n (nch of them) are split into nseg contiguous segments, segment k holding
-// chunk indices [seg_begin(k), seg_begin(k + 1)).  The prep kernel of segment k + 1 runs beside the
-// state kernel of segment k, so only the first segment's prep is exposed: with four segments they
-// take 1/8, 2/8, 2/8 and 3/8 of the chunks (a short first segment, each prep no longer than the
-// state work it hides behind).
+// The chunks of sequence n (nch of them) are split into nseg contiguous segments; segment k holds
+// chunk indices [k nch / nseg, (k + 1) nch / nseg).  The prep kernel of segment k + 1 runs beside
+// the state kernel of segment k, so only the first segment's prep is exposed.  (Equal segments:
+// a short first segment measured slower once the conv kernel runs before the call.)
 constexpr int kMaxSegments = 4;
-__host__ __device__ __forceinline__ int seg_begin(int k, int nch, int nseg) {
-  if (nseg == 4) {
-    const int eighths = k == 0 ? 0 : (k == 1 ? 1 : (k == 2 ? 3 : (k == 3 ? 5 : 8)));
-    return (int)(((long)eighths * nch) / 8);
-  }
-  return (int)(((long)k * nch) / nseg);
-}
+__host__ __device__ __forceinline__ int seg_begin(int k, int nch, int nseg) { return (int)(((long)k * nch) / nseg); }
 
 struct PrepParams {
   CUtensorMap tmap;  // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle

@@ -25,6 +25,7 @@
 // CTA's waits hide behind the other's work.
 #include <cuda.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "chunk_common.cuh"
@@ -684,8 +685,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       }
       if (!ok) break;
       const float gL = vec[V_MISC];
-      if (tid == 32 && has_next) issue_vec(gc + 1, h, vb ^ 1);  // that buffer's last reader was chunk c - 1
-      if (has_next) pend_vec |= 1u << (vb ^ 1);
+
 
       // ================= [X | O1] = S0 [K; Q]^T one 64-key half at a time: X from the hi and lo
       // parts of S0, the output-only O1 from the hi part
@@ -765,10 +765,13 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
           mma_bf16_k2_ta<2>(tmem + SC_O1, tmem + SC_X + 32 * pp + 16, sw128_desc(sb + SS_T) + 4 * pp, ID64, 1);
         mma_commit(bar_e);
       } else if (tid == 32) {
-        // the V buffer is free: the gate input of this chunk (gated), else the next chunk's v
+        // the V buffer is free: the gate input of this chunk (gated), else the next chunk's v; and
+        // the next chunk's vector block into the other buffer (last read by chunk c - 1)
         if (gated) issue_z(c0, h);
         else if (has_next) issue_v(c0 + kChunk, h);
+        if (has_next) issue_vec(gc + 1, h, vb ^ 1);
       }
+      if (has_next) pend_vec |= 1u << (vb ^ 1);
       pend_z = gated;
       pend_v = !gated && has_next;
       // o1 diag(c_o) -> the staging area (token-major fp32), free since the X MMAs completed
@@ -1143,7 +1146,11 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
     if (T > 0 && nc_max > 0) {
       pp.seg = k;
       pp.seg_pref = lay.seg_pref + (size_t)k * (N + 1);
-      chunk_prep_kernel<<<(unsigned)slots, kThreads, PR_BYTES, side>>>(pp);
+      // Segment 0's prep runs alone on the whole GPU.  Later ones run beside a state kernel: they
+      // take only the CTA slots the state kernel leaves (a prep CTA fits beside one state CTA),
+      // so the state CTAs are placed the same way whichever launch the scheduler sees first.
+      const long prep_grid = k == 0 ? slots : std::max<long>(sms / 2, slots - state_grid);
+      chunk_prep_kernel<<<(unsigned)prep_grid, kThreads, PR_BYTES, side>>>(pp);
       if ((e = cudaGetLastError()) != cudaSuccess) break;
     }
     if (nseg > 1) {

@@ -1085,15 +1085,14 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
   if ((e = device_sm_count(&sms)) != cudaSuccess) return e;
 
   // Segments: with a state_out buffer to carry the state between launches, a long enough input
-  // and no stream capture in progress, the chunks of every sequence are split into kMaxSegments
-  // parts and the prep kernel of part k + 1 (on a side stream) runs beside the state kernel of
+  // and no stream capture in progress, the chunks of every sequence are split into three parts and the prep kernel of part k + 1 (on a side stream) runs beside the state kernel of
   // part k; otherwise one part, everything on the caller's stream.
   int nseg = 1;
   cudaStream_t side = env.stream;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (state_out && T >= 64 * kChunk && cudaStreamIsCapturing(env.stream, &cap) == cudaSuccess &&
       cap == cudaStreamCaptureStatusNone && side_stream(&side) == cudaSuccess)
-    nseg = kMaxSegments;
+    nseg = 3;  // measured best of 2, 3 and 4 over the batched and the varlen workloads
   if (nseg == 1) side = env.stream;
   chunk_segments_kernel<<<1, 1024, 0, env.stream>>>(cu, N, nseg, lay.seg_pref, lay.counters);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -239,7 +239,7 @@ def test_minimum_workspace_runs_the_fused_kernel():
 
 
 def test_segmented_split_path():
-    """Inputs of 4,096 tokens or more run the split path as four chunk segments per sequence (the
+    """Inputs of 4,096 tokens or more run the split path as three chunk segments per sequence (the
     state carried through state_out between segment launches, prep of the next segment beside the
     state kernel of the current one): sequences of 1..4095 tokens, an empty one, several
     segment-boundary positions, state in place and out of place."""

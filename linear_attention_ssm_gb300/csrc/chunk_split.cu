@@ -1085,8 +1085,9 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
   if ((e = device_sm_count(&sms)) != cudaSuccess) return e;
 
   // Segments: with a state_out buffer to carry the state between launches, a long enough input
-  // and no stream capture in progress, the chunks of every sequence are split into three parts and the prep kernel of part k + 1 (on a side stream) runs beside the state kernel of
-  // part k; otherwise one part, everything on the caller's stream.
+  // and no stream capture in progress, the chunks of every sequence are split into three parts
+  // and the prep kernel of part k + 1 (on a side stream) runs beside the state kernel of part k;
+  // otherwise one part, everything on the caller's stream.
   int nseg = 1;
   cudaStream_t side = env.stream;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;

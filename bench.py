@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-steps", type=int, default=640)
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--varlen-steps", type=int, default=10)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", default=None,
@@ -322,7 +322,10 @@ def run_ours(args, rank, world, local):
                  "algorithmic_bytes_per_launch": conv_bytes, "traffic": crec["bytes_per_launch"] if crec else None}
     conv_roof["frac"] = conv_roof["achieved"] / hbm_peak
 
-    # ---------------- end to end through host buffers (pinned), same step
+    # ---------------- end to end through host buffers (pinned): every step copies its inputs from
+    # host to device, runs the prefill and reads its outputs back to the host.  Device inputs and
+    # outputs are double-buffered and the copies run on two copy streams, so the H2D copy of step
+    # i + 1 and the D2H read of step i - 1 overlap the prefill of step i (a serving loop's layout).
     h_x, h_g, h_b, h_z = (inp["x"].pin_memory(), inp["g"].pin_memory(), inp["beta"].pin_memory(),
                           inp["z"].pin_memory())
     h_state, h_cs = inp["state0"].pin_memory(), inp["conv_state0"].pin_memory()
@@ -331,30 +334,55 @@ def run_ours(args, rank, world, local):
     h_cs_out = torch.empty_like(h_cs).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (h_x, h_g, h_b, h_z, h_state, h_cs))
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_state_out, h_cs_out))
+    cin, cin2, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    bufs = [dict(x=x, g=g, beta=beta, z=z, st=state_in, cs=cs_in, out=out, st_out=state_out, cs_out=cs_out)]
+    bufs.append({k: torch.empty_like(v) for k, v in bufs[0].items()})
+    ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in", "in2", "comp", "out")}
 
-    def e2e_step():
-        x.copy_(h_x, non_blocking=True)
-        g.copy_(h_g, non_blocking=True)
-        beta.copy_(h_b, non_blocking=True)
-        z.copy_(h_z, non_blocking=True)
-        state_in.copy_(h_state, non_blocking=True)
-        cs_in.copy_(h_cs, non_blocking=True)
-        prefill_step()
-        h_out.copy_(out, non_blocking=True)
-        h_state_out.copy_(state_out, non_blocking=True)
-        h_cs_out.copy_(cs_out, non_blocking=True)
+    def e2e_step(i):
+        bi = i % 2
+        B = bufs[bi]
+        # two H2D streams (x on one, the rest on the other): two copy engines in flight
+        for st_, key, pairs in ((cin, "in", (("x", h_x),)),
+                                (cin2, "in2", (("g", h_g), ("beta", h_b), ("z", h_z), ("st", h_state), ("cs", h_cs)))):
+            with torch.cuda.stream(st_):
+                st_.wait_event(ev["comp"][bi])  # the prefill two steps back has read this buffer's inputs
+                for k, h in pairs:
+                    B[k].copy_(h, non_blocking=True)
+                ev[key][bi].record(st_)
+        stream.wait_event(ev["in"][bi])
+        stream.wait_event(ev["in2"][bi])
+        stream.wait_event(ev["out"][bi])  # the outputs two steps back have been read out
+        gdn.gdn_conv1d_prefill(B["x"], w, cu, B["cs"], B["cs_out"], qkv)
+        gdn.gdn_chunk_prefill(qkv, B["g"], B["beta"], cu, inp["q_scale"], 1e-6, B["st"], B["st_out"], B["z"], nw,
+                              1e-6, B["out"], workspace=ws)
+        ev["comp"][bi].record(stream)
+        with torch.cuda.stream(cout):
+            cout.wait_event(ev["comp"][bi])
+            h_out.copy_(B["out"], non_blocking=True)
+            h_state_out.copy_(B["st_out"], non_blocking=True)
+            h_cs_out.copy_(B["cs_out"], non_blocking=True)
+            ev["out"][bi].record(cout)
 
-    e2e_step()
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
     barrier()
     s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s2.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    cin.wait_stream(stream)  # no copy of the timed steps starts before the start mark
+    cin2.wait_stream(stream)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    stream.wait_stream(cout)
+    stream.wait_stream(cin)
+    stream.wait_stream(cin2)
     e2.record(stream)
     torch.cuda.synchronize()
+    gdn.gdn_check_device_errors()
     e2e_ms = max_over_ranks(s2.elapsed_time(e2)) / args.e2e_steps
     e2e_value = replica_throughput(T, world, e2e_ms)
-    del h_x, h_g, h_b, h_z
+    del h_x, h_g, h_b, h_z, bufs
 
     # ---------------- varlen prefill: 8 packed sequences, 31,735 tokens (same path)
     del x, qkv, z, out, ws
@@ -443,10 +471,12 @@ def run_ours(args, rank, world, local):
                        "l2": "inputs larger than L2 (x 335 MB per step)", "parallelism": f"replicas x{world}"},
             "roofline": roofline, "roofline_conv": conv_roof,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms},
+                    "ms_per_step": e2e_ms, "steps": args.e2e_steps,
+                    "pipelined": "H2D of step i+1 and D2H of step i-1 overlap the prefill of step i"},
             "decode": decode, "varlen": varlen, "cpu_baseline": cpu, "clocks": clk,
-            # per step: conv1d + conv-state kernels, then the schedule, prep and state kernels
-            "gpu_launches": 5 * args.steps,
+            # per step: conv1d + conv-state kernels, the chunk prefill's schedule and segment-table
+            # kernels, then a prep and a state kernel for each of its three chunk segments
+            "gpu_launches": (2 + 2 + 2 * 3) * args.steps,
             "arithmetic": "bf16 tensor-core operands (fp32 operands split into bf16 hi+lo), fp32 accumulate and state",
         }
         print(json.dumps(line), flush=True)

@@ -260,3 +260,64 @@ def test_segmented_split_path():
     g.gdn_check_device_errors()
     assert torch.equal(o2, out)
     assert torch.equal(s2, st)
+
+
+def _long_case(seed):
+    """4,352 tokens (segmented split path) on the small geometry, inputs on the device."""
+    geo = Geometry(num_k_heads=2, num_v_heads=6)
+    inp = prefill_inputs([3000, 1, 1351], seed=seed, geo=geo)
+    ref = run_oracle(inp, geo=geo)
+    d = {k: v.to(DEV) for k, v in inp.items() if torch.is_tensor(v)}
+    return geo, inp, ref, d
+
+
+def test_captured_call_replays_exactly():
+    """A call captured in a CUDA graph (one segment, everything on the capturing stream) replays to
+    the same bits as the eager call (three segments on two streams)."""
+    g = lib()
+    geo, inp, ref, d = _long_case(61)
+    N, T = 3, ref["y"].shape[0]
+    y = ref["y"].to(DEV)
+    ws = torch.empty(g.gdn_chunk_prefill_workspace_size(N, T, geometry=geo), dtype=torch.uint8, device=DEV)
+    out_e = torch.empty((T, 6, 128), dtype=torch.bfloat16, device=DEV)
+    st_e = torch.empty_like(d["state0"])
+    g.gdn_chunk_prefill(y, d["g"], d["beta"], d["cu_seqlens"], inp["q_scale"], 1e-6, d["state0"], st_e, d["z"],
+                        d["norm_w"], 1e-6, out_e, workspace=ws, geometry=geo)
+    g.gdn_check_device_errors()
+    assert_out_close(out_e, ref["out"])
+    out_c = torch.empty_like(out_e)
+    st_c = torch.empty_like(st_e)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            g.gdn_chunk_prefill(y, d["g"], d["beta"], d["cu_seqlens"], inp["q_scale"], 1e-6, d["state0"], st_c,
+                                d["z"], d["norm_w"], 1e-6, out_c, workspace=ws, geometry=geo)
+    graph.replay()
+    torch.cuda.synchronize()
+    g.gdn_check_device_errors()
+    assert torch.equal(out_c, out_e) and torch.equal(st_c, st_e)
+
+
+def test_concurrent_calls_on_two_streams():
+    """Two segmented calls issued on two streams at once (they share the library's side stream)
+    each match the oracle."""
+    g = lib()
+    cases = [_long_case(71), _long_case(72)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    results = []
+    for (geo, inp, ref, d), s in zip(cases, streams):
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            T = ref["y"].shape[0]
+            st = torch.empty_like(d["state0"])
+            out = g.gdn_chunk_prefill(ref["y"].to(DEV), d["g"], d["beta"], d["cu_seqlens"], inp["q_scale"], 1e-6,
+                                      d["state0"], st, d["z"], d["norm_w"], 1e-6, geometry=geo)
+            results.append((out, st))
+    torch.cuda.synchronize()
+    g.gdn_check_device_errors()
+    for (geo, inp, ref, d), (out, st) in zip(cases, results):
+        assert_out_close(out, ref["out"])
+        for n in range(3):
+            assert_state_close(st[n], ref["state"][n], f"state of sequence {n}")

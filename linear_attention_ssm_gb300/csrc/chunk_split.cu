@@ -148,9 +148,9 @@ __device__ __forceinline__ int tri(int r, int c) {
 }
 
 // T_g = (I + A_g)^-1 for G <= kGroup strictly lower triangular 64 x 64 matrices at once (head g's
-// A, T and B blocks at base + g * kHeadBuf bytes): the five steps of the blocked forward
-// substitution of solve_unit_lower, each step's independent block tasks of all G heads spread
-// over the CTA's warps, so the G solves share the five barriers.
+// A, T and scratch blocks at base + g * kHeadBuf bytes): the diagonal 16 x 16 blocks inverted by
+// forward substitution (one column per thread), then block forward substitution down each block
+// column by one warp; two CTA barriers in all.
 __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   if (tid < 64 * G) {  // step 1: diagonal blocks, one column per thread
@@ -170,75 +170,67 @@ __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
     for (int i = 0; i < 16; ++i) sT[tri(o + i, o + c)] = x[i];  // zeros above the diagonal included
   }
   __syncthreads();
-  const int c0 = (lane & 3) * 4;
-  // Row u of a 16 x 16 block, columns c0..c0+3: float4 offset u * 16 + lane_off[u & 3] (the XOR
-  // swizzle of the row's float4 index by u & 3, resolved per lane once).
-  int lane_off[4];
-#pragma unroll
-  for (int m = 0; m < 4; ++m) lane_off[m] = (((c0 >> 2) ^ m) << 2);
-  // 16 entries of row r of a tri-layout block (four float4 reads)
-  auto tri_row = [&](const float* blk, int r, float (&v)[16]) {
+  // Block columns: for each head and block column j < 3, one warp runs the forward substitution
+  // down the column, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj (i = j + 1 .. 3), with only warp-level
+  // synchronisation; the block columns of a head (and the heads) are independent.  Lane: row
+  // r = lane / 2 of a 16 x 16 block, eight columns from c8.
+  const int r = lane >> 1, c8 = (lane & 1) * 8;
+  auto blk = [](int i, int k) { return (i * (i + 1) / 2 + k) * 256; };
+  auto row16 = [&](const float* b16, int rr, float (&v)[16]) {  // row rr of a tri-layout block
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float4 f = *reinterpret_cast<const float4*>(blk + r * 16 + ((q ^ (r & 3)) << 2));
+      const float4 f = *reinterpret_cast<const float4*>(b16 + rr * 16 + ((q ^ (rr & 3)) << 2));
       v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
     }
   };
-  // acc (two chains of four columns) += sum_u a[u] * blk[u][c0..c0+3]
-  auto row_times_block = [&](const float (&a)[16], const float* blk, float2 (&acc)[4]) {
+  // acc[0..7] += sum_u a[u] * b16[u][c8 .. c8 + 7] (tri-layout block)
+  auto row_times_block = [&](const float (&a)[16], const float* b16, float2 (&acc)[4]) {
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
-      const float4 bv = *reinterpret_cast<const float4*>(blk + u * 16 + lane_off[u & 3]);
-      float2* ac = acc + 2 * (u & 1);
-      ac[0] = __ffma2_rn(make_float2(a[u], a[u]), make_float2(bv.x, bv.y), ac[0]);
-      ac[1] = __ffma2_rn(make_float2(a[u], a[u]), make_float2(bv.z, bv.w), ac[1]);
+      const float4 f0 = *reinterpret_cast<const float4*>(b16 + u * 16 + ((((c8 >> 2)) ^ (u & 3)) << 2));
+      const float4 f1 = *reinterpret_cast<const float4*>(b16 + u * 16 + ((((c8 >> 2) + 1) ^ (u & 3)) << 2));
+      const float2 au = make_float2(a[u], a[u]);
+      acc[0] = __ffma2_rn(au, make_float2(f0.x, f0.y), acc[0]);
+      acc[1] = __ffma2_rn(au, make_float2(f0.z, f0.w), acc[1]);
+      acc[2] = __ffma2_rn(au, make_float2(f1.x, f1.y), acc[2]);
+      acc[3] = __ffma2_rn(au, make_float2(f1.z, f1.w), acc[3]);
     }
   };
-  // step 2: B_ik = T_ii A_ik, twelve half-block tasks per head
-  for (int task = warp; task < 12 * G; task += kWarps) {
-    const int g = task / 12, tt = task - 12 * g;
+  for (int task = warp; task < 3 * G; task += kWarps) {  // the longest columns (j = 0) first
+    const int jb = task / G, g = task - jb * G;
     const float* sA = reinterpret_cast<const float*>(base + g * kHeadBuf);
-    const float* sT = reinterpret_cast<const float*>(base + g * kHeadBuf + kTriBytes);
-    float* sB = reinterpret_cast<float*>(base + g * kHeadBuf + 2 * kTriBytes);
-    const int pidx = tt >> 1;
-    const int i = pidx < 1 ? 1 : (pidx < 3 ? 2 : 3), k = pidx - pair_index(i, 0);
-    const int rr = (tt & 1) * 8 + (lane >> 2);
-    float a[16];
-    tri_row(sT + (i * (i + 1) / 2 + i) * 256, rr, a);  // row rr of T_ii (zero above the diagonal)
-    float2 acc[4] = {};
-    row_times_block(a, sA + (i * (i + 1) / 2 + k) * 256, acc);
-    *reinterpret_cast<float4*>(sB + pidx * 320 + rr * 20 + c0) =
-        make_float4(acc[0].x + acc[2].x, acc[0].y + acc[2].y, acc[1].x + acc[3].x, acc[1].y + acc[3].y);
+    float* sT = reinterpret_cast<float*>(base + g * kHeadBuf + kTriBytes);
+    float* sY = reinterpret_cast<float*>(base + g * kHeadBuf + 2 * kTriBytes) + jb * 320;  // 16 x 20 scratch
+    for (int i = jb + 1; i < 4; ++i) {
+      float2 y[4] = {};
+      for (int k = jb; k < i; ++k) {
+        float a[16];
+        row16(sA + blk(i, k), r, a);
+        row_times_block(a, sT + blk(k, jb), y);
+      }
+      *reinterpret_cast<float4*>(sY + r * 20 + c8) = make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
+      *reinterpret_cast<float4*>(sY + r * 20 + c8 + 4) = make_float4(y[2].x, y[2].y, y[3].x, y[3].y);
+      __syncwarp();
+      float a[16];
+      row16(sT + blk(i, i), r, a);
+      float2 t[4] = {};
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const float4 f0 = *reinterpret_cast<const float4*>(sY + u * 20 + c8);
+        const float4 f1 = *reinterpret_cast<const float4*>(sY + u * 20 + c8 + 4);
+        const float2 au = make_float2(a[u], a[u]);
+        t[0] = __ffma2_rn(au, make_float2(f0.x, f0.y), t[0]);
+        t[1] = __ffma2_rn(au, make_float2(f0.z, f0.w), t[1]);
+        t[2] = __ffma2_rn(au, make_float2(f1.x, f1.y), t[2]);
+        t[3] = __ffma2_rn(au, make_float2(f1.z, f1.w), t[3]);
+      }
+      *reinterpret_cast<float4*>(sT + tri(i * 16 + r, jb * 16 + c8)) = make_float4(-t[0].x, -t[0].y, -t[1].x, -t[1].y);
+      *reinterpret_cast<float4*>(sT + tri(i * 16 + r, jb * 16 + c8 + 4)) =
+          make_float4(-t[2].x, -t[2].y, -t[3].x, -t[3].y);
+      __syncwarp();  // T_ij feeds the next block row of this column; sY is rewritten there
+    }
   }
   __syncthreads();
-  // steps 3-5: T_ij = - sum_{k=j}^{i-1} B_ik T_kj for block distance d = i - j
-#pragma unroll
-  for (int d = 1; d < 4; ++d) {
-    const int per = 2 * (4 - d);
-    for (int task = warp; task < per * G; task += kWarps) {
-      const int g = task / per, w = task - per * g;
-      float* sT = reinterpret_cast<float*>(base + g * kHeadBuf + kTriBytes);
-      const float* sB = reinterpret_cast<const float*>(base + g * kHeadBuf + 2 * kTriBytes);
-      const int i = d + (w >> 1), jb = i - d;
-      const int r = (w & 1) * 8 + (lane >> 2);
-      float2 acc[4] = {};
-#pragma unroll
-      for (int kk = 0; kk < d; ++kk) {
-        const int k = jb + kk;
-        const float* Bik = sB + pair_index(i, k) * 320 + r * 20;
-        float a[16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 f = *reinterpret_cast<const float4*>(Bik + 4 * q);
-          a[4 * q] = f.x; a[4 * q + 1] = f.y; a[4 * q + 2] = f.z; a[4 * q + 3] = f.w;
-        }
-        row_times_block(a, sT + (k * (k + 1) / 2 + jb) * 256, acc);
-      }
-      *reinterpret_cast<float4*>(sT + tri(i * 16 + r, jb * 16 + c0)) =
-          make_float4(-(acc[0].x + acc[2].x), -(acc[0].y + acc[2].y), -(acc[1].x + acc[3].x), -(acc[1].y + acc[3].y));
-    }
-    __syncthreads();
-  }
 }
 
 // Persistent CTAs walk the (chunk, K head) units of one chunk segment.  Thread (row, part) owns
@@ -697,7 +689,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       tc_fence_after();
       if (!ok) break;
       if (tid == 0) {
-#pragma unroll
         mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W), sw128_desc(sb + SS_QK), ID128, 0);
         mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W + 16384), sw128_desc(sb + SS_QK), ID64, 1);
         mma_commit(bar_h);
@@ -707,7 +698,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       convert_half(64, gL);
       operands_ready();
       if (tid == 0) {
-#pragma unroll
         mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W), sw128_desc(sb + SS_QK + 16384), ID128, 1);
         mma_bf16_k4<2, 2>(tmem + SC_X, sw128_desc(sb + SS_W + 16384), sw128_desc(sb + SS_QK + 16384), ID64, 1);
         mma_commit(bar_x);

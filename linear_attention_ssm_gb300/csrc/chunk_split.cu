@@ -196,7 +196,11 @@ __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
       acc[3] = __ffma2_rn(au, make_float2(f1.z, f1.w), acc[3]);
     }
   };
-  for (int task = warp; task < 3 * G; task += kWarps) {  // the longest columns (j = 0) first
+  // tasks in column order (the longest, j = 0, first); warp w takes task w, and the one task past
+  // the eighth (three heads) goes to the last warp, whose own task (j = 2) is one of the shortest
+  for (int n_task = 0; n_task < 2; ++n_task) {
+    const int task = n_task == 0 ? warp : (warp == kWarps - 1 ? kWarps : 3 * G);
+    if (task >= 3 * G) break;
     const int jb = task / G, g = task - jb * G;
     const float* sA = reinterpret_cast<const float*>(base + g * kHeadBuf);
     float* sT = reinterpret_cast<float*>(base + g * kHeadBuf + kTriBytes);

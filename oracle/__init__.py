@@ -69,6 +69,13 @@ def _load():
             lib.oracle_decode_step.argtypes = [
                 I, I, I, I, I, I, P, P, P, P, P, P, P, P, D, D, D, P, P, I, I]
             lib.oracle_decode_step.restype = I
+            lib.oracle_round_f16.argtypes = [D]
+            lib.oracle_round_f16.restype = ctypes.c_uint16
+            lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_f16_to_double.restype = D
+            lib.oracle_decode_step_h16.argtypes = [
+                I, I, I, I, I, I, P, P, P, P, P, P, P, P, D, D, D, P, P, I, I]
+            lib.oracle_decode_step_h16.restype = I
             _lib = lib
     return _lib
 
@@ -104,6 +111,23 @@ def round_bf16(x: torch.Tensor) -> torch.Tensor:
     flat = x.detach().cpu().to(torch.float64).reshape(-1).tolist()
     bits = np.array([lib.oracle_round_bf16(v) for v in flat], dtype=np.uint16)
     return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).reshape(x.shape)
+
+
+def round_f16(x: torch.Tensor) -> torch.Tensor:
+    """Round float64 values to IEEE binary16 with ties to even; returns a torch.float16 tensor."""
+    lib = _load()
+    flat = x.detach().cpu().to(torch.float64).reshape(-1).tolist()
+    bits = np.array([lib.oracle_round_f16(v) for v in flat], dtype=np.uint16)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.float16).reshape(x.shape)
+
+
+def f16_to_double(h: torch.Tensor) -> torch.Tensor:
+    """Widen binary16 values (torch.float16) to float64 by decoding their bit patterns."""
+    lib = _load()
+    assert h.dtype == torch.float16, h.dtype
+    bits = h.detach().cpu().contiguous().view(torch.int16).reshape(-1).numpy().view(np.uint16)
+    vals = [lib.oracle_f16_to_double(int(b)) for b in bits]
+    return torch.tensor(vals, dtype=torch.float64).reshape(h.shape)
 
 
 def conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in=None, mutation: int = 0):
@@ -196,6 +220,34 @@ def decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, num_k_heads, n
     if rc != 0:
         raise ValueError(f"oracle_decode_step failed ({rc})")
     return out, o_raw, cs.view(torch.bfloat16), st
+
+
+def decode_step_h16(x, conv_w, conv_state, g, beta, state, z, norm_w, num_k_heads, num_v_heads,
+                    head_k_dim, head_v_dim, q_scale, l2_eps=1e-6, rms_eps=1e-6, nthreads: int = 0,
+                    mutation: int = 0):
+    """decode_step with the recurrent state stored as binary16 (torch.float16 [B,Hv,Dv,Dk]).
+
+    The state is widened exactly, the step runs in float64, the output comes from the new state
+    before rounding and the new state is rounded once to binary16.  Returns (out, o_raw,
+    conv_state', state' float16); the arguments are not modified.
+    """
+    lib = _load()
+    assert state.dtype == torch.float16, state.dtype
+    B, C = x.shape
+    W = conv_w.shape[1]
+    hk, hv, dk, dv = num_k_heads, num_v_heads, head_k_dim, head_v_dim
+    cs = _bf16_bits(conv_state).clone()
+    st = state.detach().cpu().contiguous().view(torch.int16).clone()
+    out = torch.empty((B, hv, dv), dtype=torch.float64)
+    o_raw = torch.empty((B, hv, dv), dtype=torch.float64)
+    rc = lib.oracle_decode_step_h16(hk, hv, dk, dv, W, B, _ptr(_bf16_bits(x)), _ptr(_bf16_bits(conv_w)),
+                                    _ptr(cs), _ptr(_f32(g)), _ptr(_f32(beta)), _ptr(st),
+                                    _ptr(_bf16_bits(z)), _ptr(_bf16_bits(norm_w)), float(q_scale),
+                                    float(l2_eps), float(rms_eps), _ptr(out), _ptr(o_raw),
+                                    int(nthreads), int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_step_h16 failed ({rc})")
+    return out, o_raw, cs.view(torch.bfloat16), st.view(torch.float16)
 
 
 def prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, num_k_heads, num_v_heads, head_k_dim,

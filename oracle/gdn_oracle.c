@@ -30,6 +30,9 @@
  *   5. the one-token decode step: conv step on a (W-1)-deep shift register of raw inputs,
  *      then steps 2-4 for one token -- Qwen3.8 kernel architecture and TDD ledger, "Current
  *      dense-27B kernel map" (scalar GDN recurrence and fused output gate).
+ *   6. the same decode step with the recurrent state stored as IEEE binary16: widened on load,
+ *      the step in double, rounded once (ties to even) on store -- the same ledger, the FP16
+ *      h-state twins of the decode kernels.
  *
  * Mutations (negative controls) can be planted here, on the CPU, through the `mutation`
  * bit set; 0 is the method.  See ORACLE_MUT_* below.
@@ -366,5 +369,69 @@ int oracle_decode_step(int hk, int hv, int dk, int dv, int W, int B, const uint1
   free(a);
   free(cu);
   if (!o_raw) free(o);
+  return rc;
+}
+
+/* ---------------------------------------------------------------- 6. decode with an fp16 state */
+
+/* IEEE 754 binary16 (1 sign, 5 exponent bits with bias 15, 10 stored mantissa bits) -> double.
+ * Exponent field 0 holds zero and the subnormals (mantissa * 2^-24); field 31 holds the
+ * infinities and NaNs. */
+double oracle_f16_to_double(uint16_t h) {
+  const double sign = (h & 0x8000) ? -1.0 : 1.0;
+  const int ex = (h >> 10) & 0x1F;
+  const int man = h & 0x3FF;
+  if (ex == 0x1F) return man ? NAN : sign * INFINITY;
+  if (ex == 0) return sign * ldexp((double)man, -24);
+  return sign * ldexp((double)(0x400 | man), ex - 25);
+}
+
+/* Round a double to the nearest binary16, ties to even, directly from the exact value.  Values
+ * whose rounded magnitude exceeds the largest finite binary16 (65504) become infinities. */
+uint16_t oracle_round_f16(double x) {
+  if (isnan(x)) return 0x7E00;
+  const uint16_t sign = signbit(x) ? 0x8000 : 0;
+  const double ax = fabs(x);
+  if (ax == 0.0) return sign;
+  if (isinf(ax)) return sign | 0x7C00;
+  int e;
+  (void)frexp(ax, &e);          /* ax = m * 2^e, 0.5 <= m < 1: leading bit weighs 2^(e-1) */
+  int qexp = e - 11;            /* 11 significant bits -> quantum 2^(e-11)                */
+  if (qexp < -24) qexp = -24;   /* subnormal binary16 quantum is 2^-24                    */
+  const double r = nearbyint(ldexp(ax, -qexp)); /* round to integer, ties to even          */
+  const double y = ldexp(r, qexp);
+  if (y > 65504.0) return sign | 0x7C00;
+  if (y < ldexp(1.0, -14)) return sign | (uint16_t)ldexp(y, 24); /* subnormal (or zero)   */
+  int ey;
+  const double my = frexp(y, &ey);                   /* y = my * 2^ey, my in [0.5, 1)        */
+  const int field = ey - 1 + 15;                     /* biased exponent of the leading bit   */
+  const int mant = (int)ldexp(my, 11) - 0x400;       /* the 10 bits below the leading one    */
+  return sign | (uint16_t)(field << 10) | (uint16_t)mant;
+}
+
+/*
+ * oracle_decode_step with the recurrent state held as binary16 in memory: every element is
+ * widened to double, the step runs exactly as oracle_decode_step (the output from the new state
+ * as computed, before any rounding), and the new state is rounded once to binary16 when it is
+ * stored.  Qwen3.8 kernel architecture and TDD ledger, the FP16 h-state twins of the decode and
+ * WY kernels (same expressions as the FP32 kernels; the state is half precision in memory only,
+ * rounded once per token boundary).
+ * state_h: [B, hv, dv, dk] binary16 bit patterns, in/out.  Other arguments as oracle_decode_step.
+ */
+int oracle_decode_step_h16(int hk, int hv, int dk, int dv, int W, int B, const uint16_t* x,
+                           const uint16_t* conv_w, uint16_t* conv_state, const float* g,
+                           const float* beta, uint16_t* state_h, const uint16_t* z,
+                           const uint16_t* norm_w, double q_scale, double l2_eps, double rms_eps,
+                           double* out, double* o_raw, int nthreads, int mutation) {
+  const size_t n = (size_t)B * hv * dv * dk;
+  double* st = (double*)malloc(sizeof(double) * (n ? n : 1));
+  if (!st) return -1;
+  for (size_t i = 0; i < n; ++i) st[i] = oracle_f16_to_double(state_h[i]);
+  const int rc = oracle_decode_step(hk, hv, dk, dv, W, B, x, conv_w, conv_state, g, beta, st, z,
+                                    norm_w, q_scale, l2_eps, rms_eps, out, o_raw, nthreads,
+                                    mutation);
+  if (rc == 0)
+    for (size_t i = 0; i < n; ++i) state_h[i] = oracle_round_f16(st[i]);
+  free(st);
   return rc;
 }

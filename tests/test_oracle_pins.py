@@ -388,3 +388,104 @@ def test_each_planted_mutation_changes_the_output(mut):
     mutd = oracle.prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"], inp["g"], inp["beta"], inp["z"],
                           inp["norm_w"], mutation=mut, **a)
     assert (base["out"] - mutd["out"]).abs().max() > 1e-3
+
+
+# ------------------------------------------------------------------ decode with an fp16 state
+
+def _f16_bits_numpy(xs):
+    """numpy's double -> binary16 conversion (round to nearest, ties to even), as bit patterns."""
+    with np.errstate(over="ignore"):
+        return np.asarray(xs, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def test_f16_widening_matches_numpy_for_every_pattern():
+    bits = np.arange(65536, dtype=np.uint16)
+    got = oracle.f16_to_double(torch.from_numpy(bits.view(np.int16)).view(torch.float16)).numpy()
+    want = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))  # -0 stays -0
+
+
+def test_round_f16_matches_numpy_and_ties_to_even():
+    rng = np.random.default_rng(1)
+    xs = list(rng.standard_normal(2000) * np.exp2(rng.uniform(-30, 17, 2000)))
+    # exact midpoints between neighbours (normal, subnormal, across a binade) go to the even pattern
+    for b in (0x3C00, 0x3C01, 0x0001, 0x0002, 0x03FF, 0x0400, 0x7BFE, 0xBC00, 0x8001):
+        lo = float(np.uint16(b).view(np.float16))
+        hi = float(np.uint16(b + 1).view(np.float16))
+        xs.append((lo + hi) / 2)
+        xs.append(np.nextafter((lo + hi) / 2, np.inf))
+        xs.append(np.nextafter((lo + hi) / 2, -np.inf))
+    # overflow boundary: 65504 is the largest finite value; from the midpoint 65520 up -> inf
+    xs += [65504.0, 65519.99, 65520.0, 65536.0, -65520.0, 1e6, 2.0 ** -25, 2.0 ** -26, -0.0, 0.0]
+    got = oracle.round_f16(torch.tensor(xs, dtype=torch.float64)).view(torch.int16).numpy().view(np.uint16)
+    want = _f16_bits_numpy(xs)
+    bad = [(x, hex(a), hex(b)) for x, a, b in zip(xs, got, want) if a != b]
+    assert not bad, bad[:5]
+    # the midpoint between 1 and its successor goes down to the even 1.0, the next one up to 0x3C02
+    assert int(got[2000]) == 0x3C00 and int(got[2003]) == 0x3C02
+
+
+def _h16_decode_args(d, s=0):
+    return (d["x"][s], d["conv_w"], d["conv_state0"], d["g"][s], d["beta"][s])
+
+
+def test_decode_h16_beta_zero_is_rounded_decay():
+    """beta = 0: the new fp16 state is exp(g) * S rounded once to binary16 (numpy's rounding of the
+    double product), and g = 0 as well leaves every state pattern unchanged."""
+    geo = SMALL
+    a = dict(num_k_heads=geo.num_k_heads, num_v_heads=geo.num_v_heads, head_k_dim=geo.head_k_dim,
+             head_v_dim=geo.head_v_dim, q_scale=0.3)
+    d = decode_inputs(3, 1, seed=31, geo=geo)
+    h = d["state0"].to(torch.float16)
+    beta0 = torch.zeros_like(d["beta"][0])
+    x, cw, cs, g, _ = _h16_decode_args(d)
+    _, _, _, st = oracle.decode_step_h16(x, cw, cs, g, beta0, h, d["z"][0], d["norm_w"], **a)
+    alpha = np.exp(g.double().numpy())[:, :, None, None]
+    want = _f16_bits_numpy(alpha * h.numpy().astype(np.float64))
+    assert np.array_equal(st.view(torch.int16).numpy().view(np.uint16), want)
+    h_nz = torch.where(h == 0, torch.full_like(h, 0.5), h)  # no zeros: -0 + 0 would give +0
+    _, _, _, st0 = oracle.decode_step_h16(x, cw, cs, torch.zeros_like(g), beta0, h_nz, d["z"][0], d["norm_w"], **a)
+    assert torch.equal(st0.view(torch.int16), h_nz.view(torch.int16))
+
+
+def test_decode_h16_output_uses_the_state_before_rounding():
+    """The output of an fp16-state step equals the fp64 step's output from the widened state (the
+    rounding applies to the stored state only), and the stored state is within half a binary16
+    quantum of the fp64 step's state."""
+    geo = SMALL
+    a = dict(num_k_heads=geo.num_k_heads, num_v_heads=geo.num_v_heads, head_k_dim=geo.head_k_dim,
+             head_v_dim=geo.head_v_dim, q_scale=0.3)
+    d = decode_inputs(4, 1, seed=32, geo=geo)
+    h = d["state0"].to(torch.float16)
+    args = _h16_decode_args(d)
+    out16, o16, cs16, st16 = oracle.decode_step_h16(*args, h, d["z"][0], d["norm_w"], **a)
+    out64, o64, cs64, st64 = oracle.decode_step(*args, h.double(), d["z"][0], d["norm_w"], **a)
+    assert torch.equal(out16, out64) and torch.equal(o16, o64)
+    assert torch.equal(cs16.view(torch.int16), cs64.view(torch.int16))
+    exact = st64.numpy()
+    got = st16.numpy().astype(np.float64)
+    _, ex = np.frexp(np.abs(exact))
+    quantum = np.exp2(np.maximum(ex - 11, -24))
+    assert np.all(np.abs(got - exact) <= quantum / 2)
+    assert np.any(got != exact)  # the rounding is live
+
+
+def test_decode_h16_drift_stays_at_rounding_level():
+    """Eight fp16-state steps stay within a few binary16 half-quanta of the fp64-state chain."""
+    geo = SMALL
+    a = dict(num_k_heads=geo.num_k_heads, num_v_heads=geo.num_v_heads, head_k_dim=geo.head_k_dim,
+             head_v_dim=geo.head_v_dim, q_scale=0.3)
+    d = decode_inputs(2, 8, seed=33, geo=geo)
+    h, s64 = d["state0"].to(torch.float16), d["state0"].to(torch.float16).double()
+    cs16 = cs64 = d["conv_state0"]
+    for s in range(8):
+        o16, _, cs16, h = oracle.decode_step_h16(d["x"][s], d["conv_w"], cs16, d["g"][s], d["beta"][s], h,
+                                                 d["z"][s], d["norm_w"], **a)
+        o64, _, cs64, s64 = oracle.decode_step(d["x"][s], d["conv_w"], cs64, d["g"][s], d["beta"][s], s64,
+                                               d["z"][s], d["norm_w"], **a)
+        rel = ((h.double() - s64).norm() / s64.norm()).item()
+        assert rel < 2.0 ** -10, (s, rel)
+        assert (o16 - o64).abs().max().item() <= 2e-2 * o64.abs().max().item()

@@ -5,7 +5,7 @@ One step = one pass of the prefill sublayer over the 4 x 4096-token batch (conv1
 then the chunk-wise gated delta rule kernel with the sigmoid-gated RMSNorm fused; conv and
 recurrent states written), inputs resident in HBM.  The headline value is prefill tokens/s.
 The same line carries the fused decode step (256 sequences, one token each, 64 pre-generated
-steps cycled) in seq-steps/s, the roofline of the dominant kernels, an end-to-end number
+steps cycled) in seq-steps/s, with the recurrent state fp32 and again stored as binary16, the roofline of the dominant kernels, an end-to-end number
 through host buffers, the fp64 CPU oracle timed on this host's cores, and the SM clocks seen
 during the timed region.
 
@@ -429,31 +429,40 @@ def run_ours(args, rank, world, local):
     B = DECODE_BATCH
     dx, dg, db, dz = d["x"].to(dev), d["g"].to(dev), d["beta"].to(dev), d["z"].to(dev)
     dw, dnw = d["conv_w"].to(dev), d["norm_w"].to(dev)
-    dstate, dcs = d["state0"].to(dev), d["conv_state0"].to(dev)
     dout = torch.empty((B, 48, 128), dtype=torch.bfloat16, device=dev)
 
-    def decode_step(s):
-        gdn.gdn_decode_step(dx[s], dw, dcs, dg[s], db[s], dstate, dz[s], dnw, d["q_scale"], out=dout)
+    def time_decode(state_dtype, state_bytes_per_seq, kernel):
+        dstate, dcs = d["state0"].to(dev).to(state_dtype), d["conv_state0"].to(dev)
 
-    for s in range(max(args.warmup, 1)):
-        decode_step(s % DECODE_STEPS)
-    barrier()
-    s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s3.record(stream)
-    for s in range(args.decode_steps):
-        decode_step(s % DECODE_STEPS)
-    e3.record(stream)
-    torch.cuda.synchronize()
-    gdn.gdn_check_device_errors()
-    dec_ms = max_over_ranks(s3.elapsed_time(e3)) / args.decode_steps
-    dec_bytes = DECODE_BYTES_PER_SEQ * B
-    dec_gbs = dec_bytes / (dec_ms / 1000) / 1e9
-    decode = {"metric": "decode seq-steps/s", "value": world * B / (dec_ms / 1000), "unit": "seq-steps/s",
-              "ms_per_step": dec_ms, "steps": args.decode_steps, "batch": B,
-              "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak,
-                           "unit": "GB/s", "frac": dec_gbs / hbm_peak,
-                           "traffic": (traffic_record("decode_step") or {}).get("bytes_per_launch"),
-                           "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_ms}}
+        def decode_step(s):
+            gdn.gdn_decode_step(dx[s], dw, dcs, dg[s], db[s], dstate, dz[s], dnw, d["q_scale"], out=dout)
+
+        for s in range(max(args.warmup, 1)):
+            decode_step(s % DECODE_STEPS)
+        barrier()
+        s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s3.record(stream)
+        for s in range(args.decode_steps):
+            decode_step(s % DECODE_STEPS)
+        e3.record(stream)
+        torch.cuda.synchronize()
+        gdn.gdn_check_device_errors()
+        dec_ms = max_over_ranks(s3.elapsed_time(e3)) / args.decode_steps
+        dec_bytes = (DECODE_BYTES_PER_SEQ - STATE_BYTES_PER_SEQ + state_bytes_per_seq) * B
+        dec_gbs = dec_bytes / (dec_ms / 1000) / 1e9
+        del dstate, dcs
+        return {"metric": "decode seq-steps/s", "value": world * B / (dec_ms / 1000), "unit": "seq-steps/s",
+                "ms_per_step": dec_ms, "steps": args.decode_steps, "batch": B,
+                "roofline": {"kernel": kernel, "bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak,
+                             "unit": "GB/s", "frac": dec_gbs / hbm_peak,
+                             "traffic": (traffic_record(kernel) or {}).get("bytes_per_launch"),
+                             "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_ms},
+                "roofline_seq_steps_per_s": hbm_peak * 1e9 / (dec_bytes / B)}
+
+    decode = time_decode(torch.float32, STATE_BYTES_PER_SEQ, "decode_step")
+    # the same workload with the recurrent state stored as binary16 (half the state bytes)
+    decode_f16 = time_decode(torch.float16, STATE_BYTES_PER_SEQ // 2, "decode_step_fp16_state")
+    decode_f16["state"] = "binary16 in memory, fp32 arithmetic, rounded once per step"
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
@@ -473,7 +482,7 @@ def run_ours(args, rank, world, local):
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                     "pipelined": "H2D of step i+1 and D2H of step i-1 overlap the prefill of step i"},
-            "decode": decode, "varlen": varlen, "cpu_baseline": cpu, "clocks": clk,
+            "decode": decode, "decode_fp16_state": decode_f16, "varlen": varlen, "cpu_baseline": cpu, "clocks": clk,
             # per step: conv1d + conv-state kernels, the chunk prefill's schedule and segment-table
             # kernels, then a prep and a state kernel for each of its three chunk segments
             "gpu_launches": (2 + 2 + 2 * 3) * args.steps,

@@ -48,6 +48,7 @@ extern "C" {
 #endif
 
 typedef uint16_t gdn_bf16; /* IEEE bfloat16 bit pattern */
+typedef uint16_t gdn_f16;  /* IEEE binary16 (half precision) bit pattern */
 
 typedef enum {
   GDN_OK = 0,
@@ -192,6 +193,27 @@ GDN_API gdn_status gdn_decode_step(const gdn_geometry* geo, const gdn_bf16* x,
                                    const float* beta, float* state, const gdn_bf16* z,
                                    const gdn_bf16* norm_w, float q_scale, float l2_eps,
                                    float rms_eps, gdn_bf16* out, int32_t batch, void* stream);
+
+/*
+ * gdn_decode_step with the recurrent state stored as IEEE binary16 ("FP16 h-state"): Qwen3.8
+ * kernel architecture and TDD ledger, the FP16 h-state twins of the decode kernels (the same
+ * arithmetic as the fp32 kernel; the state is half precision in memory only and is rounded once
+ * per token boundary).  Each state element is widened to fp32 on load, the step runs exactly as in
+ * gdn_decode_step (the output comes from the new state before rounding), and the new state is
+ * rounded to binary16 (to nearest, ties to even) when it is stored.  This halves the state bytes
+ * the step reads and writes.
+ *
+ *   state       [batch, Hv, Dv, Dk] binary16, in/out (16-byte aligned)
+ *   all other arguments, results and errors as gdn_decode_step.
+ *
+ * A state element whose magnitude rounds above 65504 becomes an infinity; nothing clamps it.
+ */
+GDN_API gdn_status gdn_decode_step_fp16_state(const gdn_geometry* geo, const gdn_bf16* x,
+                                              const gdn_bf16* conv_w, gdn_bf16* conv_state,
+                                              const float* g, const float* beta, gdn_f16* state,
+                                              const gdn_bf16* z, const gdn_bf16* norm_w,
+                                              float q_scale, float l2_eps, float rms_eps,
+                                              gdn_bf16* out, int32_t batch, void* stream);
 
 /* Capacity of the fixed scratch used by gdn_chunk_prefill_noalloc. */
 #define GDN_NOALLOC_MAX_SEQS 16384

@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     gdn_debug_mma_probe_ex,
     gdn_debug_set_chunk_mode,
     gdn_decode_step,
+    gdn_decode_step_fp16_state,
     gdn_gated_rmsnorm,
     gdn_prefill,
     gdn_version,

@@ -59,6 +59,7 @@ def load_library():
             "gdn_chunk_prefill_noalloc": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
             "gdn_gated_rmsnorm": ([G, P, P, P, F, P, I, P], ctypes.c_int),
             "gdn_decode_step": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
+            "gdn_decode_step_fp16_state": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
             "gdn_check_device_errors": ([P], ctypes.c_int),
             "gdn_debug_set_chunk_mode": ([ctypes.c_int], ctypes.c_int),
             "gdn_debug_get_chunk_mode": ([], ctypes.c_int),
@@ -196,8 +197,13 @@ def gdn_gated_rmsnorm(o, z, norm_w, eps=1e-6, out=None, geometry: Geometry = QWE
 
 def gdn_decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps=1e-6,
                     rms_eps=1e-6, out=None, geometry: Geometry = QWEN_GDN, stream=None):
-    """One fused decode step; conv_state and state are updated in place.  Returns out."""
+    """One fused decode step; conv_state and state are updated in place.  Returns out.
+
+    ``state`` is fp32 (gdn_decode_step) or fp16 (gdn_decode_step_fp16_state: the state is half
+    precision in memory, widened on load and rounded once on store).
+    """
     lib = load_library()
+    fp16_state = state.dtype == torch.float16
     C, W = geometry.conv_dim, geometry.conv_width
     hv, dv, dk = geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
     B = x.shape[0]
@@ -206,16 +212,25 @@ def gdn_decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l
     _dev(conv_state, torch.bfloat16, "conv_state", (B, C, W - 1))
     _dev(g, torch.float32, "g", (B, hv))
     _dev(beta, torch.float32, "beta", (B, hv))
-    _dev(state, torch.float32, "state", (B, hv, dv, dk))
+    _dev(state, torch.float16 if fp16_state else torch.float32, "state", (B, hv, dv, dk))
     _dev(z, torch.bfloat16, "z", (B, hv, dv))
     _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
     if out is None:
         out = torch.empty((B, hv, dv), dtype=torch.bfloat16, device=x.device)
     _dev(out, torch.bfloat16, "out", (B, hv, dv))
-    _check(lib.gdn_decode_step(_geo(geometry), _p(x), _p(conv_w), _p(conv_state), _p(g), _p(beta),
-                               _p(state), _p(z), _p(norm_w), float(q_scale), float(l2_eps),
-                               float(rms_eps), _p(out), B, _stream(stream)))
+    fn = lib.gdn_decode_step_fp16_state if fp16_state else lib.gdn_decode_step
+    _check(fn(_geo(geometry), _p(x), _p(conv_w), _p(conv_state), _p(g), _p(beta), _p(state), _p(z),
+              _p(norm_w), float(q_scale), float(l2_eps), float(rms_eps), _p(out), B, _stream(stream)))
     return out
+
+
+def gdn_decode_step_fp16_state(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps=1e-6,
+                               rms_eps=1e-6, out=None, geometry: Geometry = QWEN_GDN, stream=None):
+    """gdn_decode_step on an fp16 (binary16) recurrent state [B, Hv, Dv, Dk], updated in place."""
+    if state.dtype != torch.float16:
+        raise TypeError(f"state must be torch.float16, got {state.dtype}")
+    return gdn_decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps, rms_eps, out,
+                           geometry, stream)
 
 
 def gdn_check_device_errors(stream=None):

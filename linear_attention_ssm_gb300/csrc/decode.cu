@@ -1,10 +1,12 @@
 // decode.cu -- one fused GDN decode step: conv step + SiLU, L2 norm of q/k, gated delta rule
-// update of the fp32 state in place, sigmoid-gated RMSNorm.
+// update of the recurrent state in place (fp32, or fp16 in memory), sigmoid-gated RMSNorm.
 //
 // Qwen3.8 kernel architecture and TDD ledger, "Current dense-27B kernel map" (scalar GDN
 // recurrence and fused output gate); spark_model layer_struct.rs, fields of the strided decode
 // kernels (one launch for all sequences; the state read once and written once, 1R+1W);
-// GLM-5.3-Flash kernel TDD ledger, slice I3 (a conv step equals the full width-4 causal conv).
+// GLM-5.3-Flash kernel TDD ledger, slice I3 (a conv step equals the full width-4 causal conv);
+// Qwen3.8 ledger, the FP16 h-state twins of the decode kernels (same arithmetic as the fp32
+// kernel, the state half precision in memory, rounded once per token).
 //
 // One CTA per (sequence, K head): it owns the q/k channels of that K head and the v channels of
 // the Hv/Hk V heads that read it, so no two CTAs touch the same conv-state channel and the
@@ -12,6 +14,9 @@
 // head's 128 x 128 state: a row is 32 lanes x float4 over the key dimension, so both
 // contractions (S k and S q) are warp-shuffle reductions and every state byte is read once and
 // written once.
+#include <cuda_fp16.h>
+#include <string.h>
+
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 
@@ -32,9 +37,32 @@ __device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
   }
 }
 
+// Four consecutive state elements of a row (index i counts groups of four), widened to fp32.  The
+// fp16 storage form holds the state as IEEE binary16 in memory only: it is widened on load, the
+// step runs in fp32 exactly as for the fp32 state, and the new state is rounded once (to nearest,
+// ties to even) when it is stored.
+__device__ __forceinline__ float4 load_state4(const float* S, int i) { return reinterpret_cast<const float4*>(S)[i]; }
+__device__ __forceinline__ float4 load_state4(const __half* S, int i) {
+  const uint2 u = reinterpret_cast<const uint2*>(S)[i];
+  __half2 h01, h23;
+  memcpy(&h01, &u.x, 4);
+  memcpy(&h23, &u.y, 4);
+  const float2 a = __half22float2(h01), b = __half22float2(h23);
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void store_state4(float* S, int i, const float4 v) { reinterpret_cast<float4*>(S)[i] = v; }
+__device__ __forceinline__ void store_state4(__half* S, int i, const float4 v) {
+  const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+  uint2 u;
+  memcpy(&u.x, &a, 4);
+  memcpy(&u.y, &b, 4);
+  reinterpret_cast<uint2*>(S)[i] = u;
+}
+
+template <typename StateT>
 __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ conv_w, uint16_t* conv_state,
-    const float* __restrict__ g, const float* __restrict__ beta, float* state,
+    const float* __restrict__ g, const float* __restrict__ beta, StateT* state,
     const uint16_t* __restrict__ z, const uint16_t* __restrict__ norm_w, float q_scale, float l2_eps,
     float rms_eps, uint16_t* __restrict__ out, int Hk, int Hv) {
   const int j = blockIdx.x;        // K head
@@ -121,10 +149,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     const int h = j * R + hh;
     const float alpha = expf(__ldg(g + (size_t)b * Hv + h));
     const float bt = __ldg(beta + (size_t)b * Hv + h);
-    float4* S = reinterpret_cast<float4*>(state + (((size_t)b * Hv + h) * kHeadDim + warp * kRowsPerWarp) * kHeadDim);
+    StateT* S = state + (((size_t)b * Hv + h) * kHeadDim + warp * kRowsPerWarp) * kHeadDim;
     float4 row[kRowsPerWarp];
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) row[i] = S[i * 32 + lane];
+    for (int i = 0; i < kRowsPerWarp; ++i) row[i] = load_state4(S, i * 32 + lane);
     float d[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i)
@@ -143,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
       sn.y = fmaf(alpha, row[i].y, e * kn.y);
       sn.z = fmaf(alpha, row[i].z, e * kn.z);
       sn.w = fmaf(alpha, row[i].w, e * kn.w);
-      S[i * 32 + lane] = sn;
+      store_state4(S, i * 32 + lane, sn);
       o[i] = sn.x * qn.x + sn.y * qn.y + sn.z * qn.z + sn.w * qn.w;
     }
 #pragma unroll
@@ -185,13 +213,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
 int decode_max_ratio() { return kMaxRatio; }
 
 cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
-                               uint16_t* conv_state, const float* g, const float* beta, float* state,
-                               const uint16_t* z, const uint16_t* norm_w, float q_scale, float l2_eps,
-                               float rms_eps, uint16_t* out, int B, int Hk, int Hv) {
+                               uint16_t* conv_state, const float* g, const float* beta, void* state,
+                               bool fp16_state, const uint16_t* z, const uint16_t* norm_w, float q_scale,
+                               float l2_eps, float rms_eps, uint16_t* out, int B, int Hk, int Hv) {
   if (B <= 0) return cudaSuccess;
   dim3 grid(Hk, B);
-  decode_step_kernel<<<grid, kThreads, 0, env.stream>>>(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale,
-                                                        l2_eps, rms_eps, out, Hk, Hv);
+  if (fp16_state)
+    decode_step_kernel<__half><<<grid, kThreads, 0, env.stream>>>(x, conv_w, conv_state, g, beta,
+                                                                  static_cast<__half*>(state), z, norm_w, q_scale,
+                                                                  l2_eps, rms_eps, out, Hk, Hv);
+  else
+    decode_step_kernel<float><<<grid, kThreads, 0, env.stream>>>(x, conv_w, conv_state, g, beta,
+                                                                 static_cast<float*>(state), z, norm_w, q_scale,
+                                                                 l2_eps, rms_eps, out, Hk, Hv);
   return cudaGetLastError();
 }
 

@@ -227,10 +227,13 @@ gdn_status gdn_gated_rmsnorm(const gdn_geometry* geo, const gdn_bf16* o, const g
                   "gated rmsnorm launch");
 }
 
-gdn_status gdn_decode_step(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w, gdn_bf16* conv_state,
-                           const float* g, const float* beta, float* state, const gdn_bf16* z,
-                           const gdn_bf16* norm_w, float q_scale, float l2_eps, float rms_eps, gdn_bf16* out,
-                           int32_t batch, void* stream) {
+}  // extern "C"
+
+namespace {
+gdn_status decode_step(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w, gdn_bf16* conv_state,
+                       const float* g, const float* beta, void* state, bool fp16_state, const gdn_bf16* z,
+                       const gdn_bf16* norm_w, float q_scale, float l2_eps, float rms_eps, gdn_bf16* out,
+                       int32_t batch, void* stream) {
   gdn_status s = check_geometry(geo);
   if (s != GDN_OK) return s;
   if (geo->num_v_heads / geo->num_k_heads > gdn::decode_max_ratio())
@@ -251,9 +254,29 @@ gdn_status gdn_decode_step(const gdn_geometry* geo, const gdn_bf16* x, const gdn
   if (!(l2_eps >= 0.f) || !(rms_eps >= 0.f)) return fail(GDN_ERR_INVALID_ARGUMENT, "eps must be >= 0");
   gdn::LaunchEnv env;
   if ((s = make_env(stream, &env)) != GDN_OK) return s;
-  return launched(gdn::launch_decode_step(env, x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps,
-                                          rms_eps, out, batch, geo->num_k_heads, geo->num_v_heads),
+  return launched(gdn::launch_decode_step(env, x, conv_w, conv_state, g, beta, state, fp16_state, z, norm_w,
+                                          q_scale, l2_eps, rms_eps, out, batch, geo->num_k_heads,
+                                          geo->num_v_heads),
                   "decode launch");
+}
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_decode_step(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w, gdn_bf16* conv_state,
+                           const float* g, const float* beta, float* state, const gdn_bf16* z,
+                           const gdn_bf16* norm_w, float q_scale, float l2_eps, float rms_eps, gdn_bf16* out,
+                           int32_t batch, void* stream) {
+  return decode_step(geo, x, conv_w, conv_state, g, beta, state, false, z, norm_w, q_scale, l2_eps, rms_eps, out,
+                     batch, stream);
+}
+
+gdn_status gdn_decode_step_fp16_state(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w,
+                                      gdn_bf16* conv_state, const float* g, const float* beta, gdn_f16* state,
+                                      const gdn_bf16* z, const gdn_bf16* norm_w, float q_scale, float l2_eps,
+                                      float rms_eps, gdn_bf16* out, int32_t batch, void* stream) {
+  return decode_step(geo, x, conv_w, conv_state, g, beta, state, true, z, norm_w, q_scale, l2_eps, rms_eps, out,
+                     batch, stream);
 }
 
 // ---- allocation-free chunk prefill: the schedule lives in a fixed device array of this file

@@ -18,9 +18,9 @@ cudaError_t launch_gated_rmsnorm(const LaunchEnv& env, const uint16_t* o, const 
 
 int decode_max_ratio();
 cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
-                               uint16_t* conv_state, const float* g, const float* beta, float* state,
-                               const uint16_t* z, const uint16_t* norm_w, float q_scale, float l2_eps,
-                               float rms_eps, uint16_t* out, int B, int Hk, int Hv);
+                               uint16_t* conv_state, const float* g, const float* beta, void* state,
+                               bool fp16_state, const uint16_t* z, const uint16_t* norm_w, float q_scale,
+                               float l2_eps, float rms_eps, uint16_t* out, int B, int Hk, int Hv);
 
 // Workspace of the fused chunk prefill: a work counter and the longest-first sequence order.
 size_t chunk_prefill_workspace_bytes(int N);

@@ -11,6 +11,12 @@ import torch
 OUT_TOL = 2e-2
 STATE_TOL = 1e-4
 NEG_CONTROL_RATIO = 10.0  # a planted fault must exceed the output bound by this factor
+# A binary16-stored state chain against the oracle's binary16 chain.  The two round the same
+# exact values, but the GPU computes them in fp32: wherever that puts a value on the other side
+# of a rounding midpoint the stored states differ by one quantum, and the next steps turn such
+# differences into further whole-quantum differences, so after a few steps the chains differ by
+# a fraction of a quantum RMS.  One quantum is 2^-11..2^-10 of the value: bound 2^-10 rel. L2.
+STATE_TOL_F16 = 2.0 ** -10
 
 DEV = "cuda"
 
@@ -53,10 +59,10 @@ def state_rel_l2(got, want):
     return ((got - want).norm() / want.norm().clamp_min(1e-300)).item()
 
 
-def assert_state_close(got, want, what="state"):
+def assert_state_close(got, want, what="state", tol=STATE_TOL):
     assert torch.isfinite(got.detach().float()).all(), f"{what}: non-finite values"
     r = state_rel_l2(got, want)
-    assert r <= STATE_TOL, f"{what}: relative L2 error {r:.3g} > {STATE_TOL}"
+    assert r <= tol, f"{what}: relative L2 error {r:.3g} > {tol}"
     return r
 
 

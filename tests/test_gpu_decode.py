@@ -5,8 +5,8 @@ import torch
 
 import oracle
 from linear_attention_ssm_gb300.synth import QWEN_GDN, decode_inputs, cu_seqlens_of
-from tests.gpu_common import (DEV, Guarded, NEG_CONTROL_RATIO, assert_out_close, assert_state_close, lib,
-                              out_error_ratio)
+from tests.gpu_common import (DEV, Guarded, NEG_CONTROL_RATIO, STATE_TOL_F16, assert_out_close, assert_state_close,
+                              lib, out_error_ratio)
 
 pytestmark = pytest.mark.gpu
 GEO = QWEN_GDN
@@ -72,3 +72,83 @@ def test_decode_negative_controls(mutation):
     bad = oracle.decode_step(*args, q_scale=d["q_scale"], mutation=mutation, **A)[0]
     assert out_error_ratio(out, ref) <= 1.0
     assert out_error_ratio(out, bad) > NEG_CONTROL_RATIO
+
+
+# ------------------------------------------------------------------ fp16 (binary16) recurrent state
+
+def _f16_quantum(v):
+    """Spacing of binary16 values at |v| (2^-24 in the subnormal range)."""
+    _, ex = torch.frexp(v.abs().double())
+    return torch.exp2(torch.clamp(ex - 11, min=-24).double())
+
+
+def test_fp16_state_one_step_is_within_one_rounding_of_the_oracle():
+    """From the same binary16 state, one step stores every element either as the oracle's rounding
+    of the exact value or as its neighbour (the fp32 arithmetic put the value on the other side of
+    a rounding midpoint); such neighbours are rare."""
+    g = lib()
+    B = 6
+    d = decode_inputs(B, 1, seed=24)
+    h0 = d["state0"].to(torch.float16)
+    st = h0.to(DEV).clone()
+    cs = d["conv_state0"].to(DEV).clone()
+    out = Guarded((B, 48, 128), torch.bfloat16)
+    g.gdn_decode_step_fp16_state(d["x"][0].to(DEV), d["conv_w"].to(DEV), cs, d["g"][0].to(DEV),
+                                 d["beta"][0].to(DEV), st, d["z"][0].to(DEV), d["norm_w"].to(DEV), d["q_scale"],
+                                 1e-6, 1e-6, out.t)
+    g.gdn_check_device_errors()
+    out.check("out")
+    ref, _, cs_ref, st_ref = oracle.decode_step_h16(d["x"][0], d["conv_w"], d["conv_state0"], d["g"][0],
+                                                    d["beta"][0], h0, d["z"][0], d["norm_w"], q_scale=d["q_scale"],
+                                                    **A)
+    assert_out_close(out.t, ref)
+    got, want = st.cpu().double(), st_ref.double()
+    assert torch.isfinite(got).all()
+    diff = (got - want).abs()
+    assert (diff <= _f16_quantum(want) * (1 + 1e-12)).all(), "an element is more than one rounding away"
+    assert (diff > 0).double().mean().item() < 1e-2
+    assert torch.equal(cs.cpu().view(torch.int16), cs_ref.view(torch.int16))
+
+
+def test_fp16_state_decode_steps_match_oracle():
+    """Consecutive fp16-state steps: GPU chain against the oracle's binary16 chain."""
+    g = lib()
+    B, steps = 5, 6
+    d = decode_inputs(B, steps, seed=25)
+    st = d["state0"].to(torch.float16).to(DEV)
+    cs = d["conv_state0"].to(DEV).clone()
+    cs_ref, st_ref = d["conv_state0"], d["state0"].to(torch.float16)
+    for s in range(steps):
+        out = g.gdn_decode_step_fp16_state(d["x"][s].to(DEV), d["conv_w"].to(DEV), cs, d["g"][s].to(DEV),
+                                           d["beta"][s].to(DEV), st, d["z"][s].to(DEV), d["norm_w"].to(DEV),
+                                           d["q_scale"])
+        g.gdn_check_device_errors()
+        ref, _, cs_ref, st_ref = oracle.decode_step_h16(d["x"][s], d["conv_w"], cs_ref, d["g"][s], d["beta"][s],
+                                                        st_ref, d["z"][s], d["norm_w"], q_scale=d["q_scale"], **A)
+        assert_out_close(out, ref, f"out of step {s}")
+        assert_state_close(st.double(), st_ref.double(), f"state after step {s}", tol=STATE_TOL_F16)
+        assert torch.equal(cs.cpu().view(torch.int16), cs_ref.view(torch.int16))
+
+
+def test_fp16_state_zero_gate_and_beta_keep_the_state_bits():
+    """g = 0 and beta = 0: the step leaves every (nonzero) binary16 state pattern unchanged."""
+    g = lib()
+    B = 2
+    d = decode_inputs(B, 1, seed=26)
+    h0 = d["state0"].to(torch.float16)
+    h0 = torch.where(h0 == 0, torch.full_like(h0, 0.25), h0)
+    st = h0.to(DEV).clone()
+    g.gdn_decode_step_fp16_state(d["x"][0].to(DEV), d["conv_w"].to(DEV), d["conv_state0"].to(DEV).clone(),
+                                 torch.zeros_like(d["g"][0]).to(DEV), torch.zeros_like(d["beta"][0]).to(DEV), st,
+                                 d["z"][0].to(DEV), d["norm_w"].to(DEV), d["q_scale"])
+    g.gdn_check_device_errors()
+    assert torch.equal(st.cpu().view(torch.int16), h0.view(torch.int16))
+
+
+def test_fp16_state_rejects_an_fp32_state():
+    g = lib()
+    d = decode_inputs(1, 1, seed=27)
+    with pytest.raises(TypeError):
+        g.gdn_decode_step_fp16_state(d["x"][0].to(DEV), d["conv_w"].to(DEV), d["conv_state0"].to(DEV),
+                                     d["g"][0].to(DEV), d["beta"][0].to(DEV), d["state0"].to(DEV), d["z"][0].to(DEV),
+                                     d["norm_w"].to(DEV), d["q_scale"])

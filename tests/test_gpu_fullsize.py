@@ -9,7 +9,7 @@ import torch
 import oracle
 from linear_attention_ssm_gb300.synth import (BATCHED_LENGTHS, VARLEN_LENGTHS, DECODE_BATCH, DECODE_STEPS,
                                               decode_inputs, prefill_inputs)
-from tests.gpu_common import DEV, assert_out_close, assert_state_close, lib
+from tests.gpu_common import DEV, STATE_TOL_F16, assert_out_close, assert_state_close, lib
 
 pytestmark = pytest.mark.gpu
 SAMPLE_HEADS = [0, 1, 2, 25, 47]   # a whole K-head group plus heads of two other groups
@@ -67,4 +67,31 @@ def test_decode_256_sequences_64_steps():
                                                     q_scale=d["q_scale"], **A)
         assert_out_close(outs[s][sample], ref, f"out of step {s}")
     assert_state_close(st[sample], st_ref, "state after 64 steps")
+    assert torch.equal(cs.cpu()[sample].view(torch.int16), cs_ref.view(torch.int16))
+
+
+def test_decode_256_sequences_64_steps_fp16_state():
+    """The decode workload with the state stored as binary16, sampled sequences against the
+    oracle's binary16 chain."""
+    g = lib()
+    d = decode_inputs(DECODE_BATCH, DECODE_STEPS, seed=4)
+    sample = [0, 131, 255]
+    cs = d["conv_state0"].to(DEV).clone()
+    st = d["state0"].to(torch.float16).to(DEV)
+    x, gg, bb, z = d["x"].to(DEV), d["g"].to(DEV), d["beta"].to(DEV), d["z"].to(DEV)
+    w, nw = d["conv_w"].to(DEV), d["norm_w"].to(DEV)
+    outs = torch.empty((DECODE_STEPS, DECODE_BATCH, 48, 128), dtype=torch.bfloat16, device=DEV)
+    for s in range(DECODE_STEPS):
+        g.gdn_decode_step_fp16_state(x[s], w, cs, gg[s], bb[s], st, z[s], nw, d["q_scale"], out=outs[s])
+    g.gdn_check_device_errors()
+    outs, st = outs.cpu(), st.cpu()
+    assert torch.isfinite(outs.float()).all() and torch.isfinite(st.float()).all()
+    cs_ref = d["conv_state0"][sample]
+    st_ref = d["state0"][sample].to(torch.float16)
+    for s in range(DECODE_STEPS):
+        ref, _, cs_ref, st_ref = oracle.decode_step_h16(d["x"][s][sample], d["conv_w"], cs_ref, d["g"][s][sample],
+                                                        d["beta"][s][sample], st_ref, d["z"][s][sample],
+                                                        d["norm_w"], q_scale=d["q_scale"], **A)
+        assert_out_close(outs[s][sample], ref, f"out of step {s}")
+    assert_state_close(st[sample].double(), st_ref.double(), "state after 64 steps", tol=STATE_TOL_F16)
     assert torch.equal(cs.cpu()[sample].view(torch.int16), cs_ref.view(torch.int16))

@@ -8,6 +8,9 @@
 // Qwen3.8 ledger, the FP16 h-state twins of the decode kernels (same arithmetic as the fp32
 // kernel, the state half precision in memory, rounded once per token).
 //
+// With a binary16 state the CTA's state slice (96 KB) is staged in shared memory by one bulk copy
+// issued at the start, so it streams in while the conv step and the norms run.
+//
 // One CTA per (sequence, K head): it owns the q/k channels of that K head and the v channels of
 // the Hv/Hk V heads that read it, so no two CTAs touch the same conv-state channel and the
 // in-place conv-state update is race-free.  Each warp streams 16 rows ([value] index) of a
@@ -27,6 +30,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRowsPerWarp = kHeadDim / (kThreads / 32);  // 16
 constexpr int kMaxRatio = 12;                             // V heads per K head handled by one CTA
+constexpr uint32_t kStateWaitLimit = 1u << 20;            // polls of the state-slice barrier
+constexpr size_t kMaxStagedBytes = 96 * 1024;             // largest state slice staged in shared memory
 
 __device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -59,12 +64,16 @@ __device__ __forceinline__ void store_state4(__half* S, int i, const float4 v) {
   reinterpret_cast<uint2*>(S)[i] = u;
 }
 
-template <typename StateT>
+// kStaged: the CTA's whole state slice (its R V heads, contiguous in [B, Hv, Dv, Dk]) is fetched
+// into shared memory by one bulk copy issued before the conv step, so the state bytes are in
+// flight while the conv and the norms are computed; the rows are then read from shared memory.
+// Used when the slice fits (binary16 state, R <= 3: 96 KB).  Otherwise rows stream from global.
+template <typename StateT, bool kStaged>
 __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ conv_w, uint16_t* conv_state,
     const float* __restrict__ g, const float* __restrict__ beta, StateT* state,
     const uint16_t* __restrict__ z, const uint16_t* __restrict__ norm_w, float q_scale, float l2_eps,
-    float rms_eps, uint16_t* __restrict__ out, int Hk, int Hv) {
+    float rms_eps, uint16_t* __restrict__ out, int Hk, int Hv, unsigned* err) {
   const int j = blockIdx.x;        // K head
   const int b = blockIdx.y;        // sequence
   const int R = Hv / Hk;
@@ -75,6 +84,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
   __shared__ float s_v[kMaxRatio][kHeadDim];
   __shared__ float s_o[kMaxRatio][kHeadDim];
   __shared__ float s_norm[2];
+  __shared__ uint64_t s_bar;
+  extern __shared__ __align__(128) uint8_t s_state[];  // kStaged: R x Dv x Dk StateT
+
+  StateT* const slice = state + ((size_t)b * Hv + (size_t)j * R) * kHeadDim * kHeadDim;
+  if constexpr (kStaged) {
+    if (tid == 0) {
+      const uint32_t bar = smem_u32(&s_bar);
+      mbar_init(bar, 1);
+      fence_mbar_init();
+      const uint32_t bytes = (uint32_t)((size_t)R * kHeadDim * kHeadDim * sizeof(StateT));
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_load(smem_u32(s_state), slice, bytes, bar);
+    }
+  }
 
   // ---- conv step + SiLU for the CTA's 32 + 16R channel octets
   const int n_oct = 32 + 16 * R;
@@ -144,15 +167,30 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
   const float4 kn = make_float4(s_k[lane * 4] * s_norm[1], s_k[lane * 4 + 1] * s_norm[1],
                                 s_k[lane * 4 + 2] * s_norm[1], s_k[lane * 4 + 3] * s_norm[1]);
 
+  if constexpr (kStaged) {  // the state slice has landed in shared memory (bounded wait)
+    const bool got = mbar_wait(smem_u32(&s_bar), 0, kStateWaitLimit);
+    if (!got) raise_error(err, kErrTimeout);
+    if (!__syncthreads_and(got ? 1 : 0)) {
+      if (!got) mbar_wait(smem_u32(&s_bar), 0, kStateWaitLimit);  // let the copy land before leaving
+      return;
+    }
+  }
+
   // ---- state update, one V head at a time
   for (int hh = 0; hh < R; ++hh) {
     const int h = j * R + hh;
     const float alpha = expf(__ldg(g + (size_t)b * Hv + h));
     const float bt = __ldg(beta + (size_t)b * Hv + h);
-    StateT* S = state + (((size_t)b * Hv + h) * kHeadDim + warp * kRowsPerWarp) * kHeadDim;
+    StateT* S = slice + ((size_t)hh * kHeadDim + warp * kRowsPerWarp) * kHeadDim;
     float4 row[kRowsPerWarp];
+    if constexpr (kStaged) {
+      const StateT* Ss = reinterpret_cast<const StateT*>(s_state) + (hh * kHeadDim + warp * kRowsPerWarp) * kHeadDim;
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) row[i] = load_state4(S, i * 32 + lane);
+      for (int i = 0; i < kRowsPerWarp; ++i) row[i] = load_state4(Ss, i * 32 + lane);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) row[i] = load_state4(S, i * 32 + lane);
+    }
     float d[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i)
@@ -218,14 +256,32 @@ cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const ui
                                float l2_eps, float rms_eps, uint16_t* out, int B, int Hk, int Hv) {
   if (B <= 0) return cudaSuccess;
   dim3 grid(Hk, B);
-  if (fp16_state)
-    decode_step_kernel<__half><<<grid, kThreads, 0, env.stream>>>(x, conv_w, conv_state, g, beta,
-                                                                  static_cast<__half*>(state), z, norm_w, q_scale,
-                                                                  l2_eps, rms_eps, out, Hk, Hv);
-  else
-    decode_step_kernel<float><<<grid, kThreads, 0, env.stream>>>(x, conv_w, conv_state, g, beta,
-                                                                 static_cast<float*>(state), z, norm_w, q_scale,
-                                                                 l2_eps, rms_eps, out, Hk, Hv);
+  const size_t slice_bytes = (size_t)(Hv / Hk) * kHeadDim * kHeadDim * (fp16_state ? 2 : 4);
+  if (fp16_state && slice_bytes <= kMaxStagedBytes) {
+    static int configured[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !configured[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<__half, true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxStagedBytes);
+      // the largest shared-memory carveout, so that two staged CTAs share an SM
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_step_kernel<__half, true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (e != cudaSuccess) return e;
+      configured[dev] = 1;
+    }
+    decode_step_kernel<__half, true><<<grid, kThreads, slice_bytes, env.stream>>>(
+        x, conv_w, conv_state, g, beta, static_cast<__half*>(state), z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv,
+        env.err);
+  } else if (fp16_state) {
+    decode_step_kernel<__half, false><<<grid, kThreads, 0, env.stream>>>(
+        x, conv_w, conv_state, g, beta, static_cast<__half*>(state), z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv,
+        env.err);
+  } else {
+    decode_step_kernel<float, false><<<grid, kThreads, 0, env.stream>>>(
+        x, conv_w, conv_state, g, beta, static_cast<float*>(state), z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv,
+        env.err);
+  }
   return cudaGetLastError();
 }
 

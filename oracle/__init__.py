@@ -212,9 +212,12 @@ def decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, num_k_heads, n
     st = _f64(state).clone()
     out = torch.empty((B, hv, dv), dtype=torch.float64)
     o_raw = torch.empty((B, hv, dv), dtype=torch.float64)
-    rc = lib.oracle_decode_step(hk, hv, dk, dv, W, B, _ptr(_bf16_bits(x)), _ptr(_bf16_bits(conv_w)),
-                                _ptr(cs), _ptr(_f32(g)), _ptr(_f32(beta)), _ptr(st),
-                                _ptr(_bf16_bits(z)), _ptr(_bf16_bits(norm_w)), float(q_scale),
+    # the converted inputs are held in locals: a temporary copy would be freed before the call
+    xb, wb, gg, bb, zb, nb = (_bf16_bits(x), _bf16_bits(conv_w), _f32(g), _f32(beta), _bf16_bits(z),
+                              _bf16_bits(norm_w))
+    rc = lib.oracle_decode_step(hk, hv, dk, dv, W, B, _ptr(xb), _ptr(wb),
+                                _ptr(cs), _ptr(gg), _ptr(bb), _ptr(st),
+                                _ptr(zb), _ptr(nb), float(q_scale),
                                 float(l2_eps), float(rms_eps), _ptr(out), _ptr(o_raw),
                                 int(nthreads), int(mutation))
     if rc != 0:
@@ -240,14 +243,48 @@ def decode_step_h16(x, conv_w, conv_state, g, beta, state, z, norm_w, num_k_head
     st = state.detach().cpu().contiguous().view(torch.int16).clone()
     out = torch.empty((B, hv, dv), dtype=torch.float64)
     o_raw = torch.empty((B, hv, dv), dtype=torch.float64)
-    rc = lib.oracle_decode_step_h16(hk, hv, dk, dv, W, B, _ptr(_bf16_bits(x)), _ptr(_bf16_bits(conv_w)),
-                                    _ptr(cs), _ptr(_f32(g)), _ptr(_f32(beta)), _ptr(st),
-                                    _ptr(_bf16_bits(z)), _ptr(_bf16_bits(norm_w)), float(q_scale),
+    xb, wb, gg, bb, zb, nb = (_bf16_bits(x), _bf16_bits(conv_w), _f32(g), _f32(beta), _bf16_bits(z),
+                              _bf16_bits(norm_w))
+    rc = lib.oracle_decode_step_h16(hk, hv, dk, dv, W, B, _ptr(xb), _ptr(wb),
+                                    _ptr(cs), _ptr(gg), _ptr(bb), _ptr(st),
+                                    _ptr(zb), _ptr(nb), float(q_scale),
                                     float(l2_eps), float(rms_eps), _ptr(out), _ptr(o_raw),
                                     int(nthreads), int(mutation))
     if rc != 0:
         raise ValueError(f"oracle_decode_step_h16 failed ({rc})")
     return out, o_raw, cs.view(torch.bfloat16), st.view(torch.float16)
+
+
+def verify(x, conv_w, conv_state, g, beta, state, z, norm_w, committed_rows, num_k_heads, num_v_heads,
+           head_k_dim, head_v_dim, q_scale, l2_eps=1e-6, rms_eps=1e-6, nthreads: int = 0,
+           mutation: int = 0):
+    """A multi-token verify transaction: K rows per sequence, then commit of a prefix.
+
+    x [B,K,C], g/beta [B,K,Hv], z [B,K,Hv,Dv]; committed_rows: B integers in [0, K].  The rows of
+    every sequence are decoded in order from (conv_state, state), exactly as K one-token decode
+    steps; the outputs of all K rows are returned, and each sequence's states become those after
+    its first committed_rows[b] rows (0: the prior states, an abort).  Qwen3.8 kernel
+    architecture and TDD ledger, "Transaction and width vocabulary" (commit publishes only the
+    selected state; abort restores the prior state).  Returns (out float64 [B,K,Hv,Dv],
+    conv_state' bf16, state' float64); the arguments are not modified.
+    """
+    B, K = x.shape[0], x.shape[1]
+    m = [int(c) for c in committed_rows]
+    if len(m) != B or any(c < 0 or c > K for c in m):
+        raise ValueError("committed_rows must hold B values in [0, K]")
+    a = dict(num_k_heads=num_k_heads, num_v_heads=num_v_heads, head_k_dim=head_k_dim,
+             head_v_dim=head_v_dim, q_scale=q_scale, l2_eps=l2_eps, rms_eps=rms_eps,
+             nthreads=nthreads, mutation=mutation)
+    cs, st = conv_state, _f64(state)
+    cs_out, st_out = conv_state.clone(), st.clone()
+    outs = []
+    for i in range(K):
+        out, _, cs, st = decode_step(x[:, i], conv_w, cs, g[:, i], beta[:, i], st, z[:, i], norm_w, **a)
+        outs.append(out)
+        for b in range(B):
+            if m[b] == i + 1:
+                cs_out[b], st_out[b] = cs[b], st[b]
+    return torch.stack(outs, 1), cs_out, st_out
 
 
 def prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, num_k_heads, num_v_heads, head_k_dim,

@@ -489,3 +489,52 @@ def test_decode_h16_drift_stays_at_rounding_level():
         rel = ((h.double() - s64).norm() / s64.norm()).item()
         assert rel < 2.0 ** -10, (s, rel)
         assert (o16 - o64).abs().max().item() <= 2e-2 * o64.abs().max().item()
+
+
+# ------------------------------------------------------------------ multi-token verify + commit
+
+def _verify_inputs(B, K, seed, geo):
+    d = decode_inputs(B, K, seed=seed, geo=geo)
+    # [steps, B, ...] -> [B, K, ...]
+    return {k: (v.transpose(0, 1).contiguous() if k in ("x", "g", "beta", "z") else v) for k, v in d.items()}
+
+
+def test_verify_rows_equal_a_prefill_and_commit_selects_the_prefix_state():
+    """Verify outputs equal a K-token prefill of each sequence from the same states; the committed
+    states equal an m-token prefill's final states (m = 0: the prior states, bit for bit), and the
+    committed conv state is the last W-1 raw inputs of [prior conv state, the m rows]."""
+    geo = SMALL
+    B, K = 5, 6
+    v = _verify_inputs(B, K, seed=41, geo=geo)
+    a = dict(num_k_heads=geo.num_k_heads, num_v_heads=geo.num_v_heads, head_k_dim=geo.head_k_dim,
+             head_v_dim=geo.head_v_dim, q_scale=0.3)
+    m = [0, 1, 3, 6, 2]
+    out, cs, st = oracle.verify(v["x"], v["conv_w"], v["conv_state0"], v["g"], v["beta"], v["state0"], v["z"],
+                                v["norm_w"], m, **a)
+    C = v["x"].shape[-1]
+    for b in range(B):
+        ref = oracle.prefill(v["x"][b], v["conv_w"], cu_seqlens_of([K]), v["g"][b], v["beta"][b], v["z"][b],
+                             v["norm_w"], state_in=v["state0"][b:b + 1], conv_state_in=v["conv_state0"][b:b + 1], **a)
+        assert torch.allclose(out[b], ref["out"], rtol=1e-12, atol=1e-14)
+        if m[b] == 0:
+            assert torch.equal(st[b], v["state0"][b].double())
+            assert torch.equal(cs[b].view(torch.int16), v["conv_state0"][b].view(torch.int16))
+            continue
+        pre = oracle.prefill(v["x"][b, :m[b]], v["conv_w"], cu_seqlens_of([m[b]]), v["g"][b, :m[b]],
+                             v["beta"][b, :m[b]], v["z"][b, :m[b]], v["norm_w"], state_in=v["state0"][b:b + 1],
+                             conv_state_in=v["conv_state0"][b:b + 1], **a)
+        assert torch.allclose(st[b], pre["state"][0], rtol=1e-12, atol=1e-14)
+        window = torch.cat([v["conv_state0"][b].T, v["x"][b, :m[b]]], 0)  # [3 + m, C], oldest first
+        assert torch.equal(cs[b].view(torch.int16), window[-3:].T.contiguous().view(torch.int16))
+        assert cs[b].shape == (C, 3)
+
+
+def test_verify_refuses_committed_rows_out_of_range():
+    geo = SMALL
+    v = _verify_inputs(2, 3, seed=42, geo=geo)
+    a = dict(num_k_heads=geo.num_k_heads, num_v_heads=geo.num_v_heads, head_k_dim=geo.head_k_dim,
+             head_v_dim=geo.head_v_dim, q_scale=0.3)
+    for bad in ([0, 4], [-1, 0], [1]):
+        with pytest.raises(ValueError):
+            oracle.verify(v["x"], v["conv_w"], v["conv_state0"], v["g"], v["beta"], v["state0"], v["z"],
+                          v["norm_w"], bad, **a)

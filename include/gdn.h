@@ -215,6 +215,49 @@ GDN_API gdn_status gdn_decode_step_fp16_state(const gdn_geometry* geo, const gdn
                                               float q_scale, float l2_eps, float rms_eps,
                                               gdn_bf16* out, int32_t batch, void* stream);
 
+/*
+ * Multi-token verify: `rows` (K, 1..17) consecutive tokens of each of `batch` sequences run
+ * through the decode step in order -- conv step, L2 norms, gated delta rule, gated RMSNorm --
+ * starting from conv_state and state, exactly as K calls of gdn_decode_step would, but WITHOUT
+ * modifying either state.  Every row's gated output is written; what a later commit needs is
+ * written to `stash`.  Qwen3.8 kernel architecture and TDD ledger, "Transaction and width
+ * vocabulary" (verify_rows; a target transaction resolves exactly once: commit publishes only the
+ * selected GDN state, abort leaves the prior state); spark_model layer_struct.rs, the WY verify
+ * kernels (K = 2..17) and the write-on-accept twin with its post-verdict fold.
+ *
+ *   x           [batch, rows, C] bf16 raw conv inputs
+ *   conv_w      [C, W] bf16;  conv_state [batch, C, W-1] bf16 (read only)
+ *   g, beta     [batch, rows, Hv] fp32
+ *   state       [batch, Hv, Dv, Dk] fp32 (read only)
+ *   z           [batch, rows, Hv, Dv] bf16;  norm_w [Dv] bf16
+ *   out         [batch, rows, Hv, Dv] bf16: row r is the output of the r+1-th token
+ *   stash       gdn_verify_stash_size(geo, batch, rows) bytes, 16-byte aligned; one record per
+ *               (sequence, row) at ((b * rows) + r) * (stash_size / (batch * rows)) bytes: the
+ *               row's raw conv inputs (C bf16), normalised keys (Hk x Dk fp32), v channels after
+ *               the conv (Hv x Dv bf16), exp(g) and beta (Hv fp32 each).
+ * GDN_ERR_UNSUPPORTED_GEOMETRY when `rows` rows of Hv/Hk V heads do not fit the kernel's shared
+ * memory (never for Hv/Hk <= 3).
+ */
+GDN_API size_t gdn_verify_stash_size(const gdn_geometry* geo, int32_t batch, int32_t rows);
+GDN_API gdn_status gdn_verify(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w,
+                              const gdn_bf16* conv_state, const float* g, const float* beta,
+                              const float* state, const gdn_bf16* z, const gdn_bf16* norm_w,
+                              float q_scale, float l2_eps, float rms_eps, gdn_bf16* out,
+                              int32_t batch, int32_t rows, void* stash, size_t stash_bytes,
+                              void* stream);
+
+/*
+ * Resolves a verify: for each sequence b, committed_rows[b] = m (device int32, 0..rows) rows are
+ * committed -- conv_state and state become what m decode steps of that sequence's first m rows
+ * would have left (m = 0: an abort, both states untouched).  Reads only stash records of rows
+ * < m.  The states must be the ones the verify read (unchanged since).  A value outside
+ * [0, rows] leaves that sequence untouched and raises GDN_ERR_DEVICE_ARGUMENT in the device
+ * error word.
+ */
+GDN_API gdn_status gdn_verify_commit(const gdn_geometry* geo, const int32_t* committed_rows,
+                                     const void* stash, gdn_bf16* conv_state, float* state,
+                                     int32_t batch, int32_t rows, void* stream);
+
 /* Capacity of the fixed scratch used by gdn_chunk_prefill_noalloc. */
 #define GDN_NOALLOC_MAX_SEQS 16384
 #define GDN_NOALLOC_SCRATCH_BYTES (256 + 4 * GDN_NOALLOC_MAX_SEQS) /* 65,792 bytes */

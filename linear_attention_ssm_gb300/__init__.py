@@ -20,6 +20,9 @@ from .binding import (  # noqa: F401
     gdn_decode_step_fp16_state,
     gdn_gated_rmsnorm,
     gdn_prefill,
+    gdn_verify,
+    gdn_verify_commit,
+    gdn_verify_stash_size,
     gdn_version,
     load_library,
 )

@@ -279,6 +279,76 @@ gdn_status gdn_decode_step_fp16_state(const gdn_geometry* geo, const gdn_bf16* x
                      batch, stream);
 }
 
+size_t gdn_verify_stash_size(const gdn_geometry* geo, int32_t batch, int32_t rows) {
+  if (check_geometry(geo) != GDN_OK || batch < 0 || rows < 1 || rows > gdn::kMaxVerifyRows) return 0;
+  const int C = 2 * geo->num_k_heads * gdn::kHeadDim + geo->num_v_heads * gdn::kHeadDim;
+  return (size_t)batch * rows * gdn::verify_stash_layout(C, geo->num_k_heads, geo->num_v_heads).bytes;
+}
+
+}  // extern "C"
+
+namespace {
+gdn_status check_verify_shape(const gdn_geometry* geo, int32_t batch, int32_t rows) {
+  gdn_status s = check_geometry(geo);
+  if (s != GDN_OK) return s;
+  if (batch < 0 || batch > 65535) return fail(GDN_ERR_INVALID_ARGUMENT, "batch must be in [0, 65535] (got %d)", batch);
+  if (rows < 1 || rows > gdn::kMaxVerifyRows)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "rows must be in [1, %d] (got %d)", gdn::kMaxVerifyRows, rows);
+  if (!gdn::verify_supported(rows, geo->num_k_heads, geo->num_v_heads))
+    return fail(GDN_ERR_UNSUPPORTED_GEOMETRY, "%d rows with %d V heads per K head exceed the verify kernel's shared memory",
+                rows, geo->num_v_heads / geo->num_k_heads);
+  return GDN_OK;
+}
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_verify(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w, const gdn_bf16* conv_state,
+                      const float* g, const float* beta, const float* state, const gdn_bf16* z,
+                      const gdn_bf16* norm_w, float q_scale, float l2_eps, float rms_eps, gdn_bf16* out,
+                      int32_t batch, int32_t rows, void* stash, size_t stash_bytes, void* stream) {
+  gdn_status s = check_verify_shape(geo, batch, rows);
+  if (s != GDN_OK) return s;
+  if (batch == 0) return ok();
+  GDN_REQUIRE(x, "x");
+  GDN_REQUIRE(conv_w, "conv_w");
+  GDN_REQUIRE(conv_state, "conv_state");
+  GDN_REQUIRE(state, "state");
+  GDN_REQUIRE(z, "z");
+  GDN_REQUIRE(norm_w, "norm_w");
+  GDN_REQUIRE(out, "out");
+  GDN_REQUIRE(stash, "stash");
+  if (!g || !beta) return fail(GDN_ERR_INVALID_ARGUMENT, "g or beta is NULL");
+  if ((reinterpret_cast<uintptr_t>(g) | reinterpret_cast<uintptr_t>(beta)) & 3u)
+    return fail(GDN_ERR_MISALIGNED, "g or beta is not 4-byte aligned");
+  if (!(l2_eps >= 0.f) || !(rms_eps >= 0.f)) return fail(GDN_ERR_INVALID_ARGUMENT, "eps must be >= 0");
+  const size_t need = gdn_verify_stash_size(geo, batch, rows);
+  if (stash_bytes < need) return fail(GDN_ERR_WORKSPACE, "stash of %zu bytes required (got %zu)", need, stash_bytes);
+  gdn::LaunchEnv env;
+  if ((s = make_env(stream, &env)) != GDN_OK) return s;
+  return launched(gdn::launch_verify(env, x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps, rms_eps,
+                                     out, stash, batch, rows, geo->num_k_heads, geo->num_v_heads),
+                  "verify launch");
+}
+
+gdn_status gdn_verify_commit(const gdn_geometry* geo, const int32_t* committed_rows, const void* stash,
+                             gdn_bf16* conv_state, float* state, int32_t batch, int32_t rows, void* stream) {
+  gdn_status s = check_verify_shape(geo, batch, rows);
+  if (s != GDN_OK) return s;
+  if (batch == 0) return ok();
+  if (!committed_rows) return fail(GDN_ERR_INVALID_ARGUMENT, "committed_rows is NULL");
+  if (reinterpret_cast<uintptr_t>(committed_rows) & 3u)
+    return fail(GDN_ERR_MISALIGNED, "committed_rows is not 4-byte aligned");
+  GDN_REQUIRE(stash, "stash");
+  GDN_REQUIRE(conv_state, "conv_state");
+  GDN_REQUIRE(state, "state");
+  gdn::LaunchEnv env;
+  if ((s = make_env(stream, &env)) != GDN_OK) return s;
+  return launched(gdn::launch_verify_commit(env, committed_rows, stash, conv_state, state, batch, rows,
+                                            geo->num_k_heads, geo->num_v_heads),
+                  "verify commit launch");
+}
+
 // ---- allocation-free chunk prefill: the schedule lives in a fixed device array of this file
 }  // extern "C"
 

@@ -1,0 +1,141 @@
+"""GPU parity of the multi-token verify and its commit against the oracle's verify transaction:
+every row's output, the committed states for prefixes 0..K, untouched states after the verify,
+stash rows past the committed prefix never read (poisoned), bad verdicts refused, and the
+equivalence with K one-token decode steps."""
+import pytest
+import torch
+
+import oracle
+from linear_attention_ssm_gb300.synth import DECODE_BATCH, decode_inputs
+from tests.gpu_common import DEV, assert_out_close, assert_state_close, lib
+
+pytestmark = pytest.mark.gpu
+A = dict(num_k_heads=16, num_v_heads=48, head_k_dim=128, head_v_dim=128)
+RECORD = 41344  # stash bytes per (sequence, row) at the 16 / 48 / 128 geometry
+
+
+def _inputs(B, K, seed):
+    d = decode_inputs(B, K, seed=seed)
+    for k in ("x", "g", "beta", "z"):
+        d[k] = d[k].transpose(0, 1).contiguous()  # [K, B, ...] -> [B, K, ...]
+    return d
+
+
+def _dev(d):
+    return {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in d.items()}
+
+
+def _verify(g, dd, cs, st):
+    return g.gdn_verify(dd["x"], dd["conv_w"], cs, dd["g"], dd["beta"], st, dd["z"], dd["norm_w"], dd["q_scale"])
+
+
+@pytest.mark.parametrize("B,K,committed", [(5, 6, [0, 1, 3, 6, 2]), (3, 17, [17, 9, 4]), (4, 1, [1, 0, 1, 1])],
+                         ids=["k6", "k17", "k1"])
+def test_verify_and_commit_match_oracle(B, K, committed):
+    g = lib()
+    d = _inputs(B, K, seed=50 + K)
+    dd = _dev(d)
+    cs, st = dd["conv_state0"].clone(), dd["state0"].clone()
+    out, stash = _verify(g, dd, cs, st)
+    g.gdn_check_device_errors()
+    assert torch.equal(cs, dd["conv_state0"]) and torch.equal(st, dd["state0"])  # the verify reads only
+    g.gdn_verify_commit(torch.tensor(committed, dtype=torch.int32, device=DEV), stash, cs, st, K)
+    g.gdn_check_device_errors()
+    ref, cs_ref, st_ref = oracle.verify(d["x"], d["conv_w"], d["conv_state0"], d["g"], d["beta"], d["state0"],
+                                        d["z"], d["norm_w"], committed, q_scale=d["q_scale"], **A)
+    out = out.cpu()
+    for r in range(K):
+        assert_out_close(out[:, r], ref[:, r], f"out of row {r}")
+    for b in range(B):
+        assert_state_close(st[b], st_ref[b], f"state of sequence {b} after committing {committed[b]} rows")
+    assert torch.equal(cs.cpu().view(torch.int16), cs_ref.view(torch.int16))
+    for b in range(B):
+        if committed[b] == 0:
+            assert torch.equal(st[b], dd["state0"][b])
+
+
+def test_commit_never_reads_rows_past_the_prefix():
+    """Stash records of rejected rows are poisoned (all bits set: NaN keys and gates); the commit
+    gives the same bits as from the clean stash."""
+    g = lib()
+    B, K = 4, 8
+    committed = [2, 8, 0, 5]
+    d = _inputs(B, K, seed=60)
+    dd = _dev(d)
+    _, stash = _verify(g, dd, dd["conv_state0"], dd["state0"])
+    poisoned = stash.clone()
+    rec = stash.numel() // (B * K)
+    assert rec == RECORD
+    for b, m in enumerate(committed):
+        poisoned[(b * K + m) * rec:(b + 1) * K * rec] = 0xFF
+    cm = torch.tensor(committed, dtype=torch.int32, device=DEV)
+    cs1, st1 = dd["conv_state0"].clone(), dd["state0"].clone()
+    cs2, st2 = dd["conv_state0"].clone(), dd["state0"].clone()
+    g.gdn_verify_commit(cm, stash, cs1, st1, K)
+    g.gdn_verify_commit(cm, poisoned, cs2, st2, K)
+    g.gdn_check_device_errors()
+    assert torch.equal(st1, st2) and torch.equal(cs1, cs2)
+    assert torch.isfinite(st2).all()
+
+
+def test_verify_then_full_commit_equals_decode_steps():
+    """K one-token decode steps and a K-row verify committed in full give the same outputs and
+    states (the same fp32 expressions; the butterfly reduction adds the same pairs)."""
+    g = lib()
+    B, K = 3, 5
+    d = _inputs(B, K, seed=61)
+    dd = _dev(d)
+    cs, st = dd["conv_state0"].clone(), dd["state0"].clone()
+    outs = []
+    for r in range(K):
+        outs.append(g.gdn_decode_step(dd["x"][:, r].contiguous(), dd["conv_w"], cs, dd["g"][:, r].contiguous(),
+                                      dd["beta"][:, r].contiguous(), st, dd["z"][:, r].contiguous(), dd["norm_w"],
+                                      dd["q_scale"]))
+    cs_v, st_v = dd["conv_state0"].clone(), dd["state0"].clone()
+    out_v, stash = _verify(g, dd, cs_v, st_v)
+    g.gdn_verify_commit(torch.full((B,), K, dtype=torch.int32, device=DEV), stash, cs_v, st_v, K)
+    g.gdn_check_device_errors()
+    dec = torch.stack(outs, 1)
+    assert torch.equal(cs_v, cs)
+    assert (st_v - st).abs().max().item() <= 1e-6 * st.abs().max().item()
+    assert (out_v.float() - dec.float()).abs().max().item() <= 1e-2 * dec.float().abs().max().item()
+
+
+def test_commit_refuses_a_verdict_out_of_range():
+    g = lib()
+    B, K = 2, 4
+    d = _inputs(B, K, seed=62)
+    dd = _dev(d)
+    _, stash = _verify(g, dd, dd["conv_state0"], dd["state0"])
+    g.gdn_check_device_errors()
+    cs, st = dd["conv_state0"].clone(), dd["state0"].clone()
+    g.gdn_verify_commit(torch.tensor([K + 1, -1], dtype=torch.int32, device=DEV), stash, cs, st, K)
+    with pytest.raises(g.GdnError):
+        g.gdn_check_device_errors()
+    assert torch.equal(cs, dd["conv_state0"]) and torch.equal(st, dd["state0"])
+
+
+def test_verify_256_sequences_8_rows_sampled():
+    """The verify workload: 256 sequences x 8 rows, a seeded random verdict per sequence in 0..8;
+    three sequences checked against the oracle (outputs of every row, committed states)."""
+    g = lib()
+    B, K = DECODE_BATCH, 8
+    d = _inputs(B, K, seed=63)
+    gen = torch.Generator().manual_seed(63)
+    committed = torch.randint(0, K + 1, (B,), generator=gen, dtype=torch.int32)
+    dd = _dev(d)
+    cs, st = dd["conv_state0"].clone(), dd["state0"].clone()
+    out, stash = _verify(g, dd, cs, st)
+    g.gdn_verify_commit(committed.to(DEV), stash, cs, st, K)
+    g.gdn_check_device_errors()
+    out, cs, st = out.cpu(), cs.cpu(), st.cpu()
+    assert torch.isfinite(out.float()).all() and torch.isfinite(st).all()
+    sample = [0, 100, 255]
+    ref, cs_ref, st_ref = oracle.verify(d["x"][sample], d["conv_w"], d["conv_state0"][sample], d["g"][sample],
+                                        d["beta"][sample], d["state0"][sample], d["z"][sample], d["norm_w"],
+                                        [int(committed[b]) for b in sample], q_scale=d["q_scale"], **A)
+    for r in range(K):
+        assert_out_close(out[sample, r], ref[:, r], f"out of row {r}")
+    for i, b in enumerate(sample):
+        assert_state_close(st[b], st_ref[i], f"state of sequence {b}")
+    assert torch.equal(cs[sample].view(torch.int16), cs_ref.view(torch.int16))

@@ -49,10 +49,45 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--varlen-steps", type=int, default=10)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-verify", type=int, default=0, metavar="B",
+                    help="profiler mode: only the verify leg (8 rows) on B sequences, --warmup + --steps transactions")
     ap.add_argument("--profile-case", default=None,
                     help="run only the prefill (conv + chunk) on these comma-separated sequence lengths, "
                          "--steps times after --warmup, for profiling; prints one timing line")
     return ap.parse_args()
+
+
+def run_profile_verify(args, local):
+    """The verify leg alone for profilers: B sequences x 8 rows, verify + commit per transaction."""
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import linear_attention_ssm_gb300 as gdn
+    from linear_attention_ssm_gb300.synth import decode_inputs
+    B, K = args.profile_verify, VERIFY_ROWS
+    d = decode_inputs(B, K, seed=5)
+    vx, vg, vb, vz = (d[k].transpose(0, 1).contiguous().to(dev) for k in ("x", "g", "beta", "z"))
+    w, nw = d["conv_w"].to(dev), d["norm_w"].to(dev)
+    st, cs = d["state0"].to(dev), d["conv_state0"].to(dev)
+    cm = torch.randint(1, K + 1, (B,), generator=torch.Generator().manual_seed(5), dtype=torch.int32).to(dev)
+    out = torch.empty((B, K, 48, 128), dtype=torch.bfloat16, device=dev)
+    stash = torch.empty(gdn.gdn_verify_stash_size(B, K), dtype=torch.uint8, device=dev)
+
+    def step():
+        gdn.gdn_verify(vx, w, cs, vg, vb, st, vz, nw, d["q_scale"], out=out, stash=stash)
+        gdn.gdn_verify_commit(cm, stash, cs, st, K)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    gdn.gdn_check_device_errors()
+    print(json.dumps({"profile_verify": B, "rows": K, "ms_per_transaction": e0.elapsed_time(e1) / max(args.steps, 1)}))
 
 
 def run_profile_case(args, local):
@@ -562,7 +597,9 @@ def run_ours(args, rank, world, local):
 def main():
     args = parse()
     rank, world, local = dist_env()
-    if args.profile_case:
+    if args.profile_verify:
+        run_profile_verify(args, local)
+    elif args.profile_case:
         run_profile_case(args, local)
     elif args.impl == "reference":
         run_reference(args, rank, world)

@@ -79,8 +79,8 @@ def test_commit_never_reads_rows_past_the_prefix():
 
 
 def test_verify_then_full_commit_equals_decode_steps():
-    """K one-token decode steps and a K-row verify committed in full give the same outputs and
-    states (the same fp32 expressions; the butterfly reduction adds the same pairs)."""
+    """K one-token decode steps and a K-row verify committed in full agree to fp32 rounding (the
+    same per-element expressions; the dot products are summed in another order)."""
     g = lib()
     B, K = 3, 5
     d = _inputs(B, K, seed=61)
@@ -97,7 +97,7 @@ def test_verify_then_full_commit_equals_decode_steps():
     g.gdn_check_device_errors()
     dec = torch.stack(outs, 1)
     assert torch.equal(cs_v, cs)
-    assert (st_v - st).abs().max().item() <= 1e-6 * st.abs().max().item()
+    assert (st_v - st).abs().max().item() <= 1e-5 * st.abs().max().item()
     assert (out_v.float() - dec.float()).abs().max().item() <= 1e-2 * dec.float().abs().max().item()
 
 

@@ -270,10 +270,10 @@ def run_reference(args, rank, world):
 
 
 VERIFY_ROWS = 8
-VERIFY_RECORD = 41344  # stash bytes per (sequence, row): raw inputs, keys, v, exp(g), beta
+VERIFY_RECORD = 53440  # stash bytes per (sequence, row): raw inputs, keys, deltas, g
 
 
-def time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak):
+def time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak, state_dtype=None):
     """Verify of 8 rows for each of 256 sequences, then the commit of a seeded verdict in 1..8
     (the accepted proposals plus one correction row).  Both kernels are timed with events."""
     import torch
@@ -282,7 +282,7 @@ def time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak
     d = decode_inputs(B, K, seed=5)
     vx, vg, vb, vz = (d[k].transpose(0, 1).contiguous().to(dev) for k in ("x", "g", "beta", "z"))
     w, nw = d["conv_w"].to(dev), d["norm_w"].to(dev)
-    st0, cs0 = d["state0"].to(dev), d["conv_state0"].to(dev)
+    st0, cs0 = d["state0"].to(dev).to(state_dtype or torch.float32), d["conv_state0"].to(dev)
     st, cs = st0.clone(), cs0.clone()
     gen = torch.Generator().manual_seed(5)
     committed = torch.randint(1, K + 1, (B,), generator=gen, dtype=torch.int32)
@@ -310,12 +310,13 @@ def time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak
     c_ms = max_over_ranks(sum(e[1].elapsed_time(e[2]) for e in evs) / n)
     step_ms = max_over_ranks(sum(e[0].elapsed_time(e[2]) for e in evs) / n)
     C, hv = 10240, 48
-    state_bytes = B * hv * 128 * 128 * 4
+    state_bytes = B * hv * 128 * 128 * st0.element_size()
     v_bytes = (state_bytes + B * K * C * 2 + B * C * 3 * 2 + B * K * hv * 8 + 2 * B * K * hv * 128 * 2
                + B * K * VERIFY_RECORD)
     m = committed.tolist()
     c_bytes = (2 * state_bytes + 2 * B * C * 3 * 2
-               + sum(r * (16 * 128 * 4 + hv * 128 * 2 + hv * 8) + min(r, 3) * C * 2 for r in m))
+               + sum(r * (16 * 128 * 4 + hv * 128 * 4 + hv * 4) + min(r, 3) * C * 2 for r in m))
+    sfx = "_fp16_state" if st0.element_size() == 2 else ""
     roof = lambda nbytes, ms, kernel, rec: {"kernel": kernel, "bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9,
                                             "peak": hbm_peak, "unit": "GB/s",
                                             "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
@@ -324,9 +325,10 @@ def time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak
     return {"metric": "verify rows/s", "value": world * B * K / (step_ms / 1e3), "unit": "rows/s",
             "ms_per_step": step_ms, "steps": n, "batch": B, "rows": K,
             "committed_rows_mean": sum(m) / B,
-            "workload": "256 sequences x 8 verify rows (fp32 state), then the commit of a seeded verdict in 1..8",
-            "roofline_verify": roof(v_bytes, v_ms, "verify_kernel", "verify"),
-            "roofline_commit": roof(c_bytes, c_ms, "commit_kernel", "verify_commit")}
+            "workload": f"256 sequences x 8 verify rows ({'binary16' if st0.element_size() == 2 else 'fp32'} state), "
+                        "then the commit of a seeded verdict in 1..8",
+            "roofline_verify": roof(v_bytes, v_ms, "verify_kernel", "verify" + sfx),
+            "roofline_commit": roof(c_bytes, c_ms, "commit_kernel", "verify_commit" + sfx)}
 
 
 def run_ours(args, rank, world, local):
@@ -564,6 +566,7 @@ def run_ours(args, rank, world, local):
 
     # ---------------- multi-token verify: 256 sequences x 8 rows, then the commit of a verdict
     verify = time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak)
+    verify_f16 = time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak, torch.float16)
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
@@ -583,7 +586,8 @@ def run_ours(args, rank, world, local):
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                     "pipelined": "H2D of step i+1 and D2H of step i-1 overlap the prefill of step i"},
-            "decode": decode, "decode_fp16_state": decode_f16, "verify": verify, "varlen": varlen, "cpu_baseline": cpu, "clocks": clk,
+            "decode": decode, "decode_fp16_state": decode_f16, "verify": verify, "verify_fp16_state": verify_f16,
+            "varlen": varlen, "cpu_baseline": cpu, "clocks": clk,
             # per step: conv1d + conv-state kernels, the chunk prefill's schedule and segment-table
             # kernels, then a prep and a state kernel for each of its three chunk segments
             "gpu_launches": (2 + 2 + 2 * 3) * args.steps,

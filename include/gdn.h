@@ -233,8 +233,9 @@ GDN_API gdn_status gdn_decode_step_fp16_state(const gdn_geometry* geo, const gdn
  *   out         [batch, rows, Hv, Dv] bf16: row r is the output of the r+1-th token
  *   stash       gdn_verify_stash_size(geo, batch, rows) bytes, 16-byte aligned; one record per
  *               (sequence, row) at ((b * rows) + r) * (stash_size / (batch * rows)) bytes: the
- *               row's raw conv inputs (C bf16), normalised keys (Hk x Dk fp32), v channels after
- *               the conv (Hv x Dv bf16), exp(g) and beta (Hv fp32 each).
+ *               row's raw conv inputs (C bf16), normalised keys (Hk x Dk fp32), its delta
+ *               e = beta (v - decayed state . k) for every V head and value row (Hv x Dv fp32)
+ *               and g (Hv fp32).
  * GDN_ERR_UNSUPPORTED_GEOMETRY when `rows` rows of Hv/Hk V heads do not fit the kernel's shared
  * memory (never for Hv/Hk <= 3).
  */
@@ -257,6 +258,28 @@ GDN_API gdn_status gdn_verify(const gdn_geometry* geo, const gdn_bf16* x, const 
 GDN_API gdn_status gdn_verify_commit(const gdn_geometry* geo, const int32_t* committed_rows,
                                      const void* stash, gdn_bf16* conv_state, float* state,
                                      int32_t batch, int32_t rows, void* stream);
+
+/*
+ * gdn_verify and gdn_verify_commit with the recurrent state stored as IEEE binary16 (Qwen3.8
+ * ledger, the FP16 h-state twins of the WY verify kernels).  The verify widens the state and
+ * computes in fp32 exactly as gdn_verify; the commit widens it, applies the committed rows and
+ * stores the result rounded once to binary16 (to nearest, ties to even).  No per-row state is
+ * ever stored, so that is the only rounding: a commit of m rows equals m calls of
+ * gdn_decode_step_fp16_state up to the roundings those calls make between the rows.  The stash
+ * is the same as gdn_verify's; m = 0 leaves the state's bits untouched.
+ *   state       [batch, Hv, Dv, Dk] binary16 (read only in the verify; in/out in the commit)
+ */
+GDN_API gdn_status gdn_verify_fp16_state(const gdn_geometry* geo, const gdn_bf16* x,
+                                         const gdn_bf16* conv_w, const gdn_bf16* conv_state,
+                                         const float* g, const float* beta, const gdn_f16* state,
+                                         const gdn_bf16* z, const gdn_bf16* norm_w, float q_scale,
+                                         float l2_eps, float rms_eps, gdn_bf16* out, int32_t batch,
+                                         int32_t rows, void* stash, size_t stash_bytes,
+                                         void* stream);
+GDN_API gdn_status gdn_verify_commit_fp16_state(const gdn_geometry* geo,
+                                                const int32_t* committed_rows, const void* stash,
+                                                gdn_bf16* conv_state, gdn_f16* state,
+                                                int32_t batch, int32_t rows, void* stream);
 
 /* Capacity of the fixed scratch used by gdn_chunk_prefill_noalloc. */
 #define GDN_NOALLOC_MAX_SEQS 16384

@@ -63,6 +63,8 @@ def load_library():
             "gdn_verify_stash_size": ([G, I, I], S),
             "gdn_verify": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, I, P, S, P], ctypes.c_int),
             "gdn_verify_commit": ([G, P, P, P, P, I, I, P], ctypes.c_int),
+            "gdn_verify_fp16_state": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, I, P, S, P], ctypes.c_int),
+            "gdn_verify_commit_fp16_state": ([G, P, P, P, P, I, I, P], ctypes.c_int),
             "gdn_check_device_errors": ([P], ctypes.c_int),
             "gdn_debug_set_chunk_mode": ([ctypes.c_int], ctypes.c_int),
             "gdn_debug_get_chunk_mode": ([], ctypes.c_int),
@@ -244,9 +246,11 @@ def gdn_verify(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps
                out=None, stash=None, geometry: Geometry = QWEN_GDN, stream=None):
     """Multi-token verify: rows = x.shape[1] tokens per sequence, states read only.
 
-    Returns (out [B, K, Hv, Dv] bf16, stash uint8) -- pass the stash to gdn_verify_commit.
+    ``state`` is fp32 (gdn_verify) or fp16 (gdn_verify_fp16_state).  Returns (out [B, K, Hv, Dv]
+    bf16, stash uint8) -- pass the stash to gdn_verify_commit.
     """
     lib = load_library()
+    fp16_state = state.dtype == torch.float16
     C, W = geometry.conv_dim, geometry.conv_width
     hv, dv, dk = geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
     B, K = x.shape[0], x.shape[1]
@@ -255,7 +259,7 @@ def gdn_verify(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps
     _dev(conv_state, torch.bfloat16, "conv_state", (B, C, W - 1))
     _dev(g, torch.float32, "g", (B, K, hv))
     _dev(beta, torch.float32, "beta", (B, K, hv))
-    _dev(state, torch.float32, "state", (B, hv, dv, dk))
+    _dev(state, torch.float16 if fp16_state else torch.float32, "state", (B, hv, dv, dk))
     _dev(z, torch.bfloat16, "z", (B, K, hv, dv))
     _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
     if out is None:
@@ -265,27 +269,31 @@ def gdn_verify(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps
     if stash is None:
         stash = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _dev(stash, torch.uint8, "stash")
-    _check(lib.gdn_verify(_geo(geometry), _p(x), _p(conv_w), _p(conv_state), _p(g), _p(beta), _p(state), _p(z),
-                          _p(norm_w), float(q_scale), float(l2_eps), float(rms_eps), _p(out), B, K, _p(stash),
-                          stash.numel(), _stream(stream)))
+    fn = lib.gdn_verify_fp16_state if fp16_state else lib.gdn_verify
+    _check(fn(_geo(geometry), _p(x), _p(conv_w), _p(conv_state), _p(g), _p(beta), _p(state), _p(z), _p(norm_w),
+              float(q_scale), float(l2_eps), float(rms_eps), _p(out), B, K, _p(stash), stash.numel(),
+              _stream(stream)))
     return out, stash
 
 
 def gdn_verify_commit(committed_rows, stash, conv_state, state, rows: int, geometry: Geometry = QWEN_GDN,
                       stream=None):
-    """Commit committed_rows[b] (device int32, 0..rows) rows of a verify into conv_state and state."""
+    """Commit committed_rows[b] (device int32, 0..rows) rows of a verify into conv_state and state
+    (fp32, or fp16: gdn_verify_commit_fp16_state)."""
     lib = load_library()
+    fp16_state = state.dtype == torch.float16
     C, W = geometry.conv_dim, geometry.conv_width
     hv, dv, dk = geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
     B = committed_rows.shape[0]
     _dev(committed_rows, torch.int32, "committed_rows", (B,))
     _dev(stash, torch.uint8, "stash")
     _dev(conv_state, torch.bfloat16, "conv_state", (B, C, W - 1))
-    _dev(state, torch.float32, "state", (B, hv, dv, dk))
+    _dev(state, torch.float16 if fp16_state else torch.float32, "state", (B, hv, dv, dk))
     if stash.numel() < gdn_verify_stash_size(B, rows, geometry):
         raise ValueError("stash is smaller than gdn_verify_stash_size(batch, rows)")
-    _check(lib.gdn_verify_commit(_geo(geometry), _p(committed_rows), _p(stash), _p(conv_state), _p(state), B,
-                                 int(rows), _stream(stream)))
+    fn = lib.gdn_verify_commit_fp16_state if fp16_state else lib.gdn_verify_commit
+    _check(fn(_geo(geometry), _p(committed_rows), _p(stash), _p(conv_state), _p(state), B, int(rows),
+              _stream(stream)))
 
 
 def gdn_check_device_errors(stream=None):

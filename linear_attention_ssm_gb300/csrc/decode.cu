@@ -133,11 +133,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     float ns[24];
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
-      float acc = wv[ch * 4 + 0] * st[ch * 3 + 0];
-      acc = fmaf(wv[ch * 4 + 1], st[ch * 3 + 1], acc);
-      acc = fmaf(wv[ch * 4 + 2], st[ch * 3 + 2], acc);
-      acc = fmaf(wv[ch * 4 + 3], xv[ch], acc);
-      dst[ch] = bf2f(f2bf(acc / (1.0f + expf(-acc))));  // the bf16 conv output
+      // the bf16 conv output, rounded as the exact value is
+      dst[ch] = bf2f(silu_bf16_rn(wv[ch * 4 + 0], st[ch * 3 + 0], wv[ch * 4 + 1], st[ch * 3 + 1], wv[ch * 4 + 2],
+                                  st[ch * 3 + 2], wv[ch * 4 + 3], xv[ch]));
       ns[ch * 3 + 0] = st[ch * 3 + 1];
       ns[ch * 3 + 1] = st[ch * 3 + 2];
       ns[ch * 3 + 2] = xv[ch];

@@ -303,10 +303,13 @@ gdn_status check_verify_shape(const gdn_geometry* geo, int32_t batch, int32_t ro
 
 extern "C" {
 
-gdn_status gdn_verify(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w, const gdn_bf16* conv_state,
-                      const float* g, const float* beta, const float* state, const gdn_bf16* z,
-                      const gdn_bf16* norm_w, float q_scale, float l2_eps, float rms_eps, gdn_bf16* out,
-                      int32_t batch, int32_t rows, void* stash, size_t stash_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+gdn_status verify(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w, const gdn_bf16* conv_state,
+                  const float* g, const float* beta, const void* state, bool fp16_state, const gdn_bf16* z,
+                  const gdn_bf16* norm_w, float q_scale, float l2_eps, float rms_eps, gdn_bf16* out, int32_t batch,
+                  int32_t rows, void* stash, size_t stash_bytes, void* stream) {
   gdn_status s = check_verify_shape(geo, batch, rows);
   if (s != GDN_OK) return s;
   if (batch == 0) return ok();
@@ -326,13 +329,14 @@ gdn_status gdn_verify(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16
   if (stash_bytes < need) return fail(GDN_ERR_WORKSPACE, "stash of %zu bytes required (got %zu)", need, stash_bytes);
   gdn::LaunchEnv env;
   if ((s = make_env(stream, &env)) != GDN_OK) return s;
-  return launched(gdn::launch_verify(env, x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps, rms_eps,
-                                     out, stash, batch, rows, geo->num_k_heads, geo->num_v_heads),
+  return launched(gdn::launch_verify(env, x, conv_w, conv_state, g, beta, state, fp16_state, z, norm_w, q_scale,
+                                     l2_eps, rms_eps, out, stash, batch, rows, geo->num_k_heads, geo->num_v_heads),
                   "verify launch");
 }
 
-gdn_status gdn_verify_commit(const gdn_geometry* geo, const int32_t* committed_rows, const void* stash,
-                             gdn_bf16* conv_state, float* state, int32_t batch, int32_t rows, void* stream) {
+gdn_status verify_commit(const gdn_geometry* geo, const int32_t* committed_rows, const void* stash,
+                         gdn_bf16* conv_state, void* state, bool fp16_state, int32_t batch, int32_t rows,
+                         void* stream) {
   gdn_status s = check_verify_shape(geo, batch, rows);
   if (s != GDN_OK) return s;
   if (batch == 0) return ok();
@@ -344,9 +348,40 @@ gdn_status gdn_verify_commit(const gdn_geometry* geo, const int32_t* committed_r
   GDN_REQUIRE(state, "state");
   gdn::LaunchEnv env;
   if ((s = make_env(stream, &env)) != GDN_OK) return s;
-  return launched(gdn::launch_verify_commit(env, committed_rows, stash, conv_state, state, batch, rows,
+  return launched(gdn::launch_verify_commit(env, committed_rows, stash, conv_state, state, fp16_state, batch, rows,
                                             geo->num_k_heads, geo->num_v_heads),
                   "verify commit launch");
+}
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_verify(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w, const gdn_bf16* conv_state,
+                      const float* g, const float* beta, const float* state, const gdn_bf16* z,
+                      const gdn_bf16* norm_w, float q_scale, float l2_eps, float rms_eps, gdn_bf16* out,
+                      int32_t batch, int32_t rows, void* stash, size_t stash_bytes, void* stream) {
+  return verify(geo, x, conv_w, conv_state, g, beta, state, false, z, norm_w, q_scale, l2_eps, rms_eps, out, batch,
+                rows, stash, stash_bytes, stream);
+}
+
+gdn_status gdn_verify_fp16_state(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w,
+                                 const gdn_bf16* conv_state, const float* g, const float* beta, const gdn_f16* state,
+                                 const gdn_bf16* z, const gdn_bf16* norm_w, float q_scale, float l2_eps,
+                                 float rms_eps, gdn_bf16* out, int32_t batch, int32_t rows, void* stash,
+                                 size_t stash_bytes, void* stream) {
+  return verify(geo, x, conv_w, conv_state, g, beta, state, true, z, norm_w, q_scale, l2_eps, rms_eps, out, batch,
+                rows, stash, stash_bytes, stream);
+}
+
+gdn_status gdn_verify_commit(const gdn_geometry* geo, const int32_t* committed_rows, const void* stash,
+                             gdn_bf16* conv_state, float* state, int32_t batch, int32_t rows, void* stream) {
+  return verify_commit(geo, committed_rows, stash, conv_state, state, false, batch, rows, stream);
+}
+
+gdn_status gdn_verify_commit_fp16_state(const gdn_geometry* geo, const int32_t* committed_rows, const void* stash,
+                                        gdn_bf16* conv_state, gdn_f16* state, int32_t batch, int32_t rows,
+                                        void* stream) {
+  return verify_commit(geo, committed_rows, stash, conv_state, state, true, batch, rows, stream);
 }
 
 // ---- allocation-free chunk prefill: the schedule lives in a fixed device array of this file

@@ -34,6 +34,36 @@ __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf
 
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(x) = 2^(x log2 e)
 
+// a + b = s + e exactly (Knuth's two-sum; rounded-to-nearest operations that nothing may fuse)
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// SiLU of the width-4 conv tap sum w0 x0 + w1 x1 + w2 x2 + w3 x3 (bf16 weights and inputs held as
+// floats), rounded to the bf16 nearest the exact value.  Every bf16 x bf16 product is exact in
+// fp32 and the sum is carried exactly as s + e1 + e2 + e3 (two-sums), so the fp32 SiLU estimate
+// from it errs by a few ulps (more for large negative sums, where exp amplifies the argument's
+// rounding); where the estimate lies that close to a bf16 rounding midpoint, the SiLU is
+// recomputed in fp64 from the exact sum before rounding.
+__device__ __forceinline__ uint16_t silu_bf16_rn(float w0, float x0, float w1, float x1, float w2, float x2,
+                                                 float w3, float x3) {
+  float s, e1, e2, e3;
+  two_sum(__fmul_rn(w0, x0), __fmul_rn(w1, x1), s, e1);
+  two_sum(s, __fmul_rn(w2, x2), s, e2);
+  two_sum(s, __fmul_rn(w3, x3), s, e3);
+  const float acc = __fadd_rn(s, __fadd_rn(__fadd_rn(e1, e2), e3));
+  const float y = acc / (1.0f + expf(-acc));
+  const int off = (int)(__float_as_uint(y) & 0xFFFFu) - 0x8000;  // fp32 ulps from the midpoint
+  const int margin = 32 + (int)fminf(2.f * fabsf(acc), 4096.f);
+  if (off >= -margin && off <= margin) {
+    const double ad = (double)s + (double)e1 + (double)e2 + (double)e3;
+    return __bfloat16_as_ushort(__double2bfloat16(ad / (1.0 + exp(-ad))));
+  }
+  return f2bf(y);
+}
+
 // 2^x by the hardware approximation instruction (relative error ~2^-22; results below the
 // smallest normal flush to zero).
 __device__ __forceinline__ float ex2_approx(float x) {

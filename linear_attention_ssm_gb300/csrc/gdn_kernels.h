@@ -27,29 +27,29 @@ cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const ui
 constexpr int kMaxVerifyRows = 17;
 constexpr size_t kMaxVerifySmem = 110 * 1024;  // two verify CTAs per SM
 // One stash record per (sequence, row): the row's raw conv inputs (C bf16), its normalised keys
-// (Hk x 128 fp32), its v channels after the conv (Hv x 128 bf16), alpha = exp(g) and beta
-// (Hv fp32 each); records are 16-byte multiples, record (b, r) at (b * K + r) * bytes.
+// (Hk x 128 fp32), the delta e = beta (v - decayed state . k) of every V head and value row
+// (Hv x 128 fp32) and g (Hv fp32); records are 16-byte multiples, record (b, r) at
+// (b * K + r) * bytes.
 struct VerifyStash {
-  size_t x_off, khat_off, v_off, alpha_off, beta_off, bytes;
+  size_t x_off, khat_off, e_off, g_off, bytes;
 };
 __host__ __device__ inline VerifyStash verify_stash_layout(int C, int Hk, int Hv) {
   VerifyStash L;
   L.x_off = 0;
   L.khat_off = (size_t)C * 2;
-  L.v_off = L.khat_off + (size_t)Hk * kHeadDim * 4;
-  L.alpha_off = L.v_off + (size_t)Hv * kHeadDim * 2;
-  L.beta_off = L.alpha_off + (size_t)Hv * 4;
-  L.bytes = (L.beta_off + (size_t)Hv * 4 + 15) & ~(size_t)15;
+  L.e_off = L.khat_off + (size_t)Hk * kHeadDim * 4;
+  L.g_off = L.e_off + (size_t)Hv * kHeadDim * 4;
+  L.bytes = (L.g_off + (size_t)Hv * 4 + 15) & ~(size_t)15;
   return L;
 }
 int verify_max_rows();
 bool verify_supported(int K, int Hk, int Hv);
 cudaError_t launch_verify(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w, const uint16_t* conv_state,
-                          const float* g, const float* beta, const float* state, const uint16_t* z,
+                          const float* g, const float* beta, const void* state, bool fp16_state, const uint16_t* z,
                           const uint16_t* norm_w, float q_scale, float l2_eps, float rms_eps, uint16_t* out,
                           void* stash, int B, int K, int Hk, int Hv);
 cudaError_t launch_verify_commit(const LaunchEnv& env, const int32_t* committed, const void* stash,
-                                 uint16_t* conv_state, float* state, int B, int K, int Hk, int Hv);
+                                 uint16_t* conv_state, void* state, bool fp16_state, int B, int K, int Hk, int Hv);
 
 // Workspace of the fused chunk prefill: a work counter and the longest-first sequence order.
 size_t chunk_prefill_workspace_bytes(int N);

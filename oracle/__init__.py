@@ -287,6 +287,27 @@ def verify(x, conv_w, conv_state, g, beta, state, z, norm_w, committed_rows, num
     return torch.stack(outs, 1), cs_out, st_out
 
 
+def verify_h16(x, conv_w, conv_state, g, beta, state, z, norm_w, committed_rows, num_k_heads, num_v_heads,
+               head_k_dim, head_v_dim, q_scale, l2_eps=1e-6, rms_eps=1e-6, nthreads: int = 0,
+               mutation: int = 0):
+    """verify with the recurrent state stored as binary16 (torch.float16 [B,Hv,Dv,Dk]).
+
+    The state is widened exactly, the transaction runs in float64 (no state is stored between the
+    rows, so none is rounded there), and each committed state is rounded once to binary16; a
+    sequence with committed_rows 0 keeps its state's bits.  Returns (out float64, conv_state',
+    state' float16).
+    """
+    assert state.dtype == torch.float16, state.dtype
+    out, cs, st = verify(x, conv_w, conv_state, g, beta, f16_to_double(state), z, norm_w, committed_rows,
+                         num_k_heads, num_v_heads, head_k_dim, head_v_dim, q_scale, l2_eps, rms_eps,
+                         nthreads, mutation)
+    st16 = state.detach().cpu().clone()
+    for b, m in enumerate(committed_rows):
+        if int(m) > 0:
+            st16[b] = round_f16(st[b])
+    return out, cs, st16
+
+
 def prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, num_k_heads, num_v_heads, head_k_dim,
             head_v_dim, q_scale, l2_eps=1e-6, rms_eps=1e-6, state_in=None, conv_state_in=None,
             heads=None, nthreads: int = 0, mutation: int = 0):

@@ -149,19 +149,19 @@ def test_binding_refuses_cpu_tensors():
 
 
 def test_verify_stash_size_and_argument_checks(lib):
-    """One 41,344-byte record per (sequence, row): raw inputs 20,480 + keys 16 x 128 x 4 + v 48 x 128
-    x 2 + exp(g) and beta 2 x 48 x 4.  Rows outside [1, 17] and a short stash are refused before any
+    """One 53,440-byte record per (sequence, row): raw inputs 20,480 + keys 16 x 128 x 4 + deltas
+    48 x 128 x 4 + g 48 x 4.  Rows outside [1, 17] and a short stash are refused before any
     launch; batch 0 is a no-op."""
     geo = _geo()
-    assert lib.gdn_verify_stash_size(geo, 256, 8) == 256 * 8 * 41344
-    assert lib.gdn_verify_stash_size(geo, 3, 17) == 3 * 17 * 41344
+    assert lib.gdn_verify_stash_size(geo, 256, 8) == 256 * 8 * 53440
+    assert lib.gdn_verify_stash_size(geo, 3, 17) == 3 * 17 * 53440
     assert lib.gdn_verify_stash_size(geo, 1, 0) == 0 and lib.gdn_verify_stash_size(geo, 1, 18) == 0
     args = [geo, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.088, 1e-6, 1e-6, FAKE]
     big = 1 << 40
     assert lib.gdn_verify(*args, 4, 0, FAKE, big, None) == 1        # rows 0
     assert lib.gdn_verify(*args, 4, 18, FAKE, big, None) == 1       # rows 18
     assert lib.gdn_verify(*args, -1, 8, FAKE, big, None) == 1       # negative batch
-    assert lib.gdn_verify(*args, 4, 8, FAKE, 4 * 8 * 41344 - 1, None) == 7  # stash too small
+    assert lib.gdn_verify(*args, 4, 8, FAKE, 4 * 8 * 53440 - 1, None) == 7  # stash too small
     assert lib.gdn_verify(*args, 4, 8, None, big, None) == 1        # no stash
     assert lib.gdn_verify(*args, 0, 8, None, 0, None) == 0          # nothing to do
     # 12 V heads per K head: 17 rows no longer fit the kernel's shared memory
@@ -170,3 +170,6 @@ def test_verify_stash_size_and_argument_checks(lib):
     assert lib.gdn_verify_commit(geo, None, FAKE, FAKE, FAKE, 4, 8, None) == 1
     assert lib.gdn_verify_commit(geo, ctypes.c_void_p(0x10002), FAKE, FAKE, FAKE, 4, 8, None) == 3
     assert lib.gdn_verify_commit(geo, None, None, None, None, 0, 8, None) == 0
+    assert lib.gdn_verify_fp16_state(*args, 4, 18, FAKE, big, None) == 1
+    assert lib.gdn_verify_fp16_state(*args, 4, 8, FAKE, 4 * 8 * 53440 - 1, None) == 7
+    assert lib.gdn_verify_commit_fp16_state(geo, FAKE, FAKE, FAKE, ODD, 4, 8, None) == 3

@@ -7,11 +7,11 @@ import torch
 
 import oracle
 from linear_attention_ssm_gb300.synth import DECODE_BATCH, decode_inputs
-from tests.gpu_common import DEV, assert_out_close, assert_state_close, lib
+from tests.gpu_common import DEV, STATE_TOL_F16, assert_out_close, assert_state_close, lib
 
 pytestmark = pytest.mark.gpu
 A = dict(num_k_heads=16, num_v_heads=48, head_k_dim=128, head_v_dim=128)
-RECORD = 41344  # stash bytes per (sequence, row) at the 16 / 48 / 128 geometry
+RECORD = 53440  # stash bytes per (sequence, row) at the 16 / 48 / 128 geometry
 
 
 def _inputs(B, K, seed):
@@ -55,8 +55,8 @@ def test_verify_and_commit_match_oracle(B, K, committed):
 
 
 def test_commit_never_reads_rows_past_the_prefix():
-    """Stash records of rejected rows are poisoned (all bits set: NaN keys and gates); the commit
-    gives the same bits as from the clean stash."""
+    """Stash records of rejected rows are poisoned (all bits set: NaN keys, deltas and gates); the
+    commit gives the same bits as from the clean stash."""
     g = lib()
     B, K = 4, 8
     committed = [2, 8, 0, 5]
@@ -79,8 +79,9 @@ def test_commit_never_reads_rows_past_the_prefix():
 
 
 def test_verify_then_full_commit_equals_decode_steps():
-    """K one-token decode steps and a K-row verify committed in full agree to fp32 rounding (the
-    same per-element expressions; the dot products are summed in another order)."""
+    """K one-token decode steps and a K-row verify committed in full agree to fp32 rounding: the
+    same conv arithmetic (the same bf16 conv outputs) and the same recurrence, the verify's in
+    the WY form (another order of the same sums)."""
     g = lib()
     B, K = 3, 5
     d = _inputs(B, K, seed=61)
@@ -97,8 +98,10 @@ def test_verify_then_full_commit_equals_decode_steps():
     g.gdn_check_device_errors()
     dec = torch.stack(outs, 1)
     assert torch.equal(cs_v, cs)
-    assert (st_v - st).abs().max().item() <= 1e-5 * st.abs().max().item()
-    assert (out_v.float() - dec.float()).abs().max().item() <= 1e-2 * dec.float().abs().max().item()
+    for b in range(B):
+        assert_state_close(st_v[b], st[b].double(), f"state of sequence {b}", tol=1e-5)
+        for r in range(K):
+            assert_out_close(out_v[b, r], dec[b, r].double(), f"out of sequence {b}, row {r}")
 
 
 def test_commit_refuses_a_verdict_out_of_range():
@@ -139,3 +142,70 @@ def test_verify_256_sequences_8_rows_sampled():
     for i, b in enumerate(sample):
         assert_state_close(st[b], st_ref[i], f"state of sequence {b}")
     assert torch.equal(cs[sample].view(torch.int16), cs_ref.view(torch.int16))
+
+
+# ------------------------------------------------------------------ binary16 state
+
+def test_fp16_state_verify_and_commit_match_oracle():
+    g = lib()
+    B, K = 4, 6
+    committed = [0, 2, 6, 5]
+    d = _inputs(B, K, seed=64)
+    dd = _dev(d)
+    h0 = d["state0"].to(torch.float16)
+    st = h0.to(DEV)
+    cs = dd["conv_state0"].clone()
+    out, stash = _verify(g, dd, cs, st)
+    g.gdn_check_device_errors()
+    assert torch.equal(st.cpu().view(torch.int16), h0.view(torch.int16))  # the verify reads only
+    g.gdn_verify_commit(torch.tensor(committed, dtype=torch.int32, device=DEV), stash, cs, st, K)
+    g.gdn_check_device_errors()
+    ref, cs_ref, st_ref = oracle.verify_h16(d["x"], d["conv_w"], d["conv_state0"], d["g"], d["beta"], h0, d["z"],
+                                            d["norm_w"], committed, q_scale=d["q_scale"], **A)
+    out, st = out.cpu(), st.cpu()
+    for r in range(K):
+        assert_out_close(out[:, r], ref[:, r], f"out of row {r}")
+    assert torch.equal(st[0].view(torch.int16), h0[0].view(torch.int16))  # aborted: the bits stand
+    for b in range(1, B):
+        # the same values rounded once on both sides: at most one rounding apart, rarely, where the
+        # fp32 error of the terms (2^-20 of the state's scale bounds it) stays below the quantum
+        want = st_ref[b].double()
+        diff = (st[b].double() - want).abs()
+        _, ex = torch.frexp(want.abs())
+        quantum = torch.exp2(torch.clamp(ex - 11, min=-24).double())
+        bound = quantum + 2.0 ** -20 * want.abs().max()
+        bad = diff > bound
+        worst = int(torch.argmax(diff - bound))
+        assert not bad.any(), (f"sequence {b}: {int(bad.sum())} elements beyond one rounding; worst diff "
+                               f"{diff.flatten()[worst]:.3g} at value {want.flatten()[worst]:.4g} (quantum "
+                               f"{quantum.flatten()[worst]:.3g}); max diff {diff.max():.3g}, max |S| {want.abs().max():.3g}; "
+                               f"{int((diff > 0).sum())} of {diff.numel()} differ")
+        assert (diff > 0).double().mean().item() < 1e-2
+    assert torch.equal(cs.cpu().view(torch.int16), cs_ref.view(torch.int16))
+
+
+def test_fp16_state_verify_matches_decode_steps():
+    """A committed fp16-state verify against K fp16-state decode steps: they round the state at
+    different points (once, against after every row), so they agree within the binary16 chain
+    tolerance."""
+    g = lib()
+    B, K = 3, 5
+    d = _inputs(B, K, seed=65)
+    dd = _dev(d)
+    h0 = d["state0"].to(torch.float16).to(DEV)
+    cs, st = dd["conv_state0"].clone(), h0.clone()
+    outs = []
+    for r in range(K):
+        outs.append(g.gdn_decode_step_fp16_state(dd["x"][:, r].contiguous(), dd["conv_w"], cs,
+                                                 dd["g"][:, r].contiguous(), dd["beta"][:, r].contiguous(), st,
+                                                 dd["z"][:, r].contiguous(), dd["norm_w"], dd["q_scale"]))
+    cs_v, st_v = dd["conv_state0"].clone(), h0.clone()
+    out_v, stash = _verify(g, dd, cs_v, st_v)
+    g.gdn_verify_commit(torch.full((B,), K, dtype=torch.int32, device=DEV), stash, cs_v, st_v, K)
+    g.gdn_check_device_errors()
+    dec = torch.stack(outs, 1)
+    assert torch.equal(cs_v, cs)
+    for b in range(B):
+        assert_state_close(st_v[b].double(), st[b].double(), f"state of sequence {b}", tol=STATE_TOL_F16)
+        for r in range(K):
+            assert_out_close(out_v[b, r], dec[b, r].double(), f"out of sequence {b}, row {r}")

@@ -538,3 +538,25 @@ def test_verify_refuses_committed_rows_out_of_range():
         with pytest.raises(ValueError):
             oracle.verify(v["x"], v["conv_w"], v["conv_state0"], v["g"], v["beta"], v["state0"], v["z"],
                           v["norm_w"], bad, **a)
+
+
+def test_verify_h16_rounds_only_the_committed_state():
+    """The binary16-state verify: outputs equal the fp64 verify's from the widened state; a
+    committed state is numpy's binary16 rounding of the fp64 committed state; an abort keeps the
+    bits."""
+    geo = SMALL
+    B, K = 3, 4
+    v = _verify_inputs(B, K, seed=43, geo=geo)
+    a = dict(num_k_heads=geo.num_k_heads, num_v_heads=geo.num_v_heads, head_k_dim=geo.head_k_dim,
+             head_v_dim=geo.head_v_dim, q_scale=0.3)
+    h = v["state0"].to(torch.float16)
+    m = [0, 2, 4]
+    out16, cs16, st16 = oracle.verify_h16(v["x"], v["conv_w"], v["conv_state0"], v["g"], v["beta"], h, v["z"],
+                                          v["norm_w"], m, **a)
+    out64, cs64, st64 = oracle.verify(v["x"], v["conv_w"], v["conv_state0"], v["g"], v["beta"], h.double(), v["z"],
+                                      v["norm_w"], m, **a)
+    assert torch.equal(out16, out64) and torch.equal(cs16.view(torch.int16), cs64.view(torch.int16))
+    assert torch.equal(st16[0].view(torch.int16), h[0].view(torch.int16))
+    for b in (1, 2):
+        want = _f16_bits_numpy(st64[b].numpy())
+        assert np.array_equal(st16[b].view(torch.int16).numpy().view(np.uint16), want)

@@ -33,15 +33,6 @@ constexpr int kMaxRatio = 12;                             // V heads per K head 
 constexpr uint32_t kStateWaitLimit = 1u << 20;            // polls of the state-slice barrier
 constexpr size_t kMaxStagedBytes = 96 * 1024;             // largest state slice staged in shared memory
 
-__device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
 // Four consecutive state elements of a row (index i counts groups of four), widened to fp32.  The
 // fp16 storage form holds the state as IEEE binary16 in memory only: it is widened on load, the
 // step runs in fp32 exactly as for the fp32 state, and the new state is rounded once (to nearest,
@@ -99,53 +90,37 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     }
   }
 
-  // ---- conv step + SiLU for the CTA's 32 + 16R channel octets
-  const int n_oct = 32 + 16 * R;
-  if (tid < n_oct) {
+  // ---- conv step + SiLU for the CTA's 256 + 128R channels, one channel pair per thread and round
+  const int n_pairs = (2 + R) * (kHeadDim / 2);
+  for (int t = tid; t < n_pairs; t += kThreads) {
     int c;
     float* dst;
-    if (tid < 16) { c = j * kHeadDim + tid * 8; dst = s_q + tid * 8; }
-    else if (tid < 32) { c = Hk * kHeadDim + j * kHeadDim + (tid - 16) * 8; dst = s_k + (tid - 16) * 8; }
+    if (t < 64) { c = j * kHeadDim + 2 * t; dst = s_q + 2 * t; }
+    else if (t < 128) { c = Hk * kHeadDim + j * kHeadDim + 2 * (t - 64); dst = s_k + 2 * (t - 64); }
     else {
-      const int hh = (tid - 32) >> 4, o = (tid - 32) & 15;
-      c = 2 * Hk * kHeadDim + (j * R + hh) * kHeadDim + o * 8;
-      dst = s_v[hh] + o * 8;
+      const int hh = (t - 128) >> 6, o = (t - 128) & 63;
+      c = 2 * Hk * kHeadDim + (j * R + hh) * kHeadDim + 2 * o;
+      dst = s_v[hh] + 2 * o;
     }
-    float xv[8], wv[32], st[24];
-    unpack8(__ldg(reinterpret_cast<const uint4*>(x + (size_t)b * C + c)), xv);
-    const uint4* wp = reinterpret_cast<const uint4*>(conv_w + (size_t)c * kConvWidth);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float t8[8];
-      unpack8(__ldg(wp + i), t8);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) wv[i * 8 + e] = t8[e];
-    }
-    uint4* sp = reinterpret_cast<uint4*>(conv_state + ((size_t)b * C + c) * (kConvWidth - 1));
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      float t8[8];
-      unpack8(sp[i], t8);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) st[i * 8 + e] = t8[e];
-    }
-    // channel ch: weights wv[ch*4 + 0..3], state st[ch*3 + 0..2] (oldest first)
-    float ns[24];
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      // the bf16 conv output, rounded as the exact value is
-      dst[ch] = bf2f(silu_bf16_rn(wv[ch * 4 + 0], st[ch * 3 + 0], wv[ch * 4 + 1], st[ch * 3 + 1], wv[ch * 4 + 2],
-                                  st[ch * 3 + 2], wv[ch * 4 + 3], xv[ch]));
-      ns[ch * 3 + 0] = st[ch * 3 + 1];
-      ns[ch * 3 + 1] = st[ch * 3 + 2];
-      ns[ch * 3 + 2] = xv[ch];
-    }
-    uint32_t pk[12];
-#pragma unroll
-    for (int i = 0; i < 12; ++i) pk[i] = pack_bf2(ns[2 * i], ns[2 * i + 1]);  // exact (bf16 inputs)
-    sp[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    sp[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-    sp[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+    const uint32_t xu = __ldg(reinterpret_cast<const uint32_t*>(x + (size_t)b * C + c));
+    const uint4 wu = __ldg(reinterpret_cast<const uint4*>(conv_w + (size_t)c * kConvWidth));  // [2][4] taps
+    // conv state of channels c, c + 1: [2][3] bf16 in three 32-bit words, oldest slot first
+    uint32_t* sp = reinterpret_cast<uint32_t*>(conv_state + ((size_t)b * C + c) * (kConvWidth - 1));
+    const uint32_t s0 = sp[0], s1 = sp[1], s2 = sp[2];
+    const float xa = __uint_as_float(xu << 16), xb = __uint_as_float(xu & 0xFFFF0000u);
+    const float wa[4] = {__uint_as_float(wu.x << 16), __uint_as_float(wu.x & 0xFFFF0000u),
+                         __uint_as_float(wu.y << 16), __uint_as_float(wu.y & 0xFFFF0000u)};
+    const float wb[4] = {__uint_as_float(wu.z << 16), __uint_as_float(wu.z & 0xFFFF0000u),
+                         __uint_as_float(wu.w << 16), __uint_as_float(wu.w & 0xFFFF0000u)};
+    const float sa[3] = {__uint_as_float(s0 << 16), __uint_as_float(s0 & 0xFFFF0000u), __uint_as_float(s1 << 16)};
+    const float sb[3] = {__uint_as_float(s1 & 0xFFFF0000u), __uint_as_float(s2 << 16), __uint_as_float(s2 & 0xFFFF0000u)};
+    // the bf16 conv outputs, rounded as the exact values are
+    dst[0] = bf2f(silu_bf16_rn(wa[0], sa[0], wa[1], sa[1], wa[2], sa[2], wa[3], xa));
+    dst[1] = bf2f(silu_bf16_rn(wb[0], sb[0], wb[1], sb[1], wb[2], sb[2], wb[3], xb));
+    // the shift register: [s1, s2, x] per channel (exact: bf16 values)
+    sp[0] = pack_bf2(sa[1], sa[2]);
+    sp[1] = pack_bf2(xa, sb[1]);
+    sp[2] = pack_bf2(sb[2], xb);
   }
   __syncthreads();
 

@@ -47,6 +47,12 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 // from it errs by a few ulps (more for large negative sums, where exp amplifies the argument's
 // rounding); where the estimate lies that close to a bf16 rounding midpoint, the SiLU is
 // recomputed in fp64 from the exact sum before rounding.
+// the rare fp64 re-evaluation, out of line so that the fp32 path stays compact
+static __device__ __noinline__ uint16_t silu_bf16_fp64(float s, float e1, float e2, float e3) {
+  const double ad = (double)s + (double)e1 + (double)e2 + (double)e3;
+  return __bfloat16_as_ushort(__double2bfloat16(ad / (1.0 + exp(-ad))));
+}
+
 __device__ __forceinline__ uint16_t silu_bf16_rn(float w0, float x0, float w1, float x1, float w2, float x2,
                                                  float w3, float x3) {
   float s, e1, e2, e3;
@@ -57,10 +63,7 @@ __device__ __forceinline__ uint16_t silu_bf16_rn(float w0, float x0, float w1, f
   const float y = acc / (1.0f + expf(-acc));
   const int off = (int)(__float_as_uint(y) & 0xFFFFu) - 0x8000;  // fp32 ulps from the midpoint
   const int margin = 32 + (int)fminf(2.f * fabsf(acc), 4096.f);
-  if (off >= -margin && off <= margin) {
-    const double ad = (double)s + (double)e1 + (double)e2 + (double)e3;
-    return __bfloat16_as_ushort(__double2bfloat16(ad / (1.0 + exp(-ad))));
-  }
+  if (off >= -margin && off <= margin) return silu_bf16_fp64(s, e1, e2, e3);
   return f2bf(y);
 }
 

@@ -209,3 +209,31 @@ def test_fp16_state_verify_matches_decode_steps():
         assert_state_close(st_v[b].double(), st[b].double(), f"state of sequence {b}", tol=STATE_TOL_F16)
         for r in range(K):
             assert_out_close(out_v[b, r], dec[b, r].double(), f"out of sequence {b}, row {r}")
+
+
+@pytest.mark.parametrize("hk,hv", [(4, 4), (2, 8)], ids=["ratio1", "ratio4"])
+def test_verify_other_head_ratios(hk, hv):
+    """V heads per K head 1 and 4 (the CTA owns 1 or 4 V heads' channels and state slices)."""
+    from linear_attention_ssm_gb300.synth import Geometry
+    g = lib()
+    geo = Geometry(num_k_heads=hk, num_v_heads=hv)
+    B, K = 3, 7
+    committed = [7, 0, 3]
+    d = decode_inputs(B, K, seed=66, geo=geo)
+    for k in ("x", "g", "beta", "z"):
+        d[k] = d[k].transpose(0, 1).contiguous()
+    dd = _dev(d)
+    cs, st = dd["conv_state0"].clone(), dd["state0"].clone()
+    out, stash = g.gdn_verify(dd["x"], dd["conv_w"], cs, dd["g"], dd["beta"], st, dd["z"], dd["norm_w"],
+                              dd["q_scale"], geometry=geo)
+    g.gdn_verify_commit(torch.tensor(committed, dtype=torch.int32, device=DEV), stash, cs, st, K, geometry=geo)
+    g.gdn_check_device_errors()
+    a = dict(num_k_heads=hk, num_v_heads=hv, head_k_dim=128, head_v_dim=128)
+    ref, cs_ref, st_ref = oracle.verify(d["x"], d["conv_w"], d["conv_state0"], d["g"], d["beta"], d["state0"],
+                                        d["z"], d["norm_w"], committed, q_scale=d["q_scale"], **a)
+    out = out.cpu()
+    for r in range(K):
+        assert_out_close(out[:, r], ref[:, r], f"out of row {r}")
+    for b in range(B):
+        assert_state_close(st[b], st_ref[b], f"state of sequence {b}")
+    assert torch.equal(cs.cpu().view(torch.int16), cs_ref.view(torch.int16))

@@ -15,8 +15,8 @@
 // the Hv/Hk V heads that read it, so no two CTAs touch the same conv-state channel and the
 // in-place conv-state update is race-free.  Each warp streams 16 rows ([value] index) of a
 // head's 128 x 128 state: a row is 32 lanes x float4 over the key dimension, so both
-// contractions (S k and S q) are warp-shuffle reductions and every state byte is read once and
-// written once.
+// contractions (S k and S q) are warp-shuffle reductions (a halving butterfly: 16 shuffles for
+// the 16 rows' sums) and every state byte is read once and written once.
 #include <cuda_fp16.h>
 #include <string.h>
 
@@ -53,6 +53,26 @@ __device__ __forceinline__ void store_state4(__half* S, int i, const float4 v) {
   memcpy(&u.x, &a, 4);
   memcpy(&u.y, &b, 4);
   reinterpret_cast<uint2*>(S)[i] = u;
+}
+
+// Sums v[0..15] over the 32 lanes of a warp in 16 shuffles (a halving butterfly: at each of the
+// five levels a lane keeps half of its values and adds its partner's copy of that half).  Every
+// total is formed by the same pairwise additions as five xor-shuffle levels applied to each value
+// on its own, so it has the same bits.  Lanes 2i and 2i + 1 return the total of v[i].
+__device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
+  float a[8], b4[4], c2[2];
+  const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    a[k] = (h16 ? v[8 + k] : v[k]) + __shfl_xor_sync(0xffffffffu, h16 ? v[k] : v[8 + k], 16);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    b4[k] = (h8 ? a[4 + k] : a[k]) + __shfl_xor_sync(0xffffffffu, h8 ? a[k] : a[4 + k], 8);
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+    c2[k] = (h4 ? b4[2 + k] : b4[k]) + __shfl_xor_sync(0xffffffffu, h4 ? b4[k] : b4[2 + k], 4);
+  const float s = (h2 ? c2[1] : c2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? c2[0] : c2[1], 2);
+  return s + __shfl_xor_sync(0xffffffffu, s, 1);
 }
 
 // kStaged: the CTA's whole state slice (its R V heads, contiguous in [B, Hv, Dv, Dk]) is fetched
@@ -168,15 +188,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i)
       d[i] = row[i].x * kn.x + row[i].y * kn.y + row[i].z * kn.z + row[i].w * kn.w;
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1)
-#pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i) d[i] += __shfl_xor_sync(0xffffffffu, d[i], m);
+    // lanes 2i and 2i + 1 hold row i's sum; its delta (against the decayed state) is formed there
+    // and broadcast
+    const int i_mine = (lane >> 1) & 15;
+    const float e_mine =
+        bt * (s_v[hh][warp * kRowsPerWarp + i_mine] - alpha * warp_sum16(d, lane));
     float o[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
-      const int r = warp * kRowsPerWarp + i;
-      const float e = bt * (s_v[hh][r] - alpha * d[i]);  // delta against the decayed state
+      const float e = __shfl_sync(0xffffffffu, e_mine, 2 * i);
       float4 sn;
       sn.x = fmaf(alpha, row[i].x, e * kn.x);
       sn.y = fmaf(alpha, row[i].y, e * kn.y);
@@ -185,14 +205,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
       store_state4(S, i * 32 + lane, sn);
       o[i] = sn.x * qn.x + sn.y * qn.y + sn.z * qn.z + sn.w * qn.w;
     }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1)
-#pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i) o[i] += __shfl_xor_sync(0xffffffffu, o[i], m);
-    if (lane == 0) {
-#pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i) s_o[hh][warp * kRowsPerWarp + i] = q_scale * o[i];
-    }
+    const float o_mine = warp_sum16(o, lane);
+    if (!(lane & 1)) s_o[hh][warp * kRowsPerWarp + i_mine] = q_scale * o_mine;
   }
   __syncthreads();
 

@@ -321,3 +321,27 @@ def test_concurrent_calls_on_two_streams():
         assert_out_close(out, ref["out"])
         for n in range(3):
             assert_state_close(st[n], ref["state"][n], f"state of sequence {n}")
+
+
+def test_all_sequences_empty(mode):
+    """Three sequences of zero tokens (total_tokens 0): the recurrent state and the conv state pass
+    through bit for bit, in every chunk mode, with no device error."""
+    g = lib()
+    N, C = 3, GEO.conv_dim
+    gen = torch.Generator().manual_seed(70)
+    st_in = (0.1 * torch.randn((N, 48, 128, 128), generator=gen)).to(DEV)
+    cs_in = torch.randn((N, C, 3), generator=gen).to(torch.bfloat16).to(DEV)
+    cu = torch.zeros(N + 1, dtype=torch.int32, device=DEV)
+    st_out = torch.full_like(st_in, float("nan"))
+    cs_out = torch.full_like(cs_in, float("nan"))
+    qkv = g.gdn_conv1d_prefill(torch.empty((0, C), dtype=torch.bfloat16, device=DEV),
+                               (0.5 * torch.randn((C, 4), generator=gen)).to(torch.bfloat16).to(DEV), cu, cs_in,
+                               cs_out)
+    out = g.gdn_chunk_prefill(qkv, torch.empty((0, 48), device=DEV), torch.empty((0, 48), device=DEV), cu,
+                              GEO.q_scale, 1e-6, st_in, st_out, torch.empty((0, 48, 128), dtype=torch.bfloat16,
+                                                                             device=DEV),
+                              torch.ones(128, dtype=torch.bfloat16, device=DEV), 1e-6)
+    g.gdn_check_device_errors()
+    assert out.shape[0] == 0
+    assert torch.equal(st_out, st_in)
+    assert torch.equal(cs_out.view(torch.int16), cs_in.view(torch.int16))

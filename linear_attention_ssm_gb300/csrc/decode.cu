@@ -197,11 +197,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
       const float e = __shfl_sync(0xffffffffu, e_mine, 2 * i);
-      float4 sn;
-      sn.x = fmaf(alpha, row[i].x, e * kn.x);
-      sn.y = fmaf(alpha, row[i].y, e * kn.y);
-      sn.z = fmaf(alpha, row[i].z, e * kn.z);
-      sn.w = fmaf(alpha, row[i].w, e * kn.w);
+      // S <- alpha S + e k^T, element by element fma(alpha, s, e k) in f32x2 pairs
+      const float2 a2 = make_float2(alpha, alpha), e2 = make_float2(e, e);
+      const float2 xy = __ffma2_rn(a2, make_float2(row[i].x, row[i].y), __fmul2_rn(e2, make_float2(kn.x, kn.y)));
+      const float2 zw = __ffma2_rn(a2, make_float2(row[i].z, row[i].w), __fmul2_rn(e2, make_float2(kn.z, kn.w)));
+      const float4 sn = make_float4(xy.x, xy.y, zw.x, zw.y);
       store_state4(S, i * 32 + lane, sn);
       o[i] = sn.x * qn.x + sn.y * qn.y + sn.z * qn.z + sn.w * qn.w;
     }

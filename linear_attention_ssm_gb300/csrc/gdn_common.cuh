@@ -34,38 +34,6 @@ __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf
 
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(x) = 2^(x log2 e)
 
-// a + b = s + e exactly (Knuth's two-sum; rounded-to-nearest operations that nothing may fuse)
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
-
-// SiLU of the width-4 conv tap sum w0 x0 + w1 x1 + w2 x2 + w3 x3 (bf16 weights and inputs held as
-// floats), rounded to the bf16 nearest the exact value.  Every bf16 x bf16 product is exact in
-// fp32 and the sum is carried exactly as s + e1 + e2 + e3 (two-sums), so the fp32 SiLU estimate
-// from it errs by a few ulps (more for large negative sums, where exp amplifies the argument's
-// rounding); where the estimate lies that close to a bf16 rounding midpoint, the SiLU is
-// recomputed in fp64 from the exact sum before rounding.
-// the rare fp64 re-evaluation, out of line so that the fp32 path stays compact
-static __device__ __noinline__ uint16_t silu_bf16_fp64(float s, float e1, float e2, float e3) {
-  const double ad = (double)s + (double)e1 + (double)e2 + (double)e3;
-  return __bfloat16_as_ushort(__double2bfloat16(ad / (1.0 + exp(-ad))));
-}
-
-__device__ __forceinline__ uint16_t silu_bf16_rn(float w0, float x0, float w1, float x1, float w2, float x2,
-                                                 float w3, float x3) {
-  float s, e1, e2, e3;
-  two_sum(__fmul_rn(w0, x0), __fmul_rn(w1, x1), s, e1);
-  two_sum(s, __fmul_rn(w2, x2), s, e2);
-  two_sum(s, __fmul_rn(w3, x3), s, e3);
-  const float acc = __fadd_rn(s, __fadd_rn(__fadd_rn(e1, e2), e3));
-  const float y = acc / (1.0f + expf(-acc));
-  const int off = (int)(__float_as_uint(y) & 0xFFFFu) - 0x8000;  // fp32 ulps from the midpoint
-  const int margin = 32 + (int)fminf(2.f * fabsf(acc), 4096.f);
-  if (off >= -margin && off <= margin) return silu_bf16_fp64(s, e1, e2, e3);
-  return f2bf(y);
-}
 
 // 2^x by the hardware approximation instruction (relative error ~2^-22; results below the
 // smallest normal flush to zero).
@@ -87,6 +55,40 @@ __device__ __forceinline__ float rcp_approx(float x) {
 }
 // sigmoid(x) = 1 / (1 + e^-x) from the two approximations above (output-side gate only)
 __device__ __forceinline__ float sigmoid_fast(float x) { return rcp_approx(1.0f + ex2_approx(-x * kLog2e)); }
+
+// a + b = s + e exactly (Knuth's two-sum; rounded-to-nearest operations that nothing may fuse)
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// SiLU of the width-4 conv tap sum w0 x0 + w1 x1 + w2 x2 + w3 x3 (bf16 weights and inputs held as
+// floats), rounded to the bf16 nearest the exact value.  Every bf16 x bf16 product is exact in
+// fp32 and the sum is carried exactly as s + e1 + e2 + e3 (two-sums), so the fp32 SiLU estimate
+// from it (hardware exp2 and reciprocal) errs by a few ulps (more for large negative sums, where
+// exp amplifies the argument's rounding); where the estimate lies within 32 + 2 |acc| ulps of a
+// bf16 rounding midpoint, the SiLU is recomputed in fp64 from the exact sum before rounding.
+// the rare fp64 re-evaluation, out of line so that the fp32 path stays compact
+static __device__ __noinline__ uint16_t silu_bf16_fp64(float s, float e1, float e2, float e3) {
+  const double ad = (double)s + (double)e1 + (double)e2 + (double)e3;
+  return __bfloat16_as_ushort(__double2bfloat16(ad / (1.0 + exp(-ad))));
+}
+
+__device__ __forceinline__ uint16_t silu_bf16_rn(float w0, float x0, float w1, float x1, float w2, float x2,
+                                                 float w3, float x3) {
+  float s, e1, e2, e3;
+  two_sum(__fmul_rn(w0, x0), __fmul_rn(w1, x1), s, e1);
+  two_sum(s, __fmul_rn(w2, x2), s, e2);
+  two_sum(s, __fmul_rn(w3, x3), s, e3);
+  const float acc = __fadd_rn(s, __fadd_rn(__fadd_rn(e1, e2), e3));
+  // the estimate: acc / (1 + 2^(-acc log2 e)) with the hardware exp2 and reciprocal (a few ulps)
+  const float y = acc * rcp_approx(1.0f + ex2_approx(-acc * kLog2e));
+  const int off = (int)(__float_as_uint(y) & 0xFFFFu) - 0x8000;  // fp32 ulps from the midpoint
+  const int margin = 32 + (int)fminf(2.f * fabsf(acc), 4096.f);
+  if (off >= -margin && off <= margin) return silu_bf16_fp64(s, e1, e2, e3);
+  return f2bf(y);
+}
 // hardware tanh approximation (max relative error about 2^-11)
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;

@@ -237,3 +237,25 @@ def test_verify_other_head_ratios(hk, hv):
     for b in range(B):
         assert_state_close(st[b], st_ref[b], f"state of sequence {b}")
     assert torch.equal(cs.cpu().view(torch.int16), cs_ref.view(torch.int16))
+
+
+def test_fp16_state_verify_17_rows():
+    """The longest verify (17 rows, the 48-column row bucket) with a binary16 state."""
+    g = lib()
+    B, K = 2, 17
+    committed = [17, 11]
+    d = _inputs(B, K, seed=67)
+    dd = _dev(d)
+    h0 = d["state0"].to(torch.float16)
+    st, cs = h0.to(DEV), dd["conv_state0"].clone()
+    out, stash = _verify(g, dd, cs, st)
+    g.gdn_verify_commit(torch.tensor(committed, dtype=torch.int32, device=DEV), stash, cs, st, K)
+    g.gdn_check_device_errors()
+    ref, cs_ref, st_ref = oracle.verify_h16(d["x"], d["conv_w"], d["conv_state0"], d["g"], d["beta"], h0, d["z"],
+                                            d["norm_w"], committed, q_scale=d["q_scale"], **A)
+    out = out.cpu()
+    for r in range(K):
+        assert_out_close(out[:, r], ref[:, r], f"out of row {r}")
+    for b in range(B):
+        assert_state_close(st[b].cpu().double(), st_ref[b].double(), f"state of sequence {b}", tol=STATE_TOL_F16)
+    assert torch.equal(cs.cpu().view(torch.int16), cs_ref.view(torch.int16))

@@ -76,6 +76,8 @@ def _load():
             lib.oracle_decode_step_h16.argtypes = [
                 I, I, I, I, I, I, P, P, P, P, P, P, P, P, D, D, D, P, P, I, I]
             lib.oracle_decode_step_h16.restype = I
+            lib.oracle_gates.argtypes = [ctypes.c_long, I, P, P, P, P, P, P]
+            lib.oracle_gates.restype = I
             _lib = lib
     return _lib
 
@@ -128,6 +130,22 @@ def f16_to_double(h: torch.Tensor) -> torch.Tensor:
     bits = h.detach().cpu().contiguous().view(torch.int16).reshape(-1).numpy().view(np.uint16)
     vals = [lib.oracle_f16_to_double(int(b)) for b in bits]
     return torch.tensor(vals, dtype=torch.float64).reshape(h.shape)
+
+
+def gates(a, b, A_log, dt_bias):
+    """g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b) per (token, V head); float64.
+
+    Parity unpinned against the pages (they give no formula); the published Gated DeltaNet /
+    Mamba-2 gate is the reading taken.  a, b: bf16 [T, Hv]; A_log, dt_bias: fp32 [Hv].
+    """
+    lib = _load()
+    T, hv = a.shape
+    ab, bb = _bf16_bits(a), _bf16_bits(b)
+    al, db = _f32(A_log), _f32(dt_bias)
+    g = torch.empty((T, hv), dtype=torch.float64)
+    beta = torch.empty((T, hv), dtype=torch.float64)
+    lib.oracle_gates(T, hv, _ptr(ab), _ptr(bb), _ptr(al), _ptr(db), _ptr(g), _ptr(beta))
+    return g, beta
 
 
 def conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in=None, mutation: int = 0):

@@ -33,6 +33,8 @@
  *   6. the same decode step with the recurrent state stored as IEEE binary16: widened on load,
  *      the step in double, rounded once (ties to even) on store -- the same ledger, the FP16
  *      h-state twins of the decode kernels.
+ *   7. the gates g and beta from the a / b projections, A_log and dt_bias (parity unpinned: the
+ *      pages give no formula; the published Gated DeltaNet / Mamba-2 gate is taken).
  *
  * Mutations (negative controls) can be planted here, on the CPU, through the `mutation`
  * bit set; 0 is the method.  See ORACLE_MUT_* below.
@@ -434,4 +436,28 @@ int oracle_decode_step_h16(int hk, int hv, int dk, int dv, int W, int B, const u
     for (size_t i = 0; i < n; ++i) state_h[i] = oracle_round_f16(st[i]);
   free(st);
   return rc;
+}
+
+/* ---------------------------------------------------------------- 7. gate derivation */
+
+/*
+ * The per-token gates from their projections (PARITY UNPINNED: the pages name the inputs -- the
+ * a / b projections, A_log and dt_bias, Qwen3.8 kernel architecture and TDD ledger, "GDN
+ * alpha/beta transforms"; PR #1152 Summary -- but give no formula).  The reading taken is the
+ * gate of the published Gated DeltaNet / Mamba-2 layers:
+ *   g[t,h]    = -exp(A_log[h]) * softplus(a[t,h] + dt_bias[h]),   softplus(x) = log(1 + e^x)
+ *   beta[t,h] = sigmoid(b[t,h]) = 1 / (1 + e^-b)
+ * a, b: [rows, hv] bf16;  A_log, dt_bias: [hv] fp32;  g, beta: [rows, hv] double.
+ */
+int oracle_gates(long rows, int hv, const uint16_t* a, const uint16_t* b, const float* A_log,
+                 const float* dt_bias, double* g, double* beta) {
+  for (long t = 0; t < rows; ++t)
+    for (int h = 0; h < hv; ++h) {
+      const size_t i = (size_t)t * hv + h;
+      const double x = bf16_to_double(a[i]) + (double)dt_bias[h];
+      const double sp = x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); /* log(1 + e^x), no overflow */
+      g[i] = -exp((double)A_log[h]) * sp;
+      beta[i] = sigmoid(bf16_to_double(b[i]));
+    }
+  return 0;
 }

@@ -560,3 +560,41 @@ def test_verify_h16_rounds_only_the_committed_state():
     for b in (1, 2):
         want = _f16_bits_numpy(st64[b].numpy())
         assert np.array_equal(st16[b].view(torch.int16).numpy().view(np.uint16), want)
+
+
+# ------------------------------------------------------------------ gate derivation (parity unpinned)
+
+def test_gates_match_torch_softplus_and_sigmoid():
+    """The gates against torch's own softplus and sigmoid in fp64 (library routines)."""
+    gen = torch.Generator().manual_seed(44)
+    T, hv = 37, 6
+    a = (3 * torch.randn((T, hv), generator=gen)).to(torch.bfloat16)
+    b = (3 * torch.randn((T, hv), generator=gen)).to(torch.bfloat16)
+    A_log = torch.rand(hv, generator=gen) * 3 - 1
+    dt_bias = torch.randn(hv, generator=gen)
+    g, beta = oracle.gates(a, b, A_log, dt_bias)
+    want_g = -torch.exp(A_log.double()) * F.softplus(a.double() + dt_bias.double(), threshold=1e9)
+    assert torch.allclose(g, want_g, rtol=1e-13, atol=0)
+    assert torch.allclose(beta, torch.sigmoid(b.double()), rtol=1e-14, atol=0)
+
+
+def test_gates_closed_forms():
+    """a = -dt_bias gives g = -exp(A_log) ln 2; b = 0 gives beta = 1/2; beta(-b) = 1 - beta(b);
+    g < 0 and g -> 0 as a -> -inf; large arguments do not overflow."""
+    hv = 3
+    A_log = torch.tensor([0.0, 1.0, -2.0])
+    dt_bias = torch.tensor([0.5, -1.0, 2.0])
+    a = (-dt_bias).to(torch.bfloat16).reshape(1, hv)   # exact in bf16
+    b = torch.zeros((1, hv), dtype=torch.bfloat16)
+    g, beta = oracle.gates(a, b, A_log, dt_bias)
+    assert torch.allclose(g[0], -torch.exp(A_log.double()) * math.log(2.0), rtol=1e-15, atol=0)
+    assert torch.equal(beta, torch.full((1, hv), 0.5, dtype=torch.float64))
+    bb = torch.tensor([[1.5, -1.5, 7.0]]).to(torch.bfloat16)
+    _, b1 = oracle.gates(a, bb, A_log, dt_bias)
+    _, b2 = oracle.gates(a, (-bb.float()).to(torch.bfloat16), A_log, dt_bias)
+    assert torch.allclose(b1 + b2, torch.ones_like(b1), rtol=0, atol=1e-15)
+    far = torch.tensor([[-80.0, 80.0, 800.0]]).to(torch.bfloat16)
+    g2, _ = oracle.gates(far, b, A_log, torch.zeros(hv))
+    assert torch.isfinite(g2).all() and (g2 < 0).all()
+    assert abs(g2[0, 0].item()) < 1e-30                       # softplus(-80) ~ e^-80
+    assert abs(g2[0, 2].item() + math.exp(-2.0) * 800.0) < 1e-9  # softplus(x) -> x

@@ -564,6 +564,31 @@ def run_ours(args, rank, world, local):
     del d, dx, dg, db, dz
     torch.cuda.empty_cache()
 
+    # ---------------- gates from their projections for the 4 x 4096 tokens (elementwise, HBM)
+    from linear_attention_ssm_gb300.synth import gate_inputs
+    gi = gate_inputs(T, seed=6)
+    ga, gb_, gal, gdb = (gi[k].to(dev) for k in ("a", "b", "A_log", "dt_bias"))
+    g_out = torch.empty((T, 48), dtype=torch.float32, device=dev)
+    b_out = torch.empty((T, 48), dtype=torch.float32, device=dev)
+    for _ in range(max(args.warmup, 1)):
+        gdn.gdn_gates(ga, gb_, gal, gdb, g_out, b_out)
+    barrier()
+    s5, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ng = 50
+    s5.record(stream)
+    for _ in range(ng):
+        gdn.gdn_gates(ga, gb_, gal, gdb, g_out, b_out)
+    e5.record(stream)
+    torch.cuda.synchronize()
+    gdn.gdn_check_device_errors()
+    g_ms = max_over_ranks(s5.elapsed_time(e5)) / ng
+    g_bytes = T * 48 * (2 + 2 + 4 + 4)
+    gates = {"workload": "gates g, beta from the a / b projections, 16,384 tokens x 48 V heads",
+             "ms_per_launch": g_ms, "achieved_gbs": g_bytes / (g_ms / 1e3) / 1e9,
+             "algorithmic_bytes_per_launch": g_bytes, "launches": ng,
+             "note": "9.4 MB per launch: launch latency, not HBM, sets its time"}
+    del ga, gb_, gal, gdb, g_out, b_out
+
     # ---------------- multi-token verify: 256 sequences x 8 rows, then the commit of a verdict
     verify = time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak)
     verify_f16 = time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak, torch.float16)
@@ -587,6 +612,7 @@ def run_ours(args, rank, world, local):
                     "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                     "pipelined": "H2D of step i+1 and D2H of step i-1 overlap the prefill of step i"},
             "decode": decode, "decode_fp16_state": decode_f16, "verify": verify, "verify_fp16_state": verify_f16,
+            "gates": gates,
             "varlen": varlen, "cpu_baseline": cpu, "clocks": clk,
             # per step: conv1d + conv-state kernels, the chunk prefill's schedule and segment-table
             # kernels, then a prep and a state kernel for each of its three chunk segments

@@ -162,6 +162,23 @@ GDN_API gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qk
                                      void* stream);
 
 /*
+ * The gates of the recurrence from their projections, for every row (token, or sequence of a
+ * decode step) and V head:
+ *   g[r, h]    = -exp(A_log[h]) * softplus(a[r, h] + dt_bias[h]),   softplus(x) = log(1 + e^x)
+ *   beta[r, h] = sigmoid(b[r, h])
+ * The pages name these inputs (Qwen3.8 kernel architecture and TDD ledger, "GDN alpha/beta
+ * transforms"; PR #1152 Summary: A_log, dt_bias, the a / b projections, and a fixture that holds
+ * g / beta only after this derivation) but give no formula: this is the gate of the published
+ * Gated DeltaNet / Mamba-2 layers.
+ *   a, b        [rows, Hv] bf16 projection outputs
+ *   A_log, dt_bias  [Hv] fp32 (4-byte aligned)
+ *   g, beta     [rows, Hv] fp32 outputs, ready for gdn_chunk_prefill / gdn_decode_step
+ */
+GDN_API gdn_status gdn_gates(const gdn_geometry* geo, const gdn_bf16* a, const gdn_bf16* b,
+                             const float* A_log, const float* dt_bias, float* g, float* beta,
+                             int32_t rows, void* stream);
+
+/*
  * Sigmoid-gated RMSNorm, one row per (token, V head).  pegainfer PR #1152, Summary
  * (output_gate_type "sigmoid"; the in-tree kernel that hard-codes silu is wrong) and Code
  * review (rms_norm_eps == 1e-6).

@@ -19,6 +19,7 @@ from .binding import (  # noqa: F401
     gdn_decode_step,
     gdn_decode_step_fp16_state,
     gdn_gated_rmsnorm,
+    gdn_gates,
     gdn_prefill,
     gdn_verify,
     gdn_verify_commit,

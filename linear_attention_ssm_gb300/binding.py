@@ -60,6 +60,7 @@ def load_library():
             "gdn_gated_rmsnorm": ([G, P, P, P, F, P, I, P], ctypes.c_int),
             "gdn_decode_step": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
             "gdn_decode_step_fp16_state": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
+            "gdn_gates": ([G, P, P, P, P, P, P, I, P], ctypes.c_int),
             "gdn_verify_stash_size": ([G, I, I], S),
             "gdn_verify": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, I, P, S, P], ctypes.c_int),
             "gdn_verify_commit": ([G, P, P, P, P, I, I, P], ctypes.c_int),
@@ -236,6 +237,29 @@ def gdn_decode_step_fp16_state(x, conv_w, conv_state, g, beta, state, z, norm_w,
         raise TypeError(f"state must be torch.float16, got {state.dtype}")
     return gdn_decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps, rms_eps, out,
                            geometry, stream)
+
+
+def gdn_gates(a, b, A_log, dt_bias, g=None, beta=None, geometry: Geometry = QWEN_GDN, stream=None):
+    """g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b) for every row and V head.
+
+    a, b: [rows, Hv] bf16; A_log, dt_bias: [Hv] fp32.  Returns (g, beta), [rows, Hv] fp32.
+    """
+    lib = load_library()
+    hv = geometry.num_v_heads
+    rows = a.shape[0]
+    _dev(a, torch.bfloat16, "a", (rows, hv))
+    _dev(b, torch.bfloat16, "b", (rows, hv))
+    _dev(A_log, torch.float32, "A_log", (hv,))
+    _dev(dt_bias, torch.float32, "dt_bias", (hv,))
+    if g is None:
+        g = torch.empty((rows, hv), dtype=torch.float32, device=a.device)
+    if beta is None:
+        beta = torch.empty((rows, hv), dtype=torch.float32, device=a.device)
+    _dev(g, torch.float32, "g", (rows, hv))
+    _dev(beta, torch.float32, "beta", (rows, hv))
+    _check(lib.gdn_gates(_geo(geometry), _p(a), _p(b), _p(A_log), _p(dt_bias), _p(g), _p(beta), rows,
+                         _stream(stream)))
+    return g, beta
 
 
 def gdn_verify_stash_size(batch: int, rows: int, geometry: Geometry = QWEN_GDN) -> int:

@@ -279,6 +279,24 @@ gdn_status gdn_decode_step_fp16_state(const gdn_geometry* geo, const gdn_bf16* x
                      batch, stream);
 }
 
+gdn_status gdn_gates(const gdn_geometry* geo, const gdn_bf16* a, const gdn_bf16* b, const float* A_log,
+                     const float* dt_bias, float* g, float* beta, int32_t rows, void* stream) {
+  gdn_status s = check_geometry(geo);
+  if (s != GDN_OK) return s;
+  if (rows < 0) return fail(GDN_ERR_INVALID_ARGUMENT, "negative rows");
+  if (rows == 0) return ok();
+  GDN_REQUIRE(a, "a");
+  GDN_REQUIRE(b, "b");
+  GDN_REQUIRE(g, "g");
+  GDN_REQUIRE(beta, "beta");
+  if (!A_log || !dt_bias) return fail(GDN_ERR_INVALID_ARGUMENT, "A_log or dt_bias is NULL");
+  if ((reinterpret_cast<uintptr_t>(A_log) | reinterpret_cast<uintptr_t>(dt_bias)) & 3u)
+    return fail(GDN_ERR_MISALIGNED, "A_log or dt_bias is not 4-byte aligned");
+  gdn::LaunchEnv env;
+  if ((s = make_env(stream, &env)) != GDN_OK) return s;
+  return launched(gdn::launch_gates(env, a, b, A_log, dt_bias, g, beta, rows, geo->num_v_heads), "gates launch");
+}
+
 size_t gdn_verify_stash_size(const gdn_geometry* geo, int32_t batch, int32_t rows) {
   if (check_geometry(geo) != GDN_OK || batch < 0 || rows < 1 || rows > gdn::kMaxVerifyRows) return 0;
   const int C = 2 * geo->num_k_heads * gdn::kHeadDim + geo->num_v_heads * gdn::kHeadDim;

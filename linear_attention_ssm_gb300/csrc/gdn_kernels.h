@@ -16,6 +16,9 @@ cudaError_t launch_conv1d_prefill(const LaunchEnv& env, const uint16_t* x, const
 cudaError_t launch_gated_rmsnorm(const LaunchEnv& env, const uint16_t* o, const uint16_t* z, const uint16_t* w,
                                  float eps, uint16_t* out, long rows);
 
+cudaError_t launch_gates(const LaunchEnv& env, const uint16_t* a, const uint16_t* b, const float* A_log,
+                         const float* dt_bias, float* g, float* beta, long rows, int hv);
+
 int decode_max_ratio();
 cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
                                uint16_t* conv_state, const float* g, const float* beta, void* state,

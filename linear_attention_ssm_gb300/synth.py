@@ -114,3 +114,20 @@ def decode_inputs(batch: int, steps: int, seed: int, geo: Geometry = QWEN_GDN) -
         "norm_w": norm_w, "state0": state0, "conv_state0": conv_state0, "geo": geo,
         "q_scale": geo.q_scale,
     }
+
+
+def gate_inputs(rows: int, seed: int, geo: Geometry = QWEN_GDN) -> dict:
+    """Projection outputs and parameters of the gates for `rows` rows (tokens or sequences).
+
+    a, b ~ N(0, 1) -> bf16 [rows, Hv]; A_log ~ U(-1, 0.5) and dt_bias ~ 0.5 N(0, 1) fp32 [Hv] (no
+    checkpoint is available; these put g mostly in (-4, 0), near the -U(0.001, 2) of the g
+    workloads, with a tail of stronger decays).
+    """
+    gen = torch.Generator().manual_seed(int(seed))
+    hv = geo.num_v_heads
+    return {
+        "a": _normal(gen, (rows, hv)).to(torch.bfloat16),
+        "b": _normal(gen, (rows, hv)).to(torch.bfloat16),
+        "A_log": torch.rand((hv,), generator=gen, dtype=torch.float32) * 1.5 - 1.0,
+        "dt_bias": _normal(gen, (hv,), std=0.5),
+    }

@@ -173,3 +173,12 @@ def test_verify_stash_size_and_argument_checks(lib):
     assert lib.gdn_verify_fp16_state(*args, 4, 18, FAKE, big, None) == 1
     assert lib.gdn_verify_fp16_state(*args, 4, 8, FAKE, 4 * 8 * 53440 - 1, None) == 7
     assert lib.gdn_verify_commit_fp16_state(geo, FAKE, FAKE, FAKE, ODD, 4, 8, None) == 3
+
+
+def test_gates_reject_bad_arguments(lib):
+    geo = _geo()
+    assert lib.gdn_gates(geo, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1, None) == 1
+    assert lib.gdn_gates(geo, None, None, None, None, None, None, 0, None) == 0
+    assert lib.gdn_gates(geo, FAKE, FAKE, None, FAKE, FAKE, FAKE, 4, None) == 1
+    assert lib.gdn_gates(geo, FAKE, FAKE, ctypes.c_void_p(0x10001), FAKE, FAKE, FAKE, 4, None) == 3
+    assert lib.gdn_gates(geo, ODD, FAKE, FAKE, FAKE, FAKE, FAKE, 4, None) == 3

@@ -43,3 +43,16 @@ def test_prefill_from_gate_projections():
     assert_out_close(out.cpu(), ref["out"])
     for n in range(len(lengths)):
         assert_state_close(st[n].cpu(), ref["state"][n], f"state of sequence {n}")
+
+
+def test_gates_head_count_not_a_multiple_of_eight():
+    """6 V heads: the element-at-a-time path."""
+    from linear_attention_ssm_gb300.synth import Geometry
+    g = lib()
+    geo = Geometry(num_k_heads=2, num_v_heads=6)
+    gi = gate_inputs(333, seed=83, geo=geo)
+    gg, bb = g.gdn_gates(gi["a"].to(DEV), gi["b"].to(DEV), gi["A_log"].to(DEV), gi["dt_bias"].to(DEV), geometry=geo)
+    g.gdn_check_device_errors()
+    want_g, want_b = oracle.gates(gi["a"], gi["b"], gi["A_log"], gi["dt_bias"])
+    assert torch.allclose(gg.cpu().double(), want_g, rtol=2e-6, atol=1e-30)
+    assert torch.allclose(bb.cpu().double(), want_b, rtol=2e-6, atol=1e-30)

@@ -78,6 +78,9 @@ def _load():
             lib.oracle_decode_step_h16.restype = I
             lib.oracle_gates.argtypes = [ctypes.c_long, I, P, P, P, P, P, P]
             lib.oracle_gates.restype = I
+            lib.oracle_kda_decode_step.argtypes = [
+                I, I, I, I, I, I, P, P, P, P, D, P, P, P, P, D, D, D, P, P, I]
+            lib.oracle_kda_decode_step.restype = I
             _lib = lib
     return _lib
 
@@ -271,6 +274,30 @@ def decode_step_h16(x, conv_w, conv_state, g, beta, state, z, norm_w, num_k_head
     if rc != 0:
         raise ValueError(f"oracle_decode_step_h16 failed ({rc})")
     return out, o_raw, cs.view(torch.bfloat16), st.view(torch.float16)
+
+
+def kda_decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, num_k_heads, num_v_heads,
+                    head_k_dim, head_v_dim, q_scale, g_min=float("-inf"), l2_eps=1e-6, rms_eps=1e-6,
+                    mutation: int = 0):
+    """One KDA decode token per sequence: the delta rule with a per-channel decay
+    exp(max(g, g_min)), g [B, Hv, Dk] fp32.  Returns (out, o_raw, conv_state', state') like
+    decode_step (new tensors; the arguments are not modified)."""
+    lib = _load()
+    B, C = x.shape
+    W = conv_w.shape[1]
+    hk, hv, dk, dv = num_k_heads, num_v_heads, head_k_dim, head_v_dim
+    cs = _bf16_bits(conv_state).clone()
+    st = _f64(state).clone()
+    xb, wb, gg, bb, zb, nb = (_bf16_bits(x), _bf16_bits(conv_w), _f32(g), _f32(beta), _bf16_bits(z),
+                              _bf16_bits(norm_w))
+    out = torch.empty((B, hv, dv), dtype=torch.float64)
+    o_raw = torch.empty((B, hv, dv), dtype=torch.float64)
+    rc = lib.oracle_kda_decode_step(hk, hv, dk, dv, W, B, _ptr(xb), _ptr(wb), _ptr(cs), _ptr(gg),
+                                    float(g_min), _ptr(bb), _ptr(st), _ptr(zb), _ptr(nb), float(q_scale),
+                                    float(l2_eps), float(rms_eps), _ptr(out), _ptr(o_raw), int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_kda_decode_step failed ({rc})")
+    return out, o_raw, cs.view(torch.bfloat16), st
 
 
 def verify(x, conv_w, conv_state, g, beta, state, z, norm_w, committed_rows, num_k_heads, num_v_heads,

@@ -35,6 +35,8 @@
  *      h-state twins of the decode kernels.
  *   7. the gates g and beta from the a / b projections, A_log and dt_bias (parity unpinned: the
  *      pages give no formula; the published Gated DeltaNet / Mamba-2 gate is taken).
+ *   8. the KDA decode step: the same with a per-channel (key-dimension) decay, clamped and
+ *      exponentiated -- GLM-5.3-Flash kernel TDD ledger, slices I2, I2a, I3.
  *
  * Mutations (negative controls) can be planted here, on the CPU, through the `mutation`
  * bit set; 0 is the method.  See ORACLE_MUT_* below.
@@ -335,17 +337,11 @@ int oracle_gated_rmsnorm(long rows, int dv, const double* o, const uint16_t* z,
  * g, beta:    [B, hv] fp32;  z: [B, hv, dv] bf16;  norm_w: [dv] bf16
  * out:        [B, hv, dv] double gated output;  o_raw: [B, hv, dv] double or NULL (pre-norm)
  */
-int oracle_decode_step(int hk, int hv, int dk, int dv, int W, int B, const uint16_t* x,
-                       const uint16_t* conv_w, uint16_t* conv_state, const float* g,
-                       const float* beta, double* state, const uint16_t* z,
-                       const uint16_t* norm_w, double q_scale, double l2_eps, double rms_eps,
-                       double* out, double* o_raw, int nthreads, int mutation) {
-  const int C = 2 * hk * dk + hv * dv;
+/* The conv step of one token for B sequences: window = [state[0..H-1], x];
+ * y = sum_i w[c,i] window[i]; a = bf16(y * sigmoid(y)); state <- window[1..H]. */
+static void conv_decode_step(int C, int W, int B, const uint16_t* x, const uint16_t* conv_w,
+                             uint16_t* conv_state, uint16_t* a, int mutation) {
   const int H = W - 1;
-  uint16_t* a = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)B * C);
-  double* o = o_raw ? o_raw : (double*)malloc(sizeof(double) * (size_t)B * hv * dv);
-  int32_t* cu = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B + 1));
-  /* conv step: window = [state[0..H-1], x]; y = sum_i w[c,i] window[i]; state <- window[1..H] */
   for (int b = 0; b < B; ++b) {
     for (int c = 0; c < C; ++c) {
       double win[17];
@@ -362,9 +358,20 @@ int oracle_decode_step(int hk, int hv, int dk, int dv, int W, int B, const uint1
       a[(size_t)b * C + c] = oracle_round_bf16(act);
       for (int i = 0; i < H; ++i) st[i] = oracle_round_bf16(win[i + 1]);
     }
-    cu[b] = b;
   }
-  cu[B] = B;
+}
+
+int oracle_decode_step(int hk, int hv, int dk, int dv, int W, int B, const uint16_t* x,
+                       const uint16_t* conv_w, uint16_t* conv_state, const float* g,
+                       const float* beta, double* state, const uint16_t* z,
+                       const uint16_t* norm_w, double q_scale, double l2_eps, double rms_eps,
+                       double* out, double* o_raw, int nthreads, int mutation) {
+  const int C = 2 * hk * dk + hv * dv;
+  uint16_t* a = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)B * C);
+  double* o = o_raw ? o_raw : (double*)malloc(sizeof(double) * (size_t)B * hv * dv);
+  int32_t* cu = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B + 1));
+  conv_decode_step(C, W, B, x, conv_w, conv_state, a, mutation);
+  for (int b = 0; b <= B; ++b) cu[b] = b;
   int rc = oracle_gdn_recurrence(hk, hv, dk, dv, B, a, g, beta, cu, B, q_scale, l2_eps, state, o,
                                  state, NULL, 0, nthreads, mutation & ~ORACLE_MUT_DROP_CARRY);
   if (rc == 0) rc = oracle_gated_rmsnorm((long)B * hv, dv, o, z, norm_w, rms_eps, out, mutation);
@@ -460,4 +467,84 @@ int oracle_gates(long rows, int hv, const uint16_t* a, const uint16_t* b, const 
       beta[i] = sigmoid(bf16_to_double(b[i]));
     }
   return 0;
+}
+
+/* ---------------------------------------------------------------- 8. KDA decode step */
+
+/*
+ * One token of the KDA (Kimi delta attention) layer for each of B sequences: the gated delta
+ * rule with a per-channel (key-dimension) decay -- GLM-5.3-Flash kernel TDD ledger, slices I2
+ * (FP32 [value, key] state, clamped and exponentiated decay, separate q output scale), I2a
+ * (q/k normalised x / sqrt(sum x^2 + eps)) and I3 (the width-4 conv step).  Per V head h,
+ * with q, k of K head h / (hv/hk) after the conv step and the L2 norms:
+ *   alpha_i = exp(max(g[b,h,i], g_min))        (g_min = -inf: no clamp)
+ *   S[r][i] <- alpha_i S[r][i];   e_r = beta (v_r - sum_i S[r][i] k_i);   S[r][i] += e_r k_i
+ *   o_r = q_scale sum_i S[r][i] q_i;   out = gated RMSNorm(o, z) as for the GDN layer.
+ * g: [B, hv, dk] fp32 (per-channel log decay); beta: [B, hv]; state [B, hv, dv, dk] double
+ * in/out; other arguments as oracle_decode_step.
+ */
+int oracle_kda_decode_step(int hk, int hv, int dk, int dv, int W, int B, const uint16_t* x,
+                           const uint16_t* conv_w, uint16_t* conv_state, const float* g,
+                           double g_min, const float* beta, double* state, const uint16_t* z,
+                           const uint16_t* norm_w, double q_scale, double l2_eps, double rms_eps,
+                           double* out, double* o_raw, int mutation) {
+  if (hk <= 0 || hv <= 0 || dk <= 0 || dv <= 0 || hv % hk != 0 || B < 0) return 1;
+  const int C = 2 * hk * dk + hv * dv;
+  const int ratio = hv / hk;
+  uint16_t* a = (uint16_t*)malloc(sizeof(uint16_t) * ((size_t)B * C + 1));
+  double* o = o_raw ? o_raw : (double*)malloc(sizeof(double) * ((size_t)B * hv * dv + 1));
+  double* qn = (double*)malloc(sizeof(double) * dk);
+  double* kn = (double*)malloc(sizeof(double) * dk);
+  double* e = (double*)malloc(sizeof(double) * dv);
+  conv_decode_step(C, W, B, x, conv_w, conv_state, a, mutation);
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < hv; ++h) {
+      const int j = h / ratio;
+      const uint16_t* row = a + (size_t)b * C;
+      double sq = 0.0, sk = 0.0;
+      for (int i = 0; i < dk; ++i) {
+        qn[i] = bf16_to_double(row[j * dk + i]);
+        kn[i] = bf16_to_double(row[hk * dk + j * dk + i]);
+        sq += qn[i] * qn[i];
+        sk += kn[i] * kn[i];
+      }
+      const double iq = (mutation & ORACLE_MUT_NO_QNORM) ? 1.0 : 1.0 / sqrt(sq + l2_eps);
+      const double ik = 1.0 / sqrt(sk + l2_eps);
+      for (int i = 0; i < dk; ++i) {
+        qn[i] *= iq;
+        kn[i] *= ik;
+      }
+      double* S = state + ((size_t)b * hv + h) * dv * dk;
+      const float* gv = g + ((size_t)b * hv + h) * dk;
+      const double bt = (mutation & ORACLE_MUT_NO_BETA) ? 1.0 : (double)beta[(size_t)b * hv + h];
+      const uint16_t* vrow = row + 2 * hk * dk + (size_t)h * dv;
+      /* element (r, i) of the [value, key] state; the transposed mutation reads it as [key, value] */
+#define SEL(r, i) (*((mutation & ORACLE_MUT_TRANSPOSE) ? &S[(size_t)(i) * dv + (r)] : &S[(size_t)(r) * dk + (i)]))
+      for (int r = 0; r < dv; ++r)
+        for (int i = 0; i < dk; ++i) {
+          const double gi = (double)gv[i] > g_min ? (double)gv[i] : g_min;
+          SEL(r, i) *= exp((mutation & ORACLE_MUT_DECAY_SIGN) ? -gi : gi);
+        }
+      for (int r = 0; r < dv; ++r) {
+        double u = 0.0;
+        for (int i = 0; i < dk; ++i) u += SEL(r, i) * kn[i];
+        e[r] = bt * (bf16_to_double(vrow[r]) - u);
+      }
+      for (int r = 0; r < dv; ++r)
+        for (int i = 0; i < dk; ++i) SEL(r, i) += e[r] * kn[i];
+      double* orow = o + ((size_t)b * hv + h) * dv;
+      for (int r = 0; r < dv; ++r) {
+        double acc = 0.0;
+        for (int i = 0; i < dk; ++i) acc += SEL(r, i) * qn[i];
+        orow[r] = q_scale * acc;
+      }
+#undef SEL
+    }
+  const int rc = oracle_gated_rmsnorm((long)B * hv, dv, o, z, norm_w, rms_eps, out, mutation);
+  free(a);
+  free(qn);
+  free(kn);
+  free(e);
+  if (!o_raw) free(o);
+  return rc;
 }

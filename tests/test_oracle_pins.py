@@ -598,3 +598,63 @@ def test_gates_closed_forms():
     assert torch.isfinite(g2).all() and (g2 < 0).all()
     assert abs(g2[0, 0].item()) < 1e-30                       # softplus(-80) ~ e^-80
     assert abs(g2[0, 2].item() + math.exp(-2.0) * 800.0) < 1e-9  # softplus(x) -> x
+
+
+# ------------------------------------------------------------------ KDA decode (per-channel decay)
+
+KDA_GEO = Geometry(num_k_heads=3, num_v_heads=3, head_k_dim=8, head_v_dim=4, conv_width=4)
+
+
+def _kda_args(geo):
+    return dict(num_k_heads=geo.num_k_heads, num_v_heads=geo.num_v_heads, head_k_dim=geo.head_k_dim,
+                head_v_dim=geo.head_v_dim, q_scale=0.35)
+
+
+def test_kda_with_a_channel_constant_decay_is_the_gdn_step():
+    """A per-channel decay equal on every key channel is the scalar decay of the GDN step (an
+    independent code path), for every output and state element."""
+    geo = KDA_GEO
+    d = decode_inputs(4, 1, seed=45, geo=geo)
+    a = _kda_args(geo)
+    g_vec = d["g"][0][:, :, None].expand(4, geo.num_v_heads, geo.head_k_dim).contiguous()
+    args = (d["x"][0], d["conv_w"], d["conv_state0"])
+    kda = oracle.kda_decode_step(*args, g_vec, d["beta"][0], d["state0"], d["z"][0], d["norm_w"], **a)
+    gdn = oracle.decode_step(*args, d["g"][0], d["beta"][0], d["state0"], d["z"][0], d["norm_w"], **a)
+    for got, want in zip((kda[0], kda[1], kda[3]), (gdn[0], gdn[1], gdn[3])):
+        assert torch.allclose(got, want, rtol=1e-12, atol=1e-14)
+    assert torch.equal(kda[2].view(torch.int16), gdn[2].view(torch.int16))
+
+
+def test_kda_beta_zero_decays_each_key_column():
+    """beta = 0: the new state is S with key column i scaled by exp(g_i) (numpy), and the clamp
+    limits the decay to exp(g_min)."""
+    geo = KDA_GEO
+    d = decode_inputs(2, 1, seed=46, geo=geo)
+    a = _kda_args(geo)
+    gen = torch.Generator().manual_seed(46)
+    g_vec = -4 * torch.rand((2, geo.num_v_heads, geo.head_k_dim), generator=gen)
+    beta0 = torch.zeros_like(d["beta"][0])
+    args = (d["x"][0], d["conv_w"], d["conv_state0"])
+    _, _, _, st = oracle.kda_decode_step(*args, g_vec, beta0, d["state0"], d["z"][0], d["norm_w"], **a)
+    want = d["state0"].double().numpy() * np.exp(g_vec.double().numpy())[:, :, None, :]
+    np.testing.assert_allclose(st.numpy(), want, rtol=1e-14, atol=0)
+    _, _, _, stc = oracle.kda_decode_step(*args, g_vec, beta0, d["state0"], d["z"][0], d["norm_w"],
+                                          g_min=-1.0, **a)
+    wantc = d["state0"].double().numpy() * np.exp(np.maximum(g_vec.double().numpy(), -1.0))[:, :, None, :]
+    np.testing.assert_allclose(stc.numpy(), wantc, rtol=1e-14, atol=0)
+
+
+@pytest.mark.parametrize("mut", [oracle.MUT_DECAY_SIGN, oracle.MUT_NO_BETA, oracle.MUT_TRANSPOSE,
+                                 oracle.MUT_NO_QNORM])
+def test_kda_planted_mutations_change_the_result(mut):
+    """The ledger's RED list for the KDA decode (wrong decay sign, missing beta or q scaling,
+    transposed state) is live in the oracle."""
+    geo = KDA_GEO
+    d = decode_inputs(3, 1, seed=47, geo=geo)
+    a = _kda_args(geo)
+    gen = torch.Generator().manual_seed(47)
+    g_vec = -2 * torch.rand((3, geo.num_v_heads, geo.head_k_dim), generator=gen)
+    args = (d["x"][0], d["conv_w"], d["conv_state0"], g_vec, d["beta"][0], d["state0"], d["z"][0], d["norm_w"])
+    base = oracle.kda_decode_step(*args, **a)
+    bad = oracle.kda_decode_step(*args, mutation=mut, **a)
+    assert (base[0] - bad[0]).abs().max() > 1e-3 or (base[3] - bad[3]).abs().max() > 1e-3

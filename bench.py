@@ -269,6 +269,46 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def time_kda_decode(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak):
+    """KDA decode step (decay per key channel) on the pages' 64-head geometry, 256 sequences, 8
+    pre-generated steps cycled."""
+    import torch
+    from linear_attention_ssm_gb300.synth import KDA_GEO, kda_decode_inputs
+    geo, B, S = KDA_GEO, 256, 8
+    d = kda_decode_inputs(B, S, seed=7)
+    kx, kg, kb, kz = (d[k].to(dev) for k in ("x", "g", "beta", "z"))
+    kw, knw = d["conv_w"].to(dev), d["norm_w"].to(dev)
+    kst, kcs = d["state0"].to(dev), d["conv_state0"].to(dev)
+    kout = torch.empty((B, geo.num_v_heads, 128), dtype=torch.bfloat16, device=dev)
+
+    def step(s):
+        gdn.gdn_kda_decode_step(kx[s], kw, kcs, kg[s], kb[s], kst, kz[s], knw, d["q_scale"], out=kout, geometry=geo)
+
+    for s in range(max(args.warmup, 1)):
+        step(s % S)
+    barrier()
+    n = max(args.decode_steps // 2, 4)
+    s6, e6 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s6.record(stream)
+    for s in range(n):
+        step(s % S)
+    e6.record(stream)
+    torch.cuda.synchronize()
+    gdn.gdn_check_device_errors()
+    ms = max_over_ranks(s6.elapsed_time(e6)) / n
+    C, hv = geo.conv_dim, geo.num_v_heads
+    per_seq = 2 * hv * 128 * 128 * 4 + 2 * C * 3 * 2 + C * 2 + hv * 128 * 4 + hv * 4 + 2 * hv * 128 * 2
+    nbytes = per_seq * B
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del kx, kg, kb, kz, kst, kcs
+    return {"metric": "KDA decode seq-steps/s", "value": world * B / (ms / 1e3), "unit": "seq-steps/s",
+            "ms_per_step": ms, "steps": n, "batch": B,
+            "workload": "KDA decode, 256 sequences x one token, 64 heads x 128 (q, k, v), per-channel decay",
+            "roofline": {"kernel": "decode_step_kernel (per-channel decay)", "bound": "hbm", "achieved": gbs,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                         "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms}}
+
+
 VERIFY_ROWS = 8
 VERIFY_RECORD = 53440  # stash bytes per (sequence, row): raw inputs, keys, deltas, g
 
@@ -557,6 +597,7 @@ def run_ours(args, rank, world, local):
                 "roofline_seq_steps_per_s": hbm_peak * 1e9 / (dec_bytes / B)}
 
     decode = time_decode(torch.float32, STATE_BYTES_PER_SEQ, "decode_step")
+    decode_kda = time_kda_decode(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak)
     # the same workload with the recurrent state stored as binary16 (half the state bytes)
     decode_f16 = time_decode(torch.float16, STATE_BYTES_PER_SEQ // 2, "decode_step_fp16_state")
     decode_f16["state"] = "binary16 in memory, fp32 arithmetic, rounded once per step"
@@ -624,7 +665,8 @@ def run_ours(args, rank, world, local):
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                     "pipelined": "H2D of step i+1 and D2H of step i-1 overlap the prefill of step i"},
-            "decode": decode, "decode_fp16_state": decode_f16, "verify": verify, "verify_fp16_state": verify_f16,
+            "decode": decode, "decode_fp16_state": decode_f16, "decode_kda": decode_kda, "verify": verify,
+            "verify_fp16_state": verify_f16,
             "gates": gates,
             "varlen": varlen, "cpu_baseline": cpu, "clocks": clk,
             # per step: conv1d + conv-state kernels, the chunk prefill's schedule and segment-table

@@ -298,6 +298,24 @@ GDN_API gdn_status gdn_verify_commit_fp16_state(const gdn_geometry* geo,
                                                 gdn_bf16* conv_state, gdn_f16* state,
                                                 int32_t batch, int32_t rows, void* stream);
 
+/*
+ * One fused decode step of the KDA (Kimi delta attention) layer: as gdn_decode_step, with a decay
+ * per key channel instead of per head.  GLM-5.3-Flash kernel TDD ledger, slices I2 (FP32
+ * [value, key] state, clamped and exponentiated decay, separate q output scale), I2a (q/k
+ * normalised x / sqrt(sum x^2 + eps)) and I3 (the width-4 conv step).  Per V head:
+ *   S <- S diag(exp(max(g, g_min)));   e = beta (v - S k);   S <- S + e k^T;   o = q_scale S q
+ * followed by the same sigmoid-gated RMSNorm as gdn_decode_step.
+ *   g           [batch, Hv, Dk] fp32 per-channel log decay (16-byte aligned)
+ *   g_min       the clamp: decays below exp(g_min) are raised to it (-INFINITY: no clamp)
+ *   all other arguments, results and errors as gdn_decode_step (fp32 state).
+ */
+GDN_API gdn_status gdn_kda_decode_step(const gdn_geometry* geo, const gdn_bf16* x,
+                                       const gdn_bf16* conv_w, gdn_bf16* conv_state,
+                                       const float* g, float g_min, const float* beta, float* state,
+                                       const gdn_bf16* z, const gdn_bf16* norm_w, float q_scale,
+                                       float l2_eps, float rms_eps, gdn_bf16* out, int32_t batch,
+                                       void* stream);
+
 /* Capacity of the fixed scratch used by gdn_chunk_prefill_noalloc. */
 #define GDN_NOALLOC_MAX_SEQS 16384
 #define GDN_NOALLOC_SCRATCH_BYTES (256 + 4 * GDN_NOALLOC_MAX_SEQS) /* 65,792 bytes */

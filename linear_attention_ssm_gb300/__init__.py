@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     gdn_decode_step_fp16_state,
     gdn_gated_rmsnorm,
     gdn_gates,
+    gdn_kda_decode_step,
     gdn_prefill,
     gdn_verify,
     gdn_verify_commit,

@@ -61,6 +61,7 @@ def load_library():
             "gdn_decode_step": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
             "gdn_decode_step_fp16_state": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
             "gdn_gates": ([G, P, P, P, P, P, P, I, P], ctypes.c_int),
+            "gdn_kda_decode_step": ([G, P, P, P, P, F, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
             "gdn_verify_stash_size": ([G, I, I], S),
             "gdn_verify": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, I, P, S, P], ctypes.c_int),
             "gdn_verify_commit": ([G, P, P, P, P, I, I, P], ctypes.c_int),
@@ -227,6 +228,31 @@ def gdn_decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l
     fn = lib.gdn_decode_step_fp16_state if fp16_state else lib.gdn_decode_step
     _check(fn(_geo(geometry), _p(x), _p(conv_w), _p(conv_state), _p(g), _p(beta), _p(state), _p(z),
               _p(norm_w), float(q_scale), float(l2_eps), float(rms_eps), _p(out), B, _stream(stream)))
+    return out
+
+
+def gdn_kda_decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, g_min=float("-inf"),
+                        l2_eps=1e-6, rms_eps=1e-6, out=None, geometry: Geometry = QWEN_GDN, stream=None):
+    """One KDA decode step (decay per key channel, g [B, Hv, Dk] fp32, clamped below at g_min);
+    conv_state and state are updated in place.  Returns out."""
+    lib = load_library()
+    C, W = geometry.conv_dim, geometry.conv_width
+    hv, dv, dk = geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
+    B = x.shape[0]
+    _dev(x, torch.bfloat16, "x", (B, C))
+    _dev(conv_w, torch.bfloat16, "conv_w", (C, W))
+    _dev(conv_state, torch.bfloat16, "conv_state", (B, C, W - 1))
+    _dev(g, torch.float32, "g", (B, hv, dk))
+    _dev(beta, torch.float32, "beta", (B, hv))
+    _dev(state, torch.float32, "state", (B, hv, dv, dk))
+    _dev(z, torch.bfloat16, "z", (B, hv, dv))
+    _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
+    if out is None:
+        out = torch.empty((B, hv, dv), dtype=torch.bfloat16, device=x.device)
+    _dev(out, torch.bfloat16, "out", (B, hv, dv))
+    _check(lib.gdn_kda_decode_step(_geo(geometry), _p(x), _p(conv_w), _p(conv_state), _p(g), float(g_min), _p(beta),
+                                   _p(state), _p(z), _p(norm_w), float(q_scale), float(l2_eps), float(rms_eps),
+                                   _p(out), B, _stream(stream)))
     return out
 
 

@@ -79,12 +79,15 @@ __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
 // into shared memory by one bulk copy issued before the conv step, so the state bytes are in
 // flight while the conv and the norms are computed; the rows are then read from shared memory.
 // Used when the slice fits (binary16 state, R <= 3: 96 KB).  Otherwise rows stream from global.
-template <typename StateT, bool kStaged>
+// kPerChannel: the KDA form -- g is [B, Hv, Dk], a log decay per key channel, applied as
+// exp(max(g, g_min)) to the state's key columns (GLM-5.3-Flash kernel TDD ledger, slice I2);
+// otherwise g is [B, Hv], one decay per head (the GDN step).
+template <typename StateT, bool kStaged, bool kPerChannel = false>
 __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ conv_w, uint16_t* conv_state,
     const float* __restrict__ g, const float* __restrict__ beta, StateT* state,
     const uint16_t* __restrict__ z, const uint16_t* __restrict__ norm_w, float q_scale, float l2_eps,
-    float rms_eps, uint16_t* __restrict__ out, int Hk, int Hv, unsigned* err) {
+    float rms_eps, uint16_t* __restrict__ out, int Hk, int Hv, unsigned* err, float g_min = 0.f) {
   const int j = blockIdx.x;        // K head
   const int b = blockIdx.y;        // sequence
   const int R = Hv / Hk;
@@ -172,7 +175,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
   // ---- state update, one V head at a time
   for (int hh = 0; hh < R; ++hh) {
     const int h = j * R + hh;
-    const float alpha = expf(__ldg(g + (size_t)b * Hv + h));
+    float4 a4, kd;  // the decay of this lane's four key channels; the key they multiply (decayed)
+    if constexpr (kPerChannel) {
+      const float4 gv = __ldg(reinterpret_cast<const float4*>(g + ((size_t)b * Hv + h) * kHeadDim) + lane);
+      a4 = make_float4(expf(fmaxf(gv.x, g_min)), expf(fmaxf(gv.y, g_min)), expf(fmaxf(gv.z, g_min)),
+                       expf(fmaxf(gv.w, g_min)));
+      kd = make_float4(a4.x * kn.x, a4.y * kn.y, a4.z * kn.z, a4.w * kn.w);  // (S diag(a)) k = S (a * k)
+    } else {
+      const float alpha = expf(__ldg(g + (size_t)b * Hv + h));
+      a4 = make_float4(alpha, alpha, alpha, alpha);
+      kd = kn;
+    }
     const float bt = __ldg(beta + (size_t)b * Hv + h);
     StateT* S = slice + ((size_t)hh * kHeadDim + warp * kRowsPerWarp) * kHeadDim;
     float4 row[kRowsPerWarp];
@@ -187,20 +200,22 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     float d[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i)
-      d[i] = row[i].x * kn.x + row[i].y * kn.y + row[i].z * kn.z + row[i].w * kn.w;
+      d[i] = row[i].x * kd.x + row[i].y * kd.y + row[i].z * kd.z + row[i].w * kd.w;
     // lanes 2i and 2i + 1 hold row i's sum; its delta (against the decayed state) is formed there
     // and broadcast
     const int i_mine = (lane >> 1) & 15;
-    const float e_mine =
-        bt * (s_v[hh][warp * kRowsPerWarp + i_mine] - alpha * warp_sum16(d, lane));
+    const float dsum = warp_sum16(d, lane);
+    const float e_mine = bt * (s_v[hh][warp * kRowsPerWarp + i_mine] - (kPerChannel ? dsum : a4.x * dsum));
     float o[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
       const float e = __shfl_sync(0xffffffffu, e_mine, 2 * i);
       // S <- alpha S + e k^T, element by element fma(alpha, s, e k) in f32x2 pairs
-      const float2 a2 = make_float2(alpha, alpha), e2 = make_float2(e, e);
-      const float2 xy = __ffma2_rn(a2, make_float2(row[i].x, row[i].y), __fmul2_rn(e2, make_float2(kn.x, kn.y)));
-      const float2 zw = __ffma2_rn(a2, make_float2(row[i].z, row[i].w), __fmul2_rn(e2, make_float2(kn.z, kn.w)));
+      const float2 e2 = make_float2(e, e);
+      const float2 xy = __ffma2_rn(make_float2(a4.x, a4.y), make_float2(row[i].x, row[i].y),
+                                   __fmul2_rn(e2, make_float2(kn.x, kn.y)));
+      const float2 zw = __ffma2_rn(make_float2(a4.z, a4.w), make_float2(row[i].z, row[i].w),
+                                   __fmul2_rn(e2, make_float2(kn.z, kn.w)));
       const float4 sn = make_float4(xy.x, xy.y, zw.x, zw.y);
       store_state4(S, i * 32 + lane, sn);
       o[i] = sn.x * qn.x + sn.y * qn.y + sn.z * qn.z + sn.w * qn.w;
@@ -236,6 +251,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
 }  // namespace
 
 int decode_max_ratio() { return kMaxRatio; }
+
+cudaError_t launch_kda_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
+                                   uint16_t* conv_state, const float* g, float g_min, const float* beta,
+                                   float* state, const uint16_t* z, const uint16_t* norm_w, float q_scale,
+                                   float l2_eps, float rms_eps, uint16_t* out, int B, int Hk, int Hv) {
+  if (B <= 0) return cudaSuccess;
+  decode_step_kernel<float, false, true><<<dim3(Hk, B), kThreads, 0, env.stream>>>(
+      x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv, env.err, g_min);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
                                uint16_t* conv_state, const float* g, const float* beta, void* state,

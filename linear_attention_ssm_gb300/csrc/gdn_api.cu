@@ -271,6 +271,36 @@ gdn_status gdn_decode_step(const gdn_geometry* geo, const gdn_bf16* x, const gdn
                      batch, stream);
 }
 
+gdn_status gdn_kda_decode_step(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w,
+                               gdn_bf16* conv_state, const float* g, float g_min, const float* beta, float* state,
+                               const gdn_bf16* z, const gdn_bf16* norm_w, float q_scale, float l2_eps,
+                               float rms_eps, gdn_bf16* out, int32_t batch, void* stream) {
+  gdn_status s = check_geometry(geo);
+  if (s != GDN_OK) return s;
+  if (geo->num_v_heads / geo->num_k_heads > gdn::decode_max_ratio())
+    return fail(GDN_ERR_UNSUPPORTED_GEOMETRY, "decode supports at most %d V heads per K head",
+                gdn::decode_max_ratio());
+  if (batch < 0 || batch > 65535) return fail(GDN_ERR_INVALID_ARGUMENT, "batch must be in [0, 65535] (got %d)", batch);
+  if (batch == 0) return ok();
+  GDN_REQUIRE(x, "x");
+  GDN_REQUIRE(conv_w, "conv_w");
+  GDN_REQUIRE(conv_state, "conv_state");
+  GDN_REQUIRE(g, "g");
+  GDN_REQUIRE(state, "state");
+  GDN_REQUIRE(z, "z");
+  GDN_REQUIRE(norm_w, "norm_w");
+  GDN_REQUIRE(out, "out");
+  if (!beta) return fail(GDN_ERR_INVALID_ARGUMENT, "beta is NULL");
+  if (reinterpret_cast<uintptr_t>(beta) & 3u) return fail(GDN_ERR_MISALIGNED, "beta is not 4-byte aligned");
+  if (g_min != g_min) return fail(GDN_ERR_INVALID_ARGUMENT, "g_min is NaN");
+  if (!(l2_eps >= 0.f) || !(rms_eps >= 0.f)) return fail(GDN_ERR_INVALID_ARGUMENT, "eps must be >= 0");
+  gdn::LaunchEnv env;
+  if ((s = make_env(stream, &env)) != GDN_OK) return s;
+  return launched(gdn::launch_kda_decode_step(env, x, conv_w, conv_state, g, g_min, beta, state, z, norm_w, q_scale,
+                                              l2_eps, rms_eps, out, batch, geo->num_k_heads, geo->num_v_heads),
+                  "KDA decode launch");
+}
+
 gdn_status gdn_decode_step_fp16_state(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w,
                                       gdn_bf16* conv_state, const float* g, const float* beta, gdn_f16* state,
                                       const gdn_bf16* z, const gdn_bf16* norm_w, float q_scale, float l2_eps,

@@ -20,6 +20,11 @@ cudaError_t launch_gates(const LaunchEnv& env, const uint16_t* a, const uint16_t
                          const float* dt_bias, float* g, float* beta, long rows, int hv);
 
 int decode_max_ratio();
+// The KDA decode step: g is [B, Hv, Dk], a log decay per key channel, clamped below at g_min.
+cudaError_t launch_kda_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
+                                   uint16_t* conv_state, const float* g, float g_min, const float* beta,
+                                   float* state, const uint16_t* z, const uint16_t* norm_w, float q_scale,
+                                   float l2_eps, float rms_eps, uint16_t* out, int B, int Hk, int Hv);
 cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
                                uint16_t* conv_state, const float* g, const float* beta, void* state,
                                bool fp16_state, const uint16_t* z, const uint16_t* norm_w, float q_scale,

@@ -131,3 +131,17 @@ def gate_inputs(rows: int, seed: int, geo: Geometry = QWEN_GDN) -> dict:
         "A_log": torch.rand((hv,), generator=gen, dtype=torch.float32) * 1.5 - 1.0,
         "dt_bias": _normal(gen, (hv,), std=0.5),
     }
+
+
+# The KDA layer's geometry on the pages: q, k and v of 64 heads of 128 (a 3 x 64 x 128 conv),
+# one V head per K head.
+KDA_GEO = Geometry(num_k_heads=64, num_v_heads=64, head_k_dim=128, head_v_dim=128, conv_width=4)
+
+
+def kda_decode_inputs(batch: int, steps: int, seed: int, geo: Geometry = KDA_GEO) -> dict:
+    """decode_inputs with a per-key-channel log decay g = -U(0.001, 2) [steps, batch, Hv, Dk]."""
+    d = decode_inputs(batch, steps, seed, geo)
+    gen = torch.Generator().manual_seed(int(seed) + 1)
+    d["g"] = -(torch.rand((steps, batch, geo.num_v_heads, geo.head_k_dim), generator=gen,
+                          dtype=torch.float32) * (2.0 - 0.001) + 0.001)
+    return d

@@ -182,3 +182,13 @@ def test_gates_reject_bad_arguments(lib):
     assert lib.gdn_gates(geo, FAKE, FAKE, None, FAKE, FAKE, FAKE, 4, None) == 1
     assert lib.gdn_gates(geo, FAKE, FAKE, ctypes.c_void_p(0x10001), FAKE, FAKE, FAKE, 4, None) == 3
     assert lib.gdn_gates(geo, ODD, FAKE, FAKE, FAKE, FAKE, FAKE, 4, None) == 3
+
+
+def test_kda_decode_rejects_bad_arguments(lib):
+    geo = _geo(num_k_heads=64, num_v_heads=64)
+    tail = [FAKE, FAKE, FAKE, 0.088, 1e-6, 1e-6, FAKE]  # state, z, norm_w, q_scale, eps, eps, out
+    assert lib.gdn_kda_decode_step(geo, FAKE, FAKE, FAKE, FAKE, -1.0, FAKE, *tail, -1, None) == 1
+    assert lib.gdn_kda_decode_step(geo, FAKE, FAKE, FAKE, FAKE, float("nan"), FAKE, *tail, 4, None) == 1
+    assert lib.gdn_kda_decode_step(geo, FAKE, FAKE, FAKE, ODD, -1.0, FAKE, *tail, 4, None) == 3
+    assert lib.gdn_kda_decode_step(geo, None, None, None, None, -1.0, None, None, None, None, 0.088, 1e-6,
+                                   1e-6, None, 0, None) == 0

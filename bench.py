@@ -306,6 +306,7 @@ def time_kda_decode(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_
             "workload": "KDA decode, 256 sequences x one token, 64 heads x 128 (q, k, v), per-channel decay",
             "roofline": {"kernel": "decode_step_kernel (per-channel decay)", "bound": "hbm", "achieved": gbs,
                          "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                         "traffic": (traffic_record("decode_kda") or {}).get("bytes_per_launch"),
                          "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms}}
 
 

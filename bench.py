@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -142,16 +143,23 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def code_digest(text):
+    """Hash of a kernel source's code: `//` comments, trailing blanks and empty lines left out, so
+    that a comment-only edit keeps a traffic record while any change to the code drops it."""
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()[:16]
+
+
 def traffic_record(kernel):
-    """ncu DRAM bytes per launch of `kernel`, if captured on the current source."""
+    """ncu DRAM bytes per launch of `kernel`, if captured on the current code."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)[kernel]
         src = os.path.join(ROOT, "linear_attention_ssm_gb300", "csrc", rec["source"])
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if digest != rec["source_sha256_16"]:
-            return None
+        with open(src) as f:
+            if code_digest(f.read()) != rec["code_sha256_16"]:
+                return None
         return rec
     except Exception:
         return None

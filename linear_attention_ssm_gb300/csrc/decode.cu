@@ -6,7 +6,10 @@
 // kernels (one launch for all sequences; the state read once and written once, 1R+1W);
 // GLM-5.3-Flash kernel TDD ledger, slice I3 (a conv step equals the full width-4 causal conv);
 // Qwen3.8 ledger, the FP16 h-state twins of the decode kernels (same arithmetic as the fp32
-// kernel, the state half precision in memory, rounded once per token).
+// kernel, the state half precision in memory, rounded once per token); GLM ledger slice I2 (the
+// KDA step: the same update with a decay per key channel, clamped and exponentiated).
+//
+// The conv outputs are rounded to the bf16 nearest the exact value (silu_bf16_rn).
 //
 // With a binary16 state the CTA's state slice (96 KB) is staged in shared memory by one bulk copy
 // issued at the start, so it streams in while the conv step and the norms run.

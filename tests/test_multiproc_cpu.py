@@ -49,3 +49,11 @@ def test_two_gloo_ranks_agree_on_the_slowest_rank():
 def test_single_rank_needs_no_group():
     assert bench.slowest_rank_ms(1.25, 1, "cpu") == 1.25
     assert bench.replica_throughput(16384, 1, 2.0) == pytest.approx(16384 / 2e-3)
+
+
+def test_traffic_records_survive_comment_edits_only():
+    """A traffic record stays bound to a kernel's code: comments do not move the hash, code does."""
+    code = "// header\n__global__ void k(float* a) {  // trailing note\n\n  a[0] = 1.f;\n}\n"
+    assert bench.code_digest(code) == bench.code_digest("__global__ void k(float* a) {\n  a[0] = 1.f;\n}")
+    assert bench.code_digest(code) != bench.code_digest(code.replace("1.f", "2.f"))
+

@@ -145,3 +145,13 @@ def kda_decode_inputs(batch: int, steps: int, seed: int, geo: Geometry = KDA_GEO
     d["g"] = -(torch.rand((steps, batch, geo.num_v_heads, geo.head_k_dim), generator=gen,
                           dtype=torch.float32) * (2.0 - 0.001) + 0.001)
     return d
+
+
+def kda_prefill_inputs(lengths, seed: int, geo: Geometry = KDA_GEO, **kw) -> dict:
+    """prefill_inputs with a per-key-channel log decay g = -U(0.001, 2) [T, Hv, Dk]."""
+    d = prefill_inputs(lengths, seed, geo, **kw)
+    gen = torch.Generator().manual_seed(int(seed) + 1)
+    T = sum(int(L) for L in lengths)
+    d["g"] = -(torch.rand((T, geo.num_v_heads, geo.head_k_dim), generator=gen,
+                          dtype=torch.float32) * (2.0 - 0.001) + 0.001)
+    return d

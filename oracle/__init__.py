@@ -81,6 +81,9 @@ def _load():
             lib.oracle_kda_decode_step.argtypes = [
                 I, I, I, I, I, I, P, P, P, P, D, P, P, P, P, D, D, D, P, P, I]
             lib.oracle_kda_decode_step.restype = I
+            lib.oracle_kda_recurrence.argtypes = [
+                I, I, I, I, I, P, P, D, P, P, I, D, D, P, P, P, P, I, I, I]
+            lib.oracle_kda_recurrence.restype = I
             _lib = lib
     return _lib
 
@@ -365,5 +368,47 @@ def prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, num_k_heads, num_v_heads,
     o, st = gdn_recurrence(y, g, beta, cu_seqlens, num_k_heads, num_v_heads, head_k_dim,
                            head_v_dim, q_scale, l2_eps, state_in, heads=heads, nthreads=nthreads,
                            mutation=mutation)
+    out = gated_rmsnorm(o, z, norm_w, rms_eps, mutation=mutation)
+    return {"y": y, "o": o, "out": out, "state": st, "conv_state": cs}
+
+
+def kda_recurrence(qkv, g, beta, cu_seqlens, num_k_heads, num_v_heads, head_k_dim, head_v_dim,
+                   q_scale, g_min=float("-inf"), l2_eps=1e-6, state_in=None, heads=None,
+                   nthreads: int = 0, mutation: int = 0):
+    """The KDA recurrence, token by token: gdn_recurrence with g [T, Hv, Dk] fp32, a log decay
+    per key channel applied as exp(max(g, g_min)) to the state's key columns.  GLM-5.3-Flash
+    kernel TDD ledger, slices I2 and I4.  Returns (o float64 [T, Hv, Dv], state_out float64
+    [N, Hv, Dv, Dk])."""
+    lib = _load()
+    T = qkv.shape[0]
+    cu = _i32(cu_seqlens)
+    N = cu.numel() - 1
+    hk, hv, dk, dv = num_k_heads, num_v_heads, head_k_dim, head_v_dim
+    assert qkv.shape[1] == 2 * hk * dk + hv * dv
+    assert tuple(g.shape) == (T, hv, dk), g.shape
+    q = _bf16_bits(qkv)
+    gg, bb = _f32(g), _f32(beta)
+    sin = _f64(state_in)
+    o = torch.full((T, hv, dv), float("nan"), dtype=torch.float64)
+    sout = torch.full((N, hv, dv, dk), float("nan"), dtype=torch.float64)
+    hl = _i32(heads) if heads is not None else None
+    rc = lib.oracle_kda_recurrence(hk, hv, dk, dv, T, _ptr(q), _ptr(gg), float(g_min), _ptr(bb),
+                                   _ptr(cu), N, float(q_scale), float(l2_eps), _ptr(sin), _ptr(o),
+                                   _ptr(sout), _ptr(hl), 0 if hl is None else hl.numel(),
+                                   int(nthreads), int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_kda_recurrence failed ({rc})")
+    return o, sout
+
+
+def kda_prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, num_k_heads, num_v_heads, head_k_dim,
+                head_v_dim, q_scale, g_min=float("-inf"), l2_eps=1e-6, rms_eps=1e-6, state_in=None,
+                conv_state_in=None, heads=None, nthreads: int = 0, mutation: int = 0):
+    """The KDA prefill: conv1d+SiLU -> KDA recurrence -> gated RMSNorm (the output gate of the
+    GDN sublayer).  Returns the same dict as prefill."""
+    y, _, cs = conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in, mutation=mutation)
+    o, st = kda_recurrence(y, g, beta, cu_seqlens, num_k_heads, num_v_heads, head_k_dim,
+                           head_v_dim, q_scale, g_min, l2_eps, state_in, heads=heads,
+                           nthreads=nthreads, mutation=mutation)
     out = gated_rmsnorm(o, z, norm_w, rms_eps, mutation=mutation)
     return {"y": y, "o": o, "out": out, "state": st, "conv_state": cs}

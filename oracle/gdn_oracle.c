@@ -37,6 +37,9 @@
  *      pages give no formula; the published Gated DeltaNet / Mamba-2 gate is taken).
  *   8. the KDA decode step: the same with a per-channel (key-dimension) decay, clamped and
  *      exponentiated -- GLM-5.3-Flash kernel TDD ledger, slices I2, I2a, I3.
+ *   9. the KDA recurrence over packed sequences (the prefill's sequential form): step 3 with the
+ *      decay of item 8, token by token -- the same ledger, slice I4 (the chunk path must match
+ *      the sequential state and output).
  *
  * Mutations (negative controls) can be planted here, on the CPU, through the `mutation`
  * bit set; 0 is the method.  See ORACLE_MUT_* below.
@@ -151,7 +154,9 @@ int oracle_conv1d_prefill(int C, int W, int T, const uint16_t* x, const uint16_t
 typedef struct {
   int hk, hv, dk, dv;
   const uint16_t* qkv;   /* [T, 2*hk*dk + hv*dv] bf16 */
-  const float* g;        /* [T, hv] */
+  const float* g;        /* [T, hv], or NULL when gk is given */
+  const float* gk;       /* [T, hv, dk] per-key-channel log decay (KDA), or NULL */
+  double g_min;          /* clamp of gk: exp(max(gk, g_min)) */
   const float* beta;     /* [T, hv] */
   const int32_t* cu;     /* [N+1] */
   int N;
@@ -210,12 +215,22 @@ static void rec_chain(rec_job* J, int n, int h) {
       qn[i] *= iq;
       kn[i] *= ik;
     }
-    const double gt = (double)J->g[t * hv + h];
-    const double alpha = exp((J->mutation & ORACLE_MUT_DECAY_SIGN) ? -gt : gt);
     const double b = (J->mutation & ORACLE_MUT_NO_BETA) ? 1.0 : (double)J->beta[t * hv + h];
     const uint16_t* vrow = row + 2 * hk * dk + (size_t)h * dv;
     /* decay, then the delta correction against the decayed state */
-    for (size_t x = 0; x < sdim; ++x) S[x] *= alpha;
+    if (J->gk) {
+      /* KDA: key column i of the [value, key] state decays by exp(max(g_i, g_min)) */
+      const float* gv = J->gk + (t * hv + h) * dk;
+      for (int i = 0; i < dk; ++i) {
+        const double gi = (double)gv[i] > J->g_min ? (double)gv[i] : J->g_min;
+        const double ai = exp((J->mutation & ORACLE_MUT_DECAY_SIGN) ? -gi : gi);
+        for (int r = 0; r < dv; ++r) S[(size_t)r * dk + i] *= ai;
+      }
+    } else {
+      const double gt = (double)J->g[t * hv + h];
+      const double alpha = exp((J->mutation & ORACLE_MUT_DECAY_SIGN) ? -gt : gt);
+      for (size_t x = 0; x < sdim; ++x) S[x] *= alpha;
+    }
     for (int r = 0; r < dv; ++r) {
       double u = 0.0;
       for (int i = 0; i < dk; ++i) u += S[(size_t)r * dk + i] * kn[i];
@@ -265,6 +280,24 @@ int oracle_num_threads(void) {
   return c > 0 ? (int)c : 1;
 }
 
+/* runs every chain of the job on nthreads workers (<= 0: all online cores) */
+static void run_chains(rec_job* J, int nthreads) {
+  J->next = 0;
+  pthread_mutex_init(&J->lock, NULL);
+  if (nthreads <= 0) nthreads = oracle_num_threads();
+  const long work = (long)J->N * (J->heads ? J->nheads : J->hv);
+  if (nthreads > work) nthreads = work > 0 ? (int)work : 1;
+  if (nthreads <= 1) {
+    rec_worker(J);
+  } else {
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+    for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, rec_worker, J);
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    free(th);
+  }
+  pthread_mutex_destroy(&J->lock);
+}
+
 /*
  * The gated delta rule over packed variable-length sequences (one chain per (sequence, V head)).
  * qkv:      [T, 2*hk*dk + hv*dv] bf16 conv output: q heads, then k heads, then v heads
@@ -285,23 +318,35 @@ int oracle_gdn_recurrence(int hk, int hv, int dk, int dv, int T, const uint16_t*
     if (cu_seqlens[n + 1] < cu_seqlens[n]) return 2;
   rec_job J;
   J.hk = hk; J.hv = hv; J.dk = dk; J.dv = dv;
-  J.qkv = qkv; J.g = g; J.beta = beta; J.cu = cu_seqlens; J.N = N;
+  J.qkv = qkv; J.g = g; J.gk = NULL; J.g_min = 0.0; J.beta = beta; J.cu = cu_seqlens; J.N = N;
   J.q_scale = q_scale; J.l2_eps = l2_eps;
   J.state_in = state_in; J.o = o; J.state_out = state_out;
-  J.heads = heads; J.nheads = nheads; J.mutation = mutation; J.next = 0;
-  pthread_mutex_init(&J.lock, NULL);
-  if (nthreads <= 0) nthreads = oracle_num_threads();
-  const long work = (long)N * (heads ? nheads : hv);
-  if (nthreads > work) nthreads = work > 0 ? (int)work : 1;
-  if (nthreads <= 1) {
-    rec_worker(&J);
-  } else {
-    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
-    for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, rec_worker, &J);
-    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
-    free(th);
-  }
-  pthread_mutex_destroy(&J.lock);
+  J.heads = heads; J.nheads = nheads; J.mutation = mutation;
+  run_chains(&J, nthreads);
+  return 0;
+}
+
+/*
+ * The KDA recurrence over packed variable-length sequences: as oracle_gdn_recurrence, with
+ * g: [T, hv, dk] fp32, a log decay per key channel, applied as exp(max(g, g_min)) to the key
+ * columns of the [value, key] state (g_min = -inf: no clamp).
+ */
+int oracle_kda_recurrence(int hk, int hv, int dk, int dv, int T, const uint16_t* qkv,
+                          const float* g, double g_min, const float* beta,
+                          const int32_t* cu_seqlens, int N, double q_scale, double l2_eps,
+                          const double* state_in, double* o, double* state_out,
+                          const int32_t* heads, int nheads, int nthreads, int mutation) {
+  if (hk <= 0 || hv <= 0 || dk <= 0 || dv <= 0 || hv % hk != 0 || N < 0) return 1;
+  if (cu_seqlens[0] != 0 || cu_seqlens[N] != T) return 2;
+  for (int n = 0; n < N; ++n)
+    if (cu_seqlens[n + 1] < cu_seqlens[n]) return 2;
+  rec_job J;
+  J.hk = hk; J.hv = hv; J.dk = dk; J.dv = dv;
+  J.qkv = qkv; J.g = NULL; J.gk = g; J.g_min = g_min; J.beta = beta; J.cu = cu_seqlens; J.N = N;
+  J.q_scale = q_scale; J.l2_eps = l2_eps;
+  J.state_in = state_in; J.o = o; J.state_out = state_out;
+  J.heads = heads; J.nheads = nheads; J.mutation = mutation;
+  run_chains(&J, nthreads);
   return 0;
 }
 

@@ -49,3 +49,39 @@ def chunked_chain(q, k, v, g, beta, S0, q_scale, chunk=64):
         O[sl] = q_scale * ((np.exp(gam)[:, None] * Q) @ S.T + P @ E)
         S = np.exp(gam[-1]) * S + E.T @ (np.exp(gam[-1] - gam)[:, None] * K)
     return O, S
+
+
+def chunked_chain_kda(q, k, v, g, beta, S0, q_scale, chunk=64):
+    """The same chunk-wise form with a per-key-channel log decay (KDA).
+
+    q, k: [T, Dk] (L2-normalised); v: [T, Dv]; g: [T, Dk] (already clamped); beta: [T];
+    S0: [Dv, Dk].  Within a chunk, Gamma_t = sum_{i<=t} g_i is a vector over the key channels and
+    every decay between tokens j <= t is the per-channel factor exp(Gamma_t - Gamma_j), taken
+    from the difference directly (never as a product of exp(Gamma_t) and exp(-Gamma_j), which
+    leaves the range of doubles over a long chunk):
+      A[t, j] = beta_t sum_i k_ti k_ji exp(Gamma_ti - Gamma_ji)       (j < t)
+      U = T diag(beta) V,   W = T diag(beta) (K * exp(Gamma)),   E = U - W S0^T
+      P[t, j] = sum_i q_ti k_ji exp(Gamma_ti - Gamma_ji)              (j <= t)
+      O = q_scale [(Q * exp(Gamma)) S0^T + P E]
+      S_L = S0 diag(exp(Gamma_L)) + E^T (K * exp(Gamma_L - Gamma))
+    """
+    T = q.shape[0]
+    S = S0.astype(np.float64).copy()
+    O = np.zeros((T, v.shape[1]))
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(T, c0 + chunk))
+        Q, K, V, G, B = q[sl], k[sl], v[sl], g[sl], beta[sl]
+        L = Q.shape[0]
+        gam = np.cumsum(G, axis=0)                                  # [L, Dk]
+        lower_incl = np.tril(np.ones((L, L)), 0) > 0
+        diff = np.where(lower_incl[:, :, None], gam[:, None, :] - gam[None, :, :], -np.inf)
+        decay = np.exp(diff)                                        # [t, j, i]
+        A = B[:, None] * np.einsum("ti,ji,tji->tj", K, K, decay) * np.tril(np.ones((L, L)), -1)
+        Tm = solve_triangular(np.eye(L) + A, np.eye(L), lower=True, unit_diagonal=True)
+        U = Tm @ (B[:, None] * V)
+        W = Tm @ (B[:, None] * K * np.exp(gam))
+        E = U - W @ S.T
+        P = np.einsum("ti,ji,tji->tj", Q, K, decay)
+        O[sl] = q_scale * ((Q * np.exp(gam)) @ S.T + P @ E)
+        S = S * np.exp(gam[-1])[None, :] + E.T @ (K * np.exp(gam[-1][None, :] - gam))
+    return O, S

@@ -16,8 +16,9 @@ import torch
 import torch.nn.functional as F
 
 import oracle
-from linear_attention_ssm_gb300.synth import Geometry, prefill_inputs, decode_inputs, cu_seqlens_of
-from tests.chunked_numpy import chunked_chain, l2n
+from linear_attention_ssm_gb300.synth import (Geometry, prefill_inputs, decode_inputs, cu_seqlens_of,
+                                              kda_prefill_inputs)
+from tests.chunked_numpy import chunked_chain, chunked_chain_kda, l2n
 
 SMALL = Geometry(num_k_heads=2, num_v_heads=6, head_k_dim=8, head_v_dim=4, conv_width=4)
 
@@ -658,3 +659,106 @@ def test_kda_planted_mutations_change_the_result(mut):
     base = oracle.kda_decode_step(*args, **a)
     bad = oracle.kda_decode_step(*args, mutation=mut, **a)
     assert (base[0] - bad[0]).abs().max() > 1e-3 or (base[3] - bad[3]).abs().max() > 1e-3
+
+
+# ------------------------------------------------------------------ KDA prefill (sequential form)
+
+def _geo_args(geo):
+    return (geo.num_k_heads, geo.num_v_heads, geo.head_k_dim, geo.head_v_dim)
+
+
+def test_kda_recurrence_with_a_channel_constant_decay_is_the_gdn_recurrence():
+    """Ragged sequences, 3 V heads per K head: a decay equal on every key channel reproduces the
+    scalar-decay recurrence exactly."""
+    geo = SMALL
+    inp = prefill_inputs([7, 1, 12], seed=60, geo=geo, random_conv_state=True)
+    T = sum(inp["lengths"])
+    g_vec = inp["g"][:, :, None].expand(T, geo.num_v_heads, geo.head_k_dim).contiguous()
+    common = (inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    tail = (inp["beta"], inp["z"], inp["norm_w"], *_geo_args(geo), 0.3)
+    kda = oracle.kda_prefill(*common, g_vec, *tail, state_in=inp["state0"], conv_state_in=inp["conv_state0"])
+    gdn = oracle.prefill(*common, inp["g"], *tail, state_in=inp["state0"], conv_state_in=inp["conv_state0"])
+    for key in ("o", "out", "state"):
+        assert torch.equal(kda[key], gdn[key]), key
+
+
+@pytest.mark.parametrize("g_min", [float("-inf"), -1.0])
+def test_kda_prefill_equals_consecutive_kda_decode_steps(g_min):
+    """Per sequence, the prefill (conv over the packed rows, token chain) and one KDA decode step
+    per token (conv shift register, the decode oracle's own step) give the same outputs and final
+    states; the clamp enters both."""
+    geo = Geometry(num_k_heads=2, num_v_heads=4, head_k_dim=8, head_v_dim=6, conv_width=4)
+    lengths = [5, 1, 3]
+    inp = kda_prefill_inputs(lengths, seed=61, geo=geo, random_conv_state=True)
+    qs = 0.4
+    pre = oracle.kda_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"], inp["g"], inp["beta"], inp["z"],
+                             inp["norm_w"], *_geo_args(geo), qs, g_min=g_min, state_in=inp["state0"],
+                             conv_state_in=inp["conv_state0"])
+    a = dict(num_k_heads=geo.num_k_heads, num_v_heads=geo.num_v_heads, head_k_dim=geo.head_k_dim,
+             head_v_dim=geo.head_v_dim, q_scale=qs, g_min=g_min)
+    cu = inp["cu_seqlens"].tolist()
+    for n in range(len(lengths)):
+        cs, st = inp["conv_state0"][n:n + 1], inp["state0"][n:n + 1].double()
+        for t in range(cu[n], cu[n + 1]):
+            out, _, cs, st = oracle.kda_decode_step(inp["x"][t:t + 1], inp["conv_w"], cs, inp["g"][t:t + 1],
+                                                    inp["beta"][t:t + 1], st, inp["z"][t:t + 1], inp["norm_w"], **a)
+            np.testing.assert_allclose(out[0].numpy(), pre["out"][t].numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(st[0].numpy(), pre["state"][n].numpy(), rtol=1e-10, atol=1e-13)
+        assert torch.equal(cs[0].view(torch.int16), pre["conv_state"][n].view(torch.int16))
+
+
+def test_kda_recurrence_matches_the_matrix_product_form():
+    """numpy, token by token, in the product form S_t = S_{t-1} diag(alpha_t) (I - beta k k^T) +
+    beta v k^T with alpha_t = exp(max(g_t, g_min)) over the key channels; o_t = q_scale S_t q_t.
+    Dk != Dv, so a decay on the value rows instead of the key columns cannot pass."""
+    dk, dv, L, g_min, qs = 8, 5, 9, -1.5, 0.7
+    gen = torch.Generator().manual_seed(62)
+    qkv = torch.randn(L, 2 * dk + dv, generator=gen).to(torch.bfloat16)
+    g = -4 * torch.rand(L, 1, dk, generator=gen)
+    beta = torch.rand(L, 1, generator=gen)
+    S0 = torch.randn(1, 1, dv, dk, generator=gen)
+    o, st = oracle.kda_recurrence(qkv, g, beta, [0, L], 1, 1, dk, dv, qs, g_min, 1e-6, S0)
+    y = qkv.double().numpy()
+    S = S0[0, 0].double().numpy()
+    for t in range(L):
+        q, k, v = l2n(y[t, :dk], 1e-6), l2n(y[t, dk:2 * dk], 1e-6), y[t, 2 * dk:]
+        alpha = np.exp(np.maximum(g[t, 0].double().numpy(), g_min))
+        b = float(beta[t, 0])
+        S = S @ np.diag(alpha) @ (np.eye(dk) - b * np.outer(k, k)) + b * np.outer(v, k)
+        np.testing.assert_allclose(o[t, 0].numpy(), qs * S @ q, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(st[0, 0].numpy(), S, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 130])
+def test_kda_sequential_oracle_equals_chunked_wy_form(L):
+    """The ledger's KDA prefill boundary (63/64/65 tokens around a 64-token chunk): the token
+    chain and the per-channel chunk-wise form agree in output and final state."""
+    geo = Geometry(num_k_heads=1, num_v_heads=2, head_k_dim=128, head_v_dim=64, conv_width=4)
+    inp = kda_prefill_inputs([L], seed=200 + L, geo=geo)
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    qs = geo.q_scale
+    o, st = oracle.kda_recurrence(y, inp["g"], inp["beta"], [0, L], *_geo_args(geo), qs, state_in=inp["state0"])
+    q, k, v = _expand_qkv(y, geo)
+    for h in range(2):
+        O, S = chunked_chain_kda(l2n(q[:, 0], 1e-6), l2n(k[:, 0], 1e-6), v[:, h], inp["g"][:, h].double().numpy(),
+                                 inp["beta"][:, h].double().numpy(), inp["state0"][0, h].double().numpy(), qs)
+        np.testing.assert_allclose(o[:, h].numpy(), O, rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(st[0, h].numpy(), S, rtol=1e-9, atol=1e-11)
+
+
+@pytest.mark.parametrize("mut", [oracle.MUT_DECAY_SIGN, oracle.MUT_NO_BETA, oracle.MUT_TRANSPOSE,
+                                 oracle.MUT_DROP_CARRY])
+def test_kda_recurrence_planted_mutations_fail_the_chunked_form(mut):
+    """A wrong decay sign, a missing beta, a transposed state or a dropped carry in the oracle's
+    KDA chain is caught by the chunked form."""
+    geo = Geometry(num_k_heads=1, num_v_heads=1, head_k_dim=16, head_v_dim=16, conv_width=4)
+    L = 70
+    inp = kda_prefill_inputs([L], seed=63, geo=geo)
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    o, st = oracle.kda_recurrence(y, inp["g"], inp["beta"], [0, L], *_geo_args(geo), 0.5,
+                                  state_in=inp["state0"], mutation=mut)
+    q, k, v = _expand_qkv(y, geo)
+    O, S = chunked_chain_kda(l2n(q[:, 0], 1e-6), l2n(k[:, 0], 1e-6), v[:, 0], inp["g"][:, 0].double().numpy(),
+                             inp["beta"][:, 0].double().numpy(), inp["state0"][0, 0].double().numpy(), 0.5)
+    assert np.abs(o[:, 0].numpy() - O).max() > 1e-3 or np.abs(st[0, 0].numpy() - S).max() > 1e-3
+

@@ -318,6 +318,68 @@ def time_kda_decode(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_
                          "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms}}
 
 
+# Flops of one token of one head in the KDA recurrence's sequential form, per state element: the
+# decayed-key dot (2), the update a s + e k (3) and the query dot (2).
+KDA_FLOPS_PER_ELEMENT = 7
+SM_MAX_HZ = 2.07e9  # maximum SM clock of the part
+FP32_LANES_PER_SM = 128
+
+
+def time_kda_prefill(args, gdn, dev, stream, barrier, max_over_ranks, world):
+    """KDA prefill on the pages' 64-head geometry, 4 sequences x 4096 tokens: conv1d, then the KDA
+    recurrence with the gated RMSNorm fused (both kernels timed with events, and the recurrence
+    alone for its roofline).  x alone is 805 MB per step, larger than L2."""
+    import torch
+    from linear_attention_ssm_gb300.synth import KDA_GEO, kda_prefill_inputs
+    geo, lengths = KDA_GEO, [4096] * 4
+    T = sum(lengths)
+    d = kda_prefill_inputs(lengths, seed=11, geo=geo)
+    x, cu, g, beta, z = (d[k].to(dev) for k in ("x", "cu_seqlens", "g", "beta", "z"))
+    w, nw, st0 = d["conv_w"].to(dev), d["norm_w"].to(dev), d["state0"].to(dev)
+    del d
+    st = torch.empty_like(st0)
+    qkv = torch.empty((T, geo.conv_dim), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, geo.num_v_heads, 128), dtype=torch.bfloat16, device=dev)
+    qs = geo.q_scale
+
+    def whole():
+        gdn.gdn_kda_prefill(x, w, cu, g, beta, z, nw, qs, state_in=st0, state_out=st, qkv_buf=qkv, out=out,
+                            geometry=geo)
+
+    def recurrence():
+        gdn.gdn_kda_recurrence(qkv, g, beta, cu, qs, state_in=st0, state_out=st, z=z, norm_w=nw, out=out,
+                               geometry=geo)
+
+    n = 5
+    timed = {}
+    for name, fn in (("whole", whole), ("recurrence", recurrence)):
+        for _ in range(max(args.warmup, 1)):
+            fn()
+        barrier()
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(n):
+            fn()
+        e0.record(stream)
+        torch.cuda.synchronize()
+        gdn.gdn_check_device_errors()
+        timed[name] = max_over_ranks(s0.elapsed_time(e0)) / n
+    del x, cu, g, beta, z, st0, st, qkv, out
+    torch.cuda.empty_cache()
+    flops = T * geo.num_v_heads * KDA_FLOPS_PER_ELEMENT * 128 * 128
+    achieved = flops / (timed["recurrence"] / 1e3) / 1e12
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = sms * FP32_LANES_PER_SM * 2 * SM_MAX_HZ / 1e12
+    return {"metric": "KDA prefill tokens/s", "value": world * T / (timed["whole"] / 1e3), "unit": "tokens/s",
+            "ms_per_step": timed["whole"], "steps": n,
+            "workload": "KDA prefill, 4 sequences x 4096 tokens, 64 heads x 128 (q, k, v), per-channel decay, "
+                        "conv1d -> sequential KDA recurrence -> sigmoid-gated RMSNorm",
+            "roofline": {"kernel": "kda_prefill_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "algorithmic_flops_per_launch": flops, "avg_launch_ms": timed["recurrence"],
+                         "peak_source": "fp32 CUDA cores: SMs x 128 lanes x 2 flops x 2070 MHz (nominal)"}}
+
+
 VERIFY_ROWS = 8
 VERIFY_RECORD = 53440  # stash bytes per (sequence, row): raw inputs, keys, deltas, g
 
@@ -656,6 +718,12 @@ def run_ours(args, rank, world, local):
     verify = time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak)
     verify_f16 = time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak, torch.float16)
 
+    # ---------------- KDA prefill: conv1d, then the KDA recurrence (per-channel decay), 4 x 4096 tokens
+    try:
+        kda_prefill = time_kda_prefill(args, gdn, dev, stream, barrier, max_over_ranks, world)
+    except Exception as exc:  # a secondary leg reports its failure without taking the line down
+        kda_prefill = {"error": f"{type(exc).__name__}: {exc}"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         tps, cores, desc = cpu_oracle_sample(inp, 160)
@@ -676,7 +744,7 @@ def run_ours(args, rank, world, local):
                     "pipelined": "H2D of step i+1 and D2H of step i-1 overlap the prefill of step i"},
             "decode": decode, "decode_fp16_state": decode_f16, "decode_kda": decode_kda, "verify": verify,
             "verify_fp16_state": verify_f16,
-            "gates": gates,
+            "gates": gates, "kda_prefill": kda_prefill,
             "varlen": varlen, "cpu_baseline": cpu, "clocks": clk,
             # per step: conv1d + conv-state kernels, the chunk prefill's schedule and segment-table
             # kernels, then a prep and a state kernel for each of its three chunk segments

@@ -316,6 +316,33 @@ GDN_API gdn_status gdn_kda_decode_step(const gdn_geometry* geo, const gdn_bf16* 
                                        float l2_eps, float rms_eps, gdn_bf16* out, int32_t batch,
                                        void* stream);
 
+/*
+ * The KDA recurrence over packed variable-length sequences (the prefill's recurrent leg),
+ * optionally fused with the sigmoid-gated RMSNorm: the step of gdn_kda_decode_step applied to
+ * every token in order, each (sequence, V head) state carried from token to token.
+ * GLM-5.3-Flash kernel TDD ledger, slices I2 (FP32 [value, key] state, clamped and exponentiated
+ * per-channel decay, separate q output scale), I2a (q/k normalised x / sqrt(sum x^2 + eps)) and
+ * I4 (the prefill matches the sequential state and output at every length).  This is the
+ * sequential form: one CTA per (V head, sequence) walks the tokens, so a call's time grows with
+ * its longest sequence.
+ *   qkv        [total_tokens, C] bf16 conv output (gdn_conv1d_prefill's y): q heads | k heads | v heads
+ *   g          [total_tokens, Hv, Dk] fp32 per-channel log decay (16-byte aligned)
+ *   g_min      the clamp: decays below exp(g_min) are raised to it (-INFINITY: no clamp; NaN is rejected)
+ *   beta       [total_tokens, Hv] fp32 write strength (4-byte aligned)
+ *   cu_seqlens [num_seqs + 1] int32 (device), as for gdn_conv1d_prefill; num_seqs <= 65535.
+ *              Contents that are not nondecreasing within [0, total_tokens] set
+ *              GDN_ERR_DEVICE_ARGUMENT in the device error word; those sequences are not computed.
+ *   q_scale, l2_eps, state_in, state_out, z, norm_w, rms_eps, out: as gdn_chunk_prefill (fp32
+ *              states [num_seqs, Hv, Dv, Dk]; state_out may be state_in; a sequence of length 0
+ *              copies its state).  No workspace.
+ */
+GDN_API gdn_status gdn_kda_recurrence(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g,
+                                      float g_min, const float* beta, const int32_t* cu_seqlens,
+                                      int32_t num_seqs, int32_t total_tokens, float q_scale,
+                                      float l2_eps, const float* state_in, float* state_out,
+                                      const gdn_bf16* z, const gdn_bf16* norm_w, float rms_eps,
+                                      gdn_bf16* out, void* stream);
+
 /* Capacity of the fixed scratch used by gdn_chunk_prefill_noalloc. */
 #define GDN_NOALLOC_MAX_SEQS 16384
 #define GDN_NOALLOC_SCRATCH_BYTES (256 + 4 * GDN_NOALLOC_MAX_SEQS) /* 65,792 bytes */

@@ -21,6 +21,8 @@ from .binding import (  # noqa: F401
     gdn_gated_rmsnorm,
     gdn_gates,
     gdn_kda_decode_step,
+    gdn_kda_prefill,
+    gdn_kda_recurrence,
     gdn_prefill,
     gdn_verify,
     gdn_verify_commit,

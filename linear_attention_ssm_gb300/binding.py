@@ -62,6 +62,7 @@ def load_library():
             "gdn_decode_step_fp16_state": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
             "gdn_gates": ([G, P, P, P, P, P, P, I, P], ctypes.c_int),
             "gdn_kda_decode_step": ([G, P, P, P, P, F, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
+            "gdn_kda_recurrence": ([G, P, P, F, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
             "gdn_verify_stash_size": ([G, I, I], S),
             "gdn_verify": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, I, P, S, P], ctypes.c_int),
             "gdn_verify_commit": ([G, P, P, P, P, I, I, P], ctypes.c_int),
@@ -256,6 +257,36 @@ def gdn_kda_decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scal
     return out
 
 
+def gdn_kda_recurrence(qkv, g, beta, cu_seqlens, q_scale, g_min=float("-inf"), l2_eps=1e-6, state_in=None,
+                       state_out=None, z=None, norm_w=None, rms_eps=1e-6, out=None,
+                       geometry: Geometry = QWEN_GDN, stream=None):
+    """The KDA recurrence over packed sequences, token by token (g [T, Hv, Dk] fp32 per-channel log
+    decay, clamped below at g_min), optionally fused with the gated RMSNorm when z is given.
+
+    Returns out [T, Hv, Dv] bf16 (o itself when z is None).  state_out, when given, receives the
+    final fp32 states [N, Hv, Dv, Dk]; it may be state_in itself.
+    """
+    lib = load_library()
+    C, hv, dv, dk = geometry.conv_dim, geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
+    N = cu_seqlens.numel() - 1
+    T = qkv.shape[0]
+    _dev(qkv, torch.bfloat16, "qkv", (T, C))
+    _dev(g, torch.float32, "g", (T, hv, dk))
+    _dev(beta, torch.float32, "beta", (T, hv))
+    _dev(cu_seqlens, torch.int32, "cu_seqlens", (N + 1,))
+    _dev(state_in, torch.float32, "state_in", (N, hv, dv, dk))
+    _dev(state_out, torch.float32, "state_out", (N, hv, dv, dk))
+    _dev(z, torch.bfloat16, "z", (T, hv, dv))
+    _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
+    if out is None:
+        out = torch.empty((T, hv, dv), dtype=torch.bfloat16, device=qkv.device)
+    _dev(out, torch.bfloat16, "out", (T, hv, dv))
+    _check(lib.gdn_kda_recurrence(_geo(geometry), _p(qkv), _p(g), float(g_min), _p(beta), _p(cu_seqlens), N, T,
+                                  float(q_scale), float(l2_eps), _p(state_in), _p(state_out), _p(z), _p(norm_w),
+                                  float(rms_eps), _p(out), _stream(stream)))
+    return out
+
+
 def gdn_decode_step_fp16_state(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps=1e-6,
                                rms_eps=1e-6, out=None, geometry: Geometry = QWEN_GDN, stream=None):
     """gdn_decode_step on an fp16 (binary16) recurrent state [B, Hv, Dv, Dk], updated in place."""
@@ -392,3 +423,14 @@ def gdn_prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, q_scale, l2_eps=1e-6,
                              geometry=geometry, stream=stream)
     return gdn_chunk_prefill(qkv, g, beta, cu_seqlens, q_scale, l2_eps, state_in, state_out, z,
                              norm_w, rms_eps, out, geometry=geometry, stream=stream)
+
+
+def gdn_kda_prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, q_scale, g_min=float("-inf"), l2_eps=1e-6,
+                    rms_eps=1e-6, state_in=None, state_out=None, conv_state_in=None, conv_state_out=None,
+                    qkv_buf=None, out=None, geometry: Geometry = QWEN_GDN, stream=None):
+    """The KDA prefill: gdn_conv1d_prefill, then gdn_kda_recurrence with the gated RMSNorm fused.
+    Returns out [T, Hv, Dv] bf16."""
+    qkv = gdn_conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in, conv_state_out, qkv_buf,
+                             geometry=geometry, stream=stream)
+    return gdn_kda_recurrence(qkv, g, beta, cu_seqlens, q_scale, g_min, l2_eps, state_in, state_out, z,
+                              norm_w, rms_eps, out, geometry=geometry, stream=stream)

@@ -30,6 +30,15 @@ cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const ui
                                bool fp16_state, const uint16_t* z, const uint16_t* norm_w, float q_scale,
                                float l2_eps, float rms_eps, uint16_t* out, int B, int Hk, int Hv);
 
+// The KDA recurrence over packed sequences (kda_prefill.cu): qkv is the conv output [T, C], g the
+// per-channel log decay [T, Hv, Dk], clamped below at g_min; out receives the gated RMSNorm of o
+// (o itself when z is NULL); state_out may be state_in.
+size_t kda_prefill_smem_bytes();
+cudaError_t launch_kda_prefill(const LaunchEnv& env, const uint16_t* qkv, const float* g, float g_min,
+                               const float* beta, const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale,
+                               float l2_eps, const float* state_in, float* state_out, const uint16_t* z,
+                               const uint16_t* norm_w, float rms_eps, uint16_t* out);
+
 // Multi-token verify (verify.cu): K rows per sequence, the state read only; the commit folds an
 // accepted prefix of rows into the recurrent and conv states.
 constexpr int kMaxVerifyRows = 17;

@@ -192,3 +192,29 @@ def test_kda_decode_rejects_bad_arguments(lib):
     assert lib.gdn_kda_decode_step(geo, FAKE, FAKE, FAKE, ODD, -1.0, FAKE, *tail, 4, None) == 3
     assert lib.gdn_kda_decode_step(geo, None, None, None, None, -1.0, None, None, None, None, 0.088, 1e-6,
                                    1e-6, None, 0, None) == 0
+
+
+def test_kda_recurrence_rejects_bad_arguments(lib):
+    geo = _geo(num_k_heads=64, num_v_heads=64)
+
+    def call(qkv=FAKE, g=FAKE, g_min=-1.0, beta=FAKE, cu=FAKE, N=2, T=8, state_in=None, state_out=None, z=None,
+             norm_w=None, out=FAKE, l2=1e-6):
+        return lib.gdn_kda_recurrence(geo, qkv, g, g_min, beta, cu, N, T, 0.088, l2, state_in, state_out, z,
+                                      norm_w, 1e-6, out, None)
+
+    assert call(N=-1) == 1
+    assert call(N=0, T=4) == 1
+    assert call(N=70000) == 1                      # the grid's sequence dimension
+    assert call(cu=None) == 1
+    assert call(g=None) == 1
+    assert call(beta=None) == 1
+    assert call(g_min=float("nan")) == 1
+    assert call(l2=-1.0) == 1
+    assert call(z=FAKE, norm_w=None) == 1
+    assert call(g=ODD) == 3
+    assert call(qkv=ODD) == 3
+    assert call(state_in=ODD) == 3
+    assert call(state_in=FAKE, state_out=ctypes.c_void_p(0x10000 + 4096)) == 1   # partial overlap
+    assert lib.gdn_kda_recurrence(_geo(head_k_dim=64), FAKE, FAKE, -1.0, FAKE, FAKE, 1, 4, 0.088, 1e-6, None,
+                                  None, None, None, 1e-6, FAKE, None) == 2
+    assert call(N=0, T=0, qkv=None, g=None, beta=None, cu=None, out=None) == 0

@@ -12,10 +12,13 @@
 // One CTA per (V head, sequence).  Warp w holds value rows 16w .. 16w + 15 of the head's state and
 // lane l the key columns 4l .. 4l + 3 of each row, so both contractions of a token (S k and S q)
 // are warp-shuffle reductions and no step of a token waits for another warp: the arithmetic of a
-// token is that of the KDA decode kernel.  The token inputs (q and k of the K head, v, z, the
-// per-channel decay and beta of the V head) are staged in shared memory 16 tokens at a time by
-// asynchronous copies, double-buffered so that the next block streams in while this one is
-// computed; the block's fp32 outputs are then normalised by all eight warps together.
+// token is that of the KDA decode kernel up to the order of the four-term sums in each lane.  The
+// token inputs (q and k of the K head, v, z, the per-channel decay and beta of the V head) are
+// staged in shared memory 16 tokens at a time by asynchronous copies, double-buffered so that the
+// next block streams in while this one is computed.  What does not depend on the state -- each token's normalised q and k and its
+// per-channel decay factors -- is formed once per block by all eight warps together (a token per
+// warp), so the chain from one token to the next holds only the state's own work; the block's
+// fp32 outputs are likewise normalised by all warps together at the end of the block.
 //
 // This is the sequential form: per token it does O(Dv Dk) CUDA-core work on every head, so it is
 // bound by instruction issue, not by memory.
@@ -45,7 +48,9 @@ struct Stage {
 
 struct Smem {
   Stage st[2];
-  float o[kBlockTokens][kHeadDim];  // q_scale S q of the block's tokens, before the norm
+  float qn[kBlockTokens][kHeadDim];  // the block's normalised q
+  float kn[kBlockTokens][kHeadDim];  // the block's normalised k
+  float o[kBlockTokens][kHeadDim];   // q_scale S q of the block's tokens, before the norm
 };
 static_assert(sizeof(Stage) % 16 == 0, "stage buffers must stay 16-byte aligned");
 
@@ -75,6 +80,13 @@ __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
     c2[k] = (h4 ? b4[2 + k] : b4[k]) + __shfl_xor_sync(0xffffffffu, h4 ? b4[k] : b4[2 + k], 4);
   const float s = (h2 ? c2[1] : c2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? c2[0] : c2[1], 2);
   return s + __shfl_xor_sync(0xffffffffu, s, 1);
+}
+
+// a.x b.x + a.y b.y + a.z b.z + a.w b.w as two f32x2 products summed pairwise
+__device__ __forceinline__ float dot4(const float4 a, const float4 b) {
+  const float2 p = __ffma2_rn(make_float2(a.z, a.w), make_float2(b.z, b.w),
+                              __fmul2_rn(make_float2(a.x, a.y), make_float2(b.x, b.y)));
+  return p.x + p.y;
 }
 
 __device__ __forceinline__ float4 bf16x4(uint2 u) {
@@ -160,30 +172,42 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(
     cp_async_wait_all_but_one();  // this block's copies (every group but the one just issued)
     __syncthreads();
 
-    for (int tt = 0; tt < nt; ++tt) {
-      // L2 norms of q and k: x / sqrt(sum x^2 + eps), summed as the decode kernel sums them
-      const float4 q4 = bf16x4(*reinterpret_cast<const uint2*>(&cur.q[tt][lane * 4]));
-      const float4 k4 = bf16x4(*reinterpret_cast<const uint2*>(&cur.k[tt][lane * 4]));
-      float sq = 0.f, sk = 0.f;
-      sq = fmaf(q4.x, q4.x, sq); sq = fmaf(q4.y, q4.y, sq); sq = fmaf(q4.z, q4.z, sq); sq = fmaf(q4.w, q4.w, sq);
-      sk = fmaf(k4.x, k4.x, sk); sk = fmaf(k4.y, k4.y, sk); sk = fmaf(k4.z, k4.z, sk); sk = fmaf(k4.w, k4.w, sk);
+    // ---- the state-independent quantities of the block's tokens, a token per warp: q and k
+    // normalised as x / sqrt(sum x^2 + eps), and the decay factors exp(max(g, g_min)) in place of g
+    {
+      Stage& cw = sm.st[bi & 1];
+      for (int tt = warp; tt < nt; tt += kWarps) {
+        const float4 q4 = bf16x4(*reinterpret_cast<const uint2*>(&cw.q[tt][lane * 4]));
+        const float4 k4 = bf16x4(*reinterpret_cast<const uint2*>(&cw.k[tt][lane * 4]));
+        float sq = 0.f, sk = 0.f;
+        sq = fmaf(q4.x, q4.x, sq); sq = fmaf(q4.y, q4.y, sq); sq = fmaf(q4.z, q4.z, sq); sq = fmaf(q4.w, q4.w, sq);
+        sk = fmaf(k4.x, k4.x, sk); sk = fmaf(k4.y, k4.y, sk); sk = fmaf(k4.z, k4.z, sk); sk = fmaf(k4.w, k4.w, sk);
 #pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) {
-        sq += __shfl_xor_sync(0xffffffffu, sq, m);
-        sk += __shfl_xor_sync(0xffffffffu, sk, m);
+        for (int m = 16; m >= 1; m >>= 1) {
+          sq += __shfl_xor_sync(0xffffffffu, sq, m);
+          sk += __shfl_xor_sync(0xffffffffu, sk, m);
+        }
+        const float iq = rsqrtf(sq + l2_eps), ik = rsqrtf(sk + l2_eps);
+        *reinterpret_cast<float4*>(&sm.qn[tt][lane * 4]) = make_float4(q4.x * iq, q4.y * iq, q4.z * iq, q4.w * iq);
+        *reinterpret_cast<float4*>(&sm.kn[tt][lane * 4]) = make_float4(k4.x * ik, k4.y * ik, k4.z * ik, k4.w * ik);
+        const float4 gv = *reinterpret_cast<const float4*>(&cw.g[tt][lane * 4]);
+        *reinterpret_cast<float4*>(&cw.g[tt][lane * 4]) =
+            make_float4(expf(fmaxf(gv.x, g_min)), expf(fmaxf(gv.y, g_min)), expf(fmaxf(gv.z, g_min)),
+                        expf(fmaxf(gv.w, g_min)));
       }
-      const float iq = rsqrtf(sq + l2_eps), ik = rsqrtf(sk + l2_eps);
-      const float4 qn = make_float4(q4.x * iq, q4.y * iq, q4.z * iq, q4.w * iq);
-      const float4 kn = make_float4(k4.x * ik, k4.y * ik, k4.z * ik, k4.w * ik);
+    }
+    __syncthreads();
+
+    for (int tt = 0; tt < nt; ++tt) {
+      const float4 qn = *reinterpret_cast<const float4*>(&sm.qn[tt][lane * 4]);
+      const float4 kn = *reinterpret_cast<const float4*>(&sm.kn[tt][lane * 4]);
       // the decay of this lane's four key channels, and the key they multiply: (S diag(a)) k = S (a k)
-      const float4 gv = *reinterpret_cast<const float4*>(&cur.g[tt][lane * 4]);
-      const float4 a4 = make_float4(expf(fmaxf(gv.x, g_min)), expf(fmaxf(gv.y, g_min)), expf(fmaxf(gv.z, g_min)),
-                                    expf(fmaxf(gv.w, g_min)));
+      const float4 a4 = *reinterpret_cast<const float4*>(&cur.g[tt][lane * 4]);
       const float4 kd = make_float4(a4.x * kn.x, a4.y * kn.y, a4.z * kn.z, a4.w * kn.w);
       float d[kRowsPerWarp];
 #pragma unroll
       for (int i = 0; i < kRowsPerWarp; ++i)
-        d[i] = row[i].x * kd.x + row[i].y * kd.y + row[i].z * kd.z + row[i].w * kd.w;
+        d[i] = dot4(row[i], kd);
       const float dsum = warp_sum16(d, lane);
       const float e_mine = cur.beta[tt] * (bf2f(cur.v[tt][warp * kRowsPerWarp + i_mine]) - dsum);
       float o[kRowsPerWarp];
@@ -197,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(
         const float2 zw = __ffma2_rn(make_float2(a4.z, a4.w), make_float2(row[i].z, row[i].w),
                                      __fmul2_rn(e2, make_float2(kn.z, kn.w)));
         row[i] = make_float4(xy.x, xy.y, zw.x, zw.y);
-        o[i] = row[i].x * qn.x + row[i].y * qn.y + row[i].z * qn.z + row[i].w * qn.w;
+        o[i] = dot4(row[i], qn);
       }
       const float o_mine = warp_sum16(o, lane);
       if (!(lane & 1)) sm.o[tt][warp * kRowsPerWarp + i_mine] = q_scale * o_mine;

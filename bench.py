@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--profile-case", default=None,
                     help="run only the prefill (conv + chunk) on these comma-separated sequence lengths, "
                          "--steps times after --warmup, for profiling; prints one timing line")
+    ap.add_argument("--profile-kda-prefill", default=None, metavar="LENGTHS",
+                    help="run only the KDA prefill (conv + KDA recurrence, 64 heads x 128) on these "
+                         "comma-separated sequence lengths, --steps times after --warmup; prints one timing line")
     return ap.parse_args()
 
 
@@ -89,6 +92,39 @@ def run_profile_verify(args, local):
     torch.cuda.synchronize()
     gdn.gdn_check_device_errors()
     print(json.dumps({"profile_verify": B, "rows": K, "ms_per_transaction": e0.elapsed_time(e1) / max(args.steps, 1)}))
+
+
+def run_profile_kda_prefill(args, local):
+    """A KDA prefill workload for profilers: --warmup untimed calls, then --steps calls."""
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import linear_attention_ssm_gb300 as gdn
+    from linear_attention_ssm_gb300.synth import KDA_GEO, kda_prefill_inputs
+    lengths = [int(v) for v in args.profile_kda_prefill.split(",")]
+    geo, T = KDA_GEO, sum(lengths)
+    d = kda_prefill_inputs(lengths, seed=11, geo=geo)
+    x, cu, g, beta, z = (d[k].to(dev) for k in ("x", "cu_seqlens", "g", "beta", "z"))
+    w, nw, st0 = d["conv_w"].to(dev), d["norm_w"].to(dev), d["state0"].to(dev)
+    st = torch.empty_like(st0)
+    qkv = torch.empty_like(x)
+    out = torch.empty((T, geo.num_v_heads, 128), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        gdn.gdn_kda_prefill(x, w, cu, g, beta, z, nw, geo.q_scale, state_in=st0, state_out=st, qkv_buf=qkv, out=out,
+                            geometry=geo)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    gdn.gdn_check_device_errors()
+    print(json.dumps({"profile_kda_prefill": lengths, "tokens": T, "ms_per_step": e0.elapsed_time(e1) / max(args.steps, 1)}))
 
 
 def run_profile_case(args, local):
@@ -318,6 +354,22 @@ def time_kda_decode(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_
                          "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms}}
 
 
+def kda_prefill_bytes(tokens, seqs, hv):
+    """Algorithmic bytes of one KDA recurrence launch: per (token, V head) q, k, v, z (bf16 rows of
+    128), g (fp32 row of 128) and beta in, the bf16 output row out; per (sequence, V head) the fp32
+    state in and out."""
+    return tokens * hv * (4 * 256 + 512 + 4 + 256) + 2 * seqs * hv * 128 * 128 * 4
+
+
+def scaled_kda_traffic(algorithmic_bytes):
+    """The recorded DRAM traffic of the KDA recurrence, scaled from its captured workload to a
+    launch with these algorithmic bytes (None without a record for the current code)."""
+    rec = traffic_record("kda_prefill")
+    if not rec:
+        return None
+    return int(rec["bytes_per_launch"] * algorithmic_bytes / rec["algorithmic_bytes_per_launch"])
+
+
 # Flops of one token of one head in the KDA recurrence's sequential form, per state element: the
 # decayed-key dot (2), the update a s + e k (3) and the query dot (2).
 KDA_FLOPS_PER_ELEMENT = 7
@@ -370,12 +422,15 @@ def time_kda_prefill(args, gdn, dev, stream, barrier, max_over_ranks, world):
     achieved = flops / (timed["recurrence"] / 1e3) / 1e12
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     peak = sms * FP32_LANES_PER_SM * 2 * SM_MAX_HZ / 1e12
+    nbytes = kda_prefill_bytes(T, len(lengths), geo.num_v_heads)
     return {"metric": "KDA prefill tokens/s", "value": world * T / (timed["whole"] / 1e3), "unit": "tokens/s",
             "ms_per_step": timed["whole"], "steps": n,
             "workload": "KDA prefill, 4 sequences x 4096 tokens, 64 heads x 128 (q, k, v), per-channel decay, "
                         "conv1d -> sequential KDA recurrence -> sigmoid-gated RMSNorm",
             "roofline": {"kernel": "kda_prefill_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": scaled_kda_traffic(nbytes),
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "traffic_note": "ncu DRAM bytes of a 4 x 1024-token capture scaled by algorithmic bytes",
                          "algorithmic_flops_per_launch": flops, "avg_launch_ms": timed["recurrence"],
                          "peak_source": "fp32 CUDA cores: SMs x 128 lanes x 2 flops x 2070 MHz (nominal)"}}
 
@@ -763,6 +818,8 @@ def main():
         run_profile_verify(args, local)
     elif args.profile_case:
         run_profile_case(args, local)
+    elif args.profile_kda_prefill:
+        run_profile_kda_prefill(args, local)
     elif args.impl == "reference":
         run_reference(args, rank, world)
     else:

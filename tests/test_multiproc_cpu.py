@@ -57,3 +57,14 @@ def test_traffic_records_survive_comment_edits_only():
     assert bench.code_digest(code) == bench.code_digest("__global__ void k(float* a) {\n  a[0] = 1.f;\n}")
     assert bench.code_digest(code) != bench.code_digest(code.replace("1.f", "2.f"))
 
+
+
+def test_kda_prefill_traffic_scales_with_algorithmic_bytes():
+    """The recorded KDA recurrence traffic is reported at its own workload unchanged and scales
+    linearly with the algorithmic bytes (None once the kernel's code differs from the capture's)."""
+    rec = bench.traffic_record("kda_prefill")
+    if rec is None:
+        pytest.skip("no traffic record for the current kernel code")
+    assert bench.kda_prefill_bytes(4096, 4, 64) == rec["algorithmic_bytes_per_launch"]
+    assert bench.scaled_kda_traffic(rec["algorithmic_bytes_per_launch"]) == rec["bytes_per_launch"]
+    assert bench.scaled_kda_traffic(2 * rec["algorithmic_bytes_per_launch"]) == 2 * rec["bytes_per_launch"]

@@ -85,3 +85,53 @@ def chunked_chain_kda(q, k, v, g, beta, S0, q_scale, chunk=64):
         O[sl] = q_scale * ((Q * np.exp(gam)) @ S.T + P @ E)
         S = S * np.exp(gam[-1])[None, :] + E.T @ (K * np.exp(gam[-1][None, :] - gam))
     return O, S
+
+
+def kda_intra_chunk_weights(X, K, gam, sub=16, dtype=np.float32):
+    """M[t, j] = sum_i X_ti K_ji exp(Gamma_ti - Gamma_ji) for j <= t within one chunk, in `dtype`, formed
+    the way a tensor-core kernel can: 16-token sub-blocks; a diagonal sub-block takes each factor
+    exp(Gamma_ti - Gamma_ji) directly; an off-diagonal block (rows in sub-block a, columns in an
+    earlier sub-block b) is one product (X_a * exp(Gamma_a - Gamma_r)) (K_b * exp(Gamma_r - Gamma_b))^T
+    around r, the last token of sub-block b.  With g <= 0 every factor is a decay in (0, 1], so
+    nothing overflows however strong the decay; a factor that underflows stands for a term below
+    the precision of the sum.  Entries with j > t are zero."""
+    L = X.shape[0]
+    X, K, gam = X.astype(dtype), K.astype(dtype), gam.astype(dtype)
+    M = np.zeros((L, L), dtype=dtype)
+    for a0 in range(0, L, sub):
+        a1 = min(L, a0 + sub)
+        for t in range(a0, a1):  # the diagonal block, factor by factor
+            for j in range(a0, t + 1):
+                M[t, j] = np.sum(X[t] * K[j] * np.exp(gam[t] - gam[j]), dtype=dtype)
+        for b0 in range(0, a0, sub):
+            b1 = b0 + sub
+            r = b1 - 1
+            Xs = X[a0:a1] * np.exp(gam[a0:a1] - gam[r])
+            Ks = K[b0:b1] * np.exp(gam[r] - gam[b0:b1])
+            M[a0:a1, b0:b1] = Xs @ Ks.T
+    return M
+
+
+def chunked_chain_kda_fp32(q, k, v, g, beta, S0, q_scale, chunk=64, sub=16):
+    """chunked_chain_kda carried out in fp32 with the sub-block weights of kda_intra_chunk_weights:
+    the arithmetic precision and factorisation a chunked KDA kernel uses (fp32 state, fp32
+    products).  Every other decay factor is taken against the chunk's start or end, so it too is
+    at most 1: exp(Gamma_t) on Q and K, exp(Gamma_L - Gamma_t) on K in the state update."""
+    f = np.float32
+    T = q.shape[0]
+    S = S0.astype(f).copy()
+    O = np.zeros((T, v.shape[1]), dtype=f)
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(T, c0 + chunk))
+        Q, K, V, G, B = (a[sl].astype(f) for a in (q, k, v, g, beta))
+        L = Q.shape[0]
+        gam = np.cumsum(G, axis=0, dtype=f)
+        A = B[:, None] * kda_intra_chunk_weights(K, K, gam, sub) * np.tril(np.ones((L, L), dtype=f), -1)
+        Tm = solve_triangular(np.eye(L, dtype=f) + A, np.eye(L, dtype=f), lower=True, unit_diagonal=True).astype(f)
+        U = Tm @ (B[:, None] * V)
+        W = Tm @ (B[:, None] * K * np.exp(gam))
+        E = U - W @ S.T
+        P = kda_intra_chunk_weights(Q, K, gam, sub)
+        O[sl] = q_scale * ((Q * np.exp(gam)) @ S.T + P @ E)
+        S = S * np.exp(gam[-1])[None, :] + E.T @ (K * np.exp(gam[-1][None, :] - gam))
+    return O, S

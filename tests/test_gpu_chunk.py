@@ -345,3 +345,17 @@ def test_all_sequences_empty(mode):
     assert out.shape[0] == 0
     assert torch.equal(st_out, st_in)
     assert torch.equal(cs_out.view(torch.int16), cs_in.view(torch.int16))
+
+
+def test_weak_decay_long_memory(mode):
+    """Decays fifty times weaker than the workload's (g = -U(0.001, 2) / 50): the state carries
+    information across many chunks, so errors of the state path's split-bf16 products accumulate
+    instead of being forgotten within a chunk, and the carried state is checked at its tolerance."""
+    inp = prefill_inputs([1024, 700], seed=18)
+    inp["g"] = inp["g"] * 0.02
+    ref = run_oracle(inp, heads=[0, 23, 47])
+    out, st = run_gpu(inp, ref["y"])
+    for h in (0, 23, 47):
+        assert_out_close(out[:, h], ref["out"][:, h], f"out, head {h}")
+        for n in range(2):
+            assert_state_close(st[n, h], ref["state"][n, h], f"state of sequence {n}, head {h}")

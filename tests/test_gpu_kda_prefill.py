@@ -159,3 +159,23 @@ def test_kda_prefill_full_size_sampled_heads():
         assert_out_close(out[:, h], ref["out"][:, 0], f"out of head {h}")
         for n in range(4):
             assert_state_close(st[n, h], ref["state"][n, 0], f"state of sequence {n}, head {h}")
+
+
+def test_kda_weak_decay_long_memory():
+    """Per-channel decays fifty times weaker than the workload's: the state carries across many
+    16-token blocks and the fp32 chain is checked at the state tolerance."""
+    g = lib()
+    geo = GEO2
+    inp = kda_prefill_inputs([1024, 300], seed=306, geo=geo)
+    inp["g"] = inp["g"] * 0.02
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    st = torch.empty((2, geo.num_v_heads, 128, 128), dtype=torch.float32, device=DEV)
+    out = g.gdn_kda_recurrence(y.to(DEV), inp["g"].to(DEV), inp["beta"].to(DEV), inp["cu_seqlens"].to(DEV),
+                               inp["q_scale"], state_in=inp["state0"].to(DEV), state_out=st, z=inp["z"].to(DEV),
+                               norm_w=inp["norm_w"].to(DEV), geometry=geo)
+    g.gdn_check_device_errors()
+    o, st_ref = oracle.kda_recurrence(y, inp["g"], inp["beta"], inp["cu_seqlens"], q_scale=inp["q_scale"],
+                                      state_in=inp["state0"], **_a(geo))
+    assert_out_close(out, oracle.gated_rmsnorm(o, inp["z"], inp["norm_w"]))
+    for n in range(2):
+        assert_state_close(st[n], st_ref[n], f"state of sequence {n}")

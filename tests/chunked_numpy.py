@@ -135,3 +135,55 @@ def chunked_chain_kda_fp32(q, k, v, g, beta, S0, q_scale, chunk=64, sub=16):
         O[sl] = q_scale * ((Q * np.exp(gam)) @ S.T + P @ E)
         S = S * np.exp(gam[-1])[None, :] + E.T @ (K * np.exp(gam[-1][None, :] - gam))
     return O, S
+
+
+def _bf16(x):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def tc_product(a, b, split_a=True, split_b=True):
+    """a @ b as a bf16 tensor-core product with fp32 accumulation: each operand is its bf16
+    rounding (hi) or, split, hi + lo with lo the bf16 rounding of the remainder; the products
+    hi*hi, hi*lo and lo*hi are summed (lo*lo is below fp32) and the result is rounded to fp32."""
+    ah, bh = _bf16(a), _bf16(b)
+    r = ah @ bh
+    if split_b:
+        r = r + ah @ _bf16(b - bh)
+    if split_a:
+        r = r + _bf16(a - ah) @ bh
+    return r.astype(np.float32).astype(np.float64)
+
+
+TC_SPLIT_ALL = dict(T=True, Kg=True, S=True, R=True, E=True, Kd=True, Qg=True, S_o=True, P=True, E_o=True)
+
+
+def chunked_chain_kda_tc(q, k, v, g, beta, S0, q_scale, split=TC_SPLIT_ALL, chunk=64):
+    """The chunked KDA form with every contraction a bf16 tensor-core product (tc_product),
+    everything else in fp32, in the order a kernel takes it per chunk:
+      X = (K e^Gamma) S0^T            [split Kg, S]
+      R = beta (V - X)                fp32 epilogue (beta never enters an operand)
+      E = T R                         [split T, R]
+      O = q_scale ((Q e^Gamma) S0^T + P E)    [Qg, S_o; P, E_o]  -- the output only
+      S = S0 diag(e^Gamma_L) + E^T (K e^(Gamma_L - Gamma))     [E, Kd]
+    `split` says which operands are bf16 hi + lo pairs (True) or plain bf16 (False)."""
+    f32 = lambda x: np.asarray(x, dtype=np.float32).astype(np.float64)
+    T = q.shape[0]
+    S = f32(S0)
+    O = np.zeros((T, v.shape[1]))
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(T, c0 + chunk))
+        Q, K, V, G, B = q[sl], k[sl], v[sl], g[sl], beta[sl]
+        L = Q.shape[0]
+        gam = f32(np.cumsum(G, axis=0))
+        A = B[:, None] * kda_intra_chunk_weights(K, K, gam).astype(np.float64) * np.tril(np.ones((L, L)), -1)
+        Tm = f32(solve_triangular(np.eye(L) + A, np.eye(L), lower=True, unit_diagonal=True))
+        X = tc_product(K * np.exp(gam), S.T, split["Kg"], split["S"])
+        R = f32(B[:, None] * (V - X))
+        E = tc_product(Tm, R, split["T"], split["R"])
+        P = kda_intra_chunk_weights(Q, K, gam).astype(np.float64)
+        O[sl] = q_scale * (tc_product(Q * np.exp(gam), S.T, split["Qg"], split["S_o"])
+                           + tc_product(P, E, split["P"], split["E_o"]))
+        S = f32(S * np.exp(gam[-1])[None, :]
+                + tc_product(E.T, K * np.exp(gam[-1][None, :] - gam), split["E"], split["Kd"]))
+    return O, S

@@ -11,7 +11,8 @@ import pytest
 
 import oracle
 from linear_attention_ssm_gb300.synth import Geometry, kda_prefill_inputs
-from tests.chunked_numpy import chunked_chain_kda_fp32, kda_intra_chunk_weights, l2n
+from tests.chunked_numpy import (TC_SPLIT_ALL, chunked_chain_kda_fp32, chunked_chain_kda_tc, kda_intra_chunk_weights,
+                                 l2n)
 
 GEO = Geometry(num_k_heads=1, num_v_heads=1, head_k_dim=128, head_v_dim=128, conv_width=4)
 
@@ -72,3 +73,47 @@ def test_the_plain_factorisation_fails_where_the_subblocks_do_not():
         plain = (kf * np.exp(gam)) @ (kf * np.exp(-gam)).T
     assert not np.isfinite(np.tril(plain)).all()
     assert np.isfinite(kda_intra_chunk_weights(k, k, gam)).all()
+
+
+# ------------------------------------------------------------------ the tensor-core precision plan
+
+def _weak(L, seed):
+    """A sequence whose per-channel decays are fifty times weaker than the workload's, so the state
+    carries across many chunks (under the workload's decay a chunk forgets its start, which hides
+    errors of the state path)."""
+    inp = kda_prefill_inputs([L], seed=seed, geo=GEO)
+    inp["g"] = inp["g"] * 0.02
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    o, st = oracle.kda_recurrence(y, inp["g"], inp["beta"], [0, L], 1, 1, 128, 128, GEO.q_scale,
+                                  state_in=inp["state0"])
+    a = y.double().numpy()
+    args = (l2n(a[:, :128], 1e-6), l2n(a[:, 128:256], 1e-6), a[:, 256:], inp["g"][:, 0].double().numpy(),
+            inp["beta"][:, 0].double().numpy(), inp["state0"][0, 0].double().numpy(), GEO.q_scale)
+    return args, o[:, 0].numpy(), st[0, 0].numpy()
+
+
+def _errors(args, o, st, split):
+    O, S = chunked_chain_kda_tc(*args, split=split)
+    return np.abs(O - o).max() / (2e-2 * np.abs(o).max()), _rel(S, st)
+
+
+def test_tensor_core_plan_split_state_path_plain_output_path():
+    """bf16 hi + lo on every state-path operand and plain bf16 on the output-only products: the
+    state stays far inside 1e-4 relative L2 over 512 tokens of long memory, the output inside its
+    bound."""
+    args, o, st = _weak(512, 420)
+    plan = dict(TC_SPLIT_ALL, Qg=False, S_o=False, P=False, E_o=False)
+    out_ratio, state_rel = _errors(args, o, st, plan)
+    assert out_ratio <= 0.5
+    assert state_rel <= 1e-5
+
+
+@pytest.mark.parametrize("operand", ["Kd", "E", "R", "T", "Kg", "S"])
+def test_each_state_path_operand_needs_its_split(operand):
+    """Negative controls: any one state-path operand left plain bf16 puts the state beyond its
+    1e-4 tolerance under long memory."""
+    args, o, st = _weak(512, 420)
+    plan = dict(TC_SPLIT_ALL, Qg=False, S_o=False, P=False, E_o=False)
+    plan[operand] = False
+    _, state_rel = _errors(args, o, st, plan)
+    assert state_rel > 1e-4, (operand, state_rel)

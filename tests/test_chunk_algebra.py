@@ -2,8 +2,10 @@
 only): fp32 throughout, intra-chunk decay weights formed by 16-token sub-blocks around references
 that keep every factor a decay in (0, 1].  Checked against the fp64 sequential oracle, including
 decays far stronger than any workload's, where the plain factorisation exp(Gamma_t) * exp(-Gamma_j)
-leaves the range of fp32.  GLM-5.3-Flash kernel TDD ledger, slice I4 (the chunk path matches the
-sequential state and output at 63/64/65 tokens)."""
+leaves the range of fp32.  Then the tensor-core precision plan: with every contraction a bf16
+product (fp32 accumulation), which operands must be bf16 hi + lo pairs for the state to hold its
+1e-4 tolerance when it carries across many chunks.  GLM-5.3-Flash kernel TDD ledger, slice I4 (the
+chunk path matches the sequential state and output at 63/64/65 tokens)."""
 from __future__ import annotations
 
 import numpy as np

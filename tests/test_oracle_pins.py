@@ -762,3 +762,47 @@ def test_kda_recurrence_planted_mutations_fail_the_chunked_form(mut):
                              inp["beta"][:, 0].double().numpy(), inp["state0"][0, 0].double().numpy(), 0.5)
     assert np.abs(o[:, 0].numpy() - O).max() > 1e-3 or np.abs(st[0, 0].numpy() - S).max() > 1e-3
 
+
+
+# ------------------------------------------------------------------ normalisation and packing invariants
+
+def test_l2_normalisation_makes_q_and_k_scale_free():
+    """With eps = 0, doubling every q and k channel (exact in bf16) leaves outputs and states
+    unchanged: the recurrence sees only q/||q|| and k/||k||.  The planted no-q-norm mistake is not
+    scale free."""
+    geo = SMALL
+    inp = prefill_inputs([11, 6], seed=64, geo=geo)
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    y2 = y.clone()
+    nqk = 2 * geo.num_k_heads * geo.head_k_dim
+    y2[:, :nqk] = y[:, :nqk] * 2
+    a = (inp["g"], inp["beta"], inp["cu_seqlens"], geo.num_k_heads, geo.num_v_heads, geo.head_k_dim, geo.head_v_dim,
+         0.3, 0.0, inp["state0"])
+    o1, s1 = oracle.gdn_recurrence(y, *a)
+    o2, s2 = oracle.gdn_recurrence(y2, *a)
+    np.testing.assert_allclose(o2.numpy(), o1.numpy(), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(s2.numpy(), s1.numpy(), rtol=1e-13, atol=1e-15)
+    b1, _ = oracle.gdn_recurrence(y, *a, mutation=oracle.MUT_NO_QNORM)
+    b2, _ = oracle.gdn_recurrence(y2, *a, mutation=oracle.MUT_NO_QNORM)
+    assert (b2 - b1).abs().max() > 1e-3
+
+
+@pytest.mark.parametrize("kda", [False, True], ids=["gdn", "kda"])
+def test_packed_sequences_equal_separate_runs(kda):
+    """A varlen call over packed sequences (one empty) gives, per sequence, exactly what a call
+    on that sequence alone gives."""
+    geo = SMALL
+    lengths = [7, 0, 13, 1]
+    inp = (kda_prefill_inputs if kda else prefill_inputs)(lengths, seed=65, geo=geo, random_conv_state=True)
+    run = oracle.kda_prefill if kda else oracle.prefill
+    a = (geo.num_k_heads, geo.num_v_heads, geo.head_k_dim, geo.head_v_dim, 0.3)
+    packed = run(inp["x"], inp["conv_w"], inp["cu_seqlens"], inp["g"], inp["beta"], inp["z"], inp["norm_w"], *a,
+                 state_in=inp["state0"], conv_state_in=inp["conv_state0"])
+    cu = inp["cu_seqlens"].tolist()
+    for n in range(len(lengths)):
+        s, e = cu[n], cu[n + 1]
+        one = run(inp["x"][s:e], inp["conv_w"], [0, e - s], inp["g"][s:e], inp["beta"][s:e], inp["z"][s:e],
+                  inp["norm_w"], *a, state_in=inp["state0"][n:n + 1], conv_state_in=inp["conv_state0"][n:n + 1])
+        assert torch.equal(one["out"], packed["out"][s:e])
+        assert torch.equal(one["state"][0], packed["state"][n])
+        assert torch.equal(one["conv_state"][0].view(torch.int16), packed["conv_state"][n].view(torch.int16))

@@ -61,7 +61,7 @@ typedef enum {
   GDN_ERR_WORKSPACE = 7             /* workspace missing or smaller than the queried size       */
 } gdn_status;
 
-/* Head geometry.  Pages: 16 K heads, 48 V heads, head dim 128, conv kernel 4
+/* Head geometry.  The pages' model: 16 K heads and 48 V heads of width 128, a four-tap conv
  * (pegainfer PR #1152, Summary). */
 typedef struct {
   int32_t num_k_heads; /* Hk */
@@ -72,7 +72,8 @@ typedef struct {
 } gdn_geometry;
 
 /* Tokens per chunk of the chunk-wise prefill.  A chunk never crosses a sequence boundary.
- * (pegainfer PR #1152, Validation: S=16/64 run one chunk, S=80/128 run two.) */
+ * (pegainfer PR #1152, Validation: 16- and 64-token runs fit in one chunk, 80- and 128-token
+ * runs take two.) */
 #define GDN_CHUNK_SIZE 64
 
 /* Human-readable name of a status code (static storage). */
@@ -86,7 +87,7 @@ GDN_API const char* gdn_version(void);
 
 /*
  * Causal depthwise conv1d (width W, no bias) + SiLU over packed variable-length sequences.
- * pegainfer PR #1152, Summary (depthwise conv, conv kernel 4, only conv1d.weight stored) and
+ * pegainfer PR #1152, Summary (a four-tap depthwise conv; conv1d.weight is its only weight) and
  * "Commands + measured numbers" (the conv leg, compared bit-exact); GLM-5.3-Flash ledger,
  * slice I3 (a decode step equals the full width-4 causal convolution).
  *
@@ -300,9 +301,9 @@ GDN_API gdn_status gdn_verify_commit_fp16_state(const gdn_geometry* geo,
 
 /*
  * One fused decode step of the KDA (Kimi delta attention) layer: as gdn_decode_step, with a decay
- * per key channel instead of per head.  GLM-5.3-Flash kernel TDD ledger, slices I2 (FP32
- * [value, key] state, clamped and exponentiated decay, separate q output scale), I2a (q/k
- * normalised x / sqrt(sum x^2 + eps)) and I3 (the width-4 conv step).  Per V head:
+ * per key channel instead of per head.  GLM-5.3-Flash kernel TDD ledger, slices I2 (an fp32
+ * state indexed [value, key], the decay clamped then exponentiated, its own q output scale),
+ * I2a (q/k normalised x / sqrt(sum x^2 + eps)) and I3 (the width-4 conv step).  Per V head:
  *   S <- S diag(exp(max(g, g_min)));   e = beta (v - S k);   S <- S + e k^T;   o = q_scale S q
  * followed by the same sigmoid-gated RMSNorm as gdn_decode_step.
  *   g           [batch, Hv, Dk] fp32 per-channel log decay (16-byte aligned)
@@ -320,11 +321,11 @@ GDN_API gdn_status gdn_kda_decode_step(const gdn_geometry* geo, const gdn_bf16* 
  * The KDA recurrence over packed variable-length sequences (the prefill's recurrent leg),
  * optionally fused with the sigmoid-gated RMSNorm: the step of gdn_kda_decode_step applied to
  * every token in order, each (sequence, V head) state carried from token to token.
- * GLM-5.3-Flash kernel TDD ledger, slices I2 (FP32 [value, key] state, clamped and exponentiated
- * per-channel decay, separate q output scale), I2a (q/k normalised x / sqrt(sum x^2 + eps)) and
- * I4 (the prefill matches the sequential state and output at every length).  This is the
- * sequential form: one CTA per (V head, sequence) walks the tokens, so a call's time grows with
- * its longest sequence.
+ * GLM-5.3-Flash kernel TDD ledger, slices I2 (an fp32 state indexed [value, key], a per-channel
+ * decay clamped then exponentiated, its own q output scale), I2a (q/k normalised
+ * x / sqrt(sum x^2 + eps)) and I4 (the prefill matches the sequential state and output at every
+ * length).  This is the sequential form: one CTA per (V head, sequence) walks the tokens, so a
+ * call's time grows with its longest sequence.
  *   qkv        [total_tokens, C] bf16 conv output (gdn_conv1d_prefill's y): q heads | k heads | v heads
  *   g          [total_tokens, Hv, Dk] fp32 per-channel log decay (16-byte aligned)
  *   g_min      the clamp: decays below exp(g_min) are raised to it (-INFINITY: no clamp; NaN is rejected)

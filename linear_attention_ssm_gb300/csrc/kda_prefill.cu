@@ -2,10 +2,10 @@
 // recurrent leg), token by token, with each head's fp32 [value, key] state held in registers for
 // the whole sequence.
 //
-// GLM-5.3-Flash kernel TDD ledger, slices I2 (FP32 [value, key] state, per-channel decay clamped
-// and exponentiated, separate q output scale), I2a (q and k normalised as x / sqrt(sum x^2 + eps))
-// and I4 (the prefill's state and outputs match the sequential recurrence at every length, 63, 64
-// and 65 tokens included).  Per token and V head:
+// GLM-5.3-Flash kernel TDD ledger, slices I2 (an fp32 state indexed [value, key], a per-channel
+// decay clamped then exponentiated, its own q output scale), I2a (q and k normalised as
+// x / sqrt(sum x^2 + eps)) and I4 (the prefill's state and outputs match the sequential recurrence
+// at every length, 63, 64 and 65 tokens included).  Per token and V head:
 //   S <- S diag(exp(max(g, g_min)));   e = beta (v - S k);   S <- S + e k^T;   o = q_scale S q
 // then, when z is given, the sigmoid-gated RMSNorm of the GDN sublayer.
 //
@@ -15,10 +15,11 @@
 // token is that of the KDA decode kernel up to the order of the four-term sums in each lane.  The
 // token inputs (q and k of the K head, v, z, the per-channel decay and beta of the V head) are
 // staged in shared memory 16 tokens at a time by asynchronous copies, double-buffered so that the
-// next block streams in while this one is computed.  What does not depend on the state -- each token's normalised q and k and its
-// per-channel decay factors -- is formed once per block by all eight warps together (a token per
-// warp), so the chain from one token to the next holds only the state's own work; the block's
-// fp32 outputs are likewise normalised by all warps together at the end of the block.
+// next block streams in while this one is computed.  What does not depend on the state -- each
+// token's normalised q and k and its per-channel decay factors -- is formed once per block by all
+// eight warps together (a token per warp), so the chain from one token to the next holds only the
+// state's own work; the block's fp32 outputs are likewise normalised by all warps together at the
+// end of the block.
 //
 // This is the sequential form: per token it does O(Dv Dk) CUDA-core work on every head, so it is
 // bound by instruction issue, not by memory.

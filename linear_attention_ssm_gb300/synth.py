@@ -2,8 +2,8 @@
 
 This module only draws random tensors; it holds none of the method's arithmetic.  Shapes and
 distributions follow the workloads the GDN pages describe (pegainfer PR #1152 "Reference golden
-for the GDN sublayer", Summary: hidden 2560, 16 K heads and 48 V heads of dimension 128,
-conv kernel 4, sigmoid output gate):
+for the GDN sublayer", Summary: hidden size 2560, 16 K heads and 48 V heads of width 128, a
+four-tap conv, a sigmoid output gate):
 
   x (conv input)  [T, C]        bf16  ~ N(0, 1)           C = 2*Hk*Dk + Hv*Dv = 10240
   conv weight     [C, W]        bf16  ~ 0.5 * N(0, 1)

@@ -10,7 +10,7 @@
  * What it computes (sources are the pages' titles and sections):
  *   1. causal depthwise conv1d, width W (4), no bias, over the packed [q | k | v] channels,
  *      followed by SiLU and one rounding to bf16 -- pegainfer PR #1152 "Reference golden for
- *      the GDN sublayer", Summary (depthwise conv, conv kernel 4, conv1d weight only) and
+ *      the GDN sublayer", Summary (a four-tap depthwise conv whose only weight is conv1d's) and
  *      "Commands + measured numbers" (the conv leg is a bf16 tensor compared bit-exact);
  *      GLM-5.3-Flash kernel TDD ledger, slice I3 (the decode step equals the full width-4
  *      causal convolution).
@@ -22,7 +22,7 @@
  *   3. the gated delta rule with an fp32 [value, key] state carried across chunks, calls and
  *      sequences:  S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
  *      o_t = q_scale * S_t q_t  -- PR #1152 Code review (f32 recurrent state, cross-chunk
- *      carry); GLM-5.3-Flash ledger slice I2 (FP32 [value,key] state, separate q output scale).
+ *      carry); GLM-5.3-Flash ledger slice I2 (an fp32 state indexed [value, key], its own q scale).
  *      It is evaluated as its expanded form: S <- exp(g) S;  e = beta (v - S k);  S <- S + e k^T.
  *   4. gated RMSNorm with a sigmoid output gate: out = o * (mean(o^2) + eps)^-1/2 * w * sigmoid(z)
  *      -- PR #1152 Summary (output_gate_type "sigmoid", not silu) and Code review item 6
@@ -468,8 +468,8 @@ uint16_t oracle_round_f16(double x) {
  * widened to double, the step runs exactly as oracle_decode_step (the output from the new state
  * as computed, before any rounding), and the new state is rounded once to binary16 when it is
  * stored.  Qwen3.8 kernel architecture and TDD ledger, the FP16 h-state twins of the decode and
- * WY kernels (same expressions as the FP32 kernels; the state is half precision in memory only,
- * rounded once per token boundary).
+ * WY kernels (the FP32 kernels' arithmetic, with the state stored in half precision and rounded
+ * whenever a token's state is stored).
  * state_h: [B, hv, dv, dk] binary16 bit patterns, in/out.  Other arguments as oracle_decode_step.
  */
 int oracle_decode_step_h16(int hk, int hv, int dk, int dv, int W, int B, const uint16_t* x,
@@ -494,8 +494,8 @@ int oracle_decode_step_h16(int hk, int hv, int dk, int dv, int W, int B, const u
 
 /*
  * The per-token gates from their projections (PARITY UNPINNED: the pages name the inputs -- the
- * a / b projections, A_log and dt_bias, Qwen3.8 kernel architecture and TDD ledger, "GDN
- * alpha/beta transforms"; PR #1152 Summary -- but give no formula).  The reading taken is the
+ * a / b projections, A_log and dt_bias, Qwen3.8 kernel architecture and TDD ledger, the kernel
+ * map's GDN gate transforms; PR #1152 Summary -- but give no formula).  The reading taken is the
  * gate of the published Gated DeltaNet / Mamba-2 layers:
  *   g[t,h]    = -exp(A_log[h]) * softplus(a[t,h] + dt_bias[h]),   softplus(x) = log(1 + e^x)
  *   beta[t,h] = sigmoid(b[t,h]) = 1 / (1 + e^-b)
@@ -519,7 +519,7 @@ int oracle_gates(long rows, int hv, const uint16_t* a, const uint16_t* b, const 
 /*
  * One token of the KDA (Kimi delta attention) layer for each of B sequences: the gated delta
  * rule with a per-channel (key-dimension) decay -- GLM-5.3-Flash kernel TDD ledger, slices I2
- * (FP32 [value, key] state, clamped and exponentiated decay, separate q output scale), I2a
+ * (an fp32 state indexed [value, key], the decay clamped then exponentiated, its own q scale), I2a
  * (q/k normalised x / sqrt(sum x^2 + eps)) and I3 (the width-4 conv step).  Per V head h,
  * with q, k of K head h / (hv/hk) after the conv step and the L2 norms:
  *   alpha_i = exp(max(g[b,h,i], g_min))        (g_min = -inf: no clamp)

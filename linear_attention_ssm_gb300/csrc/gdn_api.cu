@@ -389,13 +389,7 @@ gdn_status check_verify_shape(const gdn_geometry* geo, int32_t batch, int32_t ro
                 rows, geo->num_v_heads / geo->num_k_heads);
   return GDN_OK;
 }
-}  // namespace
 
-extern "C" {
-
-}  // extern "C"
-
-namespace {
 gdn_status verify(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w, const gdn_bf16* conv_state,
                   const float* g, const float* beta, const void* state, bool fp16_state, const gdn_bf16* z,
                   const gdn_bf16* norm_w, float q_scale, float l2_eps, float rms_eps, gdn_bf16* out, int32_t batch,

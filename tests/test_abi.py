@@ -218,3 +218,20 @@ def test_kda_recurrence_rejects_bad_arguments(lib):
     assert lib.gdn_kda_recurrence(_geo(head_k_dim=64), FAKE, FAKE, -1.0, FAKE, FAKE, 1, 4, 0.088, 1e-6, None,
                                   None, None, None, 1e-6, FAKE, None) == 2
     assert call(N=0, T=0, qkv=None, g=None, beta=None, cu=None, out=None) == 0
+
+
+def test_header_is_a_plain_c_abi(lib, tmp_path):
+    """A C11 program built against include/*.h alone (gcc -Wall -Wextra -Werror) links against
+    libgdn.so and gets the documented status from every entry point it calls."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "c_abi_check")
+    libdir = os.path.dirname(binding.LIB_PATH)
+    src = os.path.join(ROOT, "tests", "c_abi_check.c")
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", INCLUDE, src, "-o", exe,
+                    "-L", libdir, "-lgdn", f"-Wl,-rpath,{libdir}", "-lm"], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr

@@ -228,9 +228,14 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         time.sleep(0.06)
         self.proc.terminate()
-        out = self.proc.communicate(timeout=10)[0]
+        return self.summarize(self.proc.communicate(timeout=10)[0])
+
+    @classmethod
+    def summarize(cls, text):
+        """Median SM clock, the largest maximum clock and every throttle reason seen Active in the
+        sampler's CSV lines (sm, max sm, power, then the four reasons; unparsable lines skipped)."""
         sm, mx, reasons = [], [], set()
-        for line in out.strip().splitlines():
+        for line in text.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 7:
                 continue
@@ -239,7 +244,7 @@ class ClockSampler:
                 mx.append(float(parts[1]))
             except ValueError:
                 continue
-            for name, val in zip(self.NAMES, parts[3:7]):
+            for name, val in zip(cls.NAMES, parts[3:7]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,

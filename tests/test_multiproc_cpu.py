@@ -68,3 +68,18 @@ def test_kda_prefill_traffic_scales_with_algorithmic_bytes():
     assert bench.kda_prefill_bytes(4096, 4, 64) == rec["algorithmic_bytes_per_launch"]
     assert bench.scaled_kda_traffic(rec["algorithmic_bytes_per_launch"]) == rec["bytes_per_launch"]
     assert bench.scaled_kda_traffic(2 * rec["algorithmic_bytes_per_launch"]) == 2 * rec["bytes_per_launch"]
+
+
+def test_clock_samples_are_summarised_with_every_active_reason():
+    """The bench's nvidia-smi sampler: median SM clock, maximum clock, and each throttle reason
+    seen Active at least once (Not Active and unparsable lines ignored)."""
+    lines = "\n".join([
+        "2070, 2070, 810.2, Not Active, Not Active, Not Active, Not Active",
+        "1995, 2070, 1390.0, Not Active, Not Active, Not Active, Active",
+        "[N/A], 2070, 12.0, Not Active, Not Active, Not Active, Not Active",
+        "2055, 2070, 1200.4, Active, Not Active, Not Active, Not Active",
+        "garbage",
+    ])
+    got = bench.ClockSampler.summarize(lines)
+    assert got == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["hw_slowdown", "sw_power_cap"], "samples": 3}
+    assert bench.ClockSampler.summarize("") == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}

@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     GdnError,
     gdn_check_device_errors,
     gdn_chunk_prefill,
+    gdn_chunk_prefill_noalloc,
     gdn_chunk_prefill_min_workspace_size,
     gdn_chunk_prefill_workspace_size,
     gdn_conv1d_prefill,
@@ -23,9 +24,13 @@ from .binding import (  # noqa: F401
     gdn_kda_decode_step,
     gdn_kda_prefill,
     gdn_kda_recurrence,
+    gdn_last_error_message,
     gdn_prefill,
+    gdn_status_string,
     gdn_verify,
     gdn_verify_commit,
+    gdn_verify_commit_fp16_state,
+    gdn_verify_fp16_state,
     gdn_verify_stash_size,
     gdn_version,
     load_library,

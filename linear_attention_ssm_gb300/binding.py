@@ -123,6 +123,15 @@ def gdn_version() -> str:
     return load_library().gdn_version().decode()
 
 
+def gdn_status_string(status: int) -> str:
+    return load_library().gdn_status_string(int(status)).decode()
+
+
+def gdn_last_error_message() -> str:
+    """The library's message for the last error returned on this thread ("" if none)."""
+    return load_library().gdn_last_error_message().decode()
+
+
 def gdn_conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in=None, conv_state_out=None, y=None,
                        geometry: Geometry = QWEN_GDN, stream=None):
     """Causal depthwise conv1d + SiLU over packed sequences; returns y [T, C] bf16."""
@@ -185,6 +194,33 @@ def gdn_chunk_prefill(qkv, g, beta, cu_seqlens, q_scale, l2_eps=1e-6, state_in=N
                                  float(q_scale), float(l2_eps), _p(state_in), _p(state_out), _p(z),
                                  _p(norm_w), float(rms_eps), _p(out), _p(workspace), wbytes,
                                  _stream(stream)))
+    return out
+
+
+def gdn_chunk_prefill_noalloc(qkv, g, beta, cu_seqlens, q_scale, l2_eps=1e-6, state_in=None, state_out=None,
+                              z=None, norm_w=None, rms_eps=1e-6, out=None, geometry: Geometry = QWEN_GDN,
+                              stream=None):
+    """gdn_chunk_prefill without a caller workspace: the schedule goes to a fixed scratch inside the
+    library (at most GDN_NOALLOC_MAX_SEQS sequences per call; calls that overlap on the GPU race on
+    it).  Same arguments and result as gdn_chunk_prefill otherwise."""
+    lib = load_library()
+    C, hv, dv, dk = geometry.conv_dim, geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
+    N = cu_seqlens.numel() - 1
+    T = qkv.shape[0]
+    _dev(qkv, torch.bfloat16, "qkv", (T, C))
+    _dev(g, torch.float32, "g", (T, hv))
+    _dev(beta, torch.float32, "beta", (T, hv))
+    _dev(cu_seqlens, torch.int32, "cu_seqlens", (N + 1,))
+    _dev(state_in, torch.float32, "state_in", (N, hv, dv, dk))
+    _dev(state_out, torch.float32, "state_out", (N, hv, dv, dk))
+    _dev(z, torch.bfloat16, "z", (T, hv, dv))
+    _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
+    if out is None:
+        out = torch.empty((T, hv, dv), dtype=torch.bfloat16, device=qkv.device)
+    _dev(out, torch.bfloat16, "out", (T, hv, dv))
+    _check(lib.gdn_chunk_prefill_noalloc(_geo(geometry), _p(qkv), _p(g), _p(beta), _p(cu_seqlens), N, T,
+                                         float(q_scale), float(l2_eps), _p(state_in), _p(state_out), _p(z),
+                                         _p(norm_w), float(rms_eps), _p(out), _stream(stream)))
     return out
 
 
@@ -375,6 +411,23 @@ def gdn_verify_commit(committed_rows, stash, conv_state, state, rows: int, geome
     fn = lib.gdn_verify_commit_fp16_state if fp16_state else lib.gdn_verify_commit
     _check(fn(_geo(geometry), _p(committed_rows), _p(stash), _p(conv_state), _p(state), B, int(rows),
               _stream(stream)))
+
+
+def gdn_verify_fp16_state(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps=1e-6, rms_eps=1e-6,
+                          out=None, stash=None, geometry: Geometry = QWEN_GDN, stream=None):
+    """gdn_verify on a binary16 recurrent state [B, Hv, Dv, Dk] (read only)."""
+    if state.dtype != torch.float16:
+        raise TypeError(f"state must be torch.float16, got {state.dtype}")
+    return gdn_verify(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps, rms_eps, out, stash,
+                      geometry, stream)
+
+
+def gdn_verify_commit_fp16_state(committed_rows, stash, conv_state, state, rows: int,
+                                 geometry: Geometry = QWEN_GDN, stream=None):
+    """gdn_verify_commit into a binary16 recurrent state (rounded once per committed element)."""
+    if state.dtype != torch.float16:
+        raise TypeError(f"state must be torch.float16, got {state.dtype}")
+    return gdn_verify_commit(committed_rows, stash, conv_state, state, rows, geometry, stream)
 
 
 def gdn_check_device_errors(stream=None):

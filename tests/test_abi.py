@@ -235,3 +235,27 @@ def test_header_is_a_plain_c_abi(lib, tmp_path):
                     "-L", libdir, "-lgdn", f"-Wl,-rpath,{libdir}", "-lm"], check=True)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr
+
+
+def test_python_binding_has_every_c_entry_point_by_name():
+    """The binding is the C ABI under the same names: every declared entry point has a Python
+    function of that name (exported by the package too)."""
+    import linear_attention_ssm_gb300 as pkg
+    missing = [n for n in declared_symbols() if not callable(getattr(binding, n, None))]
+    assert not missing, missing
+    not_exported = [n for n in declared_symbols() if not hasattr(pkg, n)]
+    assert not not_exported, not_exported
+
+
+def test_binding_helpers_without_a_gpu(lib):
+    import torch
+    assert binding.gdn_status_string(3) == "GDN_ERR_MISALIGNED"
+    assert isinstance(binding.gdn_last_error_message(), str)
+    f32 = torch.zeros(1, 48, 128, 128)
+    with pytest.raises(TypeError):   # the fp16 entry points refuse an fp32 state before anything else
+        binding.gdn_verify_fp16_state(None, None, None, None, None, f32, None, None, 0.088)
+    with pytest.raises(TypeError):
+        binding.gdn_verify_commit_fp16_state(None, None, None, f32, 4)
+    with pytest.raises(TypeError):   # host tensors are refused
+        binding.gdn_chunk_prefill_noalloc(torch.zeros(4, 10240, dtype=torch.bfloat16), torch.zeros(4, 48),
+                                          torch.zeros(4, 48), torch.tensor([0, 4], dtype=torch.int32), 0.088)

@@ -33,6 +33,17 @@ def lib():
     return g
 
 
+@pytest.fixture(params=[0, 1, 2], ids=["split", "emulated", "fused"], name="mode")
+def chunk_mode(request):
+    """Runs a chunk-prefill test once per chunk design: the split path (prep + state kernels), the
+    fused kernel with its MMAs emulated on the CUDA cores, and the fused kernel on the tensor
+    cores."""
+    g = lib()
+    g.gdn_debug_set_chunk_mode(request.param)
+    yield request.param
+    g.gdn_debug_set_chunk_mode(0)
+
+
 def to_dev(t):
     return None if t is None else t.to(DEV).contiguous()
 

@@ -6,19 +6,11 @@ import torch
 
 import oracle
 from linear_attention_ssm_gb300.synth import QWEN_GDN, Geometry, prefill_inputs, cu_seqlens_of
-from tests.gpu_common import (DEV, Guarded, NEG_CONTROL_RATIO, assert_out_close, assert_state_close, lib,
-                              out_error_ratio, state_rel_l2)
+from tests.gpu_common import (DEV, Guarded, NEG_CONTROL_RATIO, assert_out_close, assert_state_close, lib,  # noqa: F401
+                              chunk_mode, out_error_ratio, state_rel_l2)
 
 pytestmark = pytest.mark.gpu
 GEO = QWEN_GDN
-
-
-@pytest.fixture(params=[0, 1, 2], ids=["split", "emulated", "fused"])
-def mode(request):
-    g = lib()
-    g.gdn_debug_set_chunk_mode(request.param)
-    yield request.param
-    g.gdn_debug_set_chunk_mode(0)
 
 
 def run_gpu(inp, y_ref, fused=True, state_in=True, geo=GEO, q_scale=None):

@@ -267,9 +267,76 @@ def replica_throughput(units_per_rank, world, slowest_ms):
     return world * units_per_rank / (slowest_ms / 1000.0)
 
 
-def cpu_oracle_sample(inp, tokens_per_seq):
+def dist_stats(ms):
+    """Mean, median and the 10th / 90th percentiles of per-run times (ms)."""
+    xs = sorted(float(v) for v in ms)
+    n = len(xs)
+
+    def pct(p):  # nearest-rank percentile
+        return xs[min(n - 1, max(0, int(round(p / 100.0 * n + 0.5)) - 1))]
+    return {"runs": n, "mean_ms": statistics.mean(xs), "p10_ms": pct(10), "p50_ms": statistics.median(xs),
+            "p90_ms": pct(90)}
+
+
+def step_bytes(tokens, seqs):
+    """Algorithmic bytes of one fully fused prefill pass: per token x 20480 + z 12288 + g, beta 384 +
+    out 12288; per sequence the fp32 state and the conv state, each read and written; the conv and
+    norm weights once."""
+    return 45440 * tokens + (STATE_BYTES_PER_SEQ + 2 * 10240 * 3 * 2) * seqs + 10240 * 4 * 2 + 128 * 2
+
+
+def time_small_configs(gdn, dev, hbm_peak, runs=60, warm=10):
+    """The correctness-sized workloads: one sequence of 16 tokens from a zero state, and separate
+    sequences of 63, 64, 65, 80 and 128 tokens from a nonzero state.  Each prefill call (conv1d,
+    then the chunk prefill with the fused gate) is captured in a CUDA graph and replayed, so that
+    the host's per-call work leaves no gaps; one pair of CUDA events per replay."""
+    import torch
+    from linear_attention_ssm_gb300.synth import CHUNK_BOUNDARY_LENGTHS, prefill_inputs
+    cases = [("S16_zero_state", 16, 0, True)] + [(f"S{S}", S, 1000 + S, False) for S in CHUNK_BOUNDARY_LENGTHS]
+    res = {}
+    for name, S, seed, zero in cases:
+        inp = prefill_inputs([S], seed=seed, zero_state=zero)
+        x, w, cu = inp["x"].to(dev), inp["conv_w"].to(dev), inp["cu_seqlens"].to(dev)
+        g, beta, z, nw = inp["g"].to(dev), inp["beta"].to(dev), inp["z"].to(dev), inp["norm_w"].to(dev)
+        st_in, cs_in = inp["state0"].to(dev), inp["conv_state0"].to(dev)
+        st_out, cs_out = torch.empty_like(st_in), torch.empty_like(cs_in)
+        qkv, out = torch.empty_like(x), torch.empty((S, 48, 128), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(gdn.gdn_chunk_prefill_workspace_size(1, S), dtype=torch.uint8, device=dev)
+
+        def call():
+            gdn.gdn_conv1d_prefill(x, w, cu, cs_in, cs_out, qkv)
+            gdn.gdn_chunk_prefill(qkv, g, beta, cu, inp["q_scale"], 1e-6, None if zero else st_in, st_out, z, nw,
+                                  1e-6, out, workspace=ws)
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                call()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                call()
+            for _ in range(warm):
+                graph.replay()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+            for a, b in evs:
+                a.record(side)
+                graph.replay()
+                b.record(side)
+        torch.cuda.synchronize()
+        gdn.gdn_check_device_errors()
+        st = dist_stats([a.elapsed_time(b) for a, b in evs])
+        roof = S / (step_bytes(S, 1) / (hbm_peak * 1e9))
+        tps = S / (st["p50_ms"] / 1000.0)
+        res[name] = {"tokens": S, "tokens_per_s": tps, "roofline_tokens_per_s": roof, "frac": tps / roof,
+                     "algorithmic_bytes": step_bytes(S, 1), **st}
+        del graph
+    return res
+
+
+def cpu_oracle_sample(inp, tokens_per_seq, nthreads=0):
     """The oracle (conv -> recurrence -> gated norm, fp64, all V heads) on the first
-    `tokens_per_seq` tokens of every sequence.  Returns (tokens/s, cores, description)."""
+    `tokens_per_seq` tokens of every sequence, on `nthreads` threads (0: every core).  Returns
+    (tokens/s, threads used, description)."""
     import torch
     import oracle
     from linear_attention_ssm_gb300.synth import cu_seqlens_of
@@ -279,11 +346,12 @@ def cpu_oracle_sample(inp, tokens_per_seq):
     sub = [min(tokens_per_seq, L) for L in lengths]
     t0 = time.perf_counter()
     oracle.prefill(inp["x"][idx], inp["conv_w"], cu_seqlens_of(sub), inp["g"][idx], inp["beta"][idx], inp["z"][idx],
-                   inp["norm_w"], 16, 48, 128, 128, inp["q_scale"], state_in=inp["state0"])
+                   inp["norm_w"], 16, 48, 128, 128, inp["q_scale"], state_in=inp["state0"], nthreads=nthreads)
     dt = time.perf_counter() - t0
     ntok = sum(sub)
-    return ntok / dt, oracle.num_threads(), (f"first {tokens_per_seq} tokens of each of the {len(lengths)} "
-                                             f"sequences ({ntok} tokens, all 48 V heads), fp64, {dt:.2f} s")
+    used = min(nthreads if nthreads > 0 else oracle.num_threads(), len(lengths) * 48)
+    return ntok / dt, used, (f"first {tokens_per_seq} tokens of each of the {len(lengths)} "
+                             f"sequences ({ntok} tokens, all 48 V heads), fp64, {used} threads, {dt:.2f} s")
 
 
 def run_reference(args, rank, world):
@@ -502,6 +570,46 @@ def time_verify(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak
             "roofline_commit": roof(c_bytes, c_ms, "commit_kernel", "verify_commit" + sfx)}
 
 
+def _r(v, d=4):
+    """A number rounded to `d` significant digits (None passes through)."""
+    if v is None:
+        return None
+    return float(f"{float(v):.{d}g}")
+
+
+def compact_summary(line, step_dist):
+    """Every leg's figures in a few hundred characters, placed last on the line so that a reader
+    that keeps only the line's end still sees them."""
+    def leg(d, unit_key="value", scale=1e6):
+        if not d or "error" in d:
+            return d and {"error": d["error"][:80]}
+        r = d.get("roofline") or {}
+        return {"M_per_s": _r(d[unit_key] / scale), "ms": _r(d.get("ms_per_step")), "frac": _r(r.get("frac"), 3)}
+    out = {"prefill": {"M_tok_s": _r(line["value"] / 1e6), "frac": _r(line["roofline"]["frac"], 3),
+                       "p10_p50_p90_ms": [_r(step_dist[k]) for k in ("p10_ms", "p50_ms", "p90_ms")],
+                       "runs": step_dist["runs"]}}
+    out["decode"] = leg(line["decode"])
+    out["decode_f16"] = leg(line["decode_fp16_state"])
+    out["decode_kda"] = leg(line["decode_kda"])
+    v = line.get("varlen")
+    if v:
+        out["varlen"] = {"M_tok_s": _r(v["value"] / 1e6), "ms": _r(v["ms_per_step"]), "frac": _r(v["frac"], 3)}
+    for key in ("verify", "verify_fp16_state"):
+        d = line.get(key) or {}
+        if d and "error" not in d:
+            out[key] = {"M_rows_s": _r(d.get("value", 0) / 1e6), "ms": _r(d.get("ms_per_step")),
+                        "frac": _r((d.get("roofline_verify") or {}).get("frac"), 3),
+                        "commit_frac": _r((d.get("roofline_commit") or {}).get("frac"), 3)}
+    out["kda_prefill"] = leg(line.get("kda_prefill"))
+    out["small_configs"] = {k: {"M_tok_s": _r(d["tokens_per_s"] / 1e6, 3), "p50_us": _r(1e3 * d["p50_ms"], 3),
+                                "frac": _r(d["frac"], 3)} for k, d in line["small_configs"].items()}
+    c = line.get("cpu_baseline")
+    if c:
+        out["cpu"] = {"tok_s_all": _r(c["value"]), "threads": c["cores"],
+                      "tok_s_1thread": _r(c["single_thread"]["value"]), "nproc": c.get("nproc")}
+    return out
+
+
 def run_ours(args, rank, world, local):
     import torch
     import torch.distributed as dist
@@ -589,6 +697,23 @@ def run_ours(args, rank, world, local):
                  "peak": hbm_peak, "unit": "GB/s", "avg_launch_ms": conv_ms,
                  "algorithmic_bytes_per_launch": conv_bytes, "traffic": crec["bytes_per_launch"] if crec else None}
     conv_roof["frac"] = conv_roof["achieved"] / hbm_peak
+
+    # distribution of per-step times over a separate pass of at least 50 steps (the headline above
+    # times exactly --steps steps between two events): whole step, and the chunk prefill alone
+    nd = max(50, args.steps)
+    evd = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nd)]
+    barrier()
+    for e0, e1, e2 in evd:
+        e0.record(stream)
+        gdn.gdn_conv1d_prefill(x, w, cu, cs_in, cs_out, qkv)
+        e1.record(stream)
+        gdn.gdn_chunk_prefill(qkv, g, beta, cu, inp["q_scale"], 1e-6, state_in, state_out, z, nw, 1e-6, out,
+                              workspace=ws)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    step_dist = dist_stats([e0.elapsed_time(e2) for e0, _, e2 in evd])
+    chunk_dist = dist_stats([e1.elapsed_time(e2) for _, e1, e2 in evd])
+    roofline["launch_ms_distribution"] = chunk_dist
 
     # ---------------- end to end through host buffers (pinned): every step copies its inputs from
     # host to device, runs the prefill and reads its outputs back to the host.  Device inputs and
@@ -685,10 +810,13 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         gdn.gdn_check_device_errors()
         v_ms = max_over_ranks(s4.elapsed_time(e4)) / args.varlen_steps
+        v_roof = hbm_peak * 1e9 / (CHUNK_BYTES_PER_TOKEN + STATE_BYTES_PER_SEQ * vN / vT)
         varlen = {"workload": "varlen prefill, 8 packed sequences {1,17,63,64,65,1000,8191,22334} = 31,735 tokens",
                   "value": world * vT / (v_ms / 1000.0), "unit": "tokens/s", "ms_per_step": v_ms,
-                  "steps": args.varlen_steps,
-                  "roofline_tokens_per_s": hbm_peak * 1e9 / (CHUNK_BYTES_PER_TOKEN + STATE_BYTES_PER_SEQ * vN / vT)}
+                  "steps": args.varlen_steps, "roofline_tokens_per_s": v_roof,
+                  "frac": vT / (v_ms / 1000.0) / v_roof,
+                  "frac_note": "conv1d + chunk prefill step against the chunk prefill's HBM roofline (the "
+                               "algorithmic bytes of the chunk stage, as for the headline)"}
         del vin, vx, vqkv, vz, vout, vws
         torch.cuda.empty_cache()
 
@@ -784,10 +912,16 @@ def run_ours(args, rank, world, local):
     except Exception as exc:  # a secondary leg reports its failure without taking the line down
         kda_prefill = {"error": f"{type(exc).__name__}: {exc}"}
 
+    # ---------------- the correctness-sized workloads (16 tokens; 63 / 64 / 65 / 80 / 128 tokens)
+    small = time_small_configs(gdn, dev, hbm_peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
-        tps, cores, desc = cpu_oracle_sample(inp, 160)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+        tps, cores, desc = cpu_oracle_sample(inp, 2048)
+        tps1, _, desc1 = cpu_oracle_sample(inp, 96, nthreads=1)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "single_thread": {"value": tps1, "unit": "tokens/s", "sample": desc1},
+               "nproc": os.cpu_count()}
 
     if rank == 0:
         line = {
@@ -805,12 +939,13 @@ def run_ours(args, rank, world, local):
             "decode": decode, "decode_fp16_state": decode_f16, "decode_kda": decode_kda, "verify": verify,
             "verify_fp16_state": verify_f16,
             "gates": gates, "kda_prefill": kda_prefill,
-            "varlen": varlen, "cpu_baseline": cpu, "clocks": clk,
+            "varlen": varlen, "small_configs": small, "cpu_baseline": cpu, "clocks": clk,
             # per step: conv1d + conv-state kernels, the chunk prefill's schedule and segment-table
             # kernels, then a prep and a state kernel for each of its three chunk segments
             "gpu_launches": (2 + 2 + 2 * 3) * args.steps,
             "arithmetic": "bf16 tensor-core operands (fp32 operands split into bf16 hi+lo), fp32 accumulate and state",
         }
+        line["summary"] = compact_summary(line, step_dist)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -153,6 +153,15 @@ GDN_API size_t gdn_chunk_prefill_min_workspace_size(const gdn_geometry* geo, int
  *   out        [total_tokens, Hv, Dv] bf16
  *   workspace  256-byte aligned device memory of at least gdn_chunk_prefill_min_workspace_size()
  *              bytes (NULL if 0); gdn_chunk_prefill_workspace_size() bytes select the fast path
+ *
+ * Streams: with the fast-path workspace, a state_out buffer, at least 4,096 tokens and no stream
+ * capture in progress, the call splits each sequence's chunks into segments and runs the
+ * state-independent stage of segment k + 1 on a library-owned side stream (one per device, created
+ * on first use and shared by every caller on that device) beside the state stage of segment k,
+ * ordered by events the library creates once per host thread and device.  Everything the call
+ * writes is ordered before later work on `stream`.  Calls from different streams whose side-stream
+ * work is queued together run it one after the other.  Under stream capture, everything runs on
+ * `stream` as one segment.
  */
 GDN_API gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g,
                                      const float* beta, const int32_t* cu_seqlens,
@@ -271,11 +280,12 @@ GDN_API gdn_status gdn_verify(const gdn_geometry* geo, const gdn_bf16* x, const 
  * would have left (m = 0: an abort, both states untouched).  Reads only stash records of rows
  * < m.  The states must be the ones the verify read (unchanged since).  A value outside
  * [0, rows] leaves that sequence untouched and raises GDN_ERR_DEVICE_ARGUMENT in the device
- * error word.
+ * error word.  stash_bytes is the size of the stash buffer; a stash smaller than
+ * gdn_verify_stash_size(geo, batch, rows) is refused with GDN_ERR_WORKSPACE (nothing launched).
  */
 GDN_API gdn_status gdn_verify_commit(const gdn_geometry* geo, const int32_t* committed_rows,
-                                     const void* stash, gdn_bf16* conv_state, float* state,
-                                     int32_t batch, int32_t rows, void* stream);
+                                     const void* stash, size_t stash_bytes, gdn_bf16* conv_state,
+                                     float* state, int32_t batch, int32_t rows, void* stream);
 
 /*
  * gdn_verify and gdn_verify_commit with the recurrent state stored as IEEE binary16 (Qwen3.8
@@ -296,8 +306,9 @@ GDN_API gdn_status gdn_verify_fp16_state(const gdn_geometry* geo, const gdn_bf16
                                          void* stream);
 GDN_API gdn_status gdn_verify_commit_fp16_state(const gdn_geometry* geo,
                                                 const int32_t* committed_rows, const void* stash,
-                                                gdn_bf16* conv_state, gdn_f16* state,
-                                                int32_t batch, int32_t rows, void* stream);
+                                                size_t stash_bytes, gdn_bf16* conv_state,
+                                                gdn_f16* state, int32_t batch, int32_t rows,
+                                                void* stream);
 
 /*
  * One fused decode step of the KDA (Kimi delta attention) layer: as gdn_decode_step, with a decay
@@ -359,7 +370,13 @@ GDN_API gdn_status gdn_kda_recurrence(const gdn_geometry* geo, const gdn_bf16* q
  * every GPU that loads the library keeps until the process exits; it holds the schedule of up to
  * GDN_NOALLOC_MAX_SEQS sequences, and a larger num_seqs is refused with GDN_ERR_INVALID_ARGUMENT
  * (nothing launched).  The first call on a device looks up that array's device address with the
- * device current; make this first call before any stream capture.  All calls on a device share
+ * device current (cudaGetSymbolAddress) and the kernels' launch attributes, which under lazy
+ * module loading may load the library's module and reserve its static arrays on that device:
+ * make this first call before any stream capture, and before a caller's pool takes the device
+ * memory it will not give back.  The address is kept per device index for the life of the
+ * process; after cudaDeviceReset it is stale, and the call must not be used again.  Host threads
+ * making their first call at the same time store the same address (the cache is atomic).
+ * All calls on a device share
  * the array and it keeps the last call's contents: each call rewrites the whole schedule and
  * zeroes its work counter before the main kernel reads them, but two calls whose kernels overlap
  * on the GPU (for example on two unordered streams) race on the array and give wrong results.

@@ -1,5 +1,8 @@
 /*
- * gdn_debug.h -- verification hooks of libgdn.so (not needed on the hot path).
+ * gdn_debug.h -- verification hooks, exported only by the test build of the library,
+ * libgdn_test.so (the same sources compiled with GDN_TEST_HOOKS).  The product library libgdn.so
+ * exports none of them: it has no switch that changes results and no fault hook.  The pages have
+ * no counterpart to any of these calls.
  *
  * The chunk-wise prefill has two designs: the split path (a prep kernel for the state-independent
  * quantities of all chunks, then the state kernel) and the fused one-kernel path, which has two
@@ -19,9 +22,10 @@
 extern "C" {
 #endif
 
-/* Select the chunk-prefill build used by later gdn_chunk_prefill calls in this process:
- * 0 = split path when the workspace allows, else fused (default); 1 = fused with CUDA-core
- * emulation of the MMAs; 2 = fused on the tensor cores.  Not thread-safe. */
+/* Select the chunk-prefill build used by later gdn_chunk_prefill calls of libgdn_test.so in this
+ * process: 0 = split path when the workspace allows, else fused (default); 1 = fused with CUDA-core
+ * emulation of the MMAs; 2 = fused on the tensor cores.  A process-wide setting (an atomic store):
+ * calls already issued keep the design they were issued with. */
 GDN_API gdn_status gdn_debug_set_chunk_mode(int mode);
 
 /* The mode last selected (0, 1 or 2). */
@@ -40,6 +44,17 @@ GDN_API gdn_status gdn_debug_mma_probe(const gdn_bf16* A, const gdn_bf16* B, int
  * 64-element N blocks 8 KB apart).  Other flag bits are refused with GDN_ERR_INVALID_ARGUMENT. */
 GDN_API gdn_status gdn_debug_mma_probe_ex(const gdn_bf16* A, const gdn_bf16* B, int n_cols, int flags, float* D,
                                           unsigned* status, void* stream);
+
+/* Make a bounded in-kernel wait run out, to exercise the timeout path without a GPU fault.  Bit 0:
+ * the binary16-state decode step (gdn_decode_step_fp16_state, staged form) arms its state-slice
+ * barrier but issues no copy; bit 1: the split chunk prefill's state kernel does the same with the
+ * first vector-block copy of each (sequence, head) item.  The wait on such a barrier runs out after
+ * a short limit (4096 polls), the kernel raises the timeout bit of the device error word and
+ * returns with nothing in flight (tensor memory released), and gdn_check_device_errors() then
+ * returns GDN_ERR_TIMEOUT.  The outputs of the affected call are unspecified (the decode step has
+ * already advanced the conv state).  0 restores normal operation.  Set on the current device.
+ * Other bits: GDN_ERR_INVALID_ARGUMENT. */
+GDN_API gdn_status gdn_debug_set_dropped_copy(unsigned which);
 
 #ifdef __cplusplus
 }

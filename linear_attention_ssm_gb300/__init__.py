@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     gdn_debug_mma_probe,
     gdn_debug_mma_probe_ex,
     gdn_debug_set_chunk_mode,
+    gdn_debug_set_dropped_copy,
     gdn_decode_step,
     gdn_decode_step_fp16_state,
     gdn_gated_rmsnorm,
@@ -34,4 +35,6 @@ from .binding import (  # noqa: F401
     gdn_verify_stash_size,
     gdn_version,
     load_library,
+    load_test_library,
+    using_test_library,
 )

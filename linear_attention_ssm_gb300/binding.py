@@ -4,6 +4,11 @@ Argument marshalling only -- dtype/shape/device checks, output allocation when n
 and the current torch stream.  Every step of the computation runs in the library's CUDA kernels;
 there is no fallback of any kind: if ``libgdn.so`` is missing or cannot be loaded, every call
 raises.
+
+The verification hooks of ``include/gdn_debug.h`` live only in the test build of the library,
+``libgdn_test.so``: the ``gdn_debug_*`` functions call into it, and inside
+``with using_test_library():`` every other function does too (the tests use this to run the
+same calls under the chunk designs the hooks select).
 """
 from __future__ import annotations
 
@@ -17,10 +22,13 @@ from .synth import QWEN_GDN, Geometry
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdn.so")
+TEST_LIB_PATH = os.path.join(_HERE, "libgdn_test.so")
 
 GDN_OK = 0
 _lock = threading.Lock()
 _lib = None
+_test_lib = None
+_override = None  # the test library while inside using_test_library()
 
 
 class GdnError(RuntimeError):
@@ -36,6 +44,46 @@ class _Geo(ctypes.Structure):
                 ("conv_width", ctypes.c_int32)]
 
 
+def _configure(lib, debug: bool):
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    G = ctypes.POINTER(_Geo)
+    sig = {
+        "gdn_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "gdn_last_error_message": ([], ctypes.c_char_p),
+        "gdn_version": ([], ctypes.c_char_p),
+        "gdn_conv1d_prefill": ([G, P, P, P, I, I, P, P, P, P], ctypes.c_int),
+        "gdn_chunk_prefill_workspace_size": ([G, I, I], S),
+        "gdn_chunk_prefill_min_workspace_size": ([G, I, I], S),
+        "gdn_chunk_prefill": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P, S, P], ctypes.c_int),
+        "gdn_chunk_prefill_noalloc": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
+        "gdn_gated_rmsnorm": ([G, P, P, P, F, P, I, P], ctypes.c_int),
+        "gdn_decode_step": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
+        "gdn_decode_step_fp16_state": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
+        "gdn_gates": ([G, P, P, P, P, P, P, I, P], ctypes.c_int),
+        "gdn_kda_decode_step": ([G, P, P, P, P, F, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
+        "gdn_kda_recurrence": ([G, P, P, F, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
+        "gdn_verify_stash_size": ([G, I, I], S),
+        "gdn_verify": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, I, P, S, P], ctypes.c_int),
+        "gdn_verify_commit": ([G, P, P, S, P, P, I, I, P], ctypes.c_int),
+        "gdn_verify_fp16_state": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, I, P, S, P], ctypes.c_int),
+        "gdn_verify_commit_fp16_state": ([G, P, P, S, P, P, I, I, P], ctypes.c_int),
+        "gdn_check_device_errors": ([P], ctypes.c_int),
+    }
+    if debug:
+        sig.update({
+            "gdn_debug_set_chunk_mode": ([ctypes.c_int], ctypes.c_int),
+            "gdn_debug_get_chunk_mode": ([], ctypes.c_int),
+            "gdn_debug_mma_probe": ([P, P, ctypes.c_int, P, P, P], ctypes.c_int),
+            "gdn_debug_mma_probe_ex": ([P, P, ctypes.c_int, ctypes.c_int, P, P, P], ctypes.c_int),
+            "gdn_debug_set_dropped_copy": ([ctypes.c_uint], ctypes.c_int),
+        })
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
 def load_library():
     """Load libgdn.so (built by ``linear_attention_ssm_gb300.build``); raises if it is missing."""
     global _lib
@@ -45,46 +93,47 @@ def load_library():
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: build it with "
                                "`python -m linear_attention_ssm_gb300.build` (needs nvcc)")
-        lib = ctypes.CDLL(LIB_PATH)
-        P, I, F, S = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
-        G = ctypes.POINTER(_Geo)
-        sig = {
-            "gdn_status_string": ([ctypes.c_int], ctypes.c_char_p),
-            "gdn_last_error_message": ([], ctypes.c_char_p),
-            "gdn_version": ([], ctypes.c_char_p),
-            "gdn_conv1d_prefill": ([G, P, P, P, I, I, P, P, P, P], ctypes.c_int),
-            "gdn_chunk_prefill_workspace_size": ([G, I, I], S),
-            "gdn_chunk_prefill_min_workspace_size": ([G, I, I], S),
-            "gdn_chunk_prefill": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P, S, P], ctypes.c_int),
-            "gdn_chunk_prefill_noalloc": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
-            "gdn_gated_rmsnorm": ([G, P, P, P, F, P, I, P], ctypes.c_int),
-            "gdn_decode_step": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
-            "gdn_decode_step_fp16_state": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
-            "gdn_gates": ([G, P, P, P, P, P, P, I, P], ctypes.c_int),
-            "gdn_kda_decode_step": ([G, P, P, P, P, F, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
-            "gdn_kda_recurrence": ([G, P, P, F, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
-            "gdn_verify_stash_size": ([G, I, I], S),
-            "gdn_verify": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, I, P, S, P], ctypes.c_int),
-            "gdn_verify_commit": ([G, P, P, P, P, I, I, P], ctypes.c_int),
-            "gdn_verify_fp16_state": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, I, P, S, P], ctypes.c_int),
-            "gdn_verify_commit_fp16_state": ([G, P, P, P, P, I, I, P], ctypes.c_int),
-            "gdn_check_device_errors": ([P], ctypes.c_int),
-            "gdn_debug_set_chunk_mode": ([ctypes.c_int], ctypes.c_int),
-            "gdn_debug_get_chunk_mode": ([], ctypes.c_int),
-            "gdn_debug_mma_probe": ([P, P, ctypes.c_int, P, P, P], ctypes.c_int),
-            "gdn_debug_mma_probe_ex": ([P, P, ctypes.c_int, ctypes.c_int, P, P, P], ctypes.c_int),
-        }
-        for name, (args, res) in sig.items():
-            fn = getattr(lib, name)
-            fn.argtypes = args
-            fn.restype = res
-        _lib = lib
-        return lib
+        _lib = _configure(ctypes.CDLL(LIB_PATH), debug=False)
+        return _lib
+
+
+def load_test_library():
+    """Load libgdn_test.so, the build with the verification hooks of gdn_debug.h; raises if it is
+    missing."""
+    global _test_lib
+    with _lock:
+        if _test_lib is not None:
+            return _test_lib
+        if not os.path.exists(TEST_LIB_PATH):
+            raise RuntimeError(f"{TEST_LIB_PATH} is missing: build it with "
+                               "`python -m linear_attention_ssm_gb300.build` (needs nvcc)")
+        _test_lib = _configure(ctypes.CDLL(TEST_LIB_PATH), debug=True)
+        return _test_lib
+
+
+class using_test_library:
+    """Context manager: every binding call inside goes to libgdn_test.so (not thread-safe: for
+    tests)."""
+
+    def __enter__(self):
+        global _override
+        self._prev = _override
+        _override = load_test_library()
+        return _override
+
+    def __exit__(self, *exc):
+        global _override
+        _override = self._prev
+        return False
+
+
+def _L():
+    return _override if _override is not None else load_library()
 
 
 def _check(status: int):
     if status != GDN_OK:
-        lib = load_library()
+        lib = _L()
         name = lib.gdn_status_string(status).decode()
         msg = lib.gdn_last_error_message().decode()
         raise GdnError(status, name, msg)
@@ -120,22 +169,22 @@ def _dev(t, dtype, name, shape=None):
 
 
 def gdn_version() -> str:
-    return load_library().gdn_version().decode()
+    return _L().gdn_version().decode()
 
 
 def gdn_status_string(status: int) -> str:
-    return load_library().gdn_status_string(int(status)).decode()
+    return _L().gdn_status_string(int(status)).decode()
 
 
 def gdn_last_error_message() -> str:
     """The library's message for the last error returned on this thread ("" if none)."""
-    return load_library().gdn_last_error_message().decode()
+    return _L().gdn_last_error_message().decode()
 
 
 def gdn_conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in=None, conv_state_out=None, y=None,
                        geometry: Geometry = QWEN_GDN, stream=None):
     """Causal depthwise conv1d + SiLU over packed sequences; returns y [T, C] bf16."""
-    lib = load_library()
+    lib = _L()
     C, W = geometry.conv_dim, geometry.conv_width
     _dev(x, torch.bfloat16, "x")
     T = x.shape[0]
@@ -155,12 +204,12 @@ def gdn_conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in=None, conv_state_out
 
 def gdn_chunk_prefill_workspace_size(num_seqs: int, total_tokens: int,
                                      geometry: Geometry = QWEN_GDN) -> int:
-    return int(load_library().gdn_chunk_prefill_workspace_size(_geo(geometry), num_seqs, total_tokens))
+    return int(_L().gdn_chunk_prefill_workspace_size(_geo(geometry), num_seqs, total_tokens))
 
 
 def gdn_chunk_prefill_min_workspace_size(num_seqs: int, total_tokens: int,
                                          geometry: Geometry = QWEN_GDN) -> int:
-    return int(load_library().gdn_chunk_prefill_min_workspace_size(_geo(geometry), num_seqs, total_tokens))
+    return int(_L().gdn_chunk_prefill_min_workspace_size(_geo(geometry), num_seqs, total_tokens))
 
 
 def gdn_chunk_prefill(qkv, g, beta, cu_seqlens, q_scale, l2_eps=1e-6, state_in=None, state_out=None,
@@ -171,7 +220,7 @@ def gdn_chunk_prefill(qkv, g, beta, cu_seqlens, q_scale, l2_eps=1e-6, state_in=N
     Returns out [T, Hv, Dv] bf16 (o itself when z is None).  state_out, when given, receives the
     final fp32 states [N, Hv, Dv, Dk]; it may be state_in itself.
     """
-    lib = load_library()
+    lib = _L()
     C, hv, dv, dk = geometry.conv_dim, geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
     N = cu_seqlens.numel() - 1
     T = qkv.shape[0]
@@ -203,7 +252,7 @@ def gdn_chunk_prefill_noalloc(qkv, g, beta, cu_seqlens, q_scale, l2_eps=1e-6, st
     """gdn_chunk_prefill without a caller workspace: the schedule goes to a fixed scratch inside the
     library (at most GDN_NOALLOC_MAX_SEQS sequences per call; calls that overlap on the GPU race on
     it).  Same arguments and result as gdn_chunk_prefill otherwise."""
-    lib = load_library()
+    lib = _L()
     C, hv, dv, dk = geometry.conv_dim, geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
     N = cu_seqlens.numel() - 1
     T = qkv.shape[0]
@@ -225,7 +274,7 @@ def gdn_chunk_prefill_noalloc(qkv, g, beta, cu_seqlens, q_scale, l2_eps=1e-6, st
 
 
 def gdn_gated_rmsnorm(o, z, norm_w, eps=1e-6, out=None, geometry: Geometry = QWEN_GDN, stream=None):
-    lib = load_library()
+    lib = _L()
     hv, dv = geometry.num_v_heads, geometry.head_v_dim
     T = o.shape[0]
     _dev(o, torch.bfloat16, "o", (T, hv, dv))
@@ -246,7 +295,7 @@ def gdn_decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l
     ``state`` is fp32 (gdn_decode_step) or fp16 (gdn_decode_step_fp16_state: the state is half
     precision in memory, widened on load and rounded once on store).
     """
-    lib = load_library()
+    lib = _L()
     fp16_state = state.dtype == torch.float16
     C, W = geometry.conv_dim, geometry.conv_width
     hv, dv, dk = geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
@@ -272,7 +321,7 @@ def gdn_kda_decode_step(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scal
                         l2_eps=1e-6, rms_eps=1e-6, out=None, geometry: Geometry = QWEN_GDN, stream=None):
     """One KDA decode step (decay per key channel, g [B, Hv, Dk] fp32, clamped below at g_min);
     conv_state and state are updated in place.  Returns out."""
-    lib = load_library()
+    lib = _L()
     C, W = geometry.conv_dim, geometry.conv_width
     hv, dv, dk = geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
     B = x.shape[0]
@@ -302,7 +351,7 @@ def gdn_kda_recurrence(qkv, g, beta, cu_seqlens, q_scale, g_min=float("-inf"), l
     Returns out [T, Hv, Dv] bf16 (o itself when z is None).  state_out, when given, receives the
     final fp32 states [N, Hv, Dv, Dk]; it may be state_in itself.
     """
-    lib = load_library()
+    lib = _L()
     C, hv, dv, dk = geometry.conv_dim, geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
     N = cu_seqlens.numel() - 1
     T = qkv.shape[0]
@@ -337,7 +386,7 @@ def gdn_gates(a, b, A_log, dt_bias, g=None, beta=None, geometry: Geometry = QWEN
 
     a, b: [rows, Hv] bf16; A_log, dt_bias: [Hv] fp32.  Returns (g, beta), [rows, Hv] fp32.
     """
-    lib = load_library()
+    lib = _L()
     hv = geometry.num_v_heads
     rows = a.shape[0]
     _dev(a, torch.bfloat16, "a", (rows, hv))
@@ -356,7 +405,7 @@ def gdn_gates(a, b, A_log, dt_bias, g=None, beta=None, geometry: Geometry = QWEN
 
 
 def gdn_verify_stash_size(batch: int, rows: int, geometry: Geometry = QWEN_GDN) -> int:
-    return int(load_library().gdn_verify_stash_size(_geo(geometry), int(batch), int(rows)))
+    return int(_L().gdn_verify_stash_size(_geo(geometry), int(batch), int(rows)))
 
 
 def gdn_verify(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps=1e-6, rms_eps=1e-6,
@@ -366,7 +415,7 @@ def gdn_verify(x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps
     ``state`` is fp32 (gdn_verify) or fp16 (gdn_verify_fp16_state).  Returns (out [B, K, Hv, Dv]
     bf16, stash uint8) -- pass the stash to gdn_verify_commit.
     """
-    lib = load_library()
+    lib = _L()
     fp16_state = state.dtype == torch.float16
     C, W = geometry.conv_dim, geometry.conv_width
     hv, dv, dk = geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
@@ -397,7 +446,7 @@ def gdn_verify_commit(committed_rows, stash, conv_state, state, rows: int, geome
                       stream=None):
     """Commit committed_rows[b] (device int32, 0..rows) rows of a verify into conv_state and state
     (fp32, or fp16: gdn_verify_commit_fp16_state)."""
-    lib = load_library()
+    lib = _L()
     fp16_state = state.dtype == torch.float16
     C, W = geometry.conv_dim, geometry.conv_width
     hv, dv, dk = geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
@@ -406,10 +455,8 @@ def gdn_verify_commit(committed_rows, stash, conv_state, state, rows: int, geome
     _dev(stash, torch.uint8, "stash")
     _dev(conv_state, torch.bfloat16, "conv_state", (B, C, W - 1))
     _dev(state, torch.float16 if fp16_state else torch.float32, "state", (B, hv, dv, dk))
-    if stash.numel() < gdn_verify_stash_size(B, rows, geometry):
-        raise ValueError("stash is smaller than gdn_verify_stash_size(batch, rows)")
     fn = lib.gdn_verify_commit_fp16_state if fp16_state else lib.gdn_verify_commit
-    _check(fn(_geo(geometry), _p(committed_rows), _p(stash), _p(conv_state), _p(state), B, int(rows),
+    _check(fn(_geo(geometry), _p(committed_rows), _p(stash), stash.numel(), _p(conv_state), _p(state), B, int(rows),
               _stream(stream)))
 
 
@@ -432,38 +479,52 @@ def gdn_verify_commit_fp16_state(committed_rows, stash, conv_state, state, rows:
 
 def gdn_check_device_errors(stream=None):
     """Synchronise the stream and raise GdnError if a kernel flagged a device-side fault."""
-    _check(load_library().gdn_check_device_errors(_stream(stream)))
+    _check(_L().gdn_check_device_errors(_stream(stream)))
+
+
+def _check_test(status: int):
+    if status != GDN_OK:
+        lib = load_test_library()
+        raise GdnError(status, lib.gdn_status_string(status).decode(), lib.gdn_last_error_message().decode())
 
 
 def gdn_debug_set_chunk_mode(mode: int):
-    _check(load_library().gdn_debug_set_chunk_mode(int(mode)))
+    """Chunk design of later libgdn_test.so calls (0 default, 1 fused emulated, 2 fused)."""
+    _check_test(load_test_library().gdn_debug_set_chunk_mode(int(mode)))
 
 
 def gdn_debug_get_chunk_mode() -> int:
-    return int(load_library().gdn_debug_get_chunk_mode())
+    return int(load_test_library().gdn_debug_get_chunk_mode())
+
+
+def gdn_debug_set_dropped_copy(which: int):
+    """libgdn_test.so only: bit 0 drops the binary16 decode step's state copy, bit 1 the chunk
+    state kernel's first vector-block copy, so that the bounded wait on it runs out (0: off)."""
+    _check_test(load_test_library().gdn_debug_set_dropped_copy(int(which)))
 
 
 def gdn_debug_mma_probe(A, B, stream=None):
-    """D = A @ B.T on one tcgen05 tile (A [128, 64], B [64 or 128, 64] bf16 CUDA tensors)."""
-    lib = load_library()
+    """D = A @ B.T on one tcgen05 tile (A [128, 64], B [64 or 128, 64] bf16 CUDA tensors);
+    libgdn_test.so."""
+    lib = load_test_library()
     _dev(A, torch.bfloat16, "A", (128, 64))
     n = B.shape[0]
     _dev(B, torch.bfloat16, "B", (n, 64))
     D = torch.full((128, n), float("nan"), dtype=torch.float32, device=A.device)
     status = torch.zeros(1, dtype=torch.int32, device=A.device)
-    _check(lib.gdn_debug_mma_probe(_p(A), _p(B), n, _p(D), _p(status), _stream(stream)))
+    _check_test(lib.gdn_debug_mma_probe(_p(A), _p(B), n, _p(D), _p(status), _stream(stream)))
     return D, status
 
 
 def gdn_debug_mma_probe_ex(A, B, flags, stream=None):
     """As gdn_debug_mma_probe with flags: bit 0 A from tensor memory, bit 1 B MN-major."""
-    lib = load_library()
+    lib = load_test_library()
     _dev(A, torch.bfloat16, "A", (128, 64))
     n = B.shape[0]
     _dev(B, torch.bfloat16, "B", (n, 64))
     D = torch.full((128, n), float("nan"), dtype=torch.float32, device=A.device)
     status = torch.zeros(1, dtype=torch.int32, device=A.device)
-    _check(lib.gdn_debug_mma_probe_ex(_p(A), _p(B), n, int(flags), _p(D), _p(status), _stream(stream)))
+    _check_test(lib.gdn_debug_mma_probe_ex(_p(A), _p(B), n, int(flags), _p(D), _p(status), _stream(stream)))
     return D, status
 
 

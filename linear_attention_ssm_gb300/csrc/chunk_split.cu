@@ -88,6 +88,11 @@ constexpr uint32_t SC_COLS = 256;
 constexpr int kMaxSegments = 4;
 __host__ __device__ __forceinline__ int seg_begin(int k, int nch, int nseg) { return (int)(((long)k * nch) / nseg); }
 
+#ifdef GDN_TEST_HOOKS
+constexpr uint32_t kTestWaitLimit = 1u << 12;  // polls of a wait whose copy the hook dropped
+__device__ unsigned g_test_drop_vec_copy;      // 1: an item's first vector-block copy is not issued
+#endif
+
 struct PrepParams {
   CUtensorMap tmap;  // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle
   const float* g;
@@ -578,9 +583,13 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
     mbar_arrive_expect_tx(bar_tp, kRecTP);
     bulk_load(sb + SS_T, rec + REC_T, kRecTP, bar_tp);
   };
-  auto issue_vec = [&](int gc, int h, int vb) {
+  auto issue_vec = [&](int gc, int h, int vb, bool first = false) {
     const uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * REC_BYTES;
     mbar_arrive_expect_tx(bar_vec0 + 8 * vb, kRecVec);
+#ifdef GDN_TEST_HOOKS
+    if (first && g_test_drop_vec_copy) return;
+#endif
+    (void)first;
     bulk_load(sb + SS_VEC + vb * kRecVec, rec + REC_VEC, kRecVec, bar_vec0 + 8 * vb);
   };
   // 32 fp32 values of this thread's row (tokens part * kW ..) -> bf16 hi / lo pairs in tensor memory:
@@ -636,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       continue;
     }
     if (tid == 0 && seq_e > seq_s) {
-      issue_vec(gc0, h, 0);
+      issue_vec(gc0, h, 0, true);
       issue_qk_tiles(sb + SS_QK, &p.tmap, p.Hk, seq_s, kh, bar_qk);
       issue_v(seq_s, h);
       issue_tp(gc0, h);
@@ -673,7 +682,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
       const float* vec = reinterpret_cast<const float*>(sm + SS_VEC + vb * kRecVec);
 
       {
-        const bool got = mbar_wait(bar_vec0 + 8 * vb, (ph_vec >> vb) & 1u, kWaitLimit);
+#ifdef GDN_TEST_HOOKS
+        const uint32_t vec_limit = g_test_drop_vec_copy ? kTestWaitLimit : kWaitLimit;
+#else
+        const uint32_t vec_limit = kWaitLimit;
+#endif
+        const bool got = mbar_wait(bar_vec0 + 8 * vb, (ph_vec >> vb) & 1u, vec_limit);
         ph_vec ^= 1u << vb;
         pend_vec &= ~(1u << vb);
         if (!got) raise_error(p.err, kErrTimeout);
@@ -1035,6 +1049,39 @@ cudaError_t side_stream(cudaStream_t* out) {
   return cudaSuccess;
 }
 
+// Events ordering the segments' prep and state launches, created once per (host thread, device)
+// and reused by every later call of that thread.  They are per thread because the launcher records
+// an event and then makes the other stream wait on it: with events shared between threads, one
+// thread's wait could pick up another thread's later record.  Within one thread each wait is
+// issued right after its own record, so reuse across calls is safe.
+struct SegmentEvents {
+  cudaEvent_t ev[64][kMaxSegments + 1] = {};
+  ~SegmentEvents() {
+    for (auto& d : ev)
+      for (cudaEvent_t e : d)
+        if (e) cudaEventDestroy(e);  // after the context is gone this returns an error: ignored
+  }
+};
+
+cudaError_t segment_events(cudaEvent_t** out) {
+  thread_local SegmentEvents cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  for (int k = 0; k <= kMaxSegments; ++k) {
+    if (!cache.ev[dev][k]) {
+      e = cudaEventCreateWithFlags(&cache.ev[dev][k], cudaEventDisableTiming);
+      if (e != cudaSuccess) {
+        cache.ev[dev][k] = nullptr;
+        return e;
+      }
+    }
+  }
+  *out = cache.ev[dev];
+  return cudaSuccess;
+}
+
 template <typename K>
 cudaError_t set_smem_once(K kernel, uint32_t bytes, int (&done)[64]) {
   int dev = 0;
@@ -1048,6 +1095,10 @@ cudaError_t set_smem_once(K kernel, uint32_t bytes, int (&done)[64]) {
 }
 
 }  // namespace
+
+#ifdef GDN_TEST_HOOKS
+cudaError_t test_set_dropped_copy_chunk(unsigned on) { return cudaMemcpyToSymbol(g_test_drop_vec_copy, &on, sizeof on); }
+#endif
 
 size_t split_workspace_bytes(int N, int T, int Hk, int Hv) {
   (void)Hk;
@@ -1092,19 +1143,12 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
   chunk_segments_kernel<<<1, 1024, 0, env.stream>>>(cu, N, nseg, lay.seg_pref, lay.counters);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  cudaEvent_t ev[kMaxSegments + 1] = {};
-  auto destroy_events = [&]() {
-    for (int k = 0; k <= kMaxSegments; ++k)
-      if (ev[k]) cudaEventDestroy(ev[k]);
-  };
+  cudaEvent_t* ev = nullptr;
   if (nseg > 1) {
-    for (int k = 0; k <= nseg && e == cudaSuccess; ++k) e = cudaEventCreateWithFlags(&ev[k], cudaEventDisableTiming);
+    e = segment_events(&ev);
     if (e == cudaSuccess) e = cudaEventRecord(ev[nseg], env.stream);  // schedule and segment tables written
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side, ev[nseg], 0);
-    if (e != cudaSuccess) {
-      destroy_events();
-      return e;
-    }
+    if (e != cudaSuccess) return e;
   }
 
   PrepParams pp;
@@ -1158,7 +1202,6 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
     chunk_state_kernel<<<state_grid, kThreads, SS_BYTES, env.stream>>>(sp);
     e = cudaGetLastError();
   }
-  destroy_events();  // released once the work recorded on them completes
   return e;
 }
 

@@ -36,6 +36,11 @@ constexpr int kMaxRatio = 12;                             // V heads per K head 
 constexpr uint32_t kStateWaitLimit = 1u << 20;            // polls of the state-slice barrier
 constexpr size_t kMaxStagedBytes = 96 * 1024;             // largest state slice staged in shared memory
 
+#ifdef GDN_TEST_HOOKS
+constexpr uint32_t kTestWaitLimit = 1u << 12;  // polls of a wait whose copy the hook dropped
+__device__ unsigned g_test_drop_state_copy;    // 1: the staged state copy is not issued
+#endif
+
 // Four consecutive state elements of a row (index i counts groups of four), widened to fp32.  The
 // fp16 storage form holds the state as IEEE binary16 in memory only: it is widened on load, the
 // step runs in fp32 exactly as for the fp32 state, and the new state is rounded once (to nearest,
@@ -112,7 +117,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
       fence_mbar_init();
       const uint32_t bytes = (uint32_t)((size_t)R * kHeadDim * kHeadDim * sizeof(StateT));
       mbar_arrive_expect_tx(bar, bytes);
-      bulk_load(smem_u32(s_state), slice, bytes, bar);
+#ifdef GDN_TEST_HOOKS
+      if (!g_test_drop_state_copy)
+#endif
+        bulk_load(smem_u32(s_state), slice, bytes, bar);
     }
   }
 
@@ -167,10 +175,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
                                 s_k[lane * 4 + 2] * s_norm[1], s_k[lane * 4 + 3] * s_norm[1]);
 
   if constexpr (kStaged) {  // the state slice has landed in shared memory (bounded wait)
-    const bool got = mbar_wait(smem_u32(&s_bar), 0, kStateWaitLimit);
+#ifdef GDN_TEST_HOOKS
+    const uint32_t limit = g_test_drop_state_copy ? kTestWaitLimit : kStateWaitLimit;
+#else
+    const uint32_t limit = kStateWaitLimit;
+#endif
+    const bool got = mbar_wait(smem_u32(&s_bar), 0, limit);
     if (!got) raise_error(err, kErrTimeout);
     if (!__syncthreads_and(got ? 1 : 0)) {
-      if (!got) mbar_wait(smem_u32(&s_bar), 0, kStateWaitLimit);  // let the copy land before leaving
+      if (!got) mbar_wait(smem_u32(&s_bar), 0, limit);  // let the copy land before leaving
       return;
     }
   }
@@ -254,6 +267,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
 }  // namespace
 
 int decode_max_ratio() { return kMaxRatio; }
+
+#ifdef GDN_TEST_HOOKS
+cudaError_t test_set_dropped_copy_decode(unsigned on) {
+  return cudaMemcpyToSymbol(g_test_drop_state_copy, &on, sizeof on);
+}
+#endif
 
 cudaError_t launch_kda_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
                                    uint16_t* conv_state, const float* g, float g_min, const float* beta,

@@ -3,13 +3,16 @@
 // Every entry point checks its arguments on the host before it launches anything; a call that
 // returns an error has launched nothing.  Device-side faults (bad cu_seqlens contents, a bounded
 // wait that ran out) set bits in a per-device error word that gdn_check_device_errors() reads.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <string>
 
 #include "../../include/gdn.h"
+#ifdef GDN_TEST_HOOKS
 #include "../../include/gdn_debug.h"
+#endif
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 
@@ -18,10 +21,16 @@ namespace {
 __device__ unsigned g_gdn_error_word;
 
 thread_local std::string g_last_error;
-int g_chunk_mode = 0;
+#ifdef GDN_TEST_HOOKS
+std::atomic<int> g_chunk_mode{0};  // the test library's chunk-design selection (gdn_debug.h)
+#else
+constexpr int g_chunk_mode = 0;    // the product library always takes the default design
+#endif
 
 constexpr int kMaxDevices = 64;
-unsigned* g_err_ptr[kMaxDevices] = {nullptr};
+// Device address of the error word, per device index, looked up on the first call that needs it.
+// Two host threads making their first call at once both store the same address.
+std::atomic<unsigned*> g_err_ptr[kMaxDevices] = {};
 
 gdn_status fail(gdn_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 gdn_status fail(gdn_status s, const char* fmt, ...) {
@@ -81,13 +90,15 @@ gdn_status make_env(void* stream, gdn::LaunchEnv* env) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(GDN_ERR_CUDA, "device index %d out of range", dev);
-  if (!g_err_ptr[dev]) {
+  unsigned* err = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (!err) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_gdn_error_word);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    g_err_ptr[dev] = static_cast<unsigned*>(p);
+    err = static_cast<unsigned*>(p);
+    g_err_ptr[dev].store(err, std::memory_order_release);
   }
-  env->err = g_err_ptr[dev];
+  env->err = err;
   env->num_sms = 0;
   env->stream = static_cast<cudaStream_t>(stream);
   return GDN_OK;
@@ -419,8 +430,8 @@ gdn_status verify(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* co
 }
 
 gdn_status verify_commit(const gdn_geometry* geo, const int32_t* committed_rows, const void* stash,
-                         gdn_bf16* conv_state, void* state, bool fp16_state, int32_t batch, int32_t rows,
-                         void* stream) {
+                         size_t stash_bytes, gdn_bf16* conv_state, void* state, bool fp16_state, int32_t batch,
+                         int32_t rows, void* stream) {
   gdn_status s = check_verify_shape(geo, batch, rows);
   if (s != GDN_OK) return s;
   if (batch == 0) return ok();
@@ -430,6 +441,10 @@ gdn_status verify_commit(const gdn_geometry* geo, const int32_t* committed_rows,
   GDN_REQUIRE(stash, "stash");
   GDN_REQUIRE(conv_state, "conv_state");
   GDN_REQUIRE(state, "state");
+  const size_t need = gdn_verify_stash_size(geo, batch, rows);
+  if (stash_bytes < need)
+    return fail(GDN_ERR_WORKSPACE, "stash of %zu bytes required for batch %d x rows %d (got %zu)", need, batch, rows,
+                stash_bytes);
   gdn::LaunchEnv env;
   if ((s = make_env(stream, &env)) != GDN_OK) return s;
   return launched(gdn::launch_verify_commit(env, committed_rows, stash, conv_state, state, fp16_state, batch, rows,
@@ -458,14 +473,15 @@ gdn_status gdn_verify_fp16_state(const gdn_geometry* geo, const gdn_bf16* x, con
 }
 
 gdn_status gdn_verify_commit(const gdn_geometry* geo, const int32_t* committed_rows, const void* stash,
-                             gdn_bf16* conv_state, float* state, int32_t batch, int32_t rows, void* stream) {
-  return verify_commit(geo, committed_rows, stash, conv_state, state, false, batch, rows, stream);
+                             size_t stash_bytes, gdn_bf16* conv_state, float* state, int32_t batch, int32_t rows,
+                             void* stream) {
+  return verify_commit(geo, committed_rows, stash, stash_bytes, conv_state, state, false, batch, rows, stream);
 }
 
 gdn_status gdn_verify_commit_fp16_state(const gdn_geometry* geo, const int32_t* committed_rows, const void* stash,
-                                        gdn_bf16* conv_state, gdn_f16* state, int32_t batch, int32_t rows,
-                                        void* stream) {
-  return verify_commit(geo, committed_rows, stash, conv_state, state, true, batch, rows, stream);
+                                        size_t stash_bytes, gdn_bf16* conv_state, gdn_f16* state, int32_t batch,
+                                        int32_t rows, void* stream) {
+  return verify_commit(geo, committed_rows, stash, stash_bytes, conv_state, state, true, batch, rows, stream);
 }
 
 // ---- allocation-free chunk prefill: the schedule lives in a fixed device array of this file
@@ -473,7 +489,9 @@ gdn_status gdn_verify_commit_fp16_state(const gdn_geometry* geo, const int32_t* 
 
 namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
-void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+// The array's device address per device index (the first call on a device looks it up; racing
+// first calls store the same address).  It is not refreshed after cudaDeviceReset.
+std::atomic<void*> g_noalloc_ptr[kMaxDevices] = {};
 }  // namespace
 
 extern "C" {
@@ -492,16 +510,16 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_geometry* geo, const gdn_bf16* qk
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(GDN_ERR_CUDA, "device index %d out of range", dev);
-  if (!g_noalloc_ptr[dev]) {
+  void* scratch = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (!scratch) {
     // host code only sees a stand-in for the array: its device address comes from the runtime
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess || !ptr)
+    e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+    if (e != cudaSuccess || !scratch)
       return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-    g_noalloc_ptr[dev] = ptr;
+    g_noalloc_ptr[dev].store(scratch, std::memory_order_release);
   }
   return gdn_chunk_prefill(geo, qkv, g, beta, cu_seqlens, num_seqs, total_tokens, q_scale, l2_eps, state_in,
-                           state_out, z, norm_w, rms_eps, out, g_noalloc_ptr[dev], GDN_NOALLOC_SCRATCH_BYTES, stream);
+                           state_out, z, norm_w, rms_eps, out, scratch, GDN_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 gdn_status gdn_check_device_errors(void* stream) {
@@ -524,12 +542,22 @@ gdn_status gdn_check_device_errors(void* stream) {
   return ok();
 }
 
+#ifdef GDN_TEST_HOOKS
 gdn_status gdn_debug_set_chunk_mode(int mode) {
   if (mode < 0 || mode > 2) return fail(GDN_ERR_INVALID_ARGUMENT, "mode must be 0, 1 or 2");
-  g_chunk_mode = mode;
+  g_chunk_mode.store(mode);
   return ok();
 }
 
-int gdn_debug_get_chunk_mode(void) { return g_chunk_mode; }
+int gdn_debug_get_chunk_mode(void) { return g_chunk_mode.load(); }
+
+gdn_status gdn_debug_set_dropped_copy(unsigned which) {
+  if (which & ~3u) return fail(GDN_ERR_INVALID_ARGUMENT, "which must be a combination of bits 0 and 1");
+  cudaError_t e = gdn::test_set_dropped_copy_decode(which & 1u);
+  if (e == cudaSuccess) e = gdn::test_set_dropped_copy_chunk((which >> 1) & 1u);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "setting the dropped-copy hook: %s", cudaGetErrorString(e));
+  return ok();
+}
+#endif
 
 }  // extern "C"

@@ -96,4 +96,12 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
                                        const float* state_in, float* state_out, const uint16_t* z,
                                        const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace);
 
+#ifdef GDN_TEST_HOOKS
+// Test library only: while set (1), the copy named below is not issued although its barrier is
+// armed for its bytes, so the bounded wait on it runs out (with a short limit) and the kernel reports
+// a timeout -- nothing is in flight when the CTA leaves.  Set for the current device.
+cudaError_t test_set_dropped_copy_decode(unsigned on);  // the binary16 decode step's state-slice copy
+cudaError_t test_set_dropped_copy_chunk(unsigned on);   // the chunk state kernel's first vector-block copy
+#endif
+
 }  // namespace gdn

@@ -1,6 +1,6 @@
 /*
- * c_abi_check.c -- a plain C11 client of libgdn.so, built against include/gdn.h and
- * include/gdn_debug.h alone.  It calls only paths that end in host-side validation or pure host
+ * c_abi_check.c -- a plain C11 client of libgdn.so, built against include/gdn.h alone (the
+ * hooks of include/gdn_debug.h exist only in the test build, libgdn_test.so).  It calls only paths that end in host-side validation or pure host
  * arithmetic (no CUDA call is reached), so it runs without a GPU; tests/test_abi.py compiles it
  * with gcc -std=c11 -Wall -Wextra -Werror and expects it to print "ok".
  */
@@ -10,7 +10,6 @@
 #include <string.h>
 
 #include "gdn.h"
-#include "gdn_debug.h"
 
 #define EXPECT(expr, want)                                                                       \
   do {                                                                                           \
@@ -33,7 +32,6 @@ int main(void) {
 
   if (strncmp(gdn_version(), "gdn-gb300", 9) != 0) return 1;
   if (strcmp(gdn_status_string(GDN_ERR_MISALIGNED), "GDN_ERR_MISALIGNED") != 0) return 1;
-  if (gdn_debug_get_chunk_mode() != 0) return 1;
 
   /* geometry and size checks */
   EXPECT(gdn_conv1d_prefill(&uneven, fake, fake, fake, 1, 4, NULL, NULL, fake, NULL), GDN_ERR_UNSUPPORTED_GEOMETRY);
@@ -59,7 +57,8 @@ int main(void) {
   EXPECT(gdn_verify(&geo, fake, fake, fake, fake, fake, fake, fake, fake, 0.088f, 1e-6f, 1e-6f, fake, 4, 18, fake,
                     1u << 30, NULL),
          GDN_ERR_INVALID_ARGUMENT);
-  EXPECT(gdn_verify_commit(&geo, fake, fake, fake, fake, 4, 0, NULL), GDN_ERR_INVALID_ARGUMENT);
+  EXPECT(gdn_verify_commit(&geo, fake, fake, (size_t)1 << 30, fake, fake, 4, 0, NULL), GDN_ERR_INVALID_ARGUMENT);
+  EXPECT(gdn_verify_commit(&geo, fake, fake, 100, fake, fake, 4, 8, NULL), GDN_ERR_WORKSPACE);
 
   /* empty calls launch nothing and succeed */
   EXPECT(gdn_decode_step(&geo, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0.088f, 1e-6f, 1e-6f, NULL, 0, NULL),

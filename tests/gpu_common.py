@@ -35,13 +35,19 @@ def lib():
 
 @pytest.fixture(params=[0, 1, 2], ids=["split", "emulated", "fused"], name="mode")
 def chunk_mode(request):
-    """Runs a chunk-prefill test once per chunk design: the split path (prep + state kernels), the
-    fused kernel with its MMAs emulated on the CUDA cores, and the fused kernel on the tensor
-    cores."""
+    """Runs a chunk-prefill test once per chunk design: the product library's split path (prep +
+    state kernels), and in the test build (libgdn_test.so) the fused kernel with its MMAs emulated
+    on the CUDA cores and the fused kernel on the tensor cores."""
     g = lib()
-    g.gdn_debug_set_chunk_mode(request.param)
-    yield request.param
-    g.gdn_debug_set_chunk_mode(0)
+    if request.param == 0:  # the product library's own design
+        yield 0
+        return
+    with g.using_test_library():  # the other designs exist only in the test build
+        g.gdn_debug_set_chunk_mode(request.param)
+        try:
+            yield request.param
+        finally:
+            g.gdn_debug_set_chunk_mode(0)
 
 
 def to_dev(t):

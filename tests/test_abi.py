@@ -15,10 +15,10 @@ from linear_attention_ssm_gb300 import binding  # noqa: E402
 from linear_attention_ssm_gb300.synth import QWEN_GDN, Geometry  # noqa: E402
 
 
-def declared_symbols():
+def declared_symbols(headers=None):
     names = set()
     for fn in os.listdir(INCLUDE):
-        if fn.endswith(".h"):
+        if fn.endswith(".h") and (headers is None or fn in headers):
             text = open(os.path.join(INCLUDE, fn)).read()
             names |= set(re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", text))
     return sorted(names)
@@ -26,10 +26,15 @@ def declared_symbols():
 
 @pytest.fixture(scope="module")
 def lib():
-    if not os.path.exists(binding.LIB_PATH):
+    if not os.path.exists(binding.LIB_PATH) or not os.path.exists(binding.TEST_LIB_PATH):
         from linear_attention_ssm_gb300 import build
         build.build()
     return binding.load_library()
+
+
+@pytest.fixture(scope="module")
+def test_lib(lib):
+    return binding.load_test_library()
 
 
 def test_header_declares_the_boundary():
@@ -39,9 +44,24 @@ def test_header_declares_the_boundary():
         assert required in names
 
 
-def test_library_exports_every_declared_symbol(lib):
-    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+def test_library_exports_every_declared_symbol(lib, test_lib):
+    """libgdn.so exports every entry point of gdn.h and none of the verification hooks of
+    gdn_debug.h; the test build, libgdn_test.so, exports both."""
+    product = declared_symbols({"gdn.h"})
+    hooks = declared_symbols({"gdn_debug.h"})
+    assert hooks and set(product) | set(hooks) == set(declared_symbols())
+    missing = [n for n in product if not hasattr(lib, n)]
     assert not missing, missing
+    leaked = [n for n in hooks if hasattr(lib, n)]
+    assert not leaked, f"the product library exports test hooks: {leaked}"
+    missing = [n for n in product + hooks if not hasattr(test_lib, n)]
+    assert not missing, missing
+
+
+def test_test_hooks_validate_their_arguments(test_lib):
+    assert test_lib.gdn_debug_set_chunk_mode(3) == 1
+    assert test_lib.gdn_debug_get_chunk_mode() == 0
+    assert test_lib.gdn_debug_set_dropped_copy(4) == 1
 
 
 def test_chunk_size_constant_matches_pages():
@@ -166,13 +186,17 @@ def test_verify_stash_size_and_argument_checks(lib):
     assert lib.gdn_verify(*args, 0, 8, None, 0, None) == 0          # nothing to do
     # 12 V heads per K head: 17 rows no longer fit the kernel's shared memory
     assert lib.gdn_verify(_geo(num_k_heads=4, num_v_heads=48), *args[1:], 4, 17, FAKE, big, None) == 2
-    assert lib.gdn_verify_commit(geo, FAKE, FAKE, FAKE, FAKE, 4, 18, None) == 1
-    assert lib.gdn_verify_commit(geo, None, FAKE, FAKE, FAKE, 4, 8, None) == 1
-    assert lib.gdn_verify_commit(geo, ctypes.c_void_p(0x10002), FAKE, FAKE, FAKE, 4, 8, None) == 3
-    assert lib.gdn_verify_commit(geo, None, None, None, None, 0, 8, None) == 0
+    assert lib.gdn_verify_commit(geo, FAKE, FAKE, big, FAKE, FAKE, 4, 18, None) == 1
+    assert lib.gdn_verify_commit(geo, None, FAKE, big, FAKE, FAKE, 4, 8, None) == 1
+    assert lib.gdn_verify_commit(geo, ctypes.c_void_p(0x10002), FAKE, big, FAKE, FAKE, 4, 8, None) == 3
+    assert lib.gdn_verify_commit(geo, None, None, 0, None, None, 0, 8, None) == 0
+    # a stash sized for fewer rows (or sequences) than the commit names is refused
+    assert lib.gdn_verify_commit(geo, FAKE, FAKE, 4 * 8 * 53440 - 1, FAKE, FAKE, 4, 8, None) == 7
+    assert lib.gdn_verify_commit(geo, FAKE, FAKE, 4 * 6 * 53440, FAKE, FAKE, 4, 8, None) == 7
     assert lib.gdn_verify_fp16_state(*args, 4, 18, FAKE, big, None) == 1
     assert lib.gdn_verify_fp16_state(*args, 4, 8, FAKE, 4 * 8 * 53440 - 1, None) == 7
-    assert lib.gdn_verify_commit_fp16_state(geo, FAKE, FAKE, FAKE, ODD, 4, 8, None) == 3
+    assert lib.gdn_verify_commit_fp16_state(geo, FAKE, FAKE, big, FAKE, ODD, 4, 8, None) == 3
+    assert lib.gdn_verify_commit_fp16_state(geo, FAKE, FAKE, 3 * 8 * 53440, FAKE, FAKE, 4, 8, None) == 7
 
 
 def test_gates_reject_bad_arguments(lib):

@@ -204,8 +204,8 @@ def test_more_sequences_than_the_sorted_schedule():
 
 
 def test_minimum_workspace_runs_the_fused_kernel():
-    """With only the minimum workspace, the default mode runs the one-kernel path: bit-identical
-    to forcing it, and within the tolerances of the oracle like the split path."""
+    """With only the minimum workspace, the product library runs the one-kernel path: bit-identical
+    to forcing it in the test build, and within the tolerances of the oracle like the split path."""
     g = lib()
     inp = prefill_inputs([150, 64, 9], seed=41)
     ref = run_oracle(inp)
@@ -215,15 +215,20 @@ def test_minimum_workspace_runs_the_fused_kernel():
     small = torch.empty(g.gdn_chunk_prefill_min_workspace_size(N, T), dtype=torch.uint8, device=DEV)
     assert g.gdn_chunk_prefill_workspace_size(N, T) > small.numel()
     results = []
-    for mode_, ws in ((0, small), (2, None), (0, None)):
-        g.gdn_debug_set_chunk_mode(mode_)
+
+    def call(ws):
+        st = torch.empty((N, 48, 128, 128), dtype=torch.float32, device=DEV)
+        out = g.gdn_chunk_prefill(*args, st, inp["z"].to(DEV), inp["norm_w"].to(DEV), 1e-6, workspace=ws)
+        g.gdn_check_device_errors()
+        return out, st
+    results.append(call(small))              # the product library, minimum workspace: fused kernel
+    with g.using_test_library():             # the test build, fused kernel forced
+        g.gdn_debug_set_chunk_mode(2)
         try:
-            st = torch.empty((N, 48, 128, 128), dtype=torch.float32, device=DEV)
-            out = g.gdn_chunk_prefill(*args, st, inp["z"].to(DEV), inp["norm_w"].to(DEV), 1e-6, workspace=ws)
-            g.gdn_check_device_errors()
+            results.append(call(None))
         finally:
             g.gdn_debug_set_chunk_mode(0)
-        results.append((out, st))
+    results.append(call(None))               # the product library, full workspace: split path
     assert torch.equal(results[0][0], results[1][0]) and torch.equal(results[0][1], results[1][1])
     for out, st in results:
         assert_out_close(out, ref["out"])

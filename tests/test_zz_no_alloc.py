@@ -12,7 +12,8 @@ import ctypes
 import pytest
 import torch
 
-from linear_attention_ssm_gb300.synth import QWEN_GDN, cu_seqlens_of, prefill_inputs
+import oracle
+from linear_attention_ssm_gb300.synth import QWEN_GDN, Geometry, cu_seqlens_of, prefill_inputs
 from tests.gpu_common import DEV, assert_out_close, assert_state_close, lib
 
 pytestmark = pytest.mark.gpu
@@ -49,6 +50,51 @@ def test_noalloc_entry_point_matches_workspace_entry_point_twice():
         g.gdn_check_device_errors()
         assert_out_close(out, out_ref.double())
         assert_state_close(st, st_ref.double())
+        # and against the oracle itself, on the conv output both calls read
+        ref = oracle.gdn_recurrence(qkv.cpu(), inp["g"], inp["beta"], inp["cu_seqlens"], 16, 48, 128, 128,
+                                    inp["q_scale"], 1e-6, inp["state0"])
+        assert_out_close(out, oracle.gated_rmsnorm(ref[0], inp["z"], inp["norm_w"], 1e-6))
+        assert_state_close(st, ref[1])
+
+
+def test_noalloc_at_the_scratch_limit():
+    """16,384 sequences (the most the fixed scratch holds; beyond the longest-first sort, so the
+    schedule keeps the given order), nearly all empty, on a small head geometry (1 K head, 2 V
+    heads: 128 KB of state per sequence): the few real ones match the workspace entry point and
+    the oracle, and the empty ones pass their states through."""
+    g = lib()
+    from linear_attention_ssm_gb300 import binding
+    clib = binding.load_library()
+    gq = Geometry(num_k_heads=1, num_v_heads=2)
+    geo = binding._geo(gq)
+    n = 16384
+    real = {0: 70, 5000: 1, 9999: 130, 16383: 64}
+    lengths = [real.get(i, 0) for i in range(n)]
+    inp = prefill_inputs([real[k] for k in sorted(real)], seed=43, geo=gq)
+    T = sum(lengths)
+    cu = cu_seqlens_of(lengths).to(DEV)
+    gen = torch.Generator(device=DEV).manual_seed(44)
+    s0 = 0.1 * torch.randn((n, 2, 128, 128), generator=gen, device=DEV)
+    for j, i in enumerate(sorted(real)):
+        s0[i] = inp["state0"][j].to(DEV)
+    qkv = g.gdn_conv1d_prefill(inp["x"].to(DEV), inp["conv_w"].to(DEV), inp["cu_seqlens"].to(DEV), geometry=gq)
+    gg, bb, z, nw = inp["g"].to(DEV), inp["beta"].to(DEV), inp["z"].to(DEV), inp["norm_w"].to(DEV)
+    st_ref = torch.empty_like(s0)
+    out_ref = g.gdn_chunk_prefill(qkv, gg, bb, cu, inp["q_scale"], 1e-6, s0, st_ref, z, nw, 1e-6, geometry=gq)
+    st = torch.full_like(s0, float("nan"))
+    out = torch.full((T, 2, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    rc = _noalloc_call(clib, geo, qkv, gg, bb, cu, n, T, inp["q_scale"], s0, st, z, nw, out)
+    assert rc == 0, clib.gdn_last_error_message().decode()
+    g.gdn_check_device_errors()
+    assert_out_close(out, out_ref.double())
+    empty = torch.tensor([L == 0 for L in lengths], device=DEV)
+    assert torch.equal(st[empty], s0[empty])
+    ref = oracle.gdn_recurrence(qkv.cpu(), inp["g"], inp["beta"], inp["cu_seqlens"], 1, 2, 128, 128,
+                                inp["q_scale"], 1e-6, inp["state0"])
+    assert_out_close(out, oracle.gated_rmsnorm(ref[0], inp["z"], inp["norm_w"], 1e-6))
+    for j, i in enumerate(sorted(real)):
+        assert_state_close(st[i], ref[1][j], f"state of sequence {i}")
+        assert_state_close(st[i], st_ref[i].double(), f"state of sequence {i} against the workspace call")
 
 
 def test_noalloc_refuses_more_sequences_than_its_scratch_holds():

@@ -49,18 +49,19 @@ constexpr int V_BETA = 0, V_NCX = 64, V_CS = 128, V_CO = 192, V_MISC = 256;  // 
 // ---- prep kernel shared memory: up to kGroup V heads of one K head are solved together
 constexpr int kGroup = 3;
 constexpr uint32_t kTriBytes = 10 * 16 * 16 * 4;             // the 10 lower 16 x 16 blocks of a 64 x 64 fp32 matrix
-constexpr uint32_t kBBytes = 6 * 16 * 20 * 4;                // the solve's six B_ik blocks
-constexpr uint32_t kHeadBuf = 2 * kTriBytes + kBBytes;       // A, T, B of one V head (27.5 KB)
+constexpr uint32_t kYBytes = 32 * 32 * 4;                    // the solve's scratch products (32 x 32 fp32)
+constexpr uint32_t kHeadBuf = 2 * kTriBytes + kYBytes;       // A, T and scratch of one V head (24 KB)
 constexpr uint32_t PR_QK = 0;                                // 32 KB [K; Q] tile (TMA); dead once the Gram and
-                                                             // the norms are taken, then the heads' buffers
-constexpr uint32_t PR_HEADS = 0;
-constexpr uint32_t PR_VEC = kGroup * kHeadBuf;               // gamma, beta (kGroup x 64 each), ik, iq, partial sums,
+                                                             // the norms are taken, then it receives the next
+                                                             // unit's tile
+constexpr uint32_t PR_HEADS = 32768;
+constexpr uint32_t PR_VEC = PR_HEADS + kGroup * kHeadBuf;    // gamma, beta (kGroup x 64 each), ik, iq, partial sums,
                                                              // gamma - log2 ik (kGroup x 64)
 constexpr uint32_t PR_BAR = PR_VEC + (3 * kGroup * 64 + 2 * 64 + kParts * 128) * 4;
 constexpr uint32_t PR_USED = PR_BAR + 64;
 constexpr uint32_t PR_BYTES = PR_USED + 1024;
-static_assert(PR_VEC >= 32768, "the q/k tile must fit under the head buffers");
 static_assert(2 * (PR_BYTES + 1024) <= 233472, "two prep CTAs must share an SM");
+static_assert(kHeadBuf % 1024 == 0 && PR_HEADS % 1024 == 0, "head buffers stay 1 KB aligned");
 
 // ---- state kernel shared memory
 constexpr uint32_t SS_QK = 0;         // 32 KB [K; Q] tile (TMA)
@@ -111,7 +112,6 @@ struct StateParams {
   const float* state_src;     // state at the segment start: state_in (may be NULL) for the first, else state_out
   CUtensorMap tmap;
   CUtensorMap tmap_z;    // z [T][Hv * 128] bf16, box 128 x 64, no swizzle (valid when z != NULL)
-  CUtensorMap tmap_out;  // out, same shape and box as z (valid when z != NULL)
   const int32_t* cu;
   const int32_t* order;
   unsigned* counter;
@@ -143,100 +143,182 @@ __device__ __forceinline__ void issue_qk_tiles(uint32_t dst, const CUtensorMap* 
   }
 }
 
-// Element (r, c), c / 16 <= r / 16, of a 64 x 64 fp32 lower block-triangular matrix stored as its
-// ten 16 x 16 blocks (block row i, column j at index i (i + 1) / 2 + j), each row-major with the
-// 16-byte groups of row r XOR-permuted by r & 3: float4 accesses of one row segment by 32 lanes
-// that hold 32 consecutive rows spread over all banks.
-__device__ __forceinline__ int tri(int r, int c) {
-  const int bi = r >> 4, bj = c >> 4;
-  return ((bi * (bi + 1)) / 2 + bj) * 256 + (r & 15) * 16 + ((((c & 15) >> 2) ^ (r & 3)) << 2) + (c & 3);
-}
+// A 64 x 64 fp32 lower block-triangular matrix (A, or its inverse T) is stored as its ten 16 x 16
+// blocks on and below the diagonal (block row i, column j at index i (i + 1) / 2 + j), each
+// row-major with the 16-byte groups of row r XOR-permuted by r & 3: float4 accesses of one row
+// segment by 32 lanes that hold 32 consecutive rows spread over all banks.
 
 // T_g = (I + A_g)^-1 for G <= kGroup strictly lower triangular 64 x 64 matrices at once (head g's
-// A, T and scratch blocks at base + g * kHeadBuf bytes): the diagonal 16 x 16 blocks inverted by
-// forward substitution (one column per thread), then block forward substitution down each block
-// column by one warp; two CTA barriers in all.
+// A, T and scratch at base + g * kHeadBuf bytes), by two levels of 2 x 2 block inversion of a lower
+// block-triangular matrix, [[M11, 0], [M21, M22]]^-1 = [[T11, 0], [-T22 M21 T11, T22]]:
+//   1. the four diagonal 16 x 16 blocks by forward substitution (one column per thread);
+//   2. in each diagonal 32 x 32 block, the block below the diagonal: T_ba = -T_bb (A_ba T_aa);
+//   3. the lower-left 32 x 32 block: T_21 = -T_22 (A_21 T_11).
+// The products of steps 2 and 3 are spread over every thread (one thread: four consecutive
+// columns of one row, as f32x2 pairs), each through a scratch product and a CTA barrier: five
+// barriers in all, against the block-column walk by one warp per column it replaces.
 __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
-  const int warp = tid >> 5, lane = tid & 31;
-  if (tid < 64 * G) {  // step 1: diagonal blocks, one column per thread
-    const int g = tid >> 6, b = (tid >> 4) & 3, c = tid & 15, o = b * 16;
-    const float* sA = reinterpret_cast<const float*>(base + g * kHeadBuf);
-    float* sT = reinterpret_cast<float*>(base + g * kHeadBuf + kTriBytes);
+  // Block (bi, bj) of a tri-layout matrix; inside it, element (r, c) sits at r * 16 +
+  // ((((c >> 2) ^ (r & 3)) << 2) | (c & 3)).
+  auto blk = [](const float* m, int bi, int bj) { return m + ((bi * (bi + 1)) / 2 + bj) * 256; };
+  auto f4 = [](const float* p) { return *reinterpret_cast<const float4*>(p); };
+  if (tid < 64 * G) {  // step 1: diagonal blocks, one column per thread; A rows read as float4
+    const int g = tid >> 6, b = (tid >> 4) & 3, c = tid & 15;
+    const float* Ab = blk(reinterpret_cast<const float*>(base + g * kHeadBuf), b, b);
+    float* Tb = const_cast<float*>(blk(reinterpret_cast<const float*>(base + g * kHeadBuf + kTriBytes), b, b));
     float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
 #pragma unroll
-    for (int k = 0; k < 15; ++k) {
-      const float xk = x[k];
+    for (int i = 1; i < 16; ++i) {  // x_i -= sum_{k < i} A_ik x_k (x_k final by now)
+      float a[16];
 #pragma unroll
-      for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-sA[tri(o + i, o + k)], xk, x[i]);
+      for (int q = 0; q <= (i - 1) >> 2; ++q) {
+        const float4 v = f4(Ab + i * 16 + ((q ^ (i & 3)) << 2));
+        a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+      }
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < i; ++k) {
+        if (k & 1) s1 = fmaf(a[k], x[k], s1);
+        else s0 = fmaf(a[k], x[k], s0);
+      }
+      x[i] -= s0 + s1;
     }
+    const int cq = c >> 2, ce = c & 3;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) sT[tri(o + i, o + c)] = x[i];  // zeros above the diagonal included
+    for (int i = 0; i < 16; ++i) Tb[i * 16 + (((cq ^ (i & 3)) << 2) | ce)] = x[i];  // zeros above the diagonal too
   }
   __syncthreads();
-  // Block columns: for each head and block column j < 3, one warp runs the forward substitution
-  // down the column, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj (i = j + 1 .. 3), with only warp-level
-  // synchronisation; the block columns of a head (and the heads) are independent.  Lane: row
-  // r = lane / 2 of a 16 x 16 block, eight columns from c8.
-  const int r = lane >> 1, c8 = (lane & 1) * 8;
-  auto blk = [](int i, int k) { return (i * (i + 1) / 2 + k) * 256; };
-  auto row16 = [&](const float* b16, int rr, float (&v)[16]) {  // row rr of a tri-layout block
+  // Register-blocked products: a thread holds a 4 x 4 output tile -- rows rb, rb + S, rb + 2S,
+  // rb + 3S (so that the lanes of a warp, consecutive in rb, read rows whose 16-byte groups sit
+  // in different banks) and four consecutive columns -- and takes four k at a time: four float4
+  // rows of the left operand, four float4 rows of the right one, 32 f32x2 multiply-adds.
+  auto fma16 = [](const float4 (&a)[4], const float4 (&b)[4], float2 (&acc)[4][2]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float av[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 aa = make_float2(av[e], av[e]);
+        acc[i][0] = __ffma2_rn(aa, make_float2(b[e].x, b[e].y), acc[i][0]);
+        acc[i][1] = __ffma2_rn(aa, make_float2(b[e].z, b[e].w), acc[i][1]);
+      }
+    }
+  };
+  // step 2a: Y_h = A_{b+1,b} T_{b,b} (b = 2h), rows rb + 4i of the 16-row block; item (g, h, c4, rb)
+  for (int it = tid; it < G * 32; it += kThreads) {
+    const int g = it >> 5, b = ((it >> 4) & 1) * 2, cq = (it >> 2) & 3, rb = it & 3;
+    const float* sA = reinterpret_cast<const float*>(base + g * kHeadBuf);
+    const float* L = blk(sA, b + 1, b);
+    const float* R = blk(sA + kTriBytes / 4, b, b);
+    float* sY = reinterpret_cast<float*>(base + g * kHeadBuf + 2 * kTriBytes) + (b >> 1) * 256;
+    float2 acc[4][2] = {};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float4 f = *reinterpret_cast<const float4*>(b16 + rr * 16 + ((q ^ (rr & 3)) << 2));
-      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
-    }
-  };
-  // acc[0..7] += sum_u a[u] * b16[u][c8 .. c8 + 7] (tri-layout block)
-  auto row_times_block = [&](const float (&a)[16], const float* b16, float2 (&acc)[4]) {
+      float4 a[4], bb[4];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const float4 f0 = *reinterpret_cast<const float4*>(b16 + u * 16 + ((((c8 >> 2)) ^ (u & 3)) << 2));
-      const float4 f1 = *reinterpret_cast<const float4*>(b16 + u * 16 + ((((c8 >> 2) + 1) ^ (u & 3)) << 2));
-      const float2 au = make_float2(a[u], a[u]);
-      acc[0] = __ffma2_rn(au, make_float2(f0.x, f0.y), acc[0]);
-      acc[1] = __ffma2_rn(au, make_float2(f0.z, f0.w), acc[1]);
-      acc[2] = __ffma2_rn(au, make_float2(f1.x, f1.y), acc[2]);
-      acc[3] = __ffma2_rn(au, make_float2(f1.z, f1.w), acc[3]);
+      for (int i = 0; i < 4; ++i) {
+        const int r = rb + 4 * i;
+        a[i] = f4(L + r * 16 + ((q ^ (r & 3)) << 2));
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) bb[e] = f4(R + (4 * q + e) * 16 + ((cq ^ e) << 2));
+      fma16(a, bb, acc);
     }
-  };
-  // tasks in column order (the longest, j = 0, first); warp w takes task w, and the one task past
-  // the eighth (three heads) goes to the last warp, whose own task (j = 2) is one of the shortest
-  for (int n_task = 0; n_task < 2; ++n_task) {
-    const int task = n_task == 0 ? warp : (warp == kWarps - 1 ? kWarps : 3 * G);
-    if (task >= 3 * G) break;
-    const int jb = task / G, g = task - jb * G;
-    const float* sA = reinterpret_cast<const float*>(base + g * kHeadBuf);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(sY + (rb + 4 * i) * 16 + cq * 4) =
+          make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
+  }
+  __syncthreads();
+  // step 2b: T_{b+1,b} = -T_{b+1,b+1} Y_h
+  for (int it = tid; it < G * 32; it += kThreads) {
+    const int g = it >> 5, b = ((it >> 4) & 1) * 2, cq = (it >> 2) & 3, rb = it & 3;
     float* sT = reinterpret_cast<float*>(base + g * kHeadBuf + kTriBytes);
-    float* sY = reinterpret_cast<float*>(base + g * kHeadBuf + 2 * kTriBytes) + jb * 320;  // 16 x 20 scratch
-    for (int i = jb + 1; i < 4; ++i) {
-      float2 y[4] = {};
-      for (int k = jb; k < i; ++k) {
-        float a[16];
-        row16(sA + blk(i, k), r, a);
-        row_times_block(a, sT + blk(k, jb), y);
-      }
-      *reinterpret_cast<float4*>(sY + r * 20 + c8) = make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
-      *reinterpret_cast<float4*>(sY + r * 20 + c8 + 4) = make_float4(y[2].x, y[2].y, y[3].x, y[3].y);
-      __syncwarp();
-      float a[16];
-      row16(sT + blk(i, i), r, a);
-      float2 t[4] = {};
+    const float* L = blk(sT, b + 1, b + 1);
+    const float* sY = reinterpret_cast<const float*>(base + g * kHeadBuf + 2 * kTriBytes) + (b >> 1) * 256;
+    float2 acc[4][2] = {};
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const float4 f0 = *reinterpret_cast<const float4*>(sY + u * 20 + c8);
-        const float4 f1 = *reinterpret_cast<const float4*>(sY + u * 20 + c8 + 4);
-        const float2 au = make_float2(a[u], a[u]);
-        t[0] = __ffma2_rn(au, make_float2(f0.x, f0.y), t[0]);
-        t[1] = __ffma2_rn(au, make_float2(f0.z, f0.w), t[1]);
-        t[2] = __ffma2_rn(au, make_float2(f1.x, f1.y), t[2]);
-        t[3] = __ffma2_rn(au, make_float2(f1.z, f1.w), t[3]);
+    for (int q = 0; q < 4; ++q) {
+      float4 a[4], bb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = rb + 4 * i;
+        a[i] = f4(L + r * 16 + ((q ^ (r & 3)) << 2));
       }
-      *reinterpret_cast<float4*>(sT + tri(i * 16 + r, jb * 16 + c8)) = make_float4(-t[0].x, -t[0].y, -t[1].x, -t[1].y);
-      *reinterpret_cast<float4*>(sT + tri(i * 16 + r, jb * 16 + c8 + 4)) =
-          make_float4(-t[2].x, -t[2].y, -t[3].x, -t[3].y);
-      __syncwarp();  // T_ij feeds the next block row of this column; sY is rewritten there
+#pragma unroll
+      for (int e = 0; e < 4; ++e) bb[e] = f4(sY + (4 * q + e) * 16 + cq * 4);
+      fma16(a, bb, acc);
+    }
+    float* D = const_cast<float*>(blk(sT, b + 1, b));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = rb + 4 * i;
+      *reinterpret_cast<float4*>(D + r * 16 + ((cq ^ (r & 3)) << 2)) =
+          make_float4(-acc[i][0].x, -acc[i][0].y, -acc[i][1].x, -acc[i][1].y);
+    }
+  }
+  __syncthreads();
+  // step 3a: Y = A_21 T_11 (rows 32..63 of A, columns 0..31), rows rb + 8i; T_11 is zero above its
+  // diagonal blocks, so column block cb takes key blocks cb..1.  Item (g, c4, rb).
+  for (int it = tid; it < G * 64; it += kThreads) {
+    const int g = it >> 6, c4 = (it >> 3) & 7, rb = it & 7, cb = c4 >> 2, cq = c4 & 3;
+    const float* sA = reinterpret_cast<const float*>(base + g * kHeadBuf);
+    const float* sT = sA + kTriBytes / 4;
+    float* sY = reinterpret_cast<float*>(base + g * kHeadBuf + 2 * kTriBytes);
+    float2 acc[4][2] = {};
+    for (int kb = cb; kb < 2; ++kb) {
+      const float* R = blk(sT, kb, cb);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float4 a[4], bb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = rb + 8 * i, rr = r & 15;  // row 32 + r of A: block row 2 + r / 16
+          a[i] = f4(blk(sA, 2 + (r >> 4), kb) + rr * 16 + ((q ^ (rr & 3)) << 2));
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) bb[e] = f4(R + (4 * q + e) * 16 + ((cq ^ e) << 2));
+        fma16(a, bb, acc);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(sY + (rb + 8 * i) * 32 + c4 * 4) =
+          make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
+  }
+  __syncthreads();
+  // step 3b: T_21 = -T_22 Y; T_22 is zero above its diagonal blocks: rows 0..15 of it take Y's
+  // first 16 rows, rows 16..31 all 32
+  for (int it = tid; it < G * 64; it += kThreads) {
+    const int g = it >> 6, c4 = (it >> 3) & 7, rb = it & 7, cb = c4 >> 2, cq = c4 & 3;
+    float* sT = reinterpret_cast<float*>(base + g * kHeadBuf + kTriBytes);
+    const float* sY = reinterpret_cast<const float*>(base + g * kHeadBuf + 2 * kTriBytes);
+    float2 acc[4][2] = {};
+#pragma unroll
+    for (int ub = 0; ub < 2; ++ub) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float4 a[4], bb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = rb + 8 * i, rr = r & 15, rblk = r >> 4;  // row 32 + r: block row 2 + rblk
+          // T_22 row r, key block ub: zero when ub > rblk (above the diagonal blocks)
+          a[i] = (ub <= rblk) ? f4(blk(sT, 2 + rblk, 2 + ub) + rr * 16 + ((q ^ (rr & 3)) << 2))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) bb[e] = f4(sY + (16 * ub + 4 * q + e) * 32 + c4 * 4);
+        fma16(a, bb, acc);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = rb + 8 * i, rr = r & 15;
+      float* D = const_cast<float*>(blk(sT, 2 + (r >> 4), cb));
+      *reinterpret_cast<float4*>(D + rr * 16 + ((cq ^ (rr & 3)) << 2)) =
+          make_float4(-acc[i][0].x, -acc[i][0].y, -acc[i][1].x, -acc[i][1].y);
     }
   }
   __syncthreads();
@@ -279,47 +361,68 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
   const uint32_t tmem = *tmem_slot;
   const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
 
-  bool ok = true, qk_pending = false, gram_pending = false;
-  uint32_t ph = 0;  // parity of both barriers: each completes once per unit
-  for (long u = blockIdx.x; u < units && ok; u += gridDim.x, ph ^= 1u) {
-  const int cu_ = (int)(u / p.Hk), kh = (int)(u - (long)cu_ * p.Hk);
-  // the sequence of this unit: the last n with seg_pref[n] <= cu_ (never one without chunks here)
-  int lo = 0, hi = p.N - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(p.seg_pref + mid) <= cu_) lo = mid; else hi = mid - 1;
-  }
-  const int n = lo;
-  const int seq_s = __ldg(p.cu + n), seq_e = __ldg(p.cu + n + 1);
-  const int nch = (max(0, seq_e - seq_s) + kChunk - 1) / kChunk;
-  const int j = seg_begin(p.seg, nch, p.nseg) + (cu_ - __ldg(p.seg_pref + n));
-  const int gc = __ldg(p.chunk_off + n) + j;
-  const int c0 = seq_s + j * kChunk;
-  if (seq_s < 0 || seq_e < seq_s || seq_e > p.T || c0 >= seq_e || gc < 0 || gc >= p.nc_max) {
-    if (tid == 0) raise_error(p.err, kErrDeviceArgument);
-    ph ^= 1u;  // no barrier completed for this unit
-    continue;
-  }
-  const int L = min(kChunk, seq_e - c0);
-  if (tid == 0) issue_qk_tiles(sb + PR_QK, &p.tmap, p.Hk, c0, kh, bar_qk);
-  qk_pending = true;
-
-  // g, beta of a group of V heads: thread -> (token tid / G, head tid % G), zero past the sequence end
+  // A unit's chunk: its sequence (the last n with seg_pref[n] <= unit / Hk: never one without
+  // chunks here), first token, length and record index; false when cu_seqlens is inconsistent.
+  struct Unit {
+    int kh, c0, L, gc;
+  };
+  auto unit_of = [&](long u, Unit& un) {
+    const int cu_ = (int)(u / p.Hk);
+    un.kh = (int)(u - (long)cu_ * p.Hk);
+    int lo = 0, hi = p.N - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(p.seg_pref + mid) <= cu_) lo = mid; else hi = mid - 1;
+    }
+    const int n = lo;
+    const int seq_s = __ldg(p.cu + n), seq_e = __ldg(p.cu + n + 1);
+    const int nch = (max(0, seq_e - seq_s) + kChunk - 1) / kChunk;
+    const int j = seg_begin(p.seg, nch, p.nseg) + (cu_ - __ldg(p.seg_pref + n));
+    un.gc = __ldg(p.chunk_off + n) + j;
+    un.c0 = seq_s + j * kChunk;
+    un.L = min(kChunk, seq_e - un.c0);
+    return !(seq_s < 0 || seq_e < seq_s || seq_e > p.T || un.c0 >= seq_e || un.gc < 0 || un.gc >= p.nc_max);
+  };
+  // g, beta of a group of V heads of a unit: thread -> (token tid / G, head tid % G), zero past the
+  // sequence end
   float g_next = 0.f, b_next = 0.f;
-  auto load_gb = [&](int h0, int G) {
+  auto load_gb = [&](const Unit& un, int h0, int G) {
     g_next = 0.f;
     b_next = 0.f;
     const int t = tid / G;
-    if (tid < 64 * G && t < L) {
-      const size_t o = (size_t)(c0 + t) * p.Hv + h0 + (tid - t * G);
+    if (tid < 64 * G && t < un.L) {
+      const size_t o = (size_t)(un.c0 + t) * p.Hv + h0 + (tid - t * G);
       g_next = __ldg(p.g + o);
       b_next = __ldg(p.beta + o);
     }
   };
-  load_gb(kh * ratio, min(kGroup, ratio));
+
+  // The [K; Q] tile of a unit is dead once its Gram and norms are taken: the next unit's tile is
+  // fetched into the same buffer from there, and the next unit's first g / beta once the current
+  // unit's last group has taken its own, so both arrive while the current unit is solved.
+  bool ok = true, qk_pending = false, gram_pending = false, have_next = false;
+  uint32_t ph_qk = 0, ph_g = 0;  // parities: bar_qk completes once per tile, bar_g once per Gram
+  for (long u = blockIdx.x; u < units && ok; u += gridDim.x) {
+  Unit un;
+  if (!unit_of(u, un)) {  // never prefetched (the prefetch checks the same condition)
+    if (tid == 0) raise_error(p.err, kErrDeviceArgument);
+    have_next = false;
+    continue;
+  }
+  const int kh = un.kh, gc = un.gc, c0 = un.c0, L = un.L;
+  if (!have_next) {
+    if (tid == 0) issue_qk_tiles(sb + PR_QK, &p.tmap, p.Hk, c0, kh, bar_qk);
+    load_gb(un, kh * ratio, min(kGroup, ratio));
+  }
+  qk_pending = true;
+  have_next = false;
+  Unit nx;
+  const long u_next = u + gridDim.x;
+  const bool next_ok = u_next < units && unit_of(u_next, nx);
 
   {
-    const bool got = mbar_wait(bar_qk, ph, kWaitLimit);
+    const bool got = mbar_wait(bar_qk, ph_qk, kWaitLimit);
+    if (got) ph_qk ^= 1u;  // after a timeout ph_qk stays the parity of the copy still in flight
     if (!got) raise_error(p.err, kErrTimeout);
     ok = __syncthreads_and(got ? 1 : 0) != 0;
     qk_pending = !ok;
@@ -361,11 +464,18 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
       const float inv = 1.0f / sqrtf(ss + p.l2_eps);
       if (tid < 64) s_ik[tid] = inv; else s_iq[tid - 64] = inv;
     }
-    const bool got = mbar_wait(bar_g, ph, kWaitLimit);
+    fence_proxy_async_smem();  // this thread's generic reads of the tile (the norms) before its refill
+    const bool got = mbar_wait(bar_g, ph_g, kWaitLimit);
+    if (got) ph_g ^= 1u;
     if (!got) raise_error(p.err, kErrTimeout);
     ok = __syncthreads_and(got ? 1 : 0) != 0;  // also: the q/k tile is dead from here on
     gram_pending = !ok;
     tc_fence_after();
+    if (ok && next_ok) {  // the next unit's tile into the freed buffer
+      if (tid == 0) issue_qk_tiles(sb + PR_QK, &p.tmap, p.Hk, nx.c0, nx.kh, bar_qk);
+      qk_pending = true;
+      have_next = true;
+    }
   }
   if (ok) {
     for (int g0 = 0; g0 < ratio; g0 += kGroup) {
@@ -389,7 +499,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
         gam[2 * lane] = sc - g1v;
       }
       __syncthreads();
-      if (g0 + kGroup < ratio) load_gb(h0 + kGroup, min(kGroup, ratio - g0 - kGroup));  // in flight meanwhile
+      if (g0 + kGroup < ratio) load_gb(un, h0 + kGroup, min(kGroup, ratio - g0 - kGroup));  // in flight meanwhile
+      else if (have_next) load_gb(nx, nx.kh * ratio, min(kGroup, ratio));  // the next unit's first group
       if (tid < 64 * G) {  // per-token factors of the G heads
         const int g = tid >> 6, t = tid & 63;
         const float* gam = s_gam + g * 64;
@@ -430,13 +541,16 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
                             make_float2(ex2_approx(d.x), ex2_approx(d.y)));
         };
         if (row < 64) {
+          // row t of A, blocks (t / 16, 2 part) and (t / 16, 2 part + 1) of the tri layout
           float* sA = reinterpret_cast<float*>(sm + PR_HEADS + g * kHeadBuf);
+          const int tb = t >> 4, tx = t & 3;
+          float* rowA = sA + ((tb * (tb + 1)) / 2 + 2 * part) * 256 + (t & 15) * 16;
 #pragma unroll
           for (int i4 = 0; i4 < kW; i4 += 4) {
             const int j0 = part * kW + i4;
-            if ((j0 >> 4) > (t >> 4)) continue;  // above the diagonal blocks: never read
+            if ((j0 >> 4) > tb) continue;  // above the diagonal blocks: never read
             const float2 a01 = pair(j0, i4), a23 = pair(j0 + 2, i4 + 2);
-            *reinterpret_cast<float4*>(sA + tri(t, j0)) =
+            *reinterpret_cast<float4*>(rowA + (i4 >> 4) * 256 + ((((i4 & 15) >> 2) ^ tx) << 2)) =
                 make_float4(j0 < t ? a01.x : 0.f, j0 + 1 < t ? a01.y : 0.f, j0 + 2 < t ? a23.x : 0.f,
                             j0 + 3 < t ? a23.y : 0.f);
           }
@@ -462,10 +576,13 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
         const int g = i >> 9, t = (i >> 3) & 63, k0 = (i & 7) * 8;
         const float* sT = reinterpret_cast<const float*>(sm + PR_HEADS + g * kHeadBuf + kTriBytes);
         uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h0 + g) * REC_BYTES;
-        const bool upper = (k0 >> 4) > (t >> 4);  // strictly upper blocks of T are zero
+        const int tb = t >> 4, kb = k0 >> 4;
+        const bool upper = kb > tb;  // strictly upper blocks of T are zero
+        const float* rowT = sT + ((tb * (tb + 1)) / 2 + kb) * 256 + (t & 15) * 16;
+        const int q0 = (k0 & 15) >> 2, tx = t & 3;
         const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 v0 = upper ? z4 : *reinterpret_cast<const float4*>(sT + tri(t, k0));
-        const float4 v1 = upper ? z4 : *reinterpret_cast<const float4*>(sT + tri(t, k0 + 4));
+        const float4 v0 = upper ? z4 : *reinterpret_cast<const float4*>(rowT + ((q0 ^ tx) << 2));
+        const float4 v1 = upper ? z4 : *reinterpret_cast<const float4*>(rowT + (((q0 + 1) ^ tx) << 2));
         const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
         store8_split(rec + REC_T, rec + REC_T + 8192, 0, t, k0, v);
       }
@@ -479,8 +596,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
   tc_fence_after();
   }
   // leave only after the Gram MMA and the tile load have landed (bounded, after an early exit)
-  if (qk_pending) mbar_wait(bar_qk, ph ^ 1u, kWaitLimit);
-  if (gram_pending) mbar_wait(bar_g, ph ^ 1u, kWaitLimit);
+  if (qk_pending) mbar_wait(bar_qk, ph_qk, kWaitLimit);
+  if (gram_pending) mbar_wait(bar_g, ph_g, kWaitLimit);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -515,10 +632,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
     for (int i = 0; i < 10; ++i) mbar_init(smem_u32(&bars[i]), 1);
     fence_mbar_init();
     prefetch_tensormap(&p.tmap);
-    if (p.z) {
-      prefetch_tensormap(&p.tmap_z);
-      prefetch_tensormap(&p.tmap_out);
-    }
+    if (p.z) prefetch_tensormap(&p.tmap_z);
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), SC_COLS);
   tc_fence_before();
@@ -888,32 +1002,20 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
             r[i][1] = __fmul2_rn(__fmul2_rn(r[i][1], __fmul2_rn(w23, rs)), s23);
           }
         }
-        // a full gated chunk goes out as one TMA store of a tile staged over its z rows (each warp
-        // overwrites only the z rows it has read); otherwise rows t < L are stored directly
-        const bool tile_store = gated && L == kChunk;
+        // rows t < L go straight to global memory: a warp writes 256 contiguous bytes per token, and
+        // the z buffer is free for the next v as soon as every warp has read its rows
 #pragma unroll
         for (int i = 0; i < kTok; ++i) {
           const int t = warp + kWarps * i;
           const uint2 packed = make_uint2(pack_bf2(r[i][0].x, r[i][0].y), pack_bf2(r[i][1].x, r[i][1].y));
-          if (tile_store) {
-            *reinterpret_cast<uint2*>(sm + SS_V + t * 256 + lane * 8) = packed;
-          } else if (t < L) {
-            *reinterpret_cast<uint2*>(p.out + ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4) = packed;
-          }
+          if (t < L) *reinterpret_cast<uint2*>(p.out + ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4) = packed;
         }
       }
-      fence_proxy_async_smem();  // vector-block and z reads, output tile writes -> the async proxy
+      fence_proxy_async_smem();  // vector-block and z reads -> the async proxy (the next loads)
       tc_fence_before();
       __syncthreads();  // staging reads and accumulator reads done before the next chunk reuses them
       tc_fence_after();
-      if (tid == 64) {
-        if (gated && L == kChunk) {
-          tma_store_2d(&p.tmap_out, h * kHeadDim, c0, sb + SS_V);
-          bulk_commit_group();
-          bulk_wait_group_read0();  // the tile has been read out before the buffer takes the next v
-        }
-        if (gated && has_next) issue_v(c0 + kChunk, h);
-      }
+      if (tid == 64 && gated && has_next) issue_v(c0 + kChunk, h);
       if (gated && has_next) pend_v = true;
     }
     if (!ok) break;
@@ -936,7 +1038,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_state_kernel(const __grid_c
     tc_fence_after();
   }
 
-  if (tid == 64) bulk_wait_group0();  // output tile stores complete
   // after an early exit, let copies still in flight land before the CTA leaves (bounded)
   if (pend_qk) mbar_wait(bar_qk, ph_qk, kWaitLimit);
   if (pend_v) mbar_wait(bar_v, ph_v, kWaitLimit);
@@ -1163,11 +1264,6 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
   sp.nseg = nseg;
   sp.tmap = tmap;
   sp.tmap_z = tmap_z;
-  if (z && T > 0) {
-    if ((e = encode_bf16_2d(&sp.tmap_out, out, (uint64_t)Hv * kHeadDim, (uint64_t)T, (uint64_t)Hv * kHeadDim * 2, 128,
-                            kChunk)) != cudaSuccess)
-      return e;
-  }
   sp.cu = cu; sp.order = lay.order; sp.chunk_off = lay.chunk_off; sp.rec = lay.rec;
   sp.state_in = state_in; sp.state_out = state_out; sp.z = z; sp.norm_w = norm_w; sp.out = out; sp.err = env.err;
   sp.N = N; sp.T = T; sp.Hk = Hk; sp.Hv = Hv; sp.nc_max = (int)nc_max; sp.rms_eps = rms_eps;

@@ -589,6 +589,9 @@ def compact_summary(line, step_dist):
                        "p10_p50_p90_ms": [_r(step_dist[k]) for k in ("p10_ms", "p50_ms", "p90_ms")],
                        "runs": step_dist["runs"]}}
     out["decode"] = leg(line["decode"])
+    out["decode_fused_gates"] = leg(line["decode_fused_gates"])
+    out["prefill_fused_gates"] = {"M_tok_s": _r(line["prefill_fused_gates"]["value"] / 1e6),
+                                  "ms": _r(line["prefill_fused_gates"]["ms_per_step"])}
     out["decode_f16"] = leg(line["decode_fp16_state"])
     out["decode_kda"] = leg(line["decode_kda"])
     v = line.get("varlen")
@@ -697,6 +700,31 @@ def run_ours(args, rank, world, local):
                  "peak": hbm_peak, "unit": "GB/s", "avg_launch_ms": conv_ms,
                  "algorithmic_bytes_per_launch": conv_bytes, "traffic": crec["bytes_per_launch"] if crec else None}
     conv_roof["frac"] = conv_roof["achieved"] / hbm_peak
+
+    # the prefill step with the gates derived in the prep kernel from the a / b projections
+    from linear_attention_ssm_gb300.synth import gate_inputs as _gate_inputs
+    gpi = _gate_inputs(T, seed=6)
+    pa, pb, pal, pdb = (gpi[k].to(dev) for k in ("a", "b", "A_log", "dt_bias"))
+
+    def prefill_fg_step():
+        gdn.gdn_conv1d_prefill(x, w, cu, cs_in, cs_out, qkv)
+        gdn.gdn_chunk_prefill_fused_gates(qkv, pa, pb, pal, pdb, cu, inp["q_scale"], 1e-6, state_in, state_out, z, nw,
+                                          1e-6, out, workspace=ws)
+    for _ in range(max(args.warmup, 1)):
+        prefill_fg_step()
+    barrier()
+    sfg, efg = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sfg.record(stream)
+    for _ in range(args.steps):
+        prefill_fg_step()
+    efg.record(stream)
+    torch.cuda.synchronize()
+    gdn.gdn_check_device_errors()
+    fg_ms = max_over_ranks(sfg.elapsed_time(efg)) / args.steps
+    prefill_fg = {"workload": "the headline step with the gates derived in the prep kernel from a, b (bf16), "
+                              "A_log, dt_bias", "value": replica_throughput(T, world, fg_ms), "unit": "tokens/s",
+                  "ms_per_step": fg_ms, "steps": args.steps}
+    del pa, pb, pal, pdb
 
     # distribution of per-step times over a separate pass of at least 50 steps (the headline above
     # times exactly --steps steps between two events): whole step, and the chunk prefill alone
@@ -856,6 +884,44 @@ def run_ours(args, rank, world, local):
                 "roofline_seq_steps_per_s": hbm_peak * 1e9 / (dec_bytes / B)}
 
     decode = time_decode(torch.float32, STATE_BYTES_PER_SEQ, "decode_step")
+
+    # the same step with the gates derived in the kernel from the a / b projections (bf16) and the
+    # per-head A_log, dt_bias: 4 bytes of gate input per (sequence, V head) instead of 8
+    from linear_attention_ssm_gb300.synth import gate_inputs
+    gsteps = [gate_inputs(B, seed=40 + s) for s in range(DECODE_STEPS)]
+    ga_all = torch.stack([gs["a"] for gs in gsteps]).to(dev)
+    gb_all = torch.stack([gs["b"] for gs in gsteps]).to(dev)
+    gal, gdb = gsteps[0]["A_log"].to(dev), gsteps[0]["dt_bias"].to(dev)
+
+    def time_decode_fused_gates():
+        dstate, dcs = d["state0"].to(dev), d["conv_state0"].to(dev)
+
+        def step(s):
+            gdn.gdn_decode_step_fused_gates(dx[s], dw, dcs, ga_all[s], gb_all[s], gal, gdb, dstate, dz[s], dnw,
+                                            d["q_scale"], out=dout)
+        for s in range(max(args.warmup, 1)):
+            step(s % DECODE_STEPS)
+        barrier()
+        s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s3.record(stream)
+        for s in range(args.decode_steps):
+            step(s % DECODE_STEPS)
+        e3.record(stream)
+        torch.cuda.synchronize()
+        gdn.gdn_check_device_errors()
+        ms_ = max_over_ranks(s3.elapsed_time(e3)) / args.decode_steps
+        nbytes = (DECODE_BYTES_PER_SEQ - 384 + 48 * 4) * B + 2 * 48 * 4
+        gbs = nbytes / (ms_ / 1000) / 1e9
+        del dstate, dcs
+        return {"metric": "decode seq-steps/s", "value": world * B / (ms_ / 1000), "unit": "seq-steps/s",
+                "ms_per_step": ms_, "steps": args.decode_steps, "batch": B,
+                "gates": "derived in the decode kernel from a, b (bf16) and A_log, dt_bias",
+                "roofline": {"kernel": "decode_step (fused gates)", "bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                             "unit": "GB/s", "frac": gbs / hbm_peak, "algorithmic_bytes_per_launch": nbytes,
+                             "avg_launch_ms": ms_}}
+
+    decode_fg = time_decode_fused_gates()
+    del ga_all, gb_all
     decode_kda = time_kda_decode(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_peak)
     # the same workload with the recurrent state stored as binary16 (half the state bytes)
     decode_f16 = time_decode(torch.float16, STATE_BYTES_PER_SEQ // 2, "decode_step_fp16_state")
@@ -936,7 +1002,8 @@ def run_ours(args, rank, world, local):
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                     "pipelined": "H2D of step i+1 and D2H of step i-1 overlap the prefill of step i"},
-            "decode": decode, "decode_fp16_state": decode_f16, "decode_kda": decode_kda, "verify": verify,
+            "decode": decode, "decode_fused_gates": decode_fg, "prefill_fused_gates": prefill_fg,
+            "decode_fp16_state": decode_f16, "decode_kda": decode_kda, "verify": verify,
             "verify_fp16_state": verify_f16,
             "gates": gates, "kda_prefill": kda_prefill,
             "varlen": varlen, "small_configs": small, "cpu_baseline": cpu, "clocks": clk,

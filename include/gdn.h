@@ -189,6 +189,37 @@ GDN_API gdn_status gdn_gates(const gdn_geometry* geo, const gdn_bf16* a, const g
                              int32_t rows, void* stream);
 
 /*
+ * gdn_chunk_prefill and gdn_decode_step with the gates derived inside the kernels that use them,
+ * from the projections a, b and the per-head A_log, dt_bias (the gdn_gates formula, the same
+ * arithmetic, so the results have the same bits as gdn_gates followed by the plain call): g and
+ * beta are never written to memory and no gates launch precedes the call.  Qwen3.8 kernel
+ * architecture and TDD ledger, kernel map (the GDN alpha / beta transforms feed the recurrence);
+ * pegainfer PR #1152 Summary (A_log, dt_bias and the a / b projections are the layer's inputs).
+ *   a, b            [rows, Hv] bf16 (rows = total_tokens for the prefill, batch for the decode;
+ *                   2-byte aligned)
+ *   A_log, dt_bias  [Hv] fp32 (4-byte aligned)
+ * Every other argument, the results and the errors are those of gdn_chunk_prefill and
+ * gdn_decode_step (fp32 state).
+ */
+GDN_API gdn_status gdn_chunk_prefill_fused_gates(const gdn_geometry* geo, const gdn_bf16* qkv,
+                                                 const gdn_bf16* a, const gdn_bf16* b,
+                                                 const float* A_log, const float* dt_bias,
+                                                 const int32_t* cu_seqlens, int32_t num_seqs,
+                                                 int32_t total_tokens, float q_scale, float l2_eps,
+                                                 const float* state_in, float* state_out,
+                                                 const gdn_bf16* z, const gdn_bf16* norm_w,
+                                                 float rms_eps, gdn_bf16* out, void* workspace,
+                                                 size_t workspace_bytes, void* stream);
+GDN_API gdn_status gdn_decode_step_fused_gates(const gdn_geometry* geo, const gdn_bf16* x,
+                                               const gdn_bf16* conv_w, gdn_bf16* conv_state,
+                                               const gdn_bf16* a, const gdn_bf16* b,
+                                               const float* A_log, const float* dt_bias,
+                                               float* state, const gdn_bf16* z,
+                                               const gdn_bf16* norm_w, float q_scale, float l2_eps,
+                                               float rms_eps, gdn_bf16* out, int32_t batch,
+                                               void* stream);
+
+/*
  * Sigmoid-gated RMSNorm, one row per (token, V head).  pegainfer PR #1152, Summary
  * (output_gate_type "sigmoid"; the in-tree kernel that hard-codes silu is wrong) and Code
  * review (rms_norm_eps == 1e-6).

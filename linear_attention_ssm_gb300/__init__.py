@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     GdnError,
     gdn_check_device_errors,
     gdn_chunk_prefill,
+    gdn_chunk_prefill_fused_gates,
     gdn_chunk_prefill_noalloc,
     gdn_chunk_prefill_min_workspace_size,
     gdn_chunk_prefill_workspace_size,
@@ -19,6 +20,7 @@ from .binding import (  # noqa: F401
     gdn_debug_set_chunk_mode,
     gdn_debug_set_dropped_copy,
     gdn_decode_step,
+    gdn_decode_step_fused_gates,
     gdn_decode_step_fp16_state,
     gdn_gated_rmsnorm,
     gdn_gates,

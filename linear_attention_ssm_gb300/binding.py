@@ -60,6 +60,8 @@ def _configure(lib, debug: bool):
         "gdn_decode_step": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
         "gdn_decode_step_fp16_state": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
         "gdn_gates": ([G, P, P, P, P, P, P, I, P], ctypes.c_int),
+        "gdn_chunk_prefill_fused_gates": ([G, P, P, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P, S, P], ctypes.c_int),
+        "gdn_decode_step_fused_gates": ([G, P, P, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
         "gdn_kda_decode_step": ([G, P, P, P, P, F, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
         "gdn_kda_recurrence": ([G, P, P, F, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
         "gdn_verify_stash_size": ([G, I, I], S),
@@ -402,6 +404,66 @@ def gdn_gates(a, b, A_log, dt_bias, g=None, beta=None, geometry: Geometry = QWEN
     _check(lib.gdn_gates(_geo(geometry), _p(a), _p(b), _p(A_log), _p(dt_bias), _p(g), _p(beta), rows,
                          _stream(stream)))
     return g, beta
+
+
+def gdn_chunk_prefill_fused_gates(qkv, a, b, A_log, dt_bias, cu_seqlens, q_scale, l2_eps=1e-6, state_in=None,
+                                  state_out=None, z=None, norm_w=None, rms_eps=1e-6, out=None, workspace=None,
+                                  geometry: Geometry = QWEN_GDN, stream=None):
+    """gdn_chunk_prefill with the gates derived in the kernel from a, b ([T, Hv] bf16) and A_log,
+    dt_bias ([Hv] fp32).  Returns out [T, Hv, Dv] bf16."""
+    lib = _L()
+    C, hv, dv, dk = geometry.conv_dim, geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
+    N = cu_seqlens.numel() - 1
+    T = qkv.shape[0]
+    _dev(qkv, torch.bfloat16, "qkv", (T, C))
+    _dev(a, torch.bfloat16, "a", (T, hv))
+    _dev(b, torch.bfloat16, "b", (T, hv))
+    _dev(A_log, torch.float32, "A_log", (hv,))
+    _dev(dt_bias, torch.float32, "dt_bias", (hv,))
+    _dev(cu_seqlens, torch.int32, "cu_seqlens", (N + 1,))
+    _dev(state_in, torch.float32, "state_in", (N, hv, dv, dk))
+    _dev(state_out, torch.float32, "state_out", (N, hv, dv, dk))
+    _dev(z, torch.bfloat16, "z", (T, hv, dv))
+    _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
+    if out is None:
+        out = torch.empty((T, hv, dv), dtype=torch.bfloat16, device=qkv.device)
+    _dev(out, torch.bfloat16, "out", (T, hv, dv))
+    need = lib.gdn_chunk_prefill_workspace_size(_geo(geometry), N, T)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=qkv.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.gdn_chunk_prefill_fused_gates(_geo(geometry), _p(qkv), _p(a), _p(b), _p(A_log), _p(dt_bias),
+                                             _p(cu_seqlens), N, T, float(q_scale), float(l2_eps), _p(state_in),
+                                             _p(state_out), _p(z), _p(norm_w), float(rms_eps), _p(out),
+                                             _p(workspace), wbytes, _stream(stream)))
+    return out
+
+
+def gdn_decode_step_fused_gates(x, conv_w, conv_state, a, b, A_log, dt_bias, state, z, norm_w, q_scale, l2_eps=1e-6,
+                                rms_eps=1e-6, out=None, geometry: Geometry = QWEN_GDN, stream=None):
+    """gdn_decode_step (fp32 state) with the gates derived in the kernel from a, b ([B, Hv] bf16) and
+    A_log, dt_bias ([Hv] fp32); conv_state and state are updated in place.  Returns out."""
+    lib = _L()
+    C, W = geometry.conv_dim, geometry.conv_width
+    hv, dv, dk = geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
+    B = x.shape[0]
+    _dev(x, torch.bfloat16, "x", (B, C))
+    _dev(conv_w, torch.bfloat16, "conv_w", (C, W))
+    _dev(conv_state, torch.bfloat16, "conv_state", (B, C, W - 1))
+    _dev(a, torch.bfloat16, "a", (B, hv))
+    _dev(b, torch.bfloat16, "b", (B, hv))
+    _dev(A_log, torch.float32, "A_log", (hv,))
+    _dev(dt_bias, torch.float32, "dt_bias", (hv,))
+    _dev(state, torch.float32, "state", (B, hv, dv, dk))
+    _dev(z, torch.bfloat16, "z", (B, hv, dv))
+    _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
+    if out is None:
+        out = torch.empty((B, hv, dv), dtype=torch.bfloat16, device=x.device)
+    _dev(out, torch.bfloat16, "out", (B, hv, dv))
+    _check(lib.gdn_decode_step_fused_gates(_geo(geometry), _p(x), _p(conv_w), _p(conv_state), _p(a), _p(b),
+                                           _p(A_log), _p(dt_bias), _p(state), _p(z), _p(norm_w), float(q_scale),
+                                           float(l2_eps), float(rms_eps), _p(out), B, _stream(stream)))
+    return out
 
 
 def gdn_verify_stash_size(batch: int, rows: int, geometry: Geometry = QWEN_GDN) -> int:

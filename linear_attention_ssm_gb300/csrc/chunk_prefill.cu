@@ -71,8 +71,7 @@ constexpr uint32_t TMEM_COLS = 512;
 struct ChunkParams {
   CUtensorMap tmap;    // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle
   CUtensorMap tmap_z;  // z [T][Hv * 128] bf16, box 128 x 64, no swizzle (valid when z != NULL)
-  const float* g;
-  const float* beta;
+  GateSrc gates;
   const int32_t* cu;
   const int32_t* order;     // longest-first sequence order (workspace)
   unsigned* counter;        // work-item counter (workspace, zeroed by the schedule kernel)
@@ -199,10 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   auto load_gb = [&](int c0, int L, int h) {  // g, beta of a chunk -> registers of threads < 64
     g_next = 0.f;
     b_next = 0.f;
-    if (tid < L) {
-      g_next = __ldg(p.g + (size_t)(c0 + tid) * p.Hv + h);
-      b_next = __ldg(p.beta + (size_t)(c0 + tid) * p.Hv + h);
-    }
+    if (tid < L) load_gate(p.gates, (size_t)(c0 + tid) * p.Hv + h, h, g_next, b_next);
   };
 
   for (;;) {
@@ -797,14 +793,14 @@ size_t chunk_prefill_workspace_bytes(int N) {
   return 256 + (((size_t)(N > 0 ? N : 0) * sizeof(int32_t) + 255) / 256) * 256;
 }
 
-cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t* qkv, const float* g,
-                                 const float* beta, const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale,
+cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t* qkv, const GateSrc& gates,
+                                 const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale,
                                  float l2_eps, const float* state_in, float* state_out, const uint16_t* z,
                                  const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace,
                                  size_t workspace_bytes) {
   if (N <= 0) return cudaSuccess;
   if (mode == 0 && workspace_bytes >= split_workspace_bytes(N, T, Hk, Hv))
-    return launch_chunk_prefill_split(env, qkv, g, beta, cu, N, T, Hk, Hv, q_scale, l2_eps, state_in, state_out, z,
+    return launch_chunk_prefill_split(env, qkv, gates, cu, N, T, Hk, Hv, q_scale, l2_eps, state_in, state_out, z,
                                       norm_w, rms_eps, out, workspace);
   ChunkParams p;
   memset(&p, 0, sizeof p);
@@ -815,7 +811,7 @@ cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t*
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.counter = reinterpret_cast<unsigned*>(ws);
   p.order = reinterpret_cast<const int32_t*>(ws + 256);
-  p.g = g; p.beta = beta; p.cu = cu; p.state_in = state_in; p.state_out = state_out;
+  p.gates = gates; p.cu = cu; p.state_in = state_in; p.state_out = state_out;
   p.z = z; p.norm_w = norm_w; p.out = out; p.err = env.err;
   p.N = N; p.T = T; p.Hk = Hk; p.Hv = Hv; p.q_scale = q_scale; p.l2_eps = l2_eps; p.rms_eps = rms_eps;
   cudaError_t e = launch_chunk_schedule(env.stream, cu, N, reinterpret_cast<int32_t*>(ws + 256), p.counter, nullptr);

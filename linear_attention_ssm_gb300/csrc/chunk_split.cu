@@ -96,8 +96,7 @@ __device__ unsigned g_test_drop_vec_copy;      // 1: an item's first vector-bloc
 
 struct PrepParams {
   CUtensorMap tmap;  // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle
-  const float* g;
-  const float* beta;
+  GateSrc gates;
   const int32_t* cu;
   const int32_t* chunk_off;
   const int32_t* seg_pref;  // this segment's exclusive prefix over sequences of their chunk counts [N + 1]
@@ -391,9 +390,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const __grid_co
     b_next = 0.f;
     const int t = tid / G;
     if (tid < 64 * G && t < un.L) {
-      const size_t o = (size_t)(un.c0 + t) * p.Hv + h0 + (tid - t * G);
-      g_next = __ldg(p.g + o);
-      b_next = __ldg(p.beta + o);
+      const int hh = h0 + (tid - t * G);
+      load_gate(p.gates, (size_t)(un.c0 + t) * p.Hv + hh, hh, g_next, b_next);
     }
   };
 
@@ -1208,7 +1206,7 @@ size_t split_workspace_bytes(int N, int T, int Hk, int Hv) {
          (size_t)chunk_bound(N, T) * (size_t)Hv * REC_BYTES;
 }
 
-cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv, const float* g, const float* beta,
+cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv, const GateSrc& gates,
                                        const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale, float l2_eps,
                                        const float* state_in, float* state_out, const uint16_t* z,
                                        const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace) {
@@ -1255,7 +1253,7 @@ cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv
   PrepParams pp;
   memset(&pp, 0, sizeof pp);
   pp.tmap = tmap;
-  pp.g = g; pp.beta = beta; pp.cu = cu; pp.chunk_off = lay.chunk_off; pp.rec = lay.rec; pp.err = env.err;
+  pp.gates = gates; pp.cu = cu; pp.chunk_off = lay.chunk_off; pp.rec = lay.rec; pp.err = env.err;
   pp.N = N; pp.T = T; pp.Hk = Hk; pp.Hv = Hv; pp.nseg = nseg; pp.nc_max = (int)nc_max;
   pp.q_scale = q_scale; pp.l2_eps = l2_eps;
 

@@ -87,13 +87,14 @@ __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
 // into shared memory by one bulk copy issued before the conv step, so the state bytes are in
 // flight while the conv and the norms are computed; the rows are then read from shared memory.
 // Used when the slice fits (binary16 state, R <= 3: 96 KB).  Otherwise rows stream from global.
-// kPerChannel: the KDA form -- g is [B, Hv, Dk], a log decay per key channel, applied as
+// kPerChannel: the KDA form -- gates.g is [B, Hv, Dk], a log decay per key channel, applied as
 // exp(max(g, g_min)) to the state's key columns (GLM-5.3-Flash kernel TDD ledger, slice I2);
-// otherwise g is [B, Hv], one decay per head (the GDN step).
+// otherwise one decay per head (the GDN step), read from gates.g [B, Hv] or derived from the
+// projections a, b and A_log, dt_bias (load_gate) once per CTA, beside the conv step.
 template <typename StateT, bool kStaged, bool kPerChannel = false>
 __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ conv_w, uint16_t* conv_state,
-    const float* __restrict__ g, const float* __restrict__ beta, StateT* state,
+    const GateSrc gates, StateT* state,
     const uint16_t* __restrict__ z, const uint16_t* __restrict__ norm_w, float q_scale, float l2_eps,
     float rms_eps, uint16_t* __restrict__ out, int Hk, int Hv, unsigned* err, float g_min = 0.f) {
   const int j = blockIdx.x;        // K head
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
   __shared__ float s_v[kMaxRatio][kHeadDim];
   __shared__ float s_o[kMaxRatio][kHeadDim];
   __shared__ float s_norm[2];
+  __shared__ float s_alpha[kMaxRatio], s_bt[kMaxRatio];  // the GDN step's per-head decay and beta
   __shared__ uint64_t s_bar;
   extern __shared__ __align__(128) uint8_t s_state[];  // kStaged: R x Dv x Dk StateT
 
@@ -121,6 +123,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
       if (!g_test_drop_state_copy)
 #endif
         bulk_load(smem_u32(s_state), slice, bytes, bar);
+    }
+  }
+
+  if constexpr (!kPerChannel) {  // the gates of the CTA's R V heads (visible after the conv's barrier)
+    if (tid < R) {
+      float gg, bt;
+      load_gate(gates, (size_t)b * Hv + j * R + tid, j * R + tid, gg, bt);
+      s_alpha[tid] = expf(gg);
+      s_bt[tid] = bt;
     }
   }
 
@@ -192,17 +203,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(
   for (int hh = 0; hh < R; ++hh) {
     const int h = j * R + hh;
     float4 a4, kd;  // the decay of this lane's four key channels; the key they multiply (decayed)
+    float bt;
     if constexpr (kPerChannel) {
-      const float4 gv = __ldg(reinterpret_cast<const float4*>(g + ((size_t)b * Hv + h) * kHeadDim) + lane);
+      const float4 gv = __ldg(reinterpret_cast<const float4*>(gates.g + ((size_t)b * Hv + h) * kHeadDim) + lane);
       a4 = make_float4(expf(fmaxf(gv.x, g_min)), expf(fmaxf(gv.y, g_min)), expf(fmaxf(gv.z, g_min)),
                        expf(fmaxf(gv.w, g_min)));
       kd = make_float4(a4.x * kn.x, a4.y * kn.y, a4.z * kn.z, a4.w * kn.w);  // (S diag(a)) k = S (a * k)
+      bt = __ldg(gates.beta + (size_t)b * Hv + h);
     } else {
-      const float alpha = expf(__ldg(g + (size_t)b * Hv + h));
+      const float alpha = s_alpha[hh];
       a4 = make_float4(alpha, alpha, alpha, alpha);
       kd = kn;
+      bt = s_bt[hh];
     }
-    const float bt = __ldg(beta + (size_t)b * Hv + h);
     StateT* S = slice + ((size_t)hh * kHeadDim + warp * kRowsPerWarp) * kHeadDim;
     float4 row[kRowsPerWarp];
     if constexpr (kStaged) {
@@ -279,13 +292,14 @@ cudaError_t launch_kda_decode_step(const LaunchEnv& env, const uint16_t* x, cons
                                    float* state, const uint16_t* z, const uint16_t* norm_w, float q_scale,
                                    float l2_eps, float rms_eps, uint16_t* out, int B, int Hk, int Hv) {
   if (B <= 0) return cudaSuccess;
+  const GateSrc gates = {g, beta, nullptr, nullptr, nullptr, nullptr};
   decode_step_kernel<float, false, true><<<dim3(Hk, B), kThreads, 0, env.stream>>>(
-      x, conv_w, conv_state, g, beta, state, z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv, env.err, g_min);
+      x, conv_w, conv_state, gates, state, z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv, env.err, g_min);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
-                               uint16_t* conv_state, const float* g, const float* beta, void* state,
+                               uint16_t* conv_state, const GateSrc& gates, void* state,
                                bool fp16_state, const uint16_t* z, const uint16_t* norm_w, float q_scale,
                                float l2_eps, float rms_eps, uint16_t* out, int B, int Hk, int Hv) {
   if (B <= 0) return cudaSuccess;
@@ -305,15 +319,15 @@ cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const ui
       configured[dev] = 1;
     }
     decode_step_kernel<__half, true><<<grid, kThreads, slice_bytes, env.stream>>>(
-        x, conv_w, conv_state, g, beta, static_cast<__half*>(state), z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv,
+        x, conv_w, conv_state, gates, static_cast<__half*>(state), z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv,
         env.err);
   } else if (fp16_state) {
     decode_step_kernel<__half, false><<<grid, kThreads, 0, env.stream>>>(
-        x, conv_w, conv_state, g, beta, static_cast<__half*>(state), z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv,
+        x, conv_w, conv_state, gates, static_cast<__half*>(state), z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv,
         env.err);
   } else {
     decode_step_kernel<float, false><<<grid, kThreads, 0, env.stream>>>(
-        x, conv_w, conv_state, g, beta, static_cast<float*>(state), z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv,
+        x, conv_w, conv_state, gates, static_cast<float*>(state), z, norm_w, q_scale, l2_eps, rms_eps, out, Hk, Hv,
         env.err);
   }
   return cudaGetLastError();

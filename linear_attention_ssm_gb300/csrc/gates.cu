@@ -11,13 +11,6 @@ namespace gdn {
 
 namespace {
 
-__device__ __forceinline__ void gate_one(float a, float b, float A_log, float dt_bias, float& g, float& beta) {
-  const float x = a + dt_bias;
-  const float sp = x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x));  // log(1 + e^x), no overflow
-  g = -expf(A_log) * sp;
-  beta = 1.0f / (1.0f + expf(-b));
-}
-
 // 8 consecutive elements per thread and iteration when Hv % 8 == 0 (an octet never crosses a row:
 // 16-byte loads of a and b, two 16-byte stores each of g and beta); one element otherwise.
 __global__ void __launch_bounds__(256) gates_kernel(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,

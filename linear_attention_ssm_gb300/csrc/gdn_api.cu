@@ -173,11 +173,30 @@ size_t gdn_chunk_prefill_min_workspace_size(const gdn_geometry* geo, int32_t num
   return num_seqs > 0 ? gdn::chunk_prefill_workspace_bytes(num_seqs) : 0;
 }
 
-gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g, const float* beta,
-                             const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens, float q_scale,
-                             float l2_eps, const float* state_in, float* state_out, const gdn_bf16* z,
-                             const gdn_bf16* norm_w, float rms_eps, gdn_bf16* out, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+// The gate inputs of a call: g and beta, or the projections a, b with A_log and dt_bias.
+gdn_status check_gates(const gdn::GateSrc& gs) {
+  if (gs.a) {
+    if (!gs.b || !gs.A_log || !gs.dt_bias) return fail(GDN_ERR_INVALID_ARGUMENT, "a, b, A_log or dt_bias is NULL");
+    if ((reinterpret_cast<uintptr_t>(gs.a) | reinterpret_cast<uintptr_t>(gs.b)) & 1u)
+      return fail(GDN_ERR_MISALIGNED, "a or b is not 2-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(gs.A_log) | reinterpret_cast<uintptr_t>(gs.dt_bias)) & 3u)
+      return fail(GDN_ERR_MISALIGNED, "A_log or dt_bias is not 4-byte aligned");
+    return GDN_OK;
+  }
+  if (!gs.g || !gs.beta) return fail(GDN_ERR_INVALID_ARGUMENT, "g or beta is NULL");
+  if ((reinterpret_cast<uintptr_t>(gs.g) | reinterpret_cast<uintptr_t>(gs.beta)) & 3u)
+    return fail(GDN_ERR_MISALIGNED, "g or beta is not 4-byte aligned");
+  return GDN_OK;
+}
+
+gdn_status chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const gdn::GateSrc& gates,
+                         const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens, float q_scale,
+                         float l2_eps, const float* state_in, float* state_out, const gdn_bf16* z,
+                         const gdn_bf16* norm_w, float rms_eps, gdn_bf16* out, void* workspace,
+                         size_t workspace_bytes, void* stream) {
   gdn_status s = check_geometry(geo);
   if (s != GDN_OK) return s;
   if (num_seqs < 0 || total_tokens < 0)
@@ -192,9 +211,7 @@ gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const
   if (total_tokens > 0) {
     GDN_REQUIRE(qkv, "qkv");
     GDN_REQUIRE(out, "out");
-    if (!g || !beta) return fail(GDN_ERR_INVALID_ARGUMENT, "g or beta is NULL");
-    if ((reinterpret_cast<uintptr_t>(g) | reinterpret_cast<uintptr_t>(beta)) & 3u)
-      return fail(GDN_ERR_MISALIGNED, "g or beta is not 4-byte aligned");
+    if ((s = check_gates(gates)) != GDN_OK) return s;
   }
   GDN_OPTIONAL(state_in, "state_in");
   GDN_OPTIONAL(state_out, "state_out");
@@ -215,10 +232,35 @@ gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const
   }
   gdn::LaunchEnv env;
   if ((s = make_env(stream, &env)) != GDN_OK) return s;
-  return launched(gdn::launch_chunk_prefill(env, g_chunk_mode, qkv, g, beta, cu_seqlens, num_seqs, total_tokens,
+  return launched(gdn::launch_chunk_prefill(env, g_chunk_mode, qkv, gates, cu_seqlens, num_seqs, total_tokens,
                                             geo->num_k_heads, geo->num_v_heads, q_scale, l2_eps, state_in,
                                             state_out, z, norm_w, rms_eps, out, workspace, workspace_bytes),
                   "chunk prefill launch");
+}
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g, const float* beta,
+                             const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens, float q_scale,
+                             float l2_eps, const float* state_in, float* state_out, const gdn_bf16* z,
+                             const gdn_bf16* norm_w, float rms_eps, gdn_bf16* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  const gdn::GateSrc gates = {g, beta, nullptr, nullptr, nullptr, nullptr};
+  return chunk_prefill(geo, qkv, gates, cu_seqlens, num_seqs, total_tokens, q_scale, l2_eps, state_in, state_out, z,
+                       norm_w, rms_eps, out, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_chunk_prefill_fused_gates(const gdn_geometry* geo, const gdn_bf16* qkv, const gdn_bf16* a,
+                                         const gdn_bf16* b, const float* A_log, const float* dt_bias,
+                                         const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                                         float q_scale, float l2_eps, const float* state_in, float* state_out,
+                                         const gdn_bf16* z, const gdn_bf16* norm_w, float rms_eps, gdn_bf16* out,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!a) return fail(GDN_ERR_INVALID_ARGUMENT, "a is NULL");
+  const gdn::GateSrc gates = {nullptr, nullptr, a, b, A_log, dt_bias};
+  return chunk_prefill(geo, qkv, gates, cu_seqlens, num_seqs, total_tokens, q_scale, l2_eps, state_in, state_out, z,
+                       norm_w, rms_eps, out, workspace, workspace_bytes, stream);
 }
 
 gdn_status gdn_gated_rmsnorm(const gdn_geometry* geo, const gdn_bf16* o, const gdn_bf16* z, const gdn_bf16* norm_w,
@@ -242,7 +284,7 @@ gdn_status gdn_gated_rmsnorm(const gdn_geometry* geo, const gdn_bf16* o, const g
 
 namespace {
 gdn_status decode_step(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w, gdn_bf16* conv_state,
-                       const float* g, const float* beta, void* state, bool fp16_state, const gdn_bf16* z,
+                       const gdn::GateSrc& gates, void* state, bool fp16_state, const gdn_bf16* z,
                        const gdn_bf16* norm_w, float q_scale, float l2_eps, float rms_eps, gdn_bf16* out,
                        int32_t batch, void* stream) {
   gdn_status s = check_geometry(geo);
@@ -259,13 +301,11 @@ gdn_status decode_step(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf1
   GDN_REQUIRE(z, "z");
   GDN_REQUIRE(norm_w, "norm_w");
   GDN_REQUIRE(out, "out");
-  if (!g || !beta) return fail(GDN_ERR_INVALID_ARGUMENT, "g or beta is NULL");
-  if ((reinterpret_cast<uintptr_t>(g) | reinterpret_cast<uintptr_t>(beta)) & 3u)
-    return fail(GDN_ERR_MISALIGNED, "g or beta is not 4-byte aligned");
+  if ((s = check_gates(gates)) != GDN_OK) return s;
   if (!(l2_eps >= 0.f) || !(rms_eps >= 0.f)) return fail(GDN_ERR_INVALID_ARGUMENT, "eps must be >= 0");
   gdn::LaunchEnv env;
   if ((s = make_env(stream, &env)) != GDN_OK) return s;
-  return launched(gdn::launch_decode_step(env, x, conv_w, conv_state, g, beta, state, fp16_state, z, norm_w,
+  return launched(gdn::launch_decode_step(env, x, conv_w, conv_state, gates, state, fp16_state, z, norm_w,
                                           q_scale, l2_eps, rms_eps, out, batch, geo->num_k_heads,
                                           geo->num_v_heads),
                   "decode launch");
@@ -278,7 +318,19 @@ gdn_status gdn_decode_step(const gdn_geometry* geo, const gdn_bf16* x, const gdn
                            const float* g, const float* beta, float* state, const gdn_bf16* z,
                            const gdn_bf16* norm_w, float q_scale, float l2_eps, float rms_eps, gdn_bf16* out,
                            int32_t batch, void* stream) {
-  return decode_step(geo, x, conv_w, conv_state, g, beta, state, false, z, norm_w, q_scale, l2_eps, rms_eps, out,
+  const gdn::GateSrc gates = {g, beta, nullptr, nullptr, nullptr, nullptr};
+  return decode_step(geo, x, conv_w, conv_state, gates, state, false, z, norm_w, q_scale, l2_eps, rms_eps, out,
+                     batch, stream);
+}
+
+gdn_status gdn_decode_step_fused_gates(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w,
+                                       gdn_bf16* conv_state, const gdn_bf16* a, const gdn_bf16* b, const float* A_log,
+                                       const float* dt_bias, float* state, const gdn_bf16* z, const gdn_bf16* norm_w,
+                                       float q_scale, float l2_eps, float rms_eps, gdn_bf16* out, int32_t batch,
+                                       void* stream) {
+  if (batch > 0 && !a) return fail(GDN_ERR_INVALID_ARGUMENT, "a is NULL");
+  const gdn::GateSrc gates = {nullptr, nullptr, a, b, A_log, dt_bias};
+  return decode_step(geo, x, conv_w, conv_state, gates, state, false, z, norm_w, q_scale, l2_eps, rms_eps, out,
                      batch, stream);
 }
 
@@ -358,7 +410,8 @@ gdn_status gdn_decode_step_fp16_state(const gdn_geometry* geo, const gdn_bf16* x
                                       gdn_bf16* conv_state, const float* g, const float* beta, gdn_f16* state,
                                       const gdn_bf16* z, const gdn_bf16* norm_w, float q_scale, float l2_eps,
                                       float rms_eps, gdn_bf16* out, int32_t batch, void* stream) {
-  return decode_step(geo, x, conv_w, conv_state, g, beta, state, true, z, norm_w, q_scale, l2_eps, rms_eps, out,
+  const gdn::GateSrc gates = {g, beta, nullptr, nullptr, nullptr, nullptr};
+  return decode_step(geo, x, conv_w, conv_state, gates, state, true, z, norm_w, q_scale, l2_eps, rms_eps, out,
                      batch, stream);
 }
 

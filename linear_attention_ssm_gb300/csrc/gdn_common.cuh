@@ -106,6 +106,38 @@ __device__ __forceinline__ float2 tanh_half_bf16x2(uint32_t zz) {
 // sigmoid(x) = (1 + tanh(x / 2)) / 2: one special-function operation
 __device__ __forceinline__ float sigmoid_tanh(float x) { return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f); }
 
+// The gates of the recurrence from their projections, for one (row, V head):
+//   g = -exp(A_log) softplus(a + dt_bias),  beta = sigmoid(b),  softplus(x) = log(1 + e^x)
+// (the gate of the published Gated DeltaNet / Mamba-2 layers; the GDN pages name these inputs but
+// give no formula).  One definition serves the standalone gates kernel and every kernel that
+// derives its gates itself, so both routes compute the same bits.
+__device__ __forceinline__ void gate_one(float a, float b, float A_log, float dt_bias, float& g, float& beta) {
+  const float x = a + dt_bias;
+  const float sp = x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x));  // log(1 + e^x), no overflow
+  g = -expf(A_log) * sp;
+  beta = 1.0f / (1.0f + expf(-b));
+}
+
+// Where a kernel takes its gates from: g and beta given ([rows, Hv] fp32), or, when `a` is set,
+// derived from the projections a, b ([rows, Hv] bf16) and the per-head A_log, dt_bias ([Hv] fp32).
+struct GateSrc {
+  const float* g;
+  const float* beta;
+  const uint16_t* a;
+  const uint16_t* b;
+  const float* A_log;
+  const float* dt_bias;
+};
+// The gates of element idx = row * Hv + h.
+__device__ __forceinline__ void load_gate(const GateSrc& s, size_t idx, int h, float& g, float& beta) {
+  if (s.a) {
+    gate_one(bf2f(__ldg(s.a + idx)), bf2f(__ldg(s.b + idx)), __ldg(s.A_log + h), __ldg(s.dt_bias + h), g, beta);
+  } else {
+    g = __ldg(s.g + idx);
+    beta = __ldg(s.beta + idx);
+  }
+}
+
 __device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
 }

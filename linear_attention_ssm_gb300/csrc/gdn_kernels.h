@@ -26,7 +26,7 @@ cudaError_t launch_kda_decode_step(const LaunchEnv& env, const uint16_t* x, cons
                                    float* state, const uint16_t* z, const uint16_t* norm_w, float q_scale,
                                    float l2_eps, float rms_eps, uint16_t* out, int B, int Hk, int Hv);
 cudaError_t launch_decode_step(const LaunchEnv& env, const uint16_t* x, const uint16_t* conv_w,
-                               uint16_t* conv_state, const float* g, const float* beta, void* state,
+                               uint16_t* conv_state, const GateSrc& gates, void* state,
                                bool fp16_state, const uint16_t* z, const uint16_t* norm_w, float q_scale,
                                float l2_eps, float rms_eps, uint16_t* out, int B, int Hk, int Hv);
 
@@ -86,12 +86,12 @@ cudaError_t launch_chunk_schedule(cudaStream_t stream, const int32_t* cu, int N,
 
 // mode 0: tensor cores, split path when the workspace holds it (else fused); mode 1: fused, MMAs
 // emulated on CUDA cores; mode 2: fused, tensor cores.
-cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t* qkv, const float* g,
-                                 const float* beta, const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale,
+cudaError_t launch_chunk_prefill(const LaunchEnv& env, int mode, const uint16_t* qkv, const GateSrc& gates,
+                                 const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale,
                                  float l2_eps, const float* state_in, float* state_out, const uint16_t* z,
                                  const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace,
                                  size_t workspace_bytes);
-cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv, const float* g, const float* beta,
+cudaError_t launch_chunk_prefill_split(const LaunchEnv& env, const uint16_t* qkv, const GateSrc& gates,
                                        const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale, float l2_eps,
                                        const float* state_in, float* state_out, const uint16_t* z,
                                        const uint16_t* norm_w, float rms_eps, uint16_t* out, void* workspace);

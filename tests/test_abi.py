@@ -199,6 +199,25 @@ def test_verify_stash_size_and_argument_checks(lib):
     assert lib.gdn_verify_commit_fp16_state(geo, FAKE, FAKE, 3 * 8 * 53440, FAKE, FAKE, 4, 8, None) == 7
 
 
+def test_fused_gate_entry_points_reject_bad_arguments(lib):
+    geo = _geo()
+    P = ctypes.c_void_p
+    # prefill: (geo, qkv, a, b, A_log, dt_bias, cu, N, T, q_scale, l2_eps, s_in, s_out, z, w, rms_eps, out, ws, wsb, stream)
+    args = lambda a, b, al, db: (geo, FAKE, a, b, al, db, FAKE, 2, 8, 0.088, 1e-6, None, None, None, None, 1e-6, FAKE,
+                                 FAKE, 1 << 20, None)
+    assert lib.gdn_chunk_prefill_fused_gates(*args(None, FAKE, FAKE, FAKE)) == 1      # a missing
+    assert lib.gdn_chunk_prefill_fused_gates(*args(FAKE, None, FAKE, FAKE)) == 1      # b missing
+    assert lib.gdn_chunk_prefill_fused_gates(*args(FAKE, FAKE, None, FAKE)) == 1      # A_log missing
+    assert lib.gdn_chunk_prefill_fused_gates(*args(P(0x10001), FAKE, FAKE, FAKE)) == 3  # a odd
+    assert lib.gdn_chunk_prefill_fused_gates(*args(FAKE, FAKE, FAKE, ODD)) == 3       # dt_bias not 4-aligned
+    # decode: (geo, x, w, cs, a, b, A_log, dt_bias, state, z, nw, q_scale, l2, rms, out, batch, stream)
+    dargs = lambda a, al: (geo, FAKE, FAKE, FAKE, a, FAKE, al, FAKE, FAKE, FAKE, FAKE, 0.088, 1e-6, 1e-6, FAKE, 4, None)
+    assert lib.gdn_decode_step_fused_gates(*dargs(None, FAKE)) == 1
+    assert lib.gdn_decode_step_fused_gates(*dargs(FAKE, ODD)) == 3
+    assert lib.gdn_decode_step_fused_gates(geo, None, None, None, None, None, None, None, None, None, None, 0.088,
+                                           1e-6, 1e-6, None, 0, None) == 0    # batch 0: nothing to do
+
+
 def test_gates_reject_bad_arguments(lib):
     geo = _geo()
     assert lib.gdn_gates(geo, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1, None) == 1

@@ -774,9 +774,9 @@ def run_ours(args, rank, world, local):
         stream.wait_event(ev["in"][bi])
         stream.wait_event(ev["in2"][bi])
         stream.wait_event(ev["out"][bi])  # the outputs two steps back have been read out
-        gdn.gdn_conv1d_prefill(B["x"], w, cu, B["cs"], B["cs_out"], qkv)
-        gdn.gdn_chunk_prefill(qkv, B["g"], B["beta"], cu, inp["q_scale"], 1e-6, B["st"], B["st_out"], B["z"], nw,
-                              1e-6, B["out"], workspace=ws)
+        gdn.gdn_prefill(B["x"], w, cu, B["g"], B["beta"], B["z"], nw, inp["q_scale"], 1e-6, 1e-6, state_in=B["st"],
+                        state_out=B["st_out"], conv_state_in=B["cs"], conv_state_out=B["cs_out"], qkv_buf=qkv,
+                        out=B["out"], workspace=ws)
         ev["comp"][bi].record(stream)
         with torch.cuda.stream(cout):
             cout.wait_event(ev["comp"][bi])

@@ -56,6 +56,7 @@ def _configure(lib, debug: bool):
         "gdn_chunk_prefill_min_workspace_size": ([G, I, I], S),
         "gdn_chunk_prefill": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P, S, P], ctypes.c_int),
         "gdn_chunk_prefill_noalloc": ([G, P, P, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
+        "gdn_prefill": ([G, P, P, P, I, I, P, P, P, P, P, F, F, P, P, P, P, F, P, P, S, P], ctypes.c_int),
         "gdn_gated_rmsnorm": ([G, P, P, P, F, P, I, P], ctypes.c_int),
         "gdn_decode_step": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
         "gdn_decode_step_fp16_state": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
@@ -592,13 +593,41 @@ def gdn_debug_mma_probe_ex(A, B, flags, stream=None):
 
 def gdn_prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, q_scale, l2_eps=1e-6, rms_eps=1e-6,
                 state_in=None, state_out=None, conv_state_in=None, conv_state_out=None,
-                qkv_buf=None, out=None, geometry: Geometry = QWEN_GDN, stream=None):
-    """The whole prefill sublayer: gdn_conv1d_prefill, then gdn_chunk_prefill with the gated
-    RMSNorm fused into its epilogue.  Returns out [T, Hv, Dv] bf16."""
-    qkv = gdn_conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in, conv_state_out, qkv_buf,
-                             geometry=geometry, stream=stream)
-    return gdn_chunk_prefill(qkv, g, beta, cu_seqlens, q_scale, l2_eps, state_in, state_out, z,
-                             norm_w, rms_eps, out, geometry=geometry, stream=stream)
+                qkv_buf=None, out=None, workspace=None, geometry: Geometry = QWEN_GDN, stream=None):
+    """The whole prefill sublayer in one call (gdn_prefill): the conv1d+SiLU stage into qkv_buf,
+    then the chunk-wise gated delta rule with the gated RMSNorm fused (z, norm_w given) or not.
+    Returns out [T, Hv, Dv] bf16."""
+    lib = _L()
+    C, W = geometry.conv_dim, geometry.conv_width
+    hv, dv, dk = geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
+    N = cu_seqlens.numel() - 1
+    T = x.shape[0]
+    _dev(x, torch.bfloat16, "x", (T, C))
+    _dev(conv_w, torch.bfloat16, "conv_w", (C, W))
+    _dev(cu_seqlens, torch.int32, "cu_seqlens", (N + 1,))
+    _dev(conv_state_in, torch.bfloat16, "conv_state_in", (N, C, W - 1))
+    _dev(conv_state_out, torch.bfloat16, "conv_state_out", (N, C, W - 1))
+    _dev(g, torch.float32, "g", (T, hv))
+    _dev(beta, torch.float32, "beta", (T, hv))
+    _dev(state_in, torch.float32, "state_in", (N, hv, dv, dk))
+    _dev(state_out, torch.float32, "state_out", (N, hv, dv, dk))
+    _dev(z, torch.bfloat16, "z", (T, hv, dv))
+    _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
+    if qkv_buf is None:
+        qkv_buf = torch.empty((T, C), dtype=torch.bfloat16, device=x.device)
+    _dev(qkv_buf, torch.bfloat16, "qkv_buf", (T, C))
+    if out is None:
+        out = torch.empty((T, hv, dv), dtype=torch.bfloat16, device=x.device)
+    _dev(out, torch.bfloat16, "out", (T, hv, dv))
+    need = lib.gdn_chunk_prefill_workspace_size(_geo(geometry), N, T)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.gdn_prefill(_geo(geometry), _p(x), _p(conv_w), _p(cu_seqlens), N, T, _p(conv_state_in),
+                           _p(conv_state_out), _p(qkv_buf), _p(g), _p(beta), float(q_scale), float(l2_eps),
+                           _p(state_in), _p(state_out), _p(z), _p(norm_w), float(rms_eps), _p(out), _p(workspace),
+                           wbytes, _stream(stream)))
+    return out
 
 
 def gdn_kda_prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, q_scale, g_min=float("-inf"), l2_eps=1e-6,

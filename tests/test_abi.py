@@ -218,6 +218,25 @@ def test_fused_gate_entry_points_reject_bad_arguments(lib):
                                            1e-6, 1e-6, None, 0, None) == 0    # batch 0: nothing to do
 
 
+def test_one_call_prefill_checks_both_stages_before_launching(lib):
+    """gdn_prefill refuses a bad argument of either stage with the stage's own status, before any
+    CUDA call (here, with no GPU, any CUDA call would end in GDN_ERR_CUDA instead)."""
+    geo = _geo()
+    X, QKV = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x4000000)  # apart by more than T * C * 2 bytes
+    # (geo, x, conv_w, cu, N, T, cs_in, cs_out, qkv, g, beta, q_scale, l2, s_in, s_out, z, nw, rms, out, ws, wsb, stream)
+    def call(x=X, w=FAKE, cs_out=None, qkv=QKV, g=FAKE, ws=FAKE, wsb=1 << 30, n=2, t=8):
+        return lib.gdn_prefill(geo, x, w, FAKE, n, t, None, cs_out, qkv, g, FAKE, 0.088, 1e-6, None, None, None,
+                               None, 1e-6, FAKE, ws, wsb, None)
+    assert call(w=None) == 1                        # conv weights missing
+    assert call(qkv=None) == 1                      # conv output buffer missing
+    assert call(qkv=X) == 1                         # conv output overlaps its input
+    assert call(cs_out=ODD) == 3                    # conv state misaligned
+    assert call(g=None) == 1                        # the chunk stage's gates missing
+    assert call(ws=None) == 7                       # the chunk stage's workspace missing
+    assert call(n=0, t=0) == 0                      # nothing to do
+    assert call(n=-1) == 1
+
+
 def test_gates_reject_bad_arguments(lib):
     geo = _geo()
     assert lib.gdn_gates(geo, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1, None) == 1

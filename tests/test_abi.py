@@ -153,9 +153,13 @@ def test_fast_path_workspace_size():
     for n, t in ((1, 16), (4, 4 * 4096), (8, 32735), (3, 0)):
         chunks = (t + 63 * n) // 64
         pad = lambda b: -(-b // 256) * 256
-        # counters, order, chunk offsets, four per-segment chunk prefixes
-        head = 256 + pad(4 * n) + pad(4 * (n + 1)) + pad(4 * 4 * (n + 1))
-        assert lib.gdn_chunk_prefill_workspace_size(_geo(), n, t) == head + chunks * 48 * rec
+        # counters, order, chunk offsets, four per-segment chunk prefixes; parts per sequence, slot
+        # bases, work items (one per sequence plus up to 2 x 32 for parts), 32 x 192 completion flags
+        head = (256 + pad(4 * n) + pad(4 * (n + 1)) + pad(4 * 4 * (n + 1)) + 2 * pad(4 * n) + pad(8 * (n + 64)) +
+                pad(4 * 32 * 192))
+        # from 4,096 tokens on: 32 state slots of 48 heads x 128 x 128 fp32 for the parts of long sequences
+        slots = 32 * 48 * 128 * 128 * 4 if t >= 4096 else 0
+        assert lib.gdn_chunk_prefill_workspace_size(_geo(), n, t) == head + chunks * 48 * rec + slots
     # the bound covers the worst case: every sequence one token past a chunk boundary
     lengths = [65] * 7
     assert sum(-(-L // 64) for L in lengths) <= (sum(lengths) + 63 * 7) // 64

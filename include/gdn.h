@@ -118,8 +118,10 @@ GDN_API gdn_status gdn_conv1d_prefill(const gdn_geometry* geo, const gdn_bf16* x
  * num_seqs == 0).  With at least this much, the call runs as two kernels: one that forms, for
  * every 64-token chunk at once, the quantities that do not depend on the recurrent state (the
  * intra-chunk decay factors, the solve (I + A)^-1 and the masked query-key product, about 25 KB
- * per chunk and V head), and one that carries the state through the chunks.  The workspace
- * contents need no initialisation and are dead when the call's kernels finish.
+ * per chunk and V head), and one that carries the state through the chunks.  From 4,096 tokens
+ * on it also holds 32 state slots of Hv x 128 x 128 fp32 for the parts of long sequences (see
+ * gdn_chunk_prefill).  The workspace contents need no initialisation and are dead when the call's
+ * kernels finish.
  */
 GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_geometry* geo, int32_t num_seqs,
                                                 int32_t total_tokens);
@@ -162,6 +164,15 @@ GDN_API size_t gdn_chunk_prefill_min_workspace_size(const gdn_geometry* geo, int
  * writes is ordered before later work on `stream`.  Calls from different streams whose side-stream
  * work is queued together run it one after the other.  Under stream capture, everything runs on
  * `stream` as one segment.
+ *
+ * Long sequences: from 4,096 tokens on, a sequence whose segment holds more than 1.5 times the
+ * chunks one CTA slot would get (the segment's work spread over two CTAs per SM) is cut into up to
+ * eight parts that run at once, decided on the device from cu_seqlens; parts after the first start
+ * from a state combined from the earlier parts' transitions.  Their launch runs on a second
+ * library-owned stream (per device, like the side stream) and is joined to `stream` before the
+ * call's work ends; under stream capture it runs on `stream`.  A part waits (bounded) for the
+ * transitions it needs; a wait that runs out sets GDN_ERR_TIMEOUT in the device error word.  With
+ * one segment and state_out equal to state_in, nothing is split.
  */
 GDN_API gdn_status gdn_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g,
                                      const float* beta, const int32_t* cu_seqlens,

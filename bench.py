@@ -1007,9 +1007,10 @@ def run_ours(args, rank, world, local):
             "verify_fp16_state": verify_f16,
             "gates": gates, "kda_prefill": kda_prefill,
             "varlen": varlen, "small_configs": small, "cpu_baseline": cpu, "clocks": clk,
-            # per step: conv1d + conv-state kernels, the chunk prefill's schedule and segment-table
-            # kernels, then a prep and a state kernel for each of its three chunk segments
-            "gpu_launches": (2 + 2 + 2 * 3) * args.steps,
+            # per step: conv1d + conv-state kernels, the chunk prefill's schedule and segment / part
+            # table kernels, then for each of its three chunk segments a prep, a state and a parts
+            # launch (the state kernel of split sequences; with nothing split its CTAs return at once)
+            "gpu_launches": (2 + 2 + 3 * 3) * args.steps,
             "arithmetic": "bf16 tensor-core operands (fp32 operands split into bf16 hi+lo), fp32 accumulate and state",
         }
         line["summary"] = compact_summary(line, step_dist)

@@ -165,9 +165,9 @@ GDN_API size_t gdn_chunk_prefill_min_workspace_size(const gdn_geometry* geo, int
  * work is queued together run it one after the other.  Under stream capture, everything runs on
  * `stream` as one segment.
  *
- * Long sequences: from 4,096 tokens on, a sequence whose segment holds more than 1.5 times the
- * chunks one CTA slot would get (the segment's work spread over two CTAs per SM) is cut into up to
- * eight parts that run at once, decided on the device from cu_seqlens; parts after the first start
+ * Long sequences: from 4,096 tokens on, a sequence whose segment holds more than twice the chunks
+ * one CTA slot would get (the segment's work spread over two CTAs per SM) is cut into three or four
+ * parts that run at once, decided on the device from cu_seqlens; parts after the first start
  * from a state combined from the earlier parts' transitions.  Their launch runs on a second
  * library-owned stream (per device, like the side stream) and is joined to `stream` before the
  * call's work ends; under stream capture it runs on `stream`.  A part waits (bounded) for the

@@ -100,7 +100,7 @@ __host__ __device__ __forceinline__ int seg_begin(int k, int nch, int nseg) { re
 // wait cannot deadlock: the items it waits for were taken earlier by CTAs that are running and
 // wait for nothing.  A split sequence hands its state to the next segment through a slot of its
 // own, so no part reads a state that another part has already replaced.
-constexpr int kMaxParts = 8;          // parts per sequence and segment
+constexpr int kMaxParts = 4;          // parts per sequence and segment (measured best of 3, 4, 5 and 8)
 constexpr int kMinPart = 8;           // chunks per part at least
 constexpr int kMaxSplitSeqs = 8;      // split sequences per call
 constexpr int kSlotCap = 32;          // [Hv][128][128] fp32 state slots per call (L, Phi, hand-off)
@@ -1669,10 +1669,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_part_state_kernel(const __g
 // Run by the segment-table CTA after the schedule (order = longest first): which sequences are cut
 // into parts, and
 // the work items of the state kernel's main and auxiliary launches (the same for every segment).
-// A sequence is split when its shortest segment holds more than 1.5 x the chunks one CTA slot
-// would get if the segment's work were spread evenly (and at least 2 kMinPart): into
-// ceil(m / share) parts (at most kMaxParts), while state slots last.  `allow` is 0 where a split
-// is not possible (one segment updating its state in place, or no slots in the workspace).
+// A sequence is split when its shortest segment holds more than twice the chunks one CTA slot
+// would get if the segment's work were spread evenly (the share, at least kMinPart): into
+// ceil(m / share) parts (3 .. kMaxParts), while state slots last.  A lower threshold split an
+// evenly loaded batch (4 x 4096 tokens: 0.73 -> 1.05 ms), and two parts gain nothing, since a part
+// waits for the L and Phi chains of the part before it.  `allow` is 0 where a split is not
+// possible (one segment updating its state in place, or no slots in the workspace).
 //   items: first (n, q) for L and (n, q | 1 << 16) for Phi, q = 0 .. P - 2 of each split sequence,
 //   then the parts (n, q), q = 0 .. P - 1; counts[0]: all items, counts[1]: the L / Phi items;
 //   the slots' completion flags zeroed.
@@ -1703,10 +1705,10 @@ __device__ __forceinline__ void plan_parts(const int32_t* cu, int N, int Hv, int
       for (int i = 0; i < N && ns < kMaxSplitSeqs; ++i) {
         const int n = __ldg(order + i);
         const int m = nchunks(n) / nseg;  // the shortest segment of this sequence
-        if (2 * m <= 3 * share) break;     // longest first: no later sequence splits either
-        int P = min(kMaxParts, (m + share - 1) / share);
+        if (m <= 2 * share) break;         // longest first: no later sequence splits either
+        int P = min(kMaxParts, (m + share - 1) / share);  // at least 3 here
         while (P > 1 && used + nseg * (2 * P - 1) > kSlotCap) --P;
-        if (P < 2) break;
+        if (P < 3) break;  // two parts gain nothing: a part waits for the chains of the one before
         s_n[ns] = n;
         s_P[ns] = P;
         slot_base[n] = used;

@@ -14,10 +14,10 @@ from tests.test_gpu_chunk import run_oracle
 
 pytestmark = pytest.mark.gpu
 GEO = Geometry(num_k_heads=2, num_v_heads=6)
-# 94 chunks (4 parts per segment), 2, 47 (2 parts), 0 and 22 chunks: the share of one CTA slot is
-# 8 chunks here, and a sequence splits when a segment of it holds more than 12
-LENGTHS = [6000, 100, 3000, 0, 1351]
-PARTS = [4, 1, 2, 1, 1]
+# 55 chunks, 2, 57, 0 and 22 chunks: the share of one CTA slot is 8 chunks here, a sequence splits
+# when a segment of it holds more than 16, into ceil(m / 8) parts: 3 for the first and the third
+LENGTHS = [3500, 100, 3600, 0, 1351]
+PARTS = [3, 1, 3, 1, 1]
 
 
 def _pad(b):
@@ -89,6 +89,6 @@ def test_split_inside_a_captured_graph():
         torch.cuda.synchronize()
         g.gdn_check_device_errors()
         _check(out, st, ref, "graph replay")
-    # one segment: the longest sequence's 94 chunks give a share far below them -> parts
+    # one segment: 55 and 57 chunks against a share of 8 -> four parts each, 22 -> three
     parts = _parts_read_back(ws, N)
-    assert parts[0] > 1 and parts[2] > 1, parts
+    assert parts == [4, 1, 4, 1, 3], parts

@@ -1091,7 +1091,7 @@ struct BoolC {
   static constexpr bool value = B;
 };
 
-// The state kernel of the split sequences' parts (items from chunk_parts_kernel): L and Phi items
+// The state kernel of the split sequences' parts (items from plan_parts): L and Phi items
 // (no outputs), then the parts, each starting from its combined state.  The same chain as
 // chunk_state_kernel, compiled once with and once without the output stage.
 __global__ void __launch_bounds__(kThreads, 2) chunk_part_state_kernel(const __grid_constant__ StateParams p) {
@@ -1667,8 +1667,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_part_state_kernel(const __g
 }
 
 // Run by the segment-table CTA after the schedule (order = longest first): which sequences are cut
-// into parts, and
-// the work items of the state kernel's main and auxiliary launches (the same for every segment).
+// into parts, and the work items of the parts launches (the same for every segment).
 // A sequence is split when its shortest segment holds more than twice the chunks one CTA slot
 // would get if the segment's work were spread evenly (the share, at least kMinPart): into
 // ceil(m / share) parts (3 .. kMaxParts), while state slots last.  A lower threshold split an
@@ -1678,9 +1677,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_part_state_kernel(const __g
 //   items: first (n, q) for L and (n, q | 1 << 16) for Phi, q = 0 .. P - 2 of each split sequence,
 //   then the parts (n, q), q = 0 .. P - 1; counts[0]: all items, counts[1]: the L / Phi items;
 //   the slots' completion flags zeroed.
-__device__ __forceinline__ void plan_parts(const int32_t* cu, int N, int Hv, int nseg, int slots,
-                                           int allow, const int32_t* order, int32_t* part_cnt, int32_t* slot_base, int2* items,
-                                                           int32_t* counts, int* flags, unsigned* counters) {
+__device__ __forceinline__ void plan_parts(const int32_t* cu, int N, int Hv, int nseg, int slots, int allow,
+                                           const int32_t* order, int32_t* part_cnt, int32_t* slot_base, int2* items,
+                                           int32_t* counts, int* flags, unsigned* counters) {
   __shared__ int s_n[kMaxSplitSeqs], s_P[kMaxSplitSeqs], s_extra[kMaxSplitSeqs + 1];
   __shared__ int s_ns;
   __shared__ long long s_total;

@@ -414,6 +414,47 @@ GDN_API gdn_status gdn_kda_recurrence(const gdn_geometry* geo, const gdn_bf16* q
                                       const gdn_bf16* z, const gdn_bf16* norm_w, float rms_eps,
                                       gdn_bf16* out, void* stream);
 
+/*
+ * Workspace bytes of gdn_kda_chunk_prefill: 256 bytes of counters, the longest-first sequence
+ * order and per-sequence chunk offsets (4 bytes per sequence each, rounded up to 256), then one
+ * 108,032-byte record per (64-token chunk, V head) for at most (total_tokens + 63 num_seqs) / 64
+ * chunks.  0 when num_seqs <= 0.
+ */
+GDN_API size_t gdn_kda_chunk_prefill_workspace_size(const gdn_geometry* geo, int32_t num_seqs,
+                                                    int32_t total_tokens);
+
+/*
+ * The KDA recurrence of gdn_kda_recurrence in its chunk-wise form: the same arguments, results
+ * and errors, computed 64 tokens at a time on the tensor cores instead of token by token, plus a
+ * workspace.  GLM-5.3-Flash kernel TDD ledger, slices I2, I2a and I4 (the chunk form matches the
+ * sequential state and output at 63, 64 and 65 tokens).  Per chunk of L tokens from the state S0,
+ * with gamma_t the running sum of the clamped log decays of each key channel:
+ *   A_ts = beta_t sum_c k^_t k^_s e^(gamma_t - gamma_s) (s < t),  T = (I + A)^-1,
+ *   E = (V - S0 (K^ o e^gamma)^T) diag(beta) T^T,
+ *   O = q_scale (S0 (Q^ o e^gamma)^T + E P^T),  P_ts = sum_c q^_t k^_s e^(gamma_t - gamma_s) (s <= t),
+ *   S = S0 diag(e^gamma_L) + E (K^ o e^(gamma_L - gamma))
+ * A first kernel forms every (chunk, V head)'s state-independent part in parallel; a second walks
+ * each (sequence, V head) through its chunks with the fp32 state in tensor memory.  Every product
+ * on the state's path takes bf16 high / low pairs of both operands; o's own products plain bf16.
+ * Tolerances: those of gdn_chunk_prefill.
+ *   g          [total_tokens, Hv, Dk] fp32 per-channel log decay (16-byte aligned); after the clamp
+ *              every value must be finite and at most 0 (a decay) -- a -INFINITY log decay (with
+ *              g_min = -INFINITY) makes that chunk's results NaN: clamp it, or use
+ *              gdn_kda_recurrence
+ *   workspace  256-byte aligned device memory of gdn_kda_chunk_prefill_workspace_size() bytes
+ *              (GDN_ERR_WORKSPACE if NULL or smaller), overwritten
+ *   num_seqs   at most 2^31 / Hv; cu_seqlens outside [0, total_tokens] or decreasing set
+ *              GDN_ERR_DEVICE_ARGUMENT in the device error word, those sequences are not computed
+ *   everything else as gdn_kda_recurrence.  Everything runs on `stream`.
+ */
+GDN_API gdn_status gdn_kda_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g,
+                                         float g_min, const float* beta, const int32_t* cu_seqlens,
+                                         int32_t num_seqs, int32_t total_tokens, float q_scale,
+                                         float l2_eps, const float* state_in, float* state_out,
+                                         const gdn_bf16* z, const gdn_bf16* norm_w, float rms_eps,
+                                         gdn_bf16* out, void* workspace, size_t workspace_bytes,
+                                         void* stream);
+
 /* Capacity of the fixed scratch used by gdn_chunk_prefill_noalloc. */
 #define GDN_NOALLOC_MAX_SEQS 16384
 #define GDN_NOALLOC_SCRATCH_BYTES (256 + 4 * GDN_NOALLOC_MAX_SEQS) /* 65,792 bytes */

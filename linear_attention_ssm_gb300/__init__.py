@@ -24,6 +24,8 @@ from .binding import (  # noqa: F401
     gdn_decode_step_fp16_state,
     gdn_gated_rmsnorm,
     gdn_gates,
+    gdn_kda_chunk_prefill,
+    gdn_kda_chunk_prefill_workspace_size,
     gdn_kda_decode_step,
     gdn_kda_prefill,
     gdn_kda_recurrence,

@@ -65,6 +65,8 @@ def _configure(lib, debug: bool):
         "gdn_decode_step_fused_gates": ([G, P, P, P, P, P, P, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
         "gdn_kda_decode_step": ([G, P, P, P, P, F, P, P, P, P, F, F, F, P, I, P], ctypes.c_int),
         "gdn_kda_recurrence": ([G, P, P, F, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
+        "gdn_kda_chunk_prefill_workspace_size": ([G, I, I], S),
+        "gdn_kda_chunk_prefill": ([G, P, P, F, P, P, I, I, F, F, P, P, P, P, F, P, P, S, P], ctypes.c_int),
         "gdn_verify_stash_size": ([G, I, I], S),
         "gdn_verify": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, I, P, S, P], ctypes.c_int),
         "gdn_verify_commit": ([G, P, P, S, P, P, I, I, P], ctypes.c_int),
@@ -372,6 +374,42 @@ def gdn_kda_recurrence(qkv, g, beta, cu_seqlens, q_scale, g_min=float("-inf"), l
     _check(lib.gdn_kda_recurrence(_geo(geometry), _p(qkv), _p(g), float(g_min), _p(beta), _p(cu_seqlens), N, T,
                                   float(q_scale), float(l2_eps), _p(state_in), _p(state_out), _p(z), _p(norm_w),
                                   float(rms_eps), _p(out), _stream(stream)))
+    return out
+
+
+def gdn_kda_chunk_prefill_workspace_size(num_seqs: int, total_tokens: int,
+                                         geometry: Geometry = QWEN_GDN) -> int:
+    return int(_L().gdn_kda_chunk_prefill_workspace_size(_geo(geometry), num_seqs, total_tokens))
+
+
+def gdn_kda_chunk_prefill(qkv, g, beta, cu_seqlens, q_scale, g_min=float("-inf"), l2_eps=1e-6, state_in=None,
+                          state_out=None, z=None, norm_w=None, rms_eps=1e-6, out=None, workspace=None,
+                          geometry: Geometry = QWEN_GDN, stream=None):
+    """gdn_kda_recurrence in its chunk-wise form (64-token chunks on the tensor cores): same
+    arguments and result, plus a workspace of gdn_kda_chunk_prefill_workspace_size() bytes
+    (allocated here when None).  After the clamp g must be finite."""
+    lib = _L()
+    C, hv, dv, dk = geometry.conv_dim, geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim
+    N = cu_seqlens.numel() - 1
+    T = qkv.shape[0]
+    _dev(qkv, torch.bfloat16, "qkv", (T, C))
+    _dev(g, torch.float32, "g", (T, hv, dk))
+    _dev(beta, torch.float32, "beta", (T, hv))
+    _dev(cu_seqlens, torch.int32, "cu_seqlens", (N + 1,))
+    _dev(state_in, torch.float32, "state_in", (N, hv, dv, dk))
+    _dev(state_out, torch.float32, "state_out", (N, hv, dv, dk))
+    _dev(z, torch.bfloat16, "z", (T, hv, dv))
+    _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
+    if out is None:
+        out = torch.empty((T, hv, dv), dtype=torch.bfloat16, device=qkv.device)
+    _dev(out, torch.bfloat16, "out", (T, hv, dv))
+    need = lib.gdn_kda_chunk_prefill_workspace_size(_geo(geometry), N, T)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=qkv.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.gdn_kda_chunk_prefill(_geo(geometry), _p(qkv), _p(g), float(g_min), _p(beta), _p(cu_seqlens), N, T,
+                                     float(q_scale), float(l2_eps), _p(state_in), _p(state_out), _p(z), _p(norm_w),
+                                     float(rms_eps), _p(out), _p(workspace), wbytes, _stream(stream)))
     return out
 
 

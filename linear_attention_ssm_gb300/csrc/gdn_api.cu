@@ -446,6 +446,59 @@ gdn_status gdn_kda_recurrence(const gdn_geometry* geo, const gdn_bf16* qkv, cons
                   "KDA recurrence launch");
 }
 
+size_t gdn_kda_chunk_prefill_workspace_size(const gdn_geometry* geo, int32_t num_seqs, int32_t total_tokens) {
+  if (!geo || num_seqs <= 0 || total_tokens < 0 || geo->num_v_heads <= 0) return 0;
+  return gdn::kda_chunk_workspace_bytes(num_seqs, total_tokens, geo->num_v_heads);
+}
+
+gdn_status gdn_kda_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g, float g_min,
+                                 const float* beta, const int32_t* cu_seqlens, int32_t num_seqs,
+                                 int32_t total_tokens, float q_scale, float l2_eps, const float* state_in,
+                                 float* state_out, const gdn_bf16* z, const gdn_bf16* norm_w, float rms_eps,
+                                 gdn_bf16* out, void* workspace, size_t workspace_bytes, void* stream) {
+  gdn_status s = check_geometry(geo);
+  if (s != GDN_OK) return s;
+  if (num_seqs < 0 || total_tokens < 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "negative size (num_seqs=%d, total_tokens=%d)", num_seqs, total_tokens);
+  if (num_seqs == 0 && total_tokens > 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "total_tokens=%d with no sequence", total_tokens);
+  if ((long)num_seqs * geo->num_v_heads > 0x7FFFFFFFL)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "num_seqs * num_v_heads exceeds the grid limit");
+  if (num_seqs == 0) return ok();
+  if (!cu_seqlens) return fail(GDN_ERR_INVALID_ARGUMENT, "cu_seqlens is NULL");
+  if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) return fail(GDN_ERR_MISALIGNED, "cu_seqlens is not 4-byte aligned");
+  if (total_tokens > 0) {
+    GDN_REQUIRE(qkv, "qkv");
+    GDN_REQUIRE(g, "g");
+    GDN_REQUIRE(out, "out");
+    if (!beta) return fail(GDN_ERR_INVALID_ARGUMENT, "beta is NULL");
+    if (reinterpret_cast<uintptr_t>(beta) & 3u) return fail(GDN_ERR_MISALIGNED, "beta is not 4-byte aligned");
+  }
+  GDN_OPTIONAL(state_in, "state_in");
+  GDN_OPTIONAL(state_out, "state_out");
+  if (z) {
+    GDN_REQUIRE(z, "z");
+    GDN_REQUIRE(norm_w, "norm_w");
+  }
+  if (g_min != g_min) return fail(GDN_ERR_INVALID_ARGUMENT, "g_min is NaN");
+  if (!(l2_eps >= 0.f) || !(rms_eps >= 0.f)) return fail(GDN_ERR_INVALID_ARGUMENT, "eps must be >= 0");
+  const size_t need = gdn_kda_chunk_prefill_workspace_size(geo, num_seqs, total_tokens);
+  if (!workspace || workspace_bytes < need)
+    return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(GDN_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+  if (state_in && state_out && state_in != state_out) {
+    const size_t sb = (size_t)num_seqs * geo->num_v_heads * gdn::kHeadDim * gdn::kHeadDim * 4;
+    if (overlaps(state_in, sb, state_out, sb))
+      return fail(GDN_ERR_INVALID_ARGUMENT, "state_out partially overlaps state_in");
+  }
+  gdn::LaunchEnv env;
+  if ((s = make_env(stream, &env)) != GDN_OK) return s;
+  return launched(gdn::launch_kda_chunk_prefill(env, qkv, g, g_min, beta, cu_seqlens, num_seqs, total_tokens,
+                                                geo->num_k_heads, geo->num_v_heads, q_scale, l2_eps, state_in,
+                                                state_out, z, norm_w, rms_eps, out, workspace),
+                  "KDA chunk prefill launch");
+}
+
 gdn_status gdn_decode_step_fp16_state(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w,
                                       gdn_bf16* conv_state, const float* g, const float* beta, gdn_f16* state,
                                       const gdn_bf16* z, const gdn_bf16* norm_w, float q_scale, float l2_eps,

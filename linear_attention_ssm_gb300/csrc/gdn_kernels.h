@@ -38,6 +38,14 @@ cudaError_t launch_kda_prefill(const LaunchEnv& env, const uint16_t* qkv, const 
                                const float* beta, const int32_t* cu, int N, int T, int Hk, int Hv, float q_scale,
                                float l2_eps, const float* state_in, float* state_out, const uint16_t* z,
                                const uint16_t* norm_w, float rms_eps, uint16_t* out);
+// The KDA recurrence in its chunk-wise form (kda_chunk.cu): same arguments and results as
+// launch_kda_prefill (g finite after the clamp), plus a workspace of kda_chunk_workspace_bytes().
+size_t kda_chunk_workspace_bytes(int N, int T, int Hv);
+cudaError_t launch_kda_chunk_prefill(const LaunchEnv& env, const uint16_t* qkv, const float* g, float g_min,
+                                     const float* beta, const int32_t* cu, int N, int T, int Hk, int Hv,
+                                     float q_scale, float l2_eps, const float* state_in, float* state_out,
+                                     const uint16_t* z, const uint16_t* norm_w, float rms_eps, uint16_t* out,
+                                     void* workspace);
 
 // Multi-token verify (verify.cu): K rows per sequence, the state read only; the commit folds an
 // accepted prefix of rows into the recurrent and conv states.

@@ -67,11 +67,20 @@ int main(void) {
                             1e-6f, NULL, NULL),
          GDN_OK);
 
+  EXPECT(gdn_kda_chunk_prefill(&kda, NULL, NULL, -INFINITY, NULL, NULL, 0, 0, 0.088f, 1e-6f, NULL, NULL, NULL,
+                               NULL, 1e-6f, NULL, NULL, 0, NULL),
+         GDN_OK);
+  EXPECT(gdn_kda_chunk_prefill(&kda, fake, fake, -1.0f, fake, fake, 2, 8, 0.088f, 1e-6f, NULL, NULL, NULL, NULL,
+                               1e-6f, fake, NULL, 0, NULL),
+         GDN_ERR_WORKSPACE);
+
   /* sizes computed on the host */
   if (gdn_verify_stash_size(&geo, 256, 8) != (size_t)256 * 8 * 53440) return 1;
   if (gdn_verify_stash_size(&geo, 1, 18) != 0) return 1;
   if (gdn_chunk_prefill_workspace_size(&geo, 4, 16384) == 0) return 1;
   if (gdn_chunk_prefill_min_workspace_size(&geo, 4, 16384) == 0) return 1;
+  if (gdn_kda_chunk_prefill_workspace_size(&kda, 4, 16384) != (size_t)256 + 256 + 256 + (size_t)259 * 64 * 108032)
+    return 1;
 
   printf("ok\n");
   return 0;

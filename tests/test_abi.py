@@ -286,6 +286,50 @@ def test_kda_recurrence_rejects_bad_arguments(lib):
     assert call(N=0, T=0, qkv=None, g=None, beta=None, cu=None, out=None) == 0
 
 
+def test_kda_chunk_prefill_rejects_bad_arguments(lib):
+    geo = _geo(num_k_heads=64, num_v_heads=64)
+    need = lib.gdn_kda_chunk_prefill_workspace_size(geo, 2, 8)
+
+    def call(qkv=FAKE, g=FAKE, g_min=-1.0, beta=FAKE, cu=FAKE, N=2, T=8, state_in=None, state_out=None, z=None,
+             norm_w=None, out=FAKE, l2=1e-6, ws=ctypes.c_void_p(0x100000), wsb=need):
+        return lib.gdn_kda_chunk_prefill(geo, qkv, g, g_min, beta, cu, N, T, 0.088, l2, state_in, state_out, z,
+                                         norm_w, 1e-6, out, ws, wsb, None)
+
+    assert call(N=-1) == 1
+    assert call(N=0, T=4) == 1
+    assert call(cu=None) == 1
+    assert call(g=None) == 1
+    assert call(beta=None) == 1
+    assert call(g_min=float("nan")) == 1
+    assert call(l2=-1.0) == 1
+    assert call(z=FAKE, norm_w=None) == 1
+    assert call(g=ODD) == 3
+    assert call(qkv=ODD) == 3
+    assert call(state_in=ODD) == 3
+    assert call(state_in=FAKE, state_out=ctypes.c_void_p(0x10000 + 4096)) == 1   # partial overlap
+    assert call(ws=None) == 7                                                     # missing workspace
+    assert call(wsb=need - 1) == 7                                                # too small
+    assert call(ws=ctypes.c_void_p(0x100010)) == 3                                # not 256-byte aligned
+    assert lib.gdn_kda_chunk_prefill(_geo(head_k_dim=64), FAKE, FAKE, -1.0, FAKE, FAKE, 1, 4, 0.088, 1e-6, None,
+                                     None, None, None, 1e-6, FAKE, FAKE, need, None) == 2
+    assert call(N=0, T=0, qkv=None, g=None, beta=None, cu=None, out=None, ws=None, wsb=0) == 0
+
+
+def test_kda_chunk_workspace_size():
+    """Counters, order and chunk offsets, then one 108,032-byte record per (chunk, V head): K~ hi
+    and Q~ (64 + 64 token rows x 128 bf16), K~ lo (64 x 128), Kd hi / lo (2 x 64 x 128), T hi / lo
+    and P (3 x 64 x 64 bf16), and 384 floats of per-token and per-channel factors."""
+    lib = binding.load_library()
+    rec = 128 * 128 * 2 + 64 * 128 * 2 + 2 * 64 * 128 * 2 + 3 * 64 * 64 * 2 + 384 * 4
+    assert rec == 108032
+    pad = lambda b: -(-b // 256) * 256
+    for n, t in ((1, 16), (4, 4 * 4096), (8, 32735), (3, 0)):
+        chunks = (t + 63 * n) // 64
+        want = 256 + pad(4 * n) + pad(4 * (n + 1)) + chunks * 64 * rec
+        assert lib.gdn_kda_chunk_prefill_workspace_size(_geo(num_k_heads=64, num_v_heads=64), n, t) == want
+    assert lib.gdn_kda_chunk_prefill_workspace_size(_geo(num_k_heads=64, num_v_heads=64), 0, 0) == 0
+
+
 def test_header_is_a_plain_c_abi(lib, tmp_path):
     """A C11 program built against include/*.h alone (gcc -Wall -Wextra -Werror) links against
     libgdn.so and gets the documented status from every entry point it calls."""

@@ -109,10 +109,12 @@ def run_profile_kda_prefill(args, local):
     st = torch.empty_like(st0)
     qkv = torch.empty_like(x)
     out = torch.empty((T, geo.num_v_heads, 128), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(gdn.gdn_kda_chunk_prefill_workspace_size(len(lengths), T, geometry=geo), dtype=torch.uint8,
+                     device=dev)
 
     def step():
         gdn.gdn_kda_prefill(x, w, cu, g, beta, z, nw, geo.q_scale, state_in=st0, state_out=st, qkv_buf=qkv, out=out,
-                            geometry=geo)
+                            workspace=ws, geometry=geo)
 
     for _ in range(args.warmup):
         step()
@@ -428,36 +430,21 @@ def time_kda_decode(args, gdn, dev, stream, barrier, max_over_ranks, world, hbm_
 
 
 def kda_prefill_bytes(tokens, seqs, hv):
-    """Algorithmic bytes of one KDA recurrence launch: per (token, V head) q, k, v, z (bf16 rows of
-    128), g (fp32 row of 128) and beta in, the bf16 output row out; per (sequence, V head) the fp32
-    state in and out."""
+    """Algorithmic bytes of one KDA recurrence call (in either form): per (token, V head) q, k, v, z
+    (bf16 rows of 128), g (fp32 row of 128) and beta in, the bf16 output row out; per (sequence,
+    V head) the fp32 state in and out."""
     return tokens * hv * (4 * 256 + 512 + 4 + 256) + 2 * seqs * hv * 128 * 128 * 4
-
-
-def scaled_kda_traffic(algorithmic_bytes):
-    """The recorded DRAM traffic of the KDA recurrence, scaled from its captured workload to a
-    launch with these algorithmic bytes (None without a record for the current code)."""
-    rec = traffic_record("kda_prefill")
-    if not rec:
-        return None
-    return int(rec["bytes_per_launch"] * algorithmic_bytes / rec["algorithmic_bytes_per_launch"])
-
-
-# Flops of one token of one head in the KDA recurrence's sequential form, per state element: the
-# decayed-key dot (2), the update a s + e k (3) and the query dot (2).
-KDA_FLOPS_PER_ELEMENT = 7
-SM_MAX_HZ = 2.07e9  # maximum SM clock of the part
-FP32_LANES_PER_SM = 128
 
 
 def time_kda_prefill(args, gdn, dev, stream, barrier, max_over_ranks, world):
     """KDA prefill on the pages' 64-head geometry, 4 sequences x 4096 tokens: conv1d, then the KDA
-    recurrence with the gated RMSNorm fused (both kernels timed with events, and the recurrence
-    alone for its roofline).  x alone is 805 MB per step, larger than L2."""
+    recurrence in its chunk-wise form with the gated RMSNorm fused (both timed with events, and
+    the chunk call alone for its roofline); the sequential recurrence kernel is timed beside it.
+    x alone is 805 MB per step, larger than L2."""
     import torch
     from linear_attention_ssm_gb300.synth import KDA_GEO, kda_prefill_inputs
     geo, lengths = KDA_GEO, [4096] * 4
-    T = sum(lengths)
+    T, N = sum(lengths), len(lengths)
     d = kda_prefill_inputs(lengths, seed=11, geo=geo)
     x, cu, g, beta, z = (d[k].to(dev) for k in ("x", "cu_seqlens", "g", "beta", "z"))
     w, nw, st0 = d["conv_w"].to(dev), d["norm_w"].to(dev), d["state0"].to(dev)
@@ -465,19 +452,24 @@ def time_kda_prefill(args, gdn, dev, stream, barrier, max_over_ranks, world):
     st = torch.empty_like(st0)
     qkv = torch.empty((T, geo.conv_dim), dtype=torch.bfloat16, device=dev)
     out = torch.empty((T, geo.num_v_heads, 128), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(gdn.gdn_kda_chunk_prefill_workspace_size(N, T, geometry=geo), dtype=torch.uint8, device=dev)
     qs = geo.q_scale
 
     def whole():
         gdn.gdn_kda_prefill(x, w, cu, g, beta, z, nw, qs, state_in=st0, state_out=st, qkv_buf=qkv, out=out,
-                            geometry=geo)
+                            workspace=ws, geometry=geo)
 
-    def recurrence():
+    def chunk():
+        gdn.gdn_kda_chunk_prefill(qkv, g, beta, cu, qs, state_in=st0, state_out=st, z=z, norm_w=nw, out=out,
+                                  workspace=ws, geometry=geo)
+
+    def sequential():
         gdn.gdn_kda_recurrence(qkv, g, beta, cu, qs, state_in=st0, state_out=st, z=z, norm_w=nw, out=out,
                                geometry=geo)
 
     n = 5
     timed = {}
-    for name, fn in (("whole", whole), ("recurrence", recurrence)):
+    for name, fn in (("whole", whole), ("chunk", chunk), ("sequential", sequential)):
         for _ in range(max(args.warmup, 1)):
             fn()
         barrier()
@@ -489,23 +481,22 @@ def time_kda_prefill(args, gdn, dev, stream, barrier, max_over_ranks, world):
         torch.cuda.synchronize()
         gdn.gdn_check_device_errors()
         timed[name] = max_over_ranks(s0.elapsed_time(e0)) / n
-    del x, cu, g, beta, z, st0, st, qkv, out
+    del x, cu, g, beta, z, st0, st, qkv, out, ws
     torch.cuda.empty_cache()
-    flops = T * geo.num_v_heads * KDA_FLOPS_PER_ELEMENT * 128 * 128
-    achieved = flops / (timed["recurrence"] / 1e3) / 1e12
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    peak = sms * FP32_LANES_PER_SM * 2 * SM_MAX_HZ / 1e12
-    nbytes = kda_prefill_bytes(T, len(lengths), geo.num_v_heads)
+    hbm_peak, _, peak_kind = peaks()
+    nbytes = kda_prefill_bytes(T, N, geo.num_v_heads)
+    gbs = nbytes / (timed["chunk"] / 1e3) / 1e9
+    rec = traffic_record("kda_chunk_prefill")
     return {"metric": "KDA prefill tokens/s", "value": world * T / (timed["whole"] / 1e3), "unit": "tokens/s",
             "ms_per_step": timed["whole"], "steps": n,
             "workload": "KDA prefill, 4 sequences x 4096 tokens, 64 heads x 128 (q, k, v), per-channel decay, "
-                        "conv1d -> sequential KDA recurrence -> sigmoid-gated RMSNorm",
-            "roofline": {"kernel": "kda_prefill_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": scaled_kda_traffic(nbytes),
-                         "algorithmic_bytes_per_launch": nbytes,
-                         "traffic_note": "ncu DRAM bytes of a 4 x 1024-token capture scaled by algorithmic bytes",
-                         "algorithmic_flops_per_launch": flops, "avg_launch_ms": timed["recurrence"],
-                         "peak_source": "fp32 CUDA cores: SMs x 128 lanes x 2 flops x 2070 MHz (nominal)"}}
+                        "conv1d -> chunk-wise KDA recurrence (prep + state kernels) -> sigmoid-gated RMSNorm",
+            "sequential_recurrence_ms": timed["sequential"],
+            "roofline": {"kernel": "kda_chunk_prefill (schedule + prep + state kernels, tcgen05, fused gated norm)",
+                         "bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                         "peak_kind": peak_kind + " (copy bandwidth)",
+                         "traffic": rec["bytes_per_launch"] if rec else None,
+                         "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": timed["chunk"]}}
 
 
 VERIFY_ROWS = 8

@@ -670,10 +670,15 @@ def gdn_prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, q_scale, l2_eps=1e-6,
 
 def gdn_kda_prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, q_scale, g_min=float("-inf"), l2_eps=1e-6,
                     rms_eps=1e-6, state_in=None, state_out=None, conv_state_in=None, conv_state_out=None,
-                    qkv_buf=None, out=None, geometry: Geometry = QWEN_GDN, stream=None):
-    """The KDA prefill: gdn_conv1d_prefill, then gdn_kda_recurrence with the gated RMSNorm fused.
-    Returns out [T, Hv, Dv] bf16."""
+                    qkv_buf=None, out=None, workspace=None, chunked=True, geometry: Geometry = QWEN_GDN,
+                    stream=None):
+    """The KDA prefill: gdn_conv1d_prefill, then the KDA recurrence with the gated RMSNorm fused --
+    in its chunk-wise form (gdn_kda_chunk_prefill, with `workspace` or one allocated here), or,
+    with chunked=False, token by token (gdn_kda_recurrence).  Returns out [T, Hv, Dv] bf16."""
     qkv = gdn_conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in, conv_state_out, qkv_buf,
                              geometry=geometry, stream=stream)
+    if chunked:
+        return gdn_kda_chunk_prefill(qkv, g, beta, cu_seqlens, q_scale, g_min, l2_eps, state_in, state_out, z,
+                                     norm_w, rms_eps, out, workspace, geometry=geometry, stream=stream)
     return gdn_kda_recurrence(qkv, g, beta, cu_seqlens, q_scale, g_min, l2_eps, state_in, state_out, z,
                               norm_w, rms_eps, out, geometry=geometry, stream=stream)

@@ -1,8 +1,8 @@
-"""GPU parity of the KDA prefill (conv1d, then the KDA recurrence kernel with the gated RMSNorm
-fused) against the oracle: ragged lengths around the 16-token staging blocks and the 63/64/65
-chunk boundary, an empty sequence, the decay clamp, o without the norm, in-place states,
-one-token sequences against the KDA decode kernel, bad cu_seqlens on the device, and the 64-head
-4 x 4096 workload on sampled heads."""
+"""GPU parity of the KDA prefill (conv1d, then the KDA recurrence with the gated RMSNorm fused, in
+its sequential and its chunk-wise form) against the oracle: ragged lengths around the 16-token
+staging blocks and the 63/64/65 chunk boundary, an empty sequence, the decay clamp, o without the
+norm, in-place states, one-token sequences against the KDA decode kernel, bad cu_seqlens on the
+device, and the 64-head 4 x 4096 workload on sampled heads."""
 import pytest
 import torch
 
@@ -21,8 +21,9 @@ def _a(geo):
                 head_v_dim=geo.head_v_dim)
 
 
+@pytest.mark.parametrize("chunked", [False, True], ids=["sequential", "chunked"])
 @pytest.mark.parametrize("g_min", [float("-inf"), -1.0], ids=["no_clamp", "clamp"])
-def test_kda_prefill_matches_oracle(g_min):
+def test_kda_prefill_matches_oracle(g_min, chunked):
     g = lib()
     geo = GEO2
     inp = kda_prefill_inputs(LENGTHS, seed=300, geo=geo, random_conv_state=True)
@@ -33,7 +34,7 @@ def test_kda_prefill_matches_oracle(g_min):
     g.gdn_kda_prefill(inp["x"].to(DEV), inp["conv_w"].to(DEV), inp["cu_seqlens"].to(DEV), inp["g"].to(DEV),
                       inp["beta"].to(DEV), inp["z"].to(DEV), inp["norm_w"].to(DEV), inp["q_scale"], g_min,
                       state_in=inp["state0"].to(DEV), state_out=st.t, conv_state_in=inp["conv_state0"].to(DEV),
-                      conv_state_out=cs, out=out.t, geometry=geo)
+                      conv_state_out=cs, out=out.t, chunked=chunked, geometry=geo)
     g.gdn_check_device_errors()
     out.check("out")
     st.check("state_out")
@@ -101,7 +102,7 @@ def test_one_token_sequences_match_the_kda_decode_kernel():
     out_pre = g.gdn_kda_prefill(d["x"][0].to(DEV), d["conv_w"].to(DEV), cu_seqlens_of([1] * B).to(DEV),
                                 d["g"][0].to(DEV), d["beta"][0].to(DEV), d["z"][0].to(DEV), d["norm_w"].to(DEV),
                                 d["q_scale"], -2.0, state_in=st_pre, state_out=st_pre,
-                                conv_state_in=d["conv_state0"].to(DEV), conv_state_out=cs_pre, **args)
+                                conv_state_in=d["conv_state0"].to(DEV), conv_state_out=cs_pre, chunked=False, **args)
     g.gdn_check_device_errors()
     assert torch.equal(cs_pre, cs_dec)
     assert_out_close(out_pre, out_dec.double())
@@ -138,8 +139,9 @@ def _one_head(inp, geo, h):
                 z=inp["z"][:, h:h + 1].contiguous(), state_in=inp["state0"][:, h:h + 1].contiguous())
 
 
-def test_kda_prefill_full_size_sampled_heads():
-    """The 64-head workload, 4 sequences x 4096 tokens, in the launch configuration the benchmark
+@pytest.mark.parametrize("chunked", [False, True], ids=["sequential", "chunked"])
+def test_kda_prefill_full_size_sampled_heads(chunked):
+    """The 64-head workload, 4 sequences x 4096 tokens, in the launch configurations the benchmark
     times; the oracle computes three of the 64 V heads, each from its own channels."""
     g = lib()
     geo = KDA_GEO
@@ -149,7 +151,7 @@ def test_kda_prefill_full_size_sampled_heads():
     st = torch.empty((4, geo.num_v_heads, 128, 128), dtype=torch.float32, device=DEV)
     out = g.gdn_kda_prefill(inp["x"].to(DEV), inp["conv_w"].to(DEV), inp["cu_seqlens"].to(DEV), inp["g"].to(DEV),
                             inp["beta"].to(DEV), inp["z"].to(DEV), inp["norm_w"].to(DEV), inp["q_scale"],
-                            state_in=inp["state0"].to(DEV), state_out=st, geometry=geo)
+                            state_in=inp["state0"].to(DEV), state_out=st, chunked=chunked, geometry=geo)
     g.gdn_check_device_errors()
     assert out.shape == (T, geo.num_v_heads, 128)
     for h in (0, 37, 63):

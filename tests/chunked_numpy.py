@@ -187,3 +187,41 @@ def chunked_chain_kda_tc(q, k, v, g, beta, S0, q_scale, split=TC_SPLIT_ALL, chun
         S = f32(S * np.exp(gam[-1])[None, :]
                 + tc_product(E.T, K * np.exp(gam[-1][None, :] - gam), split["E"], split["Kd"]))
     return O, S
+
+
+def kda_gram_middle_reference(X, K, gam, ref=31):
+    """M[t, j] = sum_i X_ti K_ji exp(Gamma_ti - Gamma_ji) (j <= t, else 0) as one bf16 hi / lo tensor-core
+    product around the chunk's middle token: (X * exp(Gamma - Gamma_ref)) (K * exp(Gamma_ref - Gamma))^T.
+    Valid while every |Gamma_t - Gamma_ref| stays far inside the fp32 range; entries above the
+    diagonal are dropped by position (their factors may overflow)."""
+    f32 = lambda x: np.asarray(x, dtype=np.float32).astype(np.float64)
+    L = X.shape[0]
+    r = min(ref, L - 1)
+    e_row = f32(np.exp(f32(gam - gam[r])))
+    e_col = f32(np.exp(f32(gam[r] - gam)))
+    with np.errstate(over="ignore", invalid="ignore"):
+        M = tc_product(f32(X * e_row), f32(K * e_col).T, True, True)
+    return np.where(np.tril(np.ones((L, L), dtype=bool)), M, 0.0)
+
+
+def chunked_chain_kda_tc_middle(q, k, v, g, beta, S0, q_scale, chunk=64):
+    """chunked_chain_kda_tc (every state-path operand split, the output-only products plain) with A
+    and P from kda_gram_middle_reference instead of the sub-block form."""
+    f32 = lambda x: np.asarray(x, dtype=np.float32).astype(np.float64)
+    T = q.shape[0]
+    S = f32(S0)
+    O = np.zeros((T, v.shape[1]))
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(T, c0 + chunk))
+        Q, K, V, G, B = q[sl], k[sl], v[sl], g[sl], beta[sl]
+        L = Q.shape[0]
+        gam = f32(np.cumsum(G.astype(np.float32), axis=0))
+        A = B[:, None] * kda_gram_middle_reference(K, K, gam) * np.tril(np.ones((L, L)), -1)
+        P = kda_gram_middle_reference(Q, K, gam)
+        Tm = f32(solve_triangular(np.eye(L) + A, np.eye(L), lower=True, unit_diagonal=True))
+        X = tc_product(K * np.exp(gam), S.T, True, True)
+        R = f32(B[:, None] * (V - X))
+        E = tc_product(Tm, R, True, True)
+        O[sl] = q_scale * (tc_product(Q * np.exp(gam), S.T, False, False) + tc_product(P, E, False, False))
+        S = f32(S * np.exp(gam[-1])[None, :] + tc_product(E.T, K * np.exp(gam[-1][None, :] - gam), True, True))
+    return O, S

@@ -13,7 +13,8 @@ import pytest
 
 import oracle
 from linear_attention_ssm_gb300.synth import Geometry, kda_prefill_inputs
-from tests.chunked_numpy import (TC_SPLIT_ALL, chunked_chain_kda_fp32, chunked_chain_kda_tc, kda_intra_chunk_weights,
+from tests.chunked_numpy import (TC_SPLIT_ALL, chunked_chain_kda_fp32, chunked_chain_kda_tc, chunked_chain_kda_tc_middle,
+                                 kda_gram_middle_reference, kda_intra_chunk_weights,
                                  l2n)
 
 GEO = Geometry(num_k_heads=1, num_v_heads=1, head_k_dim=128, head_v_dim=128, conv_width=4)
@@ -119,3 +120,30 @@ def test_each_state_path_operand_needs_its_split(operand):
     plan[operand] = False
     _, state_rel = _errors(args, o, st, plan)
     assert state_rel > 1e-4, (operand, state_rel)
+
+
+def test_tensor_core_gram_around_the_middle_token():
+    """A and P of a chunk as one bf16 hi / lo tensor-core product around token 31 (the KDA prep
+    kernel's way when the chunk's decay span allows it): against the 16-token sub-block form the
+    lower triangle agrees to the split's precision, and the whole chain keeps the state within
+    1e-5 relative L2 of the fp64 oracle over 512 tokens of long memory and under the workload's
+    decay, the output within half its bound."""
+    args, o, st = _weak(512, 420)
+    q, k, gam = args[0][:64], args[1][:64], np.cumsum(args[3][:64].astype(np.float32), axis=0).astype(np.float32)
+    exact = kda_intra_chunk_weights(k, k, gam).astype(np.float64)
+    got = kda_gram_middle_reference(k, k, gam)
+    low = np.tril(np.ones((64, 64), dtype=bool))
+    assert np.abs(got - exact)[low].max() <= 1e-4 * np.abs(exact[low]).max()
+    O, S = chunked_chain_kda_tc_middle(*args)
+    assert np.abs(O - o).max() <= 0.5 * 2e-2 * np.abs(o).max()
+    assert _rel(S, st) <= 1e-5
+    inp = kda_prefill_inputs([256], seed=421, geo=GEO)   # the workload's decay, -U(0.001, 2)
+    y, _, _ = oracle.conv1d_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"])
+    o2, st2 = oracle.kda_recurrence(y, inp["g"], inp["beta"], [0, 256], 1, 1, 128, 128, GEO.q_scale,
+                                    state_in=inp["state0"])
+    a = y.double().numpy()
+    O2, S2 = chunked_chain_kda_tc_middle(l2n(a[:, :128], 1e-6), l2n(a[:, 128:256], 1e-6), a[:, 256:],
+                                         inp["g"][:, 0].double().numpy(), inp["beta"][:, 0].double().numpy(),
+                                         inp["state0"][0, 0].double().numpy(), GEO.q_scale)
+    assert np.abs(O2 - o2[:, 0].numpy()).max() <= 0.5 * 2e-2 * np.abs(o2[:, 0].numpy()).max()
+    assert _rel(S2, st2[0, 0].numpy()) <= 1e-5

@@ -59,15 +59,22 @@ def test_traffic_records_survive_comment_edits_only():
 
 
 
-def test_kda_prefill_traffic_scales_with_algorithmic_bytes():
-    """The recorded KDA recurrence traffic is reported at its own workload unchanged and scales
-    linearly with the algorithmic bytes (None once the kernel's code differs from the capture's)."""
-    rec = bench.traffic_record("kda_prefill")
+def test_kda_chunk_traffic_record_matches_its_kernels():
+    """The recorded DRAM traffic of the chunk-wise KDA call is the sum of its prep and state
+    kernels, captured on the benchmark's workload (None once the kernel file's code differs)."""
+    rec = bench.traffic_record("kda_chunk_prefill")
     if rec is None:
         pytest.skip("no traffic record for the current kernel code")
-    assert bench.kda_prefill_bytes(4096, 4, 64) == rec["algorithmic_bytes_per_launch"]
-    assert bench.scaled_kda_traffic(rec["algorithmic_bytes_per_launch"]) == rec["bytes_per_launch"]
-    assert bench.scaled_kda_traffic(2 * rec["algorithmic_bytes_per_launch"]) == 2 * rec["bytes_per_launch"]
+    kern = rec["kernels"]
+    assert set(kern) == {"kda_prep_kernel", "kda_state_kernel"}
+    assert rec["bytes_per_launch"] == rec["read"] + rec["write"]
+    assert abs(rec["read"] - sum(k["read"] for k in kern.values())) <= 2
+    assert abs(rec["write"] - sum(k["write"] for k in kern.values())) <= 2
+    # the records (one of 108,032 bytes per chunk and V head) dominate the traffic beyond the
+    # algorithmic bytes: written by the prep kernel, read by the state kernel
+    records = (4 * 4096 // 64) * 64 * 108032
+    assert kern["kda_prep_kernel"]["write"] >= 0.95 * records
+    assert rec["bytes_per_launch"] >= bench.kda_prefill_bytes(4096 * 4, 4, 64) + 2 * records * 0.95
 
 
 def test_clock_samples_are_summarised_with_every_active_reason():

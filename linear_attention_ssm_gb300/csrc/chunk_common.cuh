@@ -162,7 +162,15 @@ constexpr uint32_t kHeadBuf = 2 * kTriBytes + kYBytes;       // A, T and scratch
 //   3. the lower-left 32 x 32 block: T_21 = -T_22 (A_21 T_11).
 // The products of steps 2 and 3 are spread over every thread (one thread: four consecutive
 // columns of one row, as f32x2 pairs), each through a scratch product and a CTA barrier: five
-// barriers in all, against the block-column walk by one warp per column it replaces.
+// barriers in all, against the block-column walk by one warp per column it replaces.  With kSub,
+// only threads 0..63 run it (G = 1) and its barriers are a named barrier of those two warps, so
+// the other warps of the CTA can work meanwhile.
+template <bool kSub = false>
+__device__ __forceinline__ void solve_sync() {
+  if constexpr (kSub) asm volatile("bar.sync 1, 64;" ::: "memory");
+  else __syncthreads();
+}
+template <bool kSub = false>
 __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
   // Block (bi, bj) of a tri-layout matrix; inside it, element (r, c) sits at r * 16 +
   // ((((c >> 2) ^ (r & 3)) << 2) | (c & 3)).
@@ -195,7 +203,7 @@ __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) Tb[i * 16 + (((cq ^ (i & 3)) << 2) | ce)] = x[i];  // zeros above the diagonal too
   }
-  __syncthreads();
+  solve_sync<kSub>();
   // Register-blocked products: a thread holds a 4 x 4 output tile -- rows rb, rb + S, rb + 2S,
   // rb + 3S (so that the lanes of a warp, consecutive in rb, read rows whose 16-byte groups sit
   // in different banks) and four consecutive columns -- and takes four k at a time: four float4
@@ -237,7 +245,7 @@ __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
       *reinterpret_cast<float4*>(sY + (rb + 4 * i) * 16 + cq * 4) =
           make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
   }
-  __syncthreads();
+  solve_sync<kSub>();
   // step 2b: T_{b+1,b} = -T_{b+1,b+1} Y_h
   for (int it = tid; it < G * 32; it += kThreads) {
     const int g = it >> 5, b = ((it >> 4) & 1) * 2, cq = (it >> 2) & 3, rb = it & 3;
@@ -265,7 +273,7 @@ __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
           make_float4(-acc[i][0].x, -acc[i][0].y, -acc[i][1].x, -acc[i][1].y);
     }
   }
-  __syncthreads();
+  solve_sync<kSub>();
   // step 3a: Y = A_21 T_11 (rows 32..63 of A, columns 0..31), rows rb + 8i; T_11 is zero above its
   // diagonal blocks, so column block cb takes key blocks cb..1.  Item (g, c4, rb).
   for (int it = tid; it < G * 64; it += kThreads) {
@@ -294,7 +302,7 @@ __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
       *reinterpret_cast<float4*>(sY + (rb + 8 * i) * 32 + c4 * 4) =
           make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
   }
-  __syncthreads();
+  solve_sync<kSub>();
   // step 3b: T_21 = -T_22 Y; T_22 is zero above its diagonal blocks: rows 0..15 of it take Y's
   // first 16 rows, rows 16..31 all 32
   for (int it = tid; it < G * 64; it += kThreads) {
@@ -327,7 +335,7 @@ __device__ void solve_tri_batched(uint8_t* base, int G, int tid) {
           make_float4(-acc[i][0].x, -acc[i][0].y, -acc[i][1].x, -acc[i][1].y);
     }
   }
-  __syncthreads();
+  solve_sync<kSub>();
 }
 
 }  // namespace

@@ -58,7 +58,8 @@ constexpr uint32_t KP_AH = KP_U;          //   tensor cores: [K'; Q'] hi, two 64
 constexpr uint32_t KP_AL = KP_U + 32768;  //   [K'; Q'] lo
 constexpr uint32_t KP_BH = KP_U + 65536;  //   K'' hi, two 64-channel blocks of 64 rows
 constexpr uint32_t KP_BL = KP_U + 81920;  //   K'' lo
-constexpr uint32_t KP_A = KP_U;           //   CUDA cores: the per-token factors 2^g [64][128]
+constexpr uint32_t KP_A = KP_U;           //   CUDA cores: the per-token factors 2^g [64][128] (formed
+                                          //   from the raw log decays the inputs left at KP_U + 32 KB)
 constexpr uint32_t KP_P = KP_U + 32768;   //   P [64][64] fp32
 constexpr uint32_t KP_KB = KP_U + 49152;  //   column block k^ e^(gamma_r - gamma) [16][128]
 constexpr uint32_t KP_RK = KP_U + 57344;  //   row block k^ e^(gamma - gamma_r) [16][128]
@@ -315,9 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
       reinterpret_cast<float4*>(sTri)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();
 
-    // ---- per key channel the per-token decay factors and the running sum gamma of the log
-    // decays, each half of the chunk by its own thread; the span of gamma around token 31 decides
-    // the way A and P are formed
+    // ---- per key channel the running sum gamma of the log decays, each half of the chunk by its
+    // own thread; the span of gamma around token 31 decides the way A and P are formed
     bool wide;
     {
       const int c = tid & 127, t0 = (tid >> 7) * 32;
@@ -325,7 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
 #pragma unroll 8
       for (int t = t0; t < t0 + 32; ++t) {
         const float gl = sG[t * 128 + c];
-        sAf[t * 128 + c] = exp2f(gl);
         run += gl;
         sG[t * 128 + c] = run;
         mn = fminf(mn, run);
@@ -376,20 +375,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
       mma_flight = true;
     }
 
-    // ---- the record's operands (while the products run): K~ = k^ e^gamma (hi / lo), Q~ = q^ e^gamma,
-    // Kd = k^ e^(gamma_L - gamma) (hi / lo); a warp per token row, a float4 of channels per lane
+    // ---- the record's operands K~ = k^ e^gamma (hi / lo) and Q~ = q^ e^gamma while the products
+    // run (Kd comes beside the solve); a warp per token row, a float4 of channels per lane
     uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * KR_BYTES;
     for (int i = tid; i < 64 * 32; i += kThreads) {
       const int t = i >> 5, c4 = (i & 31) * 4;
       const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
-      const float4 gl = *reinterpret_cast<const float4*>(sG + 63 * 128 + c4);
       const float4 kk = *reinterpret_cast<const float4*>(sK + t * 128 + c4);
       const float4 qq = *reinterpret_cast<const float4*>(sQ + t * 128 + c4);
       const float4 eg = make_float4(exp2f(gm.x), exp2f(gm.y), exp2f(gm.z), exp2f(gm.w));
-      const float4 ed = f4exp2_diff(gl, gm);
       store4_split(rec + KR_KQ, 16384, rec + KR_KLO, 8192, t, c4, f4mul(kk, eg));
       store4_split(rec + KR_KQ, 16384, nullptr, 0, 64 + t, c4, f4mul(qq, eg));
-      store4_split(rec + KR_KD, 8192, rec + KR_KD + 16384, 8192, t, c4, f4mul(kk, ed));
     }
     float* vecg = reinterpret_cast<float*>(rec + KR_VEC);
     if (tid < 64) {
@@ -415,14 +411,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
       float v[32];
       tmem_ld_cols<32>(tmem + ((uint32_t)(q4 * 32) << 16) + part * 32, v);
       const int l = q4 * 32 + lane, s0 = part * 32;
-      if (l < 64) {
-        const int t = l;
+      if (l < 64) {  // the row's 16 x 16 blocks on and below the diagonal, four float4 groups each
+        const int t = l, tb = t >> 4;
         const float b = sBeta[t];
-        if (s0 <= t) {  // a block-lower entry exists in this half
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int s = s0 + j;
-            if ((s >> 4) <= (t >> 4)) sTri[tri_index(t, s)] = s < t ? b * v[j] : 0.f;
+        for (int bb = 0; bb < 2; ++bb) {
+          const int sbk = (s0 >> 4) + bb;
+          if (sbk <= tb) {
+            float* rowp = sTri + ((tb * (tb + 1)) / 2 + sbk) * 256 + (t & 15) * 16;
+#pragma unroll
+            for (int g4 = 0; g4 < 4; ++g4) {
+              const int s = 16 * sbk + 4 * g4, j = 16 * bb + 4 * g4;
+              const float4 w = make_float4(s < t ? b * v[j] : 0.f, s + 1 < t ? b * v[j + 1] : 0.f,
+                                           s + 2 < t ? b * v[j + 2] : 0.f, s + 3 < t ? b * v[j + 3] : 0.f);
+              *reinterpret_cast<float4*>(rowp + ((g4 ^ (t & 3)) << 2)) = w;
+            }
           }
         }
       } else {
@@ -437,6 +440,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
       }
       tc_fence_before();
     } else {
+      // the per-token decay factors 2^g from the raw log decays, still in the shared region (rows
+      // past L: g = 0), then P cleared over them
+      for (int i = tid; i < 64 * 32; i += kThreads) {
+        const int t = i >> 5, c4 = (i & 31) * 4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < L) {
+          v = *reinterpret_cast<const float4*>(sm + KP_U + 32768 + t * 512 + c4 * 4);
+          v = make_float4(fmaxf(v.x * kLog2e, g_min2), fmaxf(v.y * kLog2e, g_min2), fmaxf(v.z * kLog2e, g_min2),
+                          fmaxf(v.w * kLog2e, g_min2));
+        }
+        *reinterpret_cast<float4*>(sAf + t * 128 + c4) = make_float4(exp2f(v.x), exp2f(v.y), exp2f(v.z), exp2f(v.w));
+      }
+      __syncthreads();
       for (int i = tid; i < 64 * 64 / 4; i += kThreads) reinterpret_cast<float4*>(sP)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       // ---- A (beta-weighted, strictly lower) and P (q_scale) inside the four diagonal 16 x 16 blocks:
       // thread (block d, column s, channel quarter cc: float4 groups cc, cc + 4, ...), the decay
@@ -581,8 +597,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
       staged = un;
     }
 
-    // ---- T = (I + A)^-1, then T (hi / lo) into the record
-    solve_tri_batched(sm + KP_TRI, 1, tid);
+    // ---- T = (I + A)^-1 on warps 0 and 1, beside Kd = k^ e^(gamma_L - gamma) (hi / lo) on the other
+    // six; then T (hi / lo) into the record
+    if (warp < 2) {
+      solve_tri_batched<true>(sm + KP_TRI, 1, tid);
+    } else {
+      for (int i = tid - 64; i < 64 * 32; i += kThreads - 64) {
+        const int t = i >> 5, c4 = (i & 31) * 4;
+        const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
+        const float4 gl = *reinterpret_cast<const float4*>(sG + 63 * 128 + c4);
+        const float4 kk = *reinterpret_cast<const float4*>(sK + t * 128 + c4);
+        store4_split(rec + KR_KD, 8192, rec + KR_KD + 16384, 8192, t, c4, f4mul(kk, f4exp2_diff(gl, gm)));
+      }
+    }
+    __syncthreads();
     const float* sT = sTri + kTriBytes / 4;
     for (int i = tid; i < 64 * 8; i += kThreads) {
       const int t = i >> 3, k0 = (i & 7) * 8;

@@ -87,6 +87,9 @@ cudaError_t device_sm_count(int* sms);
 // Tiled 2D tensor map of a row-major bf16 matrix (no swizzle, zero fill out of bounds).
 cudaError_t encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                           uint32_t box_inner, uint32_t box_outer);
+// Tiled 2D tensor map of a row-major fp32 matrix (no swizzle, zero fill out of bounds).
+cudaError_t encode_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                         uint32_t box_inner, uint32_t box_outer);
 cudaError_t encode_chunk_tensor_maps(CUtensorMap* qkv_map, CUtensorMap* z_map, const uint16_t* qkv,
                                      const uint16_t* z, int T, int Hk, int Hv);
 cudaError_t launch_chunk_schedule(cudaStream_t stream, const int32_t* cu, int N, int32_t* order, unsigned* counter,

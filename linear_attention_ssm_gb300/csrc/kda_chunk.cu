@@ -74,6 +74,7 @@ static_assert(KP_RQ + 8192 <= KP_TRI && KP_BL + 16384 <= KP_TRI, "the shared reg
 // the chunk's tokens and channels for which it is taken: factors stay within 2^(+-86) (e^(+-60)),
 // far from fp32 overflow and from denormal operands.
 constexpr int kRefToken = 31;
+constexpr int kPrepThreads = 512;  // sixteen warps: the prep kernel's phases are latency-bound
 constexpr float kRefSpan2 = 86.f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -110,6 +111,8 @@ __device__ __forceinline__ float2 bf2x2_f(uint32_t w) {
 }
 
 struct KPrepParams {
+  CUtensorMap tmap_qkv;  // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle (the q and k tiles)
+  CUtensorMap tmap_g;    // g [T][Hv * 128] fp32, box 128 x 64, no swizzle
   const uint16_t* qkv;
   const float* g;
   const float* beta;
@@ -169,11 +172,13 @@ __device__ __forceinline__ float4 f4exp2_diff(float4 a, float4 b) {  // 2^(a - b
   return make_float4(exp2f(a.x - b.x), exp2f(a.y - b.y), exp2f(a.z - b.z), exp2f(a.w - b.w));
 }
 
-// Persistent over the (chunk, V head) units of the call.  Channel c of a 128-wide row is read in
-// float4 groups; where a warp's lanes split the channels, lane group g takes the groups g, g + G,
-// ... so that the lanes of one load cover consecutive 16-byte words (no bank conflicts).  The raw
-// q, k and g rows of the next unit are copied into the shared region (bulk copies on an mbarrier)
-// as soon as the current unit no longer needs it, so a unit starts from shared memory.
+// Persistent over the (chunk, V head) units of the call, sixteen warps per CTA (one CTA per SM):
+// every phase is latency-bound, so the warps' number, not their registers, sets its speed.
+// Channel c of a 128-wide row is read in float4 groups; where a warp's lanes split the channels,
+// lane group g takes the groups g, g + G, ... so that the lanes of one load cover consecutive
+// 16-byte words (no bank conflicts).  The raw q, k and g rows of the next unit are copied into the
+// shared region (bulk copies on an mbarrier) as soon as the current unit no longer needs it, so a
+// unit starts from shared memory.
 //
 // A and P: when every |gamma_t - gamma_31| of the chunk is small enough (always, for decays of a
 // few nats per token), the whole 64 x 64 products at once on the tensor cores around the middle
@@ -182,7 +187,8 @@ __device__ __forceinline__ float4 f4exp2_diff(float4 a, float4 b) {  // 2^(a - b
 // above the diagonal (whose factors may overflow) are discarded by position.  Otherwise the
 // diagonal 16 x 16 blocks by running products of the per-token factors and the blocks below them
 // around the last token of their column block, on the CUDA cores, where every factor is at most 1.
-__global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_constant__ KPrepParams p) {
+__global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_constant__ KPrepParams p) {
+  constexpr int NT = kPrepThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024k(smem_raw);
   const uint32_t sb = smem_u32(sm);
@@ -199,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + KP_BAR + 16);
   const uint32_t bar_mma = sb + KP_BAR, bar_in = sb + KP_BAR + 8;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int q4 = warp & 3, part = warp >> 2;
-  const int C = (2 * p.Hk + p.Hv) * kHeadDim, ratio = p.Hv / p.Hk;
+  const int q4 = warp & 3, cpart = warp >> 2;  // tensor-memory lane quarter, 16-column part
+  const int ratio = p.Hv / p.Hk;
   // chunk_off[N] exceeds the record capacity only for cu_seqlens outside [0, T]; those sequences
   // are rejected below, and no record past the capacity is written
   const long units = (long)min(__ldg(p.chunk_off + p.N), p.nc_max) * p.Hv;
@@ -210,6 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
     mbar_init(bar_mma, 1);
     mbar_init(bar_in, 1);
     fence_mbar_init();
+    prefetch_tensormap(&p.tmap_qkv);
+    prefetch_tensormap(&p.tmap_g);
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 64);
   tc_fence_before();
@@ -222,18 +230,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
   float bt_next = 0.f;  // beta of that unit (thread t < 64: token t)
   constexpr uint32_t ID64 = idesc_bf16_f32(128, 64);
 
-  // the raw rows of a unit -> the shared region: q [64][256 B] at 0, k at 16 KB, g [64][512 B] at
-  // 32 KB (rows t < L only); the region must be free and the caller's generic accesses fenced
+  // the raw rows of a unit -> the shared region by TMA: q as two 64 x 64 boxes (128-byte swizzle,
+  // 8 KB apart) at 0, k likewise at 16 KB, g [64][128] fp32 at 32 KB (rows past T zero, rows past
+  // L ignored); the region must be free and the caller's generic accesses fenced
   auto issue_in = [&](int c0, int L, int h, int kh) {
-    if (tid == 0) mbar_arrive_expect_tx(bar_in, (uint32_t)L * 1024u);
-    if (tid < 3 * kChunk) {
-      const int t = tid % kChunk, what = tid / kChunk;
-      if (t < L) {
-        const uint16_t* rowp = p.qkv + (size_t)(c0 + t) * C;
-        if (what == 0) bulk_load(sb + KP_U + t * 256, rowp + kh * kHeadDim, 256, bar_in);
-        else if (what == 1) bulk_load(sb + KP_U + 16384 + t * 256, rowp + (p.Hk + kh) * kHeadDim, 256, bar_in);
-        else bulk_load(sb + KP_U + 32768 + t * 512, p.g + ((size_t)(c0 + t) * p.Hv + h) * kHeadDim, 512, bar_in);
+    if (tid == 0) {
+      mbar_arrive_expect_tx(bar_in, 65536u);
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb) {
+        tma_load_2d(sb + KP_U + kb * 8192, &p.tmap_qkv, kh * kHeadDim + kb * 64, c0, bar_in);
+        tma_load_2d(sb + KP_U + 16384 + kb * 8192, &p.tmap_qkv, (p.Hk + kh) * kHeadDim + kb * 64, c0, bar_in);
       }
+      tma_load_2d(sb + KP_U + 32768, &p.tmap_g, h * kHeadDim, c0, bar_in);
     }
     bt_next = tid < L ? __ldg(p.beta + (size_t)(c0 + tid) * p.Hv + h) : 0.f;
     in_flight = true;
@@ -276,12 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
     // ---- q and k normalised (16 lanes per token row, 8 channels each), the clamped log decays
     // in log2 units and beta (zero past L)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = tid + j * kThreads, t = i >> 4, c8 = (i & 15) * 8;
+    for (int j = 0; j < 64 * 16 / NT; ++j) {
+      const int i = tid + j * NT, t = i >> 4, c8 = (i & 15) * 8;
       uint4 uq = make_uint4(0u, 0u, 0u, 0u), uk = uq;
-      if (t < L) {
-        uq = *reinterpret_cast<const uint4*>(sm + KP_U + t * 256 + c8 * 2);
-        uk = *reinterpret_cast<const uint4*>(sm + KP_U + 16384 + t * 256 + c8 * 2);
+      if (t < L) {  // 16-byte group c8 / 8 of row t in the swizzled boxes
+        const uint32_t off = (c8 >> 6) * 8192 + t * 128 + (((((c8 & 63) >> 3) ^ (t & 7))) << 4);
+        uq = *reinterpret_cast<const uint4*>(sm + KP_U + off);
+        uk = *reinterpret_cast<const uint4*>(sm + KP_U + 16384 + off);
       }
       const float2 a0 = bf2x2_f(uq.x), a1 = bf2x2_f(uq.y), a2 = bf2x2_f(uq.z), a3 = bf2x2_f(uq.w);
       const float2 b0 = bf2x2_f(uk.x), b1 = bf2x2_f(uk.y), b2 = bf2x2_f(uk.z), b3 = bf2x2_f(uk.w);
@@ -301,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
       *reinterpret_cast<float4*>(sK + t * 128 + c8 + 4) = make_float4(b2.x * ik, b2.y * ik, b3.x * ik, b3.y * ik);
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = tid + j * kThreads, t = i >> 5, c4 = (i & 31) * 4;
+    for (int j = 0; j < 64 * 32 / NT; ++j) {
+      const int i = tid + j * NT, t = i >> 5, c4 = (i & 31) * 4;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (t < L) {
         v = *reinterpret_cast<const float4*>(sm + KP_U + 32768 + t * 512 + c4 * 4);
@@ -312,42 +321,44 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
       *reinterpret_cast<float4*>(sG + t * 128 + c4) = v;
     }
     if (tid < 64) sBeta[tid] = bt_next;
-    for (int i = tid; i < (int)(kTriBytes / 16); i += kThreads)
+    for (int i = tid; i < (int)(kTriBytes / 16); i += NT)
       reinterpret_cast<float4*>(sTri)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();
 
-    // ---- per key channel the running sum gamma of the log decays, each half of the chunk by its
-    // own thread; the span of gamma around token 31 decides the way A and P are formed
+    // ---- per key channel the running sum gamma of the log decays, a quarter of the chunk per
+    // thread, then each quarter shifted by the totals before it; the span of gamma around token 31
+    // decides the way A and P are formed
     bool wide;
     {
-      const int c = tid & 127, t0 = (tid >> 7) * 32;
-      float run = 0.f, mn = 0.f, mx = 0.f;
+      const int c = tid & 127, qq = tid >> 7, t0 = qq * 16;
+      float run = 0.f, mn = INFINITY, mx = -INFINITY;
 #pragma unroll 8
-      for (int t = t0; t < t0 + 32; ++t) {
-        const float gl = sG[t * 128 + c];
-        run += gl;
+      for (int t = t0; t < t0 + 16; ++t) {
+        run += sG[t * 128 + c];
         sG[t * 128 + c] = run;
         mn = fminf(mn, run);
         mx = fmaxf(mx, run);
       }
-      // first half: gamma_0..31 around gamma_31 = run; second half: its sums are gamma_t - gamma_31
-      const float ref = t0 == 0 ? run : 0.f;
-      wide = !(fmaxf(mx - ref, ref - mn) <= kRefSpan2);  // NaN or infinity: wide
+      __syncthreads();
+      const float p0 = sG[15 * 128 + c], p1 = sG[31 * 128 + c], p2 = sG[47 * 128 + c];
+      const float off = qq == 0 ? 0.f : qq == 1 ? p0 : qq == 2 ? p0 + p1 : p0 + p1 + p2;
+      const float rel = off - (p0 + p1);  // gamma_t - gamma_31 = rel + (this quarter's running sum)
+      wide = !(fmaxf(fabsf(rel + mn), fabsf(rel + mx)) <= kRefSpan2);  // NaN or infinity: wide
+      // every quarter's totals are read before the barrier below; then the shifts
+      const bool tcw = __syncthreads_or(wide ? 1 : 0) == 0;
+      wide = !tcw;
+      if (qq > 0) {
+#pragma unroll 8
+        for (int t = t0; t < t0 + 16; ++t) sG[t * 128 + c] += off;
+      }
     }
-    const bool tc_way = __syncthreads_or(wide ? 1 : 0) == 0;
-    for (int i = tid; i < 32 * 32; i += kThreads) {  // the second half adds the first half's total
-      const int t = 32 + (i >> 5), c4 = (i & 31) * 4;
-      const float4 base = *reinterpret_cast<const float4*>(sG + 31 * 128 + c4);
-      float4* dst = reinterpret_cast<float4*>(sG + t * 128 + c4);
-      const float4 v = *dst;
-      *dst = make_float4(v.x + base.x, v.y + base.y, v.z + base.z, v.w + base.w);
-    }
+    const bool tc_way = !wide;
     __syncthreads();
 
     if (tc_way) {
       // ---- [K'; Q'] and K'' (hi / lo) into the shared region, then D[128 x 64] = [K'; Q'] K''^T on
       // the tensor cores (hi x hi + lo x hi + hi x lo, K = 128 channels as two 64-channel blocks)
-      for (int i = tid; i < 64 * 32; i += kThreads) {
+      for (int i = tid; i < 64 * 32; i += NT) {
         const int t = i >> 5, c4 = (i & 31) * 4;
         const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
         const float4 gr = *reinterpret_cast<const float4*>(sG + kRefToken * 128 + c4);
@@ -378,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
     // ---- the record's operands K~ = k^ e^gamma (hi / lo) and Q~ = q^ e^gamma while the products
     // run (Kd comes beside the solve); a warp per token row, a float4 of channels per lane
     uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * KR_BYTES;
-    for (int i = tid; i < 64 * 32; i += kThreads) {
+    for (int i = tid; i < 64 * 32; i += NT) {
       const int t = i >> 5, c4 = (i & 31) * 4;
       const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
       const float4 kk = *reinterpret_cast<const float4*>(sK + t * 128 + c4);
@@ -407,31 +418,27 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
       if (!ok) break;
       tc_fence_after();
       // lane row l: A row t = l (l < 64, times beta_t, s < t) or P row t = l - 64 (times q_scale,
-      // s <= t); this thread's 32 columns s = part * 32 + j
-      float v[32];
-      tmem_ld_cols<32>(tmem + ((uint32_t)(q4 * 32) << 16) + part * 32, v);
-      const int l = q4 * 32 + lane, s0 = part * 32;
-      if (l < 64) {  // the row's 16 x 16 blocks on and below the diagonal, four float4 groups each
+      // s <= t); this thread's 16 columns s = 16 cpart + j, one 16 x 16 block
+      float v[16];
+      tmem_ld_cols<16>(tmem + ((uint32_t)(q4 * 32) << 16) + cpart * 16, v);
+      const int l = q4 * 32 + lane, s0 = cpart * 16;
+      if (l < 64) {
         const int t = l, tb = t >> 4;
-        const float b = sBeta[t];
+        if (cpart <= tb) {  // the block is on or below the diagonal: four float4 groups
+          const float b = sBeta[t];
+          float* rowp = sTri + ((tb * (tb + 1)) / 2 + cpart) * 256 + (t & 15) * 16;
 #pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const int sbk = (s0 >> 4) + bb;
-          if (sbk <= tb) {
-            float* rowp = sTri + ((tb * (tb + 1)) / 2 + sbk) * 256 + (t & 15) * 16;
-#pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4) {
-              const int s = 16 * sbk + 4 * g4, j = 16 * bb + 4 * g4;
-              const float4 w = make_float4(s < t ? b * v[j] : 0.f, s + 1 < t ? b * v[j + 1] : 0.f,
-                                           s + 2 < t ? b * v[j + 2] : 0.f, s + 3 < t ? b * v[j + 3] : 0.f);
-              *reinterpret_cast<float4*>(rowp + ((g4 ^ (t & 3)) << 2)) = w;
-            }
+          for (int g4 = 0; g4 < 4; ++g4) {
+            const int s = s0 + 4 * g4, j = 4 * g4;
+            const float4 w = make_float4(s < t ? b * v[j] : 0.f, s + 1 < t ? b * v[j + 1] : 0.f,
+                                         s + 2 < t ? b * v[j + 2] : 0.f, s + 3 < t ? b * v[j + 3] : 0.f);
+            *reinterpret_cast<float4*>(rowp + ((g4 ^ (t & 3)) << 2)) = w;
           }
         }
       } else {
         const int t = l - 64;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
           float p8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) p8[e] = (s0 + 8 * q + e) <= t ? p.q_scale * v[8 * q + e] : 0.f;
@@ -442,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
     } else {
       // the per-token decay factors 2^g from the raw log decays, still in the shared region (rows
       // past L: g = 0), then P cleared over them
-      for (int i = tid; i < 64 * 32; i += kThreads) {
+      for (int i = tid; i < 64 * 32; i += NT) {
         const int t = i >> 5, c4 = (i & 31) * 4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (t < L) {
@@ -453,17 +460,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
         *reinterpret_cast<float4*>(sAf + t * 128 + c4) = make_float4(exp2f(v.x), exp2f(v.y), exp2f(v.z), exp2f(v.w));
       }
       __syncthreads();
-      for (int i = tid; i < 64 * 64 / 4; i += kThreads) reinterpret_cast<float4*>(sP)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = tid; i < 64 * 64 / 4; i += NT) reinterpret_cast<float4*>(sP)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       // ---- A (beta-weighted, strictly lower) and P (q_scale) inside the four diagonal 16 x 16 blocks:
-      // thread (block d, column s, channel quarter cc: float4 groups cc, cc + 4, ...), the decay
-      // 2^(gamma_t - gamma_s) as the running product of the per-token factors a_(s+1) .. a_t
+      // thread (block d, column s, channel eighth cc: float4 groups cc, cc + 8, cc + 16, cc + 24), the
+      // decay 2^(gamma_t - gamma_s) as the running product of the per-token factors a_(s+1) .. a_t
       {
-        const int cc = lane & 3, sl = ((warp & 1) << 3) | (lane >> 2), d = warp >> 1;
+        const int cc = lane & 7, sl = ((warp & 3) << 2) | (lane >> 3), d = warp >> 2;
         const int s = 16 * d + sl;
-        float2 ks[16], f[16];
+        float2 ks[8], f[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 kv = *reinterpret_cast<const float4*>(sK + s * 128 + 16 * j + 4 * cc);
+        for (int j = 0; j < 4; ++j) {
+          const float4 kv = *reinterpret_cast<const float4*>(sK + s * 128 + 32 * j + 4 * cc);
           ks[2 * j] = make_float2(kv.x, kv.y);
           ks[2 * j + 1] = make_float2(kv.z, kv.w);
           f[2 * j] = f[2 * j + 1] = make_float2(1.f, 1.f);
@@ -474,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
           const bool after = t > s;
           float2 pa = make_float2(0.f, 0.f), pq = pa;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int off = t * 128 + 16 * j + 4 * cc;
+          for (int j = 0; j < 4; ++j) {
+            const int off = t * 128 + 32 * j + 4 * cc;
             const float4 av = *reinterpret_cast<const float4*>(sAf + off);
             const float4 kv = *reinterpret_cast<const float4*>(sK + off);
             const float4 qv = *reinterpret_cast<const float4*>(sQ + off);
@@ -490,10 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
             pq = __ffma2_rn(make_float2(qv.z, qv.w), w1, pq);
           }
           float sa = pa.x + pa.y, sq = pq.x + pq.y;
-          sa += __shfl_xor_sync(0xffffffffu, sa, 1);
-          sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-          sa += __shfl_xor_sync(0xffffffffu, sa, 2);
-          sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+#pragma unroll
+          for (int m = 1; m <= 4; m <<= 1) {
+            sa += __shfl_xor_sync(0xffffffffu, sa, m);
+            sq += __shfl_xor_sync(0xffffffffu, sq, m);
+          }
           if (cc == 0) {
             if (after) sTri[tri_index(t, s)] = sBeta[t] * sa;
             if (t >= s) sP[t * 64 + s] = p.q_scale * sq;
@@ -506,14 +514,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
       for (int b = 0; b < 3; ++b) {
         const int r = 16 * b + 15;
         __syncthreads();  // the column buffer's previous readers are done
-        for (int i = tid; i < 16 * 32; i += kThreads) {
+        for (int i = tid; i < 16 * 32; i += NT) {
           const int jj = i >> 5, c4 = (i & 31) * 4, s = 16 * b + jj;
           const float4 e = f4exp2_diff(*reinterpret_cast<const float4*>(sG + r * 128 + c4),
                                        *reinterpret_cast<const float4*>(sG + s * 128 + c4));
           *reinterpret_cast<float4*>(sKb + jj * 128 + c4) = f4mul(*reinterpret_cast<const float4*>(sK + s * 128 + c4), e);
         }
         for (int a = b + 1; a < 4; ++a) {
-          for (int i = tid; i < 16 * 32; i += kThreads) {
+          for (int i = tid; i < 16 * 32; i += NT) {
             const int ii = i >> 5, c4 = (i & 31) * 4, t = 16 * a + ii;
             const float4 e = f4exp2_diff(*reinterpret_cast<const float4*>(sG + t * 128 + c4),
                                          *reinterpret_cast<const float4*>(sG + r * 128 + c4));
@@ -522,18 +530,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
           }
           __syncthreads();
           {
-            // thread: matrix (A or P), a 4 x 4 tile of the 16 x 16 block, the float4 groups kq, kq + 8,
-            // kq + 16, kq + 24 of the channels; the 8 lanes of a tile then reduce its 16 sums
-            // butterfly-wise, each ending with two of them
-            const int which = tid >> 7, tile = (tid >> 3) & 15, kq = tid & 7;
+            // thread: matrix (A or P), a 4 x 4 tile of the 16 x 16 block, the float4 groups kq and
+            // kq + 16 of the channels; the 16 lanes of a tile then reduce its 16 sums butterfly-wise,
+            // each ending with one of them
+            const int which = tid >> 8, tile = (tid >> 4) & 15, kq = tid & 15;
             const int i0 = (tile >> 2) * 4, j0 = (tile & 3) * 4;
             const float* R = which ? sRQ : sRK;
             float2 acc[16];
 #pragma unroll
             for (int o = 0; o < 16; ++o) acc[o] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int cb = 32 * j + 4 * kq;
+            for (int j = 0; j < 2; ++j) {
+              const int cb = 64 * j + 4 * kq;
               float4 rv[4], kv[4];
 #pragma unroll
               for (int x = 0; x < 4; ++x) {
@@ -551,46 +559,47 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
             float v16[16];
 #pragma unroll
             for (int o = 0; o < 16; ++o) v16[o] = acc[o].x + acc[o].y;
-            const bool b2 = kq & 4, b1 = kq & 2, b0 = kq & 1;
+            const bool b3 = kq & 8, b2 = kq & 4, b1 = kq & 2, b0 = kq & 1;
             float v8[8], v4[4], v2[2];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float send = b2 ? v16[i] : v16[i + 8], keep = b2 ? v16[i + 8] : v16[i];
-              v8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+              const float send = b3 ? v16[i] : v16[i + 8], keep = b3 ? v16[i + 8] : v16[i];
+              v8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float send = b1 ? v8[i] : v8[i + 4], keep = b1 ? v8[i + 4] : v8[i];
-              v4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+              const float send = b2 ? v8[i] : v8[i + 4], keep = b2 ? v8[i + 4] : v8[i];
+              v4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
             }
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-              const float send = b0 ? v4[i] : v4[i + 2], keep = b0 ? v4[i + 2] : v4[i];
-              v2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+              const float send = b1 ? v4[i] : v4[i + 2], keep = b1 ? v4[i + 2] : v4[i];
+              v2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
             }
-            // this lane holds sums 2 kq and 2 kq + 1: tile row kq / 2, columns 2 (kq & 1) + {0, 1}
-            const int t = 16 * a + i0 + (kq >> 1), s = 16 * b + j0 + 2 * (kq & 1);
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              if (which == 0) sTri[tri_index(t, s + i)] = sBeta[t] * v2[i];
-              else sP[t * 64 + s + i] = p.q_scale * v2[i];
-            }
+            const float send = b0 ? v2[0] : v2[1], keep = b0 ? v2[1] : v2[0];
+            const float v1 = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+            // this lane holds sum kq: tile row kq / 4, column kq % 4
+            const int t = 16 * a + i0 + (kq >> 2), s = 16 * b + j0 + (kq & 3);
+            if (which == 0) sTri[tri_index(t, s)] = sBeta[t] * v1;
+            else sP[t * 64 + s] = p.q_scale * v1;
           }
           __syncthreads();  // the row buffers are read before the next row block is formed
         }
       }
-      for (int i = tid; i < 64 * 8; i += kThreads) {  // P (bf16) into the record
+      for (int i = tid; i < 64 * 8; i += NT) {  // P (bf16) into the record
         const int t = i >> 3, k0 = (i & 7) * 8;
         const float4 p0 = *reinterpret_cast<const float4*>(sP + t * 64 + k0);
         const float4 p1 = *reinterpret_cast<const float4*>(sP + t * 64 + k0 + 4);
         const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
         store8_split(rec + KR_P, nullptr, 0, t, k0, pv);
       }
+      // the shared region's generic accesses, before the bulk copies below overwrite it (on the
+      // tensor-core way its last generic writes were fenced before the products, which read it)
+      fence_proxy_async_smem();
     }
     // A is complete in the solve's layout and the shared region is free: the next unit's rows
     info_u = un;
     nvalid = un < units && kda_unit(p, un, guess, nn, ngc, nh, nc0, nL);
-    fence_proxy_async_smem();
     __syncthreads();
     if (nvalid) {
       issue_in(nc0, nL, nh, nh / ratio);
@@ -598,11 +607,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
     }
 
     // ---- T = (I + A)^-1 on warps 0 and 1, beside Kd = k^ e^(gamma_L - gamma) (hi / lo) on the other
-    // six; then T (hi / lo) into the record
+    // fourteen; then T (hi / lo) into the record
     if (warp < 2) {
       solve_tri_batched<true>(sm + KP_TRI, 1, tid);
     } else {
-      for (int i = tid - 64; i < 64 * 32; i += kThreads - 64) {
+      for (int i = tid - 64; i < 64 * 32; i += NT - 64) {
         const int t = i >> 5, c4 = (i & 31) * 4;
         const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
         const float4 gl = *reinterpret_cast<const float4*>(sG + 63 * 128 + c4);
@@ -612,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const __grid_cons
     }
     __syncthreads();
     const float* sT = sTri + kTriBytes / 4;
-    for (int i = tid; i < 64 * 8; i += kThreads) {
+    for (int i = tid; i < 64 * 8; i += NT) {
       const int t = i >> 3, k0 = (i & 7) * 8;
       const int tb = t >> 4, kb = k0 >> 4;
       const bool upper = kb > tb;  // strictly upper blocks of T are zero
@@ -1180,11 +1189,15 @@ cudaError_t launch_kda_chunk_prefill(const LaunchEnv& env, const uint16_t* qkv, 
   if (T > 0 && nc_max > 0) {
     KPrepParams pp;
     memset(&pp, 0, sizeof pp);
+    if ((e = encode_chunk_tensor_maps(&pp.tmap_qkv, nullptr, qkv, nullptr, T, Hk, Hv)) != cudaSuccess) return e;
+    if ((e = encode_f32_2d(&pp.tmap_g, g, (uint64_t)Hv * kHeadDim, (uint64_t)T, (uint64_t)Hv * kHeadDim * 4, 128, 64)) !=
+        cudaSuccess)
+      return e;
     pp.qkv = qkv; pp.g = g; pp.beta = beta; pp.cu = cu; pp.chunk_off = chunk_off; pp.rec = rec; pp.err = env.err;
     pp.N = N; pp.T = T; pp.Hk = Hk; pp.Hv = Hv; pp.nc_max = (int)nc_max;
     pp.g_min = g_min; pp.q_scale = q_scale; pp.l2_eps = l2_eps;
     const long units = nc_max * Hv;  // an upper bound: the device walks chunk_off[N] x Hv units
-    kda_prep_kernel<<<(unsigned)std::min<long>(units, sms), kThreads, KP_BYTES, env.stream>>>(pp);
+    kda_prep_kernel<<<(unsigned)std::min<long>(units, sms), kPrepThreads, KP_BYTES, env.stream>>>(pp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   sp.cu = cu; sp.order = order; sp.counter = counter; sp.chunk_off = chunk_off; sp.rec = rec;

@@ -56,8 +56,7 @@ constexpr uint32_t KP_G = 65536;      // gamma [64][128], in log2 units (first t
 constexpr uint32_t KP_U = 98304;      // the shared region (96 KB):
 constexpr uint32_t KP_AH = KP_U;          //   tensor cores: [K'; Q'] hi, two 64-channel blocks of 128 rows
 constexpr uint32_t KP_AL = KP_U + 32768;  //   [K'; Q'] lo
-constexpr uint32_t KP_BH = KP_U + 65536;  //   K'' hi, two 64-channel blocks of 64 rows
-constexpr uint32_t KP_BL = KP_U + 81920;  //   K'' lo
+constexpr uint32_t KP_B = KP_U + 65536;   //   [K'' hi; K'' lo], two 64-channel blocks of 128 rows
 constexpr uint32_t KP_A = KP_U;           //   CUDA cores: the per-token factors 2^g [64][128] (formed
                                           //   from the raw log decays the inputs left at KP_U + 32 KB)
 constexpr uint32_t KP_P = KP_U + 32768;   //   P [64][64] fp32
@@ -69,7 +68,7 @@ constexpr uint32_t KP_BETA = KP_TRI + kHeadBuf;  // [64]
 constexpr uint32_t KP_BAR = KP_BETA + 256;       // the MMA and input barriers, then the tensor-memory address
 constexpr uint32_t KP_BYTES = KP_BAR + 64 + 1024;
 static_assert(KP_TRI % 1024 == 0 && KP_U % 1024 == 0, "swizzled tiles and the solve's buffers stay 1 KB aligned");
-static_assert(KP_RQ + 8192 <= KP_TRI && KP_BL + 16384 <= KP_TRI, "the shared region holds either set");
+static_assert(KP_RQ + 8192 <= KP_TRI && KP_B + 32768 <= KP_TRI, "the shared region holds either set");
 // Reference token of the tensor-core way, and the largest |gamma_t - gamma_ref| (log2 units) over
 // the chunk's tokens and channels for which it is taken: factors stay within 2^(+-86) (e^(+-60)),
 // far from fp32 overflow and from denormal operands.
@@ -154,6 +153,20 @@ __device__ __forceinline__ bool kda_unit(const KPrepParams& p, long u, const Uni
   return !(s0 < 0 || s1 < s0 || s1 > p.T || L <= 0);
 }
 
+// AND of `v` over threads 0..63 (named barrier 1; only those two warps call it)
+__device__ __forceinline__ bool bar_and_64(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\n"
+      "setp.ne.u32 p, %1, 0;\n"
+      "bar.red.and.pred q, 1, 64, p;\n"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)(v ? 1 : 0))
+      : "memory");
+  return r != 0;
+}
+
 // 4 fp32 values (columns k0..k0+3 of `row`, k0 % 4 == 0) -> bf16 hi (and lo) in K-major 128-byte
 // swizzled tiles whose 64-column blocks are hi_kbs / lo_kbs bytes apart
 __device__ __forceinline__ void store4_split(uint8_t* hi_tile, uint32_t hi_kbs, uint8_t* lo_tile, uint32_t lo_kbs,
@@ -183,7 +196,8 @@ __device__ __forceinline__ float4 f4exp2_diff(float4 a, float4 b) {  // 2^(a - b
 // A and P: when every |gamma_t - gamma_31| of the chunk is small enough (always, for decays of a
 // few nats per token), the whole 64 x 64 products at once on the tensor cores around the middle
 // token 31 -- [K'; Q'] = [k^; q^] o 2^(gamma - gamma_31) against K'' = k^ o 2^(gamma_31 - gamma),
-// each a bf16 hi / lo pair, three products of M = 128, N = 64, K = 128 into tensor memory; entries
+// each a bf16 hi / lo pair: hi x [K'' hi; K'' lo] (N = 128) and lo x K'' hi (N = 64), K = 128, into
+// tensor memory, the two column halves summed when read; entries
 // above the diagonal (whose factors may overflow) are discarded by position.  Otherwise the
 // diagonal 16 x 16 blocks by running products of the per-token factors and the blocks below them
 // around the last token of their column block, on the CUDA cores, where every factor is at most 1.
@@ -203,6 +217,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
   float* sRQ = reinterpret_cast<float*>(sm + KP_RQ);
   float* sBeta = reinterpret_cast<float*>(sm + KP_BETA);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + KP_BAR + 16);
+  int* s_issued = reinterpret_cast<int*>(sm + KP_BAR + 24);  // whether the next unit's rows were requested
   const uint32_t bar_mma = sb + KP_BAR, bar_in = sb + KP_BAR + 8;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q4 = warp & 3, cpart = warp >> 2;  // tensor-memory lane quarter, 16-column part
@@ -219,7 +234,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
     prefetch_tensormap(&p.tmap_qkv);
     prefetch_tensormap(&p.tmap_g);
   }
-  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 64);
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 128);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -228,23 +243,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
   bool ok = true, in_flight = false, mma_flight = false;
   long staged = -1;     // the unit whose rows are in flight to the shared region
   float bt_next = 0.f;  // beta of that unit (thread t < 64: token t)
-  constexpr uint32_t ID64 = idesc_bf16_f32(128, 64);
+  constexpr uint32_t ID64 = idesc_bf16_f32(128, 64), ID128 = idesc_bf16_f32(128, 128);
 
   // the raw rows of a unit -> the shared region by TMA: q as two 64 x 64 boxes (128-byte swizzle,
   // 8 KB apart) at 0, k likewise at 16 KB, g [64][128] fp32 at 32 KB (rows past T zero, rows past
   // L ignored); the region must be free and the caller's generic accesses fenced
-  auto issue_in = [&](int c0, int L, int h, int kh) {
-    if (tid == 0) {
-      mbar_arrive_expect_tx(bar_in, 65536u);
+  // the raw rows of a unit -> the shared region by TMA (one thread): q as two 64 x 64 boxes
+  // (128-byte swizzle, 8 KB apart) at 0, k likewise at 16 KB, g [64][128] fp32 at 32 KB (rows past
+  // T zero, rows past L ignored); the region must be free and its generic accesses fenced
+  auto issue_tma = [&](int c0, int h, int kh) {
+    mbar_arrive_expect_tx(bar_in, 65536u);
 #pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-        tma_load_2d(sb + KP_U + kb * 8192, &p.tmap_qkv, kh * kHeadDim + kb * 64, c0, bar_in);
-        tma_load_2d(sb + KP_U + 16384 + kb * 8192, &p.tmap_qkv, (p.Hk + kh) * kHeadDim + kb * 64, c0, bar_in);
-      }
-      tma_load_2d(sb + KP_U + 32768, &p.tmap_g, h * kHeadDim, c0, bar_in);
+    for (int kb = 0; kb < 2; ++kb) {
+      tma_load_2d(sb + KP_U + kb * 8192, &p.tmap_qkv, kh * kHeadDim + kb * 64, c0, bar_in);
+      tma_load_2d(sb + KP_U + 16384 + kb * 8192, &p.tmap_qkv, (p.Hk + kh) * kHeadDim + kb * 64, c0, bar_in);
     }
-    bt_next = tid < L ? __ldg(p.beta + (size_t)(c0 + tid) * p.Hv + h) : 0.f;
-    in_flight = true;
+    tma_load_2d(sb + KP_U + 32768, &p.tmap_g, h * kHeadDim, c0, bar_in);
   };
 
   long info_u = -1;  // the unit whose description is below
@@ -269,7 +283,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
     if (staged != u) {  // not in flight yet (the first unit, or one after a rejected unit)
       fence_proxy_async_smem();
       __syncthreads();
-      issue_in(c0, L, h, kh);
+      if (tid == 0) issue_tma(c0, h, kh);
+      bt_next = tid < L ? __ldg(p.beta + (size_t)(c0 + tid) * p.Hv + h) : 0.f;
+      in_flight = true;
       staged = u;
     }
     {
@@ -355,9 +371,53 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
     const bool tc_way = !wide;
     __syncthreads();
 
+    // the next unit (its guess loads have landed during the phases above)
+    info_u = un;
+    nvalid = un < units && kda_unit(p, un, guess, nn, ngc, nh, nc0, nL);
+    uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * KR_BYTES;
+    // the record's K~ = k^ e^gamma (hi / lo), Q~ = q^ e^gamma and vector block, then its
+    // Kd = k^ e^(gamma_L - gamma) (hi / lo), by the threads past the first two warps (a warp per
+    // token row, a float4 of channels per lane)
+    auto kq_record = [&]() {
+      for (int i = tid - 64; i < 64 * 32; i += NT - 64) {
+        const int t = i >> 5, c4 = (i & 31) * 4;
+        const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
+        const float4 kk = *reinterpret_cast<const float4*>(sK + t * 128 + c4);
+        const float4 qq = *reinterpret_cast<const float4*>(sQ + t * 128 + c4);
+        const float4 eg = make_float4(exp2f(gm.x), exp2f(gm.y), exp2f(gm.z), exp2f(gm.w));
+        store4_split(rec + KR_KQ, 16384, rec + KR_KLO, 8192, t, c4, f4mul(kk, eg));
+        store4_split(rec + KR_KQ, 16384, nullptr, 0, 64 + t, c4, f4mul(qq, eg));
+      }
+      float* vecg = reinterpret_cast<float*>(rec + KR_VEC);
+      const int j = tid - 64;
+      if (j < 64) {
+        const float b = sBeta[j];
+        vecg[KV_BETA + j] = b;
+        vecg[KV_NCX + j] = -b;
+        vecg[KV_CS + j] = 1.f;
+        vecg[KV_CO + j] = p.q_scale;
+      } else if (j < 192) {
+        vecg[KV_GL + j - 64] = exp2f(sG[63 * 128 + j - 64]);
+      }
+    };
+    auto kd_record = [&]() {
+      for (int i = tid - 64; i < 64 * 32; i += NT - 64) {
+        const int t = i >> 5, c4 = (i & 31) * 4;
+        const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
+        const float4 gl = *reinterpret_cast<const float4*>(sG + 63 * 128 + c4);
+        const float4 kk = *reinterpret_cast<const float4*>(sK + t * 128 + c4);
+        store4_split(rec + KR_KD, 8192, rec + KR_KD + 16384, 8192, t, c4, f4mul(kk, f4exp2_diff(gl, gm)));
+      }
+    };
+    // the next unit's rows into the shared region (free once the products have read it)
+    auto issue_next = [&](bool go) {
+      if (go) issue_tma(nc0, nh, nh / ratio);
+      *s_issued = go ? 1 : 0;
+    };
+
     if (tc_way) {
-      // ---- [K'; Q'] and K'' (hi / lo) into the shared region, then D[128 x 64] = [K'; Q'] K''^T on
-      // the tensor cores (hi x hi + lo x hi + hi x lo, K = 128 channels as two 64-channel blocks)
+      // ---- [K'; Q'] and K'' (hi / lo) into the shared region, then [K'; Q'] K''^T on the tensor cores:
+      // columns 0..63 take hi x hi + lo x hi, columns 64..127 hi x lo (K = 128 as two 64-channel blocks)
       for (int i = tid; i < 64 * 32; i += NT) {
         const int t = i >> 5, c4 = (i & 31) * 4;
         const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
@@ -367,7 +427,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
         const float4 er = f4exp2_diff(gm, gr), ec = f4exp2_diff(gr, gm);
         store4_split(sm + KP_AH, 16384, sm + KP_AL, 16384, t, c4, f4mul(kk, er));
         store4_split(sm + KP_AH, 16384, sm + KP_AL, 16384, 64 + t, c4, f4mul(qq, er));
-        store4_split(sm + KP_BH, 8192, sm + KP_BL, 8192, t, c4, f4mul(kk, ec));
+        store4_split(sm + KP_B, 16384, sm + KP_B + 8192, 16384, t, c4, f4mul(kk, ec));  // lo: row 64 + t
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -376,76 +436,73 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
       if (tid == 0) {
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-          mma_bf16_k4<2, 2>(tmem, sw128_desc(sb + KP_AH + kb * 16384), sw128_desc(sb + KP_BH + kb * 8192), ID64,
+          mma_bf16_k4<2, 2>(tmem, sw128_desc(sb + KP_AH + kb * 16384), sw128_desc(sb + KP_B + kb * 16384), ID128,
                             kb);
-          mma_bf16_k4<2, 2>(tmem, sw128_desc(sb + KP_AL + kb * 16384), sw128_desc(sb + KP_BH + kb * 8192), ID64, 1);
-          mma_bf16_k4<2, 2>(tmem, sw128_desc(sb + KP_AH + kb * 16384), sw128_desc(sb + KP_BL + kb * 8192), ID64, 1);
+          mma_bf16_k4<2, 2>(tmem, sw128_desc(sb + KP_AL + kb * 16384), sw128_desc(sb + KP_B + kb * 16384), ID64, 1);
         }
         mma_commit(bar_mma);
       }
       mma_flight = true;
-    }
-
-    // ---- the record's operands K~ = k^ e^gamma (hi / lo) and Q~ = q^ e^gamma while the products
-    // run (Kd comes beside the solve); a warp per token row, a float4 of channels per lane
-    uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * KR_BYTES;
-    for (int i = tid; i < 64 * 32; i += NT) {
-      const int t = i >> 5, c4 = (i & 31) * 4;
-      const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
-      const float4 kk = *reinterpret_cast<const float4*>(sK + t * 128 + c4);
-      const float4 qq = *reinterpret_cast<const float4*>(sQ + t * 128 + c4);
-      const float4 eg = make_float4(exp2f(gm.x), exp2f(gm.y), exp2f(gm.z), exp2f(gm.w));
-      store4_split(rec + KR_KQ, 16384, rec + KR_KLO, 8192, t, c4, f4mul(kk, eg));
-      store4_split(rec + KR_KQ, 16384, nullptr, 0, 64 + t, c4, f4mul(qq, eg));
-    }
-    float* vecg = reinterpret_cast<float*>(rec + KR_VEC);
-    if (tid < 64) {
-      const float b = sBeta[tid];
-      vecg[KV_BETA + tid] = b;
-      vecg[KV_NCX + tid] = -b;
-      vecg[KV_CS + tid] = 1.f;
-      vecg[KV_CO + tid] = p.q_scale;
-    } else if (tid < 192) {
-      vecg[KV_GL + tid - 64] = exp2f(sG[63 * 128 + tid - 64]);
-    }
-
-    if (tc_way) {
-      const bool got = mbar_wait(bar_mma, ph_mma, kWaitLimit);
+      bool got;
+      if (warp < 2) {
+        // ---- A from tensor memory (warp w: rows 32 w .. 32 w + 31, all 64 columns, times beta_t,
+        // s < t) into the solve's layout, then T = (I + A)^-1 on these two warps
+        got = __all_sync(0xffffffffu, mbar_wait(bar_mma, ph_mma, kWaitLimit));
+        tc_fence_after();
+        if (got) {
+          const int t = tid, tb = t >> 4;
+          const float b = sBeta[t];
+#pragma unroll
+          for (int cp = 0; cp < 4; ++cp) {
+            float v[16], w2[16];  // columns c: hi x hi + lo x hi; columns 64 + c: hi x lo
+            tmem_ld_cols<16>(tmem + ((uint32_t)(warp * 32) << 16) + cp * 16, v);
+            tmem_ld_cols<16>(tmem + ((uint32_t)(warp * 32) << 16) + 64 + cp * 16, w2);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += w2[j];
+            if (cp <= tb) {  // a block on or below the diagonal: four float4 groups
+              float* rowp = sTri + ((tb * (tb + 1)) / 2 + cp) * 256 + (t & 15) * 16;
+#pragma unroll
+              for (int g4 = 0; g4 < 4; ++g4) {
+                const int s = 16 * cp + 4 * g4, j = 4 * g4;
+                const float4 w = make_float4(s < t ? b * v[j] : 0.f, s + 1 < t ? b * v[j + 1] : 0.f,
+                                             s + 2 < t ? b * v[j + 2] : 0.f, s + 3 < t ? b * v[j + 3] : 0.f);
+                *reinterpret_cast<float4*>(rowp + ((g4 ^ (t & 3)) << 2)) = w;
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        got = bar_and_64(got);  // A complete (both warps)
+        if (got) solve_tri_batched<true>(sm + KP_TRI, 1, tid);
+      } else {
+        // ---- the other fourteen warps: K~ / Q~ while the products run; then P from tensor memory
+        // (rows 64.. of the lanes, times q_scale, s <= t) into the record, the next unit's rows, Kd
+        kq_record();
+        got = __all_sync(0xffffffffu, mbar_wait(bar_mma, ph_mma, kWaitLimit));
+        tc_fence_after();
+        if (tid == 64) issue_next(got && nvalid);
+        if (got && (q4 & 2)) {
+          float v[16], w2[16];
+          tmem_ld_cols<16>(tmem + ((uint32_t)(q4 * 32) << 16) + cpart * 16, v);
+          tmem_ld_cols<16>(tmem + ((uint32_t)(q4 * 32) << 16) + 64 + cpart * 16, w2);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] += w2[j];
+          const int t = q4 * 32 + lane - 64, s0 = cpart * 16;
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            float p8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) p8[e] = (s0 + 8 * q + e) <= t ? p.q_scale * v[8 * q + e] : 0.f;
+            store8_split(rec + KR_P, nullptr, 0, t, s0 + 8 * q, p8);
+          }
+        }
+        tc_fence_before();
+        kd_record();
+      }
       ph_mma ^= 1u;
       mma_flight = !got;
       if (!got) raise_error(p.err, kErrTimeout);
       ok = __syncthreads_and(got ? 1 : 0) != 0;
-      if (!ok) break;
-      tc_fence_after();
-      // lane row l: A row t = l (l < 64, times beta_t, s < t) or P row t = l - 64 (times q_scale,
-      // s <= t); this thread's 16 columns s = 16 cpart + j, one 16 x 16 block
-      float v[16];
-      tmem_ld_cols<16>(tmem + ((uint32_t)(q4 * 32) << 16) + cpart * 16, v);
-      const int l = q4 * 32 + lane, s0 = cpart * 16;
-      if (l < 64) {
-        const int t = l, tb = t >> 4;
-        if (cpart <= tb) {  // the block is on or below the diagonal: four float4 groups
-          const float b = sBeta[t];
-          float* rowp = sTri + ((tb * (tb + 1)) / 2 + cpart) * 256 + (t & 15) * 16;
-#pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4) {
-            const int s = s0 + 4 * g4, j = 4 * g4;
-            const float4 w = make_float4(s < t ? b * v[j] : 0.f, s + 1 < t ? b * v[j + 1] : 0.f,
-                                         s + 2 < t ? b * v[j + 2] : 0.f, s + 3 < t ? b * v[j + 3] : 0.f);
-            *reinterpret_cast<float4*>(rowp + ((g4 ^ (t & 3)) << 2)) = w;
-          }
-        }
-      } else {
-        const int t = l - 64;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float p8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) p8[e] = (s0 + 8 * q + e) <= t ? p.q_scale * v[8 * q + e] : 0.f;
-          store8_split(rec + KR_P, nullptr, 0, t, s0 + 8 * q, p8);
-        }
-      }
-      tc_fence_before();
     } else {
       // the per-token decay factors 2^g from the raw log decays, still in the shared region (rows
       // past L: g = 0), then P cleared over them
@@ -596,30 +653,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
       // the shared region's generic accesses, before the bulk copies below overwrite it (on the
       // tensor-core way its last generic writes were fenced before the products, which read it)
       fence_proxy_async_smem();
-    }
-    // A is complete in the solve's layout and the shared region is free: the next unit's rows
-    info_u = un;
-    nvalid = un < units && kda_unit(p, un, guess, nn, ngc, nh, nc0, nL);
-    __syncthreads();
-    if (nvalid) {
-      issue_in(nc0, nL, nh, nh / ratio);
-      staged = un;
-    }
-
-    // ---- T = (I + A)^-1 on warps 0 and 1, beside Kd = k^ e^(gamma_L - gamma) (hi / lo) on the other
-    // fourteen; then T (hi / lo) into the record
-    if (warp < 2) {
-      solve_tri_batched<true>(sm + KP_TRI, 1, tid);
-    } else {
-      for (int i = tid - 64; i < 64 * 32; i += NT - 64) {
-        const int t = i >> 5, c4 = (i & 31) * 4;
-        const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
-        const float4 gl = *reinterpret_cast<const float4*>(sG + 63 * 128 + c4);
-        const float4 kk = *reinterpret_cast<const float4*>(sK + t * 128 + c4);
-        store4_split(rec + KR_KD, 8192, rec + KR_KD + 16384, 8192, t, c4, f4mul(kk, f4exp2_diff(gl, gm)));
+      __syncthreads();  // A and P complete, the shared region's generic accesses fenced
+      if (tid == 64) issue_next(nvalid);
+      if (warp < 2) {
+        solve_tri_batched<true>(sm + KP_TRI, 1, tid);
+      } else {
+        kq_record();
+        kd_record();
       }
+      __syncthreads();
     }
-    __syncthreads();
+    in_flight = *s_issued != 0;
+    if (in_flight) staged = un;
+    if (!ok) break;
+    if (tid < 64) bt_next = (nvalid && tid < nL) ? __ldg(p.beta + (size_t)(nc0 + tid) * p.Hv + nh) : 0.f;
+
+    // ---- T (hi / lo) into the record
     const float* sT = sTri + kTriBytes / 4;
     for (int i = tid; i < 64 * 8; i += NT) {
       const int t = i >> 3, k0 = (i & 7) * 8;
@@ -643,7 +692,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, 128);
   }
 }
 

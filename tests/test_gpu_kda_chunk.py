@@ -247,3 +247,37 @@ def test_kda_chunk_full_size_sampled_heads():
         assert_out_close(out[:, h], ref["out"][:, 0], f"out of head {h}")
         for n in range(4):
             assert_state_close(st[n, h], ref["state"][n, 0], f"state of sequence {n}, head {h}")
+
+
+def test_kda_chunk_inside_a_captured_graph():
+    """The chunk-wise KDA call launches on the caller's stream only (no side streams, no host
+    synchronisation), so it can be captured in a CUDA graph; replays give the oracle's results."""
+    g = lib()
+    geo = GEO2
+    lengths = [130, 64, 7]
+    inp = kda_prefill_inputs(lengths, seed=330, geo=geo)
+    y = _conv(inp).to(DEV)
+    N, T = len(lengths), sum(lengths)
+    d = {k: inp[k].to(DEV) for k in ("g", "beta", "cu_seqlens", "z", "norm_w", "state0")}
+    ws = torch.empty(g.gdn_kda_chunk_prefill_workspace_size(N, T, geometry=geo), dtype=torch.uint8, device=DEV)
+    st = torch.empty_like(d["state0"])
+    out = torch.empty((T, geo.num_v_heads, 128), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            g.gdn_kda_chunk_prefill(y, d["g"], d["beta"], d["cu_seqlens"], inp["q_scale"], -4.0, state_in=d["state0"],
+                                    state_out=st, z=d["z"], norm_w=d["norm_w"], out=out, workspace=ws, geometry=geo,
+                                    stream=s)
+    want_o, want_s = _oracle(_conv(inp), inp, geo, -4.0, state_in=inp["state0"])
+    for _ in range(2):
+        st.fill_(float("nan"))
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        g.gdn_check_device_errors()
+        assert_out_close(out, want_o)
+        for n in range(N):
+            assert_state_close(st[n], want_s[n], f"state of sequence {n}")

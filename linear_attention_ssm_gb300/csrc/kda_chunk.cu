@@ -64,8 +64,8 @@ constexpr uint32_t KP_KB = KP_U + 49152;  //   column block k^ e^(gamma_r - gamm
 constexpr uint32_t KP_RK = KP_U + 57344;  //   row block k^ e^(gamma - gamma_r) [16][128]
 constexpr uint32_t KP_RQ = KP_U + 65536;  //   row block q^ e^(gamma - gamma_r) [16][128]
 constexpr uint32_t KP_TRI = KP_U + 98304;      // A, T and the solve's scratch (kHeadBuf)
-constexpr uint32_t KP_BETA = KP_TRI + kHeadBuf;  // [64]
-constexpr uint32_t KP_BAR = KP_BETA + 256;       // the MMA and input barriers, then the tensor-memory address
+constexpr uint32_t KP_BETA = KP_TRI + kHeadBuf;  // [2][64] (by unit parity)
+constexpr uint32_t KP_BAR = KP_BETA + 512;       // the MMA and input barriers, the tensor-memory address, flags
 constexpr uint32_t KP_BYTES = KP_BAR + 64 + 1024;
 static_assert(KP_TRI % 1024 == 0 && KP_U % 1024 == 0, "swizzled tiles and the solve's buffers stay 1 KB aligned");
 static_assert(KP_RQ + 8192 <= KP_TRI && KP_B + 32768 <= KP_TRI, "the shared region holds either set");
@@ -153,16 +153,35 @@ __device__ __forceinline__ bool kda_unit(const KPrepParams& p, long u, const Uni
   return !(s0 < 0 || s1 < s0 || s1 > p.T || L <= 0);
 }
 
-// AND of `v` over threads 0..63 (named barrier 1; only those two warps call it)
-__device__ __forceinline__ bool bar_and_64(bool v) {
+// Named barrier kId over the kCount threads of one warp group (only those threads call it): a plain
+// barrier, or one that returns the AND / OR of `v` over the group.
+template <int kId, int kCount>
+__device__ __forceinline__ void grp_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kId), "n"(kCount) : "memory");
+}
+template <int kId, int kCount>
+__device__ __forceinline__ bool grp_and(bool v) {
   uint32_t r;
   asm volatile(
       "{\n.reg .pred p, q;\n"
       "setp.ne.u32 p, %1, 0;\n"
-      "bar.red.and.pred q, 1, 64, p;\n"
+      "bar.red.and.pred q, %2, %3, p;\n"
       "selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)(v ? 1 : 0))
+      : "r"((uint32_t)(v ? 1 : 0)), "n"(kId), "n"(kCount)
+      : "memory");
+  return r != 0;
+}
+template <int kId, int kCount>
+__device__ __forceinline__ bool grp_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\n"
+      "setp.ne.u32 p, %1, 0;\n"
+      "bar.red.or.pred q, %2, %3, p;\n"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)(v ? 1 : 0)), "n"(kId), "n"(kCount)
       : "memory");
   return r != 0;
 }
@@ -189,20 +208,24 @@ __device__ __forceinline__ float4 f4exp2_diff(float4 a, float4 b) {  // 2^(a - b
 // every phase is latency-bound, so the warps' number, not their registers, sets its speed.
 // Channel c of a 128-wide row is read in float4 groups; where a warp's lanes split the channels,
 // lane group g takes the groups g, g + G, ... so that the lanes of one load cover consecutive
-// 16-byte words (no bank conflicts).  The raw q, k and g rows of the next unit are copied into the
-// shared region (bulk copies on an mbarrier) as soon as the current unit no longer needs it, so a
-// unit starts from shared memory.
+// 16-byte words (no bank conflicts).
+//
+// Per unit: the front phase (the unit's raw q, k and g arrive by TMA in a shared region; q and k
+// normalised, gamma = the running sum of the clamped log decays per channel, in log2 units, and its
+// span around token 31) runs on warps 2..15 beside the previous unit's solve on warps 0 and 1; then
+// A and P, the record, and T.
 //
 // A and P: when every |gamma_t - gamma_31| of the chunk is small enough (always, for decays of a
 // few nats per token), the whole 64 x 64 products at once on the tensor cores around the middle
 // token 31 -- [K'; Q'] = [k^; q^] o 2^(gamma - gamma_31) against K'' = k^ o 2^(gamma_31 - gamma),
 // each a bf16 hi / lo pair: hi x [K'' hi; K'' lo] (N = 128) and lo x K'' hi (N = 64), K = 128, into
-// tensor memory, the two column halves summed when read; entries
-// above the diagonal (whose factors may overflow) are discarded by position.  Otherwise the
-// diagonal 16 x 16 blocks by running products of the per-token factors and the blocks below them
-// around the last token of their column block, on the CUDA cores, where every factor is at most 1.
+// tensor memory, the two column halves summed when read; entries above the diagonal (whose
+// factors may overflow) are discarded by position.  Otherwise the diagonal 16 x 16 blocks by
+// running products of the per-token factors and the blocks below them around the last token of
+// their column block, on the CUDA cores, where every factor is at most 1.
 __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_constant__ KPrepParams p) {
   constexpr int NT = kPrepThreads;
+  constexpr int FT = NT - 64;  // the front group: warps 2..15
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024k(smem_raw);
   const uint32_t sb = smem_u32(sm);
@@ -215,12 +238,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
   float* sKb = reinterpret_cast<float*>(sm + KP_KB);
   float* sRK = reinterpret_cast<float*>(sm + KP_RK);
   float* sRQ = reinterpret_cast<float*>(sm + KP_RQ);
-  float* sBeta = reinterpret_cast<float*>(sm + KP_BETA);
+  float* sBeta = reinterpret_cast<float*>(sm + KP_BETA);  // two buffers of 64 (by unit parity)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + KP_BAR + 16);
-  int* s_issued = reinterpret_cast<int*>(sm + KP_BAR + 24);  // whether the next unit's rows were requested
+  int* s_flags = reinterpret_cast<int*>(sm + KP_BAR + 24);  // [0] the front's way (1: tensor cores)
   const uint32_t bar_mma = sb + KP_BAR, bar_in = sb + KP_BAR + 8;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q4 = warp & 3, cpart = warp >> 2;  // tensor-memory lane quarter, 16-column part
+  const int ft = tid - 64;                     // index in the front group (negative on warps 0, 1)
   const int ratio = p.Hv / p.Hk;
   // chunk_off[N] exceeds the record capacity only for cu_seqlens outside [0, T]; those sequences
   // are rejected below, and no record past the capacity is written
@@ -241,67 +265,40 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
   const uint32_t tmem = *tmem_slot;
   uint32_t ph_mma = 0, ph_in = 0;
   bool ok = true, in_flight = false, mma_flight = false;
-  long staged = -1;     // the unit whose rows are in flight to the shared region
-  float bt_next = 0.f;  // beta of that unit (thread t < 64: token t)
+  float bt = 0.f;  // beta of the unit whose rows were requested last (front thread ft < 64: token ft)
   constexpr uint32_t ID64 = idesc_bf16_f32(128, 64), ID128 = idesc_bf16_f32(128, 128);
 
-  // the raw rows of a unit -> the shared region by TMA: q as two 64 x 64 boxes (128-byte swizzle,
-  // 8 KB apart) at 0, k likewise at 16 KB, g [64][128] fp32 at 32 KB (rows past T zero, rows past
-  // L ignored); the region must be free and the caller's generic accesses fenced
   // the raw rows of a unit -> the shared region by TMA (one thread): q as two 64 x 64 boxes
   // (128-byte swizzle, 8 KB apart) at 0, k likewise at 16 KB, g [64][128] fp32 at 32 KB (rows past
-  // T zero, rows past L ignored); the region must be free and its generic accesses fenced
-  auto issue_tma = [&](int c0, int h, int kh) {
-    mbar_arrive_expect_tx(bar_in, 65536u);
+  // T zero, rows past L ignored); the region must be free and its generic accesses fenced.  The
+  // front group's first 64 threads load the unit's beta.
+  auto issue_unit = [&](int c0, int L, int h, int kh) {
+    if (tid == 64) {
+      mbar_arrive_expect_tx(bar_in, 65536u);
 #pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      tma_load_2d(sb + KP_U + kb * 8192, &p.tmap_qkv, kh * kHeadDim + kb * 64, c0, bar_in);
-      tma_load_2d(sb + KP_U + 16384 + kb * 8192, &p.tmap_qkv, (p.Hk + kh) * kHeadDim + kb * 64, c0, bar_in);
+      for (int kb = 0; kb < 2; ++kb) {
+        tma_load_2d(sb + KP_U + kb * 8192, &p.tmap_qkv, kh * kHeadDim + kb * 64, c0, bar_in);
+        tma_load_2d(sb + KP_U + 16384 + kb * 8192, &p.tmap_qkv, (p.Hk + kh) * kHeadDim + kb * 64, c0, bar_in);
+      }
+      tma_load_2d(sb + KP_U + 32768, &p.tmap_g, h * kHeadDim, c0, bar_in);
     }
-    tma_load_2d(sb + KP_U + 32768, &p.tmap_g, h * kHeadDim, c0, bar_in);
+    if (ft >= 0 && ft < 64) bt = ft < L ? __ldg(p.beta + (size_t)(c0 + ft) * p.Hv + h) : 0.f;
   };
 
-  long info_u = -1;  // the unit whose description is below
-  int nn = 0, ngc = 0, nh = 0, nc0 = 0, nL = 0;
-  bool nvalid = false;
-  for (long u = blockIdx.x; u < units && ok; u += gridDim.x) {
-    int n, gc, h, c0, L;
-    bool valid;
-    if (info_u == u) {
-      n = nn; gc = ngc; h = nh; c0 = nc0; L = nL; valid = nvalid;
-    } else {
-      valid = kda_unit(p, u, load_guess(p, 0), n, gc, h, c0, L);
+  // The front phase of a unit on the front group (barrier 2): wait for its rows, q and k normalised
+  // (16 lanes per token row, 8 channels each), the clamped log decays in log2 units, beta into
+  // buffer `bb`, the running sums gamma (a half of the chunk per thread of the first 256, the second
+  // half then shifted by the first half's total) and the way A and P take (s_flags[0]).  Returns
+  // false, uniformly over the group, when the rows did not arrive in time.
+  auto front = [&](int L, int bb) -> bool {
+    bool got = mbar_wait(bar_in, ph_in, kWaitLimit);
+    got = grp_and<2, FT>(got);
+    if (!got) {
+      if (ft == 0) raise_error(p.err, kErrTimeout);
+      return false;
     }
-    if (!valid) {  // uniform over the CTA
-      if (tid == 0) raise_error(p.err, kErrDeviceArgument);
-      continue;
-    }
-    const int kh = h / ratio;
-    // the next unit, guessed to lie in this unit's sequence: the guess loads while this unit computes
-    const long un = u + gridDim.x;
-    const UnitGuess guess = load_guess(p, n);
-    if (staged != u) {  // not in flight yet (the first unit, or one after a rejected unit)
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) issue_tma(c0, h, kh);
-      bt_next = tid < L ? __ldg(p.beta + (size_t)(c0 + tid) * p.Hv + h) : 0.f;
-      in_flight = true;
-      staged = u;
-    }
-    {
-      const bool got = mbar_wait(bar_in, ph_in, kWaitLimit);
-      ph_in ^= 1u;
-      in_flight = !got;
-      if (!got) raise_error(p.err, kErrTimeout);
-      ok = __syncthreads_and(got ? 1 : 0) != 0;
-      if (!ok) break;
-    }
-
-    // ---- q and k normalised (16 lanes per token row, 8 channels each), the clamped log decays
-    // in log2 units and beta (zero past L)
-#pragma unroll
-    for (int j = 0; j < 64 * 16 / NT; ++j) {
-      const int i = tid + j * NT, t = i >> 4, c8 = (i & 15) * 8;
+    for (int i = ft; i < 64 * 16; i += FT) {  // warp-uniform trip count (FT and 1024 are multiples of 32)
+      const int t = i >> 4, c8 = (i & 15) * 8;
       uint4 uq = make_uint4(0u, 0u, 0u, 0u), uk = uq;
       if (t < L) {  // 16-byte group c8 / 8 of row t in the swizzled boxes
         const uint32_t off = (c8 >> 6) * 8192 + t * 128 + (((((c8 & 63) >> 3) ^ (t & 7))) << 4);
@@ -325,9 +322,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
       *reinterpret_cast<float4*>(sK + t * 128 + c8) = make_float4(b0.x * ik, b0.y * ik, b1.x * ik, b1.y * ik);
       *reinterpret_cast<float4*>(sK + t * 128 + c8 + 4) = make_float4(b2.x * ik, b2.y * ik, b3.x * ik, b3.y * ik);
     }
-#pragma unroll
-    for (int j = 0; j < 64 * 32 / NT; ++j) {
-      const int i = tid + j * NT, t = i >> 5, c4 = (i & 31) * 4;
+    for (int i = ft; i < 64 * 32; i += FT) {
+      const int t = i >> 5, c4 = (i & 31) * 4;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (t < L) {
         v = *reinterpret_cast<const float4*>(sm + KP_U + 32768 + t * 512 + c4 * 4);
@@ -336,50 +332,78 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
       }
       *reinterpret_cast<float4*>(sG + t * 128 + c4) = v;
     }
-    if (tid < 64) sBeta[tid] = bt_next;
-    for (int i = tid; i < (int)(kTriBytes / 16); i += NT)
-      reinterpret_cast<float4*>(sTri)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    __syncthreads();
-
-    // ---- per key channel the running sum gamma of the log decays, a quarter of the chunk per
-    // thread, then each quarter shifted by the totals before it; the span of gamma around token 31
-    // decides the way A and P are formed
-    bool wide;
-    {
-      const int c = tid & 127, qq = tid >> 7, t0 = qq * 16;
+    if (ft < 64) sBeta[64 * bb + ft] = bt;
+    grp_sync<2, FT>();
+    bool wide = false;
+    if (ft < 256) {
+      const int c = ft & 127, t0 = (ft >> 7) * 32;
       float run = 0.f, mn = INFINITY, mx = -INFINITY;
 #pragma unroll 8
-      for (int t = t0; t < t0 + 16; ++t) {
+      for (int t = t0; t < t0 + 32; ++t) {
         run += sG[t * 128 + c];
         sG[t * 128 + c] = run;
         mn = fminf(mn, run);
         mx = fmaxf(mx, run);
       }
-      __syncthreads();
-      const float p0 = sG[15 * 128 + c], p1 = sG[31 * 128 + c], p2 = sG[47 * 128 + c];
-      const float off = qq == 0 ? 0.f : qq == 1 ? p0 : qq == 2 ? p0 + p1 : p0 + p1 + p2;
-      const float rel = off - (p0 + p1);  // gamma_t - gamma_31 = rel + (this quarter's running sum)
-      wide = !(fmaxf(fabsf(rel + mn), fabsf(rel + mx)) <= kRefSpan2);  // NaN or infinity: wide
-      // every quarter's totals are read before the barrier below; then the shifts
-      const bool tcw = __syncthreads_or(wide ? 1 : 0) == 0;
-      wide = !tcw;
-      if (qq > 0) {
-#pragma unroll 8
-        for (int t = t0; t < t0 + 16; ++t) sG[t * 128 + c] += off;
-      }
+      // first half: gamma_0..31 around gamma_31 = run; second half: its sums are gamma_t - gamma_31
+      const float ref = t0 == 0 ? run : 0.f;
+      wide = !(fmaxf(mx - ref, ref - mn) <= kRefSpan2);  // NaN or infinity: wide
     }
-    const bool tc_way = !wide;
-    __syncthreads();
+    wide = grp_or<2, FT>(wide);
+    for (int i = ft; i < 32 * 32; i += FT) {  // the second half adds the first half's total
+      const int t = 32 + (i >> 5), c4 = (i & 31) * 4;
+      const float4 base = *reinterpret_cast<const float4*>(sG + 31 * 128 + c4);
+      float4* dst = reinterpret_cast<float4*>(sG + t * 128 + c4);
+      const float4 v = *dst;
+      *dst = make_float4(v.x + base.x, v.y + base.y, v.z + base.z, v.w + base.w);
+    }
+    if (ft == 0) s_flags[0] = wide ? 0 : 1;
+    return true;
+  };
 
-    // the next unit (its guess loads have landed during the phases above)
+  long info_u = -1;  // the unit whose description is below
+  int nn = 0, ngc = 0, nh = 0, nc0 = 0, nL = 0;
+  bool nvalid = false;
+  long front_done = -1;  // the unit whose front phase is in shared memory
+  int bcur = 0;          // its beta buffer
+  for (long u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    int n, gc, h, c0, L;
+    bool valid;
+    if (info_u == u) {
+      n = nn; gc = ngc; h = nh; c0 = nc0; L = nL; valid = nvalid;
+    } else {
+      valid = kda_unit(p, u, load_guess(p, 0), n, gc, h, c0, L);
+    }
+    if (!valid) {  // uniform over the CTA
+      if (tid == 0) raise_error(p.err, kErrDeviceArgument);
+      continue;
+    }
+    // the next unit, guessed to lie in this unit's sequence: the guess loads while this unit computes
+    const long un = u + gridDim.x;
+    const UnitGuess guess = load_guess(p, n);
+    if (front_done != u) {  // the first unit, or one after a rejected unit: its front phase now
+      fence_proxy_async_smem();
+      __syncthreads();
+      issue_unit(c0, L, h, h / ratio);
+      in_flight = true;
+      const bool fok = ft >= 0 ? front(L, bcur) : true;
+      ok = __syncthreads_and(fok ? 1 : 0) != 0;
+      if (!ok) break;  // the rows did not arrive: in_flight stays set for the bounded wait below
+      ph_in ^= 1u;
+      in_flight = false;
+      front_done = u;
+    }
+    const bool tc_way = s_flags[0] != 0;
+    const float* sBc = sBeta + 64 * bcur;
+    const int bnext = bcur ^ 1;
     info_u = un;
     nvalid = un < units && kda_unit(p, un, guess, nn, ngc, nh, nc0, nL);
     uint8_t* rec = p.rec + ((size_t)gc * p.Hv + h) * KR_BYTES;
     // the record's K~ = k^ e^gamma (hi / lo), Q~ = q^ e^gamma and vector block, then its
-    // Kd = k^ e^(gamma_L - gamma) (hi / lo), by the threads past the first two warps (a warp per
-    // token row, a float4 of channels per lane)
+    // Kd = k^ e^(gamma_L - gamma) (hi / lo), by the front group (a warp per token row, a float4 of
+    // channels per lane)
     auto kq_record = [&]() {
-      for (int i = tid - 64; i < 64 * 32; i += NT - 64) {
+      for (int i = ft; i < 64 * 32; i += FT) {
         const int t = i >> 5, c4 = (i & 31) * 4;
         const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
         const float4 kk = *reinterpret_cast<const float4*>(sK + t * 128 + c4);
@@ -389,19 +413,18 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
         store4_split(rec + KR_KQ, 16384, nullptr, 0, 64 + t, c4, f4mul(qq, eg));
       }
       float* vecg = reinterpret_cast<float*>(rec + KR_VEC);
-      const int j = tid - 64;
-      if (j < 64) {
-        const float b = sBeta[j];
-        vecg[KV_BETA + j] = b;
-        vecg[KV_NCX + j] = -b;
-        vecg[KV_CS + j] = 1.f;
-        vecg[KV_CO + j] = p.q_scale;
-      } else if (j < 192) {
-        vecg[KV_GL + j - 64] = exp2f(sG[63 * 128 + j - 64]);
+      if (ft < 64) {
+        const float b = sBc[ft];
+        vecg[KV_BETA + ft] = b;
+        vecg[KV_NCX + ft] = -b;
+        vecg[KV_CS + ft] = 1.f;
+        vecg[KV_CO + ft] = p.q_scale;
+      } else if (ft < 192) {
+        vecg[KV_GL + ft - 64] = exp2f(sG[63 * 128 + ft - 64]);
       }
     };
     auto kd_record = [&]() {
-      for (int i = tid - 64; i < 64 * 32; i += NT - 64) {
+      for (int i = ft; i < 64 * 32; i += FT) {
         const int t = i >> 5, c4 = (i & 31) * 4;
         const float4 gm = *reinterpret_cast<const float4*>(sG + t * 128 + c4);
         const float4 gl = *reinterpret_cast<const float4*>(sG + 63 * 128 + c4);
@@ -409,12 +432,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
         store4_split(rec + KR_KD, 8192, rec + KR_KD + 16384, 8192, t, c4, f4mul(kk, f4exp2_diff(gl, gm)));
       }
     };
-    // the next unit's rows into the shared region (free once the products have read it)
-    auto issue_next = [&](bool go) {
-      if (go) issue_tma(nc0, nh, nh / ratio);
-      *s_issued = go ? 1 : 0;
-    };
 
+    bool my_ok = true;
     if (tc_way) {
       // ---- [K'; Q'] and K'' (hi / lo) into the shared region, then [K'; Q'] K''^T on the tensor cores:
       // columns 0..63 take hi x hi + lo x hi, columns 64..127 hi x lo (K = 128 as two 64-channel blocks)
@@ -443,15 +462,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
         mma_commit(bar_mma);
       }
       mma_flight = true;
-      bool got;
       if (warp < 2) {
         // ---- A from tensor memory (warp w: rows 32 w .. 32 w + 31, all 64 columns, times beta_t,
         // s < t) into the solve's layout, then T = (I + A)^-1 on these two warps
-        got = __all_sync(0xffffffffu, mbar_wait(bar_mma, ph_mma, kWaitLimit));
+        bool got = __all_sync(0xffffffffu, mbar_wait(bar_mma, ph_mma, kWaitLimit));
         tc_fence_after();
         if (got) {
           const int t = tid, tb = t >> 4;
-          const float b = sBeta[t];
+          const float b = sBc[t];
 #pragma unroll
           for (int cp = 0; cp < 4; ++cp) {
             float v[16], w2[16];  // columns c: hi x hi + lo x hi; columns 64 + c: hi x lo
@@ -472,15 +490,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
           }
         }
         tc_fence_before();
-        got = bar_and_64(got);  // A complete (both warps)
+        got = grp_and<1, 64>(got);  // A complete (both warps)
         if (got) solve_tri_batched<true>(sm + KP_TRI, 1, tid);
+        my_ok = got;
       } else {
-        // ---- the other fourteen warps: K~ / Q~ while the products run; then P from tensor memory
-        // (rows 64.. of the lanes, times q_scale, s <= t) into the record, the next unit's rows, Kd
+        // ---- the front group: K~ / Q~ while the products run; then the next unit's rows, P from
+        // tensor memory (rows 64.. of the lanes, times q_scale, s <= t) into the record, Kd, and the
+        // next unit's front phase beside the solve
         kq_record();
-        got = __all_sync(0xffffffffu, mbar_wait(bar_mma, ph_mma, kWaitLimit));
+        bool got = __all_sync(0xffffffffu, mbar_wait(bar_mma, ph_mma, kWaitLimit));
         tc_fence_after();
-        if (tid == 64) issue_next(got && nvalid);
+        got = grp_and<2, FT>(got);
+        const bool go = got && nvalid;
+        if (go) issue_unit(nc0, nL, nh, nh / ratio);
         if (got && (q4 & 2)) {
           float v[16], w2[16];
           tmem_ld_cols<16>(tmem + ((uint32_t)(q4 * 32) << 16) + cpart * 16, v);
@@ -498,14 +520,20 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
         }
         tc_fence_before();
         kd_record();
+        bool landed = false;
+        if (go) landed = front(nL, bnext);
+        if (ft == 0) {
+          s_flags[1] = go ? 1 : 0;
+          s_flags[2] = landed ? 1 : 0;
+        }
+        my_ok = got && (!go || landed);
       }
       ph_mma ^= 1u;
-      mma_flight = !got;
-      if (!got) raise_error(p.err, kErrTimeout);
-      ok = __syncthreads_and(got ? 1 : 0) != 0;
+      mma_flight = !my_ok;
+      if (!my_ok) raise_error(p.err, kErrTimeout);
     } else {
       // the per-token decay factors 2^g from the raw log decays, still in the shared region (rows
-      // past L: g = 0), then P cleared over them
+      // past L: g = 0); A's blocks cleared; then P cleared over the factors' neighbours
       for (int i = tid; i < 64 * 32; i += NT) {
         const int t = i >> 5, c4 = (i & 31) * 4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -516,6 +544,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
         }
         *reinterpret_cast<float4*>(sAf + t * 128 + c4) = make_float4(exp2f(v.x), exp2f(v.y), exp2f(v.z), exp2f(v.w));
       }
+      for (int i = tid; i < (int)(kTriBytes / 16); i += NT)
+        reinterpret_cast<float4*>(sTri)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       __syncthreads();
       for (int i = tid; i < 64 * 64 / 4; i += NT) reinterpret_cast<float4*>(sP)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       // ---- A (beta-weighted, strictly lower) and P (q_scale) inside the four diagonal 16 x 16 blocks:
@@ -560,7 +590,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
             sq += __shfl_xor_sync(0xffffffffu, sq, m);
           }
           if (cc == 0) {
-            if (after) sTri[tri_index(t, s)] = sBeta[t] * sa;
+            if (after) sTri[tri_index(t, s)] = sBc[t] * sa;
             if (t >= s) sP[t * 64 + s] = p.q_scale * sq;
           }
         }
@@ -637,7 +667,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
             const float v1 = keep + __shfl_xor_sync(0xffffffffu, send, 1);
             // this lane holds sum kq: tile row kq / 4, column kq % 4
             const int t = 16 * a + i0 + (kq >> 2), s = 16 * b + j0 + (kq & 3);
-            if (which == 0) sTri[tri_index(t, s)] = sBeta[t] * v1;
+            if (which == 0) sTri[tri_index(t, s)] = sBc[t] * v1;
             else sP[t * 64 + s] = p.q_scale * v1;
           }
           __syncthreads();  // the row buffers are read before the next row block is formed
@@ -650,23 +680,36 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
         const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
         store8_split(rec + KR_P, nullptr, 0, t, k0, pv);
       }
-      // the shared region's generic accesses, before the bulk copies below overwrite it (on the
-      // tensor-core way its last generic writes were fenced before the products, which read it)
+      // the shared region's generic accesses, before the next unit's rows overwrite it
       fence_proxy_async_smem();
-      __syncthreads();  // A and P complete, the shared region's generic accesses fenced
-      if (tid == 64) issue_next(nvalid);
+      __syncthreads();
+      const bool go = nvalid;
+      if (go) issue_unit(nc0, nL, nh, nh / ratio);
       if (warp < 2) {
         solve_tri_batched<true>(sm + KP_TRI, 1, tid);
       } else {
         kq_record();
         kd_record();
+        bool landed = false;
+        if (go) landed = front(nL, bnext);
+        if (ft == 0) {
+          s_flags[1] = go ? 1 : 0;
+          s_flags[2] = landed ? 1 : 0;
+        }
+        my_ok = !go || landed;
       }
-      __syncthreads();
     }
-    in_flight = *s_issued != 0;
-    if (in_flight) staged = un;
+    ok = __syncthreads_and(my_ok ? 1 : 0) != 0;
+    {
+      const bool issued = s_flags[1] != 0, landed = s_flags[2] != 0;
+      if (issued && landed) {  // the next unit's front phase is done
+        ph_in ^= 1u;
+        front_done = un;
+      }
+      in_flight = issued && !landed;
+    }
+    bcur = bnext;
     if (!ok) break;
-    if (tid < 64) bt_next = (nvalid && tid < nL) ? __ldg(p.beta + (size_t)(nc0 + tid) * p.Hv + nh) : 0.f;
 
     // ---- T (hi / lo) into the record
     const float* sT = sTri + kTriBytes / 4;

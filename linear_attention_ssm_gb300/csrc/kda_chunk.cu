@@ -35,15 +35,15 @@ namespace {
 constexpr uint32_t KR_KQ = 0;        // [K~ hi; Q~]: two 64-key blocks of 128 rows (tokens 0..63 of K~ hi,
                                      // then of Q~), 16 KB apart, 128-byte swizzle
 constexpr uint32_t KR_KLO = 32768;   // K~ lo: two 64-key blocks of 64 rows, 8 KB apart
-constexpr uint32_t KR_KD = 49152;    // Kd hi, then Kd lo 16 KB later: two 64-key blocks of 64 token rows each
-constexpr uint32_t KR_T = 81920;     // T hi, T lo (8 KB each)
+constexpr uint32_t KR_T = 49152;     // T hi, T lo (8 KB each)
+constexpr uint32_t KR_KD = 65536;    // Kd hi, then Kd lo 16 KB later: two 64-key blocks of 64 token rows each
 constexpr uint32_t KR_P = 98304;     // P (8 KB)
 constexpr uint32_t KR_VEC = 106496;  // beta, -beta, c_s (1), c_o (q_scale): 64 floats each; e^gamma_L: 128
 constexpr uint32_t kKRecVec = 384 * 4;
 constexpr uint32_t KR_BYTES = KR_VEC + kKRecVec;  // 108,032
-constexpr uint32_t kKRecKQ = KR_KD - KR_KQ;       // K~ hi, Q~ and K~ lo: one bulk copy
-constexpr uint32_t kKRecKD = KR_T - KR_KD;
-constexpr uint32_t kKRecTP = KR_VEC - KR_T;
+constexpr uint32_t kKRecKQ = KR_T - KR_KQ;        // K~ hi, Q~ and K~ lo: one bulk copy
+constexpr uint32_t kKRecTKD = KR_P - KR_T;        // T and Kd: one bulk copy
+constexpr uint32_t kKRecP = KR_VEC - KR_P;
 constexpr int KV_BETA = 0, KV_NCX = 64, KV_CS = 128, KV_CO = 192, KV_GL = 256;
 static_assert(KR_BYTES % 256 == 0, "records stay 256-byte aligned");
 
@@ -77,20 +77,22 @@ constexpr int kPrepThreads = 512;  // sixteen warps: the prep kernel's phases ar
 constexpr float kRefSpan2 = 86.f;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// ---- state kernel shared memory (one CTA per SM)
-constexpr uint32_t SK_QK = 0;         // [K~ hi; Q~] (record copy)
+// ---- state kernel shared memory (two CTAs per SM).  The first 48 KB hold the chunk's [K~; Q~] and
+// K~ lo until the X products have read them, then its T (hi / lo; E over T hi) and Kd (hi / lo).
+constexpr uint32_t SK_QK = 0;         // [K~ hi; Q~] (record copy), then T hi / lo
 constexpr uint32_t SK_KLO = 32768;    // K~ lo (same copy)
+constexpr uint32_t SK_T = 0;          // T hi / lo (the second copy), then E bf16 over T hi
+constexpr uint32_t SK_KD = 16384;     // Kd hi / lo (same copy), lo 16 KB after hi
 constexpr uint32_t SK_W = 49152;      // 32 KB: S0 key-half hi/lo, then the output staging
-constexpr uint32_t SK_KD = 81920;     // Kd hi / lo (record copy)
-constexpr uint32_t SK_T = 114688;     // T hi/lo (record), then E bf16
-constexpr uint32_t SK_P = 131072;     // P (record; follows T: one copy)
-constexpr uint32_t SK_V = 139264;     // V (TMA), then z
-constexpr uint32_t SK_VEC = 155648;   // 2 x vector block
+constexpr uint32_t SK_V = 81920;      // V (TMA), then z
+constexpr uint32_t SK_P = 98304;      // P (record copy)
+constexpr uint32_t SK_VEC = 106496;   // 2 x vector block
 constexpr uint32_t SK_BAR = SK_VEC + 2 * kKRecVec;
 constexpr uint32_t SK_BYTES = SK_BAR + 128 + 1024;
 constexpr uint32_t KSC_S = 0, KSC_X = 128, KSC_O1 = 192, KSC_COLS = 256;  // tensor-memory columns
-static_assert(SK_BYTES <= 232448 && KP_BYTES <= 232448, "one CTA's shared memory");
-static_assert(SK_KLO - SK_QK == KR_KLO - KR_KQ && SK_P - SK_T == KR_P - KR_T, "record parts keep their offsets");
+static_assert(2 * (SK_BYTES + 1024) <= 233472, "two state CTAs must share an SM");
+static_assert(KP_BYTES <= 232448, "one CTA's shared memory");
+static_assert(SK_KLO - SK_QK == KR_KLO - KR_KQ && SK_KD - SK_T == KR_KD - KR_T, "record parts keep their offsets");
 
 __device__ __forceinline__ uint8_t* align1024k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
@@ -766,7 +768,7 @@ struct KStateParams {
 //   S += E Kd (hi / lo pairs),  O2 = E P^T   ->  o = q_scale O1 + O2  ->  gated RMSNorm  ->  out
 // The record parts arrive by bulk copies as their buffers free up: [K~; Q~] once the X products
 // are done, Kd, T and P once the state update is done, the vector block a chunk ahead.
-__global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(const __grid_constant__ KStateParams p) {
+__global__ void __launch_bounds__(kThreads, 2) kda_state_kernel(const __grid_constant__ KStateParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024k(smem_raw);
   const uint32_t sb = smem_u32(sm);
@@ -855,13 +857,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(const __grid_con
     mbar_arrive_expect_tx(bar_qk, kKRecKQ);
     bulk_load(sb + SK_QK, recp(gc, h) + KR_KQ, kKRecKQ, bar_qk);
   };
-  auto issue_kd = [&](int gc, int h) {
-    mbar_arrive_expect_tx(bar_kd, kKRecKD);
-    bulk_load(sb + SK_KD, recp(gc, h) + KR_KD, kKRecKD, bar_kd);
+  auto issue_tkd = [&](int gc, int h) {  // into the [K~; Q~] buffer, once the X products have read it
+    mbar_arrive_expect_tx(bar_kd, kKRecTKD);
+    bulk_load(sb + SK_T, recp(gc, h) + KR_T, kKRecTKD, bar_kd);
   };
-  auto issue_tp = [&](int gc, int h) {
-    mbar_arrive_expect_tx(bar_tp, kKRecTP);
-    bulk_load(sb + SK_T, recp(gc, h) + KR_T, kKRecTP, bar_tp);
+  auto issue_p = [&](int gc, int h) {
+    mbar_arrive_expect_tx(bar_tp, kKRecP);
+    bulk_load(sb + SK_P, recp(gc, h) + KR_P, kKRecP, bar_tp);
   };
   auto issue_vec = [&](int gc, int h, int vb) {
     mbar_arrive_expect_tx(bar_vec0 + 8 * vb, kKRecVec);
@@ -925,10 +927,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(const __grid_con
       issue_vec(gc0, h, 0);
       issue_kq(gc0, h);
       issue_v(seq_s, h);
-      issue_kd(gc0, h);
-      issue_tp(gc0, h);
+      issue_p(gc0, h);
+      bulk_prefetch_l2(recp(gc0, h) + KR_T, kKRecTKD);  // T and Kd: copied once X is done
     }
-    pend_qk = pend_v = pend_tp = pend_kd = seq_e > seq_s;
+    pend_qk = pend_v = pend_tp = seq_e > seq_s;
     if (seq_e > seq_s) pend_vec |= 1u;
 
     // ---- initial state -> tensor memory
@@ -1001,8 +1003,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(const __grid_con
       }
       pend_v = false;
       if (!ok) break;
-      if (tid == 0 && has_next) issue_kq(gc + 1, h);  // the K~ / Q~ buffers are free once the X MMAs are done
-      pend_qk = has_next;
+      if (tid == 0) issue_tkd(gc, h);  // the [K~; Q~] buffer is free once the X MMAs are done
+      pend_kd = true;
 
       // ================= R = (V - X^T) diag(beta) -> hi/lo (value-major)
       {
@@ -1031,8 +1033,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(const __grid_con
       tmem_ld_cols<kW>(tl + KSC_O1 + part * kW, o1);
       fence_proxy_async_smem();
       tc_fence_before();
-      wait_bar(bar_tp, ph_tp);  // T and P of this chunk
-      pend_tp = false;
+      wait_bar(bar_kd, ph_kd);  // T and Kd of this chunk
+      pend_kd = false;
       tc_fence_after();
       if (!ok) break;
       if (tid == 0) {
@@ -1094,8 +1096,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(const __grid_con
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      wait_bar(bar_kd, ph_kd);  // Kd of this chunk (fetched when the previous chunk's update was done)
-      pend_kd = false;
+      wait_bar(bar_tp, ph_tp);  // P of this chunk (fetched when the previous chunk's update was done)
+      pend_tp = false;
       tc_fence_after();
       if (!ok) break;
       if (tid == 0) {
@@ -1120,10 +1122,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(const __grid_con
       await_mma(bar_s);
       if (!ok) break;
       if (has_next) {  // two issuing threads in different warps, so neither lags by both
-        if (tid == 0) issue_kd(gc + 1, h);
-        else if (tid == 32) issue_tp(gc + 1, h);
+        if (tid == 0) {
+          issue_kq(gc + 1, h);  // the buffer's T, Kd and E have been read by the products
+          bulk_prefetch_l2(recp(gc + 1, h) + KR_T, kKRecTKD);
+        } else if (tid == 32) {
+          issue_p(gc + 1, h);
+        }
       }
-      pend_kd = pend_tp = has_next;
+      pend_qk = pend_tp = has_next;
 
       // ================= output: o = O1 diag(c_o) (staged) + O2, then the gated RMSNorm
       {
@@ -1296,7 +1302,7 @@ cudaError_t launch_kda_chunk_prefill(const LaunchEnv& env, const uint16_t* qkv, 
   sp.state_in = state_in; sp.state_out = state_out; sp.z = z; sp.norm_w = norm_w; sp.out = out; sp.err = env.err;
   sp.N = N; sp.T = T; sp.Hk = Hk; sp.Hv = Hv; sp.nc_max = (int)nc_max; sp.rms_eps = rms_eps;
   const long items = (long)N * Hv;
-  kda_state_kernel<<<(unsigned)std::min<long>(items, sms), kThreads, SK_BYTES, env.stream>>>(sp);
+  kda_state_kernel<<<(unsigned)std::min<long>(items, 2L * sms), kThreads, SK_BYTES, env.stream>>>(sp);
   return cudaGetLastError();
 }
 

@@ -14,12 +14,15 @@
 //         P_ts = sum_c q^_t k^_s e^(gamma_t - gamma_s)
 //   S  = S0 diag(e^gamma_L) + E (k^ o e^(gamma_L - gamma))
 // -- the sequential recurrence S <- S diag(a_t); e = beta (v - S k^); S <- S + e k^T; o = q_scale S q^
-// written for a chunk at once.  Every decay factor is at most 1 (g <= 0 after the clamp): the
-// off-diagonal 16 x 16 blocks of A and P are products around the last token r of the column block,
-// (x_t e^(gamma_t - gamma_r)) (k^_s e^(gamma_r - gamma_s)), and the diagonal blocks take their
-// factors as running products of the per-token factors, so nothing overflows however strong the
-// decay.  Precision as in the GDN chunk path: every state-path operand (K~, Kd, S0, T, R, E~) is a
-// bf16 hi + lo pair, the output-only products (Q~ against S0, P E) plain bf16.
+// written for a chunk at once.  A and P: where every |gamma_t - gamma_31| of the chunk stays within
+// 60 nats, one tensor-core product around the chunk's middle token,
+// (x_t e^(gamma_t - gamma_31)) (k^_s e^(gamma_31 - gamma_s)), its entries above the diagonal
+// dropped by position; otherwise (any decay, g <= 0 after the clamp) the off-diagonal 16 x 16
+// blocks as products around the last token r of the column block, where both factors are at most
+// 1, and the diagonal blocks from running products of the per-token factors, so nothing overflows
+// however strong the decay.  Precision as in the GDN chunk path: every state-path operand (K~, Kd,
+// S0, T, R, E, and the A / P operands) is a bf16 hi + lo pair, the output-only products (Q~ against
+// S0, P E) plain bf16.
 #include <string.h>
 
 #include <algorithm>
@@ -766,8 +769,10 @@ struct KStateParams {
 //   [X | O1] = S0 [K~; Q~]^T                 (X with the hi / lo pairs of S0 and K~)
 //   R = (V - X) diag(beta) -> hi / lo        ->  E = R T^T   (R read from tensor memory)
 //   S += E Kd (hi / lo pairs),  O2 = E P^T   ->  o = q_scale O1 + O2  ->  gated RMSNorm  ->  out
-// The record parts arrive by bulk copies as their buffers free up: [K~; Q~] once the X products
-// are done, Kd, T and P once the state update is done, the vector block a chunk ahead.
+// Two CTAs per SM.  The record parts arrive by bulk copies as their buffers free up: [K~; Q~] (and
+// K~ lo) once the previous chunk's state update has read that buffer's T, Kd and E; T and Kd (one
+// copy, prefetched into L2 a chunk ahead) once the X products have read [K~; Q~]; P once the
+// previous chunk's O2 product is done; the vector block a chunk ahead.
 __global__ void __launch_bounds__(kThreads, 2) kda_state_kernel(const __grid_constant__ KStateParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024k(smem_raw);

@@ -794,6 +794,41 @@ def run_ours(args, rank, world, local):
     gdn.gdn_check_device_errors()
     e2e_ms = max_over_ranks(s2.elapsed_time(e2)) / args.e2e_steps
     e2e_value = replica_throughput(T, world, e2e_ms)
+
+    # the host link alone: the same copies without the prefill, host to device on the two input
+    # streams, device to host on the output stream, and both at once
+    def copies(i, h2d_on, d2h_on):
+        B = bufs[i % 2]
+        if h2d_on:
+            with torch.cuda.stream(cin):
+                B["x"].copy_(h_x, non_blocking=True)
+            with torch.cuda.stream(cin2):
+                for k, h in (("g", h_g), ("beta", h_b), ("z", h_z), ("st", h_state), ("cs", h_cs)):
+                    B[k].copy_(h, non_blocking=True)
+        if d2h_on:
+            with torch.cuda.stream(cout):
+                h_out.copy_(B["out"], non_blocking=True)
+                h_state_out.copy_(B["st_out"], non_blocking=True)
+                h_cs_out.copy_(B["cs_out"], non_blocking=True)
+
+    def time_copies(h2d_on, d2h_on):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for st_ in (cin, cin2, cout):
+            st_.wait_stream(stream)
+        for i in range(args.e2e_steps):
+            copies(i, h2d_on, d2h_on)
+        for st_ in (cin, cin2, cout):
+            stream.wait_stream(st_)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(a.elapsed_time(b)) / args.e2e_steps
+
+    h2d_ms, d2h_ms, both_ms = time_copies(True, False), time_copies(False, True), time_copies(True, True)
+    host_link = {"h2d_gbs": h2d / (h2d_ms / 1e3) / 1e9, "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9,
+                 "copies_only_ms_per_step": both_ms,
+                 "note": "the e2e step's pinned copies alone (no prefill): its floor"}
     del h_x, h_g, h_b, h_z, bufs
 
     # ---------------- varlen prefill: 8 packed sequences, 31,735 tokens (same path)
@@ -992,7 +1027,8 @@ def run_ours(args, rank, world, local):
             "roofline": roofline, "roofline_conv": conv_roof,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": args.e2e_steps,
-                    "pipelined": "H2D of step i+1 and D2H of step i-1 overlap the prefill of step i"},
+                    "pipelined": "H2D of step i+1 and D2H of step i-1 overlap the prefill of step i",
+                    "host_link": host_link},
             "decode": decode, "decode_fused_gates": decode_fg, "prefill_fused_gates": prefill_fg,
             "decode_fp16_state": decode_f16, "decode_kda": decode_kda, "verify": verify,
             "verify_fp16_state": verify_f16,

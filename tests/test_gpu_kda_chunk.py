@@ -281,3 +281,26 @@ def test_kda_chunk_inside_a_captured_graph():
         assert_out_close(out, want_o)
         for n in range(N):
             assert_state_close(st[n], want_s[n], f"state of sequence {n}")
+
+
+def test_kda_chunk_thousands_of_short_sequences():
+    """5,000 sequences of 0..12 tokens: more than the schedule sorts (its unsorted order is taken),
+    one chunk each, so consecutive prep units lie in different sequences and their sequence is
+    searched for each time."""
+    g = lib()
+    geo = GEO2
+    gen = torch.Generator().manual_seed(3310)
+    lengths = torch.randint(0, 13, (5000,), generator=gen).tolist()
+    inp = kda_prefill_inputs(lengths, seed=331, geo=geo)
+    y = _conv(inp)
+    N = len(lengths)
+    st = torch.empty((N, geo.num_v_heads, 128, 128), dtype=torch.float32, device=DEV)
+    out = _run(g, y, inp, geo, -6.0, state_in=inp["state0"].to(DEV), state_out=st)
+    g.gdn_check_device_errors()
+    want_o, want_s = _oracle(y, inp, geo, -6.0, state_in=inp["state0"])
+    assert_out_close(out, want_o)
+    for n in range(0, N, 97):  # a sample of the states, every length represented
+        if lengths[n] == 0:
+            assert torch.equal(st[n].cpu(), inp["state0"][n])
+        else:
+            assert_state_close(st[n], want_s[n], f"state of sequence {n} ({lengths[n]} tokens)")

@@ -455,6 +455,22 @@ GDN_API gdn_status gdn_kda_chunk_prefill(const gdn_geometry* geo, const gdn_bf16
                                          gdn_bf16* out, void* workspace, size_t workspace_bytes,
                                          void* stream);
 
+/*
+ * The KDA prefill in one call: gdn_conv1d_prefill (its output written to qkv), then
+ * gdn_kda_chunk_prefill on it.  Same arguments, results and errors as the two calls in sequence
+ * (qkv: [total_tokens, C] bf16, must not overlap x; conv_state_out may alias conv_state_in;
+ * workspace as for gdn_kda_chunk_prefill), with every argument of both stages checked before
+ * either is launched: a call that returns an error has launched nothing.
+ */
+GDN_API gdn_status gdn_kda_prefill(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w,
+                                   const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                                   const gdn_bf16* conv_state_in, gdn_bf16* conv_state_out,
+                                   gdn_bf16* qkv, const float* g, float g_min, const float* beta,
+                                   float q_scale, float l2_eps, const float* state_in,
+                                   float* state_out, const gdn_bf16* z, const gdn_bf16* norm_w,
+                                   float rms_eps, gdn_bf16* out, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
 /* Capacity of the fixed scratch used by gdn_chunk_prefill_noalloc. */
 #define GDN_NOALLOC_MAX_SEQS 16384
 #define GDN_NOALLOC_SCRATCH_BYTES (256 + 4 * GDN_NOALLOC_MAX_SEQS) /* 65,792 bytes */

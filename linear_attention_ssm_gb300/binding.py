@@ -67,6 +67,7 @@ def _configure(lib, debug: bool):
         "gdn_kda_recurrence": ([G, P, P, F, P, P, I, I, F, F, P, P, P, P, F, P, P], ctypes.c_int),
         "gdn_kda_chunk_prefill_workspace_size": ([G, I, I], S),
         "gdn_kda_chunk_prefill": ([G, P, P, F, P, P, I, I, F, F, P, P, P, P, F, P, P, S, P], ctypes.c_int),
+        "gdn_kda_prefill": ([G, P, P, P, I, I, P, P, P, P, F, P, F, F, P, P, P, P, F, P, P, S, P], ctypes.c_int),
         "gdn_verify_stash_size": ([G, I, I], S),
         "gdn_verify": ([G, P, P, P, P, P, P, P, P, F, F, F, P, I, I, P, S, P], ctypes.c_int),
         "gdn_verify_commit": ([G, P, P, S, P, P, I, I, P], ctypes.c_int),
@@ -672,13 +673,43 @@ def gdn_kda_prefill(x, conv_w, cu_seqlens, g, beta, z, norm_w, q_scale, g_min=fl
                     rms_eps=1e-6, state_in=None, state_out=None, conv_state_in=None, conv_state_out=None,
                     qkv_buf=None, out=None, workspace=None, chunked=True, geometry: Geometry = QWEN_GDN,
                     stream=None):
-    """The KDA prefill: gdn_conv1d_prefill, then the KDA recurrence with the gated RMSNorm fused --
-    in its chunk-wise form (gdn_kda_chunk_prefill, with `workspace` or one allocated here), or,
-    with chunked=False, token by token (gdn_kda_recurrence).  Returns out [T, Hv, Dv] bf16."""
-    qkv = gdn_conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in, conv_state_out, qkv_buf,
-                             geometry=geometry, stream=stream)
-    if chunked:
-        return gdn_kda_chunk_prefill(qkv, g, beta, cu_seqlens, q_scale, g_min, l2_eps, state_in, state_out, z,
-                                     norm_w, rms_eps, out, workspace, geometry=geometry, stream=stream)
-    return gdn_kda_recurrence(qkv, g, beta, cu_seqlens, q_scale, g_min, l2_eps, state_in, state_out, z,
-                              norm_w, rms_eps, out, geometry=geometry, stream=stream)
+    """The KDA prefill: conv1d, then the KDA recurrence with the gated RMSNorm fused -- in its
+    chunk-wise form as one call (gdn_kda_prefill of the C ABI; `workspace` or one allocated here),
+    or, with chunked=False, gdn_conv1d_prefill then the token-by-token gdn_kda_recurrence.  The
+    conv output goes to `qkv_buf` (allocated when None).  Returns out [T, Hv, Dv] bf16."""
+    if not chunked:
+        qkv = gdn_conv1d_prefill(x, conv_w, cu_seqlens, conv_state_in, conv_state_out, qkv_buf,
+                                 geometry=geometry, stream=stream)
+        return gdn_kda_recurrence(qkv, g, beta, cu_seqlens, q_scale, g_min, l2_eps, state_in, state_out, z,
+                                  norm_w, rms_eps, out, geometry=geometry, stream=stream)
+    lib = _L()
+    C, hv, dv, dk, W = (geometry.conv_dim, geometry.num_v_heads, geometry.head_v_dim, geometry.head_k_dim,
+                        geometry.conv_width)
+    N = cu_seqlens.numel() - 1
+    T = x.shape[0]
+    _dev(x, torch.bfloat16, "x", (T, C))
+    _dev(conv_w, torch.bfloat16, "conv_w", (C, W))
+    _dev(cu_seqlens, torch.int32, "cu_seqlens", (N + 1,))
+    _dev(conv_state_in, torch.bfloat16, "conv_state_in", (N, C, W - 1))
+    _dev(conv_state_out, torch.bfloat16, "conv_state_out", (N, C, W - 1))
+    _dev(g, torch.float32, "g", (T, hv, dk))
+    _dev(beta, torch.float32, "beta", (T, hv))
+    _dev(state_in, torch.float32, "state_in", (N, hv, dv, dk))
+    _dev(state_out, torch.float32, "state_out", (N, hv, dv, dk))
+    _dev(z, torch.bfloat16, "z", (T, hv, dv))
+    _dev(norm_w, torch.bfloat16, "norm_w", (dv,))
+    if qkv_buf is None:
+        qkv_buf = torch.empty((T, C), dtype=torch.bfloat16, device=x.device)
+    _dev(qkv_buf, torch.bfloat16, "qkv_buf", (T, C))
+    if out is None:
+        out = torch.empty((T, hv, dv), dtype=torch.bfloat16, device=x.device)
+    _dev(out, torch.bfloat16, "out", (T, hv, dv))
+    need = lib.gdn_kda_chunk_prefill_workspace_size(_geo(geometry), N, T)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.gdn_kda_prefill(_geo(geometry), _p(x), _p(conv_w), _p(cu_seqlens), N, T, _p(conv_state_in),
+                               _p(conv_state_out), _p(qkv_buf), _p(g), float(g_min), _p(beta), float(q_scale),
+                               float(l2_eps), _p(state_in), _p(state_out), _p(z), _p(norm_w), float(rms_eps),
+                               _p(out), _p(workspace), wbytes, _stream(stream)))
+    return out

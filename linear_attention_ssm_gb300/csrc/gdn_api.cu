@@ -451,11 +451,12 @@ size_t gdn_kda_chunk_prefill_workspace_size(const gdn_geometry* geo, int32_t num
   return gdn::kda_chunk_workspace_bytes(num_seqs, total_tokens, geo->num_v_heads);
 }
 
-gdn_status gdn_kda_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g, float g_min,
+static gdn_status kda_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g, float g_min,
                                  const float* beta, const int32_t* cu_seqlens, int32_t num_seqs,
                                  int32_t total_tokens, float q_scale, float l2_eps, const float* state_in,
                                  float* state_out, const gdn_bf16* z, const gdn_bf16* norm_w, float rms_eps,
-                                 gdn_bf16* out, void* workspace, size_t workspace_bytes, void* stream) {
+                                 gdn_bf16* out, void* workspace, size_t workspace_bytes, void* stream,
+                                 const ConvStage* conv = nullptr) {
   gdn_status s = check_geometry(geo);
   if (s != GDN_OK) return s;
   if (num_seqs < 0 || total_tokens < 0)
@@ -493,10 +494,49 @@ gdn_status gdn_kda_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, c
   }
   gdn::LaunchEnv env;
   if ((s = make_env(stream, &env)) != GDN_OK) return s;
+  if (conv && (total_tokens > 0 || conv->state_out)) {  // every argument checked: the conv stage first
+    s = launched(gdn::launch_conv1d_prefill(env, conv->x, conv->w, cu_seqlens, num_seqs, total_tokens, conv->C,
+                                            conv->state_in, conv->state_out, const_cast<gdn_bf16*>(qkv)),
+                 "conv1d launch");
+    if (s != GDN_OK) return s;
+  }
   return launched(gdn::launch_kda_chunk_prefill(env, qkv, g, g_min, beta, cu_seqlens, num_seqs, total_tokens,
                                                 geo->num_k_heads, geo->num_v_heads, q_scale, l2_eps, state_in,
                                                 state_out, z, norm_w, rms_eps, out, workspace),
                   "KDA chunk prefill launch");
+}
+
+gdn_status gdn_kda_chunk_prefill(const gdn_geometry* geo, const gdn_bf16* qkv, const float* g, float g_min,
+                                 const float* beta, const int32_t* cu_seqlens, int32_t num_seqs,
+                                 int32_t total_tokens, float q_scale, float l2_eps, const float* state_in,
+                                 float* state_out, const gdn_bf16* z, const gdn_bf16* norm_w, float rms_eps,
+                                 gdn_bf16* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return kda_chunk_prefill(geo, qkv, g, g_min, beta, cu_seqlens, num_seqs, total_tokens, q_scale, l2_eps, state_in,
+                           state_out, z, norm_w, rms_eps, out, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_kda_prefill(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w,
+                           const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                           const gdn_bf16* conv_state_in, gdn_bf16* conv_state_out, gdn_bf16* qkv, const float* g,
+                           float g_min, const float* beta, float q_scale, float l2_eps, const float* state_in,
+                           float* state_out, const gdn_bf16* z, const gdn_bf16* norm_w, float rms_eps,
+                           gdn_bf16* out, void* workspace, size_t workspace_bytes, void* stream) {
+  gdn_status s = check_geometry(geo);
+  if (s != GDN_OK) return s;
+  if (num_seqs > 0) {  // the conv stage's own arguments (the chunk stage checks the rest)
+    GDN_REQUIRE(conv_w, "conv_w");
+    GDN_OPTIONAL(conv_state_in, "conv_state_in");
+    GDN_OPTIONAL(conv_state_out, "conv_state_out");
+    if (total_tokens > 0) {
+      GDN_REQUIRE(x, "x");
+      GDN_REQUIRE(qkv, "qkv");
+      const size_t bytes = (size_t)total_tokens * conv_channels(geo) * 2;
+      if (overlaps(x, bytes, qkv, bytes)) return fail(GDN_ERR_INVALID_ARGUMENT, "qkv overlaps x");
+    }
+  }
+  const ConvStage conv = {x, conv_w, conv_state_in, conv_state_out, conv_channels(geo)};
+  return kda_chunk_prefill(geo, qkv, g, g_min, beta, cu_seqlens, num_seqs, total_tokens, q_scale, l2_eps, state_in,
+                           state_out, z, norm_w, rms_eps, out, workspace, workspace_bytes, stream, &conv);
 }
 
 gdn_status gdn_decode_step_fp16_state(const gdn_geometry* geo, const gdn_bf16* x, const gdn_bf16* conv_w,

@@ -74,6 +74,10 @@ int main(void) {
                                1e-6f, fake, NULL, 0, NULL),
          GDN_ERR_WORKSPACE);
 
+  EXPECT(gdn_kda_prefill(&kda, NULL, NULL, NULL, 0, 0, NULL, NULL, NULL, NULL, -INFINITY, NULL, 0.088f, 1e-6f, NULL,
+                         NULL, NULL, NULL, 1e-6f, NULL, NULL, 0, NULL),
+         GDN_OK);
+
   /* sizes computed on the host */
   if (gdn_verify_stash_size(&geo, 256, 8) != (size_t)256 * 8 * 53440) return 1;
   if (gdn_verify_stash_size(&geo, 1, 18) != 0) return 1;

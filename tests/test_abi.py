@@ -315,6 +315,28 @@ def test_kda_chunk_prefill_rejects_bad_arguments(lib):
     assert call(N=0, T=0, qkv=None, g=None, beta=None, cu=None, out=None, ws=None, wsb=0) == 0
 
 
+def test_kda_one_call_prefill_checks_both_stages_before_launching(lib):
+    """gdn_kda_prefill refuses a bad argument of either stage before it launches anything."""
+    geo = _geo(num_k_heads=64, num_v_heads=64)
+    need = lib.gdn_kda_chunk_prefill_workspace_size(geo, 2, 8)
+    WS = ctypes.c_void_p(0x100000)
+    C = (2 * 64 + 64) * 128
+
+    def call(x=FAKE, conv_w=FAKE, cs_in=None, cs_out=None, qkv=ctypes.c_void_p(0x10000 + 8 * C * 2), g=FAKE,
+             g_min=-1.0, ws=WS, wsb=need, N=2, T=8):
+        return lib.gdn_kda_prefill(geo, x, conv_w, FAKE, N, T, cs_in, cs_out, qkv, g, g_min, FAKE, 0.088, 1e-6, None,
+                                   None, None, None, 1e-6, FAKE, ws, wsb, None)
+
+    assert call(conv_w=None) == 1                        # the conv stage's own arguments
+    assert call(x=None) == 1
+    assert call(cs_in=ODD) == 3
+    assert call(qkv=ctypes.c_void_p(0x10000 + 64)) == 1  # qkv overlaps x
+    assert call(g=None) == 1                             # the chunk stage's
+    assert call(g_min=float("nan")) == 1
+    assert call(ws=None) == 7
+    assert call(N=0, T=0, x=None, conv_w=None, qkv=None, g=None, ws=None, wsb=0) == 0
+
+
 def test_kda_chunk_workspace_size():
     """Counters, order and chunk offsets, then one 108,032-byte record per (chunk, V head): K~ hi
     and Q~ (64 + 64 token rows x 128 bf16), K~ lo (64 x 128), Kd hi / lo (2 x 64 x 128), T hi / lo

@@ -304,3 +304,35 @@ def test_kda_chunk_thousands_of_short_sequences():
             assert torch.equal(st[n].cpu(), inp["state0"][n])
         else:
             assert_state_close(st[n], want_s[n], f"state of sequence {n} ({lengths[n]} tokens)")
+
+
+def test_kda_one_call_prefill_equals_the_two_calls():
+    """gdn_kda_prefill (conv, then the chunk-wise recurrence, in one call) gives the bits of
+    gdn_conv1d_prefill followed by gdn_kda_chunk_prefill: conv output, output, states, conv states."""
+    g = lib()
+    geo = GEO2
+    lengths = [150, 0, 64, 33]
+    inp = kda_prefill_inputs(lengths, seed=332, geo=geo, random_conv_state=True)
+    d = {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    N = len(lengths)
+    st1, st2 = torch.empty_like(d["state0"]), torch.empty_like(d["state0"])
+    cs1, cs2 = torch.empty_like(d["conv_state0"]), torch.empty_like(d["conv_state0"])
+    qkv1 = torch.empty_like(d["x"])
+    out1 = g.gdn_kda_prefill(d["x"], d["conv_w"], d["cu_seqlens"], d["g"], d["beta"], d["z"], d["norm_w"],
+                             inp["q_scale"], -3.0, state_in=d["state0"], state_out=st1, conv_state_in=d["conv_state0"],
+                             conv_state_out=cs1, qkv_buf=qkv1, geometry=geo)
+    qkv2 = g.gdn_conv1d_prefill(d["x"], d["conv_w"], d["cu_seqlens"], d["conv_state0"], cs2, geometry=geo)
+    out2 = g.gdn_kda_chunk_prefill(qkv2, d["g"], d["beta"], d["cu_seqlens"], inp["q_scale"], -3.0,
+                                   state_in=d["state0"], state_out=st2, z=d["z"], norm_w=d["norm_w"], geometry=geo)
+    g.gdn_check_device_errors()
+    assert torch.equal(qkv1, qkv2)
+    assert torch.equal(out1, out2)
+    assert torch.equal(st1, st2)
+    assert torch.equal(cs1, cs2)
+    ref = oracle.kda_prefill(inp["x"], inp["conv_w"], inp["cu_seqlens"], inp["g"], inp["beta"], inp["z"],
+                             inp["norm_w"], q_scale=inp["q_scale"], g_min=-3.0, state_in=inp["state0"],
+                             conv_state_in=inp["conv_state0"], **_a(geo))
+    assert_out_close(out1, ref["out"])
+    for n, L in enumerate(lengths):
+        if L:
+            assert_state_close(st1[n], ref["state"][n], f"state of sequence {n}")

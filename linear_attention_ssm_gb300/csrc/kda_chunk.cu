@@ -117,8 +117,6 @@ __device__ __forceinline__ float2 bf2x2_f(uint32_t w) {
 struct KPrepParams {
   CUtensorMap tmap_qkv;  // qkv [T][C] bf16, box 64 x 64, 128-byte swizzle (the q and k tiles)
   CUtensorMap tmap_g;    // g [T][Hv * 128] fp32, box 128 x 64, no swizzle
-  const uint16_t* qkv;
-  const float* g;
   const float* beta;
   const int32_t* cu;
   const int32_t* chunk_off;
@@ -1296,7 +1294,7 @@ cudaError_t launch_kda_chunk_prefill(const LaunchEnv& env, const uint16_t* qkv, 
     if ((e = encode_f32_2d(&pp.tmap_g, g, (uint64_t)Hv * kHeadDim, (uint64_t)T, (uint64_t)Hv * kHeadDim * 4, 128, 64)) !=
         cudaSuccess)
       return e;
-    pp.qkv = qkv; pp.g = g; pp.beta = beta; pp.cu = cu; pp.chunk_off = chunk_off; pp.rec = rec; pp.err = env.err;
+    pp.beta = beta; pp.cu = cu; pp.chunk_off = chunk_off; pp.rec = rec; pp.err = env.err;
     pp.N = N; pp.T = T; pp.Hk = Hk; pp.Hv = Hv; pp.nc_max = (int)nc_max;
     pp.g_min = g_min; pp.q_scale = q_scale; pp.l2_eps = l2_eps;
     const long units = nc_max * Hv;  // an upper bound: the device walks chunk_off[N] x Hv units

@@ -435,6 +435,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
         store4_split(rec + KR_KD, 8192, rec + KR_KD + 16384, 8192, t, c4, f4mul(kk, f4exp2_diff(gl, gm)));
       }
     };
+    // T (hi / lo) into the record, by warps 0 and 1 once their solve is done
+    auto t_record = [&]() {
+      const float* sT = sTri + kTriBytes / 4;
+      for (int i = tid; i < 64 * 8; i += 64) {
+        const int t = i >> 3, k0 = (i & 7) * 8;
+        const int tb = t >> 4, kb = k0 >> 4;
+        const bool upper = kb > tb;  // strictly upper blocks of T are zero
+        const float* rowT = sT + ((tb * (tb + 1)) / 2 + (upper ? 0 : kb)) * 256 + (t & 15) * 16;
+        const int q0 = (k0 & 15) >> 2, tx = t & 3;
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 v0 = upper ? z4 : *reinterpret_cast<const float4*>(rowT + ((q0 ^ tx) << 2));
+        const float4 v1 = upper ? z4 : *reinterpret_cast<const float4*>(rowT + (((q0 + 1) ^ tx) << 2));
+        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        store8_split(rec + KR_T, rec + KR_T + 8192, 0, t, k0, v);
+      }
+    };
 
     bool my_ok = true;
     if (tc_way) {
@@ -494,7 +510,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
         }
         tc_fence_before();
         got = grp_and<1, 64>(got);  // A complete (both warps)
-        if (got) solve_tri_batched<true>(sm + KP_TRI, 1, tid);
+        if (got) {
+          solve_tri_batched<true>(sm + KP_TRI, 1, tid);
+          t_record();
+        }
         my_ok = got;
       } else {
         // ---- the front group: K~ / Q~ while the products run; then the next unit's rows, P from
@@ -690,6 +709,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
       if (go) issue_unit(nc0, nL, nh, nh / ratio);
       if (warp < 2) {
         solve_tri_batched<true>(sm + KP_TRI, 1, tid);
+        t_record();
       } else {
         kq_record();
         kd_record();
@@ -713,22 +733,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
     }
     bcur = bnext;
     if (!ok) break;
-
-    // ---- T (hi / lo) into the record
-    const float* sT = sTri + kTriBytes / 4;
-    for (int i = tid; i < 64 * 8; i += NT) {
-      const int t = i >> 3, k0 = (i & 7) * 8;
-      const int tb = t >> 4, kb = k0 >> 4;
-      const bool upper = kb > tb;  // strictly upper blocks of T are zero
-      const float* rowT = sT + ((tb * (tb + 1)) / 2 + (upper ? 0 : kb)) * 256 + (t & 15) * 16;
-      const int q0 = (k0 & 15) >> 2, tx = t & 3;
-      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 v0 = upper ? z4 : *reinterpret_cast<const float4*>(rowT + ((q0 ^ tx) << 2));
-      const float4 v1 = upper ? z4 : *reinterpret_cast<const float4*>(rowT + (((q0 + 1) ^ tx) << 2));
-      const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      store8_split(rec + KR_T, rec + KR_T + 8192, 0, t, k0, v);
-    }
-    __syncthreads();  // the unit's buffers are read before the next unit overwrites them
   }
 
   // after an early exit, let copies and products still in flight land (bounded)

@@ -215,8 +215,9 @@ __device__ __forceinline__ float4 f4exp2_diff(float4 a, float4 b) {  // 2^(a - b
 //
 // Per unit: the front phase (the unit's raw q, k and g arrive by TMA in a shared region; q and k
 // normalised, gamma = the running sum of the clamped log decays per channel, in log2 units, and its
-// span around token 31) runs on warps 2..15 beside the previous unit's solve on warps 0 and 1; then
-// A and P, the record, and T.
+// span around token 31) has run on warps 2..15 during the previous unit; then A and P (all warps);
+// then warps 0 and 1 solve for T and write it to the record while warps 2..15 write the rest of the
+// record and run the next unit's front phase; the two groups meet at one CTA barrier per unit.
 //
 // A and P: when every |gamma_t - gamma_31| of the chunk is small enough (always, for decays of a
 // few nats per token), the whole 64 x 64 products at once on the tensor cores around the middle
@@ -243,7 +244,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(const __grid_
   float* sRQ = reinterpret_cast<float*>(sm + KP_RQ);
   float* sBeta = reinterpret_cast<float*>(sm + KP_BETA);  // two buffers of 64 (by unit parity)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + KP_BAR + 16);
-  int* s_flags = reinterpret_cast<int*>(sm + KP_BAR + 24);  // [0] the front's way (1: tensor cores)
+  // [0] the way the front phase chose (1: tensor cores); [1] the next unit's rows requested, [2] landed
+  int* s_flags = reinterpret_cast<int*>(sm + KP_BAR + 24);
   const uint32_t bar_mma = sb + KP_BAR, bar_in = sb + KP_BAR + 8;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q4 = warp & 3, cpart = warp >> 2;  // tensor-memory lane quarter, 16-column part

@@ -85,8 +85,8 @@ def assert_state_close(got, want, what="state", tol=STATE_TOL):
 
 def assert_bf16_within_one_ulp(got, want, abs_floor=0.0, what="conv"):
     """Every element within one bf16 ulp of the oracle's correctly rounded value, except where
-    the value is so close to zero that the kernel's fp32 accumulation error (abs_floor) exceeds
-    one ulp; returns the fraction of bit-exact elements."""
+    the value is so close to zero that the kernel's fp32 accumulation error (abs_floor, a scalar
+    or a per-element tensor) exceeds one ulp; returns the fraction of bit-exact elements."""
     a = got.detach().cpu().view(torch.int16).int()
     b = want.detach().cpu().view(torch.int16).int()
     # same sign => adjacent patterns differ by one; +0/-0 treated as equal
@@ -95,18 +95,36 @@ def assert_bf16_within_one_ulp(got, want, abs_floor=0.0, what="conv"):
     diff = torch.where(zero_pair, torch.zeros_like(diff), diff)
     absdiff = (got.detach().cpu().double() - want.double()).abs()
     bad = (diff > 1) & (absdiff > abs_floor)
-    assert not bad.any(), f"{what}: {int(bad.sum())} elements differ by more than one bf16 ulp and {abs_floor:.2g}"
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements differ by more than one bf16 ulp and their floor"
     return float((diff == 0).float().mean())
 
 
-def conv_accumulation_floor(x, w, conv_state=None):
-    """Absolute error bound of a 4-term fp32 multiply-add chain whose terms are at most
-    max|w| * max|x| (the SiLU after it does not increase an absolute error near zero):
-    4 * 2^-24 * 4 * max|w| * max|x|."""
-    mx = x.detach().abs().max().float().item()
-    if conv_state is not None:
-        mx = max(mx, conv_state.detach().abs().max().float().item())
-    return 16.0 * 2.0 ** -24 * w.detach().abs().max().float().item() * mx
+def conv_accumulation_floor(x, w, cu_seqlens, conv_state=None):
+    """Per-element absolute error allowance of the conv kernel near zero: 10 * 2^-24 * sum_i
+    |w_i x_(t-3+i)| over the element's four taps (the history from conv_state, else zeros).
+
+    The kernel sums four exact bf16 x bf16 products in fp32 (error at most 4 * 2^-24 times that
+    magnitude sum); SiLU's slope is at most 1.1, so the pre-rounding output is off by at most
+    E = 4.4 * 2^-24 * sum|w x|. Two correctly placed roundings differ by more than one bf16 ulp
+    only when the values they round are more than one ulp apart, and then the rounded results are
+    at most |error| + one ulp < 2E apart; 10 * 2^-24 covers 2E with room for the fp32 SiLU's own
+    relative error, which is negligible at the magnitudes where this happens."""
+    xa = x.detach().cpu().double().abs()
+    wa = w.detach().cpu().double().abs()
+    C, W = wa.shape
+    H = W - 1
+    cu = [int(v) for v in (cu_seqlens.tolist() if torch.is_tensor(cu_seqlens) else cu_seqlens)]
+    mag = torch.zeros_like(xa)
+    for n in range(len(cu) - 1):
+        s, e = cu[n], cu[n + 1]
+        if e == s:
+            continue
+        hist = (conv_state[n].detach().cpu().double().abs().t() if conv_state is not None
+                else torch.zeros(H, C, dtype=torch.float64))
+        pad = torch.cat([hist, xa[s:e]])
+        for i in range(W):
+            mag[s:e] += wa[:, i] * pad[i:i + e - s]
+    return 10.0 * 2.0 ** -24 * mag
 
 
 class Guarded:

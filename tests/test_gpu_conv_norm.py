@@ -31,7 +31,7 @@ def test_conv1d_prefill_matches_oracle(lengths, with_state):
     g.gdn_check_device_errors()
     y.check("y")
     cs_out.check("conv_state_out")
-    floor = conv_accumulation_floor(inp["x"], inp["conv_w"], cs_in)
+    floor = conv_accumulation_floor(inp["x"], inp["conv_w"], inp["cu_seqlens"], cs_in)
     exact = assert_bf16_within_one_ulp(y.t, y_ref, floor, "conv output")
     assert exact > 0.99, f"only {exact:.4f} of the conv outputs are bit-exact"
     assert torch.equal(cs_out.t.cpu().view(torch.int16), cs_ref.view(torch.int16))
